@@ -1,0 +1,391 @@
+"""Benchmark of the quantized-KV hot path on one GB300 (or N, one process per GPU).
+
+Workload (default): Llama-2-7B shape, KIVI 4-bit (K per channel over 32-token
+groups, V per token over 32-channel groups, last 128 tokens in a 16-bit
+window), 32 layers x 32 heads x D=128, batch 1, T=32768, synthetic seeded
+data.  One step is one decode step of the whole hot path for every layer:
+quantize-on-append of the new token (multi-layer kvq_append), decode
+attention over the whole cache (multi-layer kvq_decode_attention), length
+commit.  value = (packed KV bytes the decode reads + append bytes) / step
+time, in GB/s; the cache (4.9 GB) is larger than L2, so no flush is needed.
+
+Also reported: bulk append GB/s (one layer of 32768 tokens per call), the
+decode kernel's roofline fraction, an end-to-end number through the C ABI with
+host buffers, and the CPU oracle timed on a bounded sample.
+
+`--impl reference` times the CPU oracle (the reference arm of this build) on
+the same workload, a bounded sample per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized-KV decode attention: effective HBM GB/s and % of peak; append GB/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(values_bytes, times_s):
+    """Whole-job throughput: bytes of all ranks / the slowest rank's time."""
+    return sum(values_bytes) / max(times_s)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+
+def run_ours(args):
+    import torch
+
+    from bit_kv_cache_04_gb300 import kvq as K
+    from bit_kv_cache_04_gb300 import workloads as W
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    steps, warm = args.steps, args.warmup
+    extra = 2 * (steps + warm) + 16
+    w = W.make(args.workload, extra_tokens=extra)
+    cfg = w.cfg
+    L, B, H, Hq, D = cfg.L, cfg.batch, cfg.H_kv, cfg.H_q, cfg.D
+    stream = torch.cuda.current_stream(dev)
+    cache = K.KVCache(cfg, dev, block_table=W.page_table(w, rank))
+    seq_lens = torch.zeros(B, dtype=torch.int32, device=dev)
+    dt = torch.float16 if cfg.in_dtype == K.DT_F16 else torch.bfloat16
+
+    # ---- bulk append, one layer per call (timed per call) ----------------
+    app_ms, app_bytes = [], []
+    per_layer_cache = K.kvq_cache_bytes(cfg, w.lengths[0]) // L if B == 1 else None
+    for l in range(L):
+        ks, vs, cu = W.layer_batch(w, l, [0] * B, w.lengths, dev, seed=rank)
+        cu_d = torch.tensor(cu, dtype=torch.int32, device=dev)
+        e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+        e0.record(stream)
+        cache.append(l, 1, ks[None], vs[None], cu_d, seq_lens, cu[-1], max(w.lengths))
+        e1.record(stream)
+        e1.synchronize()
+        app_ms.append(e0.elapsed_time(e1))
+        src = ks.numel() * 2 * 2
+        packed = sum(K.kvq_cache_bytes(cfg, t) for t in w.lengths) // L
+        app_bytes.append(src + packed)
+        del ks, vs
+    cu_all = torch.tensor([0] + w.lengths, dtype=torch.int32, device=dev).cumsum(0, dtype=torch.int32)
+    cache.commit_lengths(cu_all, seq_lens)
+    torch.cuda.synchronize()
+    lengths = list(w.lengths)
+
+    # ---- decode steps ----------------------------------------------------
+    n_steps = warm + steps
+    g = torch.Generator(device=dev).manual_seed(1234 + rank)
+    new_k = torch.randn((n_steps, L, B, H, D), generator=g, device=dev).to(dt)
+    new_v = torch.randn((n_steps, L, B, H, D), generator=g, device=dev).to(dt)
+    qs = torch.randn((n_steps, L, B, Hq, D), generator=g, device=dev).to(dt)
+    out = torch.empty((L, B, Hq, D), dtype=torch.float32, device=dev)
+    cu1 = torch.arange(0, B + 1, dtype=torch.int32, device=dev)
+
+    def step(i):
+        cache.append(0, L, new_k[i], new_v[i], cu1, seq_lens, B, 1, stream)
+        dec0[i].record(stream)
+        cache.decode(0, L, qs[i], seq_lens, out, 0, stream)
+        dec1[i].record(stream)
+        cache.commit_lengths(cu1, seq_lens, stream)
+
+    dec0 = [torch.cuda.Event(True) for _ in range(n_steps)]
+    dec1 = [torch.cuda.Event(True) for _ in range(n_steps)]
+    step_bytes = []
+    for i in range(n_steps):
+        # the decode of step i reads the cache after its append: lengths + 1
+        lengths = [t + 1 for t in lengths]
+        step_bytes.append(sum(K.kvq_cache_bytes(cfg, t) for t in lengths)
+                          + L * B * H * D * 2 * 2)  # + append source bytes
+    for i in range(warm):
+        step(i)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    t0, t1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    t0.record(stream)
+    for i in range(warm, n_steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    elapsed = t0.elapsed_time(t1) / 1e3
+    if ws > 1:
+        tt = torch.tensor([elapsed], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        elapsed = tt.item()
+    timed_bytes = sum(step_bytes[warm:])
+    value = timed_bytes * ws / elapsed / 1e9
+    dec_ms = [dec0[i].elapsed_time(dec1[i]) for i in range(warm, n_steps)]
+    dec_bytes = [step_bytes[i] - L * B * H * D * 4 for i in range(warm, n_steps)]
+    achieved = sum(dec_bytes) / (sum(dec_ms) / 1e3) / 1e9
+    peak, peak_kind = _peaks()
+    status = cache.device_status()
+
+    # ---- end to end through the C ABI with host buffers -------------------
+    hk = new_k.cpu().pin_memory()
+    hv = new_v.cpu().pin_memory()
+    hq = qs.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    dk = torch.empty_like(new_k[0])
+    dv = torch.empty_like(new_v[0])
+    dq = torch.empty_like(qs[0])
+    e2e_bytes = 0
+
+    def e2e_step(i):
+        dk.copy_(hk[i], non_blocking=True)
+        dv.copy_(hv[i], non_blocking=True)
+        dq.copy_(hq[i], non_blocking=True)
+        cache.append(0, L, dk, dv, cu1, seq_lens, B, 1, stream)
+        cache.decode(0, L, dq, seq_lens, out, 0, stream)
+        cache.commit_lengths(cu1, seq_lens, stream)
+        hout.copy_(out, non_blocking=True)
+
+    for i in range(min(warm, 3)):
+        e2e_step(i)
+        lengths = [t + 1 for t in lengths]
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    e0.record(stream)
+    for i in range(warm, n_steps):
+        lengths = [t + 1 for t in lengths]
+        e2e_bytes += sum(K.kvq_cache_bytes(cfg, t) for t in lengths) + L * B * H * D * 4
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    h2d = (dk.numel() + dv.numel() + dq.numel()) * 2
+    d2h = hout.numel() * 4
+
+    # ---- CPU oracle on a bounded sample ------------------------------------
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, cache, seq_lens, args.cpu_heads)
+
+    append_gbs = sum(app_bytes) / (sum(app_ms) / 1e3) / 1e9
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": steps,
+        "warmup": warm,
+        "ms_per_step": round(elapsed / steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 in, packed int4 codes + fp16 scales, fp32 math",
+        "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "layers": L, "heads_q": Hq, "heads_kv": H, "head_dim": D,
+                   "batch": B, "context_tokens": w.lengths[0] if B == 1 else w.lengths,
+                   "format": "KIVI-4: K per-channel 18 B/32 tokens, V per-token 18 B/32, 128-token 16-bit window",
+                   "step": "append 1 token/seq to all layers + decode attention over all layers + length commit",
+                   "decode_launch": "one multi-layer launch",
+                   "l2": "inputs larger than L2 (cache %.2f GB)" % (K.kvq_cache_bytes(cfg, w.lengths[0]) * B / 1e9),
+                   "parallelism": f"replicas x{ws}"},
+        "decode": {"GBps": round(achieved, 2), "pct_of_peak": round(100 * achieved / peak, 2),
+                   "ms_per_launch": round(statistics.mean(dec_ms), 4),
+                   "tokens_per_s": round(B / statistics.mean(dec_ms) * 1e3, 2)},
+        "append": {"GBps": round(append_gbs, 2), "pct_of_peak": round(100 * append_gbs / peak, 2),
+                   "ms_per_layer": round(statistics.median(app_ms), 4),
+                   "what": "bulk quantize-on-append of one layer (32768 tokens x 32 heads) per call; "
+                           "bytes = fp16 source read + packed blocks and window written"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "decode attention (multi-layer launch)", "peak_source": peak_kind},
+        "e2e": {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": steps * (3 + (1 if cache.cfg.hot_window else 0)),
+        "clocks": clk,
+        "device_status": status,
+    }
+    if cpu:
+        result["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(result))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def _oracle_cfg(c):
+    from oracle import kvq_oracle as O
+
+    f = lambda x: None if x is None else O.Fmt(x.bits, x.group, x.axis)  # noqa: E731
+    return O.Config(L=c.L, H_kv=c.H_kv, H_q=c.H_q, D=c.D, batch=c.batch, max_T=c.max_T, in_dtype=c.in_dtype,
+                    k_fmt=f(c.k_fmt), v_fmt=f(c.v_fmt), k_cold=f(c.k_cold), v_cold=f(c.v_cold),
+                    hot_window=c.hot_window, residual_window=c.residual_window, flags=c.flags,
+                    rope_theta=c.rope_theta, sign_seed=c.sign_seed, page_tokens=c.page_tokens,
+                    n_pages=c.n_pages, max_pages_per_seq=c.max_pages_per_seq)
+
+
+def _oracle_sample(w, heads, T, seed=0):
+    """One oracle step on a sample: quantize-on-append of layer 0, sequence 0,
+    `heads` kv heads over T tokens, then fp64 decode attention of their query
+    heads.  Returns (seconds, packed bytes decoded)."""
+    import numpy as np
+
+    from bit_kv_cache_04_gb300 import workloads as W
+    from oracle import kvq_oracle as O
+
+    c = w.cfg
+    sub = w.scaled(L=1, lengths=[T], extra=0)
+    oc = _oracle_cfg(sub.cfg)
+    oc.H_kv = heads
+    oc.H_q = heads * (c.H_q // c.H_kv)
+    k, v = W.kv_tokens(sub, 0, 0, 0, T, "cpu", seed)
+    k = k[:, :heads].contiguous()
+    v = v[:, :heads].contiguous()
+    raw = lambda t: t.view(__import__("torch").int16).numpy().view(np.uint16)  # noqa: E731
+    q = W.queries(sub, 1, "cpu", seed)[:, :, : oc.H_q].contiguous()
+    t0 = time.perf_counter()
+    bufs = O.new_buffers(oc)
+    O.append(oc, bufs, 0, raw(k), raw(v), [T], [0])
+    O.decode_attention(oc, bufs, 0, 1, raw(q), [T])
+    dt = time.perf_counter() - t0
+    return dt, O.cache_bytes(oc, T)
+
+
+def cpu_baseline(w, cache=None, seq_lens=None, heads=2):
+    T = w.lengths[0]
+    dt, nbytes = _oracle_sample(w, heads, T)
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"layer 0, sequence 0, {heads} of {w.cfg.H_kv} kv heads, T={T}: oracle quantize-on-append "
+                      f"(fp32) + fp64 decode attention; {nbytes} packed bytes in {dt:.2f} s; numpy, one thread "
+                      f"for the elementwise work ({os.cpu_count()} host cores present)"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from bit_kv_cache_04_gb300 import workloads as W
+
+    w = W.make(args.workload, extra_tokens=0)
+    T = w.lengths[0]
+    heads = min(8, w.cfg.H_kv)
+    for _ in range(args.warmup):
+        _oracle_sample(w, heads, T // 8)
+    total_b = total_t = 0.0
+    for i in range(args.steps):
+        dt, nb = _oracle_sample(w, heads, T, seed=i)
+        total_b += nb
+        total_t += dt
+    value = total_b / total_t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_t / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 quantize, f64 attention",
+            "data": "synthetic (seeded)",
+            "config": {"workload": args.workload, "sample": f"layer 0, sequence 0, {heads} kv heads, T={T}"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"per step: oracle append + fp64 decode of {heads} kv heads over {T} tokens"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama2_7b_kivi4")
+    ap.add_argument("--cpu-heads", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,145 @@
+// Block quantization, packing and unpacking on the device, plus the warp
+// Walsh-Hadamard transform.  The quantizer keeps the fp32 op order of the
+// format: amax = max|x|; scale = fp16_rn(min(amax / qmax, 65504));
+// code = clamp(rint(x / float(scale)), -qmax, qmax), all codes 0 for a zero
+// scale.  Files that quantize are compiled without FMA contraction.
+#pragma once
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+// fp32 bits of 1/sqrt(128): the scale of the orthonormal 128-point transform.
+constexpr uint32_t kHadamardScaleBits = 0x3DB504F3u;
+
+__device__ __forceinline__ float hadamard_scale() { return __uint_as_float(kHadamardScaleBits); }
+
+// Unnormalized 128-point fast Walsh-Hadamard transform across one warp:
+// lane l holds elements 4l..4l+3.  Radix-2 stages with strides 1, 2, 4, ...,
+// 64 in that order; each maps (a, b) = (x[i], x[i+h]) to (a + b, a - b).
+__device__ __forceinline__ void warp_fwht128(float v[4]) {
+  float a0 = v[0] + v[1], a1 = v[0] - v[1];
+  float a2 = v[2] + v[3], a3 = v[2] - v[3];
+  v[0] = a0 + a2;
+  v[2] = a0 - a2;
+  v[1] = a1 + a3;
+  v[3] = a1 - a3;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float o = __shfl_xor_sync(0xffffffffu, v[e], m);
+      v[e] = upper ? (o - v[e]) : (v[e] + o);
+    }
+  }
+}
+
+// Forward randomized rotation of a 128-chunk held as in warp_fwht128:
+// y = d2 * (FWHT(d1 * x) * (1/sqrt(128))).
+__device__ __forceinline__ void warp_rotate128(float v[4], const uint32_t* d1, const uint32_t* d2) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if ((d1[(4 * lane + e) >> 5] >> ((4 * lane + e) & 31)) & 1u) v[e] = -v[e];
+  warp_fwht128(v);
+  const float c = hadamard_scale();
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    v[e] = v[e] * c;
+    if ((d2[(4 * lane + e) >> 5] >> ((4 * lane + e) & 31)) & 1u) v[e] = -v[e];
+  }
+}
+
+// Inverse rotation: x = d1 * (FWHT(d2 * y) * (1/sqrt(128))).
+__device__ __forceinline__ void warp_unrotate128(float v[4], const uint32_t* d1, const uint32_t* d2) {
+  warp_rotate128(v, d2, d1);
+}
+
+__device__ __forceinline__ int quant_code(float x, float sf, int qmax) {
+  if (sf == 0.0f) return 0;
+  float r = rintf(__fdiv_rn(x, sf));
+  r = fminf(fmaxf(r, (float)-qmax), (float)qmax);
+  return (int)r;
+}
+
+// Quantizes G values get(0..G-1) into one block at dst (scale then codes).
+// If deq is given, it receives code * scale (exact in fp32).
+template <class Get>
+__device__ void quant_block_serial(Get get, int G, int bits, uint8_t* dst, float* deq) {
+  const int qmax = qmax_of(bits);
+  float amax = 0.0f;
+  for (int i = 0; i < G; ++i) amax = fmaxf(amax, fabsf(get(i)));
+  float s32 = __fdiv_rn(amax, (float)qmax);
+  __half s16 = __float2half_rn(fminf(s32, 65504.0f));
+  const float sf = __half2float(s16);
+  const uint16_t sb = __half_as_ushort(s16);
+  dst[0] = (uint8_t)(sb & 0xFF);
+  dst[1] = (uint8_t)(sb >> 8);
+  uint8_t* p = dst + 2;
+  if (bits == 8) {
+    for (int i = 0; i < G; ++i) {
+      int c = quant_code(get(i), sf, qmax);
+      p[i] = (uint8_t)(c & 0xFF);
+      if (deq) deq[i] = (float)c * sf;
+    }
+  } else if (bits == 4) {
+    for (int i = 0; i < G; i += 2) {
+      int c0 = quant_code(get(i), sf, qmax), c1 = quant_code(get(i + 1), sf, qmax);
+      p[i >> 1] = (uint8_t)((c0 + 8) | ((c1 + 8) << 4));
+      if (deq) {
+        deq[i] = (float)c0 * sf;
+        deq[i + 1] = (float)c1 * sf;
+      }
+    }
+  } else if (bits == 3) {
+    for (int i = 0; i < G; i += 8) {
+      uint32_t w = 0;
+      for (int j = 0; j < 8; ++j) {
+        int c = quant_code(get(i + j), sf, qmax);
+        w |= (uint32_t)(c + 4) << (3 * j);
+        if (deq) deq[i + j] = (float)c * sf;
+      }
+      uint8_t* q = p + (i >> 3) * 3;
+      q[0] = (uint8_t)(w & 0xFF);
+      q[1] = (uint8_t)((w >> 8) & 0xFF);
+      q[2] = (uint8_t)((w >> 16) & 0xFF);
+    }
+  } else {  // 2 bits
+    for (int i = 0; i < G; i += 4) {
+      uint32_t b = 0;
+      for (int j = 0; j < 4; ++j) {
+        int c = quant_code(get(i + j), sf, qmax);
+        b |= (uint32_t)(c + 2) << (2 * j);
+        if (deq) deq[i + j] = (float)c * sf;
+      }
+      p[i >> 2] = (uint8_t)b;
+    }
+  }
+}
+
+// Code i of a block payload (signed).
+__device__ __forceinline__ int unpack_code(const uint8_t* p, int bits, int i) {
+  if (bits == 8) return (int)(int8_t)p[i];
+  if (bits == 4) return (int)((p[i >> 1] >> ((i & 1) * 4)) & 0xF) - 8;
+  if (bits == 3) {
+    const uint8_t* q = p + (i >> 3) * 3;
+    uint32_t w = (uint32_t)q[0] | ((uint32_t)q[1] << 8) | ((uint32_t)q[2] << 16);
+    return (int)((w >> (3 * (i & 7))) & 7u) - 4;
+  }
+  return (int)((p[i >> 2] >> (2 * (i & 3))) & 3u) - 2;
+}
+
+__device__ __forceinline__ float block_scale(const uint8_t* blk) {
+  uint16_t sb = (uint16_t)blk[0] | ((uint16_t)blk[1] << 8);
+  return __half2float(__ushort_as_half(sb));
+}
+
+// Dequantizes a whole block into out[0..G-1] (code * scale, exact).
+__device__ __forceinline__ void dequant_block_serial(const uint8_t* blk, int G, int bits, float* out, int stride) {
+  const float sf = block_scale(blk);
+  for (int i = 0; i < G; ++i) out[i * stride] = (float)unpack_code(blk + 2, bits, i) * sf;
+}
+
+}  // namespace kvq

@@ -1,0 +1,105 @@
+// kvq_dequantize (blocks -> fp32 in the original domain) and the RoPE angle
+// tables used by decode for keys stored pre-RoPE.
+#include "block_codec.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kThreads = 128;
+
+// Value of element d of token t (stored domain) of one (layer, seq, head).
+__device__ float stored_value(const Layout& lo, const CachePtrs& cp, int which, int layer, int seq, int h, int t,
+                              int d, int qe, int ce, bool* bad) {
+  if (t >= qe) return in_to_f32(resid_row(lo, cp, which, layer, seq, h, t)[d], lo.dtype);
+  const bool cold = t < ce;
+  const FmtInfo& f = cold ? fmt_cold(lo, which) : fmt_main(lo, which);
+  const uint8_t* row = cold ? cold_row(lo, cp, which, layer, seq, h, t) : main_row(lo, cp, which, layer, seq, h, t, bad);
+  if (!row) return 0.0f;
+  if (f.axis == KVQ_AXIS_CHANNEL) {
+    const uint8_t* blk = row + (int64_t)d * f.bb;
+    return (float)unpack_code(blk + 2, f.bits, t % f.group) * block_scale(blk);
+  }
+  const uint8_t* blk = row + (int64_t)(d / f.group) * f.bb;
+  return (float)unpack_code(blk + 2, f.bits, d % f.group) * block_scale(blk);
+}
+
+__global__ void __launch_bounds__(kThreads) dequantize_kernel(DequantArgs a) {
+  extern __shared__ float xs[];  // [kTile][D]
+  const Layout& lo = a.lo;
+  const int D = lo.D, h = blockIdx.y;
+  const int T = a.seq_lens[a.seq];
+  if (T < 0 || T > lo.max_T || a.t1 > T) {
+    if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) atomicOr(a.status, KVQ_DEV_RANGE);
+    return;
+  }
+  const int qe = q_end_of(lo, T), ce = c_end_of(lo, T);
+  const int t0 = a.t0 + blockIdx.x * kTile;
+  const int n = min(kTile, a.t1 - t0);
+  if (n <= 0) return;
+  __shared__ uint32_t bad_page;
+  if (threadIdx.x == 0) bad_page = 0;
+  for (int which = 0; which < 2; ++which) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < n * D; e += blockDim.x) {
+      const int j = e / D, d = e % D;
+      bool bad = false;
+      xs[e] = stored_value(lo, a.cp, which, a.layer, a.seq, h, t0 + j, d, qe, ce, &bad);
+      if (bad) bad_page = 1;
+    }
+    __syncthreads();
+    if (lo.flags & (which ? KVQ_ROTATE_V : KVQ_ROTATE_K)) {
+      // quantized tokens are stored rotated: undo it; window tokens are raw
+      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+      for (int r = warp; r < n * (D / 128); r += nw) {
+        const int j = r / (D / 128);
+        if (t0 + j >= qe) continue;
+        float* p = xs + j * D + (r % (D / 128)) * 128 + 4 * lane;
+        float v[4] = {p[0], p[1], p[2], p[3]};
+        warp_unrotate128(v, lo.d1, lo.d2);
+        p[0] = v[0];
+        p[1] = v[1];
+        p[2] = v[2];
+        p[3] = v[3];
+      }
+      __syncthreads();
+    }
+    float* out = which ? a.v_out : a.k_out;
+    for (int e = threadIdx.x; e < n * D; e += blockDim.x) {
+      const int j = e / D, d = e % D;
+      out[((int64_t)(t0 + j - a.t0) * lo.H + h) * D + d] = xs[e];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && bad_page) atomicOr(a.status, KVQ_DEV_PAGE);
+}
+
+// base[r][i] = (cos, sin)(32 r theta_i), off[j][i] = (cos, sin)(j theta_i),
+// theta_i = theta^(-2i/D), evaluated in fp64 and rounded to fp32.
+__global__ void rope_tables_kernel(float2* rope, int base_rows, int D, double theta) {
+  const int half = D / 2;
+  const int total = (base_rows + kTile) * half;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+    const int r = e / half, i = e % half;
+    const double inv = pow(theta, -2.0 * i / D);
+    const double pos = r < base_rows ? (double)r * kTile : (double)(r - base_rows);
+    double s, c;
+    sincos(pos * inv, &s, &c);
+    rope[e] = make_float2((float)c, (float)s);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dequantize(const DequantArgs& a, cudaStream_t st) {
+  dim3 grid((a.t1 - a.t0 + kTile - 1) / kTile, a.lo.H);
+  const size_t smem = sizeof(float) * kTile * a.lo.D;
+  dequantize_kernel<<<grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_tables(float2* rope, int base_rows, int D, float theta, cudaStream_t st) {
+  rope_tables_kernel<<<256, 256, 0, st>>>(rope, base_rows, D, (double)theta);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,476 @@
+// Host side of the C ABI declared in include/kvq.h: argument validation,
+// the size law, buffer and workspace sizing, and kernel launches.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <string>
+
+#include "kvq_internal.cuh"
+
+using namespace kvq;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvq_status fail(kvq_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+kvq_status ok() {
+  g_last_error.clear();
+  return KVQ_OK;
+}
+
+kvq_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(KVQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool valid_bits(int bits, bool allow16) { return bits == 8 || bits == 4 || bits == 3 || bits == 2 || (allow16 && bits == 16); }
+
+kvq_status check_fmt(const kvq_fmt& f, int D, const char* name, bool allow16) {
+  if (!valid_bits(f.bits, allow16)) return fail(KVQ_ERR_ARG, "%s.bits=%d not in {8,4,3,2}", name, f.bits);
+  if (f.axis != KVQ_AXIS_TOKEN && f.axis != KVQ_AXIS_CHANNEL) return fail(KVQ_ERR_ARG, "%s.axis=%d", name, f.axis);
+  if (f.group != 32 && f.group != 128) return fail(KVQ_ERR_ARG, "%s.group=%d not in {32,128}", name, f.group);
+  if (f.axis == KVQ_AXIS_TOKEN && D % f.group != 0) return fail(KVQ_ERR_ARG, "%s.group=%d does not divide D=%d", name, f.group, D);
+  if (f.axis == KVQ_AXIS_CHANNEL && f.group != 32) return fail(KVQ_ERR_UNSUPPORTED, "%s: per-channel groups are 32 tokens", name);
+  if (f.bits == 16 && f.axis != KVQ_AXIS_TOKEN) return fail(KVQ_ERR_ARG, "%s: 16-bit storage is per-token", name);
+  return KVQ_OK;
+}
+
+// Checks shared by all entry points. allow16: size-law-only formats.
+kvq_status check_config(const kvq_config* c, bool allow16) {
+  if (!c) return fail(KVQ_ERR_ARG, "config is NULL");
+  if (c->reserved != 0) return fail(KVQ_ERR_ARG, "reserved must be 0");
+  if (c->L < 1 || c->H_kv < 1 || c->H_q < 1 || c->batch < 1 || c->max_T < 1)
+    return fail(KVQ_ERR_ARG, "L, H_kv, H_q, batch, max_T must be >= 1");
+  if (c->H_q % c->H_kv != 0) return fail(KVQ_ERR_ARG, "H_q=%d is not a multiple of H_kv=%d", c->H_q, c->H_kv);
+  if (c->H_q / c->H_kv > kMaxGqa) return fail(KVQ_ERR_UNSUPPORTED, "H_q/H_kv=%d > %d", c->H_q / c->H_kv, kMaxGqa);
+  if (c->D != 128 && c->D != 256) return fail(KVQ_ERR_UNSUPPORTED, "D=%d not in {128,256}", c->D);
+  if (c->in_dtype != KVQ_DT_F16 && c->in_dtype != KVQ_DT_BF16) return fail(KVQ_ERR_ARG, "in_dtype=%d", c->in_dtype);
+  kvq_status st;
+  if ((st = check_fmt(c->k_fmt, c->D, "k_fmt", allow16)) != KVQ_OK) return st;
+  if ((st = check_fmt(c->v_fmt, c->D, "v_fmt", allow16)) != KVQ_OK) return st;
+  if (c->hot_window < 0 || c->residual_window < 0) return fail(KVQ_ERR_ARG, "negative window");
+  int gam = 1;
+  if (c->k_fmt.axis == KVQ_AXIS_CHANNEL) gam = c->k_fmt.group;
+  if (c->v_fmt.axis == KVQ_AXIS_CHANNEL) gam = c->v_fmt.group;
+  if (c->hot_window > 0) {
+    if ((st = check_fmt(c->k_cold, c->D, "k_cold", allow16)) != KVQ_OK) return st;
+    if ((st = check_fmt(c->v_cold, c->D, "v_cold", allow16)) != KVQ_OK) return st;
+    if (c->k_cold.axis != c->k_fmt.axis || c->k_cold.group != c->k_fmt.group ||
+        c->v_cold.axis != c->v_fmt.axis || c->v_cold.group != c->v_fmt.group)
+      return fail(KVQ_ERR_UNSUPPORTED, "cold formats must keep the hot formats' axis and group");
+    if (gam == 1) return fail(KVQ_ERR_UNSUPPORTED, "hot/cold tiers need a per-channel (token-group) format");
+    if (c->hot_window % gam != 0) return fail(KVQ_ERR_ARG, "hot_window=%d not a multiple of %d", c->hot_window, gam);
+  }
+  uint32_t known = KVQ_ROTATE_K | KVQ_ROTATE_V | KVQ_K_PRE_ROPE;
+  if (c->flags & ~known) return fail(KVQ_ERR_ARG, "unknown flags 0x%x", c->flags & ~known);
+  if ((c->flags & KVQ_ROTATE_K) && c->k_fmt.axis != KVQ_AXIS_TOKEN)
+    return fail(KVQ_ERR_UNSUPPORTED, "rotation needs per-token K blocks");
+  if ((c->flags & KVQ_ROTATE_V) && c->v_fmt.axis != KVQ_AXIS_TOKEN)
+    return fail(KVQ_ERR_UNSUPPORTED, "rotation needs per-token V blocks");
+  if ((c->flags & KVQ_ROTATE_K) && (c->flags & KVQ_K_PRE_ROPE))
+    return fail(KVQ_ERR_UNSUPPORTED, "pre-RoPE keys with rotated K: RoPE pairs do not commute with the transform");
+  if ((c->flags & KVQ_K_PRE_ROPE) && !(c->rope_theta > 1.0f)) return fail(KVQ_ERR_ARG, "rope_theta must be > 1");
+  if (c->page_tokens < 0) return fail(KVQ_ERR_ARG, "page_tokens < 0");
+  if (c->page_tokens > 0) {
+    if (c->k_fmt.axis != KVQ_AXIS_TOKEN || c->v_fmt.axis != KVQ_AXIS_TOKEN || c->hot_window > 0)
+      return fail(KVQ_ERR_UNSUPPORTED, "paging needs per-token formats and one tier");
+    if (c->n_pages < 1) return fail(KVQ_ERR_ARG, "n_pages < 1");
+    if ((int64_t)c->max_pages_per_seq * c->page_tokens < c->max_T)
+      return fail(KVQ_ERR_ARG, "max_pages_per_seq * page_tokens < max_T");
+  }
+  return KVQ_OK;
+}
+
+FmtInfo make_fmt(const kvq_fmt& f, int D) {
+  FmtInfo r{};
+  if (f.bits == 0) return r;
+  r.bits = f.bits;
+  r.group = f.group;
+  r.axis = f.axis;
+  r.bb = block_bytes_of(f.bits, f.group);
+  r.qmax = f.bits == 16 ? 0 : qmax_of(f.bits);
+  r.row = f.axis == KVQ_AXIS_TOKEN ? (D / f.group) * r.bb : D * r.bb;
+  return r;
+}
+
+uint64_t splitmix64_next(uint64_t* state) {
+  // SplitMix64 (Steele, Lea and Flood, 2014).
+  uint64_t z = (*state += 0x9E3779B97F4A7C15ull);
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+Layout make_layout(const kvq_config* c) {
+  Layout lo{};
+  lo.L = c->L;
+  lo.B = c->batch;
+  lo.H = c->H_kv;
+  lo.Hq = c->H_q;
+  lo.D = c->D;
+  lo.g = c->H_q / c->H_kv;
+  lo.max_T = c->max_T;
+  lo.dtype = c->in_dtype;
+  lo.gam = 1;
+  if (c->k_fmt.axis == KVQ_AXIS_CHANNEL) lo.gam = c->k_fmt.group;
+  if (c->v_fmt.axis == KVQ_AXIS_CHANNEL) lo.gam = c->v_fmt.group;
+  lo.R = c->residual_window;
+  lo.W = c->hot_window;
+  lo.ring = (lo.R == 0 && lo.gam == 1) ? 0 : lo.R + lo.gam;
+  lo.tiered = c->hot_window > 0;
+  lo.paged = c->page_tokens > 0;
+  lo.pt = c->page_tokens;
+  lo.n_pages = c->n_pages;
+  lo.max_pages = c->max_pages_per_seq;
+  lo.flags = c->flags;
+  lo.theta = c->rope_theta;
+  if (c->sign_seed != 0) {
+    uint64_t st = c->sign_seed, w[4];
+    for (int i = 0; i < 4; ++i) w[i] = splitmix64_next(&st);
+    for (int j = 0; j < 4; ++j) {
+      lo.d1[j] = (uint32_t)(w[j / 2] >> (32 * (j % 2)));
+      lo.d2[j] = (uint32_t)(w[2 + j / 2] >> (32 * (j % 2)));
+    }
+  }
+  lo.kf = make_fmt(c->k_fmt, c->D);
+  lo.vf = make_fmt(c->v_fmt, c->D);
+  if (lo.tiered) {
+    lo.kc = make_fmt(c->k_cold, c->D);
+    lo.vc = make_fmt(c->v_cold, c->D);
+  }
+  auto rows_abs = [&](const FmtInfo& f) -> int64_t {
+    return f.axis == KVQ_AXIS_TOKEN ? (int64_t)c->max_T : (int64_t)((c->max_T + f.group - 1) / f.group);
+  };
+  auto rows_ring = [&](const FmtInfo& f) -> int {
+    return f.axis == KVQ_AXIS_TOKEN ? c->hot_window + lo.gam : c->hot_window / f.group + 1;
+  };
+  if (lo.tiered) {
+    lo.hot_ring_k = rows_ring(lo.kf);
+    lo.hot_ring_v = rows_ring(lo.vf);
+    lo.rows_k_main = lo.hot_ring_k;
+    lo.rows_v_main = lo.hot_ring_v;
+    lo.rows_k_cold = rows_abs(lo.kc);
+    lo.rows_v_cold = rows_abs(lo.vc);
+  } else {
+    lo.rows_k_main = rows_abs(lo.kf);
+    lo.rows_v_main = rows_abs(lo.vf);
+  }
+  return lo;
+}
+
+int64_t fmt_bytes(const kvq_fmt& f, int64_t n_tokens, int D) {
+  int64_t bb = block_bytes_of(f.bits, f.group);
+  if (f.axis == KVQ_AXIS_TOKEN) return n_tokens * (D / f.group) * bb;
+  return (n_tokens / f.group) * D * bb;
+}
+
+int splits_for(const kvq_config* c, int n_layers) {
+  int64_t units = (int64_t)n_layers * c->batch * c->H_kv;
+  int64_t tiles = (c->max_T + kTile - 1) / kTile + 2;
+  int64_t s = (kTargetCtas + units - 1) / units;
+  int64_t cap = tiles / 4;
+  if (cap < 1) cap = 1;
+  if (s > cap) s = cap;
+  if (s > kMaxSplits) s = kMaxSplits;
+  if (s < 1) s = 1;
+  return (int)s;
+}
+
+size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+WsLayout ws_layout(const kvq_config* c) {
+  WsLayout w{};
+  int g = c->H_q / c->H_kv;
+  w.status = 0;
+  w.tickets = kWsAlign;
+  w.max_units = c->L * c->batch * c->H_kv;
+  size_t off = align_up(w.tickets + sizeof(uint32_t) * (size_t)w.max_units);
+  w.rope = off;
+  if (c->flags & KVQ_K_PRE_ROPE) {
+    w.rope_base_rows = (c->max_T + kTile - 1) / kTile + 1;
+    off = align_up(off + sizeof(float2) * (size_t)(w.rope_base_rows + kTile) * (c->D / 2));
+  }
+  w.partials = off;
+  int64_t mp = 0;
+  for (int n = 1; n <= c->L; ++n) {
+    int s = splits_for(c, n);
+    if (s > 1) {
+      int64_t p = (int64_t)n * c->batch * c->H_kv * s;
+      if (p > mp) mp = p;
+    }
+  }
+  // explicit split counts up to kMaxSplits for one layer are also allowed
+  int64_t one = (int64_t)c->batch * c->H_kv * kMaxSplits;
+  if (one > mp) mp = one;
+  w.max_partials = (int)mp;
+  off = align_up(off + sizeof(float) * (size_t)mp * g * (c->D + 2));
+  w.total = off;
+  return w;
+}
+
+kvq_status check_ws(const kvq_config* c, void* ws, size_t bytes, WsLayout* out) {
+  if (!ws) return fail(KVQ_ERR_WORKSPACE, "workspace is NULL");
+  WsLayout w = ws_layout(c);
+  if (bytes < w.total) return fail(KVQ_ERR_WORKSPACE, "workspace %zu B < %zu B needed", bytes, w.total);
+  if (((uintptr_t)ws) % kWsAlign) return fail(KVQ_ERR_WORKSPACE, "workspace not 256-byte aligned");
+  *out = w;
+  return KVQ_OK;
+}
+
+kvq_status cache_ptrs(const kvq_config* c, const kvq_cache* cache, CachePtrs* cp) {
+  if (!cache) return fail(KVQ_ERR_ARG, "cache is NULL");
+  cp->k_main = (uint8_t*)cache->k_main;
+  cp->v_main = (uint8_t*)cache->v_main;
+  cp->k_cold = (uint8_t*)cache->k_cold;
+  cp->v_cold = (uint8_t*)cache->v_cold;
+  cp->k_resid = (uint16_t*)cache->k_resid;
+  cp->v_resid = (uint16_t*)cache->v_resid;
+  cp->block_table = cache->block_table;
+  if (!cp->k_main || !cp->v_main) return fail(KVQ_ERR_ARG, "k_main / v_main is NULL");
+  if (c->hot_window > 0 && (!cp->k_cold || !cp->v_cold)) return fail(KVQ_ERR_ARG, "cold buffers are NULL");
+  int gam = (c->k_fmt.axis == KVQ_AXIS_CHANNEL || c->v_fmt.axis == KVQ_AXIS_CHANNEL) ? 32 : 1;
+  bool ring = !(c->residual_window == 0 && gam == 1);
+  if (ring && (!cp->k_resid || !cp->v_resid)) return fail(KVQ_ERR_ARG, "window buffers are NULL");
+  if (c->page_tokens > 0 && !cp->block_table) return fail(KVQ_ERR_ARG, "block_table is NULL");
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_version(void) { return "kvq 0.1 (sm_103a)"; }
+
+const char* kvq_last_error(void) { return g_last_error.c_str(); }
+
+kvq_status kvq_validate_config(const kvq_config* cfg) {
+  kvq_status st = check_config(cfg, false);
+  return st == KVQ_OK ? ok() : st;
+}
+
+kvq_status kvq_block_bytes(int32_t bits, int32_t group, int32_t* bytes) {
+  if (!bytes) return fail(KVQ_ERR_ARG, "bytes is NULL");
+  if (!valid_bits(bits, true) || (group != 32 && group != 128)) return fail(KVQ_ERR_ARG, "bits=%d group=%d", bits, group);
+  *bytes = block_bytes_of(bits, group);
+  return ok();
+}
+
+kvq_status kvq_bytes_per_token(const kvq_config* cfg, int64_t* bytes) {
+  kvq_status st = check_config(cfg, true);
+  if (st != KVQ_OK) return st;
+  if (!bytes) return fail(KVQ_ERR_ARG, "bytes is NULL");
+  const kvq_fmt& kf = cfg->hot_window > 0 ? cfg->k_cold : cfg->k_fmt;
+  const kvq_fmt& vf = cfg->hot_window > 0 ? cfg->v_cold : cfg->v_fmt;
+  int64_t per_head = 0;
+  for (const kvq_fmt* f : {&kf, &vf}) {
+    int64_t bb = block_bytes_of(f->bits, f->group);
+    if (f->axis == KVQ_AXIS_TOKEN) {
+      per_head += (cfg->D / f->group) * bb;
+    } else {
+      if ((cfg->D * bb) % f->group) return fail(KVQ_ERR_ARG, "fractional bytes per token");
+      per_head += cfg->D * bb / f->group;
+    }
+  }
+  *bytes = (int64_t)cfg->L * cfg->H_kv * per_head;
+  return ok();
+}
+
+kvq_status kvq_cache_bytes(const kvq_config* cfg, int64_t T, int64_t* bytes) {
+  kvq_status st = check_config(cfg, true);
+  if (st != KVQ_OK) return st;
+  if (!bytes || T < 0) return fail(KVQ_ERR_ARG, "bytes is NULL or T < 0");
+  Layout lo = make_layout(cfg);
+  int64_t qe = T <= lo.R ? 0 : ((T - lo.R) / lo.gam) * lo.gam;
+  int64_t ce = 0;
+  if (lo.W > 0 && qe > lo.W) ce = ((qe - lo.W) / lo.gam) * lo.gam;
+  int64_t per_head = 0;
+  if (lo.W > 0) per_head += fmt_bytes(cfg->k_cold, ce, cfg->D) + fmt_bytes(cfg->v_cold, ce, cfg->D);
+  per_head += fmt_bytes(cfg->k_fmt, qe - ce, cfg->D) + fmt_bytes(cfg->v_fmt, qe - ce, cfg->D);
+  per_head += 2 * (T - qe) * cfg->D * 2;
+  *bytes = (int64_t)cfg->L * cfg->H_kv * per_head;
+  return ok();
+}
+
+kvq_status kvq_buffer_sizes(const kvq_config* cfg, size_t sizes[6]) {
+  kvq_status st = check_config(cfg, false);
+  if (st != KVQ_OK) return st;
+  if (!sizes) return fail(KVQ_ERR_ARG, "sizes is NULL");
+  Layout lo = make_layout(cfg);
+  size_t per_lbh = (size_t)lo.L * lo.B * lo.H;
+  for (int i = 0; i < 6; ++i) sizes[i] = 0;
+  if (lo.paged) {
+    size_t per_page = (size_t)lo.L * lo.n_pages * lo.H * lo.pt;
+    sizes[0] = per_page * lo.kf.row;
+    sizes[1] = per_page * lo.vf.row;
+  } else {
+    sizes[0] = per_lbh * (size_t)lo.rows_k_main * lo.kf.row;
+    sizes[1] = per_lbh * (size_t)lo.rows_v_main * lo.vf.row;
+  }
+  if (lo.tiered) {
+    sizes[2] = per_lbh * (size_t)lo.rows_k_cold * lo.kc.row;
+    sizes[3] = per_lbh * (size_t)lo.rows_v_cold * lo.vc.row;
+  }
+  if (lo.ring) {
+    sizes[4] = per_lbh * (size_t)lo.ring * lo.D * 2;
+    sizes[5] = sizes[4];
+  }
+  return ok();
+}
+
+kvq_status kvq_workspace_bytes(const kvq_config* cfg, size_t* bytes) {
+  kvq_status st = check_config(cfg, false);
+  if (st != KVQ_OK) return st;
+  if (!bytes) return fail(KVQ_ERR_ARG, "bytes is NULL");
+  *bytes = ws_layout(cfg).total;
+  return ok();
+}
+
+kvq_status kvq_decode_splits(const kvq_config* cfg, int32_t n_layers, int32_t* splits) {
+  kvq_status st = check_config(cfg, false);
+  if (st != KVQ_OK) return st;
+  if (!splits || n_layers < 1 || n_layers > cfg->L) return fail(KVQ_ERR_ARG, "bad n_layers or NULL");
+  *splits = splits_for(cfg, n_layers);
+  return ok();
+}
+
+kvq_status kvq_workspace_init(const kvq_config* cfg, void* workspace, size_t ws_bytes, void* stream) {
+  kvq_status st = check_config(cfg, false);
+  if (st != KVQ_OK) return st;
+  WsLayout w;
+  if ((st = check_ws(cfg, workspace, ws_bytes, &w)) != KVQ_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, w.rope, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  if (cfg->flags & KVQ_K_PRE_ROPE) {
+    e = launch_rope_tables((float2*)((char*)workspace + w.rope), w.rope_base_rows, cfg->D, cfg->rope_theta, s);
+    if (e != cudaSuccess) return cuda_fail(e, "rope table kernel");
+  }
+  return ok();
+}
+
+kvq_status kvq_append(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0, int32_t n_layers,
+                      const void* k, const void* v, const int32_t* cu_new, const int32_t* seq_lens,
+                      int32_t total_new, int32_t max_new, void* workspace, size_t ws_bytes, void* stream) {
+  kvq_status st = check_config(cfg, false);
+  if (st != KVQ_OK) return st;
+  if (layer0 < 0 || n_layers < 1 || layer0 + n_layers > cfg->L)
+    return fail(KVQ_ERR_ARG, "layers [%d, %d) outside [0, %d)", layer0, layer0 + n_layers, cfg->L);
+  if (total_new < 0 || max_new < 0 || max_new > total_new) return fail(KVQ_ERR_ARG, "total_new / max_new");
+  if (max_new > cfg->max_T) return fail(KVQ_ERR_CAPACITY, "max_new=%d > max_T=%d", max_new, cfg->max_T);
+  if (total_new > 0 && (!k || !v)) return fail(KVQ_ERR_ARG, "k / v is NULL");
+  if (!cu_new || !seq_lens) return fail(KVQ_ERR_ARG, "cu_new / seq_lens is NULL");
+  AppendArgs a{};
+  if ((st = cache_ptrs(cfg, cache, &a.cp)) != KVQ_OK) return st;
+  WsLayout w;
+  if ((st = check_ws(cfg, workspace, ws_bytes, &w)) != KVQ_OK) return st;
+  a.lo = make_layout(cfg);
+  a.layer0 = layer0;
+  a.n_layers = n_layers;
+  a.k = (const uint16_t*)k;
+  a.v = (const uint16_t*)v;
+  a.cu_new = cu_new;
+  a.seq_lens = seq_lens;
+  a.total_new = total_new;
+  a.max_new = max_new;
+  a.status = (uint32_t*)((char*)workspace + w.status);
+  cudaError_t e = launch_append(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "append kernels");
+  return ok();
+}
+
+kvq_status kvq_commit_lengths(const kvq_config* cfg, const int32_t* cu_new, int32_t* seq_lens, void* stream) {
+  kvq_status st = check_config(cfg, false);
+  if (st != KVQ_OK) return st;
+  if (!cu_new || !seq_lens) return fail(KVQ_ERR_ARG, "cu_new / seq_lens is NULL");
+  cudaError_t e = launch_commit_lengths(cu_new, seq_lens, cfg->batch, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "commit kernel");
+  return ok();
+}
+
+kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0,
+                                int32_t n_layers, const void* q, const int32_t* seq_lens, float* out,
+                                int32_t num_splits, void* workspace, size_t ws_bytes, void* stream) {
+  kvq_status st = check_config(cfg, false);
+  if (st != KVQ_OK) return st;
+  if (layer0 < 0 || n_layers < 1 || layer0 + n_layers > cfg->L)
+    return fail(KVQ_ERR_ARG, "layers [%d, %d) outside [0, %d)", layer0, layer0 + n_layers, cfg->L);
+  if (!q || !seq_lens || !out) return fail(KVQ_ERR_ARG, "q / seq_lens / out is NULL");
+  if (num_splits < 0 || num_splits > kMaxSplits) return fail(KVQ_ERR_ARG, "num_splits=%d", num_splits);
+  DecodeArgs a{};
+  if ((st = cache_ptrs(cfg, cache, &a.cp)) != KVQ_OK) return st;
+  WsLayout w;
+  if ((st = check_ws(cfg, workspace, ws_bytes, &w)) != KVQ_OK) return st;
+  int splits = num_splits ? num_splits : splits_for(cfg, n_layers);
+  int64_t units = (int64_t)n_layers * cfg->batch * cfg->H_kv;
+  if (splits > 1 && units * splits > w.max_partials)
+    return fail(KVQ_ERR_WORKSPACE, "%d splits x %lld units exceed the workspace", splits, (long long)units);
+  a.lo = make_layout(cfg);
+  a.layer0 = layer0;
+  a.n_layers = n_layers;
+  a.q = (const uint16_t*)q;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.splits = splits;
+  a.status = (uint32_t*)((char*)workspace + w.status);
+  a.tickets = (uint32_t*)((char*)workspace + w.tickets);
+  a.partials = (float*)((char*)workspace + w.partials);
+  a.rope = (const float2*)((char*)workspace + w.rope);
+  a.rope_base_rows = w.rope_base_rows;
+  cudaError_t e = launch_decode(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+  return ok();
+}
+
+kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_cache* cache, int32_t layer, int32_t seq,
+                          int32_t t0, int32_t t1, const int32_t* seq_lens, float* k_out, float* v_out,
+                          void* workspace, size_t ws_bytes, void* stream) {
+  kvq_status st = check_config(cfg, false);
+  if (st != KVQ_OK) return st;
+  if (layer < 0 || layer >= cfg->L || seq < 0 || seq >= cfg->batch) return fail(KVQ_ERR_ARG, "layer / seq out of range");
+  if (t0 < 0 || t1 < t0 || t1 > cfg->max_T) return fail(KVQ_ERR_ARG, "token range [%d, %d)", t0, t1);
+  if (!seq_lens || !k_out || !v_out) return fail(KVQ_ERR_ARG, "seq_lens / k_out / v_out is NULL");
+  DequantArgs a{};
+  if ((st = cache_ptrs(cfg, cache, &a.cp)) != KVQ_OK) return st;
+  WsLayout w;
+  if ((st = check_ws(cfg, workspace, ws_bytes, &w)) != KVQ_OK) return st;
+  if (t1 == t0) return ok();
+  a.lo = make_layout(cfg);
+  a.layer = layer;
+  a.seq = seq;
+  a.t0 = t0;
+  a.t1 = t1;
+  a.seq_lens = seq_lens;
+  a.k_out = k_out;
+  a.v_out = v_out;
+  a.status = (uint32_t*)((char*)workspace + w.status);
+  cudaError_t e = launch_dequantize(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dequantize kernel");
+  return ok();
+}
+
+kvq_status kvq_read_device_status(const void* workspace, uint32_t* bits, void* stream) {
+  if (!workspace || !bits) return fail(KVQ_ERR_ARG, "workspace / bits is NULL");
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(bits, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  return ok();
+}
+
+kvq_status kvq_clear_device_status(void* workspace, void* stream) {
+  if (!workspace) return fail(KVQ_ERR_ARG, "workspace is NULL");
+  cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  return ok();
+}
+
+}  // extern "C"

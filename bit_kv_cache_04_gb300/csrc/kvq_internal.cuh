@@ -1,0 +1,197 @@
+// Internal definitions shared by the libkvq translation units: the derived
+// cache layout (POD, passed to kernels by value), tier arithmetic and
+// address helpers.  Everything here follows the contract stated in kvq.h.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+#define KVQ_HD __host__ __device__ __forceinline__
+
+namespace kvq {
+
+constexpr int kTile = 32;        // tokens per decode / append tile
+constexpr int kMaxGqa = 8;       // query heads per kv head
+constexpr int kTargetCtas = 608; // 4 x 152 SMs: split heuristic target
+constexpr int kMaxSplits = 256;
+constexpr size_t kWsAlign = 256;
+
+struct FmtInfo {
+  int bits;   // 8, 4, 3, 2 (0 = unused)
+  int group;  // G
+  int axis;   // KVQ_AXIS_*
+  int bb;     // block bytes
+  int qmax;   // 2^(bits-1) - 1
+  int row;    // bytes of one storage row
+};
+
+// Everything a kernel needs to find a byte of the cache.
+struct Layout {
+  int L, B, H, Hq, D, g;
+  int max_T;
+  int dtype;
+  int gam;         // Gamma: token granularity of quantization
+  int R;           // 16-bit window
+  int W;           // hot window (0 = one tier)
+  int ring;        // window ring slots (0 = none)
+  int tiered, paged;
+  int pt, n_pages, max_pages;
+  uint32_t flags;
+  float theta;
+  uint32_t d1[4], d2[4];  // Hadamard sign masks (bit set = -1)
+  FmtInfo kf, vf, kc, vc;
+  int64_t rows_k_main, rows_v_main;  // rows per (layer, seq, head) of the main tier (contiguous / ring)
+  int64_t rows_k_cold, rows_v_cold;
+  int hot_ring_k, hot_ring_v;        // ring length of the hot tier (rows) when tiered
+};
+
+struct CachePtrs {
+  uint8_t* k_main;
+  uint8_t* v_main;
+  uint8_t* k_cold;
+  uint8_t* v_cold;
+  uint16_t* k_resid;
+  uint16_t* v_resid;
+  const int32_t* block_table;
+};
+
+// Workspace layout offsets (bytes).
+struct WsLayout {
+  size_t status;    // uint32 status word
+  size_t tickets;   // uint32 per decode unit
+  size_t rope;      // float2 base[n_base][D/2] then off[kTile][D/2]
+  size_t partials;  // float per (unit, split): g * (D + 2)
+  size_t total;
+  int max_units;
+  int max_partials;  // unit-split pairs
+  int rope_base_rows;
+};
+
+KVQ_HD int qmax_of(int bits) { return (1 << (bits - 1)) - 1; }
+
+KVQ_HD int block_bytes_of(int bits, int group) {
+  return bits == 16 ? 2 * group : 2 + group * bits / 8;
+}
+
+// ---- tier arithmetic ------------------------------------------------------
+
+KVQ_HD int q_end_of(const Layout& lo, int T) {
+  if (T <= lo.R) return 0;
+  return ((T - lo.R) / lo.gam) * lo.gam;
+}
+
+KVQ_HD int c_end_of(const Layout& lo, int T) {
+  if (lo.W <= 0) return 0;
+  int qe = q_end_of(lo, T);
+  if (qe <= lo.W) return 0;
+  return ((qe - lo.W) / lo.gam) * lo.gam;
+}
+
+// ---- addresses --------------------------------------------------------------
+
+KVQ_HD const FmtInfo& fmt_main(const Layout& lo, int which) { return which ? lo.vf : lo.kf; }
+KVQ_HD const FmtInfo& fmt_cold(const Layout& lo, int which) { return which ? lo.vc : lo.kc; }
+
+// Main-tier row holding token t (per-token) or group t/G (per-channel);
+// nullptr (and *bad set) for a page id out of range.
+KVQ_HD uint8_t* main_row(const Layout& lo, const CachePtrs& cp, int which, int layer, int seq, int h,
+                         int t, bool* bad) {
+  const FmtInfo& f = fmt_main(lo, which);
+  uint8_t* base = which ? cp.v_main : cp.k_main;
+  if (lo.paged) {
+    int page = cp.block_table[(int64_t)seq * lo.max_pages + t / lo.pt];
+    if (page < 0 || page >= lo.n_pages) {
+      *bad = true;
+      return nullptr;
+    }
+    int64_t idx = (((int64_t)layer * lo.n_pages + page) * lo.H + h) * lo.pt + (t % lo.pt);
+    return base + idx * f.row;
+  }
+  int64_t rows = which ? lo.rows_v_main : lo.rows_k_main;
+  int64_t r;
+  if (f.axis == KVQ_AXIS_CHANNEL) {
+    int gi = t / f.group;
+    r = lo.tiered ? (gi % (which ? lo.hot_ring_v : lo.hot_ring_k)) : gi;
+  } else {
+    r = lo.tiered ? (t % (which ? lo.hot_ring_v : lo.hot_ring_k)) : t;
+  }
+  int64_t idx = (((int64_t)layer * lo.B + seq) * lo.H + h) * rows + r;
+  return base + idx * f.row;
+}
+
+KVQ_HD uint8_t* cold_row(const Layout& lo, const CachePtrs& cp, int which, int layer, int seq, int h, int t) {
+  const FmtInfo& f = fmt_cold(lo, which);
+  uint8_t* base = which ? cp.v_cold : cp.k_cold;
+  int64_t rows = which ? lo.rows_v_cold : lo.rows_k_cold;
+  int64_t r = (f.axis == KVQ_AXIS_CHANNEL) ? t / f.group : t;
+  int64_t idx = (((int64_t)layer * lo.B + seq) * lo.H + h) * rows + r;
+  return base + idx * f.row;
+}
+
+KVQ_HD uint16_t* resid_row(const Layout& lo, const CachePtrs& cp, int which, int layer, int seq, int h, int t) {
+  uint16_t* base = which ? cp.v_resid : cp.k_resid;
+  int64_t idx = (((int64_t)layer * lo.B + seq) * lo.H + h) * lo.ring + (t % lo.ring);
+  return base + idx * lo.D;
+}
+
+// ---- number helpers -----------------------------------------------------------
+
+__device__ __forceinline__ float in_to_f32(uint16_t bits, int dtype) {
+  if (dtype == KVQ_DT_F16) return __half2float(__ushort_as_half(bits));
+  return __uint_as_float(((uint32_t)bits) << 16);
+}
+
+__device__ __forceinline__ float sign_of(const uint32_t* mask, int i) {
+  return ((mask[i >> 5] >> (i & 31)) & 1u) ? -1.0f : 1.0f;
+}
+
+// ---- launchers (defined in the kernel translation units) -------------------
+
+struct AppendArgs {
+  Layout lo;
+  CachePtrs cp;
+  int layer0, n_layers;
+  const uint16_t* k;
+  const uint16_t* v;
+  const int32_t* cu_new;
+  const int32_t* seq_lens;
+  int total_new, max_new;
+  uint32_t* status;
+};
+
+struct DecodeArgs {
+  Layout lo;
+  CachePtrs cp;
+  int layer0, n_layers;
+  const uint16_t* q;
+  const int32_t* seq_lens;
+  float* out;
+  int splits;
+  uint32_t* status;
+  uint32_t* tickets;
+  float* partials;
+  const float2* rope;  // base rows then offsets
+  int rope_base_rows;
+};
+
+struct DequantArgs {
+  Layout lo;
+  CachePtrs cp;
+  int layer, seq, t0, t1;
+  const int32_t* seq_lens;
+  float* k_out;
+  float* v_out;
+  uint32_t* status;
+};
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_commit_lengths(const int32_t* cu_new, int32_t* seq_lens, int batch, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_dequantize(const DequantArgs& a, cudaStream_t s);
+cudaError_t launch_rope_tables(float2* rope, int base_rows, int D, float theta, cudaStream_t s);
+
+}  // namespace kvq

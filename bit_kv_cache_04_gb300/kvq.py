@@ -1,0 +1,273 @@
+"""ctypes binding of libkvq (include/kvq.h), plus a small cache holder.
+
+Argument marshalling only: every step of append, decode attention and
+dequantization runs in the library's CUDA kernels.  PyTorch provides device
+memory and streams.  Importing this module without a built libkvq.so raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass, field, fields
+from typing import Optional, Tuple
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvq.so")
+
+AXIS_TOKEN = 0
+AXIS_CHANNEL = 1
+ROTATE_K = 1
+ROTATE_V = 2
+K_PRE_ROPE = 4
+DT_F16 = 0
+DT_BF16 = 1
+
+DEV_CAPACITY = 1
+DEV_PAGE = 2
+DEV_RANGE = 4
+DEV_LENGTH = 8
+
+STATUS_NAMES = {0: "OK", 1: "ERR_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_CUDA", 4: "ERR_CAPACITY", 5: "ERR_WORKSPACE"}
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class _Fmt(ctypes.Structure):
+    _fields_ = [("bits", ctypes.c_int32), ("group", ctypes.c_int32), ("axis", ctypes.c_int32)]
+
+
+class _Config(ctypes.Structure):
+    _fields_ = [
+        ("L", ctypes.c_int32), ("H_kv", ctypes.c_int32), ("H_q", ctypes.c_int32), ("D", ctypes.c_int32),
+        ("batch", ctypes.c_int32), ("max_T", ctypes.c_int32), ("in_dtype", ctypes.c_int32),
+        ("k_fmt", _Fmt), ("v_fmt", _Fmt), ("k_cold", _Fmt), ("v_cold", _Fmt),
+        ("hot_window", ctypes.c_int32), ("residual_window", ctypes.c_int32),
+        ("flags", ctypes.c_uint32), ("rope_theta", ctypes.c_float), ("sign_seed", ctypes.c_uint64),
+        ("page_tokens", ctypes.c_int32), ("n_pages", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+class _Cache(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("k_main", "v_main", "k_cold", "v_cold", "k_resid", "v_resid",
+                                                  "block_table")]
+
+
+@dataclass(frozen=True)
+class Fmt:
+    bits: int
+    group: int
+    axis: int = AXIS_TOKEN
+
+
+@dataclass
+class Config:
+    """Mirror of kvq_config."""
+
+    L: int
+    H_kv: int
+    H_q: int
+    D: int
+    batch: int
+    max_T: int
+    in_dtype: int = DT_F16
+    k_fmt: Fmt = Fmt(4, 32)
+    v_fmt: Fmt = Fmt(4, 32)
+    k_cold: Optional[Fmt] = None
+    v_cold: Optional[Fmt] = None
+    hot_window: int = 0
+    residual_window: int = 0
+    flags: int = 0
+    rope_theta: float = 10000.0
+    sign_seed: int = 0
+    page_tokens: int = 0
+    n_pages: int = 0
+    max_pages_per_seq: int = 0
+
+    def to_c(self) -> _Config:
+        c = _Config()
+        for f in fields(self):
+            v = getattr(self, f.name)
+            if isinstance(v, Fmt) or (v is None and f.name in ("k_cold", "v_cold")):
+                v = v or Fmt(0, 0, 0)
+                setattr(c, f.name, _Fmt(v.bits, v.group, v.axis))
+            else:
+                setattr(c, f.name, v)
+        c.reserved = 0
+        return c
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER
+    vp, i32, i64, u32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_size_t
+    cfgp, cachep = P(_Config), P(_Cache)
+    sig = {
+        "kvq_version": ([], ctypes.c_char_p),
+        "kvq_last_error": ([], ctypes.c_char_p),
+        "kvq_validate_config": ([cfgp], ctypes.c_int),
+        "kvq_block_bytes": ([i32, i32, P(i32)], ctypes.c_int),
+        "kvq_bytes_per_token": ([cfgp, P(i64)], ctypes.c_int),
+        "kvq_cache_bytes": ([cfgp, i64, P(i64)], ctypes.c_int),
+        "kvq_buffer_sizes": ([cfgp, P(sz)], ctypes.c_int),
+        "kvq_workspace_bytes": ([cfgp, P(sz)], ctypes.c_int),
+        "kvq_workspace_init": ([cfgp, vp, sz, vp], ctypes.c_int),
+        "kvq_append": ([cfgp, cachep, i32, i32, vp, vp, vp, vp, i32, i32, vp, sz, vp], ctypes.c_int),
+        "kvq_commit_lengths": ([cfgp, vp, vp, vp], ctypes.c_int),
+        "kvq_decode_attention": ([cfgp, cachep, i32, i32, vp, vp, vp, i32, vp, sz, vp], ctypes.c_int),
+        "kvq_decode_splits": ([cfgp, i32, P(i32)], ctypes.c_int),
+        "kvq_dequantize": ([cfgp, cachep, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "kvq_read_device_status": ([vp, P(u32), vp], ctypes.c_int),
+        "kvq_clear_device_status": ([vp, vp], ctypes.c_int),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+LIB = _load()
+
+# C-ABI names declared in include/kvq.h (checked by the tests).
+EXPORTED = ("kvq_version", "kvq_last_error", "kvq_validate_config", "kvq_block_bytes", "kvq_bytes_per_token",
+            "kvq_cache_bytes", "kvq_buffer_sizes", "kvq_workspace_bytes", "kvq_workspace_init", "kvq_append",
+            "kvq_commit_lengths", "kvq_decode_attention", "kvq_decode_splits", "kvq_dequantize",
+            "kvq_read_device_status", "kvq_clear_device_status")
+
+
+def _check(st: int):
+    if st != 0:
+        raise KvqError(st, LIB.kvq_last_error().decode())
+
+
+# ---- thin wrappers, same names as the C ABI --------------------------------
+
+
+def kvq_version() -> str:
+    return LIB.kvq_version().decode()
+
+
+def kvq_validate_config(cfg: Config) -> None:
+    _check(LIB.kvq_validate_config(ctypes.byref(cfg.to_c())))
+
+
+def kvq_block_bytes(bits: int, group: int) -> int:
+    out = ctypes.c_int32()
+    _check(LIB.kvq_block_bytes(bits, group, ctypes.byref(out)))
+    return out.value
+
+
+def kvq_bytes_per_token(cfg: Config) -> int:
+    out = ctypes.c_int64()
+    _check(LIB.kvq_bytes_per_token(ctypes.byref(cfg.to_c()), ctypes.byref(out)))
+    return out.value
+
+
+def kvq_cache_bytes(cfg: Config, T: int) -> int:
+    out = ctypes.c_int64()
+    _check(LIB.kvq_cache_bytes(ctypes.byref(cfg.to_c()), T, ctypes.byref(out)))
+    return out.value
+
+
+def kvq_buffer_sizes(cfg: Config) -> Tuple[int, ...]:
+    arr = (ctypes.c_size_t * 6)()
+    _check(LIB.kvq_buffer_sizes(ctypes.byref(cfg.to_c()), arr))
+    return tuple(arr)
+
+
+def kvq_workspace_bytes(cfg: Config) -> int:
+    out = ctypes.c_size_t()
+    _check(LIB.kvq_workspace_bytes(ctypes.byref(cfg.to_c()), ctypes.byref(out)))
+    return out.value
+
+
+def kvq_decode_splits(cfg: Config, n_layers: int) -> int:
+    out = ctypes.c_int32()
+    _check(LIB.kvq_decode_splits(ctypes.byref(cfg.to_c()), n_layers, ctypes.byref(out)))
+    return out.value
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+BUFFER_NAMES = ("k_main", "v_main", "k_cold", "v_cold", "k_resid", "v_resid")
+
+
+class KVCache:
+    """Device buffers (torch tensors) of one quantized cache plus its workspace."""
+
+    def __init__(self, cfg: Config, device="cuda", block_table=None):
+        import torch
+
+        self.cfg = cfg
+        self.c_cfg = cfg.to_c()
+        self.device = torch.device(device)
+        sizes = kvq_buffer_sizes(cfg)
+        self.buffers = {}
+        for name, n in zip(BUFFER_NAMES, sizes):
+            self.buffers[name] = torch.zeros(n, dtype=torch.uint8, device=self.device) if n else None
+        self.block_table = None
+        if block_table is not None:
+            self.block_table = torch.as_tensor(block_table, dtype=torch.int32).to(self.device).contiguous()
+        self.ws_bytes = kvq_workspace_bytes(cfg)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        self.c_cache = _Cache(*[_ptr(self.buffers[n]) for n in BUFFER_NAMES], _ptr(self.block_table))
+        _check(LIB.kvq_workspace_init(ctypes.byref(self.c_cfg), _ptr(self.workspace), self.ws_bytes,
+                                      _stream(None)))
+
+    # -- the C calls ----------------------------------------------------------
+
+    def append(self, layer0, n_layers, k, v, cu_new, seq_lens, total_new, max_new, stream=None):
+        _check(LIB.kvq_append(ctypes.byref(self.c_cfg), ctypes.byref(self.c_cache), layer0, n_layers,
+                              _ptr(k), _ptr(v), _ptr(cu_new), _ptr(seq_lens), total_new, max_new,
+                              _ptr(self.workspace), self.ws_bytes, _stream(stream)))
+
+    def commit_lengths(self, cu_new, seq_lens, stream=None):
+        _check(LIB.kvq_commit_lengths(ctypes.byref(self.c_cfg), _ptr(cu_new), _ptr(seq_lens), _stream(stream)))
+
+    def decode(self, layer0, n_layers, q, seq_lens, out, num_splits=0, stream=None):
+        _check(LIB.kvq_decode_attention(ctypes.byref(self.c_cfg), ctypes.byref(self.c_cache), layer0, n_layers,
+                                        _ptr(q), _ptr(seq_lens), _ptr(out), num_splits,
+                                        _ptr(self.workspace), self.ws_bytes, _stream(stream)))
+
+    def dequantize(self, layer, seq, t0, t1, seq_lens, k_out, v_out, stream=None):
+        _check(LIB.kvq_dequantize(ctypes.byref(self.c_cfg), ctypes.byref(self.c_cache), layer, seq, t0, t1,
+                                  _ptr(seq_lens), _ptr(k_out), _ptr(v_out), _ptr(self.workspace), self.ws_bytes,
+                                  _stream(stream)))
+
+    def device_status(self, stream=None) -> int:
+        out = ctypes.c_uint32()
+        _check(LIB.kvq_read_device_status(_ptr(self.workspace), ctypes.byref(out), _stream(stream)))
+        return out.value
+
+    def clear_status(self, stream=None):
+        _check(LIB.kvq_clear_device_status(_ptr(self.workspace), _stream(stream)))
+
+    def buffer_numpy(self) -> dict:
+        """Host copies of the buffers shaped as the oracle expects (tests only)."""
+        import numpy as np
+
+        out = {}
+        for n in BUFFER_NAMES:
+            t = self.buffers[n]
+            if t is not None:
+                a = t.cpu().numpy()
+                out[n] = a.view(np.uint16) if n.endswith("resid") else a
+        return out

@@ -1,0 +1,248 @@
+/*
+ * kvq.h - C ABI of libkvq: a quantized KV cache for decode attention on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow five web pages on KV-cache quantization:
+ *  - troisinh.com "KV Cache Quantization - Nen cache INT4/INT3" (sections
+ *    "Tai sao Key va Value lai khac nhau?", "Mixed Precision", "Tai sao no
+ *    hoat dong": per-channel keys, per-token values, Hadamard rotation,
+ *    pre-RoPE keys rotated on the fly, hot 4-bit / cold 2-bit tokens);
+ *  - nalar.dev "Kuantisasi KV Cache dengan Error Budget yang Eksplisit"
+ *    (sections "Ukuran cache...", "Error pada key...", "Error pada value...",
+ *    "Granularitas...", "Evaluasi...": the size law 2*L*T*H_kv*D, the scores
+ *    s_i = q.k_i/sqrt(D), the output sum_i p_i v_i, a recent window kept at
+ *    higher precision);
+ *  - trefon.com "Matematyka cache KV" (sections "Bajty na token", the format
+ *    table of "Przyklad: model 27B przy 262K", "Jak 4-bitowemu cache to
+ *    uchodzi: najpierw obrot": block layouts Q8_0 34 B/32, Q4_0 18 B/32,
+ *    66 B/128, 50 B/128; the randomized Walsh-Hadamard transform; attention
+ *    in the rotated domain);
+ *  - lehuy.net "NexusQuant" (section "Cac mo hinh duoc ho tro": split-half
+ *    RoPE).
+ *
+ * Conventions shared by every entry point:
+ *  - Ownership: the library never allocates device memory.  The caller owns
+ *    every buffer and passes raw device pointers and a cudaStream_t (as
+ *    void*; NULL means the legacy default stream).
+ *  - Asynchrony: every call only enqueues work on the given stream, except
+ *    kvq_read_device_status, which synchronizes that stream.
+ *  - Errors: a kvq_status return.  Bad arguments are rejected on the host
+ *    before anything is launched, with a message in kvq_last_error().  Bad
+ *    runtime data found by a kernel (a length beyond capacity, a page id out
+ *    of range) sets a bit of the device status word in the workspace and
+ *    skips that piece of work; nothing traps and nothing waits.
+ *  - Head mapping: query head h reads kv head h / (H_q / H_kv).
+ *  - Softmax scale: fixed at 1/sqrt(D).
+ *
+ * Cache representation (per sequence of T tokens, per layer and kv head):
+ *  - tokens [q_end, T) stay unquantized in a 16-bit window (raw bits of the
+ *    input dtype), q_end = max(0, floor((T - R)/Gamma)) * Gamma, where R is
+ *    residual_window and Gamma is the token group of a per-channel format (1
+ *    when both formats are per-token);
+ *  - with hot_window W > 0: tokens [c_end, q_end) are in the hot formats
+ *    (k_fmt, v_fmt) and [0, c_end) in the cold formats (k_cold, v_cold),
+ *    c_end = max(0, floor((q_end - W)/Gamma)) * Gamma; a group that leaves
+ *    the hot tier is requantized from its dequantized hot values;
+ *  - with W = 0: tokens [0, q_end) are in k_fmt / v_fmt.
+ *
+ * Block: fp16 scale (little endian) then G*b/8 bytes of codes.  Absmax
+ * scaling in fp32: amax = max|x|, scale = fp16_rn(min(amax/qmax, 65504)),
+ * code = clamp(rint(x / float(scale)), -qmax, qmax), qmax = 2^(b-1) - 1,
+ * all codes 0 when the scale is 0.  Packing: 8-bit two's complement;
+ * 4-bit code+8, element 2i in the low nibble of byte i; 3-bit code+4,
+ * eight values per 24-bit little-endian word, value j at bits [3j, 3j+3);
+ * 2-bit code+2, value j of a byte at bits [2j, 2j+2).
+ *
+ * Buffer layouts (byte arrays; "row" = one storage row):
+ *  - per-token row: the D/G blocks of one token and kv head;
+ *  - per-channel row: D blocks (channel-ascending), each one channel over
+ *    the G tokens of one token group;
+ *  - main tier, contiguous: [L][batch][H_kv][capacity][row], capacity =
+ *    max_T tokens or ceil(max_T/G) groups;
+ *  - main tier, paged (page_tokens > 0, per-token formats, W = 0):
+ *    [L][n_pages][H_kv][page_tokens][row]; block_table is
+ *    [batch][max_pages_per_seq] int32 (device), page of token t =
+ *    block_table[seq][t / page_tokens];
+ *  - hot tier when W > 0: a ring of W/G + 1 group rows (per-channel) or
+ *    W + Gamma token rows (per-token); slot = index mod ring length;
+ *  - cold tier: [L][batch][H_kv][capacity][row];
+ *  - window: [L][batch][H_kv][R + Gamma][D] 16-bit values, slot = t mod
+ *    (R + Gamma).
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_ARG = 1,          /* invalid argument; nothing launched */
+  KVQ_ERR_UNSUPPORTED = 2,  /* valid but not implemented combination */
+  KVQ_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+  KVQ_ERR_CAPACITY = 4,     /* a host-visible size exceeds capacity */
+  KVQ_ERR_WORKSPACE = 5     /* workspace missing or too small */
+} kvq_status;
+
+typedef enum { KVQ_DT_F16 = 0, KVQ_DT_BF16 = 1 } kvq_dtype;
+
+/* A block spans G consecutive channels of one token (TOKEN) or one channel
+ * over G consecutive tokens (CHANNEL). */
+typedef enum { KVQ_AXIS_TOKEN = 0, KVQ_AXIS_CHANNEL = 1 } kvq_axis;
+
+/* bits in {8, 4, 3, 2} (16 is accepted by the size functions only, meaning
+ * plain 16-bit storage); group in {32, 128}, dividing D for TOKEN; group 32
+ * for CHANNEL. */
+typedef struct {
+  int32_t bits;
+  int32_t group;
+  int32_t axis;
+} kvq_fmt;
+
+/* flags */
+enum {
+  KVQ_ROTATE_K = 1u << 0,  /* randomized Hadamard-128 on K before quantizing (TOKEN formats) */
+  KVQ_ROTATE_V = 1u << 1,  /* the same on V */
+  KVQ_K_PRE_ROPE = 1u << 2 /* K is stored pre-RoPE; decode applies split-half RoPE at position t */
+};
+
+/* Device status bits (workspace word 0), OR-ed by kernels. */
+enum {
+  KVQ_DEV_CAPACITY = 1u << 0, /* an append would exceed max_T, or more new tokens than max_new */
+  KVQ_DEV_PAGE = 1u << 1,     /* a block_table entry outside [0, n_pages) */
+  KVQ_DEV_RANGE = 1u << 2,    /* kvq_dequantize range outside [0, T) */
+  KVQ_DEV_LENGTH = 1u << 3    /* a sequence length < 0 or > max_T, or cu_new not ascending */
+};
+
+typedef struct {
+  int32_t L;        /* layers held by the buffers */
+  int32_t H_kv;     /* kv heads */
+  int32_t H_q;      /* query heads, a multiple of H_kv, H_q/H_kv <= 8 */
+  int32_t D;        /* head dim: 128 or 256 */
+  int32_t batch;    /* sequences */
+  int32_t max_T;    /* capacity in tokens per sequence */
+  int32_t in_dtype; /* kvq_dtype of k, v, q inputs and of the window */
+  kvq_fmt k_fmt, v_fmt;   /* the only tier (W = 0) or the hot tier */
+  kvq_fmt k_cold, v_cold; /* cold tier when hot_window > 0 (same axis and group, fewer bits) */
+  int32_t hot_window;      /* W: tokens kept in the hot tier (multiple of Gamma), 0 = one tier */
+  int32_t residual_window; /* R: tokens kept in the 16-bit window, 0 allowed */
+  uint32_t flags;          /* KVQ_ROTATE_K | KVQ_ROTATE_V | KVQ_K_PRE_ROPE */
+  float rope_theta;        /* RoPE base (KVQ_K_PRE_ROPE), e.g. 10000 */
+  uint64_t sign_seed;      /* 0: plain Sylvester transform; else SplitMix64 sign vectors */
+  int32_t page_tokens;     /* 0 = contiguous; 16 = paged main tier */
+  int32_t n_pages;         /* pages in the pool (paged) */
+  int32_t max_pages_per_seq; /* block_table row length (paged) */
+  int32_t reserved;        /* must be 0 */
+} kvq_config;
+
+typedef struct {
+  void* k_main;  /* main / hot tier of K */
+  void* v_main;  /* main / hot tier of V */
+  void* k_cold;  /* cold tier of K (hot_window > 0), else NULL */
+  void* v_cold;  /* cold tier of V (hot_window > 0), else NULL */
+  void* k_resid; /* 16-bit window of K (when R + Gamma > 1), else NULL */
+  void* v_resid; /* 16-bit window of V */
+  const int32_t* block_table; /* [batch][max_pages_per_seq] device (paged), else NULL */
+} kvq_cache;
+
+/* Version string of the library. */
+KVQ_API const char* kvq_version(void);
+
+/* Message of the last error returned on this thread ("" if none). */
+KVQ_API const char* kvq_last_error(void);
+
+/* Checks a configuration (the same checks every entry point makes). */
+KVQ_API kvq_status kvq_validate_config(const kvq_config* cfg);
+
+/* Bytes of one block: 2 + group*bits/8 (2*group for bits = 16)
+ * (trefon.com, format table). */
+KVQ_API kvq_status kvq_block_bytes(int32_t bits, int32_t group, int32_t* bytes);
+
+/* Steady-state bytes per token over all L layers, K and V, in the format
+ * that holds most of a long sequence (cold when hot_window > 0).  Scales
+ * count (nalar.dev, section "Ukuran cache...": compare actual bytes per
+ * token; trefon.com, section "Bajty na token"). */
+KVQ_API kvq_status kvq_bytes_per_token(const kvq_config* cfg, int64_t* bytes);
+
+/* Exact bytes the representation keeps for one sequence of T tokens over
+ * all layers: cold + hot/main tiers + 16-bit window, K and V. */
+KVQ_API kvq_status kvq_cache_bytes(const kvq_config* cfg, int64_t T, int64_t* bytes);
+
+/* Bytes to allocate for the six kvq_cache buffers, in the order k_main,
+ * v_main, k_cold, v_cold, k_resid, v_resid (0 = buffer not used). */
+KVQ_API kvq_status kvq_buffer_sizes(const kvq_config* cfg, size_t sizes[6]);
+
+/* Bytes of the workspace every launching call takes (status word, split
+ * tickets, RoPE tables, split partials); 256-byte aligned. */
+KVQ_API kvq_status kvq_workspace_bytes(const kvq_config* cfg, size_t* bytes);
+
+/* Prepares a workspace of at least kvq_workspace_bytes: zeroes the status
+ * word and tickets and fills the RoPE tables.  Call once after allocating
+ * it; later calls keep the tickets at zero themselves. */
+KVQ_API kvq_status kvq_workspace_init(const kvq_config* cfg, void* workspace, size_t ws_bytes, void* stream);
+
+/* Quantize-on-append for layers [layer0, layer0 + n_layers).
+ *  k, v:     [n_layers][total_new][H_kv][D] in_dtype, device; sequences back
+ *            to back in batch order (post-RoPE keys, or pre-RoPE with
+ *            KVQ_K_PRE_ROPE).
+ *  cu_new:   [batch + 1] int32 device, cu_new[0] = 0, cu_new[batch] =
+ *            total_new; sequence b appends cu_new[b+1] - cu_new[b] tokens.
+ *  seq_lens: [batch] int32 device, lengths BEFORE this append (the caller
+ *            advances them after all layers, e.g. with kvq_commit_lengths).
+ *  total_new, max_new: host copies of cu_new[batch] and of the largest
+ *            per-sequence count (they size the grids).
+ * Window tokens move into the quantized tiers by whole groups; bulk append
+ * and token-by-token append give the same cache. */
+KVQ_API kvq_status kvq_append(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0, int32_t n_layers,
+                      const void* k, const void* v, const int32_t* cu_new, const int32_t* seq_lens,
+                      int32_t total_new, int32_t max_new, void* workspace, size_t ws_bytes, void* stream);
+
+/* seq_lens[b] += cu_new[b+1] - cu_new[b] on the device. */
+KVQ_API kvq_status kvq_commit_lengths(const kvq_config* cfg, const int32_t* cu_new, int32_t* seq_lens, void* stream);
+
+/* Decode attention of one query token per sequence, for layers
+ * [layer0, layer0 + n_layers) (independent per-layer queries; n_layers > 1
+ * only saves launches).
+ *  q:        [n_layers][batch][H_q][D] in_dtype, device, post-RoPE.
+ *  seq_lens: [batch] int32 device, tokens currently cached.
+ *  out:      [n_layers][batch][H_q][D] fp32, device:
+ *            out = sum_t softmax_t(q.k_t/sqrt(D)) v_t over the dequantized
+ *            cache (keys RoPE-rotated at position t when stored pre-RoPE);
+ *            0 for an empty sequence.
+ *  num_splits: token splits per (layer, seq, kv head); 0 picks one. */
+KVQ_API kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0,
+                                int32_t n_layers, const void* q, const int32_t* seq_lens, float* out,
+                                int32_t num_splits, void* workspace, size_t ws_bytes, void* stream);
+
+/* The split count kvq_decode_attention picks for num_splits = 0. */
+KVQ_API kvq_status kvq_decode_splits(const kvq_config* cfg, int32_t n_layers, int32_t* splits);
+
+/* Dequantizes tokens [t0, t1) of (layer, seq) to fp32 k_out, v_out
+ * [t1 - t0][H_kv][D] (device) in the original domain: rotation undone, keys
+ * as stored (pre-RoPE when flagged).  seq_lens as for decode; a range beyond
+ * the current length sets KVQ_DEV_RANGE and writes nothing. */
+KVQ_API kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_cache* cache, int32_t layer, int32_t seq,
+                          int32_t t0, int32_t t1, const int32_t* seq_lens, float* k_out, float* v_out,
+                          void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronizes `stream` and reads the device status word (KVQ_DEV_* bits). */
+KVQ_API kvq_status kvq_read_device_status(const void* workspace, uint32_t* bits, void* stream);
+
+/* Clears the device status word. */
+KVQ_API kvq_status kvq_clear_device_status(void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,58 @@
+"""Shared driver of the GPU parity tests: the same appends on the GPU (through
+the C ABI) and in the CPU oracle."""
+
+from __future__ import annotations
+
+import numpy as np
+
+from oracle import kvq_oracle as O
+from tests.helpers import oracle_cfg, raw16
+
+
+def appended_cache(w, chunks=None, seed=0, with_oracle=True, device="cuda"):
+    """Appends every layer of workload `w` in steps of `chunks` tokens per
+    sequence (one multi-layer kvq_append per step).  Returns (cache,
+    seq_lens (device), oracle buffers or None, block table or None)."""
+    import torch
+
+    from bit_kv_cache_04_gb300 import kvq as K
+    from bit_kv_cache_04_gb300 import workloads as W
+
+    cfg = w.cfg
+    oc = oracle_cfg(cfg)
+    table = W.page_table(w, seed)
+    cache = K.KVCache(cfg, device, block_table=table)
+    ref = O.new_buffers(oc) if with_oracle else None
+    table_np = None if table is None else table.numpy()
+    B, L = cfg.batch, cfg.L
+    full = [[W.kv_tokens(w, l, b, 0, w.lengths[b], device, seed) for b in range(B)] for l in range(L)]
+    seq_lens = torch.zeros(B, dtype=torch.int32, device=device)
+    done = [0] * B
+    sizes = list(chunks) if chunks else [max(w.lengths)]
+    i = 0
+    while any(d < t for d, t in zip(done, w.lengths)):
+        step = sizes[min(i, len(sizes) - 1)] if i < len(sizes) else sizes[-1]
+        i += 1
+        n = [min(step, t - d) for d, t in zip(done, w.lengths)]
+        cu = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+        ks = torch.stack([torch.cat([full[l][b][0][done[b]:done[b] + n[b]] for b in range(B)]) for l in range(L)])
+        vs = torch.stack([torch.cat([full[l][b][1][done[b]:done[b] + n[b]] for b in range(B)]) for l in range(L)])
+        cu_d = torch.as_tensor(cu, device=device)
+        cache.append(0, L, ks.contiguous(), vs.contiguous(), cu_d, seq_lens, int(cu[-1]), max(n))
+        cache.commit_lengths(cu_d, seq_lens)
+        if with_oracle:
+            for l in range(L):
+                O.append(oc, ref, l, raw16(ks[l]), raw16(vs[l]), n, done, block_table=table_np)
+        done = [d + x for d, x in zip(done, n)]
+    torch.cuda.synchronize()
+    return cache, seq_lens, ref, table_np
+
+
+def gpu_buffers_as_oracle(cache, oc):
+    """GPU buffers copied to the host and shaped like the oracle's."""
+    shapes = O.buffer_shapes(oc)
+    out = {}
+    for name, arr in cache.buffer_numpy().items():
+        shape, dt = shapes[name]
+        out[name] = arr.view(dt).reshape(shape)
+    return out
