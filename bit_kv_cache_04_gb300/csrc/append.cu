@@ -62,7 +62,7 @@ __device__ void store_unit(const AppendArgs& a, int which, int layer, int seq, i
     for (int c = threadIdx.x; c < lo.D; c += blockDim.x) {
       auto get = [&](int j) { return x[j * ld + c]; };
       if (to_cold) {
-        uint8_t tmp[2 + 32];
+        alignas(4) uint8_t tmp[2 + 32];
         quant_block_serial(get, f.group, f.bits, tmp, deq);
         uint8_t* dst = cold_row(lo, a.cp, which, layer, seq, h, u0) + (int64_t)c * fc.bb;
         quant_block_serial([&](int j) { return deq[j]; }, fc.group, fc.bits, dst, nullptr);
@@ -81,7 +81,7 @@ __device__ void store_unit(const AppendArgs& a, int which, int layer, int seq, i
     const float* xr = x + j * ld + b * f.group;
     auto get = [&](int i) { return xr[i]; };
     if (to_cold) {
-      uint8_t tmp[2 + 128];
+      alignas(4) uint8_t tmp[2 + 128];
       quant_block_serial(get, f.group, f.bits, tmp, deq);
       uint8_t* dst = cold_row(lo, a.cp, which, layer, seq, h, t) + (int64_t)b * fc.bb;
       quant_block_serial([&](int i) { return deq[i]; }, fc.group, fc.bits, dst, nullptr);

@@ -74,9 +74,10 @@ __device__ void quant_block_serial(Get get, int G, int bits, uint8_t* dst, float
   float s32 = __fdiv_rn(amax, (float)qmax);
   __half s16 = __float2half_rn(fminf(s32, 65504.0f));
   const float sf = __half2float(s16);
-  const uint16_t sb = __half_as_ushort(s16);
-  dst[0] = (uint8_t)(sb & 0xFF);
-  dst[1] = (uint8_t)(sb >> 8);
+  // One 16-bit store (blocks start at even offsets).  Splitting the half's
+  // bits into two byte stores was observed to store a value conversion of
+  // the scale instead of its low byte with nvcc 13.0 for sm_103a.
+  *reinterpret_cast<__half*>(dst) = s16;
   uint8_t* p = dst + 2;
   if (bits == 8) {
     for (int i = 0; i < G; ++i) {

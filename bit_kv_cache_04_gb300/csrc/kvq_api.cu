@@ -147,8 +147,11 @@ Layout make_layout(const kvq_config* c) {
     lo.kc = make_fmt(c->k_cold, c->D);
     lo.vc = make_fmt(c->v_cold, c->D);
   }
+  // per-token capacity is rounded up to whole 32-token tiles so that every
+  // tile starts 16-byte aligned and lies inside the buffer
   auto rows_abs = [&](const FmtInfo& f) -> int64_t {
-    return f.axis == KVQ_AXIS_TOKEN ? (int64_t)c->max_T : (int64_t)((c->max_T + f.group - 1) / f.group);
+    return f.axis == KVQ_AXIS_TOKEN ? (int64_t)((c->max_T + kTile - 1) / kTile * kTile)
+                                    : (int64_t)((c->max_T + f.group - 1) / f.group);
   };
   auto rows_ring = [&](const FmtInfo& f) -> int {
     return f.axis == KVQ_AXIS_TOKEN ? c->hot_window + lo.gam : c->hot_window / f.group + 1;

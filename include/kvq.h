@@ -58,14 +58,15 @@
  *  - per-channel row: D blocks (channel-ascending), each one channel over
  *    the G tokens of one token group;
  *  - main tier, contiguous: [L][batch][H_kv][capacity][row], capacity =
- *    max_T tokens or ceil(max_T/G) groups;
+ *    max_T rounded up to a multiple of 32 tokens (per-token rows) or
+ *    ceil(max_T/G) groups (per-channel rows);
  *  - main tier, paged (page_tokens > 0, per-token formats, W = 0):
  *    [L][n_pages][H_kv][page_tokens][row]; block_table is
  *    [batch][max_pages_per_seq] int32 (device), page of token t =
  *    block_table[seq][t / page_tokens];
  *  - hot tier when W > 0: a ring of W/G + 1 group rows (per-channel) or
  *    W + Gamma token rows (per-token); slot = index mod ring length;
- *  - cold tier: [L][batch][H_kv][capacity][row];
+ *  - cold tier: [L][batch][H_kv][capacity][row] (capacity as above);
  *  - window: [L][batch][H_kv][R + Gamma][D] 16-bit values, slot = t mod
  *    (R + Gamma).
  */

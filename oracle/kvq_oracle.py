@@ -45,7 +45,8 @@ written here independently from its description):
 * per-token block row: D/G blocks of one token and kv head, back to back;
 * per-channel group row: D blocks (one per channel, channel-ascending) that
   each cover the G tokens of one token group;
-* main tier, contiguous: [L][batch][H_kv][capacity][row];
+* main tier, contiguous: [L][batch][H_kv][capacity][row], capacity = max_T
+  rounded up to a multiple of 32 tokens (per-token) or ceil(max_T/G) groups;
 * main tier, paged (per-token formats only): [L][pages][H_kv][page_tokens][row],
   page = block_table[seq][t // page_tokens];
 * two tiers: the hot tier is a ring (per-channel: W/G + 1 group slots; per-token:
@@ -452,7 +453,7 @@ def row_bytes(fmt: Fmt, D: int) -> int:
 
 def _tier_rows(cfg: Config, fmt: Fmt, ring: bool) -> int:
     if fmt.axis == AXIS_TOKEN:
-        return (cfg.hot_window + unit_tokens(cfg)) if ring else cfg.max_T
+        return (cfg.hot_window + unit_tokens(cfg)) if ring else -(-cfg.max_T // 32) * 32
     if ring:
         return cfg.hot_window // fmt.group + 1
     return -(-cfg.max_T // fmt.group)
