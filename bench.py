@@ -124,6 +124,8 @@ def run_ours(args):
     steps, warm = args.steps, args.warmup
     extra = 2 * (steps + warm) + 16
     w = W.make(args.workload, extra_tokens=extra)
+    if args.layers:
+        w = w.scaled(L=args.layers, lengths=w.lengths, extra=extra)
     cfg = w.cfg
     L, B, H, Hq, D = cfg.L, cfg.batch, cfg.H_kv, cfg.H_q, cfg.D
     stream = torch.cuda.current_stream(dev)
@@ -378,6 +380,8 @@ def main():
     ap.add_argument("--workload", default="llama2_7b_kivi4")
     ap.add_argument("--cpu-heads", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="use only this many layers (small cases for profiler captures); 0 = the workload's")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

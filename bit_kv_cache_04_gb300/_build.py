@@ -21,6 +21,7 @@ SOURCES = [
     ("kvq_api.cu", []),
     ("append.cu", ["--fmad=false"]),
     ("decode_generic.cu", []),
+    ("decode_mma.cu", []),
     ("dequant.cu", []),
 ]
 

@@ -48,60 +48,140 @@ __device__ __forceinline__ const uint16_t* input_row(const AppendArgs& a, int wh
   return base + row * a.lo.D;
 }
 
-// Writes one quantized per-token row (or per-channel group row) of values
-// x (fp32, smem, row stride ld) to the main tier, or to the cold tier after
-// a requantization when to_cold.
-__device__ void store_unit(const AppendArgs& a, int which, int layer, int seq, int h, int u0, int n_tok,
-                           const float* x, int ld, bool to_cold, uint32_t* page_bad) {
-  const Layout& lo = a.lo;
-  const FmtInfo& f = fmt_main(lo, which);
-  const FmtInfo& fc = fmt_cold(lo, which);
-  float deq[128];
-  if (f.axis == KVQ_AXIS_CHANNEL) {
-    // block c = channel c over the group's 32 tokens (token order)
-    for (int c = threadIdx.x; c < lo.D; c += blockDim.x) {
-      auto get = [&](int j) { return x[j * ld + c]; };
-      if (to_cold) {
-        alignas(4) uint8_t tmp[2 + 32];
-        quant_block_serial(get, f.group, f.bits, tmp, deq);
-        uint8_t* dst = cold_row(lo, a.cp, which, layer, seq, h, u0) + (int64_t)c * fc.bb;
-        quant_block_serial([&](int j) { return deq[j]; }, fc.group, fc.bits, dst, nullptr);
-      } else {
-        bool bad = false;
-        uint8_t* row = main_row(lo, a.cp, which, layer, seq, h, u0, &bad);
-        quant_block_serial(get, f.group, f.bits, row + (int64_t)c * f.bb, nullptr);
+// ---- per-token rows: one warp per (token, kv head) ----------------------------
+//
+// Lane l holds channels 128c + 4l .. 128c + 4l + 3 of every 128-chunk c (the
+// layout of warp_rotate128), NC = D / 128 chunks.
+
+template <int NC>
+__device__ __forceinline__ void load_row(const uint16_t* src, int dtype, float (&v)[NC][4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const uint2 w = *reinterpret_cast<const uint2*>(src + 128 * c + 4 * lane);
+    v[c][0] = in_to_f32((uint16_t)(w.x & 0xFFFF), dtype);
+    v[c][1] = in_to_f32((uint16_t)(w.x >> 16), dtype);
+    v[c][2] = in_to_f32((uint16_t)(w.y & 0xFFFF), dtype);
+    v[c][3] = in_to_f32((uint16_t)(w.y >> 16), dtype);
+  }
+}
+
+// Quantizes the warp's row into `row` (skipped when row is null) with blocks
+// of G channels and `bits` bits; dq (optional) receives code * scale.
+template <int NC>
+__device__ __forceinline__ void warp_quant_row(const float (&v)[NC][4], int G, int bits, uint8_t* row,
+                                               float (*dq)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int qmax = qmax_of(bits);
+  const int bb = block_bytes_of(bits, G);
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    float m = fmaxf(fmaxf(fabsf(v[c][0]), fabsf(v[c][1])), fmaxf(fabsf(v[c][2]), fabsf(v[c][3])));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    if (G == 128) {
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+    }
+    const __half s16 = block_scale_of(m, qmax);
+    const float sf = __half2float(s16);
+    const float rcp = __frcp_rn(sf);
+    int code[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      code[e] = quant_code_fast(v[c][e], sf, rcp, qmax);
+      if (dq) dq[c][e] = (float)code[e] * sf;
+    }
+    const int ch0 = 128 * c + 4 * lane;
+    const int pos = ch0 % G;
+    uint8_t* blk = row ? row + (ch0 / G) * bb : nullptr;
+    if (bits == 3) {  // 12 bits per lane; even lanes write the 24-bit word of a lane pair
+      uint32_t w12 = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) w12 |= (uint32_t)(code[e] + 4) << (3 * e);
+      const uint32_t other = __shfl_xor_sync(0xffffffffu, w12, 1);
+      if (blk && !(lane & 1)) {
+        const uint32_t w = w12 | (other << 12);
+        uint8_t* p = blk + 2 + (pos / 8) * 3;
+        p[0] = (uint8_t)(w & 0xFFu);
+        p[1] = (uint8_t)((w >> 8) & 0xFFu);
+        p[2] = (uint8_t)((w >> 16) & 0xFFu);
       }
     }
-    return;
-  }
-  const int nb = lo.D / f.group;
-  for (int item = threadIdx.x; item < n_tok * nb; item += blockDim.x) {
-    const int j = item / nb, b = item % nb;
-    const int t = u0 + j;
-    const float* xr = x + j * ld + b * f.group;
-    auto get = [&](int i) { return xr[i]; };
-    if (to_cold) {
-      alignas(4) uint8_t tmp[2 + 128];
-      quant_block_serial(get, f.group, f.bits, tmp, deq);
-      uint8_t* dst = cold_row(lo, a.cp, which, layer, seq, h, t) + (int64_t)b * fc.bb;
-      quant_block_serial([&](int i) { return deq[i]; }, fc.group, fc.bits, dst, nullptr);
-    } else {
-      bool bad = false;
-      uint8_t* row = main_row(lo, a.cp, which, layer, seq, h, t, &bad);
-      if (bad) {
-        *page_bad = 1;
-        continue;
-      }
-      quant_block_serial(get, f.group, f.bits, row + (int64_t)b * f.bb, nullptr);
+    if (!blk) continue;
+    if (pos == 0) *reinterpret_cast<__half*>(blk) = s16;
+    uint8_t* p = blk + 2;
+    if (bits == 8) {
+      *reinterpret_cast<uint16_t*>(p + pos) = (uint16_t)((code[0] & 0xFF) | ((code[1] & 0xFF) << 8));
+      *reinterpret_cast<uint16_t*>(p + pos + 2) = (uint16_t)((code[2] & 0xFF) | ((code[3] & 0xFF) << 8));
+    } else if (bits == 4) {
+      *reinterpret_cast<uint16_t*>(p + pos / 2) =
+          (uint16_t)((code[0] + 8) | ((code[1] + 8) << 4) | ((code[2] + 8) << 8) | ((code[3] + 8) << 12));
+    } else if (bits == 2) {
+      p[pos / 4] = (uint8_t)((code[0] + 2) | ((code[1] + 2) << 2) | ((code[2] + 2) << 4) | ((code[3] + 2) << 6));
     }
   }
 }
 
+// ---- per-channel groups: one thread per channel, 32 tokens -----------------
+
+// Quantizes x[0], x[ld], ..., x[31 ld] (one channel over the group's tokens)
+// into the block at blk; dq (optional, stride 1) receives code * scale.
+__device__ __forceinline__ void thread_quant_channel(const float* x, int ld, int bits, uint8_t* blk, float* dq) {
+  const int qmax = qmax_of(bits);
+  float m = 0.f;
+#pragma unroll 8
+  for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(x[j * ld]));
+  const __half s16 = block_scale_of(m, qmax);
+  const float sf = __half2float(s16);
+  const float rcp = __frcp_rn(sf);
+  if (blk) *reinterpret_cast<__half*>(blk) = s16;
+  uint16_t* p = blk ? reinterpret_cast<uint16_t*>(blk + 2) : nullptr;
+  const int per16 = 16 / bits;  // codes per 16-bit store (8-bit: 2, 4-bit: 4, 2-bit: 8)
+  if (bits == 3) {
+    // eight codes per 24-bit word: 4 words = 12 bytes, written as 6 halves
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      w[k] = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int cd = quant_code_fast(x[(8 * k + e) * ld], sf, rcp, qmax);
+        if (dq) dq[8 * k + e] = (float)cd * sf;
+        w[k] |= (uint32_t)(cd + 4) << (3 * e);
+      }
+    }
+    if (p) {
+      const uint32_t b01 = w[0] | (w[1] << 24), b23 = (w[1] >> 8) | (w[2] << 16), b45 = (w[2] >> 16) | (w[3] << 8);
+      p[0] = (uint16_t)b01;
+      p[1] = (uint16_t)(b01 >> 16);
+      p[2] = (uint16_t)b23;
+      p[3] = (uint16_t)(b23 >> 16);
+      p[4] = (uint16_t)b45;
+      p[5] = (uint16_t)(b45 >> 16);
+    }
+    return;
+  }
+  for (int k = 0; k < 32 / per16; ++k) {
+    uint32_t hw = 0;
+    for (int e = 0; e < per16; ++e) {
+      const int cd = quant_code_fast(x[(per16 * k + e) * ld], sf, rcp, qmax);
+      if (dq) dq[per16 * k + e] = (float)cd * sf;
+      const uint32_t u = bits == 8 ? (uint32_t)(cd & 0xFF) : (uint32_t)(cd + qmax + 1);
+      hw |= u << (bits * e);
+    }
+    if (p) p[k] = (uint16_t)hw;
+  }
+}
+
 // Phase B: quantize units [q_end(T0), q_end(T1)).
+template <int NC>
 __global__ void __launch_bounds__(kAppendThreads) append_quantize_kernel(AppendArgs a) {
-  extern __shared__ float xs[];  // [kTile][D + 1]
+  extern __shared__ float xs[];  // [kTile][D + 1], per-channel groups only
   __shared__ uint32_t page_bad;
   const Layout& lo = a.lo;
+  constexpr int D = 128 * NC;
   const int li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B, h = blockIdx.y;
   const int layer = a.layer0 + li;
   SeqSpan s = read_span(a, seq);
@@ -111,42 +191,79 @@ __global__ void __launch_bounds__(kAppendThreads) append_quantize_kernel(AppendA
   const int u0 = max(base, q0), u1 = min(base + kTile, q1);
   if (u0 >= u1) return;
   const int n_tok = u1 - u0;
-  const int ld = lo.D + 1;
+  const int ld = D + 1;
+  const bool to_cold = lo.tiered && u0 < c1;
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   if (threadIdx.x == 0) page_bad = 0;
+  __syncthreads();
   for (int which = 0; which < 2; ++which) {
-    __syncthreads();
-    // gather the unit's tokens (window ring for old tokens, input for new)
-    for (int e = threadIdx.x; e < n_tok * lo.D; e += blockDim.x) {
-      const int j = e / lo.D, d = e % lo.D, t = u0 + j;
-      const uint16_t* src = t < s.T0 ? resid_row(lo, a.cp, which, layer, seq, h, t) : input_row(a, which, li, s, h, t);
-      xs[j * ld + d] = in_to_f32(src[d], lo.dtype);
-    }
-    __syncthreads();
-    const bool rotate = (lo.flags & (which ? KVQ_ROTATE_V : KVQ_ROTATE_K)) != 0;
-    if (rotate) {
-      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-      for (int r = warp; r < n_tok * (lo.D / 128); r += nw) {
-        float* p = xs + (r / (lo.D / 128)) * ld + (r % (lo.D / 128)) * 128 + 4 * lane;
-        float v[4] = {p[0], p[1], p[2], p[3]};
-        warp_rotate128(v, lo.d1, lo.d2);
-        p[0] = v[0];
-        p[1] = v[1];
-        p[2] = v[2];
-        p[3] = v[3];
+    const FmtInfo& f = fmt_main(lo, which);
+    const FmtInfo& fc = fmt_cold(lo, which);
+    auto src_row = [&](int t) -> const uint16_t* {
+      return t < s.T0 ? resid_row(lo, a.cp, which, layer, seq, h, t) : input_row(a, which, li, s, h, t);
+    };
+    if (f.axis == KVQ_AXIS_CHANNEL) {
+      // the unit is one whole group of 32 tokens: gather it, then one thread per channel
+      __syncthreads();
+      for (int e = threadIdx.x; e < kTile * (D / 4); e += blockDim.x) {
+        const int j = e / (D / 4), d4 = (e % (D / 4)) * 4;
+        const uint2 w = *reinterpret_cast<const uint2*>(src_row(u0 + j) + d4);
+        float* xr = xs + j * ld + d4;
+        xr[0] = in_to_f32((uint16_t)(w.x & 0xFFFF), lo.dtype);
+        xr[1] = in_to_f32((uint16_t)(w.x >> 16), lo.dtype);
+        xr[2] = in_to_f32((uint16_t)(w.y & 0xFFFF), lo.dtype);
+        xr[3] = in_to_f32((uint16_t)(w.y >> 16), lo.dtype);
       }
       __syncthreads();
+      for (int c = threadIdx.x; c < D; c += blockDim.x) {
+        if (to_cold) {
+          float dq[32];
+          thread_quant_channel(xs + c, ld, f.bits, nullptr, dq);
+          uint8_t* dst = cold_row(lo, a.cp, which, layer, seq, h, u0) + (int64_t)c * fc.bb;
+          thread_quant_channel(dq, 1, fc.bits, dst, nullptr);
+        } else {
+          bool bad = false;
+          uint8_t* row = main_row(lo, a.cp, which, layer, seq, h, u0, &bad);
+          thread_quant_channel(xs + c, ld, f.bits, row + (int64_t)c * f.bb, nullptr);
+        }
+      }
+      continue;
     }
-    const bool to_cold = lo.tiered && u0 < c1;
-    store_unit(a, which, layer, seq, h, u0, n_tok, xs, ld, to_cold, &page_bad);
+    const bool rotate = (lo.flags & (which ? KVQ_ROTATE_V : KVQ_ROTATE_K)) != 0;
+    for (int j = warp; j < n_tok; j += nw) {
+      const int t = u0 + j;
+      float v[NC][4];
+      load_row<NC>(src_row(t), lo.dtype, v);
+      if (rotate) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) warp_rotate128(v[c], lo.d1, lo.d2);
+      }
+      if (to_cold) {
+        float dq[NC][4];
+        warp_quant_row<NC>(v, f.group, f.bits, nullptr, dq);
+        warp_quant_row<NC>(dq, fc.group, fc.bits, cold_row(lo, a.cp, which, layer, seq, h, t), nullptr);
+      } else {
+        bool bad = false;
+        uint8_t* row = main_row(lo, a.cp, which, layer, seq, h, t, &bad);
+        if (bad) {
+          page_bad = 1;
+          continue;
+        }
+        warp_quant_row<NC>(v, f.group, f.bits, row, nullptr);
+      }
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0 && page_bad) atomicOr(a.status, KVQ_DEV_PAGE);
 }
 
-// Phase A: hot units [c_end(T0), min(c_end(T1), q_end(T0))) -> cold.
+// Phase A: hot units [c_end(T0), min(c_end(T1), q_end(T0))) -> cold, from the
+// exact dequantized hot values.
+template <int NC>
 __global__ void __launch_bounds__(kAppendThreads) append_requant_kernel(AppendArgs a) {
   extern __shared__ float xs[];
   const Layout& lo = a.lo;
+  constexpr int D = 128 * NC;
   const int li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B, h = blockIdx.y;
   const int layer = a.layer0 + li;
   SeqSpan s = read_span(a, seq);
@@ -155,41 +272,36 @@ __global__ void __launch_bounds__(kAppendThreads) append_requant_kernel(AppendAr
   const int stop = min(c1, q0);
   const int u0 = c0 + blockIdx.x * kTile;  // c0 and units are whole groups (Gamma = 32)
   if (u0 >= stop) return;
-  const int ld = lo.D + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   for (int which = 0; which < 2; ++which) {
-    __syncthreads();
     const FmtInfo& f = fmt_main(lo, which);
+    const FmtInfo& fc = fmt_cold(lo, which);
     bool bad = false;
     if (f.axis == KVQ_AXIS_CHANNEL) {
       const uint8_t* row = main_row(lo, a.cp, which, layer, seq, h, u0, &bad);
-      for (int c = threadIdx.x; c < lo.D; c += blockDim.x)
-        dequant_block_serial(row + (int64_t)c * f.bb, f.group, f.bits, xs + c, ld);
-    } else {
-      const int nb = lo.D / f.group;
-      for (int item = threadIdx.x; item < kTile * nb; item += blockDim.x) {
-        const int j = item / nb, b = item % nb;
-        const uint8_t* row = main_row(lo, a.cp, which, layer, seq, h, u0 + j, &bad);
-        dequant_block_serial(row + (int64_t)b * f.bb, f.group, f.bits, xs + j * ld + b * f.group, 1);
+      uint8_t* dst = cold_row(lo, a.cp, which, layer, seq, h, u0);
+      for (int c = threadIdx.x; c < D; c += blockDim.x) {
+        float x[32];
+        dequant_block_serial(row + (int64_t)c * f.bb, f.group, f.bits, x, 1);
+        thread_quant_channel(x, 1, fc.bits, dst + (int64_t)c * fc.bb, nullptr);
       }
+      continue;
     }
-    __syncthreads();
-    // requantize the exact dequantized values to the cold format
-    const FmtInfo& fc = fmt_cold(lo, which);
-    if (fc.axis == KVQ_AXIS_CHANNEL) {
-      for (int c = threadIdx.x; c < lo.D; c += blockDim.x) {
-        uint8_t* dst = cold_row(lo, a.cp, which, layer, seq, h, u0) + (int64_t)c * fc.bb;
-        quant_block_serial([&](int j) { return xs[j * ld + c]; }, fc.group, fc.bits, dst, nullptr);
+    for (int j = warp; j < kTile; j += nw) {
+      const uint8_t* row = main_row(lo, a.cp, which, layer, seq, h, u0 + j, &bad);
+      float v[NC][4];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const int ch0 = 128 * c + 4 * lane;
+        const uint8_t* blk = row + (ch0 / f.group) * f.bb;
+        const float sf = block_scale(blk);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[c][e] = (float)unpack_code(blk + 2, f.bits, ch0 % f.group + e) * sf;
       }
-    } else {
-      const int nb = lo.D / fc.group;
-      for (int item = threadIdx.x; item < kTile * nb; item += blockDim.x) {
-        const int j = item / nb, b = item % nb;
-        uint8_t* dst = cold_row(lo, a.cp, which, layer, seq, h, u0 + j) + (int64_t)b * fc.bb;
-        const float* xr = xs + j * ld + b * fc.group;
-        quant_block_serial([&](int i) { return xr[i]; }, fc.group, fc.bits, dst, nullptr);
-      }
+      warp_quant_row<NC>(v, fc.group, fc.bits, cold_row(lo, a.cp, which, layer, seq, h, u0 + j), nullptr);
     }
   }
+  (void)xs;
 }
 
 // Phase C: new tokens that stay in the 16-bit window.
@@ -221,22 +333,27 @@ __global__ void commit_lengths_kernel(const int32_t* cu_new, int32_t* seq_lens, 
 
 }  // namespace
 
-cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
+template <int NC>
+cudaError_t launch_append_nc(const AppendArgs& a, cudaStream_t st) {
   const Layout& lo = a.lo;
-  if (a.max_new == 0) return cudaSuccess;
   const int chunks = (a.max_new + kTile - 1) / kTile + 2;
   dim3 grid(chunks, lo.H, a.n_layers * lo.B);
   const size_t smem = sizeof(float) * kTile * (lo.D + 1);
   static bool attr_done = false;
   if (!attr_done) {
-    cudaFuncSetAttribute(append_quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-    cudaFuncSetAttribute(append_requant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    cudaFuncSetAttribute(append_quantize_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    cudaFuncSetAttribute(append_requant_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
     attr_done = true;
   }
-  if (lo.tiered) append_requant_kernel<<<grid, kAppendThreads, smem, st>>>(a);
-  append_quantize_kernel<<<grid, kAppendThreads, smem, st>>>(a);
+  if (lo.tiered) append_requant_kernel<NC><<<grid, kAppendThreads, 0, st>>>(a);
+  append_quantize_kernel<NC><<<grid, kAppendThreads, smem, st>>>(a);
   if (lo.ring) append_window_kernel<<<grid, kAppendThreads, 0, st>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
+  if (a.max_new == 0) return cudaSuccess;
+  return a.lo.D == 128 ? launch_append_nc<1>(a, st) : launch_append_nc<2>(a, st);
 }
 
 cudaError_t launch_commit_lengths(const int32_t* cu_new, int32_t* seq_lens, int batch, cudaStream_t st) {

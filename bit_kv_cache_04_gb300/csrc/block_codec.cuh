@@ -64,6 +64,26 @@ __device__ __forceinline__ int quant_code(float x, float sf, int qmax) {
   return (int)r;
 }
 
+// The same code as quant_code(x, sf, qmax) given rcp = fp32(1/sf), with one
+// multiply instead of the division: |x*rcp - fp32(x/sf)| <= 1.5 * 2^-23 *
+// |x/sf| <= 2.3e-5 for |x/sf| <= 128, so unless the product lies within 2^-14
+// of a half-integer both round to the same integer; near a half-integer the
+// exact IEEE quotient decides.
+__device__ __forceinline__ int quant_code_fast(float x, float sf, float rcp, int qmax) {
+  if (sf == 0.0f) return 0;
+  float q = x * rcp;
+  const float fr = q - floorf(q);
+  if (fabsf(fr - 0.5f) < 6.103515625e-05f) q = __fdiv_rn(x, sf);
+  float r = rintf(q);
+  r = fminf(fmaxf(r, (float)-qmax), (float)qmax);
+  return (int)r;
+}
+
+// fp16 scale of a block with absolute maximum amax: fp16_rn(min(amax/qmax, 65504)).
+__device__ __forceinline__ __half block_scale_of(float amax, int qmax) {
+  return __float2half_rn(fminf(__fdiv_rn(amax, (float)qmax), 65504.0f));
+}
+
 // Quantizes G values get(0..G-1) into one block at dst (scale then codes).
 // If deq is given, it receives code * scale (exact in fp32).
 template <class Get>

@@ -304,7 +304,7 @@ cudaError_t launch_generic(const DecodeArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
+cudaError_t launch_decode_generic(const DecodeArgs& a, cudaStream_t st) {
   if (a.lo.D == 128) return launch_generic<128>(a, st);
   return launch_generic<256>(a, st);
 }

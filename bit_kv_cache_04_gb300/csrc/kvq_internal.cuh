@@ -190,7 +190,8 @@ struct DequantArgs {
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_commit_lengths(const int32_t* cu_new, int32_t* seq_lens, int batch, cudaStream_t s);
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);  // tensor-core path when it fits, else generic
+cudaError_t launch_decode_generic(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_dequantize(const DequantArgs& a, cudaStream_t s);
 cudaError_t launch_rope_tables(float2* rope, int base_rows, int D, float theta, cudaStream_t s);
 
