@@ -3,6 +3,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <mutex>
 #include <string>
 
 #include "kvq_internal.cuh"
@@ -477,3 +478,92 @@ kvq_status kvq_clear_device_status(void* workspace, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// kvq_decode_attention_static: decode attention with library-owned scratch,
+// for callers that cannot allocate device memory.  The scratch is a fixed
+// file-scope device array; its device address is looked up once per device.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_scratch[KVQ_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device (looked up with
+// that device current, once).
+kvq_status static_scratch(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(KVQ_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" kvq_status kvq_decode_attention_static(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0,
+                                                  int32_t n_layers, const void* q, const int32_t* seq_lens,
+                                                  float* out, int32_t num_splits, void* stream) {
+  kvq_status st = check_config(cfg, false);
+  if (st != KVQ_OK) return st;
+  if (layer0 < 0 || n_layers < 1 || layer0 + n_layers > cfg->L)
+    return fail(KVQ_ERR_ARG, "layers [%d, %d) outside [0, %d)", layer0, layer0 + n_layers, cfg->L);
+  if (!q || !seq_lens || !out) return fail(KVQ_ERR_ARG, "q / seq_lens / out is NULL");
+  if (num_splits < 0 || num_splits > kMaxSplits) return fail(KVQ_ERR_ARG, "num_splits=%d", num_splits);
+  DecodeArgs a{};
+  if ((st = cache_ptrs(cfg, cache, &a.cp)) != KVQ_OK) return st;
+  const int splits = num_splits ? num_splits : splits_for(cfg, n_layers);
+  const int g = cfg->H_q / cfg->H_kv;
+  const size_t units = (size_t)n_layers * cfg->batch * cfg->H_kv;
+  // this call's scratch: status word, tickets, RoPE tables, split partials
+  const size_t off_tickets = kWsAlign;
+  size_t off = align_up(off_tickets + sizeof(uint32_t) * units);
+  const size_t off_rope = off;
+  int rope_rows = 0;
+  if (cfg->flags & KVQ_K_PRE_ROPE) {
+    rope_rows = (cfg->max_T + kTile - 1) / kTile + 1;
+    off = align_up(off + sizeof(float2) * (size_t)(rope_rows + kTile) * (cfg->D / 2));
+  }
+  const size_t off_partials = off;
+  if (splits > 1) off = align_up(off + sizeof(float) * units * splits * g * (cfg->D + 2));
+  if (off > (size_t)KVQ_STATIC_SCRATCH_BYTES)
+    return fail(KVQ_ERR_WORKSPACE, "this call needs %zu B of scratch; the static scratch holds %u B", off,
+                (unsigned)KVQ_STATIC_SCRATCH_BYTES);
+  void* base = nullptr;
+  if ((st = static_scratch(&base)) != KVQ_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  // status word and tickets must start at zero; the rest is overwritten
+  cudaError_t e = cudaMemsetAsync(base, 0, off_rope, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  if (rope_rows) {
+    e = launch_rope_tables((float2*)((char*)base + off_rope), rope_rows, cfg->D, cfg->rope_theta, s);
+    if (e != cudaSuccess) return cuda_fail(e, "rope table kernel");
+  }
+  a.lo = make_layout(cfg);
+  a.layer0 = layer0;
+  a.n_layers = n_layers;
+  a.q = (const uint16_t*)q;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.splits = splits;
+  a.status = (uint32_t*)base;
+  a.tickets = (uint32_t*)((char*)base + off_tickets);
+  a.partials = (float*)((char*)base + off_partials);
+  a.rope = (const float2*)((char*)base + off_rope);
+  a.rope_base_rows = rope_rows;
+  e = launch_decode(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+  return ok();
+}

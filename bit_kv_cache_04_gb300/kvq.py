@@ -123,6 +123,7 @@ def _load():
         "kvq_commit_lengths": ([cfgp, vp, vp, vp], ctypes.c_int),
         "kvq_decode_attention": ([cfgp, cachep, i32, i32, vp, vp, vp, i32, vp, sz, vp], ctypes.c_int),
         "kvq_decode_splits": ([cfgp, i32, P(i32)], ctypes.c_int),
+        "kvq_decode_attention_static": ([cfgp, cachep, i32, i32, vp, vp, vp, i32, vp], ctypes.c_int),
         "kvq_dequantize": ([cfgp, cachep, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "kvq_read_device_status": ([vp, P(u32), vp], ctypes.c_int),
         "kvq_clear_device_status": ([vp, vp], ctypes.c_int),
@@ -139,7 +140,8 @@ LIB = _load()
 # C-ABI names declared in include/kvq.h (checked by the tests).
 EXPORTED = ("kvq_version", "kvq_last_error", "kvq_validate_config", "kvq_block_bytes", "kvq_bytes_per_token",
             "kvq_cache_bytes", "kvq_buffer_sizes", "kvq_workspace_bytes", "kvq_workspace_init", "kvq_append",
-            "kvq_commit_lengths", "kvq_decode_attention", "kvq_decode_splits", "kvq_dequantize",
+            "kvq_commit_lengths", "kvq_decode_attention", "kvq_decode_splits", "kvq_decode_attention_static",
+            "kvq_dequantize",
             "kvq_read_device_status", "kvq_clear_device_status")
 
 

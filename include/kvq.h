@@ -236,6 +236,39 @@ KVQ_API kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_cache* cache,
                           int32_t t0, int32_t t1, const int32_t* seq_lens, float* k_out, float* v_out,
                           void* workspace, size_t ws_bytes, void* stream);
 
+/* Size of the library's built-in device scratch used by
+ * kvq_decode_attention_static (32 MiB on every GPU that loads the library,
+ * held until the process exits). */
+#define KVQ_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* Decode attention that allocates nothing and takes no workspace.
+ *
+ * There is no counterpart on the pages: this is an addition of this library
+ * for callers that cannot hand it device memory.  Examples are code whose
+ * device memory all belongs to another runtime's pool that it may not
+ * allocate from, and plugins that are given inputs and outputs but no
+ * scratch buffer.  kvq_decode_attention needs the caller to allocate a
+ * workspace; this variant keeps the same scratch (split partials, tickets,
+ * status word, RoPE tables) in a fixed device array inside the library.
+ *
+ * Arguments and results are those of kvq_decode_attention without the
+ * workspace.  The call needs 256 B + 4 B per (layer, sequence, kv head)
+ * unit + the RoPE tables (KVQ_K_PRE_ROPE) + the split partials; a call that
+ * needs more than KVQ_STATIC_SCRATCH_BYTES returns KVQ_ERR_WORKSPACE and
+ * launches nothing (pass a smaller n_layers or num_splits).  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * The first call on each device looks up the array's device address with
+ * that device current, so make that first call before any stream capture.
+ * Every call on a device uses the same array and leaves its contents
+ * behind; each call clears the parts that must start at zero (tickets and
+ * status word) on `stream`, so calls that overlap on the GPU (two streams,
+ * or two threads) race and must be serialized by the caller.  Device status
+ * bits of these calls are not reported. */
+KVQ_API kvq_status kvq_decode_attention_static(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0,
+                                               int32_t n_layers, const void* q, const int32_t* seq_lens,
+                                               float* out, int32_t num_splits, void* stream);
+
 /* Synchronizes `stream` and reads the device status word (KVQ_DEV_* bits). */
 KVQ_API kvq_status kvq_read_device_status(const void* workspace, uint32_t* bits, void* stream);
 
