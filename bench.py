@@ -90,6 +90,72 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+class NvmlClockSampler:
+    """SM clock and clock-event (throttle) reasons read through NVML every
+    `period` seconds on a background thread (read-only queries)."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index: int, period: float = 0.002):
+        import ctypes
+        import threading
+
+        self.ok = False
+        self.samples = []
+        self.period = period
+        self._stop = threading.Event()
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            count = ctypes.c_uint()
+            lib.nvmlDeviceGetCount_v2(ctypes.byref(count))
+            handle = ctypes.c_void_p()
+            idx = 0 if count.value == 1 else cuda_index
+            if lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(handle)) != 0:
+                return
+            mx = ctypes.c_uint()
+            lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx))
+            self.max_mhz = mx.value
+            self.lib, self.handle, self.ctypes = lib, handle, ctypes
+            fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.reasons_fn = fn
+            self.ok = True
+        except Exception:
+            self.ok = False
+        if self.ok:
+            self.thread = threading.Thread(target=self._run, daemon=True)
+
+    def _run(self):
+        import time as _t
+
+        c = self.ctypes
+        clk, rs = c.c_uint(), c.c_ulonglong()
+        while not self._stop.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.handle, 1, c.byref(clk)) == 0 and \
+                    self.reasons_fn(self.handle, c.byref(rs)) == 0:
+                self.samples.append((clk.value, rs.value))
+            _t.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self.thread.start()
+        return self.ok
+
+    def stop(self):
+        if not self.ok:
+            return None
+        self._stop.set()
+        self.thread.join()
+        if not self.samples:
+            return None
+        reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median([c for c, _ in self.samples]), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples), "source": "nvml, 2 ms period"}
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -183,8 +249,10 @@ def run_ours(args):
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
-    clocks = ClockSampler(local)
-    clocks.start()
+    clocks = NvmlClockSampler(local)
+    if not clocks.start():
+        clocks = ClockSampler(local)
+        clocks.start()
     t0, t1 = torch.cuda.Event(True), torch.cuda.Event(True)
     t0.record(stream)
     for i in range(warm, n_steps):

@@ -86,12 +86,18 @@ __device__ __forceinline__ void warp_quant_row(const float (&v)[NC][4], int G, i
     }
     const __half s16 = block_scale_of(m, qmax);
     const float sf = __half2float(s16);
-    const float rcp = __frcp_rn(sf);
+    const float rcp = sf == 0.f ? 0.f : __frcp_rn(sf);
     int code[4];
+    bool near = false;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      code[e] = quant_code_fast(v[c][e], sf, rcp, qmax);
-      if (dq) dq[c][e] = (float)code[e] * sf;
+    for (int e = 0; e < 4; ++e) code[e] = code_mul(v[c][e], rcp, qmax, near);
+    if (__any_sync(0xffffffffu, near)) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) code[e] = quant_code(v[c][e], sf, qmax);
+    }
+    if (dq) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dq[c][e] = (float)code[e] * sf;
     }
     const int ch0 = 128 * c + 4 * lane;
     const int pos = ch0 % G;
@@ -126,62 +132,123 @@ __device__ __forceinline__ void warp_quant_row(const float (&v)[NC][4], int G, i
 
 // ---- per-channel groups: one thread per channel, 32 tokens -----------------
 
-// Quantizes x[0], x[ld], ..., x[31 ld] (one channel over the group's tokens)
-// into the block at blk; dq (optional, stride 1) receives code * scale.
-__device__ __forceinline__ void thread_quant_channel(const float* x, int ld, int bits, uint8_t* blk, float* dq) {
-  const int qmax = qmax_of(bits);
-  float m = 0.f;
-#pragma unroll 8
-  for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(x[j * ld]));
-  const __half s16 = block_scale_of(m, qmax);
-  const float sf = __half2float(s16);
-  const float rcp = __frcp_rn(sf);
-  if (blk) *reinterpret_cast<__half*>(blk) = s16;
-  uint16_t* p = blk ? reinterpret_cast<uint16_t*>(blk + 2) : nullptr;
-  const int per16 = 16 / bits;  // codes per 16-bit store (8-bit: 2, 4-bit: 4, 2-bit: 8)
-  if (bits == 3) {
-    // eight codes per 24-bit word: 4 words = 12 bytes, written as 6 halves
-    uint32_t w[4];
+// The 32 codes of one per-channel block as a little-endian bit stream of
+// 32*B bits (code j, with its storage bias, at bit B*j; int8 two's
+// complement for B = 8): the byte layout of every packing of the format.
+template <int B, bool EXACT>
+__device__ __forceinline__ bool channel_stream(const float (&v)[32], float sf, float rcp, uint32_t (&w)[B],
+                                               float* dq) {
+  constexpr int qmax = (1 << (B - 1)) - 1;
+  bool near = false;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      w[k] = 0;
+  for (int k = 0; k < B; ++k) w[k] = 0;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int cd = quant_code_fast(x[(8 * k + e) * ld], sf, rcp, qmax);
-        if (dq) dq[8 * k + e] = (float)cd * sf;
-        w[k] |= (uint32_t)(cd + 4) << (3 * e);
-      }
-    }
-    if (p) {
-      const uint32_t b01 = w[0] | (w[1] << 24), b23 = (w[1] >> 8) | (w[2] << 16), b45 = (w[2] >> 16) | (w[3] << 8);
-      p[0] = (uint16_t)b01;
-      p[1] = (uint16_t)(b01 >> 16);
-      p[2] = (uint16_t)b23;
-      p[3] = (uint16_t)(b23 >> 16);
-      p[4] = (uint16_t)b45;
-      p[5] = (uint16_t)(b45 >> 16);
-    }
-    return;
+  for (int j = 0; j < 32; ++j) {
+    const int c = EXACT ? quant_code(v[j], sf, qmax) : code_mul(v[j], rcp, qmax, near);
+    if (dq) dq[j] = (float)c * sf;
+    const uint32_t u = B == 8 ? (uint32_t)(c & 0xFF) : (uint32_t)(c + qmax + 1);
+    const int bit = B * j, k = bit / 32, sh = bit % 32;
+    w[k] |= u << sh;
+    if (sh + B > 32) w[k + 1] |= u >> (32 - sh);
   }
-  for (int k = 0; k < 32 / per16; ++k) {
-    uint32_t hw = 0;
-    for (int e = 0; e < per16; ++e) {
-      const int cd = quant_code_fast(x[(per16 * k + e) * ld], sf, rcp, qmax);
-      if (dq) dq[per16 * k + e] = (float)cd * sf;
-      const uint32_t u = bits == 8 ? (uint32_t)(cd & 0xFF) : (uint32_t)(cd + qmax + 1);
-      hw |= u << (bits * e);
-    }
-    if (p) p[k] = (uint16_t)hw;
+  return near;
+}
+
+template <int B>
+__device__ __forceinline__ void channel_block(const float (&v)[32], float m, uint8_t* blk, float* dq) {
+  const __half s16 = block_scale_of(m, (1 << (B - 1)) - 1);
+  const float sf = __half2float(s16);
+  const float rcp = sf == 0.f ? 0.f : __frcp_rn(sf);
+  uint32_t w[B];
+  if (channel_stream<B, false>(v, sf, rcp, w, dq)) channel_stream<B, true>(v, sf, rcp, w, dq);
+  if (!blk) return;
+  *reinterpret_cast<__half*>(blk) = s16;
+  uint16_t* p = reinterpret_cast<uint16_t*>(blk + 2);
+#pragma unroll
+  for (int k = 0; k < B; ++k) {
+    p[2 * k] = (uint16_t)w[k];
+    p[2 * k + 1] = (uint16_t)(w[k] >> 16);
   }
 }
 
-// Phase B: quantize units [q_end(T0), q_end(T1)).
+// Quantizes x[0], x[ld], ..., x[31 ld] (one channel over the group's tokens)
+// into the block at blk (skipped when null); dq (optional) receives
+// code * scale.
+__device__ __forceinline__ void thread_quant_channel(const float* x, int ld, int bits, uint8_t* blk, float* dq) {
+  float v[32];
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    v[j] = x[j * ld];
+    m = fmaxf(m, fabsf(v[j]));
+  }
+  switch (bits) {
+    case 8: channel_block<8>(v, m, blk, dq); break;
+    case 4: channel_block<4>(v, m, blk, dq); break;
+    case 3: channel_block<3>(v, m, blk, dq); break;
+    default: channel_block<2>(v, m, blk, dq); break;
+  }
+}
+
+__device__ __forceinline__ float4 f16x4_to_f32(uint2 w, int dtype) {
+  return make_float4(in_to_f32((uint16_t)(w.x & 0xFFFF), dtype), in_to_f32((uint16_t)(w.x >> 16), dtype),
+                     in_to_f32((uint16_t)(w.y & 0xFFFF), dtype), in_to_f32((uint16_t)(w.y >> 16), dtype));
+}
+
+// 32 values of a block (x[0], x[st], ..., x[31 st]) quantized with the scale
+// of block absolute maximum m (shared by the threads of a 128-value block);
+// the payload (32*B bits) goes to dst, the scale to blk when blk is given.
+template <int B>
+__device__ __forceinline__ void quant32(const float* x, int st, float m, uint8_t* blk, uint8_t* dst, float* dq) {
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = x[j * st];
+  const __half s16 = block_scale_of(m, (1 << (B - 1)) - 1);
+  const float sf = __half2float(s16);
+  const float rcp = sf == 0.f ? 0.f : __frcp_rn(sf);
+  uint32_t w[B];
+  if (channel_stream<B, false>(v, sf, rcp, w, dq)) channel_stream<B, true>(v, sf, rcp, w, dq);
+  if (blk) *reinterpret_cast<__half*>(blk) = s16;
+  if (!dst) return;
+  uint16_t* p = reinterpret_cast<uint16_t*>(dst);
+#pragma unroll
+  for (int k = 0; k < B; ++k) {
+    p[2 * k] = (uint16_t)w[k];
+    p[2 * k + 1] = (uint16_t)(w[k] >> 16);
+  }
+}
+
+__device__ __forceinline__ void quant32_bits(int bits, const float* x, int st, float m, uint8_t* blk, uint8_t* dst,
+                                             float* dq) {
+  switch (bits) {
+    case 8: quant32<8>(x, st, m, blk, dst, dq); break;
+    case 4: quant32<4>(x, st, m, blk, dst, dq); break;
+    case 3: quant32<3>(x, st, m, blk, dst, dq); break;
+    default: quant32<2>(x, st, m, blk, dst, dq); break;
+  }
+}
+
+__device__ __forceinline__ float amax32(const float* x, int st) {
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(x[j * st]));
+  return m;
+}
+
+// Phase B: quantize units [q_end(T0), q_end(T1)).  The chunk's K and V rows
+// are staged in shared memory as fp32 (each 128-chunk of a row rotated on the
+// way by the warp that loads it, when asked); then every thread quantizes 32
+// values: one channel over the group's tokens (per-channel blocks) or a
+// 32-value slice of a token row (per-token blocks; a 128-value block spans 4
+// neighbouring threads, which combine their absolute maxima).
 template <int NC>
 __global__ void __launch_bounds__(kAppendThreads) append_quantize_kernel(AppendArgs a) {
-  extern __shared__ float xs[];  // [kTile][D + 1], per-channel groups only
+  constexpr int D = 128 * NC;
+  constexpr int LDX = D + 4;  // 16-byte aligned rows, conflict-free column reads
+  constexpr int SUB = D / 32;  // 32-value slices per row
+  extern __shared__ __align__(16) float xs[];  // [2][kTile][LDX]
   __shared__ uint32_t page_bad;
   const Layout& lo = a.lo;
-  constexpr int D = 128 * NC;
   const int li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B, h = blockIdx.y;
   const int layer = a.layer0 + li;
   SeqSpan s = read_span(a, seq);
@@ -191,57 +258,96 @@ __global__ void __launch_bounds__(kAppendThreads) append_quantize_kernel(AppendA
   const int u0 = max(base, q0), u1 = min(base + kTile, q1);
   if (u0 >= u1) return;
   const int n_tok = u1 - u0;
-  const int ld = D + 1;
   const bool to_cold = lo.tiered && u0 < c1;
-  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  if (threadIdx.x == 0) page_bad = 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  if (tid == 0) page_bad = 0;
+
+  // 1. stage the rows (one warp per row, lane l holds channels 128c+4l..+3)
+  {
+    uint2 raw[2][kTile / 4][NC];
+#pragma unroll
+    for (int which = 0; which < 2; ++which)
+#pragma unroll
+      for (int r = 0; r < kTile / 4; ++r) {
+        const int j = warp + 4 * r;
+        if (j < n_tok) {
+          const int t = u0 + j;
+          const uint16_t* src = t < s.T0 ? resid_row(lo, a.cp, which, layer, seq, h, t) : input_row(a, which, li, s, h, t);
+#pragma unroll
+          for (int c = 0; c < NC; ++c) raw[which][r][c] = *reinterpret_cast<const uint2*>(src + 128 * c + 4 * lane);
+        }
+      }
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const bool rotate = (lo.flags & (which ? KVQ_ROTATE_V : KVQ_ROTATE_K)) != 0;
+      float* tile = xs + which * kTile * LDX;
+#pragma unroll
+      for (int r = 0; r < kTile / 4; ++r) {
+        const int j = warp + 4 * r;
+        if (j >= n_tok) break;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const float4 x = f16x4_to_f32(raw[which][r][c], lo.dtype);
+          float v[4] = {x.x, x.y, x.z, x.w};
+          if (rotate) warp_rotate128(v, lo.d1, lo.d2);
+          *reinterpret_cast<float4*>(tile + j * LDX + 128 * c + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+      }
+    }
+  }
   __syncthreads();
+
+  // 2. quantize
+#pragma unroll
   for (int which = 0; which < 2; ++which) {
     const FmtInfo& f = fmt_main(lo, which);
     const FmtInfo& fc = fmt_cold(lo, which);
-    auto src_row = [&](int t) -> const uint16_t* {
-      return t < s.T0 ? resid_row(lo, a.cp, which, layer, seq, h, t) : input_row(a, which, li, s, h, t);
-    };
+    const float* tile = xs + which * kTile * LDX;
     if (f.axis == KVQ_AXIS_CHANNEL) {
-      // the unit is one whole group of 32 tokens: gather it, then one thread per channel
-      __syncthreads();
-      for (int e = threadIdx.x; e < kTile * (D / 4); e += blockDim.x) {
-        const int j = e / (D / 4), d4 = (e % (D / 4)) * 4;
-        const uint2 w = *reinterpret_cast<const uint2*>(src_row(u0 + j) + d4);
-        float* xr = xs + j * ld + d4;
-        xr[0] = in_to_f32((uint16_t)(w.x & 0xFFFF), lo.dtype);
-        xr[1] = in_to_f32((uint16_t)(w.x >> 16), lo.dtype);
-        xr[2] = in_to_f32((uint16_t)(w.y & 0xFFFF), lo.dtype);
-        xr[3] = in_to_f32((uint16_t)(w.y >> 16), lo.dtype);
-      }
-      __syncthreads();
-      for (int c = threadIdx.x; c < D; c += blockDim.x) {
+      // one group of 32 tokens; thread = channel
+      for (int c = tid; c < D; c += blockDim.x) {
+        const float* x = tile + c;
+        const float m = amax32(x, LDX);
         if (to_cold) {
           float dq[32];
-          thread_quant_channel(xs + c, ld, f.bits, nullptr, dq);
-          uint8_t* dst = cold_row(lo, a.cp, which, layer, seq, h, u0) + (int64_t)c * fc.bb;
-          thread_quant_channel(dq, 1, fc.bits, dst, nullptr);
+          quant32_bits(f.bits, x, LDX, m, nullptr, nullptr, dq);
+          uint8_t* blk = cold_row(lo, a.cp, which, layer, seq, h, u0) + (int64_t)c * fc.bb;
+          quant32_bits(fc.bits, dq, 1, amax32(dq, 1), blk, blk + 2, nullptr);
         } else {
           bool bad = false;
-          uint8_t* row = main_row(lo, a.cp, which, layer, seq, h, u0, &bad);
-          thread_quant_channel(xs + c, ld, f.bits, row + (int64_t)c * f.bb, nullptr);
+          uint8_t* blk = main_row(lo, a.cp, which, layer, seq, h, u0, &bad) + (int64_t)c * f.bb;
+          quant32_bits(f.bits, x, LDX, m, blk, blk + 2, nullptr);
         }
       }
       continue;
     }
-    const bool rotate = (lo.flags & (which ? KVQ_ROTATE_V : KVQ_ROTATE_K)) != 0;
-    for (int j = warp; j < n_tok; j += nw) {
-      const int t = u0 + j;
-      float v[NC][4];
-      load_row<NC>(src_row(t), lo.dtype, v);
-      if (rotate) {
-#pragma unroll
-        for (int c = 0; c < NC; ++c) warp_rotate128(v[c], lo.d1, lo.d2);
+    // per-token: thread = (row, 32-value slice); every lane runs the loop so
+    // that the 4-lane amax exchange of 128-value blocks stays warp-uniform
+    const int spb = f.group / 32;  // slices per block
+    for (int u = tid; u < kTile * SUB; u += blockDim.x) {
+      const int j = u / SUB, sl = u % SUB;
+      const bool valid = j < n_tok;
+      const float* x = tile + j * LDX + 32 * sl;
+      float m = valid ? amax32(x, 1) : 0.f;
+      if (spb == 4) {
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
       }
+      if (!valid) continue;
+      const int t = u0 + j;
+      const int b = sl / spb, within = sl % spb;  // block, slice within the block
       if (to_cold) {
-        float dq[NC][4];
-        warp_quant_row<NC>(v, f.group, f.bits, nullptr, dq);
-        warp_quant_row<NC>(dq, fc.group, fc.bits, cold_row(lo, a.cp, which, layer, seq, h, t), nullptr);
+        float dq[32];
+        quant32_bits(f.bits, x, 1, m, nullptr, nullptr, dq);
+        // the cold format keeps the hot group size: one 32-slice block when G = 32
+        uint8_t* row = cold_row(lo, a.cp, which, layer, seq, h, t);
+        uint8_t* blk = row + b * fc.bb;
+        float mc = amax32(dq, 1);
+        if (spb == 4) {
+          mc = fmaxf(mc, __shfl_xor_sync(__activemask(), mc, 1));
+          mc = fmaxf(mc, __shfl_xor_sync(__activemask(), mc, 2));
+        }
+        quant32_bits(fc.bits, dq, 1, mc, within == 0 ? blk : nullptr, blk + 2 + within * 4 * fc.bits, nullptr);
       } else {
         bool bad = false;
         uint8_t* row = main_row(lo, a.cp, which, layer, seq, h, t, &bad);
@@ -249,12 +355,13 @@ __global__ void __launch_bounds__(kAppendThreads) append_quantize_kernel(AppendA
           page_bad = 1;
           continue;
         }
-        warp_quant_row<NC>(v, f.group, f.bits, row, nullptr);
+        uint8_t* blk = row + b * f.bb;
+        quant32_bits(f.bits, x, 1, m, within == 0 ? blk : nullptr, blk + 2 + within * 4 * f.bits, nullptr);
       }
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0 && page_bad) atomicOr(a.status, KVQ_DEV_PAGE);
+  if (tid == 0 && page_bad) atomicOr(a.status, KVQ_DEV_PAGE);
 }
 
 // Phase A: hot units [c_end(T0), min(c_end(T1), q_end(T0))) -> cold, from the
@@ -338,11 +445,10 @@ cudaError_t launch_append_nc(const AppendArgs& a, cudaStream_t st) {
   const Layout& lo = a.lo;
   const int chunks = (a.max_new + kTile - 1) / kTile + 2;
   dim3 grid(chunks, lo.H, a.n_layers * lo.B);
-  const size_t smem = sizeof(float) * kTile * (lo.D + 1);
+  const size_t smem = sizeof(float) * 2 * kTile * (lo.D + 4);
   static bool attr_done = false;
   if (!attr_done) {
-    cudaFuncSetAttribute(append_quantize_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-    cudaFuncSetAttribute(append_requant_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    cudaFuncSetAttribute(append_quantize_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 80 * 1024);
     attr_done = true;
   }
   if (lo.tiered) append_requant_kernel<NC><<<grid, kAppendThreads, 0, st>>>(a);

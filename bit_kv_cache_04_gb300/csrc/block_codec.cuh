@@ -64,19 +64,17 @@ __device__ __forceinline__ int quant_code(float x, float sf, int qmax) {
   return (int)r;
 }
 
-// The same code as quant_code(x, sf, qmax) given rcp = fp32(1/sf), with one
-// multiply instead of the division: |x*rcp - fp32(x/sf)| <= 1.5 * 2^-23 *
-// |x/sf| <= 2.3e-5 for |x/sf| <= 128, so unless the product lies within 2^-14
-// of a half-integer both round to the same integer; near a half-integer the
-// exact IEEE quotient decides.
-__device__ __forceinline__ int quant_code_fast(float x, float sf, float rcp, int qmax) {
-  if (sf == 0.0f) return 0;
-  float q = x * rcp;
-  const float fr = q - floorf(q);
-  if (fabsf(fr - 0.5f) < 6.103515625e-05f) q = __fdiv_rn(x, sf);
-  float r = rintf(q);
-  r = fminf(fmaxf(r, (float)-qmax), (float)qmax);
-  return (int)r;
+// The code of x with one multiply, given rcp = fp32(1/sf) (0 for a zero
+// scale).  |x*rcp - fp32(x/sf)| <= 1.5 * 2^-23 * |x/sf| <= 3.5e-5 for the
+// quotients a block produces (|x/sf| <= 1.5 qmax, fp16 subnormal scales
+// included), so unless the product lies within 2^-14 of a half-integer it
+// rounds to the same integer as rint(x / sf); `near` is set otherwise and the
+// caller redoes the block with quant_code (the exact IEEE quotient).
+__device__ __forceinline__ int code_mul(float x, float rcp, int qmax, bool& near) {
+  const float q = x * rcp;
+  const float r = rintf(q);
+  near |= fabsf(q - r) > 0.49993896484375f;
+  return (int)fminf(fmaxf(r, (float)-qmax), (float)qmax);
 }
 
 // fp16 scale of a block with absolute maximum amax: fp16_rn(min(amax/qmax, 65504)).
@@ -152,9 +150,9 @@ __device__ __forceinline__ int unpack_code(const uint8_t* p, int bits, int i) {
   return (int)((p[i >> 2] >> (2 * (i & 3))) & 3u) - 2;
 }
 
+// fp16 scale at the start of a block (blocks start at even offsets).
 __device__ __forceinline__ float block_scale(const uint8_t* blk) {
-  uint16_t sb = (uint16_t)blk[0] | ((uint16_t)blk[1] << 8);
-  return __half2float(__ushort_as_half(sb));
+  return __half2float(*reinterpret_cast<const __half*>(blk));
 }
 
 // Dequantizes a whole block into out[0..G-1] (code * scale, exact).

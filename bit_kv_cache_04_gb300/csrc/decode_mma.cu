@@ -1,8 +1,10 @@
 // Split-K decode attention on the tensor cores (mma.sync m16n8k16, fp16
-// operands, fp32 accumulators) for single-tier caches:
-//   K per-channel 4-bit over 32-token groups, or per-token 8/4/3-bit blocks;
-//   V per-token 8/4/3-bit blocks; an optional fp16 window; optional rotation
-//   (no window then); contiguous or 16/32-token pages.
+// operands, fp32 accumulators):
+//   K per-channel 4/2-bit over 32-token groups, or per-token 8/4/3-bit blocks;
+//   V per-token 8/4/3/2-bit blocks; an optional fp16 window; a hot/cold pair
+//   of per-channel formats; keys stored pre-RoPE (split-half RoPE applied in
+//   the kernel); optional rotation (no window then); contiguous or 16/32-token
+//   pages.
 //
 // Per 32-token group the scores are S^T[token][col] = K[token][d] Q^T[d][col]
 // with tokens on M and, on N, the query heads sharing the kv head, each head
@@ -16,14 +18,22 @@
 // rotate the query once, read blocks as code x scale, rotate the output back
 // once) with nalar.dev's s_i = q.k_i / sqrt(D) and output = sum_i p_i v_i.
 //
+// Pre-RoPE keys (troisinh.com "KV Cache Quantization", "RoPE - Cai bay tinh
+// vi"; split-half pairs as lehuy.net "NexusQuant" lists): with t = t0 + j in a
+// group starting at t0, q . R(t) k = (R(-t0) q) . (R(j) k).  The query is
+// turned by -t0 once per group; each key value is dequantized, turned by its
+// in-group offset j and split into fp16 hi + lo, so the product keeps ~22
+// bits on both sides.  Angles come from fp64 tables in the workspace.
+//
 // Layout of one group: M-tile mu (0, 1) row r is token
 // tau(mu, r) = 4(r & 7) + 2mu + (r >> 3); k-chunk kc = 2s + b (span s of 32
 // channels) pairs channels (c, c+4) in k-slots (2t, 2t+1) and (c+1, c+5) in
-// (2t+8, 2t+9), c = 32s + 8t + 2b (t = lane % 4); d-tile (s, e) row r is
-// channel 32s + 4(r & 7) + 2e + (r >> 3).
+// (2t+8, 2t+9), c = 32s + 8t + 2b (t = lane % 4), so channel c + D/2 sits in
+// k-chunk kc + D/32 at the same slot (the RoPE partner); d-tile (s, e) row r
+// is channel 32s + 4(r & 7) + 2e + (r >> 3).
 //
 // Work split: CTA = 4 warps on one (layer, sequence, kv head, token split);
-// each warp streams its own groups through a 3-stage cp.async ring and keeps
+// each warp streams its own groups through a 2-stage cp.async ring and keeps
 // its own online softmax; warps merge in shared memory and splits merge in
 // the workspace (the last CTA to take a ticket combines; nobody waits).
 #include "block_codec.cuh"
@@ -34,38 +44,53 @@ cudaError_t launch_decode_generic(const DecodeArgs& a, cudaStream_t s);
 
 namespace {
 
-enum : int { KF_CH4 = 0, KF_T8 = 1, KF_T4 = 2, KF_T3 = 3 };
-enum : int { VF_T8 = 0, VF_T4 = 1, VF_T3 = 2 };
+enum : int { KF_CH4 = 0, KF_T8 = 1, KF_T4 = 2, KF_T3 = 3, KF_CH2 = 4 };
+enum : int { VF_T8 = 0, VF_T4 = 1, VF_T3 = 2, VF_T2 = 3 };
 
 constexpr int kWarps = 4;
 constexpr int kThreadsMma = kWarps * 32;
-constexpr int kStages = 3;
+constexpr int kStages = 2;  // per-warp cp.async ring: one group in flight while one is consumed
 constexpr float kLog2eF = 1.4426950408889634f;
 
-constexpr int bits_k(int kf) { return kf == KF_T8 ? 8 : kf == KF_T3 ? 3 : 4; }
-constexpr int bits_v(int vf) { return vf == VF_T8 ? 8 : vf == VF_T3 ? 3 : 4; }
+constexpr int bits_k(int kf) { return kf == KF_T8 ? 8 : kf == KF_T3 ? 3 : kf == KF_CH2 ? 2 : 4; }
+constexpr int bits_v(int vf) { return vf == VF_T8 ? 8 : vf == VF_T3 ? 3 : vf == VF_T2 ? 2 : 4; }
 constexpr int align16(int x) { return (x + 15) / 16 * 16; }
 
-template <int D_, int NT_, int KF_, int KG_, int VF_, int VG_>
-struct Cfg {
-  static constexpr int D = D_, NT = NT_, KF = KF_, KG = KG_, VF = VF_, VG = VG_;
+// Byte geometry of one tier's formats.
+template <int D, int KF_, int KG_, int VF_, int VG_>
+struct Tier {
+  static constexpr int KF = KF_, KG = KG_, VF = VF_, VG = VG_;
   static constexpr int KB = bits_k(KF), VB = bits_v(VF);
-  static constexpr bool KCH = KF == KF_CH4;
+  static constexpr bool KCH = KF == KF_CH4 || KF == KF_CH2;
   static constexpr int KBB = 2 + (KCH ? 32 : KG) * KB / 8;  // block bytes
   static constexpr int VBB = 2 + VG * VB / 8;
   static constexpr int KROW = KCH ? D * KBB : (D / KG) * KBB;  // group row / token row
   static constexpr int VROW = (D / VG) * VBB;
   static constexpr int KSTAGE = KCH ? KROW : 32 * KROW;
   static constexpr int VSTAGE = 32 * VROW;
-  static constexpr int VOFF = align16(KSTAGE + 16);
-  static constexpr int STAGE = VOFF + align16(VSTAGE + 16);
-  static constexpr int KC = D / 16;  // k-chunks
-  static constexpr int NS = D / 32;  // spans
   static constexpr int KSPB = KCH ? 1 : KG / 32;  // spans per K block
   static constexpr int VSPB = VG / 32;
   static constexpr int KSPAN = 32 * KB / 8;  // code bytes of a span of one token
   static constexpr int VSPAN = 32 * VB / 8;
-  static constexpr int QSM = KC * NT * 32 * 16;  // per-lane query values
+};
+
+constexpr int cmax(int a, int b) { return a > b ? a : b; }
+
+// HOT: the only tier (COLD_ = false) or the hot tier; COLD: the cold tier.
+template <int D_, int NT_, class HOT_, class COLD_, bool HAS_COLD_, bool ROPE_>
+struct Cfg {
+  static constexpr int D = D_, NT = NT_;
+  using HOT = HOT_;
+  using COLD = COLD_;
+  static constexpr bool HAS_COLD = HAS_COLD_, ROPE = ROPE_;
+  static constexpr int KSTAGE = HAS_COLD ? cmax(HOT::KSTAGE, COLD::KSTAGE) : HOT::KSTAGE;
+  static constexpr int VSTAGE = HAS_COLD ? cmax(HOT::VSTAGE, COLD::VSTAGE) : HOT::VSTAGE;
+  static constexpr int VOFF = align16(KSTAGE + 16);
+  static constexpr int STAGE = VOFF + align16(VSTAGE + 16);
+  static constexpr int KC = D / 16;  // k-chunks
+  static constexpr int NS = D / 32;  // spans
+  static constexpr int QSM = KC * NT * 32 * (16 + (ROPE ? 16 : 0));  // per-lane query fragments
+  static constexpr int MIN_CTAS = D == 128 ? 4 : 2;  // CTAs per SM the register budget aims at
   static constexpr int SMEM = QSM + kWarps * kStages * STAGE;
 };
 
@@ -133,6 +158,29 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t x, int j) {
   if constexpr (B == 3) return hsub2u(((x >> (3 * j)) & 0x00070007u) | 0x64006400u, 0x64046404u);
   return hsub2u(((x >> (2 * j)) & 0x00030003u) | 0x64006400u, 0x64026402u);
 }
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Eight 4-bit codes, four per 16-bit half of x (nibble j of each half), as
+// the fp16 pairs r[j] = (low-half code j, high-half code j) - 8.  Nibbles 0
+// and 2 go through 1024 + n; nibbles 1 and 3 through 1024 + 16n, scaled by
+// 1/16 and offset by -72 in one exact fma.
+__device__ __forceinline__ void dq4(uint32_t x, uint32_t (&r)[4]) {
+  r[0] = hsub2u((x & 0x000F000Fu) | 0x64006400u, 0x64086408u);
+  r[1] = hfma2u((x & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, 0xD480D480u);
+  x >>= 8;
+  r[2] = hsub2u((x & 0x000F000Fu) | 0x64006400u, 0x64086408u);
+  r[3] = hfma2u((x & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, 0xD480D480u);
+}
+
 // Two int8 codes in byte 0 of each 16-bit half of (x >> 8j).
 __device__ __forceinline__ uint32_t code_pair8(uint32_t x, int j) {
   return hsub2u(((x >> (8 * j)) & 0x00FF00FFu) ^ 0x64806480u, 0x64806480u);
@@ -143,9 +191,7 @@ __device__ __forceinline__ uint32_t code_pair8(uint32_t x, int j) {
 template <class C>
 __device__ __forceinline__ void k_token_pairs(const uint8_t* p, int tq, uint32_t (&r)[4]) {
   if constexpr (C::KB == 4) {
-    const uint32_t w = ld_u32e(p + 4 * tq);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) r[j] = code_pair<4>(w, j);
+    dq4(ld_u32e(p + 4 * tq), r);
   } else if constexpr (C::KB == 8) {
     const uint32_t w0 = ld_u32e(p + 8 * tq), w1 = ld_u32e(p + 8 * tq + 4);
     const uint32_t xa = __byte_perm(w0, w1, 0x5410), xb = __byte_perm(w0, w1, 0x7632);
@@ -178,14 +224,21 @@ __device__ __forceinline__ void v_pair4(const uint8_t* pa, const uint8_t* pb, in
     if constexpr (C::VB == 4) {
       ua = ld_u16(pa + 2 * gq);
       ub = ld_u16(pb + 2 * gq);
-    } else {  // 3 bits: 12 bits at bit 12*gq of the span
+    } else if constexpr (C::VB == 3) {  // 12 bits at bit 12*gq of the span
       const int sh = 12 * (gq & 1), bo = 3 * (gq >> 1);
       ua = (ld_u24(pa + bo) >> sh) & 0xFFFu;
       ub = (ld_u24(pb + bo) >> sh) & 0xFFFu;
+    } else {  // 2 bits: byte gq of the span
+      ua = pa[gq];
+      ub = pb[gq];
     }
-    const uint32_t x = ua | (ub << 16);
+    const uint32_t x = __byte_perm(ua, ub, 0x5410);
+    if constexpr (C::VB == 4) {
+      dq4(x, r);
+    } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) r[j] = code_pair<C::VB>(x, j);
+      for (int j = 0; j < 4; ++j) r[j] = code_pair<C::VB>(x, j);
+    }
   }
 }
 
@@ -244,12 +297,272 @@ __device__ __forceinline__ void p_fragments(float pa, float pb, uint32_t& b0, ui
   b1 = movtrans(pack_h2(hb, pb - hb));
 }
 
+// Per-thread context of the decode kernel shared with its helpers.
 template <class C>
-__global__ void __launch_bounds__(kThreadsMma) decode_mma_kernel(DecodeArgs a) {
+struct Ctx {
+  int gq, tq, lane;
+  bool lo_part;
+  uint32_t lo_mask;
+  const uint2* qb;        // [KC][NT][32]: B fragments (hi or lo part)
+  const uint2* qh;        // [KC][NT][32]: query half pairs
+  const float4* qr;       // [KC][NT][32]: fp32 query (RoPE)
+  const float2* rope_base;
+  const float2* rope_off;
+};
+
+// B fragments of the query turned by -t0 (pre-RoPE keys): lower channel c
+// and its partner c + D/2 sit in k-chunks kcp and kcp + KC/2.
+template <class C>
+__device__ __forceinline__ void rope_query(const Ctx<C>& cx, int t0, uint32_t (&qg)[C::KC][C::NT][2]) {
+  constexpr int D = C::D, NT = C::NT, KC = C::KC;
+  const float2* base = cx.rope_base + (int64_t)(t0 / kTile) * (D / 2);
+#pragma unroll
+  for (int kcp = 0; kcp < KC / 2; ++kcp) {
+    const int c = 32 * (kcp >> 1) + 8 * cx.tq + 2 * (kcp & 1);
+    const float2 f0 = __ldg(base + c), f1 = __ldg(base + c + 4), f2 = __ldg(base + c + 1), f3 = __ldg(base + c + 5);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float4 l = cx.qr[(kcp * NT + nt) * 32 + cx.lane], u = cx.qr[((kcp + KC / 2) * NT + nt) * 32 + cx.lane];
+      const float l0 = l.x * f0.x + u.x * f0.y, u0 = u.x * f0.x - l.x * f0.y;
+      const float l1 = l.y * f1.x + u.y * f1.y, u1 = u.y * f1.x - l.y * f1.y;
+      const float l2 = l.z * f2.x + u.z * f2.y, u2 = u.z * f2.x - l.z * f2.y;
+      const float l3 = l.w * f3.x + u.w * f3.y, u3 = u.w * f3.x - l.w * f3.y;
+      qg[kcp][nt][0] = pack_h2(split_part(l0, cx.lo_part), split_part(l1, cx.lo_part));
+      qg[kcp][nt][1] = pack_h2(split_part(l2, cx.lo_part), split_part(l3, cx.lo_part));
+      qg[kcp + KC / 2][nt][0] = pack_h2(split_part(u0, cx.lo_part), split_part(u1, cx.lo_part));
+      qg[kcp + KC / 2][nt][1] = pack_h2(split_part(u2, cx.lo_part), split_part(u3, cx.lo_part));
+    }
+  }
+}
+
+// fp32 key values of lower channels ch[0..3] (lv) and their partners (uv)
+// at token offset j of the group, turned by R(j), as hi/lo A fragments (row
+// rr of the A tile; [0] lower k-chunk, [1] partner k-chunk).
+template <class C>
+__device__ __forceinline__ void rope_key_frags(const Ctx<C>& cx, int j, const float (&lv)[4], const float (&uv)[4],
+                                               int rr, const int (&ch)[4], uint32_t (&ah)[2][4],
+                                               uint32_t (&al)[2][4]) {
+  float nl[4], nu[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 cs = __ldg(cx.rope_off + j * (C::D / 2) + ch[q]);
+    nl[q] = lv[q] * cs.x - uv[q] * cs.y;
+    nu[q] = lv[q] * cs.y + uv[q] * cs.x;
+  }
+  const float hl0 = rn16(nl[0]), hl1 = rn16(nl[1]), hl2 = rn16(nl[2]), hl3 = rn16(nl[3]);
+  const float hu0 = rn16(nu[0]), hu1 = rn16(nu[1]), hu2 = rn16(nu[2]), hu3 = rn16(nu[3]);
+  ah[0][rr] = pack_h2(hl0, hl1);
+  ah[0][2 + rr] = pack_h2(hl2, hl3);
+  al[0][rr] = pack_h2(nl[0] - hl0, nl[1] - hl1);
+  al[0][2 + rr] = pack_h2(nl[2] - hl2, nl[3] - hl3);
+  ah[1][rr] = pack_h2(hu0, hu1);
+  ah[1][2 + rr] = pack_h2(hu2, hu3);
+  al[1][rr] = pack_h2(nu[0] - hu0, nu[1] - hu1);
+  al[1][2 + rr] = pack_h2(nu[2] - hu2, nu[3] - hu3);
+}
+
+// PV for one packed group: P^T per V block (probabilities times the per-token
+// value scales), O^T += V^T P^T.
+template <class C, class TR>
+__device__ __forceinline__ void pv_packed(const Ctx<C>& cx, WarpState<C>& ws, const uint8_t* vsm, int n_valid,
+                                          const float (&p)[C::NT][4]) {
   constexpr int D = C::D, NT = C::NT;
+  const int gq = cx.gq, tq = cx.tq;
+#pragma unroll
+    for (int bv = 0; bv < D / TR::VG; ++bv) {
+      uint32_t pb[2][NT][2];
+#pragma unroll
+      for (int mu = 0; mu < 2; ++mu) {
+        const int ra = 4 * gq + 2 * mu;
+        const float sva = block_scale(vsm + ra * TR::VROW + bv * TR::VBB);
+        const float svb = block_scale(vsm + (ra + 1) * TR::VROW + bv * TR::VBB);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float pa = ra < n_valid ? p[nt][2 * mu] * sva : 0.f;
+          const float pbb = ra + 1 < n_valid ? p[nt][2 * mu + 1] * svb : 0.f;
+          p_fragments(pa, pbb, pb[mu][nt][0], pb[mu][nt][1]);
+        }
+      }
+#pragma unroll
+      for (int ss = 0; ss < TR::VSPB; ++ss) {
+        const int s = bv * TR::VSPB + ss;
+        const int off = bv * TR::VBB + 2 + ss * TR::VSPAN;
+#pragma unroll
+        for (int mu = 0; mu < 2; ++mu) {
+          const int T1 = 8 * tq + 2 * mu;
+          uint32_t x12[4], x34[4];
+          v_pair4<TR>(vsm + T1 * TR::VROW + off, vsm + (T1 + 4) * TR::VROW + off, gq, x12);
+          v_pair4<TR>(vsm + (T1 + 1) * TR::VROW + off, vsm + (T1 + 5) * TR::VROW + off, gq, x34);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma16816(ws.o[2 * s][nt], x12[0], x12[1], x34[0], x34[1], pb[mu][nt][0], pb[mu][nt][1]);
+            mma16816(ws.o[2 * s + 1][nt], x12[2], x12[3], x34[2], x34[3], pb[mu][nt][0], pb[mu][nt][1]);
+          }
+        }
+      }
+    }
+  }
+
+// Scores of one packed group into S (see the layout notes at the top).
+template <class C, class TR>
+__device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* ksm, int t0, float (&S)[2][C::NT][4]) {
+  constexpr int D = C::D, NT = C::NT, KC = C::KC;
+  const int gq = cx.gq, tq = cx.tq, lane = cx.lane;
+  const uint32_t lo_mask = cx.lo_mask;
+  const uint2* qb = cx.qb;
+  const uint2* qh = cx.qh;
+    if constexpr (TR::KCH && C::ROPE) {
+      uint32_t qg[KC][NT][2];
+      rope_query<C>(cx, t0, qg);
+#pragma unroll
+      for (int kcp = 0; kcp < KC / 2; ++kcp) {
+        const int c = 32 * (kcp >> 1) + 8 * tq + 2 * (kcp & 1);
+        const int ch[4] = {c, c + 4, c + 1, c + 5};
+        float sl[4], su[4];
+        uint32_t xl[2], xu[2];
+        uint32_t chl[4], chu[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint8_t* bl = ksm + ch[q] * TR::KBB;
+          const uint8_t* bu = ksm + (ch[q] + D / 2) * TR::KBB;
+          sl[q] = block_scale(bl);
+          su[q] = block_scale(bu);
+          chl[q] = TR::KB == 4 ? ld_u16(bl + 2 + 2 * gq) : (uint32_t)bl[2 + gq];
+          chu[q] = TR::KB == 4 ? ld_u16(bu + 2 + 2 * gq) : (uint32_t)bu[2 + gq];
+        }
+        xl[0] = __byte_perm(chl[0], chl[1], 0x5410);
+        xl[1] = __byte_perm(chl[2], chl[3], 0x5410);
+        xu[0] = __byte_perm(chu[0], chu[1], 0x5410);
+        xu[1] = __byte_perm(chu[2], chu[3], 0x5410);
+        uint32_t cl0[4], cl1[4], cu0[4], cu1[4];  // per token k of the thread: (ch0, ch1), (ch2, ch3)
+        if constexpr (TR::KB == 4) {
+          dq4(xl[0], cl0);
+          dq4(xl[1], cl1);
+          dq4(xu[0], cu0);
+          dq4(xu[1], cu1);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            cl0[k] = code_pair<2>(xl[0], k);
+            cl1[k] = code_pair<2>(xl[1], k);
+            cu0[k] = code_pair<2>(xu[0], k);
+            cu1[k] = code_pair<2>(xu[1], k);
+          }
+        }
+#pragma unroll
+        for (int mu = 0; mu < 2; ++mu) {
+          uint32_t ah[2][4], al[2][4];
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int k = 2 * mu + rr;
+            const float2 l01 = __half22float2(*reinterpret_cast<const __half2*>(&cl0[k]));
+            const float2 l23 = __half22float2(*reinterpret_cast<const __half2*>(&cl1[k]));
+            const float2 u01 = __half22float2(*reinterpret_cast<const __half2*>(&cu0[k]));
+            const float2 u23 = __half22float2(*reinterpret_cast<const __half2*>(&cu1[k]));
+            const float lv[4] = {l01.x * sl[0], l01.y * sl[1], l23.x * sl[2], l23.y * sl[3]};
+            const float uv[4] = {u01.x * su[0], u01.y * su[1], u23.x * su[2], u23.y * su[3]};
+            rope_key_frags<C>(cx, 4 * gq + k, lv, uv, rr, ch, ah, al);
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma16816(S[mu][nt], ah[0][0], ah[0][1], ah[0][2], ah[0][3], qg[kcp][nt][0], qg[kcp][nt][1]);
+            mma16816(S[mu][nt], al[0][0], al[0][1], al[0][2], al[0][3], qg[kcp][nt][0], qg[kcp][nt][1]);
+            mma16816(S[mu][nt], ah[1][0], ah[1][1], ah[1][2], ah[1][3], qg[kcp + KC / 2][nt][0],
+                     qg[kcp + KC / 2][nt][1]);
+            mma16816(S[mu][nt], al[1][0], al[1][1], al[1][2], al[1][3], qg[kcp + KC / 2][nt][0],
+                     qg[kcp + KC / 2][nt][1]);
+          }
+        }
+      }
+    } else if constexpr (TR::KCH) {
+      // per-channel K: block c = channel c over the group's 32 tokens; the
+      // channel scales multiply the query columns
+#pragma unroll
+      for (int kc = 0; kc < KC; ++kc) {
+        const int c = 32 * (kc >> 1) + 8 * tq + 2 * (kc & 1);
+        const uint8_t* b1p = ksm + c * TR::KBB;
+        const uint8_t* b2p = b1p + 4 * TR::KBB;
+        const uint8_t* b3p = b1p + TR::KBB;
+        const uint8_t* b4p = b1p + 5 * TR::KBB;
+        uint32_t k12[4], k34[4];
+        if constexpr (TR::KB == 4) {
+          dq4(__byte_perm(ld_u16(b1p + 2 + 2 * gq), ld_u16(b2p + 2 + 2 * gq), 0x5410), k12);
+          dq4(__byte_perm(ld_u16(b3p + 2 + 2 * gq), ld_u16(b4p + 2 + 2 * gq), 0x5410), k34);
+        } else {
+          const uint32_t x12 = __byte_perm((uint32_t)b1p[2 + gq], (uint32_t)b2p[2 + gq], 0x5410);
+          const uint32_t x34 = __byte_perm((uint32_t)b3p[2 + gq], (uint32_t)b4p[2 + gq], 0x5410);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            k12[k] = code_pair<2>(x12, k);
+            k34[k] = code_pair<2>(x34, k);
+          }
+        }
+        const uint32_t s12 = __byte_perm(ld_u16(b1p), ld_u16(b2p), 0x5410);
+        const uint32_t s34 = __byte_perm(ld_u16(b3p), ld_u16(b4p), 0x5410);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          // q' * scale as fp16: hi = rn(q' s) on even columns, the exact
+          // remainder fma(q', s, -hi) on odd columns (lo_mask all ones)
+          const uint2 qv = qh[(kc * NT + nt) * 32 + lane];
+          const uint32_t bq0 = hfma2u(qv.x, s12, (hmul2u(qv.x, s12) ^ 0x80008000u) & lo_mask);
+          const uint32_t bq1 = hfma2u(qv.y, s34, (hmul2u(qv.y, s34) ^ 0x80008000u) & lo_mask);
+#pragma unroll
+          for (int mu = 0; mu < 2; ++mu)
+            mma16816(S[mu][nt], k12[2 * mu], k12[2 * mu + 1], k34[2 * mu], k34[2 * mu + 1], bq0, bq1);
+        }
+      }
+    } else {
+      // per-token K: each K block's scale multiplies its partial scores
+#pragma unroll
+      for (int kb = 0; kb < D / TR::KG; ++kb) {
+        float acc[2][NT][4];
+#pragma unroll
+        for (int mu = 0; mu < 2; ++mu)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) acc[mu][nt][0] = acc[mu][nt][1] = acc[mu][nt][2] = acc[mu][nt][3] = 0.f;
+#pragma unroll
+        for (int ss = 0; ss < TR::KSPB; ++ss) {
+          const int s = kb * TR::KSPB + ss;
+#pragma unroll
+          for (int mu = 0; mu < 2; ++mu) {
+            const int ra = 4 * gq + 2 * mu;
+            uint32_t wa[4], wb[4];
+            k_token_pairs<TR>(ksm + ra * TR::KROW + kb * TR::KBB + 2 + ss * TR::KSPAN, tq, wa);
+            k_token_pairs<TR>(ksm + (ra + 1) * TR::KROW + kb * TR::KBB + 2 + ss * TR::KSPAN, tq, wb);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const uint2 q0 = qb[((2 * s) * NT + nt) * 32 + lane];
+              const uint2 q1 = qb[((2 * s + 1) * NT + nt) * 32 + lane];
+              mma16816(acc[mu][nt], wa[0], wb[0], wa[1], wb[1], q0.x, q0.y);
+              mma16816(acc[mu][nt], wa[2], wb[2], wa[3], wb[3], q1.x, q1.y);
+            }
+          }
+        }
+#pragma unroll
+        for (int mu = 0; mu < 2; ++mu) {
+          const float sa = block_scale(ksm + (4 * gq + 2 * mu) * TR::KROW + kb * TR::KBB);
+          const float sb = block_scale(ksm + (4 * gq + 2 * mu + 1) * TR::KROW + kb * TR::KBB);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            S[mu][nt][0] += acc[mu][nt][0] * sa;
+            S[mu][nt][1] += acc[mu][nt][1] * sa;
+            S[mu][nt][2] += acc[mu][nt][2] * sb;
+            S[mu][nt][3] += acc[mu][nt][3] * sb;
+          }
+        }
+      }
+    }
+  }
+
+template <class C>
+__global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(DecodeArgs a) {
+  constexpr int D = C::D, NT = C::NT, KC = C::KC;
   extern __shared__ __align__(16) uint8_t smem[];
-  float4* qsm = reinterpret_cast<float4*>(smem);  // [KC][NT][32 lanes]
+  uint2* qb = reinterpret_cast<uint2*>(smem);  // [KC][NT][32 lanes]: this lane's B fragment (b0, b1)
+  uint2* qh = qb + KC * NT * 32;               // [KC][NT][32 lanes]: query half pairs (per-channel K)
+  float4* qr = reinterpret_cast<float4*>(qh + KC * NT * 32);  // [KC][NT][32 lanes]: fp32 query (RoPE)
   uint8_t* stage_base = smem + C::QSM;
+  __shared__ float qmax_s[kWarps];
   __shared__ uint32_t bad_page;
   __shared__ int is_last;
 
@@ -268,14 +581,17 @@ __global__ void __launch_bounds__(kThreadsMma) decode_mma_kernel(DecodeArgs a) {
     T = 0;
   }
   const int qe = q_end_of(lo, T);
-  const int n_m = (qe + kTile - 1) / kTile;
+  const int ce = C::HAS_COLD ? c_end_of(lo, T) : 0;
+  const int n_c = ce / kTile;
+  const int n_m = (qe - ce + kTile - 1) / kTile;
   const int n_w = (T - qe + kTile - 1) / kTile;
-  const int ntiles = n_m + n_w;
+  const int ntiles = n_c + n_m + n_w;
   const int tb = (int)((int64_t)split * ntiles / a.splits);
   const int te = (int)((int64_t)(split + 1) * ntiles / a.splits);
   const int64_t qrow = ((int64_t)li * lo.B + seq) * lo.Hq + (int64_t)h * g;
 
-  // ---- query: fp32, rotated when K is stored rotated; per-lane values -------
+  // ---- query: fp32, rotated when K is stored rotated; per-lane fragments ----
+  float qexp = 1.f;
   {
     float* qf = reinterpret_cast<float*>(stage_base);  // [g][D] scratch
     for (int e = tid; e < g * D; e += kThreadsMma) qf[e] = in_to_f32(a.q[qrow * D + e], lo.dtype);
@@ -293,25 +609,57 @@ __global__ void __launch_bounds__(kThreadsMma) decode_mma_kernel(DecodeArgs a) {
       }
       __syncthreads();
     }
-    for (int e = tid; e < C::KC * NT * 32; e += kThreadsMma) {
+    // power-of-two normalization: |q'| = |q| 2^-e <= 1, so products with fp16
+    // scales cannot overflow fp16 (the factor 2^e returns with the score scale)
+    float m = 0.f;
+    for (int e = tid; e < g * D; e += kThreadsMma) m = fmaxf(m, fabsf(qf[e]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) qmax_s[warp] = m;
+    __syncthreads();
+    m = fmaxf(fmaxf(qmax_s[0], qmax_s[1]), fmaxf(qmax_s[2], qmax_s[3]));
+    int ex = 0;
+    if (m > 0.f) frexpf(m, &ex);
+    const float qnorm = ldexpf(1.f, -ex);
+    qexp = ldexpf(1.f, ex);
+    for (int e = tid; e < KC * NT * 32; e += kThreadsMma) {
       const int ln = e & 31, nt = (e >> 5) % NT, kc = (e >> 5) / NT;
       const int c = 32 * (kc >> 1) + 8 * (ln & 3) + 2 * (kc & 1);
       const int hh = 4 * nt + ((ln >> 2) >> 1);
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      const bool lo = ((ln >> 2) & 1) != 0;
+      float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
       if (hh < g) {
-        const float* qr = qf + hh * D;
-        v = make_float4(qr[c], qr[c + 4], qr[c + 1], qr[c + 5]);
+        const float* q = qf + hh * D;
+        v0 = q[c] * qnorm;
+        v1 = q[c + 4] * qnorm;
+        v2 = q[c + 1] * qnorm;
+        v3 = q[c + 5] * qnorm;
       }
-      qsm[e] = v;
+      qb[e] = make_uint2(pack_h2(split_part(v0, lo), split_part(v1, lo)),
+                         pack_h2(split_part(v2, lo), split_part(v3, lo)));
+      qh[e] = make_uint2(pack_h2(v0, v1), pack_h2(v2, v3));
+      if constexpr (C::ROPE) qr[e] = make_float4(v0, v1, v2, v3);
     }
     __syncthreads();
   }
   const bool lo_part = (gq & 1) != 0;
-  const float qscale = kLog2eF / sqrtf((float)D);
+  const uint32_t lo_mask = lo_part ? 0xFFFFFFFFu : 0u;
+  const float qscale = kLog2eF / sqrtf((float)D) * qexp;
+  Ctx<C> cx;
+  cx.gq = gq;
+  cx.tq = tq;
+  cx.lane = lane;
+  cx.lo_part = lo_part;
+  cx.lo_mask = lo_mask;
+  cx.qb = qb;
+  cx.qh = qh;
+  cx.qr = qr;
+  cx.rope_base = a.rope;
+  cx.rope_off = a.rope + (int64_t)a.rope_base_rows * (D / 2);
 
   WarpState<C> ws;
 #pragma unroll
-  for (int i = 0; i < C::KC; ++i)
+  for (int i = 0; i < KC; ++i)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -323,23 +671,27 @@ __global__ void __launch_bounds__(kThreadsMma) decode_mma_kernel(DecodeArgs a) {
   }
   uint8_t* wst = stage_base + warp * kStages * C::STAGE;
 
-  // query fragment (b0, b1) of k-chunk kc, n-tile nt, unscaled (hi or lo part)
-  auto qfrag = [&](int kc, int nt, uint32_t& b0, uint32_t& b1) {
-    const float4 v = qsm[(kc * NT + nt) * 32 + lane];
-    b0 = pack_h2(split_part(v.x, lo_part), split_part(v.y, lo_part));
-    b1 = pack_h2(split_part(v.z, lo_part), split_part(v.w, lo_part));
-  };
-
-  // copies of main-tier tile `tile` into stage `st` (nothing for window tiles)
+  // copies of packed tile `tile` (cold or hot/only tier) into stage `st`
   auto issue = [&](int tile, int st) {
-    if (tile >= te || tile >= n_m) return;
-    const int t0 = tile * kTile;
+    if (tile >= te || tile >= n_c + n_m) return;
     uint8_t* ks = wst + st * C::STAGE;
     uint8_t* vs = ks + C::VOFF;
+    if constexpr (C::HAS_COLD) {
+      if (tile < n_c) {
+        const int t0 = tile * kTile;
+        const uint8_t* kg = cold_row(lo, a.cp, 0, layer, seq, h, t0);
+        const uint8_t* vg = cold_row(lo, a.cp, 1, layer, seq, h, t0);
+        for (int c = lane; c < C::COLD::KSTAGE / 16; c += 32) cp_async16(ks + 16 * c, kg + 16 * c);
+        for (int c = lane; c < C::COLD::VSTAGE / 16; c += 32) cp_async16(vs + 16 * c, vg + 16 * c);
+        return;
+      }
+    }
+    using HT = typename C::HOT;
+    const int t0 = ce + (tile - n_c) * kTile;
     bool bad = false;
     if (lo.paged) {
       const int np = (qe - t0 > lo.pt) ? kTile / lo.pt : 1;
-      const int kb = lo.pt * C::KROW, vb = lo.pt * C::VROW;
+      const int kb = lo.pt * HT::KROW, vb = lo.pt * HT::VROW;
       for (int pg = 0; pg < np; ++pg) {
         const uint8_t* kg = main_row(lo, a.cp, 0, layer, seq, h, t0 + pg * lo.pt, &bad);
         const uint8_t* vg = main_row(lo, a.cp, 1, layer, seq, h, t0 + pg * lo.pt, &bad);
@@ -354,8 +706,8 @@ __global__ void __launch_bounds__(kThreadsMma) decode_mma_kernel(DecodeArgs a) {
     }
     const uint8_t* kg = main_row(lo, a.cp, 0, layer, seq, h, t0, &bad);
     const uint8_t* vg = main_row(lo, a.cp, 1, layer, seq, h, t0, &bad);
-    for (int c = lane; c < C::KSTAGE / 16; c += 32) cp_async16(ks + 16 * c, kg + 16 * c);
-    for (int c = lane; c < C::VSTAGE / 16; c += 32) cp_async16(vs + 16 * c, vg + 16 * c);
+    for (int c = lane; c < HT::KSTAGE / 16; c += 32) cp_async16(ks + 16 * c, kg + 16 * c);
+    for (int c = lane; c < HT::VSTAGE / 16; c += 32) cp_async16(vs + 16 * c, vg + 16 * c);
   };
 
   // ---- per-warp pipeline over this CTA's groups --------------------------------
@@ -380,140 +732,106 @@ __global__ void __launch_bounds__(kThreadsMma) decode_mma_kernel(DecodeArgs a) {
       for (int nt = 0; nt < NT; ++nt) S[mu][nt][0] = S[mu][nt][1] = S[mu][nt][2] = S[mu][nt][3] = 0.f;
     float p[NT][4];
 
-    if (tile < n_m) {
+    if (tile < n_c + n_m) {
       // ---------------- packed group from shared memory ----------------
-      const int t0 = tile * kTile;
-      const int n_valid = min(kTile, qe - t0);
       const uint8_t* ksm = wst + (it % kStages) * C::STAGE;
       const uint8_t* vsm = ksm + C::VOFF;
-      if constexpr (C::KCH) {
-        // per-channel K: block c = channel c over the group's 32 tokens; the
-        // channel scales multiply the query columns
-#pragma unroll
-        for (int kc = 0; kc < C::KC; ++kc) {
-          const int c = 32 * (kc >> 1) + 8 * tq + 2 * (kc & 1);
-          const uint8_t* b1p = ksm + c * C::KBB;
-          const uint8_t* b2p = b1p + 4 * C::KBB;
-          const uint8_t* b3p = b1p + C::KBB;
-          const uint8_t* b4p = b1p + 5 * C::KBB;
-          const uint32_t x12 = ld_u16(b1p + 2 + 2 * gq) | (ld_u16(b2p + 2 + 2 * gq) << 16);
-          const uint32_t x34 = ld_u16(b3p + 2 + 2 * gq) | (ld_u16(b4p + 2 + 2 * gq) << 16);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const float4 v = qsm[(kc * NT + nt) * 32 + lane];
-            const uint32_t bq0 = pack_h2(split_part(v.x * block_scale(b1p), lo_part),
-                                         split_part(v.y * block_scale(b2p), lo_part));
-            const uint32_t bq1 = pack_h2(split_part(v.z * block_scale(b3p), lo_part),
-                                         split_part(v.w * block_scale(b4p), lo_part));
-#pragma unroll
-            for (int mu = 0; mu < 2; ++mu)
-              mma16816(S[mu][nt], code_pair<4>(x12, 2 * mu), code_pair<4>(x12, 2 * mu + 1),
-                       code_pair<4>(x34, 2 * mu), code_pair<4>(x34, 2 * mu + 1), bq0, bq1);
-          }
+      bool cold = false;
+      if constexpr (C::HAS_COLD) cold = tile < n_c;
+      if (cold) {
+        if constexpr (C::HAS_COLD) {
+          const int t0 = tile * kTile;
+          scores_packed<C, typename C::COLD>(cx, ksm, t0, S);
+          online_softmax<C>(ws, S, kTile, gq, qscale, p);
+          pv_packed<C, typename C::COLD>(cx, ws, vsm, kTile, p);
         }
       } else {
-        // per-token K: each K block's scale multiplies its partial scores
-#pragma unroll
-        for (int kb = 0; kb < D / C::KG; ++kb) {
-          float acc[2][NT][4];
-#pragma unroll
-          for (int mu = 0; mu < 2; ++mu)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) acc[mu][nt][0] = acc[mu][nt][1] = acc[mu][nt][2] = acc[mu][nt][3] = 0.f;
-#pragma unroll
-          for (int ss = 0; ss < C::KSPB; ++ss) {
-            const int s = kb * C::KSPB + ss;
-#pragma unroll
-            for (int mu = 0; mu < 2; ++mu) {
-              const int ra = 4 * gq + 2 * mu;
-              uint32_t wa[4], wb[4];
-              k_token_pairs<C>(ksm + ra * C::KROW + kb * C::KBB + 2 + ss * C::KSPAN, tq, wa);
-              k_token_pairs<C>(ksm + (ra + 1) * C::KROW + kb * C::KBB + 2 + ss * C::KSPAN, tq, wb);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                uint32_t b0, b1;
-                qfrag(2 * s, nt, b0, b1);
-                mma16816(acc[mu][nt], wa[0], wb[0], wa[1], wb[1], b0, b1);
-                qfrag(2 * s + 1, nt, b0, b1);
-                mma16816(acc[mu][nt], wa[2], wb[2], wa[3], wb[3], b0, b1);
-              }
-            }
-          }
-#pragma unroll
-          for (int mu = 0; mu < 2; ++mu) {
-            const float sa = block_scale(ksm + (4 * gq + 2 * mu) * C::KROW + kb * C::KBB);
-            const float sb = block_scale(ksm + (4 * gq + 2 * mu + 1) * C::KROW + kb * C::KBB);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              S[mu][nt][0] += acc[mu][nt][0] * sa;
-              S[mu][nt][1] += acc[mu][nt][1] * sa;
-              S[mu][nt][2] += acc[mu][nt][2] * sb;
-              S[mu][nt][3] += acc[mu][nt][3] * sb;
-            }
-          }
-        }
-      }
-      online_softmax<C>(ws, S, n_valid, gq, qscale, p);
-      // V: P^T per V block, O^T += V^T P^T
-#pragma unroll
-      for (int bv = 0; bv < D / C::VG; ++bv) {
-        uint32_t pb[2][NT][2];
-#pragma unroll
-        for (int mu = 0; mu < 2; ++mu) {
-          const int ra = 4 * gq + 2 * mu;
-          const float sva = block_scale(vsm + ra * C::VROW + bv * C::VBB);
-          const float svb = block_scale(vsm + (ra + 1) * C::VROW + bv * C::VBB);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const float pa = ra < n_valid ? p[nt][2 * mu] * sva : 0.f;
-            const float pbb = ra + 1 < n_valid ? p[nt][2 * mu + 1] * svb : 0.f;
-            p_fragments(pa, pbb, pb[mu][nt][0], pb[mu][nt][1]);
-          }
-        }
-#pragma unroll
-        for (int ss = 0; ss < C::VSPB; ++ss) {
-          const int s = bv * C::VSPB + ss;
-          const int off = bv * C::VBB + 2 + ss * C::VSPAN;
-#pragma unroll
-          for (int mu = 0; mu < 2; ++mu) {
-            const int T1 = 8 * tq + 2 * mu;
-            uint32_t x12[4], x34[4];
-            v_pair4<C>(vsm + T1 * C::VROW + off, vsm + (T1 + 4) * C::VROW + off, gq, x12);
-            v_pair4<C>(vsm + (T1 + 1) * C::VROW + off, vsm + (T1 + 5) * C::VROW + off, gq, x34);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              mma16816(ws.o[2 * s][nt], x12[0], x12[1], x34[0], x34[1], pb[mu][nt][0], pb[mu][nt][1]);
-              mma16816(ws.o[2 * s + 1][nt], x12[2], x12[3], x34[2], x34[3], pb[mu][nt][0], pb[mu][nt][1]);
-            }
-          }
-        }
+        const int t0 = ce + (tile - n_c) * kTile;
+        const int n_valid = min(kTile, qe - t0);
+        scores_packed<C, typename C::HOT>(cx, ksm, t0, S);
+        online_softmax<C>(ws, S, n_valid, gq, qscale, p);
+        pv_packed<C, typename C::HOT>(cx, ws, vsm, n_valid, p);
       }
     } else {
       // ---------------- 16-bit window group from global memory ----------------
-      const int t0 = qe + (tile - n_m) * kTile;
+      const int t0 = qe + (tile - n_c - n_m) * kTile;
       const int n_valid = min(kTile, T - t0);
+      if constexpr (C::ROPE) {
+        uint32_t qg[KC][NT][2];
+        rope_query<C>(cx, t0, qg);
 #pragma unroll
-      for (int mu = 0; mu < 2; ++mu) {
-        const int ra = 4 * gq + 2 * mu, rb = ra + 1;
-        const uint16_t* rowa = resid_row(lo, a.cp, 0, layer, seq, h, t0 + min(ra, n_valid - 1));
-        const uint16_t* rowb = resid_row(lo, a.cp, 0, layer, seq, h, t0 + min(rb, n_valid - 1));
+        for (int mu = 0; mu < 2; ++mu) {
 #pragma unroll
-        for (int s = 0; s < C::NS; ++s) {
-          uint4 va = make_uint4(0, 0, 0, 0), vb = va;
-          if (ra < n_valid) va = *reinterpret_cast<const uint4*>(rowa + 32 * s + 8 * tq);
-          if (rb < n_valid) vb = *reinterpret_cast<const uint4*>(rowb + 32 * s + 8 * tq);
-          // pairs (c, c+4), (c+1, c+5), (c+2, c+6), (c+3, c+7)
-          const uint32_t a0 = __byte_perm(va.x, va.z, 0x5410), a1 = __byte_perm(va.x, va.z, 0x7632);
-          const uint32_t a2 = __byte_perm(va.y, va.w, 0x5410), a3 = __byte_perm(va.y, va.w, 0x7632);
-          const uint32_t b0 = __byte_perm(vb.x, vb.z, 0x5410), b1 = __byte_perm(vb.x, vb.z, 0x7632);
-          const uint32_t b2 = __byte_perm(vb.y, vb.w, 0x5410), b3 = __byte_perm(vb.y, vb.w, 0x7632);
+          for (int s = 0; s < C::NS / 2; ++s) {
+            uint32_t ah[2][2][4], al[2][2][4];  // [b][lower/upper][a0..a3]
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            uint32_t q0, q1;
-            qfrag(2 * s, nt, q0, q1);
-            mma16816(S[mu][nt], a0, b0, a1, b1, q0, q1);
-            qfrag(2 * s + 1, nt, q0, q1);
-            mma16816(S[mu][nt], a2, b2, a3, b3, q0, q1);
+            for (int rr = 0; rr < 2; ++rr) {
+              const int r = 4 * gq + 2 * mu + rr;
+              const uint16_t* row = resid_row(lo, a.cp, 0, layer, seq, h, t0 + min(r, n_valid - 1));
+              uint4 wl = make_uint4(0, 0, 0, 0), wu = wl;
+              if (r < n_valid) {
+                wl = *reinterpret_cast<const uint4*>(row + 32 * s + 8 * tq);
+                wu = *reinterpret_cast<const uint4*>(row + 32 * s + D / 2 + 8 * tq);
+              }
+              const uint32_t lw[4] = {wl.x, wl.y, wl.z, wl.w}, uw[4] = {wu.x, wu.y, wu.z, wu.w};
+              float lf[8], uf[8];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&lw[e]));
+                const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&uw[e]));
+                lf[2 * e] = a2.x;
+                lf[2 * e + 1] = a2.y;
+                uf[2 * e] = b2.x;
+                uf[2 * e + 1] = b2.y;
+              }
+#pragma unroll
+              for (int b = 0; b < 2; ++b) {
+                // k-chunk 2s + b: channels c + {0, 4, 1, 5}, c = 32s + 8tq + 2b
+                const int c = 32 * s + 8 * tq + 2 * b;
+                const int ch[4] = {c, c + 4, c + 1, c + 5};
+                const float lv[4] = {lf[2 * b], lf[2 * b + 4], lf[2 * b + 1], lf[2 * b + 5]};
+                const float uv[4] = {uf[2 * b], uf[2 * b + 4], uf[2 * b + 1], uf[2 * b + 5]};
+                rope_key_frags<C>(cx, r, lv, uv, rr, ch, ah[b], al[b]);
+              }
+            }
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+              const int kc = 2 * s + b;
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                mma16816(S[mu][nt], ah[b][0][0], ah[b][0][1], ah[b][0][2], ah[b][0][3], qg[kc][nt][0], qg[kc][nt][1]);
+                mma16816(S[mu][nt], al[b][0][0], al[b][0][1], al[b][0][2], al[b][0][3], qg[kc][nt][0], qg[kc][nt][1]);
+                mma16816(S[mu][nt], ah[b][1][0], ah[b][1][1], ah[b][1][2], ah[b][1][3], qg[kc + KC / 2][nt][0],
+                         qg[kc + KC / 2][nt][1]);
+                mma16816(S[mu][nt], al[b][1][0], al[b][1][1], al[b][1][2], al[b][1][3], qg[kc + KC / 2][nt][0],
+                         qg[kc + KC / 2][nt][1]);
+              }
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int mu = 0; mu < 2; ++mu) {
+          const int ra = 4 * gq + 2 * mu, rb = ra + 1;
+          const uint16_t* rowa = resid_row(lo, a.cp, 0, layer, seq, h, t0 + min(ra, n_valid - 1));
+          const uint16_t* rowb = resid_row(lo, a.cp, 0, layer, seq, h, t0 + min(rb, n_valid - 1));
+#pragma unroll
+          for (int s = 0; s < C::NS; ++s) {
+            uint4 va = make_uint4(0, 0, 0, 0), vb = va;
+            if (ra < n_valid) va = *reinterpret_cast<const uint4*>(rowa + 32 * s + 8 * tq);
+            if (rb < n_valid) vb = *reinterpret_cast<const uint4*>(rowb + 32 * s + 8 * tq);
+            // pairs (c, c+4), (c+1, c+5), (c+2, c+6), (c+3, c+7)
+            const uint32_t a0 = __byte_perm(va.x, va.z, 0x5410), a1 = __byte_perm(va.x, va.z, 0x7632);
+            const uint32_t a2 = __byte_perm(va.y, va.w, 0x5410), a3 = __byte_perm(va.y, va.w, 0x7632);
+            const uint32_t b0 = __byte_perm(vb.x, vb.z, 0x5410), b1 = __byte_perm(vb.x, vb.z, 0x7632);
+            const uint32_t b2 = __byte_perm(vb.y, vb.w, 0x5410), b3 = __byte_perm(vb.y, vb.w, 0x7632);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const uint2 q0 = qb[((2 * s) * NT + nt) * 32 + lane];
+              const uint2 q1 = qb[((2 * s + 1) * NT + nt) * 32 + lane];
+              mma16816(S[mu][nt], a0, b0, a1, b1, q0.x, q0.y);
+              mma16816(S[mu][nt], a2, b2, a3, b3, q1.x, q1.y);
+            }
           }
         }
       }
@@ -675,27 +993,49 @@ bool fmt_is(const FmtInfo& f, int bits, int group, int axis) {
   return f.bits == bits && f.group == group && f.axis == axis;
 }
 
+template <int D, int KF, int KG, int VF, int VG>
+using T_ = Tier<D, KF, KG, VF, VG>;
+
 }  // namespace
 
 // Tensor-core path when the cache fits it, else the generic path.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   const Layout& lo = a.lo;
-  bool ok = !lo.tiered && !(lo.flags & KVQ_K_PRE_ROPE);
+  const int TOK = KVQ_AXIS_TOKEN, CH = KVQ_AXIS_CHANNEL;
+  const bool rope = (lo.flags & KVQ_K_PRE_ROPE) != 0;
+  bool ok = true;
   if (lo.ring) ok = ok && lo.dtype == KVQ_DT_F16 && !(lo.flags & (KVQ_ROTATE_K | KVQ_ROTATE_V));
   if (lo.paged) ok = ok && (lo.pt == 16 || lo.pt == 32);
-  if (ok) {
-    const FmtInfo &k = lo.kf, &v = lo.vf;
-    const int T = KVQ_AXIS_TOKEN, CH = KVQ_AXIS_CHANNEL;
-    if (lo.D == 128 && lo.g <= 4) {
-      if (fmt_is(k, 4, 32, CH) && fmt_is(v, 4, 32, T)) return launch_mma<Cfg<128, 1, KF_CH4, 32, VF_T4, 32>>(a, st);
-      if (fmt_is(k, 4, 128, T) && fmt_is(v, 4, 128, T)) return launch_mma<Cfg<128, 1, KF_T4, 128, VF_T4, 128>>(a, st);
-      if (fmt_is(k, 4, 32, T) && fmt_is(v, 4, 32, T)) return launch_mma<Cfg<128, 1, KF_T4, 32, VF_T4, 32>>(a, st);
-      if (fmt_is(k, 8, 32, T) && fmt_is(v, 8, 32, T)) return launch_mma<Cfg<128, 1, KF_T8, 32, VF_T8, 32>>(a, st);
+  if (!ok) return launch_decode_generic(a, st);
+  const FmtInfo &k = lo.kf, &v = lo.vf;
+  const bool kivi4 = fmt_is(k, 4, 32, CH) && fmt_is(v, 4, 32, TOK);
+  using KIVI4 = T_<128, KF_CH4, 32, VF_T4, 32>;
+  using KIVI2 = T_<128, KF_CH2, 32, VF_T2, 32>;
+  if (lo.D == 128 && lo.g <= 4 && kivi4) {
+    if (lo.tiered) {
+      if (fmt_is(lo.kc, 2, 32, CH) && fmt_is(lo.vc, 2, 32, TOK)) {
+        if (rope) return launch_mma<Cfg<128, 1, KIVI4, KIVI2, true, true>>(a, st);
+        return launch_mma<Cfg<128, 1, KIVI4, KIVI2, true, false>>(a, st);
+      }
+    } else {
+      if (rope) return launch_mma<Cfg<128, 1, KIVI4, KIVI4, false, true>>(a, st);
+      return launch_mma<Cfg<128, 1, KIVI4, KIVI4, false, false>>(a, st);
     }
-    if (lo.D == 256 && lo.g <= 8) {
-      if (fmt_is(k, 4, 128, T) && fmt_is(v, 4, 128, T)) return launch_mma<Cfg<256, 2, KF_T4, 128, VF_T4, 128>>(a, st);
-      if (fmt_is(k, 3, 128, T) && fmt_is(v, 3, 128, T)) return launch_mma<Cfg<256, 2, KF_T3, 128, VF_T3, 128>>(a, st);
-    }
+  }
+  if (lo.tiered || rope) return launch_decode_generic(a, st);
+  if (lo.D == 128 && lo.g <= 4) {
+    using A = T_<128, KF_T4, 128, VF_T4, 128>;
+    using B = T_<128, KF_T4, 32, VF_T4, 32>;
+    using Q8 = T_<128, KF_T8, 32, VF_T8, 32>;
+    if (fmt_is(k, 4, 128, TOK) && fmt_is(v, 4, 128, TOK)) return launch_mma<Cfg<128, 1, A, A, false, false>>(a, st);
+    if (fmt_is(k, 4, 32, TOK) && fmt_is(v, 4, 32, TOK)) return launch_mma<Cfg<128, 1, B, B, false, false>>(a, st);
+    if (fmt_is(k, 8, 32, TOK) && fmt_is(v, 8, 32, TOK)) return launch_mma<Cfg<128, 1, Q8, Q8, false, false>>(a, st);
+  }
+  if (lo.D == 256 && lo.g <= 8) {
+    using A4 = T_<256, KF_T4, 128, VF_T4, 128>;
+    using A3 = T_<256, KF_T3, 128, VF_T3, 128>;
+    if (fmt_is(k, 4, 128, TOK) && fmt_is(v, 4, 128, TOK)) return launch_mma<Cfg<256, 2, A4, A4, false, false>>(a, st);
+    if (fmt_is(k, 3, 128, TOK) && fmt_is(v, 3, 128, TOK)) return launch_mma<Cfg<256, 2, A3, A3, false, false>>(a, st);
   }
   return launch_decode_generic(a, st);
 }

@@ -177,16 +177,30 @@ int64_t fmt_bytes(const kvq_fmt& f, int64_t n_tokens, int D) {
   return (n_tokens / f.group) * D * bb;
 }
 
+// Token splits per (layer, sequence, kv head): the count whose grid fills
+// whole waves of resident CTAs best (152 SMs x 4 CTAs for D = 128, x 2 for
+// D = 256), with at least 8 tiles per split and no more growth once the grid
+// holds 8 waves.
 int splits_for(const kvq_config* c, int n_layers) {
-  int64_t units = (int64_t)n_layers * c->batch * c->H_kv;
-  int64_t tiles = (c->max_T + kTile - 1) / kTile + 2;
-  int64_t s = (kTargetCtas + units - 1) / units;
-  int64_t cap = tiles / 4;
+  const int64_t units = (int64_t)n_layers * c->batch * c->H_kv;
+  const int64_t tiles = (c->max_T + kTile - 1) / kTile + 2;
+  const int64_t resident = 152 * (c->D == 128 ? 4 : 2);
+  int64_t cap = tiles / 8;
   if (cap < 1) cap = 1;
-  if (s > cap) s = cap;
-  if (s > kMaxSplits) s = kMaxSplits;
-  if (s < 1) s = 1;
-  return (int)s;
+  if (cap > kMaxSplits) cap = kMaxSplits;
+  int best = 1;
+  double best_eff = -1.0;
+  for (int64_t sp = 1; sp <= cap; ++sp) {
+    const int64_t ctas = units * sp;
+    const int64_t waves = (ctas + resident - 1) / resident;
+    const double eff = (double)ctas / (double)(waves * resident);
+    if (eff > best_eff + 1e-9) {
+      best = (int)sp;
+      best_eff = eff;
+    }
+    if (ctas >= 8 * resident) break;
+  }
+  return best;
 }
 
 size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
@@ -212,8 +226,8 @@ WsLayout ws_layout(const kvq_config* c) {
       if (p > mp) mp = p;
     }
   }
-  // explicit split counts up to kMaxSplits for one layer are also allowed
-  int64_t one = (int64_t)c->batch * c->H_kv * kMaxSplits;
+  // explicit split counts up to 64 for one layer are also allowed
+  int64_t one = (int64_t)c->batch * c->H_kv * 64;
   if (one > mp) mp = one;
   w.max_partials = (int)mp;
   off = align_up(off + sizeof(float) * (size_t)mp * g * (c->D + 2));
