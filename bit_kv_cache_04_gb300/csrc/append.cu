@@ -22,6 +22,16 @@ namespace {
 
 constexpr int kAppendThreads = 128;
 
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
 struct SeqSpan {
   int T0, T1, n, off;
   bool ok;
@@ -195,14 +205,12 @@ __device__ __forceinline__ float4 f16x4_to_f32(uint2 w, int dtype) {
                      in_to_f32((uint16_t)(w.y & 0xFFFF), dtype), in_to_f32((uint16_t)(w.y >> 16), dtype));
 }
 
-// 32 values of a block (x[0], x[st], ..., x[31 st]) quantized with the scale
-// of block absolute maximum m (shared by the threads of a 128-value block);
-// the payload (32*B bits) goes to dst, the scale to blk when blk is given.
+// 32 values v[] of one block slice quantized with the scale of block absolute
+// maximum m (shared by the threads of a 128-value block); the payload
+// (32*B bits) goes to dst, the scale to blk when blk is given; dq (optional)
+// receives code * scale.
 template <int B>
-__device__ __forceinline__ void quant32(const float* x, int st, float m, uint8_t* blk, uint8_t* dst, float* dq) {
-  float v[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = x[j * st];
+__device__ __forceinline__ void quant32(const float (&v)[32], float m, uint8_t* blk, uint8_t* dst, float* dq) {
   const __half s16 = block_scale_of(m, (1 << (B - 1)) - 1);
   const float sf = __half2float(s16);
   const float rcp = sf == 0.f ? 0.f : __frcp_rn(sf);
@@ -218,35 +226,39 @@ __device__ __forceinline__ void quant32(const float* x, int st, float m, uint8_t
   }
 }
 
-__device__ __forceinline__ void quant32_bits(int bits, const float* x, int st, float m, uint8_t* blk, uint8_t* dst,
+__device__ __forceinline__ void quant32_bits(int bits, const float (&v)[32], float m, uint8_t* blk, uint8_t* dst,
                                              float* dq) {
   switch (bits) {
-    case 8: quant32<8>(x, st, m, blk, dst, dq); break;
-    case 4: quant32<4>(x, st, m, blk, dst, dq); break;
-    case 3: quant32<3>(x, st, m, blk, dst, dq); break;
-    default: quant32<2>(x, st, m, blk, dst, dq); break;
+    case 8: quant32<8>(v, m, blk, dst, dq); break;
+    case 4: quant32<4>(v, m, blk, dst, dq); break;
+    case 3: quant32<3>(v, m, blk, dst, dq); break;
+    default: quant32<2>(v, m, blk, dst, dq); break;
   }
 }
 
-__device__ __forceinline__ float amax32(const float* x, int st) {
+__device__ __forceinline__ float amax32(const float (&v)[32]) {
   float m = 0.f;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(x[j * st]));
+  for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(v[j]));
   return m;
 }
 
 // Phase B: quantize units [q_end(T0), q_end(T1)).  The chunk's K and V rows
-// are staged in shared memory as fp32 (each 128-chunk of a row rotated on the
-// way by the warp that loads it, when asked); then every thread quantizes 32
-// values: one channel over the group's tokens (per-channel blocks) or a
-// 32-value slice of a token row (per-token blocks; a 128-value block spans 4
-// neighbouring threads, which combine their absolute maxima).
-template <int NC>
-__global__ void __launch_bounds__(kAppendThreads) append_quantize_kernel(AppendArgs a) {
+// are copied to shared memory as raw 16-bit values (cp.async); rotated
+// formats then pass each row through the randomized Hadamard transform into an
+// fp32 tile (one warp per row).  Every thread then quantizes 32 values: one
+// channel over the group's tokens (per-channel blocks) or a 32-value slice of
+// a token row (per-token blocks; the 4 slices of a 128-value block are
+// neighbouring lanes that combine their absolute maxima).
+template <int NC, bool ROT>
+__global__ void __launch_bounds__(kAppendThreads, 4) append_quantize_kernel(AppendArgs a) {
   constexpr int D = 128 * NC;
-  constexpr int LDX = D + 4;  // 16-byte aligned rows, conflict-free column reads
+  constexpr int RH = D + 8;    // raw row stride in 16-bit values (16-byte multiple, offset banks)
+  constexpr int LDF = D + 1;   // fp32 rotated tile stride
   constexpr int SUB = D / 32;  // 32-value slices per row
-  extern __shared__ __align__(16) float xs[];  // [2][kTile][LDX]
+  extern __shared__ __align__(16) uint8_t sm[];
+  uint16_t* raw = reinterpret_cast<uint16_t*>(sm);                          // [2][kTile][RH]
+  float* fl = reinterpret_cast<float*>(sm + 2 * kTile * RH * sizeof(uint16_t));  // [2][kTile][LDF] (ROT)
   __shared__ uint32_t page_bad;
   const Layout& lo = a.lo;
   const int li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B, h = blockIdx.y;
@@ -262,73 +274,99 @@ __global__ void __launch_bounds__(kAppendThreads) append_quantize_kernel(AppendA
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   if (tid == 0) page_bad = 0;
 
-  // 1. stage the rows (one warp per row, lane l holds channels 128c+4l..+3)
-  {
-    uint2 raw[2][kTile / 4][NC];
+  // 1. raw rows -> shared memory
 #pragma unroll
-    for (int which = 0; which < 2; ++which)
-#pragma unroll
-      for (int r = 0; r < kTile / 4; ++r) {
-        const int j = warp + 4 * r;
-        if (j < n_tok) {
-          const int t = u0 + j;
-          const uint16_t* src = t < s.T0 ? resid_row(lo, a.cp, which, layer, seq, h, t) : input_row(a, which, li, s, h, t);
-#pragma unroll
-          for (int c = 0; c < NC; ++c) raw[which][r][c] = *reinterpret_cast<const uint2*>(src + 128 * c + 4 * lane);
-        }
-      }
+  for (int which = 0; which < 2; ++which) {
+    for (int e = tid; e < n_tok * (D / 8); e += blockDim.x) {
+      const int j = e / (D / 8), c8 = e % (D / 8), t = u0 + j;
+      const uint16_t* src = t < s.T0 ? resid_row(lo, a.cp, which, layer, seq, h, t) : input_row(a, which, li, s, h, t);
+      cp_async16(raw + (which * kTile + j) * RH + 8 * c8, src + 8 * c8);
+    }
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  bool rot[2] = {(lo.flags & KVQ_ROTATE_K) != 0, (lo.flags & KVQ_ROTATE_V) != 0};
+  if constexpr (ROT) {
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
-      const bool rotate = (lo.flags & (which ? KVQ_ROTATE_V : KVQ_ROTATE_K)) != 0;
-      float* tile = xs + which * kTile * LDX;
-#pragma unroll
-      for (int r = 0; r < kTile / 4; ++r) {
-        const int j = warp + 4 * r;
-        if (j >= n_tok) break;
+      if (!rot[which]) continue;
+      for (int j = warp; j < n_tok; j += kAppendThreads / 32) {
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-          const float4 x = f16x4_to_f32(raw[which][r][c], lo.dtype);
+          const uint2 w = *reinterpret_cast<const uint2*>(raw + (which * kTile + j) * RH + 128 * c + 4 * lane);
+          const float4 x = f16x4_to_f32(w, lo.dtype);
           float v[4] = {x.x, x.y, x.z, x.w};
-          if (rotate) warp_rotate128(v, lo.d1, lo.d2);
-          *reinterpret_cast<float4*>(tile + j * LDX + 128 * c + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+          warp_rotate128(v, lo.d1, lo.d2);
+          float* dst = fl + (which * kTile + j) * LDF + 128 * c + 4 * lane;
+          dst[0] = v[0];
+          dst[1] = v[1];
+          dst[2] = v[2];
+          dst[3] = v[3];
         }
       }
     }
+    __syncthreads();
   }
-  __syncthreads();
 
   // 2. quantize
 #pragma unroll
   for (int which = 0; which < 2; ++which) {
     const FmtInfo& f = fmt_main(lo, which);
     const FmtInfo& fc = fmt_cold(lo, which);
-    const float* tile = xs + which * kTile * LDX;
+    const uint16_t* rt = raw + which * kTile * RH;
     if (f.axis == KVQ_AXIS_CHANNEL) {
       // one group of 32 tokens; thread = channel
       for (int c = tid; c < D; c += blockDim.x) {
-        const float* x = tile + c;
-        const float m = amax32(x, LDX);
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = in_to_f32(rt[j * RH + c], lo.dtype);
+        const float m = amax32(v);
         if (to_cold) {
           float dq[32];
-          quant32_bits(f.bits, x, LDX, m, nullptr, nullptr, dq);
+          quant32_bits(f.bits, v, m, nullptr, nullptr, dq);
           uint8_t* blk = cold_row(lo, a.cp, which, layer, seq, h, u0) + (int64_t)c * fc.bb;
-          quant32_bits(fc.bits, dq, 1, amax32(dq, 1), blk, blk + 2, nullptr);
+          quant32_bits(fc.bits, dq, amax32(dq), blk, blk + 2, nullptr);
         } else {
           bool bad = false;
           uint8_t* blk = main_row(lo, a.cp, which, layer, seq, h, u0, &bad) + (int64_t)c * f.bb;
-          quant32_bits(f.bits, x, LDX, m, blk, blk + 2, nullptr);
+          quant32_bits(f.bits, v, m, blk, blk + 2, nullptr);
         }
       }
       continue;
     }
-    // per-token: thread = (row, 32-value slice); every lane runs the loop so
-    // that the 4-lane amax exchange of 128-value blocks stays warp-uniform
-    const int spb = f.group / 32;  // slices per block
+    // per-token: thread = (row, 32-value slice).  32-value blocks: lane = row
+    // (conflict-free reads); 128-value blocks: the 4 slices of a block are
+    // neighbouring lanes.  Every lane runs the loop so that the exchange of
+    // 128-value block maxima stays warp-uniform.
+    const int spb = f.group / 32;
     for (int u = tid; u < kTile * SUB; u += blockDim.x) {
-      const int j = u / SUB, sl = u % SUB;
+      const int j = spb == 1 ? (u % kTile) : (u / SUB);
+      const int sl = spb == 1 ? (u / kTile) : (u % SUB);
       const bool valid = j < n_tok;
-      const float* x = tile + j * LDX + 32 * sl;
-      float m = valid ? amax32(x, 1) : 0.f;
+      float v[32];
+      if (ROT && rot[which]) {
+        const float* x = fl + (which * kTile + j) * LDF + 32 * sl;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = valid ? x[e] : 0.f;
+      } else {
+        const uint4* x = reinterpret_cast<const uint4*>(rt + j * RH + 32 * sl);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 w = valid ? x[k] : make_uint4(0, 0, 0, 0);
+          const float4 a0 = f16x4_to_f32(make_uint2(w.x, w.y), lo.dtype);
+          const float4 a1 = f16x4_to_f32(make_uint2(w.z, w.w), lo.dtype);
+          v[8 * k + 0] = a0.x;
+          v[8 * k + 1] = a0.y;
+          v[8 * k + 2] = a0.z;
+          v[8 * k + 3] = a0.w;
+          v[8 * k + 4] = a1.x;
+          v[8 * k + 5] = a1.y;
+          v[8 * k + 6] = a1.z;
+          v[8 * k + 7] = a1.w;
+        }
+      }
+      float m = amax32(v);
       if (spb == 4) {
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
@@ -337,17 +375,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_quantize_kernel(AppendA
       const int t = u0 + j;
       const int b = sl / spb, within = sl % spb;  // block, slice within the block
       if (to_cold) {
+        // tiers keep the hot group size; per-token tiers use 32-value blocks
         float dq[32];
-        quant32_bits(f.bits, x, 1, m, nullptr, nullptr, dq);
-        // the cold format keeps the hot group size: one 32-slice block when G = 32
-        uint8_t* row = cold_row(lo, a.cp, which, layer, seq, h, t);
-        uint8_t* blk = row + b * fc.bb;
-        float mc = amax32(dq, 1);
-        if (spb == 4) {
-          mc = fmaxf(mc, __shfl_xor_sync(__activemask(), mc, 1));
-          mc = fmaxf(mc, __shfl_xor_sync(__activemask(), mc, 2));
-        }
-        quant32_bits(fc.bits, dq, 1, mc, within == 0 ? blk : nullptr, blk + 2 + within * 4 * fc.bits, nullptr);
+        quant32_bits(f.bits, v, m, nullptr, nullptr, dq);
+        uint8_t* blk = cold_row(lo, a.cp, which, layer, seq, h, t) + b * fc.bb;
+        quant32_bits(fc.bits, dq, amax32(dq), blk, blk + 2, nullptr);
       } else {
         bool bad = false;
         uint8_t* row = main_row(lo, a.cp, which, layer, seq, h, t, &bad);
@@ -356,7 +388,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_quantize_kernel(AppendA
           continue;
         }
         uint8_t* blk = row + b * f.bb;
-        quant32_bits(f.bits, x, 1, m, within == 0 ? blk : nullptr, blk + 2 + within * 4 * f.bits, nullptr);
+        quant32_bits(f.bits, v, m, within == 0 ? blk : nullptr, blk + 2 + within * 4 * f.bits, nullptr);
       }
     }
   }
@@ -440,26 +472,28 @@ __global__ void commit_lengths_kernel(const int32_t* cu_new, int32_t* seq_lens, 
 
 }  // namespace
 
-template <int NC>
+template <int NC, bool ROT>
 cudaError_t launch_append_nc(const AppendArgs& a, cudaStream_t st) {
   const Layout& lo = a.lo;
   const int chunks = (a.max_new + kTile - 1) / kTile + 2;
   dim3 grid(chunks, lo.H, a.n_layers * lo.B);
-  const size_t smem = sizeof(float) * 2 * kTile * (lo.D + 4);
+  const size_t smem = 2 * kTile * (lo.D + 8) * sizeof(uint16_t) + (ROT ? 2 * kTile * (lo.D + 1) * sizeof(float) : 0);
   static bool attr_done = false;
   if (!attr_done) {
-    cudaFuncSetAttribute(append_quantize_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 80 * 1024);
+    cudaFuncSetAttribute(append_quantize_kernel<NC, ROT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
     attr_done = true;
   }
   if (lo.tiered) append_requant_kernel<NC><<<grid, kAppendThreads, 0, st>>>(a);
-  append_quantize_kernel<NC><<<grid, kAppendThreads, smem, st>>>(a);
+  append_quantize_kernel<NC, ROT><<<grid, kAppendThreads, smem, st>>>(a);
   if (lo.ring) append_window_kernel<<<grid, kAppendThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
   if (a.max_new == 0) return cudaSuccess;
-  return a.lo.D == 128 ? launch_append_nc<1>(a, st) : launch_append_nc<2>(a, st);
+  const bool rot = (a.lo.flags & (KVQ_ROTATE_K | KVQ_ROTATE_V)) != 0;
+  if (a.lo.D == 128) return rot ? launch_append_nc<1, true>(a, st) : launch_append_nc<1, false>(a, st);
+  return rot ? launch_append_nc<2, true>(a, st) : launch_append_nc<2, false>(a, st);
 }
 
 cudaError_t launch_commit_lengths(const int32_t* cu_new, int32_t* seq_lens, int batch, cudaStream_t st) {

@@ -307,58 +307,57 @@ struct Ctx {
   const uint2* qh;        // [KC][NT][32]: query half pairs
   const float4* qr;       // [KC][NT][32]: fp32 query (RoPE)
   const float2* rope_base;
-  const float2* rope_off;
+  const float4* rope_frag;  // [KC/2][4 tokens k][2 pairs][32 lanes]: R(j) of this lane's channels
 };
 
-// B fragments of the query turned by -t0 (pre-RoPE keys): lower channel c
-// and its partner c + D/2 sit in k-chunks kcp and kcp + KC/2.
+// B fragments of the query turned by -t0 (pre-RoPE keys) for the k-chunk
+// pair (kcp, kcp + KC/2): lower channel c and its partner c + D/2.
 template <class C>
-__device__ __forceinline__ void rope_query(const Ctx<C>& cx, int t0, uint32_t (&qg)[C::KC][C::NT][2]) {
-  constexpr int D = C::D, NT = C::NT, KC = C::KC;
-  const float2* base = cx.rope_base + (int64_t)(t0 / kTile) * (D / 2);
+__device__ __forceinline__ void rope_query_pair(const Ctx<C>& cx, const float2* base, int kcp,
+                                                uint32_t (&ql)[C::NT][2], uint32_t (&qu)[C::NT][2]) {
+  constexpr int NT = C::NT, KC = C::KC;
+  const int c = 32 * (kcp >> 1) + 8 * cx.tq + 2 * (kcp & 1);
+  const float2 f0 = __ldg(base + c), f1 = __ldg(base + c + 4), f2 = __ldg(base + c + 1), f3 = __ldg(base + c + 5);
 #pragma unroll
-  for (int kcp = 0; kcp < KC / 2; ++kcp) {
-    const int c = 32 * (kcp >> 1) + 8 * cx.tq + 2 * (kcp & 1);
-    const float2 f0 = __ldg(base + c), f1 = __ldg(base + c + 4), f2 = __ldg(base + c + 1), f3 = __ldg(base + c + 5);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const float4 l = cx.qr[(kcp * NT + nt) * 32 + cx.lane], u = cx.qr[((kcp + KC / 2) * NT + nt) * 32 + cx.lane];
-      const float l0 = l.x * f0.x + u.x * f0.y, u0 = u.x * f0.x - l.x * f0.y;
-      const float l1 = l.y * f1.x + u.y * f1.y, u1 = u.y * f1.x - l.y * f1.y;
-      const float l2 = l.z * f2.x + u.z * f2.y, u2 = u.z * f2.x - l.z * f2.y;
-      const float l3 = l.w * f3.x + u.w * f3.y, u3 = u.w * f3.x - l.w * f3.y;
-      qg[kcp][nt][0] = pack_h2(split_part(l0, cx.lo_part), split_part(l1, cx.lo_part));
-      qg[kcp][nt][1] = pack_h2(split_part(l2, cx.lo_part), split_part(l3, cx.lo_part));
-      qg[kcp + KC / 2][nt][0] = pack_h2(split_part(u0, cx.lo_part), split_part(u1, cx.lo_part));
-      qg[kcp + KC / 2][nt][1] = pack_h2(split_part(u2, cx.lo_part), split_part(u3, cx.lo_part));
-    }
+  for (int nt = 0; nt < NT; ++nt) {
+    const float4 l = cx.qr[(kcp * NT + nt) * 32 + cx.lane], u = cx.qr[((kcp + KC / 2) * NT + nt) * 32 + cx.lane];
+    const float l0 = l.x * f0.x + u.x * f0.y, u0 = u.x * f0.x - l.x * f0.y;
+    const float l1 = l.y * f1.x + u.y * f1.y, u1 = u.y * f1.x - l.y * f1.y;
+    const float l2 = l.z * f2.x + u.z * f2.y, u2 = u.z * f2.x - l.z * f2.y;
+    const float l3 = l.w * f3.x + u.w * f3.y, u3 = u.w * f3.x - l.w * f3.y;
+    ql[nt][0] = pack_h2(split_part(l0, cx.lo_part), split_part(l1, cx.lo_part));
+    ql[nt][1] = pack_h2(split_part(l2, cx.lo_part), split_part(l3, cx.lo_part));
+    qu[nt][0] = pack_h2(split_part(u0, cx.lo_part), split_part(u1, cx.lo_part));
+    qu[nt][1] = pack_h2(split_part(u2, cx.lo_part), split_part(u3, cx.lo_part));
   }
 }
 
 // fp32 key values of lower channels ch[0..3] (lv) and their partners (uv)
-// at token offset j of the group, turned by R(j), as hi/lo A fragments (row
-// rr of the A tile; [0] lower k-chunk, [1] partner k-chunk).
-template <class C>
-__device__ __forceinline__ void rope_key_frags(const Ctx<C>& cx, int j, const float (&lv)[4], const float (&uv)[4],
-                                               int rr, const int (&ch)[4], uint32_t (&ah)[2][4],
-                                               uint32_t (&al)[2][4]) {
+// of token k of the lane's four (4gq + k), turned by R(4gq + k), as hi/lo A
+// fragments (row rr of the A tile; [0] lower k-chunk, [1] partner k-chunk).
+// cs: (cos, sin) of channels ch[0], ch[1] and ch[2], ch[3].
+__device__ __forceinline__ void rope_key_frags(const float4 (&cs)[2], const float (&lv)[4], const float (&uv)[4],
+                                               int rr, uint32_t (&ah)[2][4], uint32_t (&al)[2][4]) {
+  const float c[4] = {cs[0].x, cs[0].z, cs[1].x, cs[1].z};
+  const float sn[4] = {cs[0].y, cs[0].w, cs[1].y, cs[1].w};
   float nl[4], nu[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const float2 cs = __ldg(cx.rope_off + j * (C::D / 2) + ch[q]);
-    nl[q] = lv[q] * cs.x - uv[q] * cs.y;
-    nu[q] = lv[q] * cs.y + uv[q] * cs.x;
+    nl[q] = lv[q] * c[q] - uv[q] * sn[q];
+    nu[q] = lv[q] * sn[q] + uv[q] * c[q];
   }
-  const float hl0 = rn16(nl[0]), hl1 = rn16(nl[1]), hl2 = rn16(nl[2]), hl3 = rn16(nl[3]);
-  const float hu0 = rn16(nu[0]), hu1 = rn16(nu[1]), hu2 = rn16(nu[2]), hu3 = rn16(nu[3]);
-  ah[0][rr] = pack_h2(hl0, hl1);
-  ah[0][2 + rr] = pack_h2(hl2, hl3);
-  al[0][rr] = pack_h2(nl[0] - hl0, nl[1] - hl1);
-  al[0][2 + rr] = pack_h2(nl[2] - hl2, nl[3] - hl3);
-  ah[1][rr] = pack_h2(hu0, hu1);
-  ah[1][2 + rr] = pack_h2(hu2, hu3);
-  al[1][rr] = pack_h2(nu[0] - hu0, nu[1] - hu1);
-  al[1][2 + rr] = pack_h2(nu[2] - hu2, nu[3] - hu3);
+  const __half2 hl01 = __floats2half2_rn(nl[0], nl[1]), hl23 = __floats2half2_rn(nl[2], nl[3]);
+  const __half2 hu01 = __floats2half2_rn(nu[0], nu[1]), hu23 = __floats2half2_rn(nu[2], nu[3]);
+  const float2 fl01 = __half22float2(hl01), fl23 = __half22float2(hl23);
+  const float2 fu01 = __half22float2(hu01), fu23 = __half22float2(hu23);
+  ah[0][rr] = *reinterpret_cast<const uint32_t*>(&hl01);
+  ah[0][2 + rr] = *reinterpret_cast<const uint32_t*>(&hl23);
+  al[0][rr] = pack_h2(nl[0] - fl01.x, nl[1] - fl01.y);
+  al[0][2 + rr] = pack_h2(nl[2] - fl23.x, nl[3] - fl23.y);
+  ah[1][rr] = *reinterpret_cast<const uint32_t*>(&hu01);
+  ah[1][2 + rr] = *reinterpret_cast<const uint32_t*>(&hu23);
+  al[1][rr] = pack_h2(nu[0] - fu01.x, nu[1] - fu01.y);
+  al[1][2 + rr] = pack_h2(nu[2] - fu23.x, nu[3] - fu23.y);
 }
 
 // PV for one packed group: P^T per V block (probabilities times the per-token
@@ -412,10 +411,11 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
   const uint2* qb = cx.qb;
   const uint2* qh = cx.qh;
     if constexpr (TR::KCH && C::ROPE) {
-      uint32_t qg[KC][NT][2];
-      rope_query<C>(cx, t0, qg);
-#pragma unroll
+      const float2* base = cx.rope_base + (int64_t)(t0 / kTile) * (D / 2);
+#pragma unroll 1
       for (int kcp = 0; kcp < KC / 2; ++kcp) {
+        uint32_t ql[NT][2], qu[NT][2];
+        rope_query_pair<C>(cx, base, kcp, ql, qu);
         const int c = 32 * (kcp >> 1) + 8 * tq + 2 * (kcp & 1);
         const int ch[4] = {c, c + 4, c + 1, c + 5};
         float sl[4], su[4];
@@ -449,28 +449,28 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
             cu1[k] = code_pair<2>(xu[1], k);
           }
         }
+        const float4* fr = cx.rope_frag + kcp * 256 + lane;
 #pragma unroll
         for (int mu = 0; mu < 2; ++mu) {
           uint32_t ah[2][4], al[2][4];
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
             const int k = 2 * mu + rr;
+            const float4 cs[2] = {__ldg(fr + (2 * k) * 32), __ldg(fr + (2 * k + 1) * 32)};
             const float2 l01 = __half22float2(*reinterpret_cast<const __half2*>(&cl0[k]));
             const float2 l23 = __half22float2(*reinterpret_cast<const __half2*>(&cl1[k]));
             const float2 u01 = __half22float2(*reinterpret_cast<const __half2*>(&cu0[k]));
             const float2 u23 = __half22float2(*reinterpret_cast<const __half2*>(&cu1[k]));
             const float lv[4] = {l01.x * sl[0], l01.y * sl[1], l23.x * sl[2], l23.y * sl[3]};
             const float uv[4] = {u01.x * su[0], u01.y * su[1], u23.x * su[2], u23.y * su[3]};
-            rope_key_frags<C>(cx, 4 * gq + k, lv, uv, rr, ch, ah, al);
+            rope_key_frags(cs, lv, uv, rr, ah, al);
           }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            mma16816(S[mu][nt], ah[0][0], ah[0][1], ah[0][2], ah[0][3], qg[kcp][nt][0], qg[kcp][nt][1]);
-            mma16816(S[mu][nt], al[0][0], al[0][1], al[0][2], al[0][3], qg[kcp][nt][0], qg[kcp][nt][1]);
-            mma16816(S[mu][nt], ah[1][0], ah[1][1], ah[1][2], ah[1][3], qg[kcp + KC / 2][nt][0],
-                     qg[kcp + KC / 2][nt][1]);
-            mma16816(S[mu][nt], al[1][0], al[1][1], al[1][2], al[1][3], qg[kcp + KC / 2][nt][0],
-                     qg[kcp + KC / 2][nt][1]);
+            mma16816(S[mu][nt], ah[0][0], ah[0][1], ah[0][2], ah[0][3], ql[nt][0], ql[nt][1]);
+            mma16816(S[mu][nt], al[0][0], al[0][1], al[0][2], al[0][3], ql[nt][0], ql[nt][1]);
+            mma16816(S[mu][nt], ah[1][0], ah[1][1], ah[1][2], ah[1][3], qu[nt][0], qu[nt][1]);
+            mma16816(S[mu][nt], al[1][0], al[1][1], al[1][2], al[1][3], qu[nt][0], qu[nt][1]);
           }
         }
       }
@@ -655,7 +655,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   cx.qh = qh;
   cx.qr = qr;
   cx.rope_base = a.rope;
-  cx.rope_off = a.rope + (int64_t)a.rope_base_rows * (D / 2);
+  cx.rope_frag = reinterpret_cast<const float4*>(a.rope + (int64_t)(a.rope_base_rows + kTile) * (D / 2));
 
   WarpState<C> ws;
 #pragma unroll
@@ -757,55 +757,43 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
       const int t0 = qe + (tile - n_c - n_m) * kTile;
       const int n_valid = min(kTile, T - t0);
       if constexpr (C::ROPE) {
-        uint32_t qg[KC][NT][2];
-        rope_query<C>(cx, t0, qg);
+        const float2* base = cx.rope_base + (int64_t)(t0 / kTile) * (D / 2);
+#pragma unroll 1
+        for (int kcp = 0; kcp < KC / 2; ++kcp) {
+          uint32_t ql[NT][2], qu[NT][2];
+          rope_query_pair<C>(cx, base, kcp, ql, qu);
+          // k-chunk kcp: channels c + {0, 4, 1, 5}, c = 32 (kcp / 2) + 8 tq + 2 (kcp % 2)
+          const int c = 32 * (kcp >> 1) + 8 * tq + 2 * (kcp & 1);
+          const float4* fr = cx.rope_frag + kcp * 256 + lane;
 #pragma unroll
-        for (int mu = 0; mu < 2; ++mu) {
-#pragma unroll
-          for (int s = 0; s < C::NS / 2; ++s) {
-            uint32_t ah[2][2][4], al[2][2][4];  // [b][lower/upper][a0..a3]
+          for (int mu = 0; mu < 2; ++mu) {
+            uint32_t ah[2][4], al[2][4];
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-              const int r = 4 * gq + 2 * mu + rr;
+              const int k = 2 * mu + rr, r = 4 * gq + k;
               const uint16_t* row = resid_row(lo, a.cp, 0, layer, seq, h, t0 + min(r, n_valid - 1));
-              uint4 wl = make_uint4(0, 0, 0, 0), wu = wl;
+              uint32_t wl0 = 0, wl1 = 0, wu0 = 0, wu1 = 0;  // (c, c+1), (c+4, c+5) and partners
               if (r < n_valid) {
-                wl = *reinterpret_cast<const uint4*>(row + 32 * s + 8 * tq);
-                wu = *reinterpret_cast<const uint4*>(row + 32 * s + D / 2 + 8 * tq);
+                wl0 = *reinterpret_cast<const uint32_t*>(row + c);
+                wl1 = *reinterpret_cast<const uint32_t*>(row + c + 4);
+                wu0 = *reinterpret_cast<const uint32_t*>(row + c + D / 2);
+                wu1 = *reinterpret_cast<const uint32_t*>(row + c + 4 + D / 2);
               }
-              const uint32_t lw[4] = {wl.x, wl.y, wl.z, wl.w}, uw[4] = {wu.x, wu.y, wu.z, wu.w};
-              float lf[8], uf[8];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&lw[e]));
-                const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&uw[e]));
-                lf[2 * e] = a2.x;
-                lf[2 * e + 1] = a2.y;
-                uf[2 * e] = b2.x;
-                uf[2 * e + 1] = b2.y;
-              }
-#pragma unroll
-              for (int b = 0; b < 2; ++b) {
-                // k-chunk 2s + b: channels c + {0, 4, 1, 5}, c = 32s + 8tq + 2b
-                const int c = 32 * s + 8 * tq + 2 * b;
-                const int ch[4] = {c, c + 4, c + 1, c + 5};
-                const float lv[4] = {lf[2 * b], lf[2 * b + 4], lf[2 * b + 1], lf[2 * b + 5]};
-                const float uv[4] = {uf[2 * b], uf[2 * b + 4], uf[2 * b + 1], uf[2 * b + 5]};
-                rope_key_frags<C>(cx, r, lv, uv, rr, ch, ah[b], al[b]);
-              }
+              const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&wl0));
+              const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&wl1));
+              const float2 b0 = __half22float2(*reinterpret_cast<const __half2*>(&wu0));
+              const float2 b1 = __half22float2(*reinterpret_cast<const __half2*>(&wu1));
+              const float lv[4] = {a0.x, a1.x, a0.y, a1.y};
+              const float uv[4] = {b0.x, b1.x, b0.y, b1.y};
+              const float4 cs[2] = {__ldg(fr + (2 * k) * 32), __ldg(fr + (2 * k + 1) * 32)};
+              rope_key_frags(cs, lv, uv, rr, ah, al);
             }
 #pragma unroll
-            for (int b = 0; b < 2; ++b) {
-              const int kc = 2 * s + b;
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                mma16816(S[mu][nt], ah[b][0][0], ah[b][0][1], ah[b][0][2], ah[b][0][3], qg[kc][nt][0], qg[kc][nt][1]);
-                mma16816(S[mu][nt], al[b][0][0], al[b][0][1], al[b][0][2], al[b][0][3], qg[kc][nt][0], qg[kc][nt][1]);
-                mma16816(S[mu][nt], ah[b][1][0], ah[b][1][1], ah[b][1][2], ah[b][1][3], qg[kc + KC / 2][nt][0],
-                         qg[kc + KC / 2][nt][1]);
-                mma16816(S[mu][nt], al[b][1][0], al[b][1][1], al[b][1][2], al[b][1][3], qg[kc + KC / 2][nt][0],
-                         qg[kc + KC / 2][nt][1]);
-              }
+            for (int nt = 0; nt < NT; ++nt) {
+              mma16816(S[mu][nt], ah[0][0], ah[0][1], ah[0][2], ah[0][3], ql[nt][0], ql[nt][1]);
+              mma16816(S[mu][nt], al[0][0], al[0][1], al[0][2], al[0][3], ql[nt][0], ql[nt][1]);
+              mma16816(S[mu][nt], ah[1][0], ah[1][1], ah[1][2], ah[1][3], qu[nt][0], qu[nt][1]);
+              mma16816(S[mu][nt], al[1][0], al[1][1], al[1][2], al[1][3], qu[nt][0], qu[nt][1]);
             }
           }
         }

@@ -74,14 +74,31 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(DequantArgs a) {
 }
 
 // base[r][i] = (cos, sin)(32 r theta_i), off[j][i] = (cos, sin)(j theta_i),
-// theta_i = theta^(-2i/D), evaluated in fp64 and rounded to fp32.
+// theta_i = theta^(-2i/D), evaluated in fp64 and rounded to fp32; then the
+// same off values regrouped in the order the tensor-core decode's lanes read
+// them: float4 [D/32 chunk pairs kcp][4 tokens k][2 channel pairs][32 lanes],
+// lane (gq, tq) holding token j = 4gq + k and channels c + {0, 4} or
+// c + {1, 5}, c = 32 (kcp / 2) + 8 tq + 2 (kcp % 2).
 __global__ void rope_tables_kernel(float2* rope, int base_rows, int D, double theta) {
   const int half = D / 2;
-  const int total = (base_rows + kTile) * half;
+  const int plain = (base_rows + kTile) * half;
+  const int total = plain + kTile * half;
   for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
-    const int r = e / half, i = e % half;
+    int i;
+    double pos;
+    if (e < plain) {
+      const int r = e / half;
+      i = e % half;
+      pos = r < base_rows ? (double)r * kTile : (double)(r - base_rows);
+    } else {
+      const int f2 = e - plain, F = f2 >> 1, hf = f2 & 1;
+      const int lane = F & 31, qp = (F >> 5) & 1, k = (F >> 6) & 3, kcp = F >> 8;
+      const int q = 2 * qp + hf;
+      const int dq = q == 0 ? 0 : q == 1 ? 4 : q == 2 ? 1 : 5;
+      i = 32 * (kcp >> 1) + 8 * (lane & 3) + 2 * (kcp & 1) + dq;
+      pos = (double)(4 * (lane >> 2) + k);
+    }
     const double inv = pow(theta, -2.0 * i / D);
-    const double pos = r < base_rows ? (double)r * kTile : (double)(r - base_rows);
     double s, c;
     sincos(pos * inv, &s, &c);
     rope[e] = make_float2((float)c, (float)s);
