@@ -130,14 +130,50 @@ __device__ __forceinline__ float split_part(float x, bool lo) {
   return lo ? x - hi : hi;
 }
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
+// ---- bulk copies (TMA engine) completing on a per-stage mbarrier ----------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+// Makes the barrier initialization visible to the async proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+// Orders this thread's earlier shared-memory accesses (generic proxy) before
+// later bulk copies into the same bytes (async proxy).
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+// `bytes` (a multiple of 16) from global `src` to shared `dst`, both 16-byte
+// aligned; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for phase `parity` of `bar`; false when the limit ran out
+// (the same answer on every lane of the warp).
+constexpr int kSpinLimit = 1 << 22;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  bool ok = false;
+  for (int i = 0; i < kSpinLimit && !ok; ++i) ok = mbar_test(bar, parity);
+  return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
@@ -476,7 +512,13 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
       }
     } else if constexpr (TR::KCH) {
       // per-channel K: block c = channel c over the group's 32 tokens; the
-      // channel scales multiply the query columns
+      // channel scales multiply the query columns.  Even and odd k-chunks
+      // accumulate separately (two independent MMA chains).
+      float Sx[2][NT][4];
+#pragma unroll
+      for (int mu = 0; mu < 2; ++mu)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) Sx[mu][nt][0] = Sx[mu][nt][1] = Sx[mu][nt][2] = Sx[mu][nt][3] = 0.f;
 #pragma unroll
       for (int kc = 0; kc < KC; ++kc) {
         const int c = 32 * (kc >> 1) + 8 * tq + 2 * (kc & 1);
@@ -507,10 +549,18 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
           const uint32_t bq0 = hfma2u(qv.x, s12, (hmul2u(qv.x, s12) ^ 0x80008000u) & lo_mask);
           const uint32_t bq1 = hfma2u(qv.y, s34, (hmul2u(qv.y, s34) ^ 0x80008000u) & lo_mask);
 #pragma unroll
-          for (int mu = 0; mu < 2; ++mu)
-            mma16816(S[mu][nt], k12[2 * mu], k12[2 * mu + 1], k34[2 * mu], k34[2 * mu + 1], bq0, bq1);
+          for (int mu = 0; mu < 2; ++mu) {
+            float (&acc)[4] = (kc & 1) ? Sx[mu][nt] : S[mu][nt];
+            mma16816(acc, k12[2 * mu], k12[2 * mu + 1], k34[2 * mu], k34[2 * mu + 1], bq0, bq1);
+          }
         }
       }
+#pragma unroll
+      for (int mu = 0; mu < 2; ++mu)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) S[mu][nt][e] += Sx[mu][nt][e];
     } else {
       // per-token K: each K block's scale multiplies its partial scores
 #pragma unroll
@@ -564,6 +614,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   uint8_t* stage_base = smem + C::QSM;
   __shared__ float qmax_s[kWarps];
   __shared__ uint32_t bad_page;
+  __shared__ uint64_t mbar[kWarps * kStages];
   __shared__ int is_last;
 
   const Layout& lo = a.lo;
@@ -596,6 +647,8 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     float* qf = reinterpret_cast<float*>(stage_base);  // [g][D] scratch
     for (int e = tid; e < g * D; e += kThreadsMma) qf[e] = in_to_f32(a.q[qrow * D + e], lo.dtype);
     if (tid == 0) bad_page = 0;
+    if (tid < kWarps * kStages) mbar_init(mbar + tid, 1);
+    fence_mbar_init();
     __syncthreads();
     if (lo.flags & KVQ_ROTATE_K) {
       for (int r = warp; r < g * (D / 128); r += kWarps) {
@@ -671,18 +724,23 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   }
   uint8_t* wst = stage_base + warp * kStages * C::STAGE;
 
-  // copies of packed tile `tile` (cold or hot/only tier) into stage `st`
+  // Bulk copies of packed tile `tile` (cold or hot/only tier) into stage
+  // `st`, issued by lane 0: exactly one arrival on the stage's barrier per
+  // packed tile of this warp (with no bytes when a page id is bad).
   auto issue = [&](int tile, int st) {
     if (tile >= te || tile >= n_c + n_m) return;
+    if (lane != 0) return;
     uint8_t* ks = wst + st * C::STAGE;
     uint8_t* vs = ks + C::VOFF;
+    uint64_t* bar = mbar + warp * kStages + st;
     if constexpr (C::HAS_COLD) {
       if (tile < n_c) {
         const int t0 = tile * kTile;
         const uint8_t* kg = cold_row(lo, a.cp, 0, layer, seq, h, t0);
         const uint8_t* vg = cold_row(lo, a.cp, 1, layer, seq, h, t0);
-        for (int c = lane; c < C::COLD::KSTAGE / 16; c += 32) cp_async16(ks + 16 * c, kg + 16 * c);
-        for (int c = lane; c < C::COLD::VSTAGE / 16; c += 32) cp_async16(vs + 16 * c, vg + 16 * c);
+        mbar_arrive_tx(bar, C::COLD::KSTAGE + C::COLD::VSTAGE);
+        bulk_g2s(ks, kg, C::COLD::KSTAGE, bar);
+        bulk_g2s(vs, vg, C::COLD::VSTAGE, bar);
         return;
       }
     }
@@ -692,38 +750,53 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     if (lo.paged) {
       const int np = (qe - t0 > lo.pt) ? kTile / lo.pt : 1;
       const int kb = lo.pt * HT::KROW, vb = lo.pt * HT::VROW;
-      for (int pg = 0; pg < np; ++pg) {
-        const uint8_t* kg = main_row(lo, a.cp, 0, layer, seq, h, t0 + pg * lo.pt, &bad);
-        const uint8_t* vg = main_row(lo, a.cp, 1, layer, seq, h, t0 + pg * lo.pt, &bad);
-        if (bad) {
-          bad_page = 1;
-          return;
-        }
-        for (int c = lane; c < kb / 16; c += 32) cp_async16(ks + pg * kb + 16 * c, kg + 16 * c);
-        for (int c = lane; c < vb / 16; c += 32) cp_async16(vs + pg * vb + 16 * c, vg + 16 * c);
+      // one or two pages (16-token pages when the group is complete)
+      const uint8_t* kg0 = main_row(lo, a.cp, 0, layer, seq, h, t0, &bad);
+      const uint8_t* vg0 = main_row(lo, a.cp, 1, layer, seq, h, t0, &bad);
+      const uint8_t* kg1 = kg0;
+      const uint8_t* vg1 = vg0;
+      if (np == 2) {
+        kg1 = main_row(lo, a.cp, 0, layer, seq, h, t0 + lo.pt, &bad);
+        vg1 = main_row(lo, a.cp, 1, layer, seq, h, t0 + lo.pt, &bad);
+      }
+      if (bad) {
+        bad_page = 1;
+        mbar_arrive_tx(bar, 0);
+        return;
+      }
+      mbar_arrive_tx(bar, np * (kb + vb));
+      bulk_g2s(ks, kg0, kb, bar);
+      bulk_g2s(vs, vg0, vb, bar);
+      if (np == 2) {
+        bulk_g2s(ks + kb, kg1, kb, bar);
+        bulk_g2s(vs + vb, vg1, vb, bar);
       }
       return;
     }
     const uint8_t* kg = main_row(lo, a.cp, 0, layer, seq, h, t0, &bad);
     const uint8_t* vg = main_row(lo, a.cp, 1, layer, seq, h, t0, &bad);
-    for (int c = lane; c < HT::KSTAGE / 16; c += 32) cp_async16(ks + 16 * c, kg + 16 * c);
-    for (int c = lane; c < HT::VSTAGE / 16; c += 32) cp_async16(vs + 16 * c, vg + 16 * c);
+    mbar_arrive_tx(bar, HT::KSTAGE + HT::VSTAGE);
+    bulk_g2s(ks, kg, HT::KSTAGE, bar);
+    bulk_g2s(vs, vg, HT::VSTAGE, bar);
   };
 
   // ---- per-warp pipeline over this CTA's groups --------------------------------
   const int first = tb + warp;
+  // the query scratch in the stage buffers was written through the generic
+  // proxy; order it before the bulk copies, and publish the barriers
+  fence_proxy_async();
+  __syncthreads();
 #pragma unroll
-  for (int i = 0; i < kStages - 1; ++i) {
-    issue(first + kWarps * i, i);
-    cp_async_commit();
-  }
+  for (int i = 0; i < kStages - 1; ++i) issue(first + kWarps * i, i);
+  int stall_it = -1;
   for (int it = 0;; ++it) {
     const int tile = first + kWarps * it;
     if (tile >= te) break;
     issue(tile + kWarps * (kStages - 1), (it + kStages - 1) % kStages);
-    cp_async_commit();
-    cp_async_wait<kStages - 1>();
-    __syncwarp();
+    if (tile < n_c + n_m && !mbar_wait(mbar + warp * kStages + it % kStages, (it / kStages) & 1)) {
+      stall_it = it;
+      break;
+    }
 
     float S[2][NT][4];
 #pragma unroll
@@ -861,9 +934,20 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
         }
       }
     }
+    // every lane is done with this stage before lane 0 refills it
+    fence_proxy_async();
     __syncwarp();
   }
-  cp_async_wait<0>();
+  if (stall_it >= 0) {
+    // a copy did not land in time: flag it, give this warp's copies still in
+    // flight (that tile's and the next one's) a last bounded wait, and merge
+    // whatever is there
+    if (lane == 0) atomicOr(a.status, KVQ_DEV_STALL);
+    for (int j = stall_it; j < stall_it + kStages; ++j) {
+      const int tj = first + kWarps * j;
+      if (tj < te && tj < n_c + n_m) (void)mbar_wait(mbar + warp * kStages + j % kStages, (j / kStages) & 1);
+    }
+  }
   __syncthreads();
 
   // ---- merge the warps (shared memory), then the splits (workspace) -------------

@@ -27,6 +27,7 @@ DEV_CAPACITY = 1
 DEV_PAGE = 2
 DEV_RANGE = 4
 DEV_LENGTH = 8
+DEV_STALL = 16
 
 STATUS_NAMES = {0: "OK", 1: "ERR_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_CUDA", 4: "ERR_CAPACITY", 5: "ERR_WORKSPACE"}
 

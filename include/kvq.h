@@ -30,7 +30,9 @@
  *    before anything is launched, with a message in kvq_last_error().  Bad
  *    runtime data found by a kernel (a length beyond capacity, a page id out
  *    of range) sets a bit of the device status word in the workspace and
- *    skips that piece of work; nothing traps and nothing waits.
+ *    skips that piece of work; nothing traps.  The only waits are bounded
+ *    waits of a kernel for its own copies into shared memory
+ *    (KVQ_DEV_STALL when one runs out).
  *  - Head mapping: query head h reads kv head h / (H_q / H_kv).
  *  - Softmax scale: fixed at 1/sqrt(D).
  *
@@ -122,7 +124,9 @@ enum {
   KVQ_DEV_CAPACITY = 1u << 0, /* an append would exceed max_T, or more new tokens than max_new */
   KVQ_DEV_PAGE = 1u << 1,     /* a block_table entry outside [0, n_pages) */
   KVQ_DEV_RANGE = 1u << 2,    /* kvq_dequantize range outside [0, T) */
-  KVQ_DEV_LENGTH = 1u << 3    /* a sequence length < 0 or > max_T, or cu_new not ascending */
+  KVQ_DEV_LENGTH = 1u << 3,   /* a sequence length < 0 or > max_T, or cu_new not ascending */
+  KVQ_DEV_STALL = 1u << 4     /* a decode kernel's own bulk copy into shared memory did not complete
+                                 within its bounded wait; that call's outputs are undefined */
 };
 
 typedef struct {
