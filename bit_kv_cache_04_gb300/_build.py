@@ -20,6 +20,7 @@ COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler",
 SOURCES = [
     ("kvq_api.cu", []),
     ("append.cu", ["--fmad=false"]),
+    ("append_fast.cu", ["--fmad=false"]),
     ("decode_generic.cu", []),
     ("decode_mma.cu", []),
     ("dequant.cu", []),

@@ -15,48 +15,10 @@
 // "KV Cache Quantization", "Tai sao Key va Value lai khac nhau?"); rotated
 // formats pass each token's 128-chunks through the randomized Hadamard
 // transform first (trefon.com "Matematyka cache KV", "najpierw obrot").
-#include "block_codec.cuh"
+#include "append_common.cuh"
 
 namespace kvq {
 namespace {
-
-constexpr int kAppendThreads = 128;
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
-
-struct SeqSpan {
-  int T0, T1, n, off;
-  bool ok;
-};
-
-__device__ SeqSpan read_span(const AppendArgs& a, int seq) {
-  SeqSpan s;
-  s.off = a.cu_new[seq];
-  s.n = a.cu_new[seq + 1] - s.off;
-  s.T0 = a.seq_lens[seq];
-  s.T1 = s.T0 + s.n;
-  uint32_t bad = 0;
-  if (s.n < 0 || s.T0 < 0 || s.T0 > a.lo.max_T || s.off < 0 || a.cu_new[seq + 1] > a.total_new) bad |= KVQ_DEV_LENGTH;
-  else if (s.n > a.max_new || s.T1 > a.lo.max_T) bad |= KVQ_DEV_CAPACITY;
-  s.ok = bad == 0;
-  if (bad && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, bad);
-  return s;
-}
-
-__device__ __forceinline__ const uint16_t* input_row(const AppendArgs& a, int which, int li, const SeqSpan& s,
-                                                     int h, int t) {
-  const uint16_t* base = which ? a.v : a.k;
-  int64_t row = ((int64_t)li * a.total_new + s.off + (t - s.T0)) * a.lo.H + h;
-  return base + row * a.lo.D;
-}
 
 // ---- per-token rows: one warp per (token, kv head) ----------------------------
 //
@@ -484,7 +446,7 @@ cudaError_t launch_append_nc(const AppendArgs& a, cudaStream_t st) {
     attr_done = true;
   }
   if (lo.tiered) append_requant_kernel<NC><<<grid, kAppendThreads, 0, st>>>(a);
-  append_quantize_kernel<NC, ROT><<<grid, kAppendThreads, smem, st>>>(a);
+  if (!launch_fast_quantize(a, st)) append_quantize_kernel<NC, ROT><<<grid, kAppendThreads, smem, st>>>(a);
   if (lo.ring) append_window_kernel<<<grid, kAppendThreads, 0, st>>>(a);
   return cudaGetLastError();
 }

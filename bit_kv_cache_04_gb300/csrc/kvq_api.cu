@@ -259,6 +259,9 @@ kvq_status cache_ptrs(const kvq_config* c, const kvq_cache* cache, CachePtrs* cp
   bool ring = !(c->residual_window == 0 && gam == 1);
   if (ring && (!cp->k_resid || !cp->v_resid)) return fail(KVQ_ERR_ARG, "window buffers are NULL");
   if (c->page_tokens > 0 && !cp->block_table) return fail(KVQ_ERR_ARG, "block_table is NULL");
+  const uintptr_t any = (uintptr_t)cp->k_main | (uintptr_t)cp->v_main | (uintptr_t)cp->k_cold |
+                        (uintptr_t)cp->v_cold | (uintptr_t)cp->k_resid | (uintptr_t)cp->v_resid;
+  if (any & 15u) return fail(KVQ_ERR_ARG, "cache buffers must be 16-byte aligned");
   return KVQ_OK;
 }
 
@@ -385,6 +388,7 @@ kvq_status kvq_append(const kvq_config* cfg, const kvq_cache* cache, int32_t lay
   if (total_new < 0 || max_new < 0 || max_new > total_new) return fail(KVQ_ERR_ARG, "total_new / max_new");
   if (max_new > cfg->max_T) return fail(KVQ_ERR_CAPACITY, "max_new=%d > max_T=%d", max_new, cfg->max_T);
   if (total_new > 0 && (!k || !v)) return fail(KVQ_ERR_ARG, "k / v is NULL");
+  if (((uintptr_t)k | (uintptr_t)v) & 15u) return fail(KVQ_ERR_ARG, "k / v must be 16-byte aligned");
   if (!cu_new || !seq_lens) return fail(KVQ_ERR_ARG, "cu_new / seq_lens is NULL");
   AppendArgs a{};
   if ((st = cache_ptrs(cfg, cache, &a.cp)) != KVQ_OK) return st;
@@ -402,6 +406,17 @@ kvq_status kvq_append(const kvq_config* cfg, const kvq_cache* cache, int32_t lay
   a.status = (uint32_t*)((char*)workspace + w.status);
   cudaError_t e = launch_append(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "append kernels");
+  return ok();
+}
+
+kvq_status kvq_launch_counts(const kvq_config* cfg, int32_t* append_launches, int32_t* decode_launches) {
+  kvq_status st = check_config(cfg, false);
+  if (st != KVQ_OK) return st;
+  if (!append_launches || !decode_launches) return fail(KVQ_ERR_ARG, "output pointer is NULL");
+  AppendArgs a{};
+  a.lo = make_layout(cfg);
+  *append_launches = (a.lo.tiered ? 1 : 0) + (fast_quantize_available(a) ? 2 : 1) + (a.lo.ring ? 1 : 0);
+  *decode_launches = 1;
   return ok();
 }
 

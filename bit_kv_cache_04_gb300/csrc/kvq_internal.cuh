@@ -189,6 +189,10 @@ struct DequantArgs {
 };
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+// Specialized phase B (quantize) of an append when one exists for both
+// tensors' formats; false when nothing was launched.
+bool launch_fast_quantize(const AppendArgs& a, cudaStream_t s);
+bool fast_quantize_available(const AppendArgs& a);
 cudaError_t launch_commit_lengths(const int32_t* cu_new, int32_t* seq_lens, int batch, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);  // tensor-core path when it fits, else generic
 cudaError_t launch_decode_generic(const DecodeArgs& a, cudaStream_t s);

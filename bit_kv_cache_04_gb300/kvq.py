@@ -124,6 +124,7 @@ def _load():
         "kvq_commit_lengths": ([cfgp, vp, vp, vp], ctypes.c_int),
         "kvq_decode_attention": ([cfgp, cachep, i32, i32, vp, vp, vp, i32, vp, sz, vp], ctypes.c_int),
         "kvq_decode_splits": ([cfgp, i32, P(i32)], ctypes.c_int),
+        "kvq_launch_counts": ([cfgp, P(i32), P(i32)], ctypes.c_int),
         "kvq_decode_attention_static": ([cfgp, cachep, i32, i32, vp, vp, vp, i32, vp], ctypes.c_int),
         "kvq_dequantize": ([cfgp, cachep, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "kvq_read_device_status": ([vp, P(u32), vp], ctypes.c_int),
@@ -142,7 +143,7 @@ LIB = _load()
 EXPORTED = ("kvq_version", "kvq_last_error", "kvq_validate_config", "kvq_block_bytes", "kvq_bytes_per_token",
             "kvq_cache_bytes", "kvq_buffer_sizes", "kvq_workspace_bytes", "kvq_workspace_init", "kvq_append",
             "kvq_commit_lengths", "kvq_decode_attention", "kvq_decode_splits", "kvq_decode_attention_static",
-            "kvq_dequantize",
+            "kvq_dequantize", "kvq_launch_counts",
             "kvq_read_device_status", "kvq_clear_device_status")
 
 
@@ -184,6 +185,13 @@ def kvq_buffer_sizes(cfg: Config) -> Tuple[int, ...]:
     arr = (ctypes.c_size_t * 6)()
     _check(LIB.kvq_buffer_sizes(ctypes.byref(cfg.to_c()), arr))
     return tuple(arr)
+
+
+def kvq_launch_counts(cfg: Config):
+    """(kernel launches of one kvq_append call, of one kvq_decode_attention call)."""
+    a, d = ctypes.c_int32(), ctypes.c_int32()
+    _check(LIB.kvq_launch_counts(ctypes.byref(cfg.to_c()), ctypes.byref(a), ctypes.byref(d)))
+    return a.value, d.value
 
 
 def kvq_workspace_bytes(cfg: Config) -> int:

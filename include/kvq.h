@@ -150,6 +150,7 @@ typedef struct {
   int32_t reserved;        /* must be 0 */
 } kvq_config;
 
+/* Every buffer is 16-byte aligned (KVQ_ERR_ARG otherwise). */
 typedef struct {
   void* k_main;  /* main / hot tier of K */
   void* v_main;  /* main / hot tier of V */
@@ -197,7 +198,8 @@ KVQ_API kvq_status kvq_workspace_bytes(const kvq_config* cfg, size_t* bytes);
 KVQ_API kvq_status kvq_workspace_init(const kvq_config* cfg, void* workspace, size_t ws_bytes, void* stream);
 
 /* Quantize-on-append for layers [layer0, layer0 + n_layers).
- *  k, v:     [n_layers][total_new][H_kv][D] in_dtype, device; sequences back
+ *  k, v:     [n_layers][total_new][H_kv][D] in_dtype, device, 16-byte
+ *            aligned (KVQ_ERR_ARG otherwise); sequences back
  *            to back in batch order (post-RoPE keys, or pre-RoPE with
  *            KVQ_K_PRE_ROPE).
  *  cu_new:   [batch + 1] int32 device, cu_new[0] = 0, cu_new[batch] =
@@ -272,6 +274,11 @@ KVQ_API kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_cache* cache,
 KVQ_API kvq_status kvq_decode_attention_static(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0,
                                                int32_t n_layers, const void* q, const int32_t* seq_lens,
                                                float* out, int32_t num_splits, void* stream);
+
+/* Kernel launches one kvq_append call (with new tokens) and one
+ * kvq_decode_attention call make for this configuration, e.g. to budget
+ * launches per decode step.  No pages counterpart: library bookkeeping. */
+KVQ_API kvq_status kvq_launch_counts(const kvq_config* cfg, int32_t* append_launches, int32_t* decode_launches);
 
 /* Synchronizes `stream` and reads the device status word (KVQ_DEV_* bits). */
 KVQ_API kvq_status kvq_read_device_status(const void* workspace, uint32_t* bits, void* stream);

@@ -109,3 +109,12 @@ def test_split_heuristic_fits_workspace():
             units = n * cfg.batch * cfg.H_kv
             g = cfg.H_q // cfg.H_kv
             assert ws >= units * s * g * (cfg.D + 2) * 4 or s == 1
+
+
+def test_launch_counts():
+    # append: [requant to cold] + quantize (two specialized kernels or one
+    # generic) + [window copy]; decode: one launch
+    assert K.kvq_launch_counts(W.make("llama2_7b_kivi4").cfg) == (1 + 2, 1)
+    assert K.kvq_launch_counts(W.make("mistral7b_hotcold").cfg) == (1 + 2 + 1, 1)
+    assert K.kvq_launch_counts(W.make("q8_0_mha_1k").cfg) == (2, 1)
+    assert K.kvq_launch_counts(W.make("ctx262k_hadamard4").cfg) == (1, 1)

@@ -1,0 +1,110 @@
+"""Byte parity of quantize-on-append for every bit width, block axis, input
+dtype and head dim of the 32-value block formats, on two kinds of input:
+
+* exact ties: every block's absolute maximum is qmax * s with s a power of two
+  (so s16 = s exactly) and every other value is (k + 1/2) s, so every code is
+  decided by round-half-to-even.  The maxima sit where token index and
+  channel index agree mod 32, so per-token blocks (32 channels of a token) and
+  per-channel blocks (one channel over 32 tokens) both hold one.  One kv head
+  uses s = 2^-20, a subnormal fp16 scale;
+* seeded N(0, 1) values with a few large channels.
+
+Each case appends in two calls (a bulk prefix, then a ragged remainder) and
+compares every packed byte with the oracle.
+"""
+
+import zlib
+
+import numpy as np
+import pytest
+
+from oracle import kvq_oracle as O
+from tests.helpers import codes_differ, oracle_cfg, raw16
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+from bit_kv_cache_04_gb300 import kvq as K  # noqa: E402
+
+CH, TOK = K.AXIS_CHANNEL, K.AXIS_TOKEN
+
+# (name, D, dtype, k_fmt, v_fmt, k_cold, v_cold, hot_window, residual_window)
+CASES = [
+    ("t8_f16", 128, K.DT_F16, K.Fmt(8, 32), K.Fmt(8, 32), None, None, 0, 0),
+    ("t8_bf16_d256", 256, K.DT_BF16, K.Fmt(8, 32), K.Fmt(8, 32), None, None, 0, 16),
+    ("t4_bf16", 128, K.DT_BF16, K.Fmt(4, 32), K.Fmt(4, 32), None, None, 0, 0),
+    ("t3_f16", 128, K.DT_F16, K.Fmt(3, 32), K.Fmt(3, 32), None, None, 0, 0),
+    ("t2_bf16", 128, K.DT_BF16, K.Fmt(2, 32), K.Fmt(2, 32), None, None, 0, 0),
+    ("kivi4_bf16", 128, K.DT_BF16, K.Fmt(4, 32, CH), K.Fmt(4, 32), None, None, 0, 128),
+    ("kivi2_f16_d256", 256, K.DT_F16, K.Fmt(2, 32, CH), K.Fmt(2, 32), None, None, 0, 64),
+    ("tiers_bf16", 128, K.DT_BF16, K.Fmt(4, 32, CH), K.Fmt(4, 32), K.Fmt(2, 32, CH), K.Fmt(2, 32), 64, 32),
+    ("tiers_f16_d256", 256, K.DT_F16, K.Fmt(4, 32, CH), K.Fmt(4, 32), K.Fmt(2, 32, CH), K.Fmt(2, 32), 96, 0),
+]
+
+LENGTHS = [301, 160, 33]
+PREFIX = [200, 64, 0]
+
+
+def _inputs(kind, n_tok, H, D, bits, gen):
+    """[n_tok, H, D] input values (float64) for one tensor; token index is the
+    position within the sequence."""
+    if kind == "ties":
+        qmax = (1 << (bits - 1)) - 1
+        k = torch.randint(-qmax, qmax, (n_tok, H, D), generator=gen, dtype=torch.int64).double() + 0.5
+        t = torch.arange(n_tok).view(-1, 1, 1)
+        c = torch.arange(D).view(1, 1, -1)
+        diag = (t % 32) == (c % 32)
+        sign = torch.where(torch.rand((n_tok, H, D), generator=gen) < 0.5, -1.0, 1.0).double()
+        x = torch.where(diag.expand(n_tok, H, D), sign * qmax, k)
+        s = torch.tensor([2.0 ** (-3 * (h % 3)) for h in range(H)], dtype=torch.float64).view(1, H, 1)
+        s[0, -1, 0] = 2.0 ** -20
+        return x * s
+    x = torch.randn((n_tok, H, D), generator=gen, dtype=torch.float64)
+    x[..., 5] *= 12
+    x[..., D - 9] *= 30
+    return x
+
+
+def _case_tensors(kind, cfg, lengths, which, gen):
+    bits = (cfg.k_fmt if which == 0 else cfg.v_fmt).bits
+    dt = torch.float16 if cfg.in_dtype == K.DT_F16 else torch.bfloat16
+    return [_inputs(kind, T, cfg.H_kv, cfg.D, bits, gen).to(dt) for T in lengths]
+
+
+@pytest.mark.parametrize("kind", ["ties", "random"])
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_append_bytes_match_oracle(case, kind):
+    name, D, dtype, kf, vf, kc, vc, hot, R = case
+    cfg = K.Config(L=1, H_kv=3, H_q=3, D=D, batch=len(LENGTHS), max_T=max(LENGTHS) + 32, in_dtype=dtype,
+                   k_fmt=kf, v_fmt=vf, k_cold=kc, v_cold=vc, hot_window=hot, residual_window=R)
+    oc = oracle_cfg(cfg)
+    gen = torch.Generator().manual_seed(zlib.crc32(f"{name}/{kind}".encode()))
+    ks = _case_tensors(kind, cfg, LENGTHS, 0, gen)
+    vs = _case_tensors(kind, cfg, LENGTHS, 1, gen)
+    cache = K.KVCache(cfg, "cuda")
+    ref = O.new_buffers(oc)
+    seq_lens = torch.zeros(cfg.batch, dtype=torch.int32, device="cuda")
+    done = [0] * cfg.batch
+    for step in (PREFIX, [T - p for T, p in zip(LENGTHS, PREFIX)]):
+        kk = torch.cat([ks[b][done[b]:done[b] + step[b]] for b in range(cfg.batch)])
+        vv = torch.cat([vs[b][done[b]:done[b] + step[b]] for b in range(cfg.batch)])
+        cu = np.concatenate([[0], np.cumsum(step)]).astype(np.int32)
+        cu_d = torch.as_tensor(cu, device="cuda")
+        cache.append(0, 1, kk[None].cuda().contiguous(), vv[None].cuda().contiguous(), cu_d, seq_lens,
+                     int(cu[-1]), max(step))
+        cache.commit_lengths(cu_d, seq_lens)
+        O.append(oc, ref, 0, raw16(kk), raw16(vv), step, done)
+        done = [d + x for d, x in zip(done, step)]
+    torch.cuda.synchronize()
+    assert cache.device_status() == 0
+    shapes = O.buffer_shapes(oc)
+    for n, arr in cache.buffer_numpy().items():
+        shape, dt = shapes[n]
+        got = arr.view(dt).reshape(shape)
+        if not np.array_equal(got, ref[n]):
+            total, diff, maxd, sdiff = codes_differ(oc, {n: got}, {n: ref[n]}) \
+                if not n.endswith("resid") else (0, -1, -1, -1)
+            pytest.fail(f"{name}/{kind} {n}: bytes differ (codes {diff}/{total}, max |dc| {maxd}, scales {sdiff})")

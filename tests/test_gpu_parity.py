@@ -201,3 +201,11 @@ def test_host_validation_launches_nothing():
         cache.decode(0, 2, q, sl, out)  # layers beyond L
     with pytest.raises(K.KvqError):
         cache.decode(0, 1, q, sl, out, num_splits=1000)
+    # misaligned input rows are refused before any launch
+    kv = torch.zeros((1, 2 * 4 * 128 + 8), dtype=torch.float16, device="cuda")
+    k_bad = kv[:, 1:1 + 4 * 128].view(1, 1, 4, 128)
+    cu = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+    with pytest.raises(K.KvqError):
+        cache.append(0, 1, k_bad, k_bad, cu, sl, 1, 1)
+    torch.cuda.synchronize()
+    assert cache.device_status() == 0
