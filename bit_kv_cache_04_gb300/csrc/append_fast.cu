@@ -32,6 +32,12 @@ __device__ __forceinline__ float2 raw_pair_to_f32(uint32_t w) {
   }
 }
 
+template <int DT>
+__device__ __forceinline__ float in_to_f32_t(uint32_t bits16) {
+  if constexpr (DT == KVQ_DT_F16) return __half2float(__ushort_as_half((unsigned short)bits16));
+  else return __uint_as_float(bits16 << 16);
+}
+
 __device__ __forceinline__ float div_by_scale(float x, float sf, float rcp) {
   const float q0 = __fmul_rn(x, rcp);
   const float e = __fmaf_rn(-q0, sf, x);
@@ -40,22 +46,43 @@ __device__ __forceinline__ float div_by_scale(float x, float sf, float rcp) {
 
 // Codes of v[0..31] with scale sf (rcp = RN(1/sf), 0 when sf = 0) as a
 // 32*B-bit little-endian stream (biased codes; two's complement for B = 8);
-// dq (optional) receives code * sf.
+// dq (optional) receives code * sf.  The rounded value's float bits are
+// kRoundMagicBits + code + bias; each word accumulates those bits shifted into
+// place (one integer multiply-add per code) and subtracts the magic parts
+// once, which is exact modulo 2^32 because every biased code fits its field.
+// For B = 8 the bias is 128 and flipping each byte's top bit afterwards gives
+// two's complement.
+constexpr uint32_t kRoundMagicBits = 0x4B400000u;  // bits of 1.5 * 2^23
+
 template <int B>
 __device__ __forceinline__ void codes32(const float (&v)[32], float sf, float rcp, uint32_t (&w)[B], float* dq) {
   constexpr int qmax = (1 << (B - 1)) - 1;
-  constexpr float magic = kRoundMagic + (B == 8 ? 0.f : (float)(qmax + 1));
-  constexpr uint32_t mask = (1u << B) - 1u;
+  constexpr int bias = qmax + 1;
+  constexpr float magic = kRoundMagic + (float)bias;
 #pragma unroll
   for (int k = 0; k < B; ++k) w[k] = 0;
+  uint32_t corr[B];
+#pragma unroll
+  for (int k = 0; k < B; ++k) corr[k] = 0;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const float r = __fadd_rn(div_by_scale(v[j], sf, rcp), magic);
     if (dq) dq[j] = __fmul_rn(__fsub_rn(r, magic), sf);
-    const uint32_t u = __float_as_uint(r) & mask;
+    const uint32_t bits = __float_as_uint(r);
     const int bit = B * j, k = bit / 32, sh = bit % 32;
-    w[k] |= u << sh;
-    if (sh + B > 32) w[k + 1] |= u >> (32 - sh);
+    if (sh + B > 32) {  // a 3-bit code across two words: place the true biased code
+      const uint32_t u = bits - kRoundMagicBits;
+      w[k] += u << sh;
+      w[k + 1] += u >> (32 - sh);
+    } else {
+      w[k] += bits << sh;
+      corr[k] += kRoundMagicBits << sh;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < B; ++k) {
+    w[k] -= corr[k];
+    if (B == 8) w[k] ^= 0x80808080u;
   }
 }
 
@@ -211,17 +238,32 @@ __global__ void __launch_bounds__(kAppendThreads) quant_channel32_kernel(AppendA
   const int t0 = base + kTile * gi;
   if (t0 >= q0 && t0 < q1) {
     const bool to_cold = CB != 0 && lo.tiered && t0 < c1;
+    // the group's rows: window ring slots for tokens below T0, new input rows
+    // (a fixed stride apart) from T0 on
+    const int n_rw = min(max(s.T0 - t0, 0), kTile);  // leading tokens from the window
+    const uint32_t* in = nullptr;
+    if (n_rw < kTile) in = reinterpret_cast<const uint32_t*>(input_row(a, which, li, s, h, t0 + n_rw)) + cp;
+    const int in_stride = lo.H * D / 2;
     uint32_t raw[32];
+    if (n_rw == 0) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      raw[j] = reinterpret_cast<const uint32_t*>(src_row(a, which, li, layer, s, seq, h, t0 + j))[cp];
+      for (int j = 0; j < 32; ++j) raw[j] = in[j * in_stride];
+    } else {
+      const uint32_t* rw = reinterpret_cast<const uint32_t*>(resid_row(lo, a.cp, which, layer, seq, h, 0)) + cp;
+      int slot = t0 % lo.ring;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        raw[j] = j < n_rw ? rw[slot * (D / 2)] : in[(j - n_rw) * in_stride];
+        slot = slot + 1 == lo.ring ? 0 : slot + 1;
+      }
+    }
 #pragma unroll
     for (int hc = 0; hc < 2; ++hc) {
       float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float2 f = raw_pair_to_f32<DT>(raw[j]);
-        v[j] = hc ? f.y : f.x;
+        const uint32_t h16 = hc ? (raw[j] >> 16) : (raw[j] & 0xFFFFu);
+        v[j] = in_to_f32_t<DT>(h16);
       }
       const int c = 2 * cp + hc;
       hot_or_cold<B, CB>(v, to_cold, out + gi * SLOT + c * BB, out + gi * SLOT + c * CBB);
