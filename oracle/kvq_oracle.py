@@ -27,6 +27,12 @@ What it computes, step by step, with the page each step follows:
 * Keys stored before RoPE and rotated on the fly with split-half RoPE
   (troisinh.com, "RoPE - Cai bay tinh vi"; lehuy.net "NexusQuant", section
   "Cac mo hinh duoc ho tro": split-half pairs).
+* TBQ4 (trefon.com, section "Jak 4-bitowemu cache to uchodzi: najpierw
+  obrot"): after the rotation, a 128-value block is stored as its L2 norm
+  (fp16) and, per value, the 4-bit index of the nearest of the 16 Lloyd-Max
+  centroids for N(0, sigma^2), sigma = 1/sqrt(128); the centroids come from
+  Lloyd's algorithm run here in fp64 (S. P. Lloyd, "Least squares
+  quantization in PCM", 1982; J. Max, 1960).
 * Decode attention, the plain definition in fp64: s_i = q.k_i / sqrt(D),
   p = softmax(s), output = sum_i p_i v_i (nalar.dev, sections "Error pada key
   mengubah input softmax" and "Error pada value masuk setelah attention
@@ -69,6 +75,8 @@ AXIS_CHANNEL = 1
 ROTATE_K = 1
 ROTATE_V = 2
 K_PRE_ROPE = 4
+TBQ4_K = 8
+TBQ4_V = 16
 
 DT_F16 = 0
 DT_BF16 = 1
@@ -370,6 +378,99 @@ def dequantize_f64(s16: np.ndarray, codes: np.ndarray) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
+# TBQ4: L2 norm + Lloyd-Max codebook of the rotated block
+# ----------------------------------------------------------------------------
+
+
+def _normal_pdf(z: float) -> float:
+    return math.exp(-0.5 * z * z) / math.sqrt(2.0 * math.pi)
+
+
+def _normal_upper(z: float) -> float:
+    """P(Z > z) for a standard normal Z."""
+    return 0.5 * math.erfc(z / math.sqrt(2.0))
+
+
+def lloyd_max_normal(levels: int = 16, sigma: float = 1.0 / math.sqrt(128.0), tol: float = 1e-15,
+                     max_iter: int = 100000):
+    """Lloyd's algorithm for the minimum mean-square-error quantizer with
+    `levels` (even) points for N(0, sigma^2), in fp64.
+
+    Alternates the two optimality conditions until the centroids stop moving
+    (max change <= tol, in units of sigma): each threshold is the midpoint of
+    its two neighbouring centroids; each centroid is the conditional mean of
+    the distribution between its thresholds, E[Z | a < Z < b] =
+    (pdf(a) - pdf(b)) / (P(Z > a) - P(Z > b)).  The density is symmetric, so
+    the positive half is iterated (middle threshold 0) and mirrored.
+    Returns (centroids [levels], thresholds [levels - 1], iterations), fp64,
+    ascending.
+    """
+    half = levels // 2
+    c = [(j + 0.5) * 0.5 for j in range(half)]
+    it = 0
+    for it in range(1, max_iter + 1):
+        t = [0.0] + [(c[j] + c[j + 1]) / 2.0 for j in range(half - 1)]
+        new = []
+        for j in range(half):
+            a = t[j]
+            upper_b = _normal_upper(t[j + 1]) if j + 1 < half else 0.0
+            pdf_b = _normal_pdf(t[j + 1]) if j + 1 < half else 0.0
+            new.append((_normal_pdf(a) - pdf_b) / (_normal_upper(a) - upper_b))
+        moved = max(abs(x - y) for x, y in zip(new, c))
+        c = new
+        if moved <= tol:
+            break
+    pos = np.array(c, np.float64) * sigma
+    cent = np.concatenate([-pos[::-1], pos])
+    thr = (cent[:-1] + cent[1:]) / 2.0
+    return cent, thr, it
+
+
+_CODEBOOK = None
+
+
+def tbq4_codebook() -> Tuple[np.ndarray, np.ndarray]:
+    """The format's tables: the 16 centroids and 15 decision thresholds
+    (midpoints computed in fp64), each rounded once to fp32."""
+    global _CODEBOOK
+    if _CODEBOOK is None:
+        c, t, _ = lloyd_max_normal()
+        _CODEBOOK = (c.astype(np.float32), t.astype(np.float32))
+    return _CODEBOOK
+
+
+def tbq4_quantize(y: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Rotated fp32 blocks y [..., 128] -> (n16 float16 [...], indices uint8
+    [..., 128]), with this op order (all fp32, round to nearest):
+
+    * S = (p0 + p1) + (p2 + p3), p_k = the sum of y_i*y_i over the k-th run of
+      32 values, accumulated in index order from 0;
+    * n16 = fp16(min(sqrt(S), 65504)); nf = float(n16);
+    * u_i = y_i / nf (0 when nf = 0); index_i = the number of thresholds
+      strictly below u_i.
+    """
+    y = np.asarray(y, np.float32)
+    _, thr = tbq4_codebook()
+    sq = (y * y).astype(np.float32).reshape(*y.shape[:-1], 4, 32)
+    p = np.zeros(sq.shape[:-1], np.float32)
+    for e in range(32):
+        p = (p + sq[..., e]).astype(np.float32)
+    S = ((p[..., 0] + p[..., 1]).astype(np.float32) + (p[..., 2] + p[..., 3]).astype(np.float32)).astype(np.float32)
+    n16 = np.minimum(np.sqrt(S).astype(np.float32), np.float32(65504.0)).astype(np.float16)
+    nf = n16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        u = np.where(nf > 0, np.divide(y, nf, dtype=np.float32), np.float32(0.0))
+    idx = (u[..., None] > thr).sum(axis=-1).astype(np.uint8)
+    return n16, idx
+
+
+def tbq4_dequantize_f64(n16: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """centroid (fp32 table) * norm, exact in fp64."""
+    cent, _ = tbq4_codebook()
+    return cent.astype(np.float64)[np.asarray(idx, np.int64)] * np.asarray(n16, np.float16).astype(np.float64)[..., None]
+
+
+# ----------------------------------------------------------------------------
 # Packing
 # ----------------------------------------------------------------------------
 
@@ -425,10 +526,15 @@ def unpack(payload: np.ndarray, bits: int, G: int) -> np.ndarray:
     raise ValueError(bits)
 
 
-def encode_blocks(x: np.ndarray, bits: int) -> np.ndarray:
+def encode_blocks(x: np.ndarray, bits: int, codebook: bool = False) -> np.ndarray:
     """fp32 blocks [..., G] -> bytes [..., block_bytes]: fp16 scale (little
-    endian) then the packed codes."""
-    s16, codes = quantize(x, bits)
+    endian) then the packed codes.  codebook: TBQ4 blocks (the fp16 is the
+    norm, the nibbles are centroid indices 0..15)."""
+    if codebook:
+        s16, idx = tbq4_quantize(x)
+        codes = idx.astype(np.int64) - 8
+    else:
+        s16, codes = quantize(x, bits)
     sb = np.asarray(s16, np.float16).reshape(*s16.shape, 1).view(np.uint8)
     return np.concatenate([sb, pack(codes, bits)], axis=-1)
 
@@ -509,7 +615,11 @@ def _rotation_for(cfg: Config, which: str) -> bool:
     return bool(cfg.flags & (ROTATE_K if which == "k" else ROTATE_V))
 
 
-def quantize_rows(cfg: Config, fmt: Fmt, x: np.ndarray, rotate: bool, signs) -> np.ndarray:
+def _codebook_for(cfg: Config, which: str) -> bool:
+    return bool(cfg.flags & (TBQ4_K if which == "k" else TBQ4_V))
+
+
+def quantize_rows(cfg: Config, fmt: Fmt, x: np.ndarray, rotate: bool, signs, codebook: bool = False) -> np.ndarray:
     """fp32 values [n_tok, H_kv, D] -> storage rows.
 
     Per-token: [n_tok, H_kv, row], each token on its own (rotated first when
@@ -522,7 +632,7 @@ def quantize_rows(cfg: Config, fmt: Fmt, x: np.ndarray, rotate: bool, signs) -> 
         if rotate:
             x = rotate_f32(x, *signs)
         blocks = x.reshape(*x.shape[:-1], D // fmt.group, fmt.group)
-        return encode_blocks(blocks, fmt.bits).reshape(*x.shape[:-1], -1)
+        return encode_blocks(blocks, fmt.bits, codebook).reshape(*x.shape[:-1], -1)
     G = fmt.group
     n_units = x.shape[0] // G
     xt = np.transpose(x.reshape(n_units, G, x.shape[1], D), (0, 2, 3, 1))  # [u, H, D, G]
@@ -636,7 +746,7 @@ def append(cfg: Config, bufs: Dict[str, np.ndarray], layer: int, k_new: np.ndarr
                 if (~old).any():
                     raw[~old] = new[t[~old] - T0]
                 x = input_to_f32(raw, cfg.in_dtype)
-                rows = quantize_rows(cfg, fmt, x, _rotation_for(cfg, which), signs)
+                rows = quantize_rows(cfg, fmt, x, _rotation_for(cfg, which), signs, _codebook_for(cfg, which))
                 split = min(max(c1, q0), q1) if tiered else q0  # units below `split` go cold
                 ns = (split - q0) // gam if per_ch else split - q0
                 if ns > 0:
@@ -711,7 +821,10 @@ def dequantize(cfg: Config, bufs: Dict[str, np.ndarray], layer: int, seq: int, T
                 bb = block_bytes(f.bits, f.group)
                 s16, codes = decode_blocks(rows.reshape(hi - lo, len(heads), cfg.D // f.group, bb),
                                            f.bits, f.group)
-                val = dequantize_f64(s16, codes).reshape(hi - lo, len(heads), cfg.D)
+                if _codebook_for(cfg, which):
+                    val = tbq4_dequantize_f64(s16, codes.astype(np.int64) + 8).reshape(hi - lo, len(heads), cfg.D)
+                else:
+                    val = dequantize_f64(s16, codes).reshape(hi - lo, len(heads), cfg.D)
                 if _rotation_for(cfg, which):
                     val = unrotate_f64(val, *signs)
                 res[lo - t0:hi - t0] = val

@@ -1,0 +1,107 @@
+"""Pins of the oracle's TBQ4 codec (trefon.com, "Jak 4-bitowemu cache to
+uchodzi: najpierw obrot": rotated 128-value blocks stored as an fp16 L2 norm
+plus 4-bit indices of the 16 Lloyd-Max centroids of N(0, 1/128)).
+
+* Lloyd-Max: the optimality conditions (centroid = conditional mean between
+  its thresholds, threshold = midpoint), checked by numerical quadrature of
+  the density, independent of the closed form the iteration uses; the
+  2-level quantizer's known centroids +-sigma*sqrt(2/pi); symmetry.
+* Encoder: every index is the nearest centroid of u = y / norm (brute force
+  over all 16); the norm is the block's L2 norm to fp16 rounding; the
+  relative distortion on Gaussian blocks is the 16-level Lloyd-Max
+  distortion.
+* Cache: the dequantized keys of a TBQ4 cache are the original keys to that
+  distortion, rotation undone.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+from oracle import kvq_oracle as O
+
+SIGMA = 1.0 / math.sqrt(128.0)
+
+
+def test_two_level_closed_form():
+    c, t, _ = O.lloyd_max_normal(levels=2, sigma=1.0)
+    assert np.allclose(c, [-math.sqrt(2 / math.pi), math.sqrt(2 / math.pi)], rtol=0, atol=1e-14)
+    assert t.tolist() == [0.0]
+
+
+def test_sixteen_levels_fixed_point_by_quadrature():
+    integrate = pytest.importorskip("scipy.integrate")
+    c, t, it = O.lloyd_max_normal(levels=16, sigma=1.0)
+    assert it < 100000
+    pdf = lambda x: math.exp(-0.5 * x * x) / math.sqrt(2 * math.pi)  # noqa: E731
+    edges = [-math.inf] + t.tolist() + [math.inf]
+    for k in range(16):
+        num = integrate.quad(lambda x: x * pdf(x), edges[k], edges[k + 1], epsabs=1e-14, epsrel=1e-13)[0]
+        den = integrate.quad(pdf, edges[k], edges[k + 1], epsabs=1e-14, epsrel=1e-13)[0]
+        assert abs(num / den - c[k]) < 1e-10, (k, num / den, c[k])
+    assert np.allclose(t, (c[:-1] + c[1:]) / 2, rtol=0, atol=0)
+    assert np.array_equal(c, -c[::-1]) and np.all(np.diff(c) > 0)
+
+
+def test_codebook_scales_with_sigma():
+    c1, _, _ = O.lloyd_max_normal(16, 1.0)
+    cs, _, _ = O.lloyd_max_normal(16, SIGMA)
+    assert np.allclose(cs, c1 * SIGMA, rtol=1e-15, atol=0)
+    cent, thr = O.tbq4_codebook()
+    assert cent.dtype == np.float32 and thr.dtype == np.float32
+    assert np.array_equal(cent, cs.astype(np.float32))
+
+
+def test_indices_are_nearest_centroids_and_norm_is_l2():
+    rng = np.random.default_rng(3)
+    cent, _ = O.tbq4_codebook()
+    y = (rng.standard_normal((500, 128)) * rng.lognormal(0, 2, (500, 1))).astype(np.float32)
+    y[0] = 0.0  # zero block: norm 0, every value decodes to 0
+    n16, idx = O.tbq4_quantize(y)
+    nf = n16.astype(np.float32)
+    norm = np.sqrt((y.astype(np.float64) ** 2).sum(-1))
+    big = norm > 1e-3
+    assert np.all(np.abs(nf[big] - norm[big]) <= np.abs(norm[big]) * 2.0 ** -11 * 1.01)
+    assert nf[0] == 0 and np.all(O.tbq4_dequantize_f64(n16[:1], idx[:1]) == 0)
+    u = np.divide(y[1:], nf[1:, None], dtype=np.float32).astype(np.float64)
+    d = np.abs(u[..., None] - cent.astype(np.float64))
+    best = d.min(-1)
+    chosen = np.take_along_axis(d, idx[1:, :, None].astype(np.int64), -1)[..., 0]
+    assert np.all(chosen <= best + 1e-7)
+
+
+def test_distortion_is_lloyd_max():
+    rng = np.random.default_rng(4)
+    y = rng.standard_normal((4000, 128)).astype(np.float32)
+    n16, idx = O.tbq4_quantize(y)
+    xh = O.tbq4_dequantize_f64(n16, idx)
+    rel = ((xh - y) ** 2).sum() / (y.astype(np.float64) ** 2).sum()
+    c, t, _ = O.lloyd_max_normal(16, 1.0)
+    # the quantizer's own MSE for N(0, 1), by quadrature of (z - c_k)^2
+    integrate = pytest.importorskip("scipy.integrate")
+    pdf = lambda x: math.exp(-0.5 * x * x) / math.sqrt(2 * math.pi)  # noqa: E731
+    edges = [-math.inf] + t.tolist() + [math.inf]
+    mse = sum(integrate.quad(lambda x, k=k: (x - c[k]) ** 2 * pdf(x), edges[k], edges[k + 1])[0] for k in range(16))
+    assert abs(rel - mse) < 0.03 * mse, (rel, mse)
+
+
+def test_tbq4_cache_round_trip():
+    cfg = O.Config(L=1, H_kv=2, H_q=4, D=256, batch=1, max_T=64, in_dtype=O.DT_F16, k_fmt=O.Fmt(4, 128),
+                   v_fmt=O.Fmt(4, 128), flags=O.ROTATE_K | O.ROTATE_V | O.TBQ4_K | O.TBQ4_V, sign_seed=7)
+    bufs = O.new_buffers(cfg)
+    rng = np.random.default_rng(5)
+    k = rng.standard_normal((40, 2, 256)).astype(np.float16)
+    v = rng.standard_normal((40, 2, 256)).astype(np.float16)
+    O.append(cfg, bufs, 0, k.view(np.uint16), v.view(np.uint16), [40], [0])
+    K, V = O.dequantize(cfg, bufs, 0, 0, 40)
+    for got, ref in ((K, k), (V, v)):
+        ref = ref.astype(np.float64)
+        rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+        assert 0.08 < rel < 0.11, rel
+    # bytes: the scale slot holds the rotated block's norm
+    rot = O.rotate_f32(k.astype(np.float32), *O.hadamard_signs(7))
+    n16, idx = O.tbq4_quantize(rot.reshape(40, 2, 2, 128))
+    rows = bufs["k_main"][0, 0, :, :40]  # [H, T, row]
+    got = np.moveaxis(rows, 0, 1).reshape(40, 2, 2, 66)
+    assert np.array_equal(got[..., :2].copy().view(np.float16)[..., 0], n16)
