@@ -32,7 +32,8 @@ What it computes, step by step, with the page each step follows:
   (fp16) and, per value, the 4-bit index of the nearest of the 16 Lloyd-Max
   centroids for N(0, sigma^2), sigma = 1/sqrt(128); the centroids come from
   Lloyd's algorithm run here in fp64 (S. P. Lloyd, "Least squares
-  quantization in PCM", 1982; J. Max, 1960).
+  quantization in PCM", 1982; J. Max, 1960) and the lookup table holds them
+  rounded to fp16.
 * Decode attention, the plain definition in fp64: s_i = q.k_i / sqrt(D),
   p = softmax(s), output = sum_i p_i v_i (nalar.dev, sections "Error pada key
   mengubah input softmax" and "Error pada value masuk setelah attention
@@ -430,12 +431,16 @@ _CODEBOOK = None
 
 
 def tbq4_codebook() -> Tuple[np.ndarray, np.ndarray]:
-    """The format's tables: the 16 centroids and 15 decision thresholds
-    (midpoints computed in fp64), each rounded once to fp32."""
+    """The format's tables, as fp32 arrays: the 16-entry centroid table holds
+    the fp64 Lloyd-Max centroids rounded once to fp16 (the decoder's lookup
+    table); the 15 decision thresholds are the midpoints of neighbouring table
+    entries (exact in fp32)."""
     global _CODEBOOK
     if _CODEBOOK is None:
-        c, t, _ = lloyd_max_normal()
-        _CODEBOOK = (c.astype(np.float32), t.astype(np.float32))
+        c, _, _ = lloyd_max_normal()
+        c16 = c.astype(np.float16).astype(np.float64)
+        t = (c16[:-1] + c16[1:]) / 2.0
+        _CODEBOOK = (c16.astype(np.float32), t.astype(np.float32))
     return _CODEBOOK
 
 
@@ -465,7 +470,7 @@ def tbq4_quantize(y: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
 
 
 def tbq4_dequantize_f64(n16: np.ndarray, idx: np.ndarray) -> np.ndarray:
-    """centroid (fp32 table) * norm, exact in fp64."""
+    """table entry (an fp16 value) * norm, exact in fp64."""
     cent, _ = tbq4_codebook()
     return cent.astype(np.float64)[np.asarray(idx, np.int64)] * np.asarray(n16, np.float16).astype(np.float64)[..., None]
 

@@ -50,7 +50,11 @@ def test_codebook_scales_with_sigma():
     assert np.allclose(cs, c1 * SIGMA, rtol=1e-15, atol=0)
     cent, thr = O.tbq4_codebook()
     assert cent.dtype == np.float32 and thr.dtype == np.float32
-    assert np.array_equal(cent, cs.astype(np.float32))
+    # the table holds the centroids rounded to fp16 (nearest), thresholds are
+    # the exact midpoints of neighbouring entries
+    assert np.array_equal(cent, cs.astype(np.float16).astype(np.float32))
+    assert np.all(np.abs(cent.astype(np.float64) - cs) <= np.abs(cs) * 2.0 ** -11)
+    assert np.array_equal(thr.astype(np.float64), (cent[:-1].astype(np.float64) + cent[1:]) / 2)
 
 
 def test_indices_are_nearest_centroids_and_norm_is_l2():
