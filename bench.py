@@ -319,6 +319,18 @@ def run_ours(args):
     h2d = (dk.numel() + dv.numel() + dq.numel()) * 2
     d2h = hout.numel() * 4
 
+    # ---- the same decode as L single-layer calls (one round after a warm round)
+    per_layer_ms = None
+    if L > 1:
+        for rnd in range(2):
+            p0, p1 = torch.cuda.Event(True), torch.cuda.Event(True)
+            p0.record(stream)
+            for l in range(L):
+                cache.decode(l, 1, qs[0][l:l + 1], seq_lens, out[l:l + 1], 0, stream)
+            p1.record(stream)
+            torch.cuda.synchronize()
+        per_layer_ms = p0.elapsed_time(p1)
+
     # ---- CPU oracle on a bounded sample ------------------------------------
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -345,7 +357,8 @@ def run_ours(args):
                    "decode_launch": "one multi-layer launch",
                    "l2": "inputs larger than L2 (cache %.2f GB)" % (K.kvq_cache_bytes(cfg, w.lengths[0]) * B / 1e9),
                    "parallelism": f"replicas x{ws}"},
-        "decode": {"GBps": round(achieved, 2), "pct_of_peak": round(100 * achieved / peak, 2),
+        "decode": {"per_layer_calls_ms": None if per_layer_ms is None else round(per_layer_ms, 4),
+                   "GBps": round(achieved, 2), "pct_of_peak": round(100 * achieved / peak, 2),
                    "ms_per_launch": round(statistics.mean(dec_ms), 4),
                    "tokens_per_s": round(B / statistics.mean(dec_ms) * 1e3, 2)},
         "append": {"GBps": round(append_gbs, 2), "pct_of_peak": round(100 * append_gbs / peak, 2),
@@ -434,14 +447,43 @@ def _traffic(workload: str, layers: int):
     return round(rec["bytes_per_layer"] * layers)
 
 
+def _cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
+_ONE_THREAD = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+
+
+def _oracle_samples_subprocess(workload: str, heads: int, runs):
+    """_oracle_sample for each (T, seed) of `runs`, in one fresh interpreter
+    whose BLAS runs one thread.  Returns [(seconds, packed bytes)]."""
+    code = ("import json, bench; from bit_kv_cache_04_gb300 import workloads as W; "
+            f"w = W.make({workload!r}, extra_tokens=0); "
+            f"print(json.dumps([bench._oracle_sample(w, {heads}, T, seed) for T, seed in {list(runs)!r}]))")
+    env = dict(os.environ, **_ONE_THREAD)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       cwd=os.path.dirname(os.path.abspath(__file__)), check=True)
+    return [tuple(x) for x in json.loads(r.stdout.strip().splitlines()[-1])]
+
+
 def cpu_baseline(w, cache=None, seq_lens=None, heads=2):
     T = w.lengths[0]
-    dt, nbytes = _oracle_sample(w, heads, T)
+    dt, nbytes = _oracle_samples_subprocess(w.name, heads, [(T, 0)])[0]
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
             "kind": "oracle",
             "sample": f"layer 0, sequence 0, {heads} of {w.cfg.H_kv} kv heads, T={T}: oracle quantize-on-append "
-                      f"(fp32) + fp64 decode attention; {nbytes} packed bytes in {dt:.2f} s; numpy, one thread "
-                      f"for the elementwise work ({os.cpu_count()} host cores present)"}
+                      f"(fp32) + fp64 decode attention; {nbytes} packed bytes in {dt:.2f} s; numpy with one "
+                      f"thread (BLAS included)",
+            "cpu_model": _cpu_model(), "host_cores": os.cpu_count()}
 
 
 # ---------------------------------------------------------------------------
@@ -458,13 +500,10 @@ def run_reference(args):
     w = W.make(args.workload, extra_tokens=0)
     T = w.lengths[0]
     heads = min(8, w.cfg.H_kv)
-    for _ in range(args.warmup):
-        _oracle_sample(w, heads, T // 8)
-    total_b = total_t = 0.0
-    for i in range(args.steps):
-        dt, nb = _oracle_sample(w, heads, T, seed=i)
-        total_b += nb
-        total_t += dt
+    runs = [(T // 8, 0)] * args.warmup + [(T, i) for i in range(args.steps)]
+    res = _oracle_samples_subprocess(args.workload, heads, runs)[args.warmup:]
+    total_t = sum(dt for dt, _ in res)
+    total_b = sum(nb for _, nb in res)
     value = total_b / total_t / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_t / args.steps * 1e3, 3),
@@ -472,7 +511,9 @@ def run_reference(args):
             "data": "synthetic (seeded)",
             "config": {"workload": args.workload, "sample": f"layer 0, sequence 0, {heads} kv heads, T={T}"},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"per step: oracle append + fp64 decode of {heads} kv heads over {T} tokens"},
+                             "sample": f"per step: oracle append + fp64 decode of {heads} kv heads over {T} tokens "
+                                       f"(numpy, one thread, BLAS included)",
+                             "cpu_model": _cpu_model(), "host_cores": os.cpu_count()},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 

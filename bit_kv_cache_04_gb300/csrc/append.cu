@@ -15,6 +15,8 @@
 // "KV Cache Quantization", "Tai sao Key va Value lai khac nhau?"); rotated
 // formats pass each token's 128-chunks through the randomized Hadamard
 // transform first (trefon.com "Matematyka cache KV", "najpierw obrot").
+#include <algorithm>
+
 #include "append_common.cuh"
 
 namespace kvq {
@@ -333,9 +335,43 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_quantize_kernel(Appe
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
       }
+      // TBQ4: sum of squares of the 128-value block, in the format's order
+      // (each slice in index order, then (s0 + s1) + (s2 + s3))
+      float ss = 0.f;
+      if (f.codebook) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ss = __fadd_rn(ss, __fmul_rn(v[e], v[e]));
+        ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 1));
+        ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 2));
+      }
       if (!valid) continue;
       const int t = u0 + j;
       const int b = sl / spb, within = sl % spb;  // block, slice within the block
+      if (f.codebook) {
+        bool bad = false;
+        uint8_t* row = main_row(lo, a.cp, which, layer, seq, h, t, &bad);
+        if (bad) {
+          page_bad = 1;
+          continue;
+        }
+        uint8_t* blk = row + b * f.bb;
+        const __half n16 = __float2half_rn(fminf(__fsqrt_rn(ss), 65504.0f));
+        const float nf = __half2float(n16);
+        uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float u = nf > 0.f ? __fdiv_rn(v[e], nf) : 0.f;
+          w[e >> 3] |= tbq4_index(u, lo.cbt) << (4 * (e & 7));
+        }
+        if (within == 0) *reinterpret_cast<__half*>(blk) = n16;
+        uint16_t* p = reinterpret_cast<uint16_t*>(blk + 2 + within * 16);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          p[2 * k] = (uint16_t)w[k];
+          p[2 * k + 1] = (uint16_t)(w[k] >> 16);
+        }
+        continue;
+      }
       if (to_cold) {
         // tiers keep the hot group size; per-token tiers use 32-value blocks
         float dq[32];
@@ -412,9 +448,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_window_kernel(AppendArg
   const int layer = a.layer0 + li;
   SeqSpan s = read_span(a, seq);
   if (!s.ok) return;
+  // at most R + Gamma - 1 tokens stay in the window: the grid covers that
+  // span from its first token
   const int w0 = max(s.T0, q_end_of(lo, s.T1));
-  const int t0 = s.T0 + blockIdx.x * kTile;
-  const int ta = max(t0, w0), tb = min(t0 + kTile, s.T1);
+  const int ta = w0 + blockIdx.x * kTile, tb = min(ta + kTile, s.T1);
   if (ta >= tb) return;
   const int halfD = lo.D / 2;
   for (int which = 0; which < 2; ++which) {
@@ -447,7 +484,10 @@ cudaError_t launch_append_nc(const AppendArgs& a, cudaStream_t st) {
   }
   if (lo.tiered) append_requant_kernel<NC><<<grid, kAppendThreads, 0, st>>>(a);
   if (!launch_fast_quantize(a, st)) append_quantize_kernel<NC, ROT><<<grid, kAppendThreads, smem, st>>>(a);
-  if (lo.ring) append_window_kernel<<<grid, kAppendThreads, 0, st>>>(a);
+  if (lo.ring) {
+    const int wchunks = (std::min(a.max_new, lo.ring) + kTile - 1) / kTile;
+    append_window_kernel<<<dim3(wchunks, lo.H, a.n_layers * lo.B), kAppendThreads, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

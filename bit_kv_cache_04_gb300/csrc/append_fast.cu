@@ -133,11 +133,6 @@ __device__ __forceinline__ void hot_or_cold(float (&v)[32], bool to_cold, uint8_
   block32<B>(v, amax_of(v), dst, nullptr);
 }
 
-__device__ __forceinline__ const uint16_t* src_row(const AppendArgs& a, int which, int li, int layer, const SeqSpan& s,
-                                                   int seq, int h, int t) {
-  return t < s.T0 ? resid_row(a.lo, a.cp, which, layer, seq, h, t) : input_row(a, which, li, s, h, t);
-}
-
 // Copies `bytes` (a multiple of 4) from shared `src` to global `dst` (4-byte
 // aligned) with all threads of the block; 16-byte words when both allow.
 __device__ __forceinline__ void block_copy_out(uint8_t* dst, const uint8_t* src, int bytes) {
@@ -150,15 +145,19 @@ __device__ __forceinline__ void block_copy_out(uint8_t* dst, const uint8_t* src,
   }
 }
 
-// Per-token 32-value blocks: thread = (token row j, 32-value slice sl), rows
-// on neighbouring lanes.  The chunk's rows are built in shared memory and
-// written out as whole rows.
+// Per-token 32-value blocks: a block of 128 threads takes 128 consecutive
+// tokens of one (layer, sequence, kv head); thread j quantizes token row j
+// slice by slice, loading the next slice while it works on the current one.
+// The rows are built in shared memory and written out whole.
+constexpr int kTokItem = 128;
+
 template <int NC, int DT, int B, int CB, int which>
 __global__ void __launch_bounds__(kAppendThreads) quant_token32_kernel(AppendArgs a) {
   constexpr int D = 128 * NC, SPR = D / 32;
   constexpr int BB = 2 + 4 * B, ROW = SPR * BB;
   constexpr int CBB = CB ? 2 + 4 * CB : 0, CROW = SPR * CBB;
-  constexpr int OUTB = kTile * (ROW > CROW ? ROW : CROW);
+  constexpr int OUTB = kTokItem * (ROW > CROW ? ROW : CROW);
+  static_assert(kTokItem == kAppendThreads, "one token row per thread");
   __shared__ __align__(16) uint8_t out[OUTB];
   __shared__ uint32_t page_bad;
   const Layout& lo = a.lo;
@@ -167,32 +166,46 @@ __global__ void __launch_bounds__(kAppendThreads) quant_token32_kernel(AppendArg
   SeqSpan s = read_span(a, seq);
   if (!s.ok) return;
   const int q0 = q_end_of(lo, s.T0), q1 = q_end_of(lo, s.T1), c1 = c_end_of(lo, s.T1);
-  const int base = (q0 / kTile) * kTile + blockIdx.x * kTile;
-  const int u0 = max(base, q0), u1 = min(base + kTile, q1);
+  const int base = (q0 / kTokItem) * kTokItem + blockIdx.x * kTokItem;
+  const int u0 = max(base, q0), u1 = min(base + kTokItem, q1);
   if (u0 >= u1) return;
   const int n_tok = u1 - u0;
-  const bool to_cold = CB != 0 && lo.tiered && u0 < c1;  // tiered chunks are whole groups
-  const int rowb = to_cold ? CROW : ROW;
   if (threadIdx.x == 0) page_bad = 0;
-  for (int u = threadIdx.x; u < kTile * SPR; u += blockDim.x) {
-    const int j = u % kTile, sl = u / kTile;
-    if (j >= n_tok) continue;
-    const uint4* src = reinterpret_cast<const uint4*>(src_row(a, which, li, layer, s, seq, h, u0 + j) + 32 * sl);
-    uint4 r[4];
+  const int j = threadIdx.x;
+  const int t = u0 + j;
+  // tiered chunks start at multiples of 32 (Gamma = 32), and cold rows come
+  // before hot rows, so rows of both strides never overlap in the tile
+  const bool to_cold = CB != 0 && lo.tiered && t < c1;
+  if (j < n_tok) {
+    const uint4* src = reinterpret_cast<const uint4*>(t < s.T0 ? resid_row(lo, a.cp, which, layer, seq, h, t)
+                                                                 : input_row(a, which, li, s, h, t));
+    uint8_t* dst = out + j * (to_cold ? CROW : ROW);
+    uint4 cur[4], nxt[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) r[k] = src[k];
-    float v[32];
+    for (int q = 0; q < 4; ++q) cur[q] = src[q];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t ww[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
+    for (int sl = 0; sl < SPR; ++sl) {
+      if (sl + 1 < SPR) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = raw_pair_to_f32<DT>(ww[e]);
-        v[8 * k + 2 * e] = f.x;
-        v[8 * k + 2 * e + 1] = f.y;
+        for (int q = 0; q < 4; ++q) nxt[q] = src[4 * (sl + 1) + q];
+      }
+      float v[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t ww[4] = {cur[q].x, cur[q].y, cur[q].z, cur[q].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = raw_pair_to_f32<DT>(ww[e]);
+          v[8 * q + 2 * e] = f.x;
+          v[8 * q + 2 * e + 1] = f.y;
+        }
+      }
+      hot_or_cold<B, CB>(v, to_cold, dst + sl * BB, dst + sl * CBB);
+      if (sl + 1 < SPR) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
       }
     }
-    hot_or_cold<B, CB>(v, to_cold, out + j * ROW + sl * BB, out + j * CROW + sl * CBB);
   }
   __syncthreads();
   if (!lo.paged && !lo.tiered) {
@@ -200,43 +213,52 @@ __global__ void __launch_bounds__(kAppendThreads) quant_token32_kernel(AppendArg
     block_copy_out(main_row(lo, a.cp, which, layer, seq, h, u0, &bad), out, n_tok * ROW);
     return;
   }
+  // tiered or paged: whole rows, one warp per row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int j = warp; j < n_tok; j += kAppendThreads / 32) {
+  for (int r = warp; r < n_tok; r += kAppendThreads / 32) {
+    const bool cold = CB != 0 && lo.tiered && u0 + r < c1;
+    const int rowb = cold ? CROW : ROW;
     bool bad = false;
-    uint8_t* dst = to_cold ? cold_row(lo, a.cp, which, layer, seq, h, u0 + j)
-                           : main_row(lo, a.cp, which, layer, seq, h, u0 + j, &bad);
+    uint8_t* dst = cold ? cold_row(lo, a.cp, which, layer, seq, h, u0 + r)
+                        : main_row(lo, a.cp, which, layer, seq, h, u0 + r, &bad);
     if (bad) {
       page_bad = 1;
       continue;
     }
     for (int e = lane; e < rowb / 4; e += 32)
-      reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(out + j * rowb)[e];
+      reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(out + r * rowb)[e];
   }
   __syncthreads();
   if (threadIdx.x == 0 && page_bad) atomicOr(a.status, KVQ_DEV_PAGE);
 }
 
-// Per-channel blocks over 32-token groups: thread = (group, channel pair),
-// GPC groups per block.  Each group row (D blocks) is built in shared memory
-// and written out whole.
+// Per-channel blocks over 32-token groups: thread = (group lane, channel
+// pair); a block takes NG = GPC x kGroupSteps consecutive groups, each thread
+// kGroupSteps of them in turn.  Each group row (D blocks) is built in shared
+// memory and written out whole.
+constexpr int kGroupSteps = 2;
+
 template <int NC, int DT, int B, int CB, int which>
-__global__ void __launch_bounds__(kAppendThreads) quant_channel32_kernel(AppendArgs a) {
-  constexpr int D = 128 * NC, PAIRS = D / 2, GPC = kAppendThreads / PAIRS;
+__global__ void __launch_bounds__(kAppendThreads, 4) quant_channel32_kernel(AppendArgs a) {
+  constexpr int D = 128 * NC, PAIRS = D / 2, GPC = kAppendThreads / PAIRS, NG = GPC * kGroupSteps;
   constexpr int BB = 2 + 4 * B, GROW = D * BB;
   constexpr int CBB = CB ? 2 + 4 * CB : 0, CGROW = D * CBB;
   constexpr int SLOT = GROW > CGROW ? GROW : CGROW;
-  __shared__ __align__(16) uint8_t out[GPC * SLOT];
+  __shared__ __align__(16) uint8_t out[NG * SLOT];
   const Layout& lo = a.lo;
   const int li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B, h = blockIdx.y;
   const int layer = a.layer0 + li;
   SeqSpan s = read_span(a, seq);
   if (!s.ok) return;
   const int q0 = q_end_of(lo, s.T0), q1 = q_end_of(lo, s.T1), c1 = c_end_of(lo, s.T1);
-  const int base = (q0 / (kTile * GPC)) * (kTile * GPC) + blockIdx.x * (kTile * GPC);
-  if (base + kTile * GPC <= q0 || base >= q1) return;
-  const int gi = threadIdx.x / PAIRS, cp = threadIdx.x % PAIRS;
-  const int t0 = base + kTile * gi;
-  if (t0 >= q0 && t0 < q1) {
+  const int base = (q0 / (kTile * NG)) * (kTile * NG) + blockIdx.x * (kTile * NG);
+  if (base + kTile * NG <= q0 || base >= q1) return;
+  const int gl = threadIdx.x / PAIRS, cp = threadIdx.x % PAIRS;
+#pragma unroll 1
+  for (int gs = 0; gs < kGroupSteps; ++gs) {
+    const int gi = gs * GPC + gl;
+    const int t0 = base + kTile * gi;
+    if (t0 < q0 || t0 >= q1) continue;
     const bool to_cold = CB != 0 && lo.tiered && t0 < c1;
     // the group's rows: window ring slots for tokens below T0, new input rows
     // (a fixed stride apart) from T0 on
@@ -271,7 +293,7 @@ __global__ void __launch_bounds__(kAppendThreads) quant_channel32_kernel(AppendA
   }
   __syncthreads();
 #pragma unroll
-  for (int g = 0; g < GPC; ++g) {
+  for (int g = 0; g < NG; ++g) {
     const int tg = base + kTile * g;
     if (tg < q0 || tg >= q1) continue;
     const bool cold = CB != 0 && lo.tiered && tg < c1;
@@ -283,7 +305,7 @@ __global__ void __launch_bounds__(kAppendThreads) quant_channel32_kernel(AppendA
 
 template <int NC, int DT, int B, int CB>
 void launch_token32(const AppendArgs& a, int which, cudaStream_t st) {
-  const int chunks = (a.max_new + kTile - 1) / kTile + 2;
+  const int chunks = (a.max_new + kTokItem - 1) / kTokItem + 2;
   const dim3 grid(chunks, a.lo.H, a.n_layers * a.lo.B);
   if (which == 0) quant_token32_kernel<NC, DT, B, CB, 0><<<grid, kAppendThreads, 0, st>>>(a);
   else quant_token32_kernel<NC, DT, B, CB, 1><<<grid, kAppendThreads, 0, st>>>(a);
@@ -291,7 +313,7 @@ void launch_token32(const AppendArgs& a, int which, cudaStream_t st) {
 
 template <int NC, int DT, int B, int CB>
 void launch_channel32(const AppendArgs& a, cudaStream_t st) {
-  constexpr int span = kTile * (kAppendThreads / (64 * NC));
+  constexpr int span = kTile * (kAppendThreads / (64 * NC)) * kGroupSteps;
   const int chunks = (a.max_new + span - 1) / span + 2;
   quant_channel32_kernel<NC, DT, B, CB, 0><<<dim3(chunks, a.lo.H, a.n_layers * a.lo.B), kAppendThreads, 0, st>>>(a);
 }

@@ -161,4 +161,25 @@ __device__ __forceinline__ void dequant_block_serial(const uint8_t* blk, int G, 
   for (int i = 0; i < G; ++i) out[i * stride] = (float)unpack_code(blk + 2, bits, i) * sf;
 }
 
+// TBQ4 block (fp16 norm, 4-bit centroid indices): element i = cb[index] * norm
+// (exact: both factors are fp16 values).
+__device__ __forceinline__ void dequant_tbq4_serial(const uint8_t* blk, const float* cb, float* out, int stride) {
+  const float n = block_scale(blk);
+  for (int i = 0; i < 128; ++i) out[i * stride] = cb[(blk[2 + (i >> 1)] >> ((i & 1) * 4)) & 0xF] * n;
+}
+
+// Element i of a block (TBQ4 or uniform codes), in the stored domain.
+__device__ __forceinline__ float block_value(const uint8_t* blk, int bits, int codebook, const float* cb, int i) {
+  if (codebook) return cb[(blk[2 + (i >> 1)] >> ((i & 1) * 4)) & 0xF] * block_scale(blk);
+  return (float)unpack_code(blk + 2, bits, i) * block_scale(blk);
+}
+
+// Index of u among the 15 ascending thresholds: how many lie strictly below.
+__device__ __forceinline__ uint32_t tbq4_index(float u, const float* t) {
+  uint32_t k = 0;
+#pragma unroll
+  for (int j = 0; j < 15; ++j) k += u > t[j] ? 1u : 0u;
+  return k;
+}
+
 }  // namespace kvq

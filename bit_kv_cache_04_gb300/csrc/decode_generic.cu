@@ -75,7 +75,8 @@ __device__ void load_tile(const Layout& lo, const CachePtrs& cp, int which, int 
       for (int i = 0; i < f.group; ++i) dst[i] = 0.0f;
       continue;
     }
-    dequant_block_serial(row + (int64_t)b * f.bb, f.group, f.bits, dst, 1);
+    if (f.codebook) dequant_tbq4_serial(row + (int64_t)b * f.bb, lo.cb, dst, 1);
+    else dequant_block_serial(row + (int64_t)b * f.bb, f.group, f.bits, dst, 1);
   }
 }
 

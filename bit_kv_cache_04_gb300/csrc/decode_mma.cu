@@ -1078,6 +1078,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   bool ok = true;
   if (lo.ring) ok = ok && lo.dtype == KVQ_DT_F16 && !(lo.flags & (KVQ_ROTATE_K | KVQ_ROTATE_V));
   if (lo.paged) ok = ok && (lo.pt == 16 || lo.pt == 32);
+  if (lo.kf.codebook || lo.vf.codebook) ok = false;  // TBQ4 centroids: generic kernel
   if (!ok) return launch_decode_generic(a, st);
   const FmtInfo &k = lo.kf, &v = lo.vf;
   const bool kivi4 = fmt_is(k, 4, 32, CH) && fmt_is(v, 4, 32, TOK);

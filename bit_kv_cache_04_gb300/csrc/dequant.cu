@@ -20,7 +20,7 @@ __device__ float stored_value(const Layout& lo, const CachePtrs& cp, int which, 
     return (float)unpack_code(blk + 2, f.bits, t % f.group) * block_scale(blk);
   }
   const uint8_t* blk = row + (int64_t)(d / f.group) * f.bb;
-  return (float)unpack_code(blk + 2, f.bits, d % f.group) * block_scale(blk);
+  return block_value(blk, f.bits, f.codebook, lo.cb, d % f.group);
 }
 
 __global__ void __launch_bounds__(kThreads) dequantize_kernel(DequantArgs a) {

@@ -3,6 +3,9 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <algorithm>
+#include <cmath>
+#include <cstring>
 #include <mutex>
 #include <string>
 
@@ -71,7 +74,7 @@ kvq_status check_config(const kvq_config* c, bool allow16) {
     if (gam == 1) return fail(KVQ_ERR_UNSUPPORTED, "hot/cold tiers need a per-channel (token-group) format");
     if (c->hot_window % gam != 0) return fail(KVQ_ERR_ARG, "hot_window=%d not a multiple of %d", c->hot_window, gam);
   }
-  uint32_t known = KVQ_ROTATE_K | KVQ_ROTATE_V | KVQ_K_PRE_ROPE;
+  uint32_t known = KVQ_ROTATE_K | KVQ_ROTATE_V | KVQ_K_PRE_ROPE | KVQ_TBQ4_K | KVQ_TBQ4_V;
   if (c->flags & ~known) return fail(KVQ_ERR_ARG, "unknown flags 0x%x", c->flags & ~known);
   if ((c->flags & KVQ_ROTATE_K) && c->k_fmt.axis != KVQ_AXIS_TOKEN)
     return fail(KVQ_ERR_UNSUPPORTED, "rotation needs per-token K blocks");
@@ -80,6 +83,13 @@ kvq_status check_config(const kvq_config* c, bool allow16) {
   if ((c->flags & KVQ_ROTATE_K) && (c->flags & KVQ_K_PRE_ROPE))
     return fail(KVQ_ERR_UNSUPPORTED, "pre-RoPE keys with rotated K: RoPE pairs do not commute with the transform");
   if ((c->flags & KVQ_K_PRE_ROPE) && !(c->rope_theta > 1.0f)) return fail(KVQ_ERR_ARG, "rope_theta must be > 1");
+  for (int t = 0; t < 2; ++t) {
+    const uint32_t tb = t ? KVQ_TBQ4_V : KVQ_TBQ4_K, rb = t ? KVQ_ROTATE_V : KVQ_ROTATE_K;
+    const kvq_fmt& f = t ? c->v_fmt : c->k_fmt;
+    if (!(c->flags & tb)) continue;
+    if (!(c->flags & rb) || f.bits != 4 || f.group != 128 || f.axis != KVQ_AXIS_TOKEN || c->hot_window > 0)
+      return fail(KVQ_ERR_UNSUPPORTED, "TBQ4 needs the rotation, 4-bit per-token blocks of 128 and one tier");
+  }
   if (c->page_tokens < 0) return fail(KVQ_ERR_ARG, "page_tokens < 0");
   if (c->page_tokens > 0) {
     if (c->k_fmt.axis != KVQ_AXIS_TOKEN || c->v_fmt.axis != KVQ_AXIS_TOKEN || c->hot_window > 0)
@@ -91,8 +101,9 @@ kvq_status check_config(const kvq_config* c, bool allow16) {
   return KVQ_OK;
 }
 
-FmtInfo make_fmt(const kvq_fmt& f, int D) {
+FmtInfo make_fmt(const kvq_fmt& f, int D, bool codebook = false) {
   FmtInfo r{};
+  r.codebook = codebook ? 1 : 0;
   if (f.bits == 0) return r;
   r.bits = f.bits;
   r.group = f.group;
@@ -101,6 +112,40 @@ FmtInfo make_fmt(const kvq_fmt& f, int D) {
   r.qmax = f.bits == 16 ? 0 : qmax_of(f.bits);
   r.row = f.axis == KVQ_AXIS_TOKEN ? (D / f.group) * r.bb : D * r.bb;
   return r;
+}
+
+// Lloyd's algorithm (S. P. Lloyd 1982; J. Max 1960) for the 16-point
+// minimum-MSE quantizer of N(0, sigma^2), sigma = 1/sqrt(128), in double:
+// thresholds at the midpoints of neighbouring centroids, centroids at the
+// conditional means E[Z | a < Z < b] = (pdf(a) - pdf(b)) / (Q(a) - Q(b)) with
+// Q the upper tail, iterated on the positive half (the density is symmetric)
+// until no centroid moves by more than 1e-15 sigma.
+void lloyd_max_normal16(double* centroids) {
+  const double inv_sqrt2pi = 0.3989422804014327, inv_sqrt2 = 0.7071067811865476;
+  auto pdf = [&](double z) { return inv_sqrt2pi * std::exp(-0.5 * z * z); };
+  auto upper = [&](double z) { return 0.5 * std::erfc(z * inv_sqrt2); };
+  double c[8];
+  for (int j = 0; j < 8; ++j) c[j] = 0.5 * (j + 0.5);
+  for (int it = 0; it < 100000; ++it) {
+    double t[9];
+    t[0] = 0.0;
+    for (int j = 1; j < 8; ++j) t[j] = 0.5 * (c[j - 1] + c[j]);
+    double moved = 0.0;
+    double nc[8];
+    for (int j = 0; j < 8; ++j) {
+      const double a = t[j];
+      const double pb = j + 1 < 8 ? pdf(t[j + 1]) : 0.0, qb = j + 1 < 8 ? upper(t[j + 1]) : 0.0;
+      nc[j] = (pdf(a) - pb) / (upper(a) - qb);
+      moved = std::max(moved, std::fabs(nc[j] - c[j]));
+    }
+    for (int j = 0; j < 8; ++j) c[j] = nc[j];
+    if (moved <= 1e-15) break;
+  }
+  const double sigma = 1.0 / std::sqrt(128.0);
+  for (int j = 0; j < 8; ++j) {
+    centroids[8 + j] = c[j] * sigma;
+    centroids[7 - j] = -c[j] * sigma;
+  }
 }
 
 uint64_t splitmix64_next(uint64_t* state) {
@@ -142,8 +187,9 @@ Layout make_layout(const kvq_config* c) {
       lo.d2[j] = (uint32_t)(w[2 + j / 2] >> (32 * (j % 2)));
     }
   }
-  lo.kf = make_fmt(c->k_fmt, c->D);
-  lo.vf = make_fmt(c->v_fmt, c->D);
+  lo.kf = make_fmt(c->k_fmt, c->D, (c->flags & KVQ_TBQ4_K) != 0);
+  lo.vf = make_fmt(c->v_fmt, c->D, (c->flags & KVQ_TBQ4_V) != 0);
+  if (c->flags & (KVQ_TBQ4_K | KVQ_TBQ4_V)) tbq4_tables(lo.cb, lo.cbt);
   if (lo.tiered) {
     lo.kc = make_fmt(c->k_cold, c->D);
     lo.vc = make_fmt(c->v_cold, c->D);
@@ -266,6 +312,32 @@ kvq_status cache_ptrs(const kvq_config* c, const kvq_cache* cache, CachePtrs* cp
 }
 
 }  // namespace
+
+namespace kvq {
+
+void tbq4_tables(float* centroids, float* thresholds) {
+  static float c32[16], t32[15];
+  static std::once_flag once;
+  std::call_once(once, [] {
+    double c[16];
+    lloyd_max_normal16(c);
+    // the lookup table holds each centroid rounded to fp16 (11 significant
+    // bits, nearest, ties to even: every centroid is in fp16's normal range);
+    // the thresholds are the exact midpoints of neighbouring entries
+    double c16[16];
+    for (int i = 0; i < 16; ++i) {
+      int e = 0;
+      const double m = std::frexp(c[i], &e);  // c = m 2^e, 0.5 <= |m| < 1
+      c16[i] = std::ldexp(std::nearbyint(std::ldexp(m, 11)), e - 11);
+      c32[i] = (float)c16[i];
+    }
+    for (int i = 0; i < 15; ++i) t32[i] = (float)(0.5 * (c16[i] + c16[i + 1]));
+  });
+  std::memcpy(centroids, c32, sizeof(c32));
+  std::memcpy(thresholds, t32, sizeof(t32));
+}
+
+}  // namespace kvq
 
 extern "C" {
 
@@ -406,6 +478,12 @@ kvq_status kvq_append(const kvq_config* cfg, const kvq_cache* cache, int32_t lay
   a.status = (uint32_t*)((char*)workspace + w.status);
   cudaError_t e = launch_append(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "append kernels");
+  return ok();
+}
+
+kvq_status kvq_tbq4_codebook(float centroids[16], float thresholds[15]) {
+  if (!centroids || !thresholds) return fail(KVQ_ERR_ARG, "output pointer is NULL");
+  tbq4_tables(centroids, thresholds);
   return ok();
 }
 

@@ -27,6 +27,7 @@ struct FmtInfo {
   int bb;     // block bytes
   int qmax;   // 2^(bits-1) - 1
   int row;    // bytes of one storage row
+  int codebook;  // 1: TBQ4 blocks (fp16 L2 norm + Lloyd-Max centroid indices)
 };
 
 // Everything a kernel needs to find a byte of the cache.
@@ -47,6 +48,8 @@ struct Layout {
   int64_t rows_k_main, rows_v_main;  // rows per (layer, seq, head) of the main tier (contiguous / ring)
   int64_t rows_k_cold, rows_v_cold;
   int hot_ring_k, hot_ring_v;        // ring length of the hot tier (rows) when tiered
+  float cb[16];                      // TBQ4 centroid table (fp16 values, ascending), when used
+  float cbt[15];                     // TBQ4 decision thresholds
 };
 
 struct CachePtrs {
@@ -79,16 +82,18 @@ KVQ_HD int block_bytes_of(int bits, int group) {
 
 // ---- tier arithmetic ------------------------------------------------------
 
+// Gamma is 1 or 32 (per-channel groups are 32 tokens), so rounding down to a
+// multiple of Gamma is a mask.
 KVQ_HD int q_end_of(const Layout& lo, int T) {
   if (T <= lo.R) return 0;
-  return ((T - lo.R) / lo.gam) * lo.gam;
+  return (T - lo.R) & ~(lo.gam - 1);
 }
 
 KVQ_HD int c_end_of(const Layout& lo, int T) {
   if (lo.W <= 0) return 0;
   int qe = q_end_of(lo, T);
   if (qe <= lo.W) return 0;
-  return ((qe - lo.W) / lo.gam) * lo.gam;
+  return (qe - lo.W) & ~(lo.gam - 1);
 }
 
 // ---- addresses --------------------------------------------------------------
@@ -148,6 +153,9 @@ __device__ __forceinline__ float in_to_f32(uint16_t bits, int dtype) {
 __device__ __forceinline__ float sign_of(const uint32_t* mask, int i) {
   return ((mask[i >> 5] >> (i & 31)) & 1u) ? -1.0f : 1.0f;
 }
+
+// TBQ4 tables (host, computed once): 16 centroids, 15 thresholds, fp32.
+void tbq4_tables(float* centroids, float* thresholds);
 
 // ---- launchers (defined in the kernel translation units) -------------------
 

@@ -20,6 +20,8 @@ AXIS_CHANNEL = 1
 ROTATE_K = 1
 ROTATE_V = 2
 K_PRE_ROPE = 4
+TBQ4_K = 8
+TBQ4_V = 16
 DT_F16 = 0
 DT_BF16 = 1
 
@@ -125,6 +127,7 @@ def _load():
         "kvq_decode_attention": ([cfgp, cachep, i32, i32, vp, vp, vp, i32, vp, sz, vp], ctypes.c_int),
         "kvq_decode_splits": ([cfgp, i32, P(i32)], ctypes.c_int),
         "kvq_launch_counts": ([cfgp, P(i32), P(i32)], ctypes.c_int),
+        "kvq_tbq4_codebook": ([P(ctypes.c_float), P(ctypes.c_float)], ctypes.c_int),
         "kvq_decode_attention_static": ([cfgp, cachep, i32, i32, vp, vp, vp, i32, vp], ctypes.c_int),
         "kvq_dequantize": ([cfgp, cachep, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "kvq_read_device_status": ([vp, P(u32), vp], ctypes.c_int),
@@ -143,7 +146,7 @@ LIB = _load()
 EXPORTED = ("kvq_version", "kvq_last_error", "kvq_validate_config", "kvq_block_bytes", "kvq_bytes_per_token",
             "kvq_cache_bytes", "kvq_buffer_sizes", "kvq_workspace_bytes", "kvq_workspace_init", "kvq_append",
             "kvq_commit_lengths", "kvq_decode_attention", "kvq_decode_splits", "kvq_decode_attention_static",
-            "kvq_dequantize", "kvq_launch_counts",
+            "kvq_dequantize", "kvq_launch_counts", "kvq_tbq4_codebook",
             "kvq_read_device_status", "kvq_clear_device_status")
 
 
@@ -185,6 +188,14 @@ def kvq_buffer_sizes(cfg: Config) -> Tuple[int, ...]:
     arr = (ctypes.c_size_t * 6)()
     _check(LIB.kvq_buffer_sizes(ctypes.byref(cfg.to_c()), arr))
     return tuple(arr)
+
+
+def kvq_tbq4_codebook():
+    """(16 centroids, 15 thresholds) of the TBQ4 format, fp32 lists."""
+    c = (ctypes.c_float * 16)()
+    t = (ctypes.c_float * 15)()
+    _check(LIB.kvq_tbq4_codebook(c, t))
+    return list(c), list(t)
 
 
 def kvq_launch_counts(cfg: Config):

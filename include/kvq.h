@@ -116,7 +116,14 @@ typedef struct {
 enum {
   KVQ_ROTATE_K = 1u << 0,  /* randomized Hadamard-128 on K before quantizing (TOKEN formats) */
   KVQ_ROTATE_V = 1u << 1,  /* the same on V */
-  KVQ_K_PRE_ROPE = 1u << 2 /* K is stored pre-RoPE; decode applies split-half RoPE at position t */
+  KVQ_K_PRE_ROPE = 1u << 2, /* K is stored pre-RoPE; decode applies split-half RoPE at position t */
+  /* TBQ4 (trefon.com, "Jak 4-bitowemu cache to uchodzi: najpierw obrot"): a rotated
+   * 4-bit 128-value block holds the block's L2 norm (fp16) and, per value, the index
+   * of the nearest of the 16 Lloyd-Max centroids of N(0, 1/128) (see
+   * kvq_tbq4_codebook).  Needs the tensor's rotation flag, 4 bits, group 128,
+   * per-token blocks, one tier.  Same 66 B per 128 values. */
+  KVQ_TBQ4_K = 1u << 3,
+  KVQ_TBQ4_V = 1u << 4
 };
 
 /* Device status bits (workspace word 0), OR-ed by kernels. */
@@ -279,6 +286,17 @@ KVQ_API kvq_status kvq_decode_attention_static(const kvq_config* cfg, const kvq_
  * kvq_decode_attention call make for this configuration, e.g. to budget
  * launches per decode step.  No pages counterpart: library bookkeeping. */
 KVQ_API kvq_status kvq_launch_counts(const kvq_config* cfg, int32_t* append_launches, int32_t* decode_launches);
+
+/* The TBQ4 tables the library uses: the 16 Lloyd-Max centroids of
+ * N(0, sigma^2), sigma = 1/sqrt(128), ascending, from Lloyd's algorithm run
+ * on the host in fp64 and rounded once to fp16 (the lookup table), and the
+ * 15 decision thresholds, the exact midpoints of neighbouring entries.  A
+ * value u = y / norm (fp32, y the rotated value) takes the index of the
+ * number of thresholds strictly below u; it decodes as centroid[index] *
+ * norm.  The norm is fp16(min(sqrt(S), 65504)) with S = (p0 + p1) + (p2 + p3)
+ * in fp32, p_k the sum of y_i^2 over the k-th run of 32 values in index
+ * order.  No device work; the tables are computed once per process. */
+KVQ_API kvq_status kvq_tbq4_codebook(float centroids[16], float thresholds[15]);
 
 /* Synchronizes `stream` and reads the device status word (KVQ_DEV_* bits). */
 KVQ_API kvq_status kvq_read_device_status(const void* workspace, uint32_t* bits, void* stream);

@@ -118,3 +118,28 @@ def test_launch_counts():
     assert K.kvq_launch_counts(W.make("mistral7b_hotcold").cfg) == (1 + 2 + 1, 1)
     assert K.kvq_launch_counts(W.make("q8_0_mha_1k").cfg) == (2, 1)
     assert K.kvq_launch_counts(W.make("ctx262k_hadamard4").cfg) == (1, 1)
+
+
+def test_tbq4_codebook_matches_oracle():
+    import numpy as np
+
+    c, t = K.kvq_tbq4_codebook()
+    oc, ot = O.tbq4_codebook()
+    assert np.array_equal(np.array(c, np.float32), oc)
+    assert np.array_equal(np.array(t, np.float32), ot)
+
+
+@pytest.mark.parametrize("kw,ok", [
+    (dict(flags=K.ROTATE_K | K.TBQ4_K, k_fmt=K.Fmt(4, 128)), True),
+    (dict(flags=K.ROTATE_K | K.ROTATE_V | K.TBQ4_K | K.TBQ4_V, k_fmt=K.Fmt(4, 128), v_fmt=K.Fmt(4, 128)), True),
+    (dict(flags=K.TBQ4_K, k_fmt=K.Fmt(4, 128)), False),
+    (dict(flags=K.ROTATE_K | K.TBQ4_K, k_fmt=K.Fmt(4, 32)), False),
+    (dict(flags=K.ROTATE_V | K.TBQ4_V, v_fmt=K.Fmt(3, 128)), False),
+])
+def test_tbq4_validation(kw, ok):
+    if ok:
+        K.kvq_validate_config(_bad(**kw))
+    else:
+        with pytest.raises(K.KvqError) as e:
+            K.kvq_validate_config(_bad(**kw))
+        assert e.value.status == 2

@@ -1,5 +1,7 @@
 """Byte parity of quantize-on-append for every bit width, block axis, input
-dtype and head dim of the 32-value block formats, on two kinds of input:
+dtype and head dim of the 32-value block formats (and of TBQ4 blocks: norm +
+Lloyd-Max indices, where decode and dequantize are checked too), on two kinds
+of input:
 
 * exact ties: every block's absolute maximum is qmax * s with s a power of two
   (so s16 = s exactly) and every other value is (k + 1/2) s, so every code is
@@ -19,7 +21,7 @@ import numpy as np
 import pytest
 
 from oracle import kvq_oracle as O
-from tests.helpers import codes_differ, oracle_cfg, raw16
+from tests.helpers import codes_differ, oracle_cfg, raw16, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -108,3 +110,66 @@ def test_append_bytes_match_oracle(case, kind):
             total, diff, maxd, sdiff = codes_differ(oc, {n: got}, {n: ref[n]}) \
                 if not n.endswith("resid") else (0, -1, -1, -1)
             pytest.fail(f"{name}/{kind} {n}: bytes differ (codes {diff}/{total}, max |dc| {maxd}, scales {sdiff})")
+
+
+# ---- TBQ4 (norm + Lloyd-Max codebook) -------------------------------------------
+
+TBQ4_CASES = [
+    ("tbq4_f16_d128", 128, K.DT_F16, 0, 32),
+    ("tbq4_bf16_d256_seed", 256, K.DT_BF16, 0x5EED, 0),
+]
+
+
+@pytest.mark.parametrize("case", TBQ4_CASES, ids=[c[0] for c in TBQ4_CASES])
+def test_tbq4_bytes_decode_and_dequantize(case):
+    name, D, dtype, seed, R = case
+    flags = K.ROTATE_K | K.ROTATE_V | K.TBQ4_K | K.TBQ4_V
+    cfg = K.Config(L=1, H_kv=3, H_q=6, D=D, batch=len(LENGTHS), max_T=max(LENGTHS) + 32, in_dtype=dtype,
+                   k_fmt=K.Fmt(4, 128), v_fmt=K.Fmt(4, 128), residual_window=R, flags=flags, sign_seed=seed)
+    oc = oracle_cfg(cfg)
+    gen = torch.Generator().manual_seed(zlib.crc32(name.encode()))
+    dt = torch.float16 if dtype == K.DT_F16 else torch.bfloat16
+    ks = [_inputs("random", T, cfg.H_kv, D, 4, gen).to(dt) for T in LENGTHS]
+    vs = [_inputs("random", T, cfg.H_kv, D, 4, gen).to(dt) for T in LENGTHS]
+    cache = K.KVCache(cfg, "cuda")
+    ref = O.new_buffers(oc)
+    seq_lens = torch.zeros(cfg.batch, dtype=torch.int32, device="cuda")
+    done = [0] * cfg.batch
+    for step in (PREFIX, [T - p for T, p in zip(LENGTHS, PREFIX)]):
+        kk = torch.cat([ks[b][done[b]:done[b] + step[b]] for b in range(cfg.batch)])
+        vv = torch.cat([vs[b][done[b]:done[b] + step[b]] for b in range(cfg.batch)])
+        cu = np.concatenate([[0], np.cumsum(step)]).astype(np.int32)
+        cu_d = torch.as_tensor(cu, device="cuda")
+        cache.append(0, 1, kk[None].cuda().contiguous(), vv[None].cuda().contiguous(), cu_d, seq_lens,
+                     int(cu[-1]), max(step))
+        cache.commit_lengths(cu_d, seq_lens)
+        O.append(oc, ref, 0, raw16(kk), raw16(vv), step, done)
+        done = [d + x for d, x in zip(done, step)]
+    torch.cuda.synchronize()
+    assert cache.device_status() == 0
+    shapes = O.buffer_shapes(oc)
+    got = {}
+    for n, arr in cache.buffer_numpy().items():
+        shape, dtn = shapes[n]
+        got[n] = arr.view(dtn).reshape(shape)
+        if not np.array_equal(got[n], ref[n]):
+            total, diff, maxd, sdiff = codes_differ(oc, {n: got[n]}, {n: ref[n]}) \
+                if not n.endswith("resid") else (0, -1, -1, -1)
+            pytest.fail(f"{name} {n}: bytes differ (codes {diff}/{total}, max |dc| {maxd}, scales {sdiff})")
+    # decode over the GPU's own bytes, against fp64 attention
+    q = torch.randn((1, cfg.batch, cfg.H_q, D), generator=gen).to(dt).cuda()
+    out = torch.full((1, cfg.batch, cfg.H_q, D), float("nan"), dtype=torch.float32, device="cuda")
+    cache.decode(0, 1, q, seq_lens, out)
+    torch.cuda.synchronize()
+    o_ref = O.decode_attention(oc, got, 0, 1, raw16(q), LENGTHS)
+    assert rel_err(out.cpu().numpy(), o_ref) <= 2e-3
+    # dequantize (original domain; the GPU undoes the rotation in fp32)
+    for b, T in enumerate(LENGTHS):
+        kd = torch.empty((T, cfg.H_kv, D), dtype=torch.float32, device="cuda")
+        vd = torch.empty_like(kd)
+        cache.dequantize(0, b, 0, T, seq_lens, kd, vd)
+        torch.cuda.synchronize()
+        rk, rv = O.dequantize(oc, got, 0, b, T)
+        for g_, r_ in ((kd, rk), (vd, rv)):
+            diff = np.abs(g_.cpu().numpy().astype(np.float64) - r_)
+            assert diff.max() <= 1e-5 * max(1.0, np.abs(r_).max()), (name, b, diff.max())
