@@ -147,7 +147,7 @@ __device__ __forceinline__ void block_copy_out(uint8_t* dst, const uint8_t* src,
 
 // Per-token 32-value blocks: a block of 128 threads takes 128 consecutive
 // tokens of one (layer, sequence, kv head); thread j quantizes token row j
-// slice by slice, loading the next slice while it works on the current one.
+// slice by slice, with the loads of the following slices in flight.
 // The rows are built in shared memory and written out whole.
 constexpr int kTokItem = 128;
 
@@ -180,19 +180,21 @@ __global__ void __launch_bounds__(kAppendThreads) quant_token32_kernel(AppendArg
     const uint4* src = reinterpret_cast<const uint4*>(t < s.T0 ? resid_row(lo, a.cp, which, layer, seq, h, t)
                                                                  : input_row(a, which, li, s, h, t));
     uint8_t* dst = out + j * (to_cold ? CROW : ROW);
-    uint4 cur[4], nxt[4];
+    // PF slices of the row in flight: the whole 128-value row, or two slices
+    // of a 256-value row
+    constexpr int PF = SPR <= 4 ? SPR : 2;
+    uint4 r[PF][4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) cur[q] = src[q];
+    for (int p = 0; p < PF; ++p)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) r[p][q] = src[4 * p + q];
 #pragma unroll
     for (int sl = 0; sl < SPR; ++sl) {
-      if (sl + 1 < SPR) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) nxt[q] = src[4 * (sl + 1) + q];
-      }
       float v[32];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint32_t ww[4] = {cur[q].x, cur[q].y, cur[q].z, cur[q].w};
+        const uint4 c = r[sl % PF][q];
+        const uint32_t ww[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = raw_pair_to_f32<DT>(ww[e]);
@@ -200,11 +202,11 @@ __global__ void __launch_bounds__(kAppendThreads) quant_token32_kernel(AppendArg
           v[8 * q + 2 * e + 1] = f.y;
         }
       }
-      hot_or_cold<B, CB>(v, to_cold, dst + sl * BB, dst + sl * CBB);
-      if (sl + 1 < SPR) {
+      if (sl + PF < SPR) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
+        for (int q = 0; q < 4; ++q) r[sl % PF][q] = src[4 * (sl + PF) + q];
       }
+      hot_or_cold<B, CB>(v, to_cold, dst + sl * BB, dst + sl * CBB);
     }
   }
   __syncthreads();
