@@ -376,6 +376,8 @@ def run_ours(args):
     }
     if cpu:
         result["cpu_baseline"] = cpu
+    if args.ablation:
+        result["ablation_unfused"] = unfused_ablation(cache, cfg, w, seq_lens, stream)
     if rank == 0:
         print(json.dumps(result))
     if ws > 1:
@@ -445,6 +447,55 @@ def _traffic(workload: str, layers: int):
     if rec is None or rec["sha256"] != _kernel_sha():
         return None
     return round(rec["bytes_per_layer"] * layers)
+
+
+def unfused_ablation(cache, cfg, w, seq_lens, stream, layers=4):
+    """What fusion buys: per layer, the fused decode of one step against
+    kvq_dequantize of the whole cache to fp32 followed by dense attention
+    (torch scaled_dot_product_attention over the dequantized, rotation-undone
+    K and V; keys stored pre-RoPE are not turned, so that case times the
+    memory traffic only).  Averages over the first `layers` layers."""
+    import torch
+
+    from bit_kv_cache_04_gb300 import kvq as K
+
+    L, B, H, Hq, D = cfg.L, cfg.batch, cfg.H_kv, cfg.H_q, cfg.D
+    g = Hq // H
+    layers = min(layers, L)
+    dt = torch.float16 if cfg.in_dtype == K.DT_F16 else torch.bfloat16
+    q = torch.randn((1, B, Hq, D), device=stream.device).to(dt)
+    out = torch.empty((1, B, Hq, D), dtype=torch.float32, device=stream.device)
+    lens = seq_lens.cpu().tolist()
+    Tmax = max(lens)
+    kf = torch.empty((Tmax, H, D), dtype=torch.float32, device=stream.device)
+    vf = torch.empty_like(kf)
+    fused, deq, att = [], [], []
+    for l in range(layers):
+        for rep in range(2):  # second round timed
+            ev = [torch.cuda.Event(True) for _ in range(2 + 2 * B)]
+            ev[0].record(stream)
+            cache.decode(l, 1, q, seq_lens, out, 0, stream)
+            ev[1].record(stream)
+            with torch.cuda.stream(stream):
+                for b in range(B):
+                    T = lens[b]
+                    cache.dequantize(l, b, 0, T, seq_lens, kf[:T], vf[:T], stream)
+                    ev[2 + 2 * b].record(stream)
+                    kk = kf[:T].permute(1, 0, 2).repeat_interleave(g, 0)[None]
+                    vv = vf[:T].permute(1, 0, 2).repeat_interleave(g, 0)[None]
+                    qq = q[0, b].float()[None, :, None, :]
+                    torch.nn.functional.scaled_dot_product_attention(qq, kk, vv)
+                    ev[3 + 2 * b].record(stream)
+            torch.cuda.synchronize()
+        fused.append(ev[0].elapsed_time(ev[1]))
+        deq.append(sum(ev[(1 if b == 0 else 1 + 2 * b)].elapsed_time(ev[2 + 2 * b]) for b in range(B)))
+        att.append(sum(ev[2 + 2 * b].elapsed_time(ev[3 + 2 * b]) for b in range(B)))
+    f, d, a_ = statistics.mean(fused), statistics.mean(deq), statistics.mean(att)
+    u = d + a_
+    return {"fused_ms_per_layer": round(f, 4), "unfused_ms_per_layer": round(u, 4), "speedup": round(u / f, 2),
+            "unfused_dequantize_ms": round(d, 4), "unfused_attention_ms": round(a_, 4),
+            "what": "per layer: one fused decode launch vs kvq_dequantize (fp32) of every sequence + torch "
+                    "scaled_dot_product_attention in fp32 (GQA by repeating kv heads)", "layers": layers}
 
 
 def _cpu_model() -> str:
@@ -527,6 +578,8 @@ def main():
     ap.add_argument("--workload", default="llama2_7b_kivi4")
     ap.add_argument("--cpu-heads", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ablation", action="store_true",
+                    help="also time the unfused path: kvq_dequantize to fp32, then dense attention (torch)")
     ap.add_argument("--layers", type=int, default=0,
                     help="use only this many layers (small cases for profiler captures); 0 = the workload's")
     args = ap.parse_args()

@@ -44,8 +44,9 @@ cudaError_t launch_decode_generic(const DecodeArgs& a, cudaStream_t s);
 
 namespace {
 
-enum : int { KF_CH4 = 0, KF_T8 = 1, KF_T4 = 2, KF_T3 = 3, KF_CH2 = 4 };
-enum : int { VF_T8 = 0, VF_T4 = 1, VF_T3 = 2, VF_T2 = 3 };
+// KF_TQ / VF_TQ: TBQ4 blocks (4-bit indices into the 16-entry fp16 table).
+enum : int { KF_CH4 = 0, KF_T8 = 1, KF_T4 = 2, KF_T3 = 3, KF_CH2 = 4, KF_TQ = 5 };
+enum : int { VF_T8 = 0, VF_T4 = 1, VF_T3 = 2, VF_T2 = 3, VF_TQ = 4 };
 
 constexpr int kWarps = 4;
 constexpr int kThreadsMma = kWarps * 32;
@@ -62,6 +63,7 @@ struct Tier {
   static constexpr int KF = KF_, KG = KG_, VF = VF_, VG = VG_;
   static constexpr int KB = bits_k(KF), VB = bits_v(VF);
   static constexpr bool KCH = KF == KF_CH4 || KF == KF_CH2;
+  static constexpr bool KLUT = KF == KF_TQ, VLUT = VF == VF_TQ;  // codes index the TBQ4 table
   static constexpr int KBB = 2 + (KCH ? 32 : KG) * KB / 8;  // block bytes
   static constexpr int VBB = 2 + VG * VB / 8;
   static constexpr int KROW = KCH ? D * KBB : (D / KG) * KBB;  // group row / token row
@@ -222,11 +224,36 @@ __device__ __forceinline__ uint32_t code_pair8(uint32_t x, int j) {
   return hsub2u(((x >> (8 * j)) & 0x00FF00FFu) ^ 0x64806480u, 0x64806480u);
 }
 
+// Eight TBQ4 indices, four per 16-bit half of x (nibble j of each half), as
+// the fp16 pairs r[j] = (T[low-half nibble j], T[high-half nibble j]) of the
+// 16-entry table T.  T is symmetric (T[15 - k] = -T[k]), so an index k maps to
+// the magnitude M[k ^ (k < 8 ? 7 : 0) & 7] = T[8 + ...] with the sign of
+// bit 3; lut holds the low bytes (lut[0], lut[1]) and high bytes (lut[2],
+// lut[3]) of the eight magnitudes, looked up four at a time by byte permutes.
+__device__ __forceinline__ void dqt(uint32_t x, uint32_t (&r)[4], const uint32_t (&lut)[4]) {
+  const uint32_t neg = ~x & 0x88888888u;                         // bit 3 clear: negative entry
+  const uint32_t mx = (x ^ ((neg >> 3) * 7u)) & 0x77777777u;     // magnitude index per nibble
+  const uint32_t a = mx & 0x0F0F0F0Fu, b = (mx >> 4) & 0x0F0F0F0Fu;
+  const uint32_t c = a | (a >> 12), d = b | (b >> 12);           // byte0: (m0, m4), byte1: (m2, m6) | (m1, m5), (m3, m7)
+  const uint32_t sel[2] = {__byte_perm(c, d, 0x0040), __byte_perm(c, d, 0x0051)};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t lo = __byte_perm(lut[0], lut[1], sel[h]);     // low bytes of 4 entries
+    const uint32_t hi = __byte_perm(lut[2], lut[3], sel[h]);     // high bytes
+    const uint32_t p0 = __byte_perm(lo, hi, 0x5140), p1 = __byte_perm(lo, hi, 0x7362);
+    const int j0 = 2 * h, j1 = 2 * h + 1;
+    r[j0] = p0 | ((neg << (12 - 4 * j0)) & 0x80008000u);
+    r[j1] = p1 | ((neg << (12 - 4 * j1)) & 0x80008000u);
+  }
+}
+
 // Eight K codes (channels c0..c0+7 of one token) as four fp16 pairs
 // (c0+j, c0+j+4), j = 0..3.  `p` points at the first code byte of the span.
 template <class C>
-__device__ __forceinline__ void k_token_pairs(const uint8_t* p, int tq, uint32_t (&r)[4]) {
-  if constexpr (C::KB == 4) {
+__device__ __forceinline__ void k_token_pairs(const uint8_t* p, int tq, uint32_t (&r)[4], const uint32_t (&lut)[4]) {
+  if constexpr (C::KLUT) {
+    dqt(ld_u32e(p + 4 * tq), r, lut);
+  } else if constexpr (C::KB == 4) {
     dq4(ld_u32e(p + 4 * tq), r);
   } else if constexpr (C::KB == 8) {
     const uint32_t w0 = ld_u32e(p + 8 * tq), w1 = ld_u32e(p + 8 * tq + 4);
@@ -247,7 +274,8 @@ __device__ __forceinline__ void k_token_pairs(const uint8_t* p, int tq, uint32_t
 // four fp16 pairs (row a, row b) for channel 4gq+j.  p* point at the span's
 // first code byte of each row.
 template <class C>
-__device__ __forceinline__ void v_pair4(const uint8_t* pa, const uint8_t* pb, int gq, uint32_t (&r)[4]) {
+__device__ __forceinline__ void v_pair4(const uint8_t* pa, const uint8_t* pb, int gq, uint32_t (&r)[4],
+                                        const uint32_t (&lut)[4]) {
   if constexpr (C::VB == 8) {
     const uint32_t wa = ld_u32e(pa + 4 * gq), wb = ld_u32e(pb + 4 * gq);
     const uint32_t xa = __byte_perm(wa, wb, 0x5410), xb = __byte_perm(wa, wb, 0x7632);
@@ -269,7 +297,9 @@ __device__ __forceinline__ void v_pair4(const uint8_t* pa, const uint8_t* pb, in
       ub = pb[gq];
     }
     const uint32_t x = __byte_perm(ua, ub, 0x5410);
-    if constexpr (C::VB == 4) {
+    if constexpr (C::VLUT) {
+      dqt(x, r, lut);
+    } else if constexpr (C::VB == 4) {
       dq4(x, r);
     } else {
 #pragma unroll
@@ -344,6 +374,7 @@ struct Ctx {
   const float4* qr;       // [KC][NT][32]: fp32 query (RoPE)
   const float2* rope_base;
   const float4* rope_frag;  // [KC/2][4 tokens k][2 pairs][32 lanes]: R(j) of this lane's channels
+  uint32_t lut[4];          // TBQ4 table magnitudes: low bytes (2 words), high bytes (2 words)
 };
 
 // B fragments of the query turned by -t0 (pre-RoPE keys) for the k-chunk
@@ -426,8 +457,8 @@ __device__ __forceinline__ void pv_packed(const Ctx<C>& cx, WarpState<C>& ws, co
         for (int mu = 0; mu < 2; ++mu) {
           const int T1 = 8 * tq + 2 * mu;
           uint32_t x12[4], x34[4];
-          v_pair4<TR>(vsm + T1 * TR::VROW + off, vsm + (T1 + 4) * TR::VROW + off, gq, x12);
-          v_pair4<TR>(vsm + (T1 + 1) * TR::VROW + off, vsm + (T1 + 5) * TR::VROW + off, gq, x34);
+          v_pair4<TR>(vsm + T1 * TR::VROW + off, vsm + (T1 + 4) * TR::VROW + off, gq, x12, cx.lut);
+          v_pair4<TR>(vsm + (T1 + 1) * TR::VROW + off, vsm + (T1 + 5) * TR::VROW + off, gq, x34, cx.lut);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             mma16816(ws.o[2 * s][nt], x12[0], x12[1], x34[0], x34[1], pb[mu][nt][0], pb[mu][nt][1]);
@@ -577,8 +608,8 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
           for (int mu = 0; mu < 2; ++mu) {
             const int ra = 4 * gq + 2 * mu;
             uint32_t wa[4], wb[4];
-            k_token_pairs<TR>(ksm + ra * TR::KROW + kb * TR::KBB + 2 + ss * TR::KSPAN, tq, wa);
-            k_token_pairs<TR>(ksm + (ra + 1) * TR::KROW + kb * TR::KBB + 2 + ss * TR::KSPAN, tq, wb);
+            k_token_pairs<TR>(ksm + ra * TR::KROW + kb * TR::KBB + 2 + ss * TR::KSPAN, tq, wa, cx.lut);
+            k_token_pairs<TR>(ksm + (ra + 1) * TR::KROW + kb * TR::KBB + 2 + ss * TR::KSPAN, tq, wb, cx.lut);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               const uint2 q0 = qb[((2 * s) * NT + nt) * 32 + lane];
@@ -709,6 +740,17 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   cx.qr = qr;
   cx.rope_base = a.rope;
   cx.rope_frag = reinterpret_cast<const float4*>(a.rope + (int64_t)(a.rope_base_rows + kTile) * (D / 2));
+  if constexpr (C::HOT::KLUT || C::HOT::VLUT) {
+    uint32_t m[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m[k] = __half_as_ushort(__float2half_rn(lo.cb[8 + k]));  // exact: fp16 entries
+    cx.lut[0] = (m[0] & 0xFF) | (m[1] & 0xFF) << 8 | (m[2] & 0xFF) << 16 | (m[3] & 0xFF) << 24;
+    cx.lut[1] = (m[4] & 0xFF) | (m[5] & 0xFF) << 8 | (m[6] & 0xFF) << 16 | (m[7] & 0xFF) << 24;
+    cx.lut[2] = (m[0] >> 8) | (m[1] >> 8) << 8 | (m[2] >> 8) << 16 | (m[3] >> 8) << 24;
+    cx.lut[3] = (m[4] >> 8) | (m[5] >> 8) << 8 | (m[6] >> 8) << 16 | (m[7] >> 8) << 24;
+  } else {
+    cx.lut[0] = cx.lut[1] = cx.lut[2] = cx.lut[3] = 0;
+  }
 
   WarpState<C> ws;
 #pragma unroll
@@ -1078,8 +1120,15 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   bool ok = true;
   if (lo.ring) ok = ok && lo.dtype == KVQ_DT_F16 && !(lo.flags & (KVQ_ROTATE_K | KVQ_ROTATE_V));
   if (lo.paged) ok = ok && (lo.pt == 16 || lo.pt == 32);
-  if (lo.kf.codebook || lo.vf.codebook) ok = false;  // TBQ4 centroids: generic kernel
+  if (lo.kf.codebook != lo.vf.codebook) ok = false;  // one tensor TBQ4, the other not: generic kernel
   if (!ok) return launch_decode_generic(a, st);
+  if (lo.kf.codebook) {  // TBQ4 K and V (rotated 4-bit blocks of 128)
+    if (lo.D == 128 && lo.g <= 4)
+      return launch_mma<Cfg<128, 1, T_<128, KF_TQ, 128, VF_TQ, 128>, T_<128, KF_TQ, 128, VF_TQ, 128>, false, false>>(a, st);
+    if (lo.D == 256 && lo.g <= 8)
+      return launch_mma<Cfg<256, 2, T_<256, KF_TQ, 128, VF_TQ, 128>, T_<256, KF_TQ, 128, VF_TQ, 128>, false, false>>(a, st);
+    return launch_decode_generic(a, st);
+  }
   const FmtInfo &k = lo.kf, &v = lo.vf;
   const bool kivi4 = fmt_is(k, 4, 32, CH) && fmt_is(v, 4, 32, TOK);
   using KIVI4 = T_<128, KF_CH4, 32, VF_T4, 32>;

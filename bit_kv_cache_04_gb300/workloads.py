@@ -25,7 +25,8 @@ from typing import List, Optional
 
 import torch
 
-from .kvq import AXIS_CHANNEL, AXIS_TOKEN, DT_BF16, DT_F16, K_PRE_ROPE, ROTATE_K, ROTATE_V, Config, Fmt
+from .kvq import (AXIS_CHANNEL, AXIS_TOKEN, DT_BF16, DT_F16, K_PRE_ROPE, ROTATE_K, ROTATE_V, TBQ4_K, TBQ4_V, Config,
+                  Fmt)
 
 SIGN_SEED = 0x5EED5EED
 
@@ -76,10 +77,11 @@ def make(name: str, extra_tokens: int = 64) -> Workload:
                      k_fmt=Fmt(4, 128), v_fmt=Fmt(4, 128), flags=ROTATE_K | ROTATE_V, sign_seed=SIGN_SEED,
                      page_tokens=16, n_pages=pages, max_pages_per_seq=-(-max_T // 16))
         return Workload(name, cfg, lengths, "llama", extra_tokens)
-    if name in ("ctx262k_hadamard4", "ctx262k_hadamard3"):
-        b = 4 if name.endswith("4") else 3
+    if name in ("ctx262k_hadamard4", "ctx262k_hadamard3", "ctx262k_tbq4"):
+        b = 3 if name.endswith("3") else 4
+        flags = ROTATE_K | ROTATE_V | (TBQ4_K | TBQ4_V if name.endswith("tbq4") else 0)
         cfg = Config(L=16, H_kv=4, H_q=24, D=256, batch=1, max_T=262144 + extra_tokens, in_dtype=BF16,
-                     k_fmt=Fmt(b, 128), v_fmt=Fmt(b, 128), flags=ROTATE_K | ROTATE_V, sign_seed=SIGN_SEED)
+                     k_fmt=Fmt(b, 128), v_fmt=Fmt(b, 128), flags=flags, sign_seed=SIGN_SEED)
         return Workload(name, cfg, [262144], "ctx262k", extra_tokens)
     if name == "mistral7b_hotcold":
         cfg = Config(L=32, H_kv=8, H_q=32, D=128, batch=64, max_T=32768 + extra_tokens, in_dtype=F16,
@@ -91,7 +93,7 @@ def make(name: str, extra_tokens: int = 64) -> Workload:
 
 
 ALL = ("q8_0_mha_1k", "q4_0_mha_1k", "llama2_7b_kivi4", "gqa8b_hadamard4_paged", "ctx262k_hadamard4",
-       "ctx262k_hadamard3", "mistral7b_hotcold")
+       "ctx262k_hadamard3", "mistral7b_hotcold", "ctx262k_tbq4")
 
 
 def _torch_dtype(cfg: Config):

@@ -115,8 +115,9 @@ def test_append_bytes_match_oracle(case, kind):
 # ---- TBQ4 (norm + Lloyd-Max codebook) -------------------------------------------
 
 TBQ4_CASES = [
-    ("tbq4_f16_d128", 128, K.DT_F16, 0, 32),
-    ("tbq4_bf16_d256_seed", 256, K.DT_BF16, 0x5EED, 0),
+    ("tbq4_f16_d128", 128, K.DT_F16, 0, 32),          # window: the generic decode kernel
+    ("tbq4_f16_d128_mma", 128, K.DT_F16, 7, 0),        # the tensor-core decode, D = 128
+    ("tbq4_bf16_d256_seed", 256, K.DT_BF16, 0x5EED, 0),  # the tensor-core decode, D = 256
 ]
 
 

@@ -69,6 +69,7 @@ SAMPLES = {
     "ctx262k_hadamard4": [(0, 0, 0), (15, 0, 23)],
     "ctx262k_hadamard3": [(0, 0, 5), (15, 0, 18)],
     "mistral7b_hotcold": [(0, 0, 0), (20, 33, 14), (31, 63, 31)],
+    "ctx262k_tbq4": [(0, 0, 2), (15, 0, 20)],
 }
 
 
