@@ -7,19 +7,31 @@ namespace {
 
 constexpr int kThreads = 128;
 
-// Value of element d of token t (stored domain) of one (layer, seq, head).
-__device__ float stored_value(const Layout& lo, const CachePtrs& cp, int which, int layer, int seq, int h, int t,
-                              int d, int qe, int ce, bool* bad) {
-  if (t >= qe) return in_to_f32(resid_row(lo, cp, which, layer, seq, h, t)[d], lo.dtype);
-  const bool cold = t < ce;
-  const FmtInfo& f = cold ? fmt_cold(lo, which) : fmt_main(lo, which);
-  const uint8_t* row = cold ? cold_row(lo, cp, which, layer, seq, h, t) : main_row(lo, cp, which, layer, seq, h, t, bad);
-  if (!row) return 0.0f;
+// Storage of token t of one (layer, seq, head): its row (window row, or the
+// main / cold tier row holding it) and the tier (0 main, 1 cold, 2 window);
+// row = nullptr for a page id out of range.
+struct TokRow {
+  const uint8_t* row;
+  int tier;
+};
+
+__device__ TokRow token_row(const Layout& lo, const CachePtrs& cp, int which, int layer, int seq, int h, int t,
+                            int qe, int ce, bool* bad) {
+  if (t >= qe) return {reinterpret_cast<const uint8_t*>(resid_row(lo, cp, which, layer, seq, h, t)), 2};
+  if (t < ce) return {cold_row(lo, cp, which, layer, seq, h, t), 1};
+  return {main_row(lo, cp, which, layer, seq, h, t, bad), 0};
+}
+
+// Value of element d of token t (stored domain), its storage row known.
+__device__ __forceinline__ float stored_value(const Layout& lo, const TokRow& r, int which, int t, int d) {
+  if (r.tier == 2) return in_to_f32(reinterpret_cast<const uint16_t*>(r.row)[d], lo.dtype);
+  if (!r.row) return 0.0f;
+  const FmtInfo& f = r.tier == 1 ? fmt_cold(lo, which) : fmt_main(lo, which);
   if (f.axis == KVQ_AXIS_CHANNEL) {
-    const uint8_t* blk = row + (int64_t)d * f.bb;
+    const uint8_t* blk = r.row + (int64_t)d * f.bb;
     return (float)unpack_code(blk + 2, f.bits, t % f.group) * block_scale(blk);
   }
-  const uint8_t* blk = row + (int64_t)(d / f.group) * f.bb;
+  const uint8_t* blk = r.row + (int64_t)(d / f.group) * f.bb;
   return block_value(blk, f.bits, f.codebook, lo.cb, d % f.group);
 }
 
@@ -37,14 +49,19 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(DequantArgs a) {
   const int n = min(kTile, a.t1 - t0);
   if (n <= 0) return;
   __shared__ uint32_t bad_page;
+  __shared__ TokRow rows[kTile];
   if (threadIdx.x == 0) bad_page = 0;
   for (int which = 0; which < 2; ++which) {
     __syncthreads();
+    if (threadIdx.x < n) {  // each token's row once
+      bool bad = false;
+      rows[threadIdx.x] = token_row(lo, a.cp, which, a.layer, a.seq, h, t0 + threadIdx.x, qe, ce, &bad);
+      if (bad) bad_page = 1;
+    }
+    __syncthreads();
     for (int e = threadIdx.x; e < n * D; e += blockDim.x) {
       const int j = e / D, d = e % D;
-      bool bad = false;
-      xs[e] = stored_value(lo, a.cp, which, a.layer, a.seq, h, t0 + j, d, qe, ce, &bad);
-      if (bad) bad_page = 1;
+      xs[e] = stored_value(lo, rows[j], which, t0 + j, d);
     }
     __syncthreads();
     if (lo.flags & (which ? KVQ_ROTATE_V : KVQ_ROTATE_K)) {
