@@ -34,6 +34,11 @@ What it computes, step by step, with the page each step follows:
   Lloyd's algorithm run here in fp64 (S. P. Lloyd, "Least squares
   quantization in PCM", 1982; J. Max, 1960) and the lookup table holds them
   rounded to fp16.
+* Asymmetric ("scale and zero point") blocks, the next step the pages name
+  for KIVI's 2/4-bit cache (nalar.dev, section "Granularitas kuantisasi...":
+  low-bit codes need a scale and sometimes a zero point; troisinh.com
+  "Asymmetric Quantization"): the block stores its fp16 scale and its fp16
+  minimum, codes c in [0, 2^b - 1] and x = c * scale + zero.
 * Decode attention, the plain definition in fp64: s_i = q.k_i / sqrt(D),
   p = softmax(s), output = sum_i p_i v_i (nalar.dev, sections "Error pada key
   mengubah input softmax" and "Error pada value masuk setelah attention
@@ -108,6 +113,7 @@ class Fmt:
     bits: int
     group: int
     axis: int = AXIS_TOKEN
+    zp: bool = False  # asymmetric blocks: fp16 scale + fp16 zero (the block minimum), codes 0..2^b-1
 
 
 @dataclass
@@ -133,12 +139,13 @@ class Config:
     max_pages_per_seq: int = 0
 
 
-def block_bytes(bits: int, group: int) -> int:
+def block_bytes(bits: int, group: int, zp: bool = False) -> int:
     """One block: fp16 scale (2 B) + group*bits/8 bytes of codes (trefon.com
-    format table).  bits == 16 means plain 16-bit values with no scale."""
+    format table); asymmetric blocks add an fp16 zero point (2 B).  bits == 16
+    means plain 16-bit values with no scale."""
     if bits == 16:
         return 2 * group
-    return 2 + group * bits // 8
+    return 2 + (2 if zp else 0) + group * bits // 8
 
 
 def unit_tokens(cfg: Config) -> int:
@@ -189,7 +196,7 @@ def ring_slots(cfg: Config) -> int:
 
 def fmt_bytes(fmt: Fmt, n_tokens: int, D: int) -> int:
     """Bytes that hold n_tokens of one kv head in `fmt`."""
-    bb = block_bytes(fmt.bits, fmt.group)
+    bb = block_bytes(fmt.bits, fmt.group, fmt.zp)
     if fmt.axis == AXIS_TOKEN:
         return n_tokens * (D // fmt.group) * bb
     assert n_tokens % fmt.group == 0
@@ -210,7 +217,7 @@ def bytes_per_token(cfg: Config) -> int:
     vf = cfg.v_cold if cfg.hot_window > 0 else cfg.v_fmt
     total = 0
     for f in (kf, vf):
-        bb = block_bytes(f.bits, f.group)
+        bb = block_bytes(f.bits, f.group, f.zp)
         if f.axis == AXIS_TOKEN:
             total += (cfg.D // f.group) * bb
         else:
@@ -367,6 +374,46 @@ def quantize(x: np.ndarray, bits: int) -> Tuple[np.ndarray, np.ndarray]:
     r = np.where(sf == 0, np.float32(0), r)
     codes = np.clip(r, -qmax, qmax).astype(np.int8)
     return s16, codes
+
+
+def quantize_zp(x: np.ndarray, bits: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Asymmetric blocks along the last axis, fp32 op order:
+
+    mn, mx = min x, max x; qlev = 2^b - 1; s32 = (mx - mn) / qlev;
+    s16 = fp16(min(s32, 65504)); z16 = fp16(mn clipped to +-65504);
+    code = clamp(rint((x - float(z16)) / float(s16)), 0, qlev), all codes 0
+    when s16 == 0.  Returns (s16, z16 as float16 [...], codes uint8 [..., G]).
+    """
+    x = np.asarray(x, np.float32)
+    qlev = np.float32((1 << bits) - 1)
+    mn = np.min(x, axis=-1)
+    mx = np.max(x, axis=-1)
+    s32 = ((mx - mn).astype(np.float32) / qlev).astype(np.float32)
+    s16 = np.minimum(s32, np.float32(65504.0)).astype(np.float16)
+    z16 = np.clip(mn, np.float32(-65504.0), np.float32(65504.0)).astype(np.float16)
+    sf = s16.astype(np.float32)[..., None]
+    zf = z16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        r = np.rint(np.divide((x - zf).astype(np.float32), sf, dtype=np.float32))
+    r = np.where(sf == 0, np.float32(0), r)
+    codes = np.clip(r, 0, qlev).astype(np.uint8)
+    return s16, z16, codes
+
+
+def dequantize_zp_f32(s16: np.ndarray, z16: np.ndarray, codes: np.ndarray) -> np.ndarray:
+    """code * scale + zero in fp32: the product is exact, the sum rounds once."""
+    sf = np.asarray(s16, np.float16).astype(np.float32)[..., None]
+    zf = np.asarray(z16, np.float16).astype(np.float32)[..., None]
+    return (codes.astype(np.float32) * sf + zf).astype(np.float32)
+
+
+def dequantize_zp_f64(s16: np.ndarray, z16: np.ndarray, codes: np.ndarray) -> np.ndarray:
+    """code * scale + zero, exact in fp64."""
+    return (codes.astype(np.float64) * np.asarray(s16, np.float16).astype(np.float64)[..., None]
+            + np.asarray(z16, np.float16).astype(np.float64)[..., None])
+
+
+_PACK_BIAS = {8: 0, 4: 8, 3: 4, 2: 2}
 
 
 def dequantize_f32(s16: np.ndarray, codes: np.ndarray) -> np.ndarray:
@@ -531,10 +578,16 @@ def unpack(payload: np.ndarray, bits: int, G: int) -> np.ndarray:
     raise ValueError(bits)
 
 
-def encode_blocks(x: np.ndarray, bits: int, codebook: bool = False) -> np.ndarray:
+def encode_blocks(x: np.ndarray, bits: int, codebook: bool = False, zp: bool = False) -> np.ndarray:
     """fp32 blocks [..., G] -> bytes [..., block_bytes]: fp16 scale (little
     endian) then the packed codes.  codebook: TBQ4 blocks (the fp16 is the
-    norm, the nibbles are centroid indices 0..15)."""
+    norm, the nibbles are centroid indices 0..15).  zp: asymmetric blocks
+    (fp16 scale, fp16 zero, then the codes 0..2^b-1 in the same bit fields)."""
+    if zp:
+        s16, z16, c = quantize_zp(x, bits)
+        sb = np.asarray(s16, np.float16).reshape(*s16.shape, 1).view(np.uint8)
+        zb = np.asarray(z16, np.float16).reshape(*z16.shape, 1).view(np.uint8)
+        return np.concatenate([sb, zb, pack(c.astype(np.int64) - _PACK_BIAS[bits], bits)], axis=-1)
     if codebook:
         s16, idx = tbq4_quantize(x)
         codes = idx.astype(np.int64) - 8
@@ -542,6 +595,15 @@ def encode_blocks(x: np.ndarray, bits: int, codebook: bool = False) -> np.ndarra
         s16, codes = quantize(x, bits)
     sb = np.asarray(s16, np.float16).reshape(*s16.shape, 1).view(np.uint8)
     return np.concatenate([sb, pack(codes, bits)], axis=-1)
+
+
+def decode_blocks_zp(blob: np.ndarray, bits: int, G: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """asymmetric block bytes -> (s16, z16 float16 [...], codes uint8 [..., G])."""
+    blob = np.ascontiguousarray(blob, np.uint8)
+    s16 = blob[..., 0:2].copy().view(np.float16)[..., 0]
+    z16 = blob[..., 2:4].copy().view(np.float16)[..., 0]
+    codes = (unpack(blob[..., 4:], bits, G).astype(np.int64) + _PACK_BIAS[bits]).astype(np.uint8)
+    return s16, z16, codes
 
 
 def decode_blocks(blob: np.ndarray, bits: int, G: int) -> Tuple[np.ndarray, np.ndarray]:
@@ -558,7 +620,7 @@ def decode_blocks(blob: np.ndarray, bits: int, G: int) -> Tuple[np.ndarray, np.n
 
 def row_bytes(fmt: Fmt, D: int) -> int:
     """Bytes of one storage row: a token row (per-token) or a group row (per-channel)."""
-    bb = block_bytes(fmt.bits, fmt.group)
+    bb = block_bytes(fmt.bits, fmt.group, fmt.zp)
     return (D // fmt.group) * bb if fmt.axis == AXIS_TOKEN else D * bb
 
 
@@ -637,25 +699,28 @@ def quantize_rows(cfg: Config, fmt: Fmt, x: np.ndarray, rotate: bool, signs, cod
         if rotate:
             x = rotate_f32(x, *signs)
         blocks = x.reshape(*x.shape[:-1], D // fmt.group, fmt.group)
-        return encode_blocks(blocks, fmt.bits, codebook).reshape(*x.shape[:-1], -1)
+        return encode_blocks(blocks, fmt.bits, codebook, fmt.zp).reshape(*x.shape[:-1], -1)
     G = fmt.group
     n_units = x.shape[0] // G
     xt = np.transpose(x.reshape(n_units, G, x.shape[1], D), (0, 2, 3, 1))  # [u, H, D, G]
-    return encode_blocks(xt, fmt.bits).reshape(n_units, x.shape[1], -1)
+    return encode_blocks(xt, fmt.bits, zp=fmt.zp).reshape(n_units, x.shape[1], -1)
 
 
 def dequant_rows_f32(cfg: Config, fmt: Fmt, rows: np.ndarray) -> np.ndarray:
     """Storage rows -> fp32 values in the stored (possibly rotated) domain,
     [n_tok, H_kv, D]; the inverse of quantize_rows up to rounding."""
     D = cfg.D
-    bb = block_bytes(fmt.bits, fmt.group)
+    bb = block_bytes(fmt.bits, fmt.group, fmt.zp)
+    def deq(blk):
+        if fmt.zp:
+            return dequantize_zp_f32(*decode_blocks_zp(blk, fmt.bits, fmt.group))
+        return dequantize_f32(*decode_blocks(blk, fmt.bits, fmt.group))
+
     if fmt.axis == AXIS_TOKEN:
         blk = rows.reshape(*rows.shape[:-1], D // fmt.group, bb)
-        s16, codes = decode_blocks(blk, fmt.bits, fmt.group)
-        return dequantize_f32(s16, codes).reshape(*rows.shape[:-1], D)
+        return deq(blk).reshape(*rows.shape[:-1], D)
     n_units, H = rows.shape[0], rows.shape[1]
-    s16, codes = decode_blocks(rows.reshape(n_units, H, D, bb), fmt.bits, fmt.group)
-    v = dequantize_f32(s16, codes)  # [u, H, D, G]
+    v = deq(rows.reshape(n_units, H, D, bb))  # [u, H, D, G]
     return np.transpose(v, (0, 3, 1, 2)).reshape(n_units * fmt.group, H, D)
 
 
@@ -811,10 +876,14 @@ def dequantize(cfg: Config, bufs: Dict[str, np.ndarray], layer: int, seq: int, T
                     rows = np.moveaxis(bufs[which + "_cold"][layer, seq, :, g_lo:g_hi], 1, 0)
                 else:
                     rows = _read_main(cfg, bufs, main, f, layer, seq, g_lo, g_hi, block_table)
-                bb = block_bytes(f.bits, f.group)
+                bb = block_bytes(f.bits, f.group, f.zp)
                 rows = rows[:, heads]
-                s16, codes = decode_blocks(rows.reshape(g_hi - g_lo, len(heads), cfg.D, bb), f.bits, f.group)
-                v = codes.astype(np.float64) * s16.astype(np.float64)[..., None]  # [u, H, D, G]
+                blk = rows.reshape(g_hi - g_lo, len(heads), cfg.D, bb)
+                if f.zp:
+                    v = dequantize_zp_f64(*decode_blocks_zp(blk, f.bits, f.group))  # [u, H, D, G]
+                else:
+                    s16, codes = decode_blocks(blk, f.bits, f.group)
+                    v = codes.astype(np.float64) * s16.astype(np.float64)[..., None]  # [u, H, D, G]
                 v = np.transpose(v, (0, 3, 1, 2)).reshape((g_hi - g_lo) * gam, len(heads), cfg.D)
                 res[lo - t0:hi - t0] = v[lo - g_lo * gam:hi - g_lo * gam]
             else:
@@ -823,10 +892,16 @@ def dequantize(cfg: Config, bufs: Dict[str, np.ndarray], layer: int, seq: int, T
                 else:
                     rows = _read_main(cfg, bufs, main, f, layer, seq, lo, hi, block_table)
                 rows = rows[:, heads]
-                bb = block_bytes(f.bits, f.group)
-                s16, codes = decode_blocks(rows.reshape(hi - lo, len(heads), cfg.D // f.group, bb),
-                                           f.bits, f.group)
-                if _codebook_for(cfg, which):
+                bb = block_bytes(f.bits, f.group, f.zp)
+                blk = rows.reshape(hi - lo, len(heads), cfg.D // f.group, bb)
+                if f.zp:
+                    s16, z16, zc = decode_blocks_zp(blk, f.bits, f.group)
+                    codes = None
+                else:
+                    s16, codes = decode_blocks(blk, f.bits, f.group)
+                if f.zp:
+                    val = dequantize_zp_f64(s16, z16, zc).reshape(hi - lo, len(heads), cfg.D)
+                elif _codebook_for(cfg, which):
                     val = tbq4_dequantize_f64(s16, codes.astype(np.int64) + 8).reshape(hi - lo, len(heads), cfg.D)
                 else:
                     val = dequantize_f64(s16, codes).reshape(hi - lo, len(heads), cfg.D)
