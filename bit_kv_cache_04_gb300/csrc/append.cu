@@ -285,6 +285,17 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_quantize_kernel(Appe
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = in_to_f32(rt[j * RH + c], lo.dtype);
+        if (f.zp) {  // asymmetric blocks
+          bool bad = false;
+          if (to_cold) {
+            float dq[32];
+            quant_zp32(v, f.bits, nullptr, dq);
+            quant_zp32(dq, fc.bits, cold_row(lo, a.cp, which, layer, seq, h, u0) + (int64_t)c * fc.bb, nullptr);
+          } else {
+            quant_zp32(v, f.bits, main_row(lo, a.cp, which, layer, seq, h, u0, &bad) + (int64_t)c * f.bb, nullptr);
+          }
+          continue;
+        }
         const float m = amax32(v);
         if (to_cold) {
           float dq[32];
@@ -372,6 +383,22 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_quantize_kernel(Appe
         }
         continue;
       }
+      if (f.zp) {  // asymmetric 32-value blocks
+        if (to_cold) {
+          float dq[32];
+          quant_zp32(v, f.bits, nullptr, dq);
+          quant_zp32(dq, fc.bits, cold_row(lo, a.cp, which, layer, seq, h, t) + b * fc.bb, nullptr);
+        } else {
+          bool bad = false;
+          uint8_t* row = main_row(lo, a.cp, which, layer, seq, h, t, &bad);
+          if (bad) {
+            page_bad = 1;
+            continue;
+          }
+          quant_zp32(v, f.bits, row + b * f.bb, nullptr);
+        }
+        continue;
+      }
       if (to_cold) {
         // tiers keep the hot group size; per-token tiers use 32-value blocks
         float dq[32];
@@ -419,8 +446,24 @@ __global__ void __launch_bounds__(kAppendThreads) append_requant_kernel(AppendAr
       uint8_t* dst = cold_row(lo, a.cp, which, layer, seq, h, u0);
       for (int c = threadIdx.x; c < D; c += blockDim.x) {
         float x[32];
+        if (f.zp) {
+          dequant_zp_serial(row + (int64_t)c * f.bb, 32, f.bits, x, 1);
+          quant_zp32(x, fc.bits, dst + (int64_t)c * fc.bb, nullptr);
+          continue;
+        }
         dequant_block_serial(row + (int64_t)c * f.bb, f.group, f.bits, x, 1);
         thread_quant_channel(x, 1, fc.bits, dst + (int64_t)c * fc.bb, nullptr);
+      }
+      continue;
+    }
+    if (f.zp) {  // per-token asymmetric 32-value blocks: thread = (token, block)
+      for (int item = threadIdx.x; item < kTile * (D / 32); item += blockDim.x) {
+        const int j = item / (D / 32), b = item % (D / 32);
+        const uint8_t* row = main_row(lo, a.cp, which, layer, seq, h, u0 + j, &bad);
+        if (!row) continue;
+        float x[32];
+        dequant_zp_serial(row + b * f.bb, 32, f.bits, x, 1);
+        quant_zp32(x, fc.bits, cold_row(lo, a.cp, which, layer, seq, h, u0 + j) + b * fc.bb, nullptr);
       }
       continue;
     }

@@ -327,7 +327,7 @@ bool launch_fast_tensor(const AppendArgs& a, int which, bool dry, cudaStream_t s
   const Layout& lo = a.lo;
   const FmtInfo& f = fmt_main(lo, which);
   const bool rot = (lo.flags & (which ? KVQ_ROTATE_V : KVQ_ROTATE_K)) != 0;
-  if (rot || f.group != 32) return false;
+  if (rot || f.group != 32 || f.zp) return false;
   const int cb = lo.tiered ? fmt_cold(lo, which).bits : 0;
   if (f.axis == KVQ_AXIS_CHANNEL) {  // keys (values grouped per channel take the generic kernel)
     if (which != 0) return false;

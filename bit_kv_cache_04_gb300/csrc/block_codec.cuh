@@ -168,10 +168,57 @@ __device__ __forceinline__ void dequant_tbq4_serial(const uint8_t* blk, const fl
   for (int i = 0; i < 128; ++i) out[i * stride] = cb[(blk[2 + (i >> 1)] >> ((i & 1) * 4)) & 0xF] * n;
 }
 
-// Element i of a block (TBQ4 or uniform codes), in the stored domain.
-__device__ __forceinline__ float block_value(const uint8_t* blk, int bits, int codebook, const float* cb, int i) {
+// Asymmetric block (fp16 scale, fp16 zero, unbiased codes): element i =
+// code * scale + zero in fp32 (the product is exact, the sum rounds once).
+__device__ __forceinline__ float zp_value(const uint8_t* blk, int bits, int i) {
+  const int c = unpack_code(blk + 4, bits, i) + (bits == 8 ? 0 : 1 << (bits - 1));  // the raw field
+  return __fadd_rn(__fmul_rn((float)c, block_scale(blk)), __half2float(*reinterpret_cast<const __half*>(blk + 2)));
+}
+
+__device__ __forceinline__ void dequant_zp_serial(const uint8_t* blk, int G, int bits, float* out, int stride) {
+  for (int i = 0; i < G; ++i) out[i * stride] = zp_value(blk, bits, i);
+}
+
+// Element i of a block (TBQ4, asymmetric or uniform codes), in the stored domain.
+__device__ __forceinline__ float block_value(const uint8_t* blk, int bits, int codebook, int zp, const float* cb,
+                                             int i) {
   if (codebook) return cb[(blk[2 + (i >> 1)] >> ((i & 1) * 4)) & 0xF] * block_scale(blk);
+  if (zp) return zp_value(blk, bits, i);
   return (float)unpack_code(blk + 2, bits, i) * block_scale(blk);
+}
+
+// Asymmetric block of 32 values (op order of the format): mn, mx = min, max;
+// s16 = fp16(min((mx - mn) / (2^b - 1), 65504)); z16 = fp16(mn clipped to
+// +-65504); code = clamp(rint((x - z) / s), 0, 2^b - 1), 0 when s = 0.  The
+// block (scale, zero, codes in little-endian b-bit fields) goes to blk when
+// given; dq (optional) receives code * s + z.
+__device__ __forceinline__ void quant_zp32(const float* v, int bits, uint8_t* blk, float* dq) {
+  const int qlev = (1 << bits) - 1;
+  float mn = v[0], mx = v[0];
+  for (int j = 1; j < 32; ++j) {
+    mn = fminf(mn, v[j]);
+    mx = fmaxf(mx, v[j]);
+  }
+  const __half s16 = __float2half_rn(fminf(__fdiv_rn(__fsub_rn(mx, mn), (float)qlev), 65504.0f));
+  const __half z16 = __float2half_rn(fminf(fmaxf(mn, -65504.0f), 65504.0f));
+  const float sf = __half2float(s16), zf = __half2float(z16);
+  uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int j = 0; j < 32; ++j) {
+    int c = 0;
+    if (sf != 0.f) c = (int)fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v[j], zf), sf)), 0.f), (float)qlev);
+    if (dq) dq[j] = __fadd_rn(__fmul_rn((float)c, sf), zf);
+    const int bit = bits * j, k = bit / 32, sh = bit % 32;
+    w[k] |= (uint32_t)c << sh;
+    if (sh + bits > 32) w[k + 1] |= (uint32_t)c >> (32 - sh);
+  }
+  if (!blk) return;
+  uint16_t* p = reinterpret_cast<uint16_t*>(blk);
+  p[0] = __half_as_ushort(s16);
+  p[1] = __half_as_ushort(z16);
+  for (int k = 0; k < bits; ++k) {
+    p[2 + 2 * k] = (uint16_t)w[k];
+    p[3 + 2 * k] = (uint16_t)(w[k] >> 16);
+  }
 }
 
 // Index of u among the 15 ascending thresholds: how many lie strictly below.

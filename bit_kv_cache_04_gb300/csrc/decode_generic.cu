@@ -60,7 +60,8 @@ __device__ void load_tile(const Layout& lo, const CachePtrs& cp, int which, int 
     const uint8_t* row = tr.seg == 0 ? cold_row(lo, cp, which, layer, seq, h, tr.t0)
                                      : main_row(lo, cp, which, layer, seq, h, tr.t0, &bad);
     for (int c = threadIdx.x; c < D; c += blockDim.x)
-      dequant_block_serial(row + (int64_t)c * f.bb, f.group, f.bits, x + c, ld);
+      if (f.zp) dequant_zp_serial(row + (int64_t)c * f.bb, f.group, f.bits, x + c, ld);
+      else dequant_block_serial(row + (int64_t)c * f.bb, f.group, f.bits, x + c, ld);
     return;
   }
   const int nb = D / f.group;
@@ -76,6 +77,7 @@ __device__ void load_tile(const Layout& lo, const CachePtrs& cp, int which, int 
       continue;
     }
     if (f.codebook) dequant_tbq4_serial(row + (int64_t)b * f.bb, lo.cb, dst, 1);
+    else if (f.zp) dequant_zp_serial(row + (int64_t)b * f.bb, f.group, f.bits, dst, 1);
     else dequant_block_serial(row + (int64_t)b * f.bb, f.group, f.bits, dst, 1);
   }
 }

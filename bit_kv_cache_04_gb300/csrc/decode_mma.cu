@@ -1121,6 +1121,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   if (lo.ring) ok = ok && lo.dtype == KVQ_DT_F16 && !(lo.flags & (KVQ_ROTATE_K | KVQ_ROTATE_V));
   if (lo.paged) ok = ok && (lo.pt == 16 || lo.pt == 32);
   if (lo.kf.codebook != lo.vf.codebook) ok = false;  // one tensor TBQ4, the other not: generic kernel
+  if (lo.kf.zp || lo.vf.zp) ok = false;               // asymmetric blocks: generic kernel
   if (!ok) return launch_decode_generic(a, st);
   if (lo.kf.codebook) {  // TBQ4 K and V (rotated 4-bit blocks of 128)
     if (lo.D == 128 && lo.g <= 4)

@@ -29,10 +29,10 @@ __device__ __forceinline__ float stored_value(const Layout& lo, const TokRow& r,
   const FmtInfo& f = r.tier == 1 ? fmt_cold(lo, which) : fmt_main(lo, which);
   if (f.axis == KVQ_AXIS_CHANNEL) {
     const uint8_t* blk = r.row + (int64_t)d * f.bb;
-    return (float)unpack_code(blk + 2, f.bits, t % f.group) * block_scale(blk);
+    return block_value(blk, f.bits, 0, f.zp, lo.cb, t % f.group);
   }
   const uint8_t* blk = r.row + (int64_t)(d / f.group) * f.bb;
-  return block_value(blk, f.bits, f.codebook, lo.cb, d % f.group);
+  return block_value(blk, f.bits, f.codebook, f.zp, lo.cb, d % f.group);
 }
 
 __global__ void __launch_bounds__(kThreads) dequantize_kernel(DequantArgs a) {

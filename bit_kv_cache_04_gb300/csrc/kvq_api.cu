@@ -74,7 +74,7 @@ kvq_status check_config(const kvq_config* c, bool allow16) {
     if (gam == 1) return fail(KVQ_ERR_UNSUPPORTED, "hot/cold tiers need a per-channel (token-group) format");
     if (c->hot_window % gam != 0) return fail(KVQ_ERR_ARG, "hot_window=%d not a multiple of %d", c->hot_window, gam);
   }
-  uint32_t known = KVQ_ROTATE_K | KVQ_ROTATE_V | KVQ_K_PRE_ROPE | KVQ_TBQ4_K | KVQ_TBQ4_V;
+  uint32_t known = KVQ_ROTATE_K | KVQ_ROTATE_V | KVQ_K_PRE_ROPE | KVQ_TBQ4_K | KVQ_TBQ4_V | KVQ_ZP_K | KVQ_ZP_V;
   if (c->flags & ~known) return fail(KVQ_ERR_ARG, "unknown flags 0x%x", c->flags & ~known);
   if ((c->flags & KVQ_ROTATE_K) && c->k_fmt.axis != KVQ_AXIS_TOKEN)
     return fail(KVQ_ERR_UNSUPPORTED, "rotation needs per-token K blocks");
@@ -83,6 +83,15 @@ kvq_status check_config(const kvq_config* c, bool allow16) {
   if ((c->flags & KVQ_ROTATE_K) && (c->flags & KVQ_K_PRE_ROPE))
     return fail(KVQ_ERR_UNSUPPORTED, "pre-RoPE keys with rotated K: RoPE pairs do not commute with the transform");
   if ((c->flags & KVQ_K_PRE_ROPE) && !(c->rope_theta > 1.0f)) return fail(KVQ_ERR_ARG, "rope_theta must be > 1");
+  for (int t = 0; t < 2; ++t) {
+    const uint32_t zb = t ? KVQ_ZP_V : KVQ_ZP_K, rz = t ? KVQ_ROTATE_V : KVQ_ROTATE_K;
+    if (!(c->flags & zb)) continue;
+    const kvq_fmt& f = t ? c->v_fmt : c->k_fmt;
+    const kvq_fmt& fc = t ? c->v_cold : c->k_cold;
+    auto zp_ok = [](const kvq_fmt& x) { return (x.bits == 4 || x.bits == 2) && x.group == 32; };
+    if ((c->flags & rz) || !zp_ok(f) || (c->hot_window > 0 && !zp_ok(fc)))
+      return fail(KVQ_ERR_UNSUPPORTED, "zero-point blocks need 4- or 2-bit blocks of 32 values and no rotation");
+  }
   for (int t = 0; t < 2; ++t) {
     const uint32_t tb = t ? KVQ_TBQ4_V : KVQ_TBQ4_K, rb = t ? KVQ_ROTATE_V : KVQ_ROTATE_K;
     const kvq_fmt& f = t ? c->v_fmt : c->k_fmt;
@@ -101,14 +110,15 @@ kvq_status check_config(const kvq_config* c, bool allow16) {
   return KVQ_OK;
 }
 
-FmtInfo make_fmt(const kvq_fmt& f, int D, bool codebook = false) {
+FmtInfo make_fmt(const kvq_fmt& f, int D, bool codebook = false, bool zp = false) {
   FmtInfo r{};
   r.codebook = codebook ? 1 : 0;
+  r.zp = zp ? 1 : 0;
   if (f.bits == 0) return r;
   r.bits = f.bits;
   r.group = f.group;
   r.axis = f.axis;
-  r.bb = block_bytes_of(f.bits, f.group);
+  r.bb = block_bytes_of(f.bits, f.group) + (zp ? 2 : 0);
   r.qmax = f.bits == 16 ? 0 : qmax_of(f.bits);
   r.row = f.axis == KVQ_AXIS_TOKEN ? (D / f.group) * r.bb : D * r.bb;
   return r;
@@ -187,12 +197,13 @@ Layout make_layout(const kvq_config* c) {
       lo.d2[j] = (uint32_t)(w[2 + j / 2] >> (32 * (j % 2)));
     }
   }
-  lo.kf = make_fmt(c->k_fmt, c->D, (c->flags & KVQ_TBQ4_K) != 0);
-  lo.vf = make_fmt(c->v_fmt, c->D, (c->flags & KVQ_TBQ4_V) != 0);
+  const bool zk = (c->flags & KVQ_ZP_K) != 0, zv = (c->flags & KVQ_ZP_V) != 0;
+  lo.kf = make_fmt(c->k_fmt, c->D, (c->flags & KVQ_TBQ4_K) != 0, zk);
+  lo.vf = make_fmt(c->v_fmt, c->D, (c->flags & KVQ_TBQ4_V) != 0, zv);
   if (c->flags & (KVQ_TBQ4_K | KVQ_TBQ4_V)) tbq4_tables(lo.cb, lo.cbt);
   if (lo.tiered) {
-    lo.kc = make_fmt(c->k_cold, c->D);
-    lo.vc = make_fmt(c->v_cold, c->D);
+    lo.kc = make_fmt(c->k_cold, c->D, false, zk);
+    lo.vc = make_fmt(c->v_cold, c->D, false, zv);
   }
   // per-token capacity is rounded up to whole 32-token tiles so that every
   // tile starts 16-byte aligned and lies inside the buffer
@@ -217,8 +228,8 @@ Layout make_layout(const kvq_config* c) {
   return lo;
 }
 
-int64_t fmt_bytes(const kvq_fmt& f, int64_t n_tokens, int D) {
-  int64_t bb = block_bytes_of(f.bits, f.group);
+int64_t fmt_bytes(const kvq_fmt& f, int64_t n_tokens, int D, bool zp) {
+  int64_t bb = block_bytes_of(f.bits, f.group) + (zp ? 2 : 0);
   if (f.axis == KVQ_AXIS_TOKEN) return n_tokens * (D / f.group) * bb;
   return (n_tokens / f.group) * D * bb;
 }
@@ -365,7 +376,8 @@ kvq_status kvq_bytes_per_token(const kvq_config* cfg, int64_t* bytes) {
   const kvq_fmt& vf = cfg->hot_window > 0 ? cfg->v_cold : cfg->v_fmt;
   int64_t per_head = 0;
   for (const kvq_fmt* f : {&kf, &vf}) {
-    int64_t bb = block_bytes_of(f->bits, f->group);
+    const bool zp = (cfg->flags & (f == &kf ? KVQ_ZP_K : KVQ_ZP_V)) != 0;
+    int64_t bb = block_bytes_of(f->bits, f->group) + (zp ? 2 : 0);
     if (f->axis == KVQ_AXIS_TOKEN) {
       per_head += (cfg->D / f->group) * bb;
     } else {
@@ -386,8 +398,9 @@ kvq_status kvq_cache_bytes(const kvq_config* cfg, int64_t T, int64_t* bytes) {
   int64_t ce = 0;
   if (lo.W > 0 && qe > lo.W) ce = ((qe - lo.W) / lo.gam) * lo.gam;
   int64_t per_head = 0;
-  if (lo.W > 0) per_head += fmt_bytes(cfg->k_cold, ce, cfg->D) + fmt_bytes(cfg->v_cold, ce, cfg->D);
-  per_head += fmt_bytes(cfg->k_fmt, qe - ce, cfg->D) + fmt_bytes(cfg->v_fmt, qe - ce, cfg->D);
+  const bool zk = (cfg->flags & KVQ_ZP_K) != 0, zv = (cfg->flags & KVQ_ZP_V) != 0;
+  if (lo.W > 0) per_head += fmt_bytes(cfg->k_cold, ce, cfg->D, zk) + fmt_bytes(cfg->v_cold, ce, cfg->D, zv);
+  per_head += fmt_bytes(cfg->k_fmt, qe - ce, cfg->D, zk) + fmt_bytes(cfg->v_fmt, qe - ce, cfg->D, zv);
   per_head += 2 * (T - qe) * cfg->D * 2;
   *bytes = (int64_t)cfg->L * cfg->H_kv * per_head;
   return ok();

@@ -28,6 +28,7 @@ struct FmtInfo {
   int qmax;   // 2^(bits-1) - 1
   int row;    // bytes of one storage row
   int codebook;  // 1: TBQ4 blocks (fp16 L2 norm + Lloyd-Max centroid indices)
+  int zp;        // 1: asymmetric blocks (fp16 scale, fp16 zero, codes 0..2^b-1)
 };
 
 // Everything a kernel needs to find a byte of the cache.

@@ -22,6 +22,8 @@ ROTATE_V = 2
 K_PRE_ROPE = 4
 TBQ4_K = 8
 TBQ4_V = 16
+ZP_K = 32
+ZP_V = 64
 DT_F16 = 0
 DT_BF16 = 1
 

@@ -123,7 +123,15 @@ enum {
    * kvq_tbq4_codebook).  Needs the tensor's rotation flag, 4 bits, group 128,
    * per-token blocks, one tier.  Same 66 B per 128 values. */
   KVQ_TBQ4_K = 1u << 3,
-  KVQ_TBQ4_V = 1u << 4
+  KVQ_TBQ4_V = 1u << 4,
+  /* Asymmetric blocks ("scale and zero point", nalar.dev, "Granularitas
+   * kuantisasi..."): every block of that tensor (both tiers) is the fp16 scale
+   * s, the fp16 zero z (the block minimum), then codes c in [0, 2^b - 1] in the
+   * usual bit fields, x = c s + z: 2 more bytes per block (20 B / 32 values
+   * at 4 bits, 12 B / 32 at 2 bits).  Needs 4- or 2-bit
+   * blocks of 32 values, no rotation.  Decode takes the generic kernel. */
+  KVQ_ZP_K = 1u << 5,
+  KVQ_ZP_V = 1u << 6
 };
 
 /* Device status bits (workspace word 0), OR-ed by kernels. */

@@ -9,11 +9,13 @@ from oracle import kvq_oracle as O
 
 
 def oracle_cfg(c) -> O.Config:
-    def f(x):
-        return None if x is None else O.Fmt(x.bits, x.group, x.axis)
+    zk, zv = bool(c.flags & 32), bool(c.flags & 64)  # the library's asymmetric-block flags
+
+    def f(x, zp):
+        return None if x is None else O.Fmt(x.bits, x.group, x.axis, zp)
 
     return O.Config(L=c.L, H_kv=c.H_kv, H_q=c.H_q, D=c.D, batch=c.batch, max_T=c.max_T, in_dtype=c.in_dtype,
-                    k_fmt=f(c.k_fmt), v_fmt=f(c.v_fmt), k_cold=f(c.k_cold), v_cold=f(c.v_cold),
+                    k_fmt=f(c.k_fmt, zk), v_fmt=f(c.v_fmt, zv), k_cold=f(c.k_cold, zk), v_cold=f(c.v_cold, zv),
                     hot_window=c.hot_window, residual_window=c.residual_window, flags=c.flags,
                     rope_theta=c.rope_theta, sign_seed=c.sign_seed, page_tokens=c.page_tokens,
                     n_pages=c.n_pages, max_pages_per_seq=c.max_pages_per_seq)
@@ -47,11 +49,15 @@ def codes_differ(cfg: O.Config, gpu: dict, ref: dict):
         which = name[0]
         tier_cold = name.endswith("cold")
         fmt = (cfg.k_cold if which == "k" else cfg.v_cold) if tier_cold else (cfg.k_fmt if which == "k" else cfg.v_fmt)
-        bb = O.block_bytes(fmt.bits, fmt.group)
+        bb = O.block_bytes(fmt.bits, fmt.group, fmt.zp)
         a = gpu[name].reshape(-1, bb)
         b = ref[name].reshape(-1, bb)
-        sa, ca = O.decode_blocks(a, fmt.bits, fmt.group)
-        sb, cb = O.decode_blocks(b, fmt.bits, fmt.group)
+        if fmt.zp:
+            sa, _, ca = O.decode_blocks_zp(a, fmt.bits, fmt.group)
+            sb, _, cb = O.decode_blocks_zp(b, fmt.bits, fmt.group)
+        else:
+            sa, ca = O.decode_blocks(a, fmt.bits, fmt.group)
+            sb, cb = O.decode_blocks(b, fmt.bits, fmt.group)
         d = np.abs(ca.astype(np.int32) - cb.astype(np.int32))
         total += d.size
         diff += int(np.count_nonzero(d))

@@ -82,7 +82,7 @@ def _bad(**kw):
     (dict(D=96), 2), (dict(H_q=3), 1), (dict(H_q=36, H_kv=2), 2), (dict(k_fmt=K.Fmt(5, 32)), 1),
     (dict(k_fmt=K.Fmt(4, 64)), 1), (dict(k_fmt=K.Fmt(4, 128, K.AXIS_CHANNEL)), 2),
     (dict(flags=K.ROTATE_K, k_fmt=K.Fmt(4, 32, K.AXIS_CHANNEL)), 2),
-    (dict(flags=K.ROTATE_K | K.K_PRE_ROPE), 2), (dict(flags=64), 1), (dict(hot_window=64), 1),
+    (dict(flags=K.ROTATE_K | K.K_PRE_ROPE), 2), (dict(flags=128), 1), (dict(hot_window=64), 1),
     (dict(hot_window=64, k_cold=K.Fmt(2, 32), v_cold=K.Fmt(2, 32)), 2),
     (dict(page_tokens=16, n_pages=0), 1), (dict(max_T=0), 1), (dict(in_dtype=7), 1),
     (dict(k_fmt=K.Fmt(16, 32)), 1),
@@ -118,6 +118,9 @@ def test_launch_counts():
     assert K.kvq_launch_counts(W.make("mistral7b_hotcold").cfg) == (1 + 2 + 1, 1)
     assert K.kvq_launch_counts(W.make("q8_0_mha_1k").cfg) == (2, 1)
     assert K.kvq_launch_counts(W.make("ctx262k_hadamard4").cfg) == (1, 1)
+    # asymmetric blocks take the generic quantize kernel (+ window copy)
+    zp = _bad(flags=K.ZP_K | K.ZP_V, k_fmt=K.Fmt(4, 32, K.AXIS_CHANNEL), residual_window=128)
+    assert K.kvq_launch_counts(zp) == (1 + 1, 1)
 
 
 def test_tbq4_codebook_matches_oracle():
@@ -143,3 +146,43 @@ def test_tbq4_validation(kw, ok):
         with pytest.raises(K.KvqError) as e:
             K.kvq_validate_config(_bad(**kw))
         assert e.value.status == 2
+
+
+@pytest.mark.parametrize("kw,ok", [
+    (dict(flags=K.ZP_K | K.ZP_V, k_fmt=K.Fmt(4, 32, K.AXIS_CHANNEL)), True),
+    (dict(flags=K.ZP_K | K.ZP_V, k_fmt=K.Fmt(2, 32), v_fmt=K.Fmt(2, 32)), True),
+    (dict(flags=K.ZP_V, k_fmt=K.Fmt(4, 32, K.AXIS_CHANNEL), hot_window=64, k_cold=K.Fmt(2, 32, K.AXIS_CHANNEL),
+          v_cold=K.Fmt(2, 32)), True),
+    (dict(flags=K.ZP_K, k_fmt=K.Fmt(8, 32)), False),
+    (dict(flags=K.ZP_K, k_fmt=K.Fmt(3, 128)), False),
+    (dict(flags=K.ZP_K, k_fmt=K.Fmt(4, 128)), False),
+    (dict(flags=K.ZP_K | K.ROTATE_K, k_fmt=K.Fmt(4, 32)), False),
+    (dict(flags=K.ZP_V, k_fmt=K.Fmt(4, 32, K.AXIS_CHANNEL), hot_window=64, k_cold=K.Fmt(2, 32, K.AXIS_CHANNEL),
+          v_cold=K.Fmt(8, 32)), False),
+])
+def test_zp_validation(kw, ok):
+    if ok:
+        K.kvq_validate_config(_bad(**kw))
+    else:
+        with pytest.raises(K.KvqError) as e:
+            K.kvq_validate_config(_bad(**kw))
+        assert e.value.status == 2
+
+
+@pytest.mark.parametrize("kw", [
+    dict(flags=K.ZP_K | K.ZP_V, k_fmt=K.Fmt(4, 32, K.AXIS_CHANNEL), residual_window=128),
+    dict(flags=K.ZP_K | K.ZP_V, k_fmt=K.Fmt(2, 32), v_fmt=K.Fmt(2, 32)),
+    dict(flags=K.ZP_V, k_fmt=K.Fmt(4, 32, K.AXIS_CHANNEL), hot_window=64, residual_window=32,
+         k_cold=K.Fmt(2, 32, K.AXIS_CHANNEL), v_cold=K.Fmt(2, 32), max_T=1000),
+])
+def test_zp_size_law_matches_oracle(kw):
+    cfg = _bad(**kw)
+    oc = oracle_cfg(cfg)
+    assert K.kvq_bytes_per_token(cfg) == O.bytes_per_token(oc)
+    for T in (0, 1, 31, 32, 33, 63, 64, 200, cfg.max_T):
+        assert K.kvq_cache_bytes(cfg, T) == O.cache_bytes(oc, T), T
+    shapes = O.buffer_shapes(oc)
+    for n, sz in zip(K.BUFFER_NAMES, K.kvq_buffer_sizes(cfg)):
+        if n in shapes:
+            shape, dt = shapes[n]
+            assert sz == int(__import__("numpy").prod(shape)) * (2 if dt.__name__ == "uint16" else 1), n

@@ -11,6 +11,9 @@ of input:
   uses s = 2^-20, a subnormal fp16 scale;
 * seeded N(0, 1) values with a few large channels.
 
+* for the asymmetric (scale + zero point) blocks, exact half steps between
+  each block's minimum and maximum with a power-of-two range / (2^b - 1).
+
 Each case appends in two calls (a bulk prefix, then a ragged remainder) and
 compares every packed byte with the oracle.
 """
@@ -33,7 +36,7 @@ from bit_kv_cache_04_gb300 import kvq as K  # noqa: E402
 
 CH, TOK = K.AXIS_CHANNEL, K.AXIS_TOKEN
 
-# (name, D, dtype, k_fmt, v_fmt, k_cold, v_cold, hot_window, residual_window)
+# (name, D, dtype, k_fmt, v_fmt, k_cold, v_cold, hot_window, residual_window[, flags])
 CASES = [
     ("t8_f16", 128, K.DT_F16, K.Fmt(8, 32), K.Fmt(8, 32), None, None, 0, 0),
     ("t8_bf16_d256", 256, K.DT_BF16, K.Fmt(8, 32), K.Fmt(8, 32), None, None, 0, 16),
@@ -44,15 +47,37 @@ CASES = [
     ("kivi2_f16_d256", 256, K.DT_F16, K.Fmt(2, 32, CH), K.Fmt(2, 32), None, None, 0, 64),
     ("tiers_bf16", 128, K.DT_BF16, K.Fmt(4, 32, CH), K.Fmt(4, 32), K.Fmt(2, 32, CH), K.Fmt(2, 32), 64, 32),
     ("tiers_f16_d256", 256, K.DT_F16, K.Fmt(4, 32, CH), K.Fmt(4, 32), K.Fmt(2, 32, CH), K.Fmt(2, 32), 96, 0),
+    # asymmetric blocks (scale + zero point)
+    ("zp_kivi4_f16", 128, K.DT_F16, K.Fmt(4, 32, CH), K.Fmt(4, 32), None, None, 0, 128, K.ZP_K | K.ZP_V),
+    ("zp_t2_bf16", 128, K.DT_BF16, K.Fmt(2, 32), K.Fmt(2, 32), None, None, 0, 0, K.ZP_K | K.ZP_V),
+    ("zp_tiers_f16", 128, K.DT_F16, K.Fmt(4, 32, CH), K.Fmt(4, 32), K.Fmt(2, 32, CH), K.Fmt(2, 32), 64, 32,
+     K.ZP_K | K.ZP_V),
+    ("zp_v_only_d256", 256, K.DT_F16, K.Fmt(4, 32, CH), K.Fmt(2, 32), None, None, 0, 32, K.ZP_V),
 ]
 
 LENGTHS = [301, 160, 33]
 PREFIX = [200, 64, 0]
 
 
-def _inputs(kind, n_tok, H, D, bits, gen):
+def _inputs(kind, n_tok, H, D, bits, gen, zp=False):
     """[n_tok, H, D] input values (float64) for one tensor; token index is the
     position within the sequence."""
+    if kind == "ties" and zp:
+        # asymmetric ties: every block holds its minimum -off*s (where token
+        # and channel agree mod 32, shifted by one) and its maximum
+        # (qlev - off)*s, so the scale is s and the zero -off*s exactly; every
+        # other value is (k + 1/2 - off)*s, an exact half step
+        qlev = (1 << bits) - 1
+        off = qlev // 2
+        k = torch.randint(0, qlev, (n_tok, H, D), generator=gen, dtype=torch.int64).double() + 0.5
+        t = torch.arange(n_tok).view(-1, 1, 1)
+        c = torch.arange(D).view(1, 1, -1)
+        hi = ((t % 32) == (c % 32)).expand(n_tok, H, D)
+        lo = ((t % 32) == ((c + 1) % 32)).expand(n_tok, H, D)
+        x = torch.where(hi, float(qlev), torch.where(lo, 0.0, k)) - off
+        s = torch.tensor([2.0 ** (-3 * (h % 3)) for h in range(H)], dtype=torch.float64).view(1, H, 1)
+        s[0, -1, 0] = 2.0 ** -20
+        return x * s
     if kind == "ties":
         qmax = (1 << (bits - 1)) - 1
         k = torch.randint(-qmax, qmax, (n_tok, H, D), generator=gen, dtype=torch.int64).double() + 0.5
@@ -72,16 +97,18 @@ def _inputs(kind, n_tok, H, D, bits, gen):
 
 def _case_tensors(kind, cfg, lengths, which, gen):
     bits = (cfg.k_fmt if which == 0 else cfg.v_fmt).bits
+    zp = bool(cfg.flags & (K.ZP_K if which == 0 else K.ZP_V))
     dt = torch.float16 if cfg.in_dtype == K.DT_F16 else torch.bfloat16
-    return [_inputs(kind, T, cfg.H_kv, cfg.D, bits, gen).to(dt) for T in lengths]
+    return [_inputs(kind, T, cfg.H_kv, cfg.D, bits, gen, zp).to(dt) for T in lengths]
 
 
 @pytest.mark.parametrize("kind", ["ties", "random"])
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_append_bytes_match_oracle(case, kind):
-    name, D, dtype, kf, vf, kc, vc, hot, R = case
+    name, D, dtype, kf, vf, kc, vc, hot, R = case[:9]
+    flags = case[9] if len(case) > 9 else 0
     cfg = K.Config(L=1, H_kv=3, H_q=3, D=D, batch=len(LENGTHS), max_T=max(LENGTHS) + 32, in_dtype=dtype,
-                   k_fmt=kf, v_fmt=vf, k_cold=kc, v_cold=vc, hot_window=hot, residual_window=R)
+                   k_fmt=kf, v_fmt=vf, k_cold=kc, v_cold=vc, hot_window=hot, residual_window=R, flags=flags)
     oc = oracle_cfg(cfg)
     gen = torch.Generator().manual_seed(zlib.crc32(f"{name}/{kind}".encode()))
     ks = _case_tensors(kind, cfg, LENGTHS, 0, gen)
@@ -103,13 +130,23 @@ def test_append_bytes_match_oracle(case, kind):
     torch.cuda.synchronize()
     assert cache.device_status() == 0
     shapes = O.buffer_shapes(oc)
+    bufs = {}
     for n, arr in cache.buffer_numpy().items():
         shape, dt = shapes[n]
         got = arr.view(dt).reshape(shape)
+        bufs[n] = got
         if not np.array_equal(got, ref[n]):
             total, diff, maxd, sdiff = codes_differ(oc, {n: got}, {n: ref[n]}) \
                 if not n.endswith("resid") else (0, -1, -1, -1)
             pytest.fail(f"{name}/{kind} {n}: bytes differ (codes {diff}/{total}, max |dc| {maxd}, scales {sdiff})")
+    if flags:  # asymmetric blocks: decode over the GPU's bytes against fp64 attention
+        dtq = torch.float16 if dtype == K.DT_F16 else torch.bfloat16
+        q = torch.randn((1, cfg.batch, cfg.H_q, D), generator=gen).to(dtq).cuda()
+        out = torch.full((1, cfg.batch, cfg.H_q, D), float("nan"), dtype=torch.float32, device="cuda")
+        cache.decode(0, 1, q, seq_lens, out)
+        torch.cuda.synchronize()
+        o_ref = O.decode_attention(oc, bufs, 0, 1, raw16(q), LENGTHS)
+        assert rel_err(out.cpu().numpy(), o_ref) <= 2e-3
 
 
 # ---- TBQ4 (norm + Lloyd-Max codebook) -------------------------------------------
