@@ -21,6 +21,8 @@ SOURCES = [
     ("kvq_api.cu", []),
     ("append.cu", ["--fmad=false"]),
     ("append_fast.cu", ["--fmad=false"]),
+    ("append_fast_zp_f16.cu", ["--fmad=false"]),
+    ("append_fast_zp_bf16.cu", ["--fmad=false"]),
     ("decode_generic.cu", []),
     ("decode_mma.cu", []),
     ("dequant.cu", []),

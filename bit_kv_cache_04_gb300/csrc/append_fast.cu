@@ -1,324 +1,10 @@
 // Specialized phase B of quantize-on-append (compiled with --fmad=false like
-// the generic kernels): 32-value blocks of unrotated formats.
-#include "append_common.cuh"
+// the generic kernels): 32-value blocks of unrotated formats with symmetric
+// codes, and the dispatch of every specialized format.
+#include "append_fast.cuh"
 
 namespace kvq {
 namespace {
-
-// ---- specialized phase B: 32-value blocks of unrotated formats ------------------
-//
-// Formats with 32-value blocks and no rotation get their own kernels, one per
-// tensor (K or V), specialized on the bit width, the input dtype and the cold
-// tier's bit width.  The inputs are 16-bit floats, so x / s16 is computed
-// exactly without a divide: with rcp = RN(1/s), q0 = RN(x rcp) and the exact
-// remainder e = x - q0 s (one fma), RN(q0 + e rcp) is RN(x / s) (Markstein's
-// correction step, P. Markstein, IBM J. Res. Dev. 34(1), 1990).  Adding
-// 1.5 * 2^23 (+ the storage bias) then rounds to the nearest integer, ties to
-// even, like rint, and leaves the biased code in the low mantissa bits.  A
-// block only needs the clamp to [-qmax, qmax] when its scale is subnormal or
-// saturated in fp16 (otherwise |x / s16| <= qmax (1 + 2^-10) < qmax + 1/2);
-// it is then applied to x, as |x| <= qmax s16 (an exact product), which
-// gives the same codes as clamping the rounded quotient.
-
-constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
-constexpr float kMinNormalF16 = 6.103515625e-05f;
-
-template <int DT>
-__device__ __forceinline__ float2 raw_pair_to_f32(uint32_t w) {
-  if constexpr (DT == KVQ_DT_F16) {
-    return __half22float2(*reinterpret_cast<const __half2*>(&w));
-  } else {
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-  }
-}
-
-template <int DT>
-__device__ __forceinline__ float in_to_f32_t(uint32_t bits16) {
-  if constexpr (DT == KVQ_DT_F16) return __half2float(__ushort_as_half((unsigned short)bits16));
-  else return __uint_as_float(bits16 << 16);
-}
-
-__device__ __forceinline__ float div_by_scale(float x, float sf, float rcp) {
-  const float q0 = __fmul_rn(x, rcp);
-  const float e = __fmaf_rn(-q0, sf, x);
-  return __fmaf_rn(e, rcp, q0);
-}
-
-// Codes of v[0..31] with scale sf (rcp = RN(1/sf), 0 when sf = 0) as a
-// 32*B-bit little-endian stream (biased codes; two's complement for B = 8);
-// dq (optional) receives code * sf.  The rounded value's float bits are
-// kRoundMagicBits + code + bias; each word accumulates those bits shifted into
-// place (one integer multiply-add per code) and subtracts the magic parts
-// once, which is exact modulo 2^32 because every biased code fits its field.
-// For B = 8 the bias is 128 and flipping each byte's top bit afterwards gives
-// two's complement.
-constexpr uint32_t kRoundMagicBits = 0x4B400000u;  // bits of 1.5 * 2^23
-
-template <int B>
-__device__ __forceinline__ void codes32(const float (&v)[32], float sf, float rcp, uint32_t (&w)[B], float* dq) {
-  constexpr int qmax = (1 << (B - 1)) - 1;
-  constexpr int bias = qmax + 1;
-  constexpr float magic = kRoundMagic + (float)bias;
-#pragma unroll
-  for (int k = 0; k < B; ++k) w[k] = 0;
-  uint32_t corr[B];
-#pragma unroll
-  for (int k = 0; k < B; ++k) corr[k] = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float r = __fadd_rn(div_by_scale(v[j], sf, rcp), magic);
-    if (dq) dq[j] = __fmul_rn(__fsub_rn(r, magic), sf);
-    const uint32_t bits = __float_as_uint(r);
-    const int bit = B * j, k = bit / 32, sh = bit % 32;
-    if (sh + B > 32) {  // a 3-bit code across two words: place the true biased code
-      const uint32_t u = bits - kRoundMagicBits;
-      w[k] += u << sh;
-      w[k + 1] += u >> (32 - sh);
-    } else {
-      w[k] += bits << sh;
-      corr[k] += kRoundMagicBits << sh;
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < B; ++k) {
-    w[k] -= corr[k];
-    if (B == 8) w[k] ^= 0x80808080u;
-  }
-}
-
-// One block of 32 values: scale of absolute maximum m, codes; the block (fp16
-// scale then payload) goes to dst (2-byte aligned) when given.
-template <int B>
-__device__ __forceinline__ void block32(float (&v)[32], float m, uint8_t* dst, float* dq) {
-  constexpr int qmax = (1 << (B - 1)) - 1;
-  const __half s16 = block_scale_of(m, qmax);
-  const float sf = __half2float(s16);
-  const float rcp = sf == 0.f ? 0.f : __frcp_rn(sf);
-  if (!(sf >= kMinNormalF16 && sf < 65504.f)) {
-    const float lim = __fmul_rn((float)qmax, sf);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = fminf(fmaxf(v[j], -lim), lim);
-  }
-  uint32_t w[B];
-  codes32<B>(v, sf, rcp, w, dq);
-  if (!dst) return;
-  uint16_t* p = reinterpret_cast<uint16_t*>(dst);
-  p[0] = __half_as_ushort(s16);
-#pragma unroll
-  for (int k = 0; k < B; ++k) {
-    p[1 + 2 * k] = (uint16_t)w[k];
-    p[2 + 2 * k] = (uint16_t)(w[k] >> 16);
-  }
-}
-
-__device__ __forceinline__ float amax_of(const float (&v)[32]) {
-  float m = 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(v[j]));
-  return m;
-}
-
-// Hot block of v into dst, or (to_cold) the cold block of its dequantized
-// values into dstc.
-template <int B, int CB>
-__device__ __forceinline__ void hot_or_cold(float (&v)[32], bool to_cold, uint8_t* dst, uint8_t* dstc) {
-  if constexpr (CB != 0) {
-    if (to_cold) {
-      float dq[32];
-      block32<B>(v, amax_of(v), nullptr, dq);
-      block32<CB>(dq, amax_of(dq), dstc, nullptr);
-      return;
-    }
-  }
-  block32<B>(v, amax_of(v), dst, nullptr);
-}
-
-// Copies `bytes` (a multiple of 4) from shared `src` to global `dst` (4-byte
-// aligned) with all threads of the block; 16-byte words when both allow.
-__device__ __forceinline__ void block_copy_out(uint8_t* dst, const uint8_t* src, int bytes) {
-  if (((reinterpret_cast<uintptr_t>(dst) | (uintptr_t)bytes) & 15u) == 0) {
-    for (int e = threadIdx.x; e < bytes / 16; e += blockDim.x)
-      reinterpret_cast<uint4*>(dst)[e] = reinterpret_cast<const uint4*>(src)[e];
-  } else {
-    for (int e = threadIdx.x; e < bytes / 4; e += blockDim.x)
-      reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(src)[e];
-  }
-}
-
-// Per-token 32-value blocks: a block of 128 threads takes 128 consecutive
-// tokens of one (layer, sequence, kv head); thread j quantizes token row j
-// slice by slice, with the loads of the following slices in flight.
-// The rows are built in shared memory and written out whole.
-constexpr int kTokItem = 128;
-
-template <int NC, int DT, int B, int CB, int which>
-__global__ void __launch_bounds__(kAppendThreads) quant_token32_kernel(AppendArgs a) {
-  constexpr int D = 128 * NC, SPR = D / 32;
-  constexpr int BB = 2 + 4 * B, ROW = SPR * BB;
-  constexpr int CBB = CB ? 2 + 4 * CB : 0, CROW = SPR * CBB;
-  constexpr int OUTB = kTokItem * (ROW > CROW ? ROW : CROW);
-  static_assert(kTokItem == kAppendThreads, "one token row per thread");
-  __shared__ __align__(16) uint8_t out[OUTB];
-  __shared__ uint32_t page_bad;
-  const Layout& lo = a.lo;
-  const int li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B, h = blockIdx.y;
-  const int layer = a.layer0 + li;
-  SeqSpan s = read_span(a, seq);
-  if (!s.ok) return;
-  const int q0 = q_end_of(lo, s.T0), q1 = q_end_of(lo, s.T1), c1 = c_end_of(lo, s.T1);
-  const int base = (q0 / kTokItem) * kTokItem + blockIdx.x * kTokItem;
-  const int u0 = max(base, q0), u1 = min(base + kTokItem, q1);
-  if (u0 >= u1) return;
-  const int n_tok = u1 - u0;
-  if (threadIdx.x == 0) page_bad = 0;
-  const int j = threadIdx.x;
-  const int t = u0 + j;
-  // tiered chunks start at multiples of 32 (Gamma = 32), and cold rows come
-  // before hot rows, so rows of both strides never overlap in the tile
-  const bool to_cold = CB != 0 && lo.tiered && t < c1;
-  if (j < n_tok) {
-    const uint4* src = reinterpret_cast<const uint4*>(t < s.T0 ? resid_row(lo, a.cp, which, layer, seq, h, t)
-                                                                 : input_row(a, which, li, s, h, t));
-    uint8_t* dst = out + j * (to_cold ? CROW : ROW);
-    // PF slices of the row in flight: the whole 128-value row, or two slices
-    // of a 256-value row
-    constexpr int PF = SPR <= 4 ? SPR : 2;
-    uint4 r[PF][4];
-#pragma unroll
-    for (int p = 0; p < PF; ++p)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) r[p][q] = src[4 * p + q];
-#pragma unroll
-    for (int sl = 0; sl < SPR; ++sl) {
-      float v[32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 c = r[sl % PF][q];
-        const uint32_t ww[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = raw_pair_to_f32<DT>(ww[e]);
-          v[8 * q + 2 * e] = f.x;
-          v[8 * q + 2 * e + 1] = f.y;
-        }
-      }
-      if (sl + PF < SPR) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) r[sl % PF][q] = src[4 * (sl + PF) + q];
-      }
-      hot_or_cold<B, CB>(v, to_cold, dst + sl * BB, dst + sl * CBB);
-    }
-  }
-  __syncthreads();
-  if (!lo.paged && !lo.tiered) {
-    bool bad = false;
-    block_copy_out(main_row(lo, a.cp, which, layer, seq, h, u0, &bad), out, n_tok * ROW);
-    return;
-  }
-  // tiered or paged: whole rows, one warp per row
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < n_tok; r += kAppendThreads / 32) {
-    const bool cold = CB != 0 && lo.tiered && u0 + r < c1;
-    const int rowb = cold ? CROW : ROW;
-    bool bad = false;
-    uint8_t* dst = cold ? cold_row(lo, a.cp, which, layer, seq, h, u0 + r)
-                        : main_row(lo, a.cp, which, layer, seq, h, u0 + r, &bad);
-    if (bad) {
-      page_bad = 1;
-      continue;
-    }
-    for (int e = lane; e < rowb / 4; e += 32)
-      reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(out + r * rowb)[e];
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && page_bad) atomicOr(a.status, KVQ_DEV_PAGE);
-}
-
-// Per-channel blocks over 32-token groups: thread = (group lane, channel
-// pair); a block takes NG = GPC x kGroupSteps consecutive groups, each thread
-// kGroupSteps of them in turn.  Each group row (D blocks) is built in shared
-// memory and written out whole.
-constexpr int kGroupSteps = 2;
-
-template <int NC, int DT, int B, int CB, int which>
-__global__ void __launch_bounds__(kAppendThreads, 4) quant_channel32_kernel(AppendArgs a) {
-  constexpr int D = 128 * NC, PAIRS = D / 2, GPC = kAppendThreads / PAIRS, NG = GPC * kGroupSteps;
-  constexpr int BB = 2 + 4 * B, GROW = D * BB;
-  constexpr int CBB = CB ? 2 + 4 * CB : 0, CGROW = D * CBB;
-  constexpr int SLOT = GROW > CGROW ? GROW : CGROW;
-  __shared__ __align__(16) uint8_t out[NG * SLOT];
-  const Layout& lo = a.lo;
-  const int li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B, h = blockIdx.y;
-  const int layer = a.layer0 + li;
-  SeqSpan s = read_span(a, seq);
-  if (!s.ok) return;
-  const int q0 = q_end_of(lo, s.T0), q1 = q_end_of(lo, s.T1), c1 = c_end_of(lo, s.T1);
-  const int base = (q0 / (kTile * NG)) * (kTile * NG) + blockIdx.x * (kTile * NG);
-  if (base + kTile * NG <= q0 || base >= q1) return;
-  const int gl = threadIdx.x / PAIRS, cp = threadIdx.x % PAIRS;
-#pragma unroll 1
-  for (int gs = 0; gs < kGroupSteps; ++gs) {
-    const int gi = gs * GPC + gl;
-    const int t0 = base + kTile * gi;
-    if (t0 < q0 || t0 >= q1) continue;
-    const bool to_cold = CB != 0 && lo.tiered && t0 < c1;
-    // the group's rows: window ring slots for tokens below T0, new input rows
-    // (a fixed stride apart) from T0 on
-    const int n_rw = min(max(s.T0 - t0, 0), kTile);  // leading tokens from the window
-    const uint32_t* in = nullptr;
-    if (n_rw < kTile) in = reinterpret_cast<const uint32_t*>(input_row(a, which, li, s, h, t0 + n_rw)) + cp;
-    const int in_stride = lo.H * D / 2;
-    uint32_t raw[32];
-    if (n_rw == 0) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) raw[j] = in[j * in_stride];
-    } else {
-      const uint32_t* rw = reinterpret_cast<const uint32_t*>(resid_row(lo, a.cp, which, layer, seq, h, 0)) + cp;
-      int slot = t0 % lo.ring;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        raw[j] = j < n_rw ? rw[slot * (D / 2)] : in[(j - n_rw) * in_stride];
-        slot = slot + 1 == lo.ring ? 0 : slot + 1;
-      }
-    }
-#pragma unroll
-    for (int hc = 0; hc < 2; ++hc) {
-      float v[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const uint32_t h16 = hc ? (raw[j] >> 16) : (raw[j] & 0xFFFFu);
-        v[j] = in_to_f32_t<DT>(h16);
-      }
-      const int c = 2 * cp + hc;
-      hot_or_cold<B, CB>(v, to_cold, out + gi * SLOT + c * BB, out + gi * SLOT + c * CBB);
-    }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int g = 0; g < NG; ++g) {
-    const int tg = base + kTile * g;
-    if (tg < q0 || tg >= q1) continue;
-    const bool cold = CB != 0 && lo.tiered && tg < c1;
-    bool bad = false;
-    uint8_t* dst = cold ? cold_row(lo, a.cp, which, layer, seq, h, tg) : main_row(lo, a.cp, which, layer, seq, h, tg, &bad);
-    block_copy_out(dst, out + g * SLOT, cold ? CGROW : GROW);
-  }
-}
-
-template <int NC, int DT, int B, int CB>
-void launch_token32(const AppendArgs& a, int which, cudaStream_t st) {
-  const int chunks = (a.max_new + kTokItem - 1) / kTokItem + 2;
-  const dim3 grid(chunks, a.lo.H, a.n_layers * a.lo.B);
-  if (which == 0) quant_token32_kernel<NC, DT, B, CB, 0><<<grid, kAppendThreads, 0, st>>>(a);
-  else quant_token32_kernel<NC, DT, B, CB, 1><<<grid, kAppendThreads, 0, st>>>(a);
-}
-
-template <int NC, int DT, int B, int CB>
-void launch_channel32(const AppendArgs& a, cudaStream_t st) {
-  constexpr int span = kTile * (kAppendThreads / (64 * NC)) * kGroupSteps;
-  const int chunks = (a.max_new + span - 1) / span + 2;
-  quant_channel32_kernel<NC, DT, B, CB, 0><<<dim3(chunks, a.lo.H, a.n_layers * a.lo.B), kAppendThreads, 0, st>>>(a);
-}
 
 // Launches the specialized phase B of tensor `which` when one exists for its
 // format; false otherwise (nothing launched).
@@ -327,8 +13,11 @@ bool launch_fast_tensor(const AppendArgs& a, int which, bool dry, cudaStream_t s
   const Layout& lo = a.lo;
   const FmtInfo& f = fmt_main(lo, which);
   const bool rot = (lo.flags & (which ? KVQ_ROTATE_V : KVQ_ROTATE_K)) != 0;
-  if (rot || f.group != 32 || f.zp) return false;
+  if (rot || f.group != 32) return false;
   const int cb = lo.tiered ? fmt_cold(lo, which).bits : 0;
+  if (f.zp) {  // asymmetric blocks (4- or 2-bit, 4 -> 2 tiers): their own translation units
+    return DT == KVQ_DT_F16 ? launch_fast_zp_f16(a, which, dry, st) : launch_fast_zp_bf16(a, which, dry, st);
+  }
   if (f.axis == KVQ_AXIS_CHANNEL) {  // keys (values grouped per channel take the generic kernel)
     if (which != 0) return false;
     if (f.bits == 4 && cb == 0) return dry || (launch_channel32<NC, DT, 4, 0>(a, st), true);

@@ -191,8 +191,9 @@ __device__ __forceinline__ float block_value(const uint8_t* blk, int bits, int c
 // s16 = fp16(min((mx - mn) / (2^b - 1), 65504)); z16 = fp16(mn clipped to
 // +-65504); code = clamp(rint((x - z) / s), 0, 2^b - 1), 0 when s = 0.  The
 // block (scale, zero, codes in little-endian b-bit fields) goes to blk when
-// given; dq (optional) receives code * s + z.
-__device__ __forceinline__ void quant_zp32(const float* v, int bits, uint8_t* blk, float* dq) {
+// given; dq (optional) receives code * s + z.  Not inlined: the generic
+// kernels call it from many places and it holds 32 IEEE divides.
+static __device__ __noinline__ void quant_zp32_mem(const float* v, int bits, uint8_t* blk, float* dq) {
   const int qlev = (1 << bits) - 1;
   float mn = v[0], mx = v[0];
   for (int j = 1; j < 32; ++j) {
@@ -219,6 +220,15 @@ __device__ __forceinline__ void quant_zp32(const float* v, int bits, uint8_t* bl
     p[2 + 2 * k] = (uint16_t)w[k];
     p[3 + 2 * k] = (uint16_t)(w[k] >> 16);
   }
+}
+
+// Array form of quant_zp32_mem: passes a copy, so that the caller's array
+// keeps its registers.
+__device__ __forceinline__ void quant_zp32(const float (&v)[32], int bits, uint8_t* blk, float* dq) {
+  float t[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) t[j] = v[j];
+  quant_zp32_mem(t, bits, blk, dq);
 }
 
 // Index of u among the 15 ascending thresholds: how many lie strictly below.

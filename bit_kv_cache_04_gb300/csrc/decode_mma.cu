@@ -56,16 +56,23 @@ constexpr float kLog2eF = 1.4426950408889634f;
 constexpr int bits_k(int kf) { return kf == KF_T8 ? 8 : kf == KF_T3 ? 3 : kf == KF_CH2 ? 2 : 4; }
 constexpr int bits_v(int vf) { return vf == VF_T8 ? 8 : vf == VF_T3 ? 3 : vf == VF_T2 ? 2 : 4; }
 constexpr int align16(int x) { return (x + 15) / 16 * 16; }
+__host__ __device__ constexpr float code_bias(int bits) { return (float)(1 << (bits - 1)); }  // symmetric storage bias
 
-// Byte geometry of one tier's formats.
-template <int D, int KF_, int KG_, int VF_, int VG_>
+// Byte geometry of one tier's formats.  Z: asymmetric blocks (fp16 scale,
+// fp16 zero, codes 0..2^b-1) for K and V.  The code unpackers return the
+// field minus the symmetric storage bias beta = 2^(b-1), so an asymmetric
+// value c s + z is read as (c - beta) s + (z + beta s): the codes take the
+// symmetric path unchanged and the zero z' = z + beta s adds a term per block.
+template <int D, int KF_, int KG_, int VF_, int VG_, bool Z_ = false>
 struct Tier {
   static constexpr int KF = KF_, KG = KG_, VF = VF_, VG = VG_;
+  static constexpr bool Z = Z_;
   static constexpr int KB = bits_k(KF), VB = bits_v(VF);
   static constexpr bool KCH = KF == KF_CH4 || KF == KF_CH2;
   static constexpr bool KLUT = KF == KF_TQ, VLUT = VF == VF_TQ;  // codes index the TBQ4 table
-  static constexpr int KBB = 2 + (KCH ? 32 : KG) * KB / 8;  // block bytes
-  static constexpr int VBB = 2 + VG * VB / 8;
+  static constexpr int HDR = Z ? 4 : 2;                     // block header bytes
+  static constexpr int KBB = HDR + (KCH ? 32 : KG) * KB / 8;  // block bytes
+  static constexpr int VBB = HDR + VG * VB / 8;
   static constexpr int KROW = KCH ? D * KBB : (D / KG) * KBB;  // group row / token row
   static constexpr int VROW = (D / VG) * VBB;
   static constexpr int KSTAGE = KCH ? KROW : 32 * KROW;
@@ -74,6 +81,7 @@ struct Tier {
   static constexpr int VSPB = VG / 32;
   static constexpr int KSPAN = 32 * KB / 8;  // code bytes of a span of one token
   static constexpr int VSPAN = 32 * VB / 8;
+  static_assert(!Z || (KCH && VG == 32 && !KLUT && !VLUT), "asymmetric blocks: per-channel K, 32-value V blocks");
 };
 
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
@@ -85,13 +93,16 @@ struct Cfg {
   using HOT = HOT_;
   using COLD = COLD_;
   static constexpr bool HAS_COLD = HAS_COLD_, ROPE = ROPE_;
+  static constexpr bool Z = HOT::Z;
+  static_assert(!HAS_COLD || COLD::Z == HOT::Z, "both tiers asymmetric or neither");
   static constexpr int KSTAGE = HAS_COLD ? cmax(HOT::KSTAGE, COLD::KSTAGE) : HOT::KSTAGE;
   static constexpr int VSTAGE = HAS_COLD ? cmax(HOT::VSTAGE, COLD::VSTAGE) : HOT::VSTAGE;
   static constexpr int VOFF = align16(KSTAGE + 16);
   static constexpr int STAGE = VOFF + align16(VSTAGE + 16);
   static constexpr int KC = D / 16;  // k-chunks
   static constexpr int NS = D / 32;  // spans
-  static constexpr int QSM = KC * NT * 32 * (16 + (ROPE ? 16 : 0));  // per-lane query fragments
+  // per-lane query fragments (+ fp32 query for RoPE, + fp32 query by head for the zero terms)
+  static constexpr int QSM = KC * NT * 32 * (16 + (ROPE ? 16 : 0) + (Z ? 8 : 0));
   static constexpr int MIN_CTAS = D == 128 ? 4 : 2;  // CTAs per SM the register budget aims at
   static constexpr int SMEM = QSM + kWarps * kStages * STAGE;
 };
@@ -312,6 +323,9 @@ template <class C>
 struct WarpState {
   float o[C::KC][C::NT][4];
   float m[C::NT], l[C::NT];
+  // asymmetric V: sum over this lane's tokens of p z' per 32-channel block
+  // (for the lane's head 4 nt + tq), rescaled with o
+  float zo[C::Z ? C::NS : 1][C::NT];
 };
 
 // Online softmax over one group's scores; returns the probabilities of the
@@ -350,6 +364,10 @@ __device__ __forceinline__ void online_softmax(WarpState<C>& ws, float (&S)[2][C
       for (int i = 0; i < C::KC; ++i)
 #pragma unroll
         for (int e = 0; e < 4; ++e) ws.o[i][nt][e] *= alpha;
+      if constexpr (C::Z) {
+#pragma unroll
+        for (int s = 0; s < C::NS; ++s) ws.zo[s][nt] *= alpha;
+      }
     }
   }
 }
@@ -366,12 +384,13 @@ __device__ __forceinline__ void p_fragments(float pa, float pb, uint32_t& b0, ui
 // Per-thread context of the decode kernel shared with its helpers.
 template <class C>
 struct Ctx {
-  int gq, tq, lane;
+  int gq, tq, lane, g;
   bool lo_part;
   uint32_t lo_mask;
   const uint2* qb;        // [KC][NT][32]: B fragments (hi or lo part)
   const uint2* qh;        // [KC][NT][32]: query half pairs
   const float4* qr;       // [KC][NT][32]: fp32 query (RoPE)
+  const float* qz;        // [4 NT][D]: fp32 query by head, zero past g (asymmetric K)
   const float2* rope_base;
   const float4* rope_frag;  // [KC/2][4 tokens k][2 pairs][32 lanes]: R(j) of this lane's channels
   uint32_t lut[4];          // TBQ4 table magnitudes: low bytes (2 words), high bytes (2 words)
@@ -440,19 +459,31 @@ __device__ __forceinline__ void pv_packed(const Ctx<C>& cx, WarpState<C>& ws, co
 #pragma unroll
       for (int mu = 0; mu < 2; ++mu) {
         const int ra = 4 * gq + 2 * mu;
-        const float sva = block_scale(vsm + ra * TR::VROW + bv * TR::VBB);
-        const float svb = block_scale(vsm + (ra + 1) * TR::VROW + bv * TR::VBB);
+        const uint8_t* ha = vsm + ra * TR::VROW + bv * TR::VBB;
+        const uint8_t* hb = ha + TR::VROW;
+        const float sva = block_scale(ha);
+        const float svb = block_scale(hb);
+        float zpa = 0.f, zpb = 0.f;  // z' = z + beta s of rows a and b (asymmetric V)
+        if constexpr (TR::Z) {
+          zpa = fmaf(code_bias(TR::VB), sva, block_scale(ha + 2));
+          zpb = fmaf(code_bias(TR::VB), svb, block_scale(hb + 2));
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const float pa = ra < n_valid ? p[nt][2 * mu] * sva : 0.f;
           const float pbb = ra + 1 < n_valid ? p[nt][2 * mu + 1] * svb : 0.f;
           p_fragments(pa, pbb, pb[mu][nt][0], pb[mu][nt][1]);
+          if constexpr (TR::Z) {
+            const float za = ra < n_valid ? p[nt][2 * mu] * zpa : 0.f;
+            const float zb = ra + 1 < n_valid ? p[nt][2 * mu + 1] * zpb : 0.f;
+            ws.zo[bv][nt] += za + zb;
+          }
         }
       }
 #pragma unroll
       for (int ss = 0; ss < TR::VSPB; ++ss) {
         const int s = bv * TR::VSPB + ss;
-        const int off = bv * TR::VBB + 2 + ss * TR::VSPAN;
+        const int off = bv * TR::VBB + TR::HDR + ss * TR::VSPAN;
 #pragma unroll
         for (int mu = 0; mu < 2; ++mu) {
           const int T1 = 8 * tq + 2 * mu;
@@ -485,7 +516,7 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
         rope_query_pair<C>(cx, base, kcp, ql, qu);
         const int c = 32 * (kcp >> 1) + 8 * tq + 2 * (kcp & 1);
         const int ch[4] = {c, c + 4, c + 1, c + 5};
-        float sl[4], su[4];
+        float sl[4], su[4], zl[4] = {0.f, 0.f, 0.f, 0.f}, zu[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t xl[2], xu[2];
         uint32_t chl[4], chu[4];
 #pragma unroll
@@ -494,8 +525,12 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
           const uint8_t* bu = ksm + (ch[q] + D / 2) * TR::KBB;
           sl[q] = block_scale(bl);
           su[q] = block_scale(bu);
-          chl[q] = TR::KB == 4 ? ld_u16(bl + 2 + 2 * gq) : (uint32_t)bl[2 + gq];
-          chu[q] = TR::KB == 4 ? ld_u16(bu + 2 + 2 * gq) : (uint32_t)bu[2 + gq];
+          if constexpr (TR::Z) {  // z' = z + beta s
+            zl[q] = fmaf(code_bias(TR::KB), sl[q], block_scale(bl + 2));
+            zu[q] = fmaf(code_bias(TR::KB), su[q], block_scale(bu + 2));
+          }
+          chl[q] = TR::KB == 4 ? ld_u16(bl + TR::HDR + 2 * gq) : (uint32_t)bl[TR::HDR + gq];
+          chu[q] = TR::KB == 4 ? ld_u16(bu + TR::HDR + 2 * gq) : (uint32_t)bu[TR::HDR + gq];
         }
         xl[0] = __byte_perm(chl[0], chl[1], 0x5410);
         xl[1] = __byte_perm(chl[2], chl[3], 0x5410);
@@ -528,8 +563,10 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
             const float2 l23 = __half22float2(*reinterpret_cast<const __half2*>(&cl1[k]));
             const float2 u01 = __half22float2(*reinterpret_cast<const __half2*>(&cu0[k]));
             const float2 u23 = __half22float2(*reinterpret_cast<const __half2*>(&cu1[k]));
-            const float lv[4] = {l01.x * sl[0], l01.y * sl[1], l23.x * sl[2], l23.y * sl[3]};
-            const float uv[4] = {u01.x * su[0], u01.y * su[1], u23.x * su[2], u23.y * su[3]};
+            const float lv[4] = {fmaf(l01.x, sl[0], zl[0]), fmaf(l01.y, sl[1], zl[1]), fmaf(l23.x, sl[2], zl[2]),
+                                 fmaf(l23.y, sl[3], zl[3])};
+            const float uv[4] = {fmaf(u01.x, su[0], zu[0]), fmaf(u01.y, su[1], zu[1]), fmaf(u23.x, su[2], zu[2]),
+                                 fmaf(u23.y, su[3], zu[3])};
             rope_key_frags(cs, lv, uv, rr, ah, al);
           }
 #pragma unroll
@@ -559,11 +596,11 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
         const uint8_t* b4p = b1p + 5 * TR::KBB;
         uint32_t k12[4], k34[4];
         if constexpr (TR::KB == 4) {
-          dq4(__byte_perm(ld_u16(b1p + 2 + 2 * gq), ld_u16(b2p + 2 + 2 * gq), 0x5410), k12);
-          dq4(__byte_perm(ld_u16(b3p + 2 + 2 * gq), ld_u16(b4p + 2 + 2 * gq), 0x5410), k34);
+          dq4(__byte_perm(ld_u16(b1p + TR::HDR + 2 * gq), ld_u16(b2p + TR::HDR + 2 * gq), 0x5410), k12);
+          dq4(__byte_perm(ld_u16(b3p + TR::HDR + 2 * gq), ld_u16(b4p + TR::HDR + 2 * gq), 0x5410), k34);
         } else {
-          const uint32_t x12 = __byte_perm((uint32_t)b1p[2 + gq], (uint32_t)b2p[2 + gq], 0x5410);
-          const uint32_t x34 = __byte_perm((uint32_t)b3p[2 + gq], (uint32_t)b4p[2 + gq], 0x5410);
+          const uint32_t x12 = __byte_perm((uint32_t)b1p[TR::HDR + gq], (uint32_t)b2p[TR::HDR + gq], 0x5410);
+          const uint32_t x34 = __byte_perm((uint32_t)b3p[TR::HDR + gq], (uint32_t)b4p[TR::HDR + gq], 0x5410);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             k12[k] = code_pair<2>(x12, k);
@@ -592,6 +629,47 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) S[mu][nt][e] += Sx[mu][nt][e];
+      if constexpr (TR::Z) {
+        // zero term of the group, the same for its 32 tokens: sum_c q'_c z'_c
+        // with z'_c = z_c + beta s_c; lane l takes channels CPL l .. CPL l + CPL - 1
+        constexpr int CPL = D / 32;
+        static_assert(CPL % 4 == 0, "whole float4 query loads");
+        float zq[CPL];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+          const uint8_t* blk = ksm + (CPL * lane + j) * TR::KBB;
+          zq[j] = fmaf(code_bias(TR::KB), block_scale(blk), block_scale(blk + 2));
+        }
+        const int g = cx.g;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float zs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int hl = 0; hl < 4; ++hl) {
+            if (4 * nt + hl >= g) continue;  // warp-uniform
+            const float* qrow = cx.qz + (4 * nt + hl) * D + CPL * lane;
+            float acc = 0.f;
+#pragma unroll
+            for (int j4 = 0; j4 < CPL / 4; ++j4) {
+              const float4 qv = *reinterpret_cast<const float4*>(qrow + 4 * j4);
+              acc = fmaf(qv.x, zq[4 * j4], acc);
+              acc = fmaf(qv.y, zq[4 * j4 + 1], acc);
+              acc = fmaf(qv.z, zq[4 * j4 + 2], acc);
+              acc = fmaf(qv.w, zq[4 * j4 + 3], acc);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            zs[hl] = acc;
+          }
+          // this lane's head is 4 nt + tq: add to its hi column (rows gq, gq + 8)
+          const float zt = tq == 0 ? zs[0] : tq == 1 ? zs[1] : tq == 2 ? zs[2] : zs[3];
+#pragma unroll
+          for (int mu = 0; mu < 2; ++mu) {
+            S[mu][nt][0] += zt;
+            S[mu][nt][2] += zt;
+          }
+        }
+      }
     } else {
       // per-token K: each K block's scale multiplies its partial scores
 #pragma unroll
@@ -608,8 +686,8 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
           for (int mu = 0; mu < 2; ++mu) {
             const int ra = 4 * gq + 2 * mu;
             uint32_t wa[4], wb[4];
-            k_token_pairs<TR>(ksm + ra * TR::KROW + kb * TR::KBB + 2 + ss * TR::KSPAN, tq, wa, cx.lut);
-            k_token_pairs<TR>(ksm + (ra + 1) * TR::KROW + kb * TR::KBB + 2 + ss * TR::KSPAN, tq, wb, cx.lut);
+            k_token_pairs<TR>(ksm + ra * TR::KROW + kb * TR::KBB + TR::HDR + ss * TR::KSPAN, tq, wa, cx.lut);
+            k_token_pairs<TR>(ksm + (ra + 1) * TR::KROW + kb * TR::KBB + TR::HDR + ss * TR::KSPAN, tq, wb, cx.lut);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               const uint2 q0 = qb[((2 * s) * NT + nt) * 32 + lane];
@@ -642,6 +720,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   uint2* qb = reinterpret_cast<uint2*>(smem);  // [KC][NT][32 lanes]: this lane's B fragment (b0, b1)
   uint2* qh = qb + KC * NT * 32;               // [KC][NT][32 lanes]: query half pairs (per-channel K)
   float4* qr = reinterpret_cast<float4*>(qh + KC * NT * 32);  // [KC][NT][32 lanes]: fp32 query (RoPE)
+  float* qz = reinterpret_cast<float*>(qr + (C::ROPE ? KC * NT * 32 : 0));  // [4 NT][D] (asymmetric K)
   uint8_t* stage_base = smem + C::QSM;
   __shared__ float qmax_s[kWarps];
   __shared__ uint32_t bad_page;
@@ -724,6 +803,12 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
       qh[e] = make_uint2(pack_h2(v0, v1), pack_h2(v2, v3));
       if constexpr (C::ROPE) qr[e] = make_float4(v0, v1, v2, v3);
     }
+    if constexpr (C::Z) {
+      for (int e = tid; e < 4 * NT * D; e += kThreadsMma) {
+        const int hh = e / D;
+        qz[e] = hh < g ? qf[e] * qnorm : 0.f;
+      }
+    }
     __syncthreads();
   }
   const bool lo_part = (gq & 1) != 0;
@@ -738,6 +823,8 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   cx.qb = qb;
   cx.qh = qh;
   cx.qr = qr;
+  cx.qz = qz;
+  cx.g = g;
   cx.rope_base = a.rope;
   cx.rope_frag = reinterpret_cast<const float4*>(a.rope + (int64_t)(a.rope_base_rows + kTile) * (D / 2));
   if constexpr (C::HOT::KLUT || C::HOT::VLUT) {
@@ -763,6 +850,8 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   for (int nt = 0; nt < NT; ++nt) {
     ws.m[nt] = -INFINITY;
     ws.l[nt] = 0.f;
+#pragma unroll
+    for (int s = 0; s < (C::Z ? C::NS : 1); ++s) ws.zo[s][nt] = 0.f;
   }
   uint8_t* wst = stage_base + warp * kStages * C::STAGE;
 
@@ -1003,6 +1092,17 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     l += __shfl_xor_sync(0xffffffffu, l, 4);
     l += __shfl_xor_sync(0xffffffffu, l, 8);
     l += __shfl_xor_sync(0xffffffffu, l, 16);
+    float zo[C::Z ? C::NS : 1] = {};  // zero-point part of the output per 32-channel block
+    if constexpr (C::Z) {
+#pragma unroll
+      for (int s = 0; s < C::NS; ++s) {
+        float z = ws.zo[s][nt];
+        z += __shfl_xor_sync(0xffffffffu, z, 4);
+        z += __shfl_xor_sync(0xffffffffu, z, 8);
+        z += __shfl_xor_sync(0xffffffffu, z, 16);
+        zo[s] = z;
+      }
+    }
     const int hh = 4 * nt + tq;
     if (hh < g) {
       if (gq == 0) {
@@ -1015,8 +1115,9 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int ch = 32 * s + 4 * gq + 2 * e;
-          orow[ch] = ws.o[2 * s + e][nt][0] + ws.o[2 * s + e][nt][1];
-          orow[ch + 1] = ws.o[2 * s + e][nt][2] + ws.o[2 * s + e][nt][3];
+          const float zadd = C::Z ? zo[C::Z ? s : 0] : 0.f;
+          orow[ch] = ws.o[2 * s + e][nt][0] + ws.o[2 * s + e][nt][1] + zadd;
+          orow[ch + 1] = ws.o[2 * s + e][nt][2] + ws.o[2 * s + e][nt][3] + zadd;
         }
     }
   }
@@ -1107,8 +1208,8 @@ bool fmt_is(const FmtInfo& f, int bits, int group, int axis) {
   return f.bits == bits && f.group == group && f.axis == axis;
 }
 
-template <int D, int KF, int KG, int VF, int VG>
-using T_ = Tier<D, KF, KG, VF, VG>;
+template <int D, int KF, int KG, int VF, int VG, bool Z = false>
+using T_ = Tier<D, KF, KG, VF, VG, Z>;
 
 }  // namespace
 
@@ -1121,7 +1222,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   if (lo.ring) ok = ok && lo.dtype == KVQ_DT_F16 && !(lo.flags & (KVQ_ROTATE_K | KVQ_ROTATE_V));
   if (lo.paged) ok = ok && (lo.pt == 16 || lo.pt == 32);
   if (lo.kf.codebook != lo.vf.codebook) ok = false;  // one tensor TBQ4, the other not: generic kernel
-  if (lo.kf.zp || lo.vf.zp) ok = false;               // asymmetric blocks: generic kernel
+  if (lo.kf.zp != lo.vf.zp) ok = false;              // one tensor asymmetric, the other not: generic kernel
   if (!ok) return launch_decode_generic(a, st);
   if (lo.kf.codebook) {  // TBQ4 K and V (rotated 4-bit blocks of 128)
     if (lo.D == 128 && lo.g <= 4)
@@ -1134,6 +1235,25 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   const bool kivi4 = fmt_is(k, 4, 32, CH) && fmt_is(v, 4, 32, TOK);
   using KIVI4 = T_<128, KF_CH4, 32, VF_T4, 32>;
   using KIVI2 = T_<128, KF_CH2, 32, VF_T2, 32>;
+  if (k.zp) {  // asymmetric KIVI: per-channel K, per-token V, blocks of 32
+    using Z4 = T_<128, KF_CH4, 32, VF_T4, 32, true>;
+    using Z2 = T_<128, KF_CH2, 32, VF_T2, 32, true>;
+    const bool kivi2 = fmt_is(k, 2, 32, CH) && fmt_is(v, 2, 32, TOK);
+    if (lo.D == 128 && lo.g <= 4) {
+      if (lo.tiered) {
+        if (kivi4 && fmt_is(lo.kc, 2, 32, CH) && fmt_is(lo.vc, 2, 32, TOK)) {
+          if (rope) return launch_mma<Cfg<128, 1, Z4, Z2, true, true>>(a, st);
+          return launch_mma<Cfg<128, 1, Z4, Z2, true, false>>(a, st);
+        }
+      } else if (kivi4) {
+        if (rope) return launch_mma<Cfg<128, 1, Z4, Z4, false, true>>(a, st);
+        return launch_mma<Cfg<128, 1, Z4, Z4, false, false>>(a, st);
+      } else if (kivi2 && !rope) {
+        return launch_mma<Cfg<128, 1, Z2, Z2, false, false>>(a, st);
+      }
+    }
+    return launch_decode_generic(a, st);
+  }
   if (lo.D == 128 && lo.g <= 4 && kivi4) {
     if (lo.tiered) {
       if (fmt_is(lo.kc, 2, 32, CH) && fmt_is(lo.vc, 2, 32, TOK)) {

@@ -25,8 +25,8 @@ from typing import List, Optional
 
 import torch
 
-from .kvq import (AXIS_CHANNEL, AXIS_TOKEN, DT_BF16, DT_F16, K_PRE_ROPE, ROTATE_K, ROTATE_V, TBQ4_K, TBQ4_V, Config,
-                  Fmt)
+from .kvq import (AXIS_CHANNEL, AXIS_TOKEN, DT_BF16, DT_F16, K_PRE_ROPE, ROTATE_K, ROTATE_V, TBQ4_K, TBQ4_V, ZP_K, ZP_V,
+                  Config, Fmt)
 
 SIGN_SEED = 0x5EED5EED
 
@@ -69,6 +69,11 @@ def make(name: str, extra_tokens: int = 64) -> Workload:
         cfg = Config(L=32, H_kv=32, H_q=32, D=128, batch=1, max_T=32768 + extra_tokens, in_dtype=F16,
                      k_fmt=Fmt(4, 32, AXIS_CHANNEL), v_fmt=Fmt(4, 32), residual_window=128)
         return Workload(name, cfg, [32768], "llama", extra_tokens)
+    if name in ("llama2_7b_kivi4_zp", "llama2_7b_kivi2_zp"):
+        b = 4 if "kivi4" in name else 2
+        cfg = Config(L=32, H_kv=32, H_q=32, D=128, batch=1, max_T=32768 + extra_tokens, in_dtype=F16,
+                     k_fmt=Fmt(b, 32, AXIS_CHANNEL), v_fmt=Fmt(b, 32), residual_window=128, flags=ZP_K | ZP_V)
+        return Workload(name, cfg, [32768], "llama", extra_tokens)
     if name == "gqa8b_hadamard4_paged":
         lengths = _ragged(16, 2048, 8192, 3)
         max_T = 8192 + extra_tokens
@@ -93,7 +98,7 @@ def make(name: str, extra_tokens: int = 64) -> Workload:
 
 
 ALL = ("q8_0_mha_1k", "q4_0_mha_1k", "llama2_7b_kivi4", "gqa8b_hadamard4_paged", "ctx262k_hadamard4",
-       "ctx262k_hadamard3", "mistral7b_hotcold", "ctx262k_tbq4")
+       "ctx262k_hadamard3", "mistral7b_hotcold", "ctx262k_tbq4", "llama2_7b_kivi4_zp", "llama2_7b_kivi2_zp")
 
 
 def _torch_dtype(cfg: Config):

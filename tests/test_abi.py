@@ -118,9 +118,12 @@ def test_launch_counts():
     assert K.kvq_launch_counts(W.make("mistral7b_hotcold").cfg) == (1 + 2 + 1, 1)
     assert K.kvq_launch_counts(W.make("q8_0_mha_1k").cfg) == (2, 1)
     assert K.kvq_launch_counts(W.make("ctx262k_hadamard4").cfg) == (1, 1)
-    # asymmetric blocks take the generic quantize kernel (+ window copy)
+    # asymmetric KIVI blocks take the specialized kernels too; per-token
+    # 4-bit K with 2-bit V has no specialized pair: one generic launch
     zp = _bad(flags=K.ZP_K | K.ZP_V, k_fmt=K.Fmt(4, 32, K.AXIS_CHANNEL), residual_window=128)
-    assert K.kvq_launch_counts(zp) == (1 + 1, 1)
+    assert K.kvq_launch_counts(zp) == (1 + 2, 1)
+    zp8 = _bad(flags=K.ZP_V, k_fmt=K.Fmt(8, 32), v_fmt=K.Fmt(2, 32))
+    assert K.kvq_launch_counts(zp8) == (2, 1)
 
 
 def test_tbq4_codebook_matches_oracle():

@@ -53,6 +53,11 @@ CASES = [
     ("zp_tiers_f16", 128, K.DT_F16, K.Fmt(4, 32, CH), K.Fmt(4, 32), K.Fmt(2, 32, CH), K.Fmt(2, 32), 64, 32,
      K.ZP_K | K.ZP_V),
     ("zp_v_only_d256", 256, K.DT_F16, K.Fmt(4, 32, CH), K.Fmt(2, 32), None, None, 0, 32, K.ZP_V),
+    ("zp_kivi2_f16", 128, K.DT_F16, K.Fmt(2, 32, CH), K.Fmt(2, 32), None, None, 0, 64, K.ZP_K | K.ZP_V),
+    ("zp_tiers_rope_f16", 128, K.DT_F16, K.Fmt(4, 32, CH), K.Fmt(4, 32), K.Fmt(2, 32, CH), K.Fmt(2, 32), 64, 32,
+     K.ZP_K | K.ZP_V | K.K_PRE_ROPE),
+    ("zp_kivi4_rope_f16", 128, K.DT_F16, K.Fmt(4, 32, CH), K.Fmt(4, 32), None, None, 0, 0,
+     K.ZP_K | K.ZP_V | K.K_PRE_ROPE),
 ]
 
 LENGTHS = [301, 160, 33]
@@ -107,8 +112,10 @@ def _case_tensors(kind, cfg, lengths, which, gen):
 def test_append_bytes_match_oracle(case, kind):
     name, D, dtype, kf, vf, kc, vc, hot, R = case[:9]
     flags = case[9] if len(case) > 9 else 0
-    cfg = K.Config(L=1, H_kv=3, H_q=3, D=D, batch=len(LENGTHS), max_T=max(LENGTHS) + 32, in_dtype=dtype,
-                   k_fmt=kf, v_fmt=vf, k_cold=kc, v_cold=vc, hot_window=hot, residual_window=R, flags=flags)
+    # asymmetric cases also decode, with three query heads per kv head
+    cfg = K.Config(L=1, H_kv=3, H_q=9 if flags else 3, D=D, batch=len(LENGTHS), max_T=max(LENGTHS) + 32,
+                   in_dtype=dtype, k_fmt=kf, v_fmt=vf, k_cold=kc, v_cold=vc, hot_window=hot, residual_window=R,
+                   flags=flags)
     oc = oracle_cfg(cfg)
     gen = torch.Generator().manual_seed(zlib.crc32(f"{name}/{kind}".encode()))
     ks = _case_tensors(kind, cfg, LENGTHS, 0, gen)

@@ -70,6 +70,8 @@ SAMPLES = {
     "ctx262k_hadamard3": [(0, 0, 5), (15, 0, 18)],
     "mistral7b_hotcold": [(0, 0, 0), (20, 33, 14), (31, 63, 31)],
     "ctx262k_tbq4": [(0, 0, 2), (15, 0, 20)],
+    "llama2_7b_kivi4_zp": [(0, 0, 0), (31, 0, 17)],
+    "llama2_7b_kivi2_zp": [(0, 0, 3), (31, 0, 30)],
 }
 
 
