@@ -115,52 +115,86 @@ __device__ __forceinline__ void block32(float (&v)[32], float m, uint8_t* dst, f
 }
 
 // Asymmetric block of 32 values (fp16 scale, fp16 zero, codes 0..2^B-1), in
-// the format's op order: s16 = fp16(min((max - min) / (2^B - 1), 65504)),
-// z16 = fp16(min clipped to +-65504), code = clamp(rint((x - z) / s), 0,
-// 2^B - 1), 0 when s = 0.  The numerator x - z is a general fp32 value, so the
-// divide-free quotient is only trusted away from the rounding boundaries: a
-// quotient within 2^-16 of a half step (always below 2^B, where its ulp is at
-// most 2^-20) is recomputed with the IEEE divide.  Clamping the magic-number
-// sum to [magic, magic + 2^B - 1] is the clamp of the rounded quotient.
+// the format's op order: with mn, mx the block's minimum (a zero as +0) and
+// maximum, s16 = fp16(min((mx - mn) / (2^B - 1), 65504)), z16 = fp16(mn
+// clipped to +-65504), code = clamp(rint((x - z) / s), 0, 2^B - 1), 0 when
+// s = 0.  The quotient is first taken as q = RN(RN(x - z) RN(1/s)), within
+// two ulps of RN((x - z) / s); the rounding to an integer can differ only when
+// q lies that close to a half step, and below 2^B + 1 (the only range where
+// a code is decided) two ulps are at most 2^-18.  A value whose q lies within
+// 2^-16 of a half step is therefore recomputed with the IEEE divide.
+// Clamping the magic-number sum to [magic, magic + 2^B - 1] is the clamp of
+// the rounded quotient.
+constexpr float kNearHalf = 0.5f - 1.52587890625e-05f;  // 1/2 - 2^-16
+
 template <int B>
-__device__ __forceinline__ void block32_zp(const float (&v)[32], uint8_t* dst, float* dq) {
-  constexpr int qlev = (1 << B) - 1;
-  float mn = v[0], mx = v[0];
-#pragma unroll
-  for (int j = 1; j < 32; ++j) {
-    mn = fminf(mn, v[j]);
-    mx = fmaxf(mx, v[j]);
-  }
-  const __half s16 = __float2half_rn(fminf(__fdiv_rn(__fsub_rn(mx, mn), (float)qlev), 65504.0f));
-  const __half z16 = __float2half_rn(fminf(fmaxf(mn, -65504.0f), 65504.0f));
-  const float sf = __half2float(s16), zf = __half2float(z16);
-  const float rcp = sf == 0.f ? 0.f : __frcp_rn(sf);
-  uint32_t w[B], corr[B];
+__device__ __forceinline__ void codes_zp(const float (&v)[32], float sf, float zf, float rcp, uint32_t (&w)[B],
+                                         float* dq) {
+  constexpr float top = kRoundMagic + (float)((1 << B) - 1);
+  uint32_t corr[B];
 #pragma unroll
   for (int k = 0; k < B; ++k) w[k] = corr[k] = 0;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const float d = __fsub_rn(v[j], zf);
-    float q = div_by_scale(d, sf, rcp);
-    const float t = __fsub_rn(__fadd_rn(q, kRoundMagic), kRoundMagic);  // rint(q) for |q| < 2^22
-    if (fabsf(__fsub_rn(q, t)) > 0.5f - 1.52587890625e-05f) q = __fdiv_rn(d, sf);
-    const float r = fminf(fmaxf(__fadd_rn(q, kRoundMagic), kRoundMagic), kRoundMagic + (float)qlev);
+    float r0 = __fadd_rn(__fmul_rn(d, rcp), kRoundMagic);
+    if (fabsf(__fsub_rn(__fmul_rn(d, rcp), __fsub_rn(r0, kRoundMagic))) > kNearHalf)
+      r0 = __fadd_rn(__fdiv_rn(d, sf), kRoundMagic);
+    const float r = fminf(fmaxf(r0, kRoundMagic), top);
     if (dq) dq[j] = __fadd_rn(__fmul_rn(__fsub_rn(r, kRoundMagic), sf), zf);
-    const uint32_t bits = __float_as_uint(r);
     const int bit = B * j, k = bit / 32, sh = bit % 32;
-    w[k] += bits << sh;
+    w[k] += __float_as_uint(r) << sh;
     corr[k] += kRoundMagicBits << sh;
   }
+#pragma unroll
+  for (int k = 0; k < B; ++k) w[k] -= corr[k];
+}
+
+template <int B>
+__device__ __forceinline__ void block32_zp(const float (&v)[32], float mn, float mx, uint8_t* dst, float* dq) {
+  constexpr int qlev = (1 << B) - 1;
+  mn = __fadd_rn(mn, 0.0f);
+  const __half s16 = __float2half_rn(fminf(__fdiv_rn(__fsub_rn(mx, mn), (float)qlev), 65504.0f));
+  const __half z16 = __float2half_rn(fminf(fmaxf(mn, -65504.0f), 65504.0f));
+  const float sf = __half2float(s16), zf = __half2float(z16);
+  const float rcp = sf == 0.f ? 0.f : __frcp_rn(sf);
+  uint32_t w[B];
+  codes_zp<B>(v, sf, zf, rcp, w, dq);
   if (!dst) return;
   uint16_t* p = reinterpret_cast<uint16_t*>(dst);
   p[0] = __half_as_ushort(s16);
   p[1] = __half_as_ushort(z16);
 #pragma unroll
   for (int k = 0; k < B; ++k) {
-    const uint32_t x = w[k] - corr[k];
-    p[2 + 2 * k] = (uint16_t)x;
-    p[3 + 2 * k] = (uint16_t)(x >> 16);
+    p[2 + 2 * k] = (uint16_t)w[k];
+    p[3 + 2 * k] = (uint16_t)(w[k] >> 16);
   }
+}
+
+__device__ __forceinline__ void minmax_of(const float (&v)[32], float& mn, float& mx) {
+  mn = mx = v[0];
+#pragma unroll
+  for (int j = 1; j < 32; ++j) {
+    mn = fminf(mn, v[j]);
+    mx = fmaxf(mx, v[j]);
+  }
+}
+
+// Elementwise min / max of two pairs of 16-bit floats (NaN-ignoring, like
+// fminf / fmaxf; exact, so the fp32 extremes are those of the pairs).
+template <int DT>
+__device__ __forceinline__ uint32_t min2_16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if constexpr (DT == KVQ_DT_F16) asm("min.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+  else asm("min.bf16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <int DT>
+__device__ __forceinline__ uint32_t max2_16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if constexpr (DT == KVQ_DT_F16) asm("max.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+  else asm("max.bf16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 __device__ __forceinline__ float amax_of(const float (&v)[32]) {
@@ -173,17 +207,19 @@ __device__ __forceinline__ float amax_of(const float (&v)[32]) {
 // Hot block of v into dst, or (to_cold) the cold block of its dequantized
 // values into dstc.  Z: asymmetric blocks in both tiers.
 template <int B, int CB, bool Z = false>
-__device__ __forceinline__ void hot_or_cold(float (&v)[32], bool to_cold, uint8_t* dst, uint8_t* dstc) {
-  if constexpr (Z) {
+__device__ __forceinline__ void hot_or_cold(float (&v)[32], bool to_cold, uint8_t* dst, uint8_t* dstc,
+                                            float mn = 0.f, float mx = 0.f) {
+  if constexpr (Z) {  // mn, mx: the block's minimum and maximum
     if constexpr (CB != 0) {
       if (to_cold) {
-        float dq[32];
-        block32_zp<B>(v, nullptr, dq);
-        block32_zp<CB>(dq, dstc, nullptr);
+        float dq[32], cmn, cmx;
+        block32_zp<B>(v, mn, mx, nullptr, dq);
+        minmax_of(dq, cmn, cmx);
+        block32_zp<CB>(dq, cmn, cmx, dstc, nullptr);
         return;
       }
     }
-    block32_zp<B>(v, dst, nullptr);
+    block32_zp<B>(v, mn, mx, dst, nullptr);
     return;
   }
   if constexpr (CB != 0) {
@@ -254,7 +290,23 @@ __global__ void __launch_bounds__(kAppendThreads) quant_token32_kernel(AppendArg
       for (int q = 0; q < 4; ++q) r[p][q] = src[4 * p + q];
 #pragma unroll
     for (int sl = 0; sl < SPR; ++sl) {
-      float v[32];
+      float v[32], mn = 0.f, mx = 0.f;
+      if constexpr (Z) {  // block extremes on the 16-bit pairs
+        uint32_t lo2 = r[sl % PF][0].x, hi2 = lo2;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 c = r[sl % PF][q];
+          const uint32_t ww[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+          for (int e = (q == 0 ? 1 : 0); e < 4; ++e) {
+            lo2 = min2_16<DT>(lo2, ww[e]);
+            hi2 = max2_16<DT>(hi2, ww[e]);
+          }
+        }
+        const float2 l = raw_pair_to_f32<DT>(lo2), h = raw_pair_to_f32<DT>(hi2);
+        mn = fminf(l.x, l.y);
+        mx = fmaxf(h.x, h.y);
+      }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint4 c = r[sl % PF][q];
@@ -270,7 +322,7 @@ __global__ void __launch_bounds__(kAppendThreads) quant_token32_kernel(AppendArg
 #pragma unroll
         for (int q = 0; q < 4; ++q) r[sl % PF][q] = src[4 * (sl + PF) + q];
       }
-      hot_or_cold<B, CB, Z>(v, to_cold, dst + sl * BB, dst + sl * CBB);
+      hot_or_cold<B, CB, Z>(v, to_cold, dst + sl * BB, dst + sl * CBB, mn, mx);
     }
   }
   __syncthreads();
@@ -346,6 +398,17 @@ __global__ void __launch_bounds__(kAppendThreads, 4) quant_channel32_kernel(Appe
         slot = slot + 1 == lo.ring ? 0 : slot + 1;
       }
     }
+    float2 mn2 = make_float2(0.f, 0.f), mx2 = mn2;
+    if constexpr (Z) {  // extremes of both channels' blocks on the 16-bit pairs
+      uint32_t lo2 = raw[0], hi2 = raw[0];
+#pragma unroll
+      for (int j = 1; j < 32; ++j) {
+        lo2 = min2_16<DT>(lo2, raw[j]);
+        hi2 = max2_16<DT>(hi2, raw[j]);
+      }
+      mn2 = raw_pair_to_f32<DT>(lo2);
+      mx2 = raw_pair_to_f32<DT>(hi2);
+    }
 #pragma unroll
     for (int hc = 0; hc < 2; ++hc) {
       float v[32];
@@ -355,7 +418,8 @@ __global__ void __launch_bounds__(kAppendThreads, 4) quant_channel32_kernel(Appe
         v[j] = in_to_f32_t<DT>(h16);
       }
       const int c = 2 * cp + hc;
-      hot_or_cold<B, CB, Z>(v, to_cold, out + gi * SLOT + c * BB, out + gi * SLOT + c * CBB);
+      hot_or_cold<B, CB, Z>(v, to_cold, out + gi * SLOT + c * BB, out + gi * SLOT + c * CBB, hc ? mn2.y : mn2.x,
+                            hc ? mx2.y : mx2.x);
     }
   }
   __syncthreads();

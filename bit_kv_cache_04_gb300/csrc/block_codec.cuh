@@ -187,9 +187,9 @@ __device__ __forceinline__ float block_value(const uint8_t* blk, int bits, int c
   return (float)unpack_code(blk + 2, bits, i) * block_scale(blk);
 }
 
-// Asymmetric block of 32 values (op order of the format): mn, mx = min, max;
-// s16 = fp16(min((mx - mn) / (2^b - 1), 65504)); z16 = fp16(mn clipped to
-// +-65504); code = clamp(rint((x - z) / s), 0, 2^b - 1), 0 when s = 0.  The
+// Asymmetric block of 32 values (op order of the format): mn, mx = min, max
+// (a zero minimum as +0); s16 = fp16(min((mx - mn) / (2^b - 1), 65504));
+// z16 = fp16(mn clipped to +-65504); code = clamp(rint((x - z) / s), 0, 2^b - 1), 0 when s = 0.  The
 // block (scale, zero, codes in little-endian b-bit fields) goes to blk when
 // given; dq (optional) receives code * s + z.  Not inlined: the generic
 // kernels call it from many places and it holds 32 IEEE divides.
@@ -200,6 +200,7 @@ static __device__ __noinline__ void quant_zp32_mem(const float* v, int bits, uin
     mn = fminf(mn, v[j]);
     mx = fmaxf(mx, v[j]);
   }
+  mn = __fadd_rn(mn, 0.0f);  // a zero minimum is stored as +0
   const __half s16 = __float2half_rn(fminf(__fdiv_rn(__fsub_rn(mx, mn), (float)qlev), 65504.0f));
   const __half z16 = __float2half_rn(fminf(fmaxf(mn, -65504.0f), 65504.0f));
   const float sf = __half2float(s16), zf = __half2float(z16);

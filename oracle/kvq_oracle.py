@@ -380,13 +380,14 @@ def quantize_zp(x: np.ndarray, bits: int) -> Tuple[np.ndarray, np.ndarray, np.nd
     """Asymmetric blocks along the last axis, fp32 op order:
 
     mn, mx = min x, max x; qlev = 2^b - 1; s32 = (mx - mn) / qlev;
-    s16 = fp16(min(s32, 65504)); z16 = fp16(mn clipped to +-65504);
+    s16 = fp16(min(s32, 65504)); z16 = fp16(mn clipped to +-65504), a zero
+    minimum stored as +0 (the minimum is a value; -0 and +0 are the same one);
     code = clamp(rint((x - float(z16)) / float(s16)), 0, qlev), all codes 0
     when s16 == 0.  Returns (s16, z16 as float16 [...], codes uint8 [..., G]).
     """
     x = np.asarray(x, np.float32)
     qlev = np.float32((1 << bits) - 1)
-    mn = np.min(x, axis=-1)
+    mn = (np.min(x, axis=-1) + np.float32(0.0)).astype(np.float32)  # -0 + +0 = +0
     mx = np.max(x, axis=-1)
     s32 = ((mx - mn).astype(np.float32) / qlev).astype(np.float32)
     s16 = np.minimum(s32, np.float32(65504.0)).astype(np.float16)

@@ -67,6 +67,20 @@ def test_zero_range_block():
     assert np.array_equal(O.dequantize_zp_f64(s16, z16, codes), x.astype(np.float64))
 
 
+def test_signed_zero_minimum_is_stored_as_plus_zero():
+    x = np.abs(np.random.default_rng(3).standard_normal((4, 32))).astype(np.float32)
+    x[0, 5], x[0, 9] = -0.0, 0.0
+    x[1, 0] = -0.0
+    x[2, :] = -0.0
+    x[3, 7] = -0.0
+    x[3, 8] = -1.0
+    s16, z16, codes = O.quantize_zp(x, 4)
+    assert list(z16[:3].view(np.uint16)) == [0, 0, 0]
+    assert z16[3] == -1.0 and s16[2] == 0 and np.all(codes[2] == 0)
+    blob = O.encode_blocks(x, 4, zp=True)
+    assert np.all(blob[:3, 2:4] == 0)
+
+
 def test_byte_layout():
     x = np.arange(32, dtype=np.float32) / 2 - 3.0  # min -3, step 0.5: scale 15.5/15 -> fp16
     blob = O.encode_blocks(x[None], 4, zp=True)[0]
