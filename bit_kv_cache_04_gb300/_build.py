@@ -23,6 +23,7 @@ SOURCES = [
     ("append_fast.cu", ["--fmad=false"]),
     ("append_fast_zp_f16.cu", ["--fmad=false"]),
     ("append_fast_zp_bf16.cu", ["--fmad=false"]),
+    ("append_rot.cu", ["--fmad=false"]),
     ("decode_generic.cu", []),
     ("decode_mma.cu", []),
     ("dequant.cu", []),

@@ -13,7 +13,8 @@ bool launch_fast_tensor(const AppendArgs& a, int which, bool dry, cudaStream_t s
   const Layout& lo = a.lo;
   const FmtInfo& f = fmt_main(lo, which);
   const bool rot = (lo.flags & (which ? KVQ_ROTATE_V : KVQ_ROTATE_K)) != 0;
-  if (rot || f.group != 32) return false;
+  if (rot) return launch_fast_rot(a, which, dry, st);  // Hadamard formats: their own translation unit
+  if (f.group != 32) return false;
   const int cb = lo.tiered ? fmt_cold(lo, which).bits : 0;
   if (f.zp) {  // asymmetric blocks (4- or 2-bit, 4 -> 2 tiers): their own translation units
     return DT == KVQ_DT_F16 ? launch_fast_zp_f16(a, which, dry, st) : launch_fast_zp_bf16(a, which, dry, st);

@@ -471,6 +471,10 @@ bool launch_fast_zp_tensor(const AppendArgs& a, int which, bool dry, cudaStream_
 
 }  // namespace
 
+// Rotated per-token 128-value formats (4 or 3 bits): launches (or with `dry`,
+// only checks) the specialized phase B of tensor `which`.
+bool launch_fast_rot(const AppendArgs& a, int which, bool dry, cudaStream_t st);
+
 // Asymmetric-format launchers, one translation unit per input dtype.
 bool launch_fast_zp_f16(const AppendArgs& a, int which, bool dry, cudaStream_t st);
 bool launch_fast_zp_bf16(const AppendArgs& a, int which, bool dry, cudaStream_t st);
