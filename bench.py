@@ -337,6 +337,8 @@ def run_ours(args):
         cpu = cpu_baseline(w, cache, seq_lens, args.cpu_heads)
 
     append_gbs = sum(app_bytes) / (sum(app_ms) / 1e3) / 1e9
+    fmt_text, bits_text = _format_text(cfg)
+    in_text = "f16" if cfg.in_dtype == K.DT_F16 else "bf16"
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -348,11 +350,11 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16 in, packed int4 codes + fp16 scales, fp32 math",
+        "dtype": f"{in_text} in, packed {bits_text} codes + fp16 scales, fp32 math",
         "data": "synthetic (seeded)",
         "config": {"workload": args.workload, "layers": L, "heads_q": Hq, "heads_kv": H, "head_dim": D,
                    "batch": B, "context_tokens": w.lengths[0] if B == 1 else w.lengths,
-                   "format": "KIVI-4: K per-channel 18 B/32 tokens, V per-token 18 B/32, 128-token 16-bit window",
+                   "format": fmt_text,
                    "step": "append 1 token/seq to all layers + decode attention over all layers + length commit",
                    "decode_launch": "one multi-layer launch",
                    "l2": "inputs larger than L2 (cache %.2f GB)" % (K.kvq_cache_bytes(cfg, w.lengths[0]) * B / 1e9),
@@ -363,8 +365,8 @@ def run_ours(args):
                    "tokens_per_s": round(B / statistics.mean(dec_ms) * 1e3, 2)},
         "append": {"GBps": round(append_gbs, 2), "pct_of_peak": round(100 * append_gbs / peak, 2),
                    "ms_per_layer": round(statistics.median(app_ms), 4),
-                   "what": "bulk quantize-on-append of one layer (32768 tokens x 32 heads) per call; "
-                           "bytes = fp16 source read + packed blocks and window written"},
+                   "what": f"bulk quantize-on-append of one layer ({sum(w.lengths)} tokens x {H} kv heads) per "
+                           f"call; bytes = {in_text} source read + packed blocks and window written"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": _traffic(args.workload, L),
                      "kernel": "decode attention (multi-layer launch)", "peak_source": peak_kind},
@@ -440,6 +442,34 @@ def _kernel_sha() -> str:
         with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "bit_kv_cache_04_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
+
+
+def _format_text(cfg):
+    """Human-readable cache format of a config and the code widths it holds."""
+    from bit_kv_cache_04_gb300 import kvq as K
+    def one(f, zp, tb):
+        if f is None or f.bits == 0:
+            return None
+        axis = "per-channel (32 tokens)" if f.axis == K.AXIS_CHANNEL else f"per-token ({f.group} values)"
+        bb = K.kvq_block_bytes(f.bits, f.group) + (2 if zp else 0)
+        kind = "TBQ4 norm + Lloyd-Max indices" if tb else ("scale + zero" if zp else "scale")
+        return f"{f.bits}-bit {axis}, {bb} B/{f.group if f.axis == K.AXIS_TOKEN else 32} ({kind})"
+    fl = cfg.flags
+    parts = [f"K {one(cfg.k_fmt, fl & K.ZP_K, fl & K.TBQ4_K)}", f"V {one(cfg.v_fmt, fl & K.ZP_V, fl & K.TBQ4_V)}"]
+    if cfg.hot_window:
+        parts.append(f"hot {cfg.hot_window} tokens, cold K {one(cfg.k_cold, fl & K.ZP_K, 0)}, "
+                     f"cold V {one(cfg.v_cold, fl & K.ZP_V, 0)}")
+    if fl & (K.ROTATE_K | K.ROTATE_V):
+        parts.append("randomized Hadamard-128 on " + "+".join(n for n, b in (("K", K.ROTATE_K), ("V", K.ROTATE_V))
+                                                          if fl & b))
+    if fl & K.K_PRE_ROPE:
+        parts.append("keys pre-RoPE (turned in the kernel)")
+    if cfg.residual_window:
+        parts.append(f"{cfg.residual_window}-token 16-bit window")
+    if cfg.page_tokens:
+        parts.append(f"{cfg.page_tokens}-token pages")
+    bits = sorted({f.bits for f in (cfg.k_fmt, cfg.v_fmt, cfg.k_cold, cfg.v_cold) if f is not None and f.bits})
+    return "; ".join(parts), "/".join(f"int{b}" for b in bits)
 
 
 def _traffic(workload: str, layers: int):
