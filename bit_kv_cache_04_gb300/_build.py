@@ -26,6 +26,10 @@ SOURCES = [
     ("append_rot.cu", ["--fmad=false"]),
     ("decode_generic.cu", []),
     ("decode_mma.cu", []),
+    ("decode_step.cu", []),
+    ("decode_step_kivi.cu", []),
+    ("decode_step_d128.cu", []),
+    ("decode_step_d256.cu", []),
     ("dequant.cu", []),
 ]
 

@@ -24,14 +24,19 @@ struct SeqSpan {
   bool ok;
 };
 
-__device__ SeqSpan read_span(const AppendArgs& a, int seq) {
+__device__ __forceinline__ SeqSpan read_span(const AppendArgs& a, int seq) {
   SeqSpan s;
-  s.off = a.cu_new[seq];
-  s.n = a.cu_new[seq + 1] - s.off;
+  if (a.one_per_seq) {
+    s.off = seq;
+    s.n = 1;
+  } else {
+    s.off = a.cu_new[seq];
+    s.n = a.cu_new[seq + 1] - s.off;
+  }
   s.T0 = a.seq_lens[seq];
   s.T1 = s.T0 + s.n;
   uint32_t bad = 0;
-  if (s.n < 0 || s.T0 < 0 || s.T0 > a.lo.max_T || s.off < 0 || a.cu_new[seq + 1] > a.total_new) bad |= KVQ_DEV_LENGTH;
+  if (s.n < 0 || s.T0 < 0 || s.T0 > a.lo.max_T || s.off < 0 || s.off + s.n > a.total_new) bad |= KVQ_DEV_LENGTH;
   else if (s.n > a.max_new || s.T1 > a.lo.max_T) bad |= KVQ_DEV_CAPACITY;
   s.ok = bad == 0;
   if (bad && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(a.status, bad);

@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
   const int layer = a.layer0 + li;
   const int tid = threadIdx.x;
 
-  int T = a.seq_lens[seq];
+  int T = a.seq_lens[seq] + a.len_add;
   if (T < 0 || T > lo.max_T) {
     if (split == 0 && h == 0 && tid == 0) atomicOr(a.status, KVQ_DEV_LENGTH);
     T = 0;

@@ -1,1235 +1,27 @@
-// Split-K decode attention on the tensor cores (mma.sync m16n8k16, fp16
-// operands, fp32 accumulators):
-//   K per-channel 4/2-bit over 32-token groups, or per-token 8/4/3-bit blocks;
-//   V per-token 8/4/3/2-bit blocks; an optional fp16 window; a hot/cold pair
-//   of per-channel formats; keys stored pre-RoPE (split-half RoPE applied in
-//   the kernel); optional rotation (no window then); contiguous or 16/32-token
-//   pages.
-//
-// Per 32-token group the scores are S^T[token][col] = K[token][d] Q^T[d][col]
-// with tokens on M and, on N, the query heads sharing the kv head, each head
-// twice: column 2h holds the fp16 part ("hi") of head h's query and column
-// 2h+1 the fp16 remainder ("lo"), so q = hi + lo to about 22 bits.  The PV
-// product is O^T[d][col] = V^T[d][token] P^T[token][col] with the same hi/lo
-// split of the probabilities.  Codes enter the tensor cores as exact fp16
-// integers; block scales multiply the fp32 scores (per-token K), the query
-// (per-channel K) or the probabilities (per-token V).  This is the rotated-
-// domain attention of trefon.com "Matematyka cache KV" ("najpierw obrot":
-// rotate the query once, read blocks as code x scale, rotate the output back
-// once) with nalar.dev's s_i = q.k_i / sqrt(D) and output = sum_i p_i v_i.
-//
-// Pre-RoPE keys (troisinh.com "KV Cache Quantization", "RoPE - Cai bay tinh
-// vi"; split-half pairs as lehuy.net "NexusQuant" lists): with t = t0 + j in a
-// group starting at t0, q . R(t) k = (R(-t0) q) . (R(j) k).  The query is
-// turned by -t0 once per group; each key value is dequantized, turned by its
-// in-group offset j and split into fp16 hi + lo, so the product keeps ~22
-// bits on both sides.  Angles come from fp64 tables in the workspace.
-//
-// Layout of one group: M-tile mu (0, 1) row r is token
-// tau(mu, r) = 4(r & 7) + 2mu + (r >> 3); k-chunk kc = 2s + b (span s of 32
-// channels) pairs channels (c, c+4) in k-slots (2t, 2t+1) and (c+1, c+5) in
-// (2t+8, 2t+9), c = 32s + 8t + 2b (t = lane % 4), so channel c + D/2 sits in
-// k-chunk kc + D/32 at the same slot (the RoPE partner); d-tile (s, e) row r
-// is channel 32s + 4(r & 7) + 2e + (r >> 3).
-//
-// Work split: CTA = 4 warps on one (layer, sequence, kv head, token split);
-// each warp streams its own groups through a 2-stage cp.async ring and keeps
-// its own online softmax; warps merge in shared memory and splits merge in
-// the workspace (the last CTA to take a ticket combines; nobody waits).
-#include "block_codec.cuh"
+// Decode attention: the tensor-core kernel (decode_mma.cuh) when the cache's
+// formats fit it, else the generic kernel.
+#include "decode_mma.cuh"
 
 namespace kvq {
-
-cudaError_t launch_decode_generic(const DecodeArgs& a, cudaStream_t s);
-
 namespace {
 
-// KF_TQ / VF_TQ: TBQ4 blocks (4-bit indices into the 16-entry fp16 table).
-enum : int { KF_CH4 = 0, KF_T8 = 1, KF_T4 = 2, KF_T3 = 3, KF_CH2 = 4, KF_TQ = 5 };
-enum : int { VF_T8 = 0, VF_T4 = 1, VF_T3 = 2, VF_T2 = 3, VF_TQ = 4 };
-
-constexpr int kWarps = 4;
-constexpr int kThreadsMma = kWarps * 32;
-constexpr int kStages = 2;  // per-warp cp.async ring: one group in flight while one is consumed
-constexpr float kLog2eF = 1.4426950408889634f;
-
-constexpr int bits_k(int kf) { return kf == KF_T8 ? 8 : kf == KF_T3 ? 3 : kf == KF_CH2 ? 2 : 4; }
-constexpr int bits_v(int vf) { return vf == VF_T8 ? 8 : vf == VF_T3 ? 3 : vf == VF_T2 ? 2 : 4; }
-constexpr int align16(int x) { return (x + 15) / 16 * 16; }
-__host__ __device__ constexpr float code_bias(int bits) { return (float)(1 << (bits - 1)); }  // symmetric storage bias
-
-// Byte geometry of one tier's formats.  Z: asymmetric blocks (fp16 scale,
-// fp16 zero, codes 0..2^b-1) for K and V.  The code unpackers return the
-// field minus the symmetric storage bias beta = 2^(b-1), so an asymmetric
-// value c s + z is read as (c - beta) s + (z + beta s): the codes take the
-// symmetric path unchanged and the zero z' = z + beta s adds a term per block.
-template <int D, int KF_, int KG_, int VF_, int VG_, bool Z_ = false>
-struct Tier {
-  static constexpr int KF = KF_, KG = KG_, VF = VF_, VG = VG_;
-  static constexpr bool Z = Z_;
-  static constexpr int KB = bits_k(KF), VB = bits_v(VF);
-  static constexpr bool KCH = KF == KF_CH4 || KF == KF_CH2;
-  static constexpr bool KLUT = KF == KF_TQ, VLUT = VF == VF_TQ;  // codes index the TBQ4 table
-  static constexpr int HDR = Z ? 4 : 2;                     // block header bytes
-  static constexpr int KBB = HDR + (KCH ? 32 : KG) * KB / 8;  // block bytes
-  static constexpr int VBB = HDR + VG * VB / 8;
-  static constexpr int KROW = KCH ? D * KBB : (D / KG) * KBB;  // group row / token row
-  static constexpr int VROW = (D / VG) * VBB;
-  static constexpr int KSTAGE = KCH ? KROW : 32 * KROW;
-  static constexpr int VSTAGE = 32 * VROW;
-  static constexpr int KSPB = KCH ? 1 : KG / 32;  // spans per K block
-  static constexpr int VSPB = VG / 32;
-  static constexpr int KSPAN = 32 * KB / 8;  // code bytes of a span of one token
-  static constexpr int VSPAN = 32 * VB / 8;
-  static_assert(!Z || (KCH && VG == 32 && !KLUT && !VLUT), "asymmetric blocks: per-channel K, 32-value V blocks");
-};
-
-constexpr int cmax(int a, int b) { return a > b ? a : b; }
-
-// HOT: the only tier (COLD_ = false) or the hot tier; COLD: the cold tier.
-template <int D_, int NT_, class HOT_, class COLD_, bool HAS_COLD_, bool ROPE_>
-struct Cfg {
-  static constexpr int D = D_, NT = NT_;
-  using HOT = HOT_;
-  using COLD = COLD_;
-  static constexpr bool HAS_COLD = HAS_COLD_, ROPE = ROPE_;
-  static constexpr bool Z = HOT::Z;
-  static_assert(!HAS_COLD || COLD::Z == HOT::Z, "both tiers asymmetric or neither");
-  static constexpr int KSTAGE = HAS_COLD ? cmax(HOT::KSTAGE, COLD::KSTAGE) : HOT::KSTAGE;
-  static constexpr int VSTAGE = HAS_COLD ? cmax(HOT::VSTAGE, COLD::VSTAGE) : HOT::VSTAGE;
-  static constexpr int VOFF = align16(KSTAGE + 16);
-  static constexpr int STAGE = VOFF + align16(VSTAGE + 16);
-  static constexpr int KC = D / 16;  // k-chunks
-  static constexpr int NS = D / 32;  // spans
-  // per-lane query fragments (+ fp32 query for RoPE, + fp32 query by head for the zero terms)
-  static constexpr int QSM = KC * NT * 32 * (16 + (ROPE ? 16 : 0) + (Z ? 8 : 0));
-  static constexpr int MIN_CTAS = D == 128 ? 4 : 2;  // CTAs per SM the register budget aims at
-  static constexpr int SMEM = QSM + kWarps * kStages * STAGE;
-};
-
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t movtrans(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t hsub2u(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-// fp16 pair (lo half = a, hi half = b), round to nearest.
-__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(b), "f"(a));
-  return r;
-}
-
-__device__ __forceinline__ float rn16(float x) { return __half2float(__float2half_rn(x)); }
-
-// fp16 part of x (hi) or the remainder x - hi (lo), as fp32.
-__device__ __forceinline__ float split_part(float x, bool lo) {
-  const float hi = rn16(x);
-  return lo ? x - hi : hi;
-}
-
-// ---- bulk copies (TMA engine) completing on a per-stage mbarrier ----------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-// Makes the barrier initialization visible to the async proxy.
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-}
-// Orders this thread's earlier shared-memory accesses (generic proxy) before
-// later bulk copies into the same bytes (async proxy).
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-// `bytes` (a multiple of 16) from global `src` to shared `dst`, both 16-byte
-// aligned; completion is counted on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-                   smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for phase `parity` of `bar`; false when the limit ran out
-// (the same answer on every lane of the warp).
-constexpr int kSpinLimit = 1 << 22;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  bool ok = false;
-  for (int i = 0; i < kSpinLimit && !ok; ++i) ok = mbar_test(bar, parity);
-  return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
-// four bytes at an even address
-__device__ __forceinline__ uint32_t ld_u32e(const uint8_t* p) { return ld_u16(p) | (ld_u16(p + 2) << 16); }
-// 24 bits at any byte address (reads the aligned word after it too)
-__device__ __forceinline__ uint32_t ld_u24(const uint8_t* p) {
-  const uintptr_t ad = reinterpret_cast<uintptr_t>(p);
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(ad & ~uintptr_t(3));
-  return __funnelshift_r(w[0], w[1], (uint32_t)(ad & 3) * 8) & 0xFFFFFFu;
-}
-
-// Two codes of B bits at bit B*j of each 16-bit half of x, as an exact fp16
-// pair (code with the storage bias removed).
-template <int B>
-__device__ __forceinline__ uint32_t code_pair(uint32_t x, int j) {
-  if constexpr (B == 4) return hsub2u(((x >> (4 * j)) & 0x000F000Fu) | 0x64006400u, 0x64086408u);
-  if constexpr (B == 3) return hsub2u(((x >> (3 * j)) & 0x00070007u) | 0x64006400u, 0x64046404u);
-  return hsub2u(((x >> (2 * j)) & 0x00030003u) | 0x64006400u, 0x64026402u);
-}
-__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
-// Eight 4-bit codes, four per 16-bit half of x (nibble j of each half), as
-// the fp16 pairs r[j] = (low-half code j, high-half code j) - 8.  Nibbles 0
-// and 2 go through 1024 + n; nibbles 1 and 3 through 1024 + 16n, scaled by
-// 1/16 and offset by -72 in one exact fma.
-__device__ __forceinline__ void dq4(uint32_t x, uint32_t (&r)[4]) {
-  r[0] = hsub2u((x & 0x000F000Fu) | 0x64006400u, 0x64086408u);
-  r[1] = hfma2u((x & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, 0xD480D480u);
-  x >>= 8;
-  r[2] = hsub2u((x & 0x000F000Fu) | 0x64006400u, 0x64086408u);
-  r[3] = hfma2u((x & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, 0xD480D480u);
-}
-
-// Two int8 codes in byte 0 of each 16-bit half of (x >> 8j).
-__device__ __forceinline__ uint32_t code_pair8(uint32_t x, int j) {
-  return hsub2u(((x >> (8 * j)) & 0x00FF00FFu) ^ 0x64806480u, 0x64806480u);
-}
-
-// Eight TBQ4 indices, four per 16-bit half of x (nibble j of each half), as
-// the fp16 pairs r[j] = (T[low-half nibble j], T[high-half nibble j]) of the
-// 16-entry table T.  T is symmetric (T[15 - k] = -T[k]), so an index k maps to
-// the magnitude M[k ^ (k < 8 ? 7 : 0) & 7] = T[8 + ...] with the sign of
-// bit 3; lut holds the low bytes (lut[0], lut[1]) and high bytes (lut[2],
-// lut[3]) of the eight magnitudes, looked up four at a time by byte permutes.
-__device__ __forceinline__ void dqt(uint32_t x, uint32_t (&r)[4], const uint32_t (&lut)[4]) {
-  const uint32_t neg = ~x & 0x88888888u;                         // bit 3 clear: negative entry
-  const uint32_t mx = (x ^ ((neg >> 3) * 7u)) & 0x77777777u;     // magnitude index per nibble
-  const uint32_t a = mx & 0x0F0F0F0Fu, b = (mx >> 4) & 0x0F0F0F0Fu;
-  const uint32_t c = a | (a >> 12), d = b | (b >> 12);           // byte0: (m0, m4), byte1: (m2, m6) | (m1, m5), (m3, m7)
-  const uint32_t sel[2] = {__byte_perm(c, d, 0x0040), __byte_perm(c, d, 0x0051)};
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t lo = __byte_perm(lut[0], lut[1], sel[h]);     // low bytes of 4 entries
-    const uint32_t hi = __byte_perm(lut[2], lut[3], sel[h]);     // high bytes
-    const uint32_t p0 = __byte_perm(lo, hi, 0x5140), p1 = __byte_perm(lo, hi, 0x7362);
-    const int j0 = 2 * h, j1 = 2 * h + 1;
-    r[j0] = p0 | ((neg << (12 - 4 * j0)) & 0x80008000u);
-    r[j1] = p1 | ((neg << (12 - 4 * j1)) & 0x80008000u);
-  }
-}
-
-// Eight K codes (channels c0..c0+7 of one token) as four fp16 pairs
-// (c0+j, c0+j+4), j = 0..3.  `p` points at the first code byte of the span.
-template <class C>
-__device__ __forceinline__ void k_token_pairs(const uint8_t* p, int tq, uint32_t (&r)[4], const uint32_t (&lut)[4]) {
-  if constexpr (C::KLUT) {
-    dqt(ld_u32e(p + 4 * tq), r, lut);
-  } else if constexpr (C::KB == 4) {
-    dq4(ld_u32e(p + 4 * tq), r);
-  } else if constexpr (C::KB == 8) {
-    const uint32_t w0 = ld_u32e(p + 8 * tq), w1 = ld_u32e(p + 8 * tq + 4);
-    const uint32_t xa = __byte_perm(w0, w1, 0x5410), xb = __byte_perm(w0, w1, 0x7632);
-    r[0] = code_pair8(xa, 0);
-    r[1] = code_pair8(xa, 1);
-    r[2] = code_pair8(xb, 0);
-    r[3] = code_pair8(xb, 1);
-  } else {  // 3 bits, 8 codes in 24 bits
-    const uint32_t w = ld_u24(p + 3 * tq);
-    const uint32_t x = (w & 0xFFFu) | ((w << 4) & 0x0FFF0000u);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) r[j] = code_pair<3>(x, j);
-  }
-}
-
-// Four V codes (channels 4*gq..4*gq+3 of a span) of token rows ra and rb as
-// four fp16 pairs (row a, row b) for channel 4gq+j.  p* point at the span's
-// first code byte of each row.
-template <class C>
-__device__ __forceinline__ void v_pair4(const uint8_t* pa, const uint8_t* pb, int gq, uint32_t (&r)[4],
-                                        const uint32_t (&lut)[4]) {
-  if constexpr (C::VB == 8) {
-    const uint32_t wa = ld_u32e(pa + 4 * gq), wb = ld_u32e(pb + 4 * gq);
-    const uint32_t xa = __byte_perm(wa, wb, 0x5410), xb = __byte_perm(wa, wb, 0x7632);
-    r[0] = code_pair8(xa, 0);
-    r[1] = code_pair8(xa, 1);
-    r[2] = code_pair8(xb, 0);
-    r[3] = code_pair8(xb, 1);
-  } else {
-    uint32_t ua, ub;
-    if constexpr (C::VB == 4) {
-      ua = ld_u16(pa + 2 * gq);
-      ub = ld_u16(pb + 2 * gq);
-    } else if constexpr (C::VB == 3) {  // 12 bits at bit 12*gq of the span
-      const int sh = 12 * (gq & 1), bo = 3 * (gq >> 1);
-      ua = (ld_u24(pa + bo) >> sh) & 0xFFFu;
-      ub = (ld_u24(pb + bo) >> sh) & 0xFFFu;
-    } else {  // 2 bits: byte gq of the span
-      ua = pa[gq];
-      ub = pb[gq];
-    }
-    const uint32_t x = __byte_perm(ua, ub, 0x5410);
-    if constexpr (C::VLUT) {
-      dqt(x, r, lut);
-    } else if constexpr (C::VB == 4) {
-      dq4(x, r);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) r[j] = code_pair<C::VB>(x, j);
-    }
-  }
-}
-
-template <class C>
-struct WarpState {
-  float o[C::KC][C::NT][4];
-  float m[C::NT], l[C::NT];
-  // asymmetric V: sum over this lane's tokens of p z' per 32-channel block
-  // (for the lane's head 4 nt + tq), rescaled with o
-  float zo[C::Z ? C::NS : 1][C::NT];
-};
-
-// Online softmax over one group's scores; returns the probabilities of the
-// thread's four tokens 4gq..4gq+3 for each n-tile.
-template <class C>
-__device__ __forceinline__ void online_softmax(WarpState<C>& ws, float (&S)[2][C::NT][4], int n_valid, int gq,
-                                               float qscale, float (&p)[C::NT][4]) {
-#pragma unroll
-  for (int nt = 0; nt < C::NT; ++nt) {
-    float s[4];
-    s[0] = (S[0][nt][0] + S[0][nt][1]) * qscale;
-    s[1] = (S[0][nt][2] + S[0][nt][3]) * qscale;
-    s[2] = (S[1][nt][0] + S[1][nt][1]) * qscale;
-    s[3] = (S[1][nt][2] + S[1][nt][3]) * qscale;
-    float mx = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (4 * gq + k >= n_valid) s[k] = -INFINITY;
-      mx = fmaxf(mx, s[k]);
-    }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    const float m_new = fmaxf(ws.m[nt], mx);
-    const float alpha = exp2f(ws.m[nt] - m_new);
-    ws.m[nt] = m_new;
-    float sum = 0.f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      p[nt][k] = exp2f(s[k] - m_new);
-      sum += p[nt][k];
-    }
-    ws.l[nt] = ws.l[nt] * alpha + sum;
-    if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-      for (int i = 0; i < C::KC; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) ws.o[i][nt][e] *= alpha;
-      if constexpr (C::Z) {
-#pragma unroll
-        for (int s = 0; s < C::NS; ++s) ws.zo[s][nt] *= alpha;
-      }
-    }
-  }
-}
-
-// P^T fragments of M-tile mu, n-tile nt: probabilities times the per-token
-// value scales sa (row gq) / sb (row gq+8), split into fp16 hi/lo columns and
-// transposed with movmatrix into the B layout.
-__device__ __forceinline__ void p_fragments(float pa, float pb, uint32_t& b0, uint32_t& b1) {
-  const float ha = rn16(pa), hb = rn16(pb);
-  b0 = movtrans(pack_h2(ha, pa - ha));
-  b1 = movtrans(pack_h2(hb, pb - hb));
-}
-
-// Per-thread context of the decode kernel shared with its helpers.
-template <class C>
-struct Ctx {
-  int gq, tq, lane, g;
-  bool lo_part;
-  uint32_t lo_mask;
-  const uint2* qb;        // [KC][NT][32]: B fragments (hi or lo part)
-  const uint2* qh;        // [KC][NT][32]: query half pairs
-  const float4* qr;       // [KC][NT][32]: fp32 query (RoPE)
-  const float* qz;        // [4 NT][D]: fp32 query by head, zero past g (asymmetric K)
-  const float2* rope_base;
-  const float4* rope_frag;  // [KC/2][4 tokens k][2 pairs][32 lanes]: R(j) of this lane's channels
-  uint32_t lut[4];          // TBQ4 table magnitudes: low bytes (2 words), high bytes (2 words)
-};
-
-// B fragments of the query turned by -t0 (pre-RoPE keys) for the k-chunk
-// pair (kcp, kcp + KC/2): lower channel c and its partner c + D/2.
-template <class C>
-__device__ __forceinline__ void rope_query_pair(const Ctx<C>& cx, const float2* base, int kcp,
-                                                uint32_t (&ql)[C::NT][2], uint32_t (&qu)[C::NT][2]) {
-  constexpr int NT = C::NT, KC = C::KC;
-  const int c = 32 * (kcp >> 1) + 8 * cx.tq + 2 * (kcp & 1);
-  const float2 f0 = __ldg(base + c), f1 = __ldg(base + c + 4), f2 = __ldg(base + c + 1), f3 = __ldg(base + c + 5);
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const float4 l = cx.qr[(kcp * NT + nt) * 32 + cx.lane], u = cx.qr[((kcp + KC / 2) * NT + nt) * 32 + cx.lane];
-    const float l0 = l.x * f0.x + u.x * f0.y, u0 = u.x * f0.x - l.x * f0.y;
-    const float l1 = l.y * f1.x + u.y * f1.y, u1 = u.y * f1.x - l.y * f1.y;
-    const float l2 = l.z * f2.x + u.z * f2.y, u2 = u.z * f2.x - l.z * f2.y;
-    const float l3 = l.w * f3.x + u.w * f3.y, u3 = u.w * f3.x - l.w * f3.y;
-    ql[nt][0] = pack_h2(split_part(l0, cx.lo_part), split_part(l1, cx.lo_part));
-    ql[nt][1] = pack_h2(split_part(l2, cx.lo_part), split_part(l3, cx.lo_part));
-    qu[nt][0] = pack_h2(split_part(u0, cx.lo_part), split_part(u1, cx.lo_part));
-    qu[nt][1] = pack_h2(split_part(u2, cx.lo_part), split_part(u3, cx.lo_part));
-  }
-}
-
-// fp32 key values of lower channels ch[0..3] (lv) and their partners (uv)
-// of token k of the lane's four (4gq + k), turned by R(4gq + k), as hi/lo A
-// fragments (row rr of the A tile; [0] lower k-chunk, [1] partner k-chunk).
-// cs: (cos, sin) of channels ch[0], ch[1] and ch[2], ch[3].
-__device__ __forceinline__ void rope_key_frags(const float4 (&cs)[2], const float (&lv)[4], const float (&uv)[4],
-                                               int rr, uint32_t (&ah)[2][4], uint32_t (&al)[2][4]) {
-  const float c[4] = {cs[0].x, cs[0].z, cs[1].x, cs[1].z};
-  const float sn[4] = {cs[0].y, cs[0].w, cs[1].y, cs[1].w};
-  float nl[4], nu[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    nl[q] = lv[q] * c[q] - uv[q] * sn[q];
-    nu[q] = lv[q] * sn[q] + uv[q] * c[q];
-  }
-  const __half2 hl01 = __floats2half2_rn(nl[0], nl[1]), hl23 = __floats2half2_rn(nl[2], nl[3]);
-  const __half2 hu01 = __floats2half2_rn(nu[0], nu[1]), hu23 = __floats2half2_rn(nu[2], nu[3]);
-  const float2 fl01 = __half22float2(hl01), fl23 = __half22float2(hl23);
-  const float2 fu01 = __half22float2(hu01), fu23 = __half22float2(hu23);
-  ah[0][rr] = *reinterpret_cast<const uint32_t*>(&hl01);
-  ah[0][2 + rr] = *reinterpret_cast<const uint32_t*>(&hl23);
-  al[0][rr] = pack_h2(nl[0] - fl01.x, nl[1] - fl01.y);
-  al[0][2 + rr] = pack_h2(nl[2] - fl23.x, nl[3] - fl23.y);
-  ah[1][rr] = *reinterpret_cast<const uint32_t*>(&hu01);
-  ah[1][2 + rr] = *reinterpret_cast<const uint32_t*>(&hu23);
-  al[1][rr] = pack_h2(nu[0] - fu01.x, nu[1] - fu01.y);
-  al[1][2 + rr] = pack_h2(nu[2] - fu23.x, nu[3] - fu23.y);
-}
-
-// PV for one packed group: P^T per V block (probabilities times the per-token
-// value scales), O^T += V^T P^T.
-template <class C, class TR>
-__device__ __forceinline__ void pv_packed(const Ctx<C>& cx, WarpState<C>& ws, const uint8_t* vsm, int n_valid,
-                                          const float (&p)[C::NT][4]) {
-  constexpr int D = C::D, NT = C::NT;
-  const int gq = cx.gq, tq = cx.tq;
-#pragma unroll
-    for (int bv = 0; bv < D / TR::VG; ++bv) {
-      uint32_t pb[2][NT][2];
-#pragma unroll
-      for (int mu = 0; mu < 2; ++mu) {
-        const int ra = 4 * gq + 2 * mu;
-        const uint8_t* ha = vsm + ra * TR::VROW + bv * TR::VBB;
-        const uint8_t* hb = ha + TR::VROW;
-        const float sva = block_scale(ha);
-        const float svb = block_scale(hb);
-        float zpa = 0.f, zpb = 0.f;  // z' = z + beta s of rows a and b (asymmetric V)
-        if constexpr (TR::Z) {
-          zpa = fmaf(code_bias(TR::VB), sva, block_scale(ha + 2));
-          zpb = fmaf(code_bias(TR::VB), svb, block_scale(hb + 2));
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const float pa = ra < n_valid ? p[nt][2 * mu] * sva : 0.f;
-          const float pbb = ra + 1 < n_valid ? p[nt][2 * mu + 1] * svb : 0.f;
-          p_fragments(pa, pbb, pb[mu][nt][0], pb[mu][nt][1]);
-          if constexpr (TR::Z) {
-            const float za = ra < n_valid ? p[nt][2 * mu] * zpa : 0.f;
-            const float zb = ra + 1 < n_valid ? p[nt][2 * mu + 1] * zpb : 0.f;
-            ws.zo[bv][nt] += za + zb;
-          }
-        }
-      }
-#pragma unroll
-      for (int ss = 0; ss < TR::VSPB; ++ss) {
-        const int s = bv * TR::VSPB + ss;
-        const int off = bv * TR::VBB + TR::HDR + ss * TR::VSPAN;
-#pragma unroll
-        for (int mu = 0; mu < 2; ++mu) {
-          const int T1 = 8 * tq + 2 * mu;
-          uint32_t x12[4], x34[4];
-          v_pair4<TR>(vsm + T1 * TR::VROW + off, vsm + (T1 + 4) * TR::VROW + off, gq, x12, cx.lut);
-          v_pair4<TR>(vsm + (T1 + 1) * TR::VROW + off, vsm + (T1 + 5) * TR::VROW + off, gq, x34, cx.lut);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma16816(ws.o[2 * s][nt], x12[0], x12[1], x34[0], x34[1], pb[mu][nt][0], pb[mu][nt][1]);
-            mma16816(ws.o[2 * s + 1][nt], x12[2], x12[3], x34[2], x34[3], pb[mu][nt][0], pb[mu][nt][1]);
-          }
-        }
-      }
-    }
-  }
-
-// Scores of one packed group into S (see the layout notes at the top).
-template <class C, class TR>
-__device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* ksm, int t0, float (&S)[2][C::NT][4]) {
-  constexpr int D = C::D, NT = C::NT, KC = C::KC;
-  const int gq = cx.gq, tq = cx.tq, lane = cx.lane;
-  const uint32_t lo_mask = cx.lo_mask;
-  const uint2* qb = cx.qb;
-  const uint2* qh = cx.qh;
-    if constexpr (TR::KCH && C::ROPE) {
-      const float2* base = cx.rope_base + (int64_t)(t0 / kTile) * (D / 2);
-#pragma unroll 1
-      for (int kcp = 0; kcp < KC / 2; ++kcp) {
-        uint32_t ql[NT][2], qu[NT][2];
-        rope_query_pair<C>(cx, base, kcp, ql, qu);
-        const int c = 32 * (kcp >> 1) + 8 * tq + 2 * (kcp & 1);
-        const int ch[4] = {c, c + 4, c + 1, c + 5};
-        float sl[4], su[4], zl[4] = {0.f, 0.f, 0.f, 0.f}, zu[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t xl[2], xu[2];
-        uint32_t chl[4], chu[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint8_t* bl = ksm + ch[q] * TR::KBB;
-          const uint8_t* bu = ksm + (ch[q] + D / 2) * TR::KBB;
-          sl[q] = block_scale(bl);
-          su[q] = block_scale(bu);
-          if constexpr (TR::Z) {  // z' = z + beta s
-            zl[q] = fmaf(code_bias(TR::KB), sl[q], block_scale(bl + 2));
-            zu[q] = fmaf(code_bias(TR::KB), su[q], block_scale(bu + 2));
-          }
-          chl[q] = TR::KB == 4 ? ld_u16(bl + TR::HDR + 2 * gq) : (uint32_t)bl[TR::HDR + gq];
-          chu[q] = TR::KB == 4 ? ld_u16(bu + TR::HDR + 2 * gq) : (uint32_t)bu[TR::HDR + gq];
-        }
-        xl[0] = __byte_perm(chl[0], chl[1], 0x5410);
-        xl[1] = __byte_perm(chl[2], chl[3], 0x5410);
-        xu[0] = __byte_perm(chu[0], chu[1], 0x5410);
-        xu[1] = __byte_perm(chu[2], chu[3], 0x5410);
-        uint32_t cl0[4], cl1[4], cu0[4], cu1[4];  // per token k of the thread: (ch0, ch1), (ch2, ch3)
-        if constexpr (TR::KB == 4) {
-          dq4(xl[0], cl0);
-          dq4(xl[1], cl1);
-          dq4(xu[0], cu0);
-          dq4(xu[1], cu1);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            cl0[k] = code_pair<2>(xl[0], k);
-            cl1[k] = code_pair<2>(xl[1], k);
-            cu0[k] = code_pair<2>(xu[0], k);
-            cu1[k] = code_pair<2>(xu[1], k);
-          }
-        }
-        const float4* fr = cx.rope_frag + kcp * 256 + lane;
-#pragma unroll
-        for (int mu = 0; mu < 2; ++mu) {
-          uint32_t ah[2][4], al[2][4];
-#pragma unroll
-          for (int rr = 0; rr < 2; ++rr) {
-            const int k = 2 * mu + rr;
-            const float4 cs[2] = {__ldg(fr + (2 * k) * 32), __ldg(fr + (2 * k + 1) * 32)};
-            const float2 l01 = __half22float2(*reinterpret_cast<const __half2*>(&cl0[k]));
-            const float2 l23 = __half22float2(*reinterpret_cast<const __half2*>(&cl1[k]));
-            const float2 u01 = __half22float2(*reinterpret_cast<const __half2*>(&cu0[k]));
-            const float2 u23 = __half22float2(*reinterpret_cast<const __half2*>(&cu1[k]));
-            const float lv[4] = {fmaf(l01.x, sl[0], zl[0]), fmaf(l01.y, sl[1], zl[1]), fmaf(l23.x, sl[2], zl[2]),
-                                 fmaf(l23.y, sl[3], zl[3])};
-            const float uv[4] = {fmaf(u01.x, su[0], zu[0]), fmaf(u01.y, su[1], zu[1]), fmaf(u23.x, su[2], zu[2]),
-                                 fmaf(u23.y, su[3], zu[3])};
-            rope_key_frags(cs, lv, uv, rr, ah, al);
-          }
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma16816(S[mu][nt], ah[0][0], ah[0][1], ah[0][2], ah[0][3], ql[nt][0], ql[nt][1]);
-            mma16816(S[mu][nt], al[0][0], al[0][1], al[0][2], al[0][3], ql[nt][0], ql[nt][1]);
-            mma16816(S[mu][nt], ah[1][0], ah[1][1], ah[1][2], ah[1][3], qu[nt][0], qu[nt][1]);
-            mma16816(S[mu][nt], al[1][0], al[1][1], al[1][2], al[1][3], qu[nt][0], qu[nt][1]);
-          }
-        }
-      }
-    } else if constexpr (TR::KCH) {
-      // per-channel K: block c = channel c over the group's 32 tokens; the
-      // channel scales multiply the query columns.  Even and odd k-chunks
-      // accumulate separately (two independent MMA chains).
-      float Sx[2][NT][4];
-#pragma unroll
-      for (int mu = 0; mu < 2; ++mu)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) Sx[mu][nt][0] = Sx[mu][nt][1] = Sx[mu][nt][2] = Sx[mu][nt][3] = 0.f;
-#pragma unroll
-      for (int kc = 0; kc < KC; ++kc) {
-        const int c = 32 * (kc >> 1) + 8 * tq + 2 * (kc & 1);
-        const uint8_t* b1p = ksm + c * TR::KBB;
-        const uint8_t* b2p = b1p + 4 * TR::KBB;
-        const uint8_t* b3p = b1p + TR::KBB;
-        const uint8_t* b4p = b1p + 5 * TR::KBB;
-        uint32_t k12[4], k34[4];
-        if constexpr (TR::KB == 4) {
-          dq4(__byte_perm(ld_u16(b1p + TR::HDR + 2 * gq), ld_u16(b2p + TR::HDR + 2 * gq), 0x5410), k12);
-          dq4(__byte_perm(ld_u16(b3p + TR::HDR + 2 * gq), ld_u16(b4p + TR::HDR + 2 * gq), 0x5410), k34);
-        } else {
-          const uint32_t x12 = __byte_perm((uint32_t)b1p[TR::HDR + gq], (uint32_t)b2p[TR::HDR + gq], 0x5410);
-          const uint32_t x34 = __byte_perm((uint32_t)b3p[TR::HDR + gq], (uint32_t)b4p[TR::HDR + gq], 0x5410);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            k12[k] = code_pair<2>(x12, k);
-            k34[k] = code_pair<2>(x34, k);
-          }
-        }
-        const uint32_t s12 = __byte_perm(ld_u16(b1p), ld_u16(b2p), 0x5410);
-        const uint32_t s34 = __byte_perm(ld_u16(b3p), ld_u16(b4p), 0x5410);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          // q' * scale as fp16: hi = rn(q' s) on even columns, the exact
-          // remainder fma(q', s, -hi) on odd columns (lo_mask all ones)
-          const uint2 qv = qh[(kc * NT + nt) * 32 + lane];
-          const uint32_t bq0 = hfma2u(qv.x, s12, (hmul2u(qv.x, s12) ^ 0x80008000u) & lo_mask);
-          const uint32_t bq1 = hfma2u(qv.y, s34, (hmul2u(qv.y, s34) ^ 0x80008000u) & lo_mask);
-#pragma unroll
-          for (int mu = 0; mu < 2; ++mu) {
-            float (&acc)[4] = (kc & 1) ? Sx[mu][nt] : S[mu][nt];
-            mma16816(acc, k12[2 * mu], k12[2 * mu + 1], k34[2 * mu], k34[2 * mu + 1], bq0, bq1);
-          }
-        }
-      }
-#pragma unroll
-      for (int mu = 0; mu < 2; ++mu)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) S[mu][nt][e] += Sx[mu][nt][e];
-      if constexpr (TR::Z) {
-        // zero term of the group, the same for its 32 tokens: sum_c q'_c z'_c
-        // with z'_c = z_c + beta s_c; lane l takes channels CPL l .. CPL l + CPL - 1
-        constexpr int CPL = D / 32;
-        static_assert(CPL % 4 == 0, "whole float4 query loads");
-        float zq[CPL];
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-          const uint8_t* blk = ksm + (CPL * lane + j) * TR::KBB;
-          zq[j] = fmaf(code_bias(TR::KB), block_scale(blk), block_scale(blk + 2));
-        }
-        const int g = cx.g;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float zs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int hl = 0; hl < 4; ++hl) {
-            if (4 * nt + hl >= g) continue;  // warp-uniform
-            const float* qrow = cx.qz + (4 * nt + hl) * D + CPL * lane;
-            float acc = 0.f;
-#pragma unroll
-            for (int j4 = 0; j4 < CPL / 4; ++j4) {
-              const float4 qv = *reinterpret_cast<const float4*>(qrow + 4 * j4);
-              acc = fmaf(qv.x, zq[4 * j4], acc);
-              acc = fmaf(qv.y, zq[4 * j4 + 1], acc);
-              acc = fmaf(qv.z, zq[4 * j4 + 2], acc);
-              acc = fmaf(qv.w, zq[4 * j4 + 3], acc);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            zs[hl] = acc;
-          }
-          // this lane's head is 4 nt + tq: add to its hi column (rows gq, gq + 8)
-          const float zt = tq == 0 ? zs[0] : tq == 1 ? zs[1] : tq == 2 ? zs[2] : zs[3];
-#pragma unroll
-          for (int mu = 0; mu < 2; ++mu) {
-            S[mu][nt][0] += zt;
-            S[mu][nt][2] += zt;
-          }
-        }
-      }
-    } else {
-      // per-token K: each K block's scale multiplies its partial scores
-#pragma unroll
-      for (int kb = 0; kb < D / TR::KG; ++kb) {
-        float acc[2][NT][4];
-#pragma unroll
-        for (int mu = 0; mu < 2; ++mu)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) acc[mu][nt][0] = acc[mu][nt][1] = acc[mu][nt][2] = acc[mu][nt][3] = 0.f;
-#pragma unroll
-        for (int ss = 0; ss < TR::KSPB; ++ss) {
-          const int s = kb * TR::KSPB + ss;
-#pragma unroll
-          for (int mu = 0; mu < 2; ++mu) {
-            const int ra = 4 * gq + 2 * mu;
-            uint32_t wa[4], wb[4];
-            k_token_pairs<TR>(ksm + ra * TR::KROW + kb * TR::KBB + TR::HDR + ss * TR::KSPAN, tq, wa, cx.lut);
-            k_token_pairs<TR>(ksm + (ra + 1) * TR::KROW + kb * TR::KBB + TR::HDR + ss * TR::KSPAN, tq, wb, cx.lut);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              const uint2 q0 = qb[((2 * s) * NT + nt) * 32 + lane];
-              const uint2 q1 = qb[((2 * s + 1) * NT + nt) * 32 + lane];
-              mma16816(acc[mu][nt], wa[0], wb[0], wa[1], wb[1], q0.x, q0.y);
-              mma16816(acc[mu][nt], wa[2], wb[2], wa[3], wb[3], q1.x, q1.y);
-            }
-          }
-        }
-#pragma unroll
-        for (int mu = 0; mu < 2; ++mu) {
-          const float sa = block_scale(ksm + (4 * gq + 2 * mu) * TR::KROW + kb * TR::KBB);
-          const float sb = block_scale(ksm + (4 * gq + 2 * mu + 1) * TR::KROW + kb * TR::KBB);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            S[mu][nt][0] += acc[mu][nt][0] * sa;
-            S[mu][nt][1] += acc[mu][nt][1] * sa;
-            S[mu][nt][2] += acc[mu][nt][2] * sb;
-            S[mu][nt][3] += acc[mu][nt][3] * sb;
-          }
-        }
-      }
-    }
-  }
-
-template <class C>
-__global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(DecodeArgs a) {
-  constexpr int D = C::D, NT = C::NT, KC = C::KC;
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint2* qb = reinterpret_cast<uint2*>(smem);  // [KC][NT][32 lanes]: this lane's B fragment (b0, b1)
-  uint2* qh = qb + KC * NT * 32;               // [KC][NT][32 lanes]: query half pairs (per-channel K)
-  float4* qr = reinterpret_cast<float4*>(qh + KC * NT * 32);  // [KC][NT][32 lanes]: fp32 query (RoPE)
-  float* qz = reinterpret_cast<float*>(qr + (C::ROPE ? KC * NT * 32 : 0));  // [4 NT][D] (asymmetric K)
-  uint8_t* stage_base = smem + C::QSM;
-  __shared__ float qmax_s[kWarps];
-  __shared__ uint32_t bad_page;
-  __shared__ uint64_t mbar[kWarps * kStages];
-  __shared__ int is_last;
-
+// Launches (unless `dry`) the tensor-core decode kernel for the cache's
+// formats into *err; false when none fits.
+bool dispatch_mma(const DecodeArgs& a, cudaStream_t st, bool dry, cudaError_t* err) {
   const Layout& lo = a.lo;
-  const int g = lo.g;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = lane >> 2, tq = lane & 3;
-  const int split = blockIdx.x, h = blockIdx.y;
-  const int li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B;
-  const int layer = a.layer0 + li;
-  const int tid = threadIdx.x;
-
-  int T = a.seq_lens[seq];
-  if (T < 0 || T > lo.max_T) {
-    if (split == 0 && h == 0 && tid == 0) atomicOr(a.status, KVQ_DEV_LENGTH);
-    T = 0;
-  }
-  const int qe = q_end_of(lo, T);
-  const int ce = C::HAS_COLD ? c_end_of(lo, T) : 0;
-  const int n_c = ce / kTile;
-  const int n_m = (qe - ce + kTile - 1) / kTile;
-  const int n_w = (T - qe + kTile - 1) / kTile;
-  const int ntiles = n_c + n_m + n_w;
-  const int tb = (int)((int64_t)split * ntiles / a.splits);
-  const int te = (int)((int64_t)(split + 1) * ntiles / a.splits);
-  const int64_t qrow = ((int64_t)li * lo.B + seq) * lo.Hq + (int64_t)h * g;
-
-  // ---- query: fp32, rotated when K is stored rotated; per-lane fragments ----
-  float qexp = 1.f;
-  {
-    float* qf = reinterpret_cast<float*>(stage_base);  // [g][D] scratch
-    for (int e = tid; e < g * D; e += kThreadsMma) qf[e] = in_to_f32(a.q[qrow * D + e], lo.dtype);
-    if (tid == 0) bad_page = 0;
-    if (tid < kWarps * kStages) mbar_init(mbar + tid, 1);
-    fence_mbar_init();
-    __syncthreads();
-    if (lo.flags & KVQ_ROTATE_K) {
-      for (int r = warp; r < g * (D / 128); r += kWarps) {
-        float* p = qf + r * 128 + 4 * lane;
-        float v[4] = {p[0], p[1], p[2], p[3]};
-        warp_rotate128(v, lo.d1, lo.d2);
-        p[0] = v[0];
-        p[1] = v[1];
-        p[2] = v[2];
-        p[3] = v[3];
-      }
-      __syncthreads();
-    }
-    // power-of-two normalization: |q'| = |q| 2^-e <= 1, so products with fp16
-    // scales cannot overflow fp16 (the factor 2^e returns with the score scale)
-    float m = 0.f;
-    for (int e = tid; e < g * D; e += kThreadsMma) m = fmaxf(m, fabsf(qf[e]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) qmax_s[warp] = m;
-    __syncthreads();
-    m = fmaxf(fmaxf(qmax_s[0], qmax_s[1]), fmaxf(qmax_s[2], qmax_s[3]));
-    int ex = 0;
-    if (m > 0.f) frexpf(m, &ex);
-    const float qnorm = ldexpf(1.f, -ex);
-    qexp = ldexpf(1.f, ex);
-    for (int e = tid; e < KC * NT * 32; e += kThreadsMma) {
-      const int ln = e & 31, nt = (e >> 5) % NT, kc = (e >> 5) / NT;
-      const int c = 32 * (kc >> 1) + 8 * (ln & 3) + 2 * (kc & 1);
-      const int hh = 4 * nt + ((ln >> 2) >> 1);
-      const bool lo = ((ln >> 2) & 1) != 0;
-      float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
-      if (hh < g) {
-        const float* q = qf + hh * D;
-        v0 = q[c] * qnorm;
-        v1 = q[c + 4] * qnorm;
-        v2 = q[c + 1] * qnorm;
-        v3 = q[c + 5] * qnorm;
-      }
-      qb[e] = make_uint2(pack_h2(split_part(v0, lo), split_part(v1, lo)),
-                         pack_h2(split_part(v2, lo), split_part(v3, lo)));
-      qh[e] = make_uint2(pack_h2(v0, v1), pack_h2(v2, v3));
-      if constexpr (C::ROPE) qr[e] = make_float4(v0, v1, v2, v3);
-    }
-    if constexpr (C::Z) {
-      for (int e = tid; e < 4 * NT * D; e += kThreadsMma) {
-        const int hh = e / D;
-        qz[e] = hh < g ? qf[e] * qnorm : 0.f;
-      }
-    }
-    __syncthreads();
-  }
-  const bool lo_part = (gq & 1) != 0;
-  const uint32_t lo_mask = lo_part ? 0xFFFFFFFFu : 0u;
-  const float qscale = kLog2eF / sqrtf((float)D) * qexp;
-  Ctx<C> cx;
-  cx.gq = gq;
-  cx.tq = tq;
-  cx.lane = lane;
-  cx.lo_part = lo_part;
-  cx.lo_mask = lo_mask;
-  cx.qb = qb;
-  cx.qh = qh;
-  cx.qr = qr;
-  cx.qz = qz;
-  cx.g = g;
-  cx.rope_base = a.rope;
-  cx.rope_frag = reinterpret_cast<const float4*>(a.rope + (int64_t)(a.rope_base_rows + kTile) * (D / 2));
-  if constexpr (C::HOT::KLUT || C::HOT::VLUT) {
-    uint32_t m[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) m[k] = __half_as_ushort(__float2half_rn(lo.cb[8 + k]));  // exact: fp16 entries
-    cx.lut[0] = (m[0] & 0xFF) | (m[1] & 0xFF) << 8 | (m[2] & 0xFF) << 16 | (m[3] & 0xFF) << 24;
-    cx.lut[1] = (m[4] & 0xFF) | (m[5] & 0xFF) << 8 | (m[6] & 0xFF) << 16 | (m[7] & 0xFF) << 24;
-    cx.lut[2] = (m[0] >> 8) | (m[1] >> 8) << 8 | (m[2] >> 8) << 16 | (m[3] >> 8) << 24;
-    cx.lut[3] = (m[4] >> 8) | (m[5] >> 8) << 8 | (m[6] >> 8) << 16 | (m[7] >> 8) << 24;
-  } else {
-    cx.lut[0] = cx.lut[1] = cx.lut[2] = cx.lut[3] = 0;
-  }
-
-  WarpState<C> ws;
-#pragma unroll
-  for (int i = 0; i < KC; ++i)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) ws.o[i][nt][e] = 0.f;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    ws.m[nt] = -INFINITY;
-    ws.l[nt] = 0.f;
-#pragma unroll
-    for (int s = 0; s < (C::Z ? C::NS : 1); ++s) ws.zo[s][nt] = 0.f;
-  }
-  uint8_t* wst = stage_base + warp * kStages * C::STAGE;
-
-  // Bulk copies of packed tile `tile` (cold or hot/only tier) into stage
-  // `st`, issued by lane 0: exactly one arrival on the stage's barrier per
-  // packed tile of this warp (with no bytes when a page id is bad).
-  auto issue = [&](int tile, int st) {
-    if (tile >= te || tile >= n_c + n_m) return;
-    if (lane != 0) return;
-    uint8_t* ks = wst + st * C::STAGE;
-    uint8_t* vs = ks + C::VOFF;
-    uint64_t* bar = mbar + warp * kStages + st;
-    if constexpr (C::HAS_COLD) {
-      if (tile < n_c) {
-        const int t0 = tile * kTile;
-        const uint8_t* kg = cold_row(lo, a.cp, 0, layer, seq, h, t0);
-        const uint8_t* vg = cold_row(lo, a.cp, 1, layer, seq, h, t0);
-        mbar_arrive_tx(bar, C::COLD::KSTAGE + C::COLD::VSTAGE);
-        bulk_g2s(ks, kg, C::COLD::KSTAGE, bar);
-        bulk_g2s(vs, vg, C::COLD::VSTAGE, bar);
-        return;
-      }
-    }
-    using HT = typename C::HOT;
-    const int t0 = ce + (tile - n_c) * kTile;
-    bool bad = false;
-    if (lo.paged) {
-      const int np = (qe - t0 > lo.pt) ? kTile / lo.pt : 1;
-      const int kb = lo.pt * HT::KROW, vb = lo.pt * HT::VROW;
-      // one or two pages (16-token pages when the group is complete)
-      const uint8_t* kg0 = main_row(lo, a.cp, 0, layer, seq, h, t0, &bad);
-      const uint8_t* vg0 = main_row(lo, a.cp, 1, layer, seq, h, t0, &bad);
-      const uint8_t* kg1 = kg0;
-      const uint8_t* vg1 = vg0;
-      if (np == 2) {
-        kg1 = main_row(lo, a.cp, 0, layer, seq, h, t0 + lo.pt, &bad);
-        vg1 = main_row(lo, a.cp, 1, layer, seq, h, t0 + lo.pt, &bad);
-      }
-      if (bad) {
-        bad_page = 1;
-        mbar_arrive_tx(bar, 0);
-        return;
-      }
-      mbar_arrive_tx(bar, np * (kb + vb));
-      bulk_g2s(ks, kg0, kb, bar);
-      bulk_g2s(vs, vg0, vb, bar);
-      if (np == 2) {
-        bulk_g2s(ks + kb, kg1, kb, bar);
-        bulk_g2s(vs + vb, vg1, vb, bar);
-      }
-      return;
-    }
-    const uint8_t* kg = main_row(lo, a.cp, 0, layer, seq, h, t0, &bad);
-    const uint8_t* vg = main_row(lo, a.cp, 1, layer, seq, h, t0, &bad);
-    mbar_arrive_tx(bar, HT::KSTAGE + HT::VSTAGE);
-    bulk_g2s(ks, kg, HT::KSTAGE, bar);
-    bulk_g2s(vs, vg, HT::VSTAGE, bar);
+  auto run = [&](auto cfg) {
+    if (!dry) *err = launch_mma<decltype(cfg), 0>(a, st);
+    return true;
   };
-
-  // ---- per-warp pipeline over this CTA's groups --------------------------------
-  const int first = tb + warp;
-  // the query scratch in the stage buffers was written through the generic
-  // proxy; order it before the bulk copies, and publish the barriers
-  fence_proxy_async();
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < kStages - 1; ++i) issue(first + kWarps * i, i);
-  int stall_it = -1;
-  for (int it = 0;; ++it) {
-    const int tile = first + kWarps * it;
-    if (tile >= te) break;
-    issue(tile + kWarps * (kStages - 1), (it + kStages - 1) % kStages);
-    if (tile < n_c + n_m && !mbar_wait(mbar + warp * kStages + it % kStages, (it / kStages) & 1)) {
-      stall_it = it;
-      break;
-    }
-
-    float S[2][NT][4];
-#pragma unroll
-    for (int mu = 0; mu < 2; ++mu)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) S[mu][nt][0] = S[mu][nt][1] = S[mu][nt][2] = S[mu][nt][3] = 0.f;
-    float p[NT][4];
-
-    if (tile < n_c + n_m) {
-      // ---------------- packed group from shared memory ----------------
-      const uint8_t* ksm = wst + (it % kStages) * C::STAGE;
-      const uint8_t* vsm = ksm + C::VOFF;
-      bool cold = false;
-      if constexpr (C::HAS_COLD) cold = tile < n_c;
-      if (cold) {
-        if constexpr (C::HAS_COLD) {
-          const int t0 = tile * kTile;
-          scores_packed<C, typename C::COLD>(cx, ksm, t0, S);
-          online_softmax<C>(ws, S, kTile, gq, qscale, p);
-          pv_packed<C, typename C::COLD>(cx, ws, vsm, kTile, p);
-        }
-      } else {
-        const int t0 = ce + (tile - n_c) * kTile;
-        const int n_valid = min(kTile, qe - t0);
-        scores_packed<C, typename C::HOT>(cx, ksm, t0, S);
-        online_softmax<C>(ws, S, n_valid, gq, qscale, p);
-        pv_packed<C, typename C::HOT>(cx, ws, vsm, n_valid, p);
-      }
-    } else {
-      // ---------------- 16-bit window group from global memory ----------------
-      const int t0 = qe + (tile - n_c - n_m) * kTile;
-      const int n_valid = min(kTile, T - t0);
-      if constexpr (C::ROPE) {
-        const float2* base = cx.rope_base + (int64_t)(t0 / kTile) * (D / 2);
-#pragma unroll 1
-        for (int kcp = 0; kcp < KC / 2; ++kcp) {
-          uint32_t ql[NT][2], qu[NT][2];
-          rope_query_pair<C>(cx, base, kcp, ql, qu);
-          // k-chunk kcp: channels c + {0, 4, 1, 5}, c = 32 (kcp / 2) + 8 tq + 2 (kcp % 2)
-          const int c = 32 * (kcp >> 1) + 8 * tq + 2 * (kcp & 1);
-          const float4* fr = cx.rope_frag + kcp * 256 + lane;
-#pragma unroll
-          for (int mu = 0; mu < 2; ++mu) {
-            uint32_t ah[2][4], al[2][4];
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-              const int k = 2 * mu + rr, r = 4 * gq + k;
-              const uint16_t* row = resid_row(lo, a.cp, 0, layer, seq, h, t0 + min(r, n_valid - 1));
-              uint32_t wl0 = 0, wl1 = 0, wu0 = 0, wu1 = 0;  // (c, c+1), (c+4, c+5) and partners
-              if (r < n_valid) {
-                wl0 = *reinterpret_cast<const uint32_t*>(row + c);
-                wl1 = *reinterpret_cast<const uint32_t*>(row + c + 4);
-                wu0 = *reinterpret_cast<const uint32_t*>(row + c + D / 2);
-                wu1 = *reinterpret_cast<const uint32_t*>(row + c + 4 + D / 2);
-              }
-              const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&wl0));
-              const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&wl1));
-              const float2 b0 = __half22float2(*reinterpret_cast<const __half2*>(&wu0));
-              const float2 b1 = __half22float2(*reinterpret_cast<const __half2*>(&wu1));
-              const float lv[4] = {a0.x, a1.x, a0.y, a1.y};
-              const float uv[4] = {b0.x, b1.x, b0.y, b1.y};
-              const float4 cs[2] = {__ldg(fr + (2 * k) * 32), __ldg(fr + (2 * k + 1) * 32)};
-              rope_key_frags(cs, lv, uv, rr, ah, al);
-            }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              mma16816(S[mu][nt], ah[0][0], ah[0][1], ah[0][2], ah[0][3], ql[nt][0], ql[nt][1]);
-              mma16816(S[mu][nt], al[0][0], al[0][1], al[0][2], al[0][3], ql[nt][0], ql[nt][1]);
-              mma16816(S[mu][nt], ah[1][0], ah[1][1], ah[1][2], ah[1][3], qu[nt][0], qu[nt][1]);
-              mma16816(S[mu][nt], al[1][0], al[1][1], al[1][2], al[1][3], qu[nt][0], qu[nt][1]);
-            }
-          }
-        }
-      } else {
-#pragma unroll
-        for (int mu = 0; mu < 2; ++mu) {
-          const int ra = 4 * gq + 2 * mu, rb = ra + 1;
-          const uint16_t* rowa = resid_row(lo, a.cp, 0, layer, seq, h, t0 + min(ra, n_valid - 1));
-          const uint16_t* rowb = resid_row(lo, a.cp, 0, layer, seq, h, t0 + min(rb, n_valid - 1));
-#pragma unroll
-          for (int s = 0; s < C::NS; ++s) {
-            uint4 va = make_uint4(0, 0, 0, 0), vb = va;
-            if (ra < n_valid) va = *reinterpret_cast<const uint4*>(rowa + 32 * s + 8 * tq);
-            if (rb < n_valid) vb = *reinterpret_cast<const uint4*>(rowb + 32 * s + 8 * tq);
-            // pairs (c, c+4), (c+1, c+5), (c+2, c+6), (c+3, c+7)
-            const uint32_t a0 = __byte_perm(va.x, va.z, 0x5410), a1 = __byte_perm(va.x, va.z, 0x7632);
-            const uint32_t a2 = __byte_perm(va.y, va.w, 0x5410), a3 = __byte_perm(va.y, va.w, 0x7632);
-            const uint32_t b0 = __byte_perm(vb.x, vb.z, 0x5410), b1 = __byte_perm(vb.x, vb.z, 0x7632);
-            const uint32_t b2 = __byte_perm(vb.y, vb.w, 0x5410), b3 = __byte_perm(vb.y, vb.w, 0x7632);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              const uint2 q0 = qb[((2 * s) * NT + nt) * 32 + lane];
-              const uint2 q1 = qb[((2 * s + 1) * NT + nt) * 32 + lane];
-              mma16816(S[mu][nt], a0, b0, a1, b1, q0.x, q0.y);
-              mma16816(S[mu][nt], a2, b2, a3, b3, q1.x, q1.y);
-            }
-          }
-        }
-      }
-      online_softmax<C>(ws, S, n_valid, gq, qscale, p);
-      uint32_t pb[2][NT][2];
-#pragma unroll
-      for (int mu = 0; mu < 2; ++mu) {
-        const int ra = 4 * gq + 2 * mu;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          p_fragments(ra < n_valid ? p[nt][2 * mu] : 0.f, ra + 1 < n_valid ? p[nt][2 * mu + 1] : 0.f,
-                      pb[mu][nt][0], pb[mu][nt][1]);
-      }
-#pragma unroll
-      for (int mu = 0; mu < 2; ++mu) {
-        const int T1 = 8 * tq + 2 * mu;
-        const int tk[4] = {T1, T1 + 4, T1 + 1, T1 + 5};
-        const uint16_t* rows[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) rows[k] = resid_row(lo, a.cp, 1, layer, seq, h, t0 + min(tk[k], n_valid - 1));
-#pragma unroll
-        for (int s = 0; s < C::NS; ++s) {
-          uint2 r[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            r[k] = make_uint2(0, 0);
-            if (tk[k] < n_valid) r[k] = *reinterpret_cast<const uint2*>(rows[k] + 32 * s + 4 * gq);
-          }
-          // (token pair, channel 4gq+j) halves
-          const uint32_t x0 = __byte_perm(r[0].x, r[1].x, 0x5410), x1 = __byte_perm(r[0].x, r[1].x, 0x7632);
-          const uint32_t x2 = __byte_perm(r[0].y, r[1].y, 0x5410), x3 = __byte_perm(r[0].y, r[1].y, 0x7632);
-          const uint32_t y0 = __byte_perm(r[2].x, r[3].x, 0x5410), y1 = __byte_perm(r[2].x, r[3].x, 0x7632);
-          const uint32_t y2 = __byte_perm(r[2].y, r[3].y, 0x5410), y3 = __byte_perm(r[2].y, r[3].y, 0x7632);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma16816(ws.o[2 * s][nt], x0, x1, y0, y1, pb[mu][nt][0], pb[mu][nt][1]);
-            mma16816(ws.o[2 * s + 1][nt], x2, x3, y2, y3, pb[mu][nt][0], pb[mu][nt][1]);
-          }
-        }
-      }
-    }
-    // every lane is done with this stage before lane 0 refills it
-    fence_proxy_async();
-    __syncwarp();
-  }
-  if (stall_it >= 0) {
-    // a copy did not land in time: flag it, give this warp's copies still in
-    // flight (that tile's and the next one's) a last bounded wait, and merge
-    // whatever is there
-    if (lane == 0) atomicOr(a.status, KVQ_DEV_STALL);
-    for (int j = stall_it; j < stall_it + kStages; ++j) {
-      const int tj = first + kWarps * j;
-      if (tj < te && tj < n_c + n_m) (void)mbar_wait(mbar + warp * kStages + j % kStages, (j / kStages) & 1);
-    }
-  }
-  __syncthreads();
-
-  // ---- merge the warps (shared memory), then the splits (workspace) -------------
-  float* wm = reinterpret_cast<float*>(stage_base);  // [kWarps][g]
-  float* wl = wm + kWarps * kMaxGqa;                  // [kWarps][g]
-  float* wo = wl + kWarps * kMaxGqa;                  // [kWarps][g][D]
-  float* obuf = wo + kWarps * kMaxGqa * D;            // [g][D]
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    float l = ws.l[nt];
-    l += __shfl_xor_sync(0xffffffffu, l, 4);
-    l += __shfl_xor_sync(0xffffffffu, l, 8);
-    l += __shfl_xor_sync(0xffffffffu, l, 16);
-    float zo[C::Z ? C::NS : 1] = {};  // zero-point part of the output per 32-channel block
-    if constexpr (C::Z) {
-#pragma unroll
-      for (int s = 0; s < C::NS; ++s) {
-        float z = ws.zo[s][nt];
-        z += __shfl_xor_sync(0xffffffffu, z, 4);
-        z += __shfl_xor_sync(0xffffffffu, z, 8);
-        z += __shfl_xor_sync(0xffffffffu, z, 16);
-        zo[s] = z;
-      }
-    }
-    const int hh = 4 * nt + tq;
-    if (hh < g) {
-      if (gq == 0) {
-        wm[warp * kMaxGqa + hh] = ws.m[nt];
-        wl[warp * kMaxGqa + hh] = l;
-      }
-      float* orow = wo + (warp * kMaxGqa + hh) * D;
-#pragma unroll
-      for (int s = 0; s < C::NS; ++s)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int ch = 32 * s + 4 * gq + 2 * e;
-          const float zadd = C::Z ? zo[C::Z ? s : 0] : 0.f;
-          orow[ch] = ws.o[2 * s + e][nt][0] + ws.o[2 * s + e][nt][1] + zadd;
-          orow[ch + 1] = ws.o[2 * s + e][nt][2] + ws.o[2 * s + e][nt][3] + zadd;
-        }
-    }
-  }
-  __syncthreads();
-  if (tid == 0 && bad_page) atomicOr(a.status, KVQ_DEV_PAGE);
-  // CTA partial per head: M = max_w m_w, L = sum_w 2^(m_w - M) l_w, O likewise
-  const int64_t unit = ((int64_t)li * lo.B + seq) * lo.H + h;
-  float* part = a.partials + (unit * a.splits + split) * (int64_t)g * (D + 2);
-  for (int e = tid; e < g * D; e += kThreadsMma) {
-    const int hh = e / D, d = e % D;
-    float M = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * kMaxGqa + hh]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-      for (int w = 0; w < kWarps; ++w) {
-        const float sc = exp2f(wm[w * kMaxGqa + hh] - M);
-        L += sc * wl[w * kMaxGqa + hh];
-        O += sc * wo[(w * kMaxGqa + hh) * D + d];
-      }
-    }
-    if (a.splits == 1) {
-      obuf[e] = L > 0.f ? O / L : 0.f;
-    } else {
-      part[hh * (D + 2) + 2 + d] = O;
-      if (d == 0) {
-        part[hh * (D + 2)] = M;
-        part[hh * (D + 2) + 1] = L;
-      }
-    }
-  }
-  if (a.splits > 1) {
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) is_last = atomicAdd(a.tickets + unit, 1u) == (unsigned)(a.splits - 1);
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    const float* base = a.partials + unit * a.splits * (int64_t)g * (D + 2);
-    for (int e = tid; e < g * D; e += kThreadsMma) {
-      const int hh = e / D, d = e % D;
-      float M = -INFINITY;
-      for (int sp = 0; sp < a.splits; ++sp) M = fmaxf(M, __ldcg(base + ((int64_t)sp * g + hh) * (D + 2)));
-      float L = 0.f, O = 0.f;
-      if (M != -INFINITY) {
-        for (int sp = 0; sp < a.splits; ++sp) {
-          const float* pp = base + ((int64_t)sp * g + hh) * (D + 2);
-          const float w = exp2f(__ldcg(pp) - M);
-          L += w * __ldcg(pp + 1);
-          O += w * __ldcg(pp + 2 + d);
-        }
-      }
-      obuf[e] = L > 0.f ? O / L : 0.f;
-    }
-    if (tid == 0) a.tickets[unit] = 0;
-  }
-  __syncthreads();
-  if (lo.flags & KVQ_ROTATE_V) {
-    for (int r = warp; r < g * (D / 128); r += kWarps) {
-      float* pp = obuf + r * 128 + 4 * lane;
-      float v[4] = {pp[0], pp[1], pp[2], pp[3]};
-      warp_unrotate128(v, lo.d1, lo.d2);
-      pp[0] = v[0];
-      pp[1] = v[1];
-      pp[2] = v[2];
-      pp[3] = v[3];
-    }
-    __syncthreads();
-  }
-  for (int e = tid; e < g * D; e += kThreadsMma) a.out[qrow * D + e] = obuf[e];
-}
-
-template <class C>
-cudaError_t launch_mma(const DecodeArgs& a, cudaStream_t st) {
-  static_assert(C::SMEM >= C::QSM + (2 * kWarps * kMaxGqa + kWarps * kMaxGqa * C::D + kMaxGqa * C::D) * 4,
-                "merge scratch must fit in the stage buffers");
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
-  dim3 grid(a.splits, a.lo.H, a.n_layers * a.lo.B);
-  decode_mma_kernel<C><<<grid, kThreadsMma, C::SMEM, st>>>(a);
-  return cudaGetLastError();
-}
-
-bool fmt_is(const FmtInfo& f, int bits, int group, int axis) {
-  return f.bits == bits && f.group == group && f.axis == axis;
-}
-
-template <int D, int KF, int KG, int VF, int VG, bool Z = false>
-using T_ = Tier<D, KF, KG, VF, VG, Z>;
-
-}  // namespace
-
-// Tensor-core path when the cache fits it, else the generic path.
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
-  const Layout& lo = a.lo;
   const int TOK = KVQ_AXIS_TOKEN, CH = KVQ_AXIS_CHANNEL;
   const bool rope = (lo.flags & KVQ_K_PRE_ROPE) != 0;
-  bool ok = true;
-  if (lo.ring) ok = ok && lo.dtype == KVQ_DT_F16 && !(lo.flags & (KVQ_ROTATE_K | KVQ_ROTATE_V));
-  if (lo.paged) ok = ok && (lo.pt == 16 || lo.pt == 32);
-  if (lo.kf.codebook != lo.vf.codebook) ok = false;  // one tensor TBQ4, the other not: generic kernel
-  if (lo.kf.zp != lo.vf.zp) ok = false;              // one tensor asymmetric, the other not: generic kernel
-  if (!ok) return launch_decode_generic(a, st);
+  if (!mma_layout_ok(lo)) return false;
   if (lo.kf.codebook) {  // TBQ4 K and V (rotated 4-bit blocks of 128)
     if (lo.D == 128 && lo.g <= 4)
-      return launch_mma<Cfg<128, 1, T_<128, KF_TQ, 128, VF_TQ, 128>, T_<128, KF_TQ, 128, VF_TQ, 128>, false, false>>(a, st);
+      return run(Cfg<128, 1, T_<128, KF_TQ, 128, VF_TQ, 128>, T_<128, KF_TQ, 128, VF_TQ, 128>, false, false>{});
     if (lo.D == 256 && lo.g <= 8)
-      return launch_mma<Cfg<256, 2, T_<256, KF_TQ, 128, VF_TQ, 128>, T_<256, KF_TQ, 128, VF_TQ, 128>, false, false>>(a, st);
-    return launch_decode_generic(a, st);
+      return run(Cfg<256, 2, T_<256, KF_TQ, 128, VF_TQ, 128>, T_<256, KF_TQ, 128, VF_TQ, 128>, false, false>{});
+    return false;
   }
   const FmtInfo &k = lo.kf, &v = lo.vf;
   const bool kivi4 = fmt_is(k, 4, 32, CH) && fmt_is(v, 4, 32, TOK);
@@ -1242,44 +34,52 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
     if (lo.D == 128 && lo.g <= 4) {
       if (lo.tiered) {
         if (kivi4 && fmt_is(lo.kc, 2, 32, CH) && fmt_is(lo.vc, 2, 32, TOK)) {
-          if (rope) return launch_mma<Cfg<128, 1, Z4, Z2, true, true>>(a, st);
-          return launch_mma<Cfg<128, 1, Z4, Z2, true, false>>(a, st);
+          if (rope) return run(Cfg<128, 1, Z4, Z2, true, true>{});
+          return run(Cfg<128, 1, Z4, Z2, true, false>{});
         }
       } else if (kivi4) {
-        if (rope) return launch_mma<Cfg<128, 1, Z4, Z4, false, true>>(a, st);
-        return launch_mma<Cfg<128, 1, Z4, Z4, false, false>>(a, st);
+        if (rope) return run(Cfg<128, 1, Z4, Z4, false, true>{});
+        return run(Cfg<128, 1, Z4, Z4, false, false>{});
       } else if (kivi2 && !rope) {
-        return launch_mma<Cfg<128, 1, Z2, Z2, false, false>>(a, st);
+        return run(Cfg<128, 1, Z2, Z2, false, false>{});
       }
     }
-    return launch_decode_generic(a, st);
+    return false;
   }
   if (lo.D == 128 && lo.g <= 4 && kivi4) {
     if (lo.tiered) {
       if (fmt_is(lo.kc, 2, 32, CH) && fmt_is(lo.vc, 2, 32, TOK)) {
-        if (rope) return launch_mma<Cfg<128, 1, KIVI4, KIVI2, true, true>>(a, st);
-        return launch_mma<Cfg<128, 1, KIVI4, KIVI2, true, false>>(a, st);
+        if (rope) return run(Cfg<128, 1, KIVI4, KIVI2, true, true>{});
+        return run(Cfg<128, 1, KIVI4, KIVI2, true, false>{});
       }
     } else {
-      if (rope) return launch_mma<Cfg<128, 1, KIVI4, KIVI4, false, true>>(a, st);
-      return launch_mma<Cfg<128, 1, KIVI4, KIVI4, false, false>>(a, st);
+      if (rope) return run(Cfg<128, 1, KIVI4, KIVI4, false, true>{});
+      return run(Cfg<128, 1, KIVI4, KIVI4, false, false>{});
     }
   }
-  if (lo.tiered || rope) return launch_decode_generic(a, st);
+  if (lo.tiered || rope) return false;
   if (lo.D == 128 && lo.g <= 4) {
     using A = T_<128, KF_T4, 128, VF_T4, 128>;
     using B = T_<128, KF_T4, 32, VF_T4, 32>;
     using Q8 = T_<128, KF_T8, 32, VF_T8, 32>;
-    if (fmt_is(k, 4, 128, TOK) && fmt_is(v, 4, 128, TOK)) return launch_mma<Cfg<128, 1, A, A, false, false>>(a, st);
-    if (fmt_is(k, 4, 32, TOK) && fmt_is(v, 4, 32, TOK)) return launch_mma<Cfg<128, 1, B, B, false, false>>(a, st);
-    if (fmt_is(k, 8, 32, TOK) && fmt_is(v, 8, 32, TOK)) return launch_mma<Cfg<128, 1, Q8, Q8, false, false>>(a, st);
+    if (fmt_is(k, 4, 128, TOK) && fmt_is(v, 4, 128, TOK)) return run(Cfg<128, 1, A, A, false, false>{});
+    if (fmt_is(k, 4, 32, TOK) && fmt_is(v, 4, 32, TOK)) return run(Cfg<128, 1, B, B, false, false>{});
+    if (fmt_is(k, 8, 32, TOK) && fmt_is(v, 8, 32, TOK)) return run(Cfg<128, 1, Q8, Q8, false, false>{});
   }
   if (lo.D == 256 && lo.g <= 8) {
     using A4 = T_<256, KF_T4, 128, VF_T4, 128>;
     using A3 = T_<256, KF_T3, 128, VF_T3, 128>;
-    if (fmt_is(k, 4, 128, TOK) && fmt_is(v, 4, 128, TOK)) return launch_mma<Cfg<256, 2, A4, A4, false, false>>(a, st);
-    if (fmt_is(k, 3, 128, TOK) && fmt_is(v, 3, 128, TOK)) return launch_mma<Cfg<256, 2, A3, A3, false, false>>(a, st);
+    if (fmt_is(k, 4, 128, TOK) && fmt_is(v, 4, 128, TOK)) return run(Cfg<256, 2, A4, A4, false, false>{});
+    if (fmt_is(k, 3, 128, TOK) && fmt_is(v, 3, 128, TOK)) return run(Cfg<256, 2, A3, A3, false, false>{});
   }
+  return false;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
+  if (dispatch_mma(a, st, false, &e)) return e;
   return launch_decode_generic(a, st);
 }
 

@@ -520,37 +520,96 @@ kvq_status kvq_commit_lengths(const kvq_config* cfg, const int32_t* cu_new, int3
   return ok();
 }
 
-kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0,
-                                int32_t n_layers, const void* q, const int32_t* seq_lens, float* out,
-                                int32_t num_splits, void* workspace, size_t ws_bytes, void* stream) {
+// Checks the decode arguments and fills *a (everything but the step).
+static kvq_status prep_decode(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0, int32_t n_layers,
+                       const void* q, const int32_t* seq_lens, float* out, int32_t num_splits, void* workspace,
+                       size_t ws_bytes, DecodeArgs* a) {
   kvq_status st = check_config(cfg, false);
   if (st != KVQ_OK) return st;
   if (layer0 < 0 || n_layers < 1 || layer0 + n_layers > cfg->L)
     return fail(KVQ_ERR_ARG, "layers [%d, %d) outside [0, %d)", layer0, layer0 + n_layers, cfg->L);
   if (!q || !seq_lens || !out) return fail(KVQ_ERR_ARG, "q / seq_lens / out is NULL");
   if (num_splits < 0 || num_splits > kMaxSplits) return fail(KVQ_ERR_ARG, "num_splits=%d", num_splits);
-  DecodeArgs a{};
-  if ((st = cache_ptrs(cfg, cache, &a.cp)) != KVQ_OK) return st;
+  if ((st = cache_ptrs(cfg, cache, &a->cp)) != KVQ_OK) return st;
   WsLayout w;
   if ((st = check_ws(cfg, workspace, ws_bytes, &w)) != KVQ_OK) return st;
   int splits = num_splits ? num_splits : splits_for(cfg, n_layers);
   int64_t units = (int64_t)n_layers * cfg->batch * cfg->H_kv;
   if (splits > 1 && units * splits > w.max_partials)
     return fail(KVQ_ERR_WORKSPACE, "%d splits x %lld units exceed the workspace", splits, (long long)units);
-  a.lo = make_layout(cfg);
-  a.layer0 = layer0;
-  a.n_layers = n_layers;
-  a.q = (const uint16_t*)q;
-  a.seq_lens = seq_lens;
-  a.out = out;
-  a.splits = splits;
-  a.status = (uint32_t*)((char*)workspace + w.status);
-  a.tickets = (uint32_t*)((char*)workspace + w.tickets);
-  a.partials = (float*)((char*)workspace + w.partials);
-  a.rope = (const float2*)((char*)workspace + w.rope);
-  a.rope_base_rows = w.rope_base_rows;
+  a->lo = make_layout(cfg);
+  a->layer0 = layer0;
+  a->n_layers = n_layers;
+  a->q = (const uint16_t*)q;
+  a->seq_lens = seq_lens;
+  a->out = out;
+  a->splits = splits;
+  a->status = (uint32_t*)((char*)workspace + w.status);
+  a->tickets = (uint32_t*)((char*)workspace + w.tickets);
+  a->partials = (float*)((char*)workspace + w.partials);
+  a->rope = (const float2*)((char*)workspace + w.rope);
+  a->rope_base_rows = w.rope_base_rows;
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0,
+                                int32_t n_layers, const void* q, const int32_t* seq_lens, float* out,
+                                int32_t num_splits, void* workspace, size_t ws_bytes, void* stream) {
+  DecodeArgs a{};
+  kvq_status st = prep_decode(cfg, cache, layer0, n_layers, q, seq_lens, out, num_splits, workspace, ws_bytes, &a);
+  if (st != KVQ_OK) return st;
   cudaError_t e = launch_decode(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+  return ok();
+}
+
+kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0, int32_t n_layers,
+                           const void* k_new, const void* v_new, const void* q, const int32_t* seq_lens,
+                           float* out, int32_t num_splits, void* workspace, size_t ws_bytes, void* stream) {
+  DecodeArgs a{};
+  kvq_status st = prep_decode(cfg, cache, layer0, n_layers, q, seq_lens, out, num_splits, workspace, ws_bytes, &a);
+  if (st != KVQ_OK) return st;
+  if (!k_new || !v_new) return fail(KVQ_ERR_ARG, "k_new / v_new is NULL");
+  if (((uintptr_t)k_new | (uintptr_t)v_new) & 15u) return fail(KVQ_ERR_ARG, "k_new / v_new must be 16-byte aligned");
+  AppendArgs& s = a.step;
+  s.lo = a.lo;
+  s.cp = a.cp;
+  s.layer0 = layer0;
+  s.n_layers = n_layers;
+  s.k = (const uint16_t*)k_new;
+  s.v = (const uint16_t*)v_new;
+  s.cu_new = nullptr;
+  s.seq_lens = seq_lens;
+  s.total_new = cfg->batch;
+  s.max_new = 1;
+  s.status = a.status;
+  s.one_per_seq = 1;
+  a.len_add = 1;
+  cudaError_t e = cudaSuccess;
+  if (!launch_decode_step_fused(a, (cudaStream_t)stream, false, &e)) {
+    // formats of the generic decode: append, then decode over the new length
+    e = launch_append(s, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = launch_decode(a, (cudaStream_t)stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "decode step kernels");
+  return ok();
+}
+
+kvq_status kvq_step_launches(const kvq_config* cfg, int32_t* launches) {
+  kvq_status st = check_config(cfg, false);
+  if (st != KVQ_OK) return st;
+  if (!launches) return fail(KVQ_ERR_ARG, "output pointer is NULL");
+  DecodeArgs a{};
+  a.lo = make_layout(cfg);
+  a.step.lo = a.lo;
+  cudaError_t e = cudaSuccess;
+  if (launch_decode_step_fused(a, nullptr, true, &e)) {
+    *launches = 1;
+  } else {
+    int32_t app = 0, dec = 0;
+    kvq_launch_counts(cfg, &app, &dec);
+    *launches = app + dec;
+  }
   return ok();
 }
 

@@ -170,6 +170,7 @@ struct AppendArgs {
   const int32_t* seq_lens;
   int total_new, max_new;
   uint32_t* status;
+  int one_per_seq;  // 1: one new token per sequence, row `seq` of k / v (cu_new unused)
 };
 
 struct DecodeArgs {
@@ -185,6 +186,8 @@ struct DecodeArgs {
   float* partials;
   const float2* rope;  // base rows then offsets
   int rope_base_rows;
+  int len_add;      // the attended length is seq_lens[b] + len_add (1 in a decode step)
+  AppendArgs step;  // fused decode step: the append of the new token (step.k == nullptr otherwise)
 };
 
 struct DequantArgs {
@@ -205,6 +208,9 @@ bool fast_quantize_available(const AppendArgs& a);
 cudaError_t launch_commit_lengths(const int32_t* cu_new, int32_t* seq_lens, int batch, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);  // tensor-core path when it fits, else generic
 cudaError_t launch_decode_generic(const DecodeArgs& a, cudaStream_t s);
+// Fused decode step (a.step holds the append of one token per sequence, a.len_add = 1): one tensor-core
+// launch into *err unless `dry`; false when the formats take the generic path.
+bool launch_decode_step_fused(const DecodeArgs& a, cudaStream_t s, bool dry, cudaError_t* err);
 cudaError_t launch_dequantize(const DequantArgs& a, cudaStream_t s);
 cudaError_t launch_rope_tables(float2* rope, int base_rows, int D, float theta, cudaStream_t s);
 

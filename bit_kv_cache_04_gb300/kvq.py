@@ -128,6 +128,8 @@ def _load():
         "kvq_commit_lengths": ([cfgp, vp, vp, vp], ctypes.c_int),
         "kvq_decode_attention": ([cfgp, cachep, i32, i32, vp, vp, vp, i32, vp, sz, vp], ctypes.c_int),
         "kvq_decode_splits": ([cfgp, i32, P(i32)], ctypes.c_int),
+        "kvq_decode_step": ([cfgp, cachep, i32, i32, vp, vp, vp, vp, vp, i32, vp, sz, vp], ctypes.c_int),
+        "kvq_step_launches": ([cfgp, P(i32)], ctypes.c_int),
         "kvq_launch_counts": ([cfgp, P(i32), P(i32)], ctypes.c_int),
         "kvq_tbq4_codebook": ([P(ctypes.c_float), P(ctypes.c_float)], ctypes.c_int),
         "kvq_decode_attention_static": ([cfgp, cachep, i32, i32, vp, vp, vp, i32, vp], ctypes.c_int),
@@ -148,7 +150,7 @@ LIB = _load()
 EXPORTED = ("kvq_version", "kvq_last_error", "kvq_validate_config", "kvq_block_bytes", "kvq_bytes_per_token",
             "kvq_cache_bytes", "kvq_buffer_sizes", "kvq_workspace_bytes", "kvq_workspace_init", "kvq_append",
             "kvq_commit_lengths", "kvq_decode_attention", "kvq_decode_splits", "kvq_decode_attention_static",
-            "kvq_dequantize", "kvq_launch_counts", "kvq_tbq4_codebook",
+            "kvq_dequantize", "kvq_launch_counts", "kvq_tbq4_codebook", "kvq_decode_step", "kvq_step_launches",
             "kvq_read_device_status", "kvq_clear_device_status")
 
 
@@ -205,6 +207,13 @@ def kvq_launch_counts(cfg: Config):
     a, d = ctypes.c_int32(), ctypes.c_int32()
     _check(LIB.kvq_launch_counts(ctypes.byref(cfg.to_c()), ctypes.byref(a), ctypes.byref(d)))
     return a.value, d.value
+
+
+def kvq_step_launches(cfg: Config) -> int:
+    """Kernel launches of one kvq_decode_step call (1 when fused)."""
+    n = ctypes.c_int32()
+    _check(LIB.kvq_step_launches(ctypes.byref(cfg.to_c()), ctypes.byref(n)))
+    return n.value
 
 
 def kvq_workspace_bytes(cfg: Config) -> int:
@@ -270,6 +279,11 @@ class KVCache:
         _check(LIB.kvq_decode_attention(ctypes.byref(self.c_cfg), ctypes.byref(self.c_cache), layer0, n_layers,
                                         _ptr(q), _ptr(seq_lens), _ptr(out), num_splits,
                                         _ptr(self.workspace), self.ws_bytes, _stream(stream)))
+
+    def decode_step(self, layer0, n_layers, k_new, v_new, q, seq_lens, out, num_splits=0, stream=None):
+        _check(LIB.kvq_decode_step(ctypes.byref(self.c_cfg), ctypes.byref(self.c_cache), layer0, n_layers,
+                                   _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(seq_lens), _ptr(out), num_splits,
+                                   _ptr(self.workspace), self.ws_bytes, _stream(stream)))
 
     def dequantize(self, layer, seq, t0, t1, seq_lens, k_out, v_out, stream=None):
         _check(LIB.kvq_dequantize(ctypes.byref(self.c_cfg), ctypes.byref(self.c_cache), layer, seq, t0, t1,

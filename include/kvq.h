@@ -246,6 +246,32 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* 
                                 int32_t n_layers, const void* q, const int32_t* seq_lens, float* out,
                                 int32_t num_splits, void* workspace, size_t ws_bytes, void* stream);
 
+/* One decode step: appends one token to every sequence, then decode
+ * attention over the cache including it (nalar.dev, "Pertumbuhan cache
+ * dinamis mengubah persoalan kalibrasi": the cache grows by one entry per
+ * generated token and is written online).  Equivalent to kvq_append of
+ * k_new / v_new with one token per sequence followed by
+ * kvq_decode_attention over seq_lens[b] + 1 tokens: the same cache bytes
+ * and the same outputs.
+ *  k_new, v_new: [n_layers][batch][H_kv][D] in_dtype, device, 16-byte
+ *            aligned: the new token of every (layer, sequence).
+ *  q, out, num_splits: as kvq_decode_attention.
+ *  seq_lens: [batch] int32 device, lengths BEFORE the step; the new token
+ *            is at position seq_lens[b].  Not advanced here: the caller
+ *            advances them after all layers (kvq_commit_lengths with
+ *            cu_new = 0, 1, ..., batch).
+ * When the tensor-core decode handles the formats the step is one launch:
+ * the blocks that own the (at most three) tiles the token changes -- its
+ * window slot, the unit leaving the window, the group leaving the hot tier
+ * -- write them and then decode them; no block waits for another.  Other
+ * formats run the append and decode launches in turn. */
+KVQ_API kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0, int32_t n_layers,
+                                   const void* k_new, const void* v_new, const void* q, const int32_t* seq_lens,
+                                   float* out, int32_t num_splits, void* workspace, size_t ws_bytes, void* stream);
+
+/* Kernel launches one kvq_decode_step call makes (1 when fused). */
+KVQ_API kvq_status kvq_step_launches(const kvq_config* cfg, int32_t* launches);
+
 /* The split count kvq_decode_attention picks for num_splits = 0. */
 KVQ_API kvq_status kvq_decode_splits(const kvq_config* cfg, int32_t n_layers, int32_t* splits);
 

@@ -190,3 +190,14 @@ def test_zp_size_law_matches_oracle(kw):
         if n in shapes:
             shape, dt = shapes[n]
             assert sz == int(__import__("numpy").prod(shape)) * (2 if dt.__name__ == "uint16" else 1), n
+
+
+def test_step_launches():
+    # one fused launch for the layouts of the tensor-core decode the step
+    # files instantiate; append + decode launches for the others
+    for name in ("llama2_7b_kivi4", "llama2_7b_kivi4_zp", "mistral7b_hotcold", "gqa8b_hadamard4_paged",
+                 "ctx262k_hadamard4", "ctx262k_hadamard3"):
+        assert K.kvq_step_launches(W.make(name).cfg) == 1, name
+    for name in ("q4_0_mha_1k", "ctx262k_tbq4", "llama2_7b_kivi2_zp"):
+        a, d = K.kvq_launch_counts(W.make(name).cfg)
+        assert K.kvq_step_launches(W.make(name).cfg) == a + d, name
