@@ -188,7 +188,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     steps, warm = args.steps, args.warmup
-    extra = 2 * (steps + warm) + 16
+    extra = 3 * (steps + warm) + 16  # fused steps, unfused steps, end-to-end steps
     w = W.make(args.workload, extra_tokens=extra)
     if args.layers:
         w = w.scaled(L=args.layers, lengths=w.lengths, extra=extra)
@@ -241,9 +241,11 @@ def run_ours(args):
     cu1 = torch.arange(0, B + 1, dtype=torch.int32, device=dev)
 
     def step(i):
-        cache.append(0, L, new_k[i], new_v[i], cu1, seq_lens, B, 1, stream)
+        # one decode step: the new token of every (layer, sequence) appended and
+        # attention over the grown cache (one fused launch where the formats
+        # allow), then the length commit
         dec0[i].record(stream)
-        cache.decode(0, L, qs[i], seq_lens, out, 0, stream)
+        cache.decode_step(0, L, new_k[i], new_v[i], qs[i], seq_lens, out, 0, stream)
         dec1[i].record(stream)
         cache.commit_lengths(cu1, seq_lens, stream)
 
@@ -251,10 +253,10 @@ def run_ours(args):
     dec1 = [torch.cuda.Event(True) for _ in range(n_steps)]
     step_bytes = []
     for i in range(n_steps):
-        # the decode of step i reads the cache after its append: lengths + 1
+        # step i reads the cache grown by its token: lengths + 1, plus the
+        # token's source bytes
         lengths = [t + 1 for t in lengths]
-        step_bytes.append(sum(K.kvq_cache_bytes(cfg, t) for t in lengths)
-                          + L * B * H * D * 2 * 2)  # + append source bytes
+        step_bytes.append(sum(K.kvq_cache_bytes(cfg, t) for t in lengths) + L * B * H * D * 2 * 2)
     for i in range(warm):
         step(i)
     torch.cuda.synchronize()
@@ -279,10 +281,29 @@ def run_ours(args):
     timed_bytes = sum(step_bytes[warm:])
     value = timed_bytes * ws / elapsed / 1e9
     dec_ms = [dec0[i].elapsed_time(dec1[i]) for i in range(warm, n_steps)]
-    dec_bytes = [step_bytes[i] - L * B * H * D * 4 for i in range(warm, n_steps)]
-    achieved = sum(dec_bytes) / (sum(dec_ms) / 1e3) / 1e9
+    achieved = sum(step_bytes[warm:]) / (sum(dec_ms) / 1e3) / 1e9
     peak, peak_kind = _peaks()
     status = cache.device_status()
+    step_launches = K.kvq_step_launches(cfg)
+
+    # ---- the same steps unfused: kvq_append, decode attention, commit -----
+    def step_unfused(i):
+        cache.append(0, L, new_k[i], new_v[i], cu1, seq_lens, B, 1, stream)
+        cache.decode(0, L, qs[i], seq_lens, out, 0, stream)
+        cache.commit_lengths(cu1, seq_lens, stream)
+
+    for i in range(warm):
+        step_unfused(i)
+        lengths = [t + 1 for t in lengths]
+    torch.cuda.synchronize()
+    u0, u1 = torch.cuda.Event(True), torch.cuda.Event(True)
+    u0.record(stream)
+    for i in range(warm, n_steps):
+        step_unfused(i)
+        lengths = [t + 1 for t in lengths]
+    u1.record(stream)
+    torch.cuda.synchronize()
+    unfused_ms = u0.elapsed_time(u1) / steps
 
     # ---- end to end through the C ABI with host buffers -------------------
     hk = new_k.cpu().pin_memory()
@@ -298,8 +319,7 @@ def run_ours(args):
         dk.copy_(hk[i], non_blocking=True)
         dv.copy_(hv[i], non_blocking=True)
         dq.copy_(hq[i], non_blocking=True)
-        cache.append(0, L, dk, dv, cu1, seq_lens, B, 1, stream)
-        cache.decode(0, L, dq, seq_lens, out, 0, stream)
+        cache.decode_step(0, L, dk, dv, dq, seq_lens, out, 0, stream)
         cache.commit_lengths(cu1, seq_lens, stream)
         hout.copy_(out, non_blocking=True)
 
@@ -355,10 +375,14 @@ def run_ours(args):
         "config": {"workload": args.workload, "layers": L, "heads_q": Hq, "heads_kv": H, "head_dim": D,
                    "batch": B, "context_tokens": w.lengths[0] if B == 1 else w.lengths,
                    "format": fmt_text,
-                   "step": "append 1 token/seq to all layers + decode attention over all layers + length commit",
-                   "decode_launch": "one multi-layer launch",
+                   "step": "kvq_decode_step over all layers (1 new token per sequence appended, attention over the "
+                           "grown cache) + length commit",
+                   "decode_launch": "one fused multi-layer launch" if step_launches == 1
+                   else f"{step_launches} launches (append, then decode)",
                    "l2": "inputs larger than L2 (cache %.2f GB)" % (K.kvq_cache_bytes(cfg, w.lengths[0]) * B / 1e9),
                    "parallelism": f"replicas x{ws}"},
+        "step": {"fused_ms": round(statistics.mean(dec_ms), 4), "unfused_ms": round(unfused_ms, 4),
+                 "unfused": "kvq_append + kvq_decode_attention + commit per step", "launches": step_launches},
         "decode": {"per_layer_calls_ms": None if per_layer_ms is None else round(per_layer_ms, 4),
                    "GBps": round(achieved, 2), "pct_of_peak": round(100 * achieved / peak, 2),
                    "ms_per_launch": round(statistics.mean(dec_ms), 4),
@@ -369,10 +393,12 @@ def run_ours(args):
                            f"call; bytes = {in_text} source read + packed blocks and window written"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": _traffic(args.workload, L),
-                     "kernel": "decode attention (multi-layer launch)", "peak_source": peak_kind},
+                     "kernel": ("fused decode step: append + decode attention, one multi-layer launch"
+                                if step_launches == 1 else "decode step: append and decode launches"),
+                     "peak_source": peak_kind},
         "e2e": {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": steps * (sum(K.kvq_launch_counts(cfg)) + 1),  # append + decode + length commit
+        "gpu_launches": steps * (step_launches + 1),  # decode step + length commit
         "clocks": clk,
         "device_status": status,
     }
@@ -438,7 +464,7 @@ def _kernel_sha() -> str:
     import hashlib
 
     h = hashlib.sha256()
-    for f in ("decode_mma.cu", "block_codec.cuh"):
+    for f in ("decode_mma.cuh", "decode_step_kivi.cu", "append_generic.cuh", "append_common.cuh", "block_codec.cuh"):
         with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "bit_kv_cache_04_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()

@@ -722,42 +722,92 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
 // packed tier (phase B) and the window slot of the token itself (phase C).
 // Each tile belongs to exactly one block, which writes it before decoding it,
 // and no block reads a tile it does not own, so no block waits for another.
-// The step's phases, compiled once per head dim and called by every fused
-// kernel (they run in a few blocks per step).
+// The step for per-token 128-value blocks without a window (the rotated
+// layouts): the new token is quantized at once.  Warp w takes chunk w of the
+// token (K chunks, then V chunks), lane l its values 4l..4l+3: the same
+// randomized transform as the append kernels, the block's absolute maximum,
+// the fp16 scale, and code = clamp(rint(x / s)) with the IEEE quotient, packed
+// in the format's bit fields (4 bits: nibbles, value i in byte i / 2; 3 bits:
+// a little-endian stream, 8 values per 24-bit word).
 template <int NC>
-__device__ __noinline__ void step_phase_a(const AppendArgs& s, int li, int seq, int h) {
-  append_requant_unit<NC>(s, li, seq, h, 0);
-}
-template <int NC, bool ROT>
-__device__ __noinline__ void step_phase_b(const AppendArgs& s, int li, int seq, int h, uint8_t* sm) {
-  append_quantize_unit<NC, ROT>(s, li, seq, h, 0, sm);
-}
-__device__ __noinline__ void step_phase_c(const AppendArgs& s, int li, int seq, int h) {
-  append_window_unit(s, li, seq, h, 0);
+__device__ __forceinline__ void step_token128(const AppendArgs& s, int li, int seq, int h, int t) {
+  const Layout& lo = s.lo;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int layer = s.layer0 + li;
+  for (int item = warp; item < 2 * NC; item += kWarps) {
+    const int which = item / NC, c = item % NC;
+    const FmtInfo& f = fmt_main(lo, which);
+    const uint16_t* src = (which ? s.v : s.k) + (((int64_t)li * s.total_new + seq) * lo.H + h) * lo.D + 128 * c;
+    const float4 x = f16x4_to_f32(*reinterpret_cast<const uint2*>(src + 4 * lane), lo.dtype);
+    float v[4] = {x.x, x.y, x.z, x.w};
+    if (lo.flags & (which ? KVQ_ROTATE_V : KVQ_ROTATE_K)) warp_rotate128(v, lo.d1, lo.d2);
+    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const __half s16 = block_scale_of(m, f.qmax);
+    const float sf = __half2float(s16);
+    const int bias = 1 << (f.bits - 1);
+    uint32_t fld = 0;  // this lane's 4 biased codes, f.bits bits each
+#pragma unroll
+    for (int e = 0; e < 4; ++e) fld |= (uint32_t)(quant_code(v[e], sf, f.qmax) + bias) << (f.bits * e);
+    const uint32_t nxt = __shfl_down_sync(0xffffffffu, fld, 1);
+    bool bad = false;
+    uint8_t* blk = main_row(lo, s.cp, which, layer, seq, h, t, &bad);
+    if (bad) {  // warp-uniform
+      if (lane == 0) atomicOr(s.status, KVQ_DEV_PAGE);
+      continue;
+    }
+    blk += c * f.bb;
+    if (lane == 0) *reinterpret_cast<__half*>(blk) = s16;
+    if (f.bits == 4) {
+      *reinterpret_cast<uint16_t*>(blk + 2 + 2 * lane) = (uint16_t)fld;
+    } else if ((lane & 1) == 0) {  // 3 bits: lanes 2m, 2m + 1 form the 24-bit word m
+      const uint32_t w24 = fld | (nxt << 12);
+      uint8_t* p = blk + 2 + 3 * (lane >> 1);
+      p[0] = (uint8_t)w24;
+      p[1] = (uint8_t)(w24 >> 8);
+      p[2] = (uint8_t)(w24 >> 16);
+    }
+  }
 }
 
 template <class C, bool ROT>
-__device__ __forceinline__ void step_append(const DecodeArgs& a, int li, int seq, int h, int T, int qe, int ce,
-                                            int n_c, int n_m, int tb, int te, uint8_t* sm) {
+__device__ __forceinline__ void step_append(const DecodeArgs& a, uint8_t* sm) {
   const Layout& lo = a.lo;
-  const int T0 = T - 1;
-  if (T0 < 0) return;
+  const int split = blockIdx.x, h = blockIdx.y, li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B;
+  const int T0 = a.seq_lens[seq], T = T0 + 1;
+  if (T0 < 0 || T > lo.max_T) return;  // flagged by the decode
+  const int qe = q_end_of(lo, T);
+  const int ce = C::HAS_COLD ? c_end_of(lo, T) : 0;
+  const int n_c = ce / kTile;
+  const int n_m = (qe - ce + kTile - 1) / kTile;
+  const int n_w = (T - qe + kTile - 1) / kTile;
+  const int ntiles = n_c + n_m + n_w;
+  const int tb = (int)((int64_t)split * ntiles / a.splits);
+  const int te = (int)((int64_t)(split + 1) * ntiles / a.splits);
   const int q0 = q_end_of(lo, T0);
   const int c0 = C::HAS_COLD ? c_end_of(lo, T0) : 0;
   auto mine = [&](int tile) { return tile >= tb && tile < te; };
-  if (C::HAS_COLD && ce > c0 && mine(n_c - 1)) step_phase_a<C::D / 128>(a.step, li, seq, h);
-  if (qe > q0 && mine(q0 < ce ? q0 / kTile : n_c + (q0 - ce) / kTile)) step_phase_b<C::D / 128, ROT>(a.step, li, seq, h, sm);
-  if (T0 >= qe && mine(n_c + n_m + (T0 - qe) / kTile)) step_phase_c(a.step, li, seq, h);
+  if constexpr (ROT) {  // per-token 128-value blocks, no window: the token itself, in tile T0 / 32
+    if (mine(T0 / kTile)) step_token128<C::D / 128>(a.step, li, seq, h, T0);
+    return;
+  }
+  if (C::HAS_COLD && ce > c0 && mine(n_c - 1)) append_requant_unit<C::D / 128>(a.step, li, seq, h, 0);
+  if (qe > q0 && mine(q0 < ce ? q0 / kTile : n_c + (q0 - ce) / kTile))
+    append_quantize_unit<C::D / 128, ROT>(a.step, li, seq, h, 0, sm);
+  if (T0 >= qe && mine(n_c + n_m + (T0 - qe) / kTile)) append_window_unit(a.step, li, seq, h, 0);
 }
 
-// Shared-memory scratch of the step's phase B (raw rows, + rotated fp32 rows).
+// Shared-memory scratch of the step's generic phase B (raw rows); the
+// 128-value path needs none.
 template <class C, bool ROT>
 constexpr int step_smem() {
-  return 2 * kTile * (C::D + 8) * 2 + (ROT ? 2 * kTile * (C::D + 1) * 4 : 0);
+  return ROT ? 0 : 2 * kTile * (C::D + 8) * 2;
 }
 
-// STEP: 0 decode only; 1 fused decode step, unrotated formats; 2 fused
-// decode step, rotated formats.
+// STEP: 0 decode only; 1 fused decode step through the generic append
+// phases (windows, tiers, per-channel groups); 2 fused decode step of
+// per-token 128-value blocks without a window (step_token128).
 template <class C, int STEP>
 __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(DecodeArgs a) {
   constexpr int D = C::D, NT = C::NT, KC = C::KC;
@@ -772,6 +822,13 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   __shared__ uint64_t mbar[kWarps * kStages];
   __shared__ int is_last;
 
+  if constexpr (STEP != 0) {
+    // the step's cache writes first, then this block's decode reads them:
+    // generic-proxy writes ordered before the bulk copies (async proxy)
+    step_append<C, STEP == 2>(a, smem);
+    asm volatile("fence.proxy.async.global;\n" ::: "memory");
+    __syncthreads();
+  }
   const Layout& lo = a.lo;
   const int g = lo.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -795,13 +852,6 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   const int tb = (int)((int64_t)split * ntiles / a.splits);
   const int te = (int)((int64_t)(split + 1) * ntiles / a.splits);
   const int64_t qrow = ((int64_t)li * lo.B + seq) * lo.Hq + (int64_t)h * g;
-  if constexpr (STEP != 0) {
-    step_append<C, STEP == 2>(a, li, seq, h, T, qe, ce, n_c, n_m, tb, te, smem);
-    // this block's cache writes (generic proxy) before its bulk copies
-    // (async proxy) and loads of the same bytes
-    asm volatile("fence.proxy.async.global;\n" ::: "memory");
-    __syncthreads();
-  }
 
   // ---- query: fp32, rotated when K is stored rotated; per-lane fragments ----
   float qexp = 1.f;

@@ -27,7 +27,8 @@ bool step_fused_d128(const DecodeArgs& a, cudaStream_t st, bool dry, cudaError_t
       return false;
     return run(Cfg<128, 1, T_<128, KF_CH4, 32, VF_T4, 32>, T_<128, KF_CH2, 32, VF_T2, 32>, true, true>{}, S1{});
   }
-  if (rope || !fmt_is(k, 4, 128, TOK) || !fmt_is(v, 4, 128, TOK)) return false;  // 66 B / 128, rotated or not
+  // 66 B / 128, rotated or not, no window
+  if (rope || lo.ring || !fmt_is(k, 4, 128, TOK) || !fmt_is(v, 4, 128, TOK)) return false;
   return run(Cfg<128, 1, T_<128, KF_T4, 128, VF_T4, 128>, T_<128, KF_T4, 128, VF_T4, 128>, false, false>{}, S2{});
   return false;
 }
