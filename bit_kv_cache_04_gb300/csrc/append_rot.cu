@@ -24,6 +24,13 @@
 // 32-value slice with any q within 2^-16 of a half step, or with a subnormal
 // or saturated scale (where x is clamped to +-qmax s first), is redone with
 // the exact quotient.  Rows are built in shared memory and written out whole.
+//
+// TBQ4 blocks (same 66 B: fp16 L2 norm, 4-bit indices into the 16-entry
+// Lloyd-Max table; trefon.com, same section): a lane's 32 consecutive values
+// are exactly one of the norm's partial sums p_k (index order), S = (p0 + p1)
+// + (p2 + p3) by two shuffles, u = y / norm with the IEEE divide, and the
+// index counts the table midpoints strictly below u (a 4-step search over the
+// 15 ascending midpoints in shared memory).
 #include "append_fast.cuh"
 
 namespace kvq {
@@ -153,7 +160,7 @@ __device__ __forceinline__ float rot_codes_packed(const uint64_t (&P)[16], float
   return dmax;
 }
 
-template <int NC, int DT, int B, int which>
+template <int NC, int DT, int B, int which, bool TQ>
 __global__ void __launch_bounds__(kAppendThreads) quant_rot128_kernel(AppendArgs a) {
   constexpr int BB = 2 + 16 * B;  // 66 or 50 bytes per 128 values
   constexpr int ROW = NC * BB;
@@ -164,6 +171,7 @@ __global__ void __launch_bounds__(kAppendThreads) quant_rot128_kernel(AppendArgs
   static_assert(kAppendThreads == 128 && WTOK % TPS == 0, "tile geometry");
   __shared__ __align__(16) uint8_t out[kRotItem * ROW];
   __shared__ uint32_t page_bad;
+  __shared__ float cbt[16];  // TBQ4 midpoints
   const Layout& lo = a.lo;
   const int li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B, h = blockIdx.y;
   const int layer = a.layer0 + li;
@@ -175,6 +183,8 @@ __global__ void __launch_bounds__(kAppendThreads) quant_rot128_kernel(AppendArgs
   if (u0 >= u1) return;
   const int n_tok = u1 - u0;
   if (threadIdx.x == 0) page_bad = 0;
+  if (TQ && threadIdx.x < 15) cbt[threadIdx.x] = a.lo.cbt[threadIdx.x];
+  if (TQ) __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int a4 = lane & 3, slot = lane >> 2;
   const int tok_in_step = slot / NC, chunk = slot % NC;
@@ -261,6 +271,44 @@ __global__ void __launch_bounds__(kAppendThreads) quant_rot128_kernel(AppendArgs
         P[i] = fma2(SG, P[i], O);  // o + v (lower) or o - v (upper), exact sign
       }
     }
+    if constexpr (TQ) {
+      float y[32];  // the format's values d2 RN(t c), signed
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float lo, hi;
+        upk2(P[i], lo, hi);
+        y[2 * i] = __uint_as_float(__float_as_uint(__fmul_rn(lo, hadamard_scale())) ^ (((d2w >> (2 * i)) & 1u) << 31));
+        y[2 * i + 1] =
+            __uint_as_float(__float_as_uint(__fmul_rn(hi, hadamard_scale())) ^ (((d2w >> (2 * i + 1)) & 1u) << 31));
+        ss = __fadd_rn(ss, __fmul_rn(y[2 * i], y[2 * i]));
+        ss = __fadd_rn(ss, __fmul_rn(y[2 * i + 1], y[2 * i + 1]));
+      }
+      ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 1));
+      ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 2));
+      if (j >= n_tok) continue;  // the shuffles above are done
+      const __half n16 = __float2half_rn(fminf(__fsqrt_rn(ss), 65504.0f));
+      const float nf = __half2float(n16);
+      uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int b = 0; b < 32; ++b) {
+        const float u = nf > 0.f ? __fdiv_rn(y[b], nf) : 0.f;
+        int k = u > cbt[7] ? 8 : 0;
+        k += u > cbt[k + 3] ? 4 : 0;
+        k += u > cbt[k + 1] ? 2 : 0;
+        k += u > cbt[k] ? 1 : 0;
+        w[b >> 3] |= (uint32_t)k << (4 * (b & 7));
+      }
+      uint8_t* blk = out + j * ROW + chunk * BB;
+      if (a4 == 0) *reinterpret_cast<__half*>(blk) = n16;
+      uint16_t* p = reinterpret_cast<uint16_t*>(blk + 2 + 16 * a4);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        p[2 * k] = (uint16_t)w[k];
+        p[2 * k + 1] = (uint16_t)(w[k] >> 16);
+      }
+      continue;
+    }
     float v[32];
     float mt = 0.f;  // max |t|
 #pragma unroll
@@ -341,17 +389,18 @@ __global__ void __launch_bounds__(kAppendThreads) quant_rot128_kernel(AppendArgs
   if (threadIdx.x == 0 && page_bad) atomicOr(a.status, KVQ_DEV_PAGE);
 }
 
-template <int NC, int DT, int B>
+template <int NC, int DT, int B, bool TQ = false>
 void launch_rot(const AppendArgs& a, int which, cudaStream_t st) {
   const int chunks = (a.max_new + kRotItem - 1) / kRotItem + 2;
   const dim3 grid(chunks, a.lo.H, a.n_layers * a.lo.B);
-  if (which == 0) quant_rot128_kernel<NC, DT, B, 0><<<grid, kAppendThreads, 0, st>>>(a);
-  else quant_rot128_kernel<NC, DT, B, 1><<<grid, kAppendThreads, 0, st>>>(a);
+  if (which == 0) quant_rot128_kernel<NC, DT, B, 0, TQ><<<grid, kAppendThreads, 0, st>>>(a);
+  else quant_rot128_kernel<NC, DT, B, 1, TQ><<<grid, kAppendThreads, 0, st>>>(a);
 }
 
 template <int NC, int DT>
 bool rot_tensor(const AppendArgs& a, int which, bool dry, cudaStream_t st) {
   const FmtInfo& f = fmt_main(a.lo, which);
+  if (f.codebook) return dry || (launch_rot<NC, DT, 4, true>(a, which, st), true);
   if (f.bits == 4) return dry || (launch_rot<NC, DT, 4>(a, which, st), true);
   if (f.bits == 3) return dry || (launch_rot<NC, DT, 3>(a, which, st), true);
   return false;
@@ -362,7 +411,7 @@ bool rot_tensor(const AppendArgs& a, int which, bool dry, cudaStream_t st) {
 bool launch_fast_rot(const AppendArgs& a, int which, bool dry, cudaStream_t st) {
   const Layout& lo = a.lo;
   const FmtInfo& f = fmt_main(lo, which);
-  if (lo.tiered || f.axis != KVQ_AXIS_TOKEN || f.group != 128 || f.codebook || f.zp) return false;
+  if (lo.tiered || f.axis != KVQ_AXIS_TOKEN || f.group != 128 || f.zp) return false;
   if (lo.paged && lo.pt < 16) return false;  // the page-id cache holds kRotItem / 16 + 2 entries
   if (lo.dtype == KVQ_DT_F16)
     return lo.D == 128 ? rot_tensor<1, KVQ_DT_F16>(a, which, dry, st) : rot_tensor<2, KVQ_DT_F16>(a, which, dry, st);

@@ -118,7 +118,7 @@ def test_launch_counts():
     assert K.kvq_launch_counts(W.make("mistral7b_hotcold").cfg) == (1 + 2 + 1, 1)
     assert K.kvq_launch_counts(W.make("q8_0_mha_1k").cfg) == (2, 1)
     assert K.kvq_launch_counts(W.make("ctx262k_hadamard4").cfg) == (2, 1)  # rotated kernels for K and V
-    assert K.kvq_launch_counts(W.make("ctx262k_tbq4").cfg) == (1, 1)  # TBQ4: the generic kernel
+    assert K.kvq_launch_counts(W.make("ctx262k_tbq4").cfg) == (2, 1)  # TBQ4 too
     # asymmetric KIVI blocks take the specialized kernels too; per-token
     # 4-bit K with 2-bit V has no specialized pair: one generic launch
     zp = _bad(flags=K.ZP_K | K.ZP_V, k_fmt=K.Fmt(4, 32, K.AXIS_CHANNEL), residual_window=128)
