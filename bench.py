@@ -455,8 +455,8 @@ def _oracle_sample(w, heads, T, seed=0):
 # with the SHA-256 of the kernel source it was taken on; the roofline reports
 # them scaled to the timed launch while the source is unchanged, else null.
 DECODE_TRAFFIC = {
-    "llama2_7b_kivi4": {"sha256": "4e85b648efd5f4d78e64dcc52eac99707db4719d825add55305391b86affcce1", "bytes_per_layer": (610.409216e6 + 8.020736e6) / 4,
-                        "capture": "4-layer launch, profiles/decode_mma_llama2_7b_kivi4_4layers.md"},
+    "llama2_7b_kivi4": {"sha256": "b9fe5a1d958aa663cdf841866d47f54679a7255eb45f7484f91eee791a33f440", "bytes_per_layer": (610.763776e6 + 11.770624e6) / 4,
+                        "capture": "4-layer fused step launch, profiles/decode_step_llama2_7b_kivi4_4layers.md"},
 }
 
 

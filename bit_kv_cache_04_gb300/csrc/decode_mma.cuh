@@ -771,6 +771,20 @@ __device__ __forceinline__ void step_token128(const AppendArgs& s, int li, int s
   }
 }
 
+// The generic append phases of the step, out of line: inlined, they push
+// the decode loop out of the instruction cache.
+template <int NC>
+__device__ __noinline__ void step_phase_a(const AppendArgs& s, int li, int seq, int h) {
+  append_requant_unit<NC>(s, li, seq, h, 0);
+}
+template <int NC>
+__device__ __noinline__ void step_phase_b(const AppendArgs& s, int li, int seq, int h, uint8_t* sm) {
+  append_quantize_unit<NC, false>(s, li, seq, h, 0, sm);
+}
+__device__ __noinline__ void step_phase_c(const AppendArgs& s, int li, int seq, int h) {
+  append_window_unit(s, li, seq, h, 0);
+}
+
 template <class C, bool ROT>
 __device__ __forceinline__ void step_append(const DecodeArgs& a, uint8_t* sm) {
   const Layout& lo = a.lo;
@@ -792,10 +806,9 @@ __device__ __forceinline__ void step_append(const DecodeArgs& a, uint8_t* sm) {
     if (mine(T0 / kTile)) step_token128<C::D / 128>(a.step, li, seq, h, T0);
     return;
   }
-  if (C::HAS_COLD && ce > c0 && mine(n_c - 1)) append_requant_unit<C::D / 128>(a.step, li, seq, h, 0);
-  if (qe > q0 && mine(q0 < ce ? q0 / kTile : n_c + (q0 - ce) / kTile))
-    append_quantize_unit<C::D / 128, ROT>(a.step, li, seq, h, 0, sm);
-  if (T0 >= qe && mine(n_c + n_m + (T0 - qe) / kTile)) append_window_unit(a.step, li, seq, h, 0);
+  if (C::HAS_COLD && ce > c0 && mine(n_c - 1)) step_phase_a<C::D / 128>(a.step, li, seq, h);
+  if (qe > q0 && mine(q0 < ce ? q0 / kTile : n_c + (q0 - ce) / kTile)) step_phase_b<C::D / 128>(a.step, li, seq, h, sm);
+  if (T0 >= qe && mine(n_c + n_m + (T0 - qe) / kTile)) step_phase_c(a.step, li, seq, h);
 }
 
 // Shared-memory scratch of the step's generic phase B (raw rows); the
