@@ -41,6 +41,36 @@ __device__ __forceinline__ float in_to_f32_t(uint32_t bits16) {
   else return __uint_as_float(bits16 << 16);
 }
 
+// Packed pairs of fp32 (low half = first element).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 __device__ __forceinline__ float div_by_scale(float x, float sf, float rcp) {
   const float q0 = __fmul_rn(x, rcp);
   const float e = __fmaf_rn(-q0, sf, x);
@@ -62,24 +92,36 @@ __device__ __forceinline__ void codes32(const float (&v)[32], float sf, float rc
   constexpr int qmax = (1 << (B - 1)) - 1;
   constexpr int bias = qmax + 1;
   constexpr float magic = kRoundMagic + (float)bias;
+  // the quotient and the rounding on pairs of values (each half rounded like
+  // the scalar operation): q0 = RN(x rcp), e = RN(x - q0 s) exactly, RN(q0 + e rcp)
+  const uint64_t R2 = pk2(rcp, rcp), NS2 = pk2(-sf, -sf), M2 = pk2(magic, magic);
 #pragma unroll
   for (int k = 0; k < B; ++k) w[k] = 0;
   uint32_t corr[B];
 #pragma unroll
   for (int k = 0; k < B; ++k) corr[k] = 0;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float r = __fadd_rn(div_by_scale(v[j], sf, rcp), magic);
-    if (dq) dq[j] = __fmul_rn(__fsub_rn(r, magic), sf);
-    const uint32_t bits = __float_as_uint(r);
-    const int bit = B * j, k = bit / 32, sh = bit % 32;
-    if (sh + B > 32) {  // a 3-bit code across two words: place the true biased code
-      const uint32_t u = bits - kRoundMagicBits;
-      w[k] += u << sh;
-      w[k + 1] += u >> (32 - sh);
-    } else {
-      w[k] += bits << sh;
-      corr[k] += kRoundMagicBits << sh;
+  for (int i = 0; i < 16; ++i) {
+    const uint64_t X = pk2(v[2 * i], v[2 * i + 1]);
+    const uint64_t Q0 = mul2(X, R2);
+    const uint64_t Q1 = fma2(fma2(Q0, NS2, X), R2, Q0);
+    const uint64_t R = add2(Q1, M2);
+    float rr[2];
+    upk2(R, rr[0], rr[1]);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int j = 2 * i + c;
+      if (dq) dq[j] = __fmul_rn(__fsub_rn(rr[c], magic), sf);
+      const uint32_t bits = __float_as_uint(rr[c]);
+      const int bit = B * j, k = bit / 32, sh = bit % 32;
+      if (sh + B > 32) {  // a 3-bit code across two words: place the true biased code
+        const uint32_t u = bits - kRoundMagicBits;
+        w[k] += u << sh;
+        w[k + 1] += u >> (32 - sh);
+      } else {
+        w[k] += bits << sh;
+        corr[k] += kRoundMagicBits << sh;
+      }
     }
   }
 #pragma unroll
@@ -134,17 +176,29 @@ __device__ __forceinline__ void codes_zp(const float (&v)[32], float sf, float z
   uint32_t corr[B];
 #pragma unroll
   for (int k = 0; k < B; ++k) w[k] = corr[k] = 0;
+  // x - z, the quotient, the rounding and the half-step distance on pairs of
+  // values (each half rounded like the scalar operation)
+  const uint64_t Z2 = pk2(zf, zf), R2 = pk2(rcp, rcp), M2 = pk2(kRoundMagic, kRoundMagic);
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float d = __fsub_rn(v[j], zf);
-    float r0 = __fadd_rn(__fmul_rn(d, rcp), kRoundMagic);
-    if (fabsf(__fsub_rn(__fmul_rn(d, rcp), __fsub_rn(r0, kRoundMagic))) > kNearHalf)
-      r0 = __fadd_rn(__fdiv_rn(d, sf), kRoundMagic);
-    const float r = fminf(fmaxf(r0, kRoundMagic), top);
-    if (dq) dq[j] = __fadd_rn(__fmul_rn(__fsub_rn(r, kRoundMagic), sf), zf);
-    const int bit = B * j, k = bit / 32, sh = bit % 32;
-    w[k] += __float_as_uint(r) << sh;
-    corr[k] += kRoundMagicBits << sh;
+  for (int i = 0; i < 16; ++i) {
+    const uint64_t Dd = sub2(pk2(v[2 * i], v[2 * i + 1]), Z2);
+    const uint64_t Q = mul2(Dd, R2);
+    const uint64_t R0 = add2(Q, M2);
+    float d[2], r0[2], df[2];
+    upk2(Dd, d[0], d[1]);
+    upk2(R0, r0[0], r0[1]);
+    upk2(sub2(Q, sub2(R0, M2)), df[0], df[1]);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int j = 2 * i + c;
+      float rc = r0[c];
+      if (fabsf(df[c]) > kNearHalf) rc = __fadd_rn(__fdiv_rn(d[c], sf), kRoundMagic);
+      const float r = fminf(fmaxf(rc, kRoundMagic), top);
+      if (dq) dq[j] = __fadd_rn(__fmul_rn(__fsub_rn(r, kRoundMagic), sf), zf);
+      const int bit = B * j, k = bit / 32, sh = bit % 32;
+      w[k] += __float_as_uint(r) << sh;
+      corr[k] += kRoundMagicBits << sh;
+    }
   }
 #pragma unroll
   for (int k = 0; k < B; ++k) w[k] -= corr[k];
