@@ -44,7 +44,7 @@ What it computes, step by step, with the page each step follows:
   mengubah input softmax" and "Error pada value masuk setelah attention
   probability").
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent (the plainest reading in each case):
 symmetric codes in [-qmax, qmax] with qmax = 2^(b-1)-1; half-to-even rounding;
 fp16 scale saturating at 65504; a zero scale gives all-zero codes; nibble and
 bit order little-endian and element-ascending; 3-bit values packed eight to a
