@@ -168,6 +168,25 @@ def aggregate(values_bytes, times_s):
     return sum(values_bytes) / max(times_s)
 
 
+def _job_seconds(local_s: float, device) -> float:
+    """The slowest rank's timed seconds, returned on every rank (the local
+    time when there is one rank)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return local_s
+    t = torch.tensor([local_s], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_gbs(bytes_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job GB/s: every rank processes its own sequences (weak scaling),
+    so the job moves world x the bytes of one rank in the slowest rank's time."""
+    return bytes_per_rank * world / seconds / 1e9
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -273,13 +292,9 @@ def run_ours(args):
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    elapsed = t0.elapsed_time(t1) / 1e3
-    if ws > 1:
-        tt = torch.tensor([elapsed], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed = tt.item()
+    elapsed = _job_seconds(t0.elapsed_time(t1) / 1e3, dev)
     timed_bytes = sum(step_bytes[warm:])
-    value = timed_bytes * ws / elapsed / 1e9
+    value = _job_gbs(timed_bytes, ws, elapsed)
     dec_ms = [dec0[i].elapsed_time(dec1[i]) for i in range(warm, n_steps)]
     achieved = sum(step_bytes[warm:]) / (sum(dec_ms) / 1e3) / 1e9
     peak, peak_kind = _peaks()
@@ -415,9 +430,10 @@ def run_ours(args):
 def _oracle_cfg(c):
     from oracle import kvq_oracle as O
 
-    f = lambda x: None if x is None else O.Fmt(x.bits, x.group, x.axis)  # noqa: E731
+    zk, zv = bool(c.flags & 32), bool(c.flags & 64)  # the library's asymmetric-block flags
+    f = lambda x, zp: None if x is None else O.Fmt(x.bits, x.group, x.axis, zp)  # noqa: E731
     return O.Config(L=c.L, H_kv=c.H_kv, H_q=c.H_q, D=c.D, batch=c.batch, max_T=c.max_T, in_dtype=c.in_dtype,
-                    k_fmt=f(c.k_fmt), v_fmt=f(c.v_fmt), k_cold=f(c.k_cold), v_cold=f(c.v_cold),
+                    k_fmt=f(c.k_fmt, zk), v_fmt=f(c.v_fmt, zv), k_cold=f(c.k_cold, zk), v_cold=f(c.v_cold, zv),
                     hot_window=c.hot_window, residual_window=c.residual_window, flags=c.flags,
                     rope_theta=c.rope_theta, sign_seed=c.sign_seed, page_tokens=c.page_tokens,
                     n_pages=c.n_pages, max_pages_per_seq=c.max_pages_per_seq)
