@@ -394,7 +394,7 @@ struct Ctx {
   const float4* qr;       // [KC][NT][32]: fp32 query (RoPE)
   const float* qz;        // [4 NT][D]: fp32 query by head, zero past g (asymmetric K)
   const float2* rope_base;
-  const float4* rope_frag;  // [KC/2][4 tokens k][2 pairs][32 lanes]: R(j) of this lane's channels
+  const float4* rope_frag;  // [KC/2][4 tokens k][2 pairs][32 lanes]: (cos, cos, sin, sin) of R(j), lane's channels
   uint32_t lut[4];          // TBQ4 table magnitudes: low bytes (2 words), high bytes (2 words)
 };
 
@@ -420,32 +420,31 @@ __device__ __forceinline__ void rope_query_pair(const Ctx<C>& cx, const float2* 
   }
 }
 
-// fp32 key values of lower channels ch[0..3] (lv) and their partners (uv)
-// of token k of the lane's four (4gq + k), turned by R(4gq + k), as hi/lo A
-// fragments (row rr of the A tile; [0] lower k-chunk, [1] partner k-chunk).
-// cs: (cos, sin) of channels ch[0], ch[1] and ch[2], ch[3].
-__device__ __forceinline__ void rope_key_frags(const float4 (&cs)[2], const float (&lv)[4], const float (&uv)[4],
+// Key values of lower channels ch[0..3] (L: pairs (ch0, ch1), (ch2, ch3))
+// and their partners (U) of token k of the lane's four (4gq + k), turned by
+// R(4gq + k), as hi/lo A fragments (row rr of the A tile; [0] lower k-chunk,
+// [1] partner k-chunk).  cs[h]: (cos, cos, sin, sin) of the pair h.  The turn
+// and the hi/lo remainders run on packed fp32 pairs.
+__device__ __forceinline__ void rope_key_frags(const float4 (&cs)[2], const uint64_t (&L)[2], const uint64_t (&U)[2],
                                                int rr, uint32_t (&ah)[2][4], uint32_t (&al)[2][4]) {
-  const float c[4] = {cs[0].x, cs[0].z, cs[1].x, cs[1].z};
-  const float sn[4] = {cs[0].y, cs[0].w, cs[1].y, cs[1].w};
-  float nl[4], nu[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    nl[q] = lv[q] * c[q] - uv[q] * sn[q];
-    nu[q] = lv[q] * sn[q] + uv[q] * c[q];
+  for (int hp = 0; hp < 2; ++hp) {
+    const uint64_t C = pk2(cs[hp].x, cs[hp].y), S = pk2(cs[hp].z, cs[hp].w);
+    const uint64_t NL = sub2(mul2(L[hp], C), mul2(U[hp], S));  // l cos - u sin
+    const uint64_t NU = fma2(L[hp], S, mul2(U[hp], C));        // l sin + u cos
+    float l0, l1, u0, u1;
+    upk2(NL, l0, l1);
+    upk2(NU, u0, u1);
+    const __half2 hl = __floats2half2_rn(l0, l1), hu = __floats2half2_rn(u0, u1);
+    const float2 fl = __half22float2(hl), fu = __half22float2(hu);
+    float dl0, dl1, du0, du1;
+    upk2(sub2(NL, pk2(fl.x, fl.y)), dl0, dl1);
+    upk2(sub2(NU, pk2(fu.x, fu.y)), du0, du1);
+    ah[0][2 * hp + rr] = *reinterpret_cast<const uint32_t*>(&hl);
+    al[0][2 * hp + rr] = pack_h2(dl0, dl1);
+    ah[1][2 * hp + rr] = *reinterpret_cast<const uint32_t*>(&hu);
+    al[1][2 * hp + rr] = pack_h2(du0, du1);
   }
-  const __half2 hl01 = __floats2half2_rn(nl[0], nl[1]), hl23 = __floats2half2_rn(nl[2], nl[3]);
-  const __half2 hu01 = __floats2half2_rn(nu[0], nu[1]), hu23 = __floats2half2_rn(nu[2], nu[3]);
-  const float2 fl01 = __half22float2(hl01), fl23 = __half22float2(hl23);
-  const float2 fu01 = __half22float2(hu01), fu23 = __half22float2(hu23);
-  ah[0][rr] = *reinterpret_cast<const uint32_t*>(&hl01);
-  ah[0][2 + rr] = *reinterpret_cast<const uint32_t*>(&hl23);
-  al[0][rr] = pack_h2(nl[0] - fl01.x, nl[1] - fl01.y);
-  al[0][2 + rr] = pack_h2(nl[2] - fl23.x, nl[3] - fl23.y);
-  ah[1][rr] = *reinterpret_cast<const uint32_t*>(&hu01);
-  ah[1][2 + rr] = *reinterpret_cast<const uint32_t*>(&hu23);
-  al[1][rr] = pack_h2(nu[0] - fu01.x, nu[1] - fu01.y);
-  al[1][2 + rr] = pack_h2(nu[2] - fu23.x, nu[3] - fu23.y);
 }
 
 // PV for one packed group: P^T per V block (probabilities times the per-token
@@ -554,6 +553,9 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
           }
         }
         const float4* fr = cx.rope_frag + kcp * 256 + lane;
+        // scales (and zeros) of the pairs (ch0, ch1), (ch2, ch3), lower and partner
+        const uint64_t SL[2] = {pk2(sl[0], sl[1]), pk2(sl[2], sl[3])}, SU[2] = {pk2(su[0], su[1]), pk2(su[2], su[3])};
+        const uint64_t ZL[2] = {pk2(zl[0], zl[1]), pk2(zl[2], zl[3])}, ZU[2] = {pk2(zu[0], zu[1]), pk2(zu[2], zu[3])};
 #pragma unroll
         for (int mu = 0; mu < 2; ++mu) {
           uint32_t ah[2][4], al[2][4];
@@ -565,11 +567,13 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
             const float2 l23 = __half22float2(*reinterpret_cast<const __half2*>(&cl1[k]));
             const float2 u01 = __half22float2(*reinterpret_cast<const __half2*>(&cu0[k]));
             const float2 u23 = __half22float2(*reinterpret_cast<const __half2*>(&cu1[k]));
-            const float lv[4] = {fmaf(l01.x, sl[0], zl[0]), fmaf(l01.y, sl[1], zl[1]), fmaf(l23.x, sl[2], zl[2]),
-                                 fmaf(l23.y, sl[3], zl[3])};
-            const float uv[4] = {fmaf(u01.x, su[0], zu[0]), fmaf(u01.y, su[1], zu[1]), fmaf(u23.x, su[2], zu[2]),
-                                 fmaf(u23.y, su[3], zu[3])};
-            rope_key_frags(cs, lv, uv, rr, ah, al);
+            uint64_t Lv[2] = {pk2(l01.x, l01.y), pk2(l23.x, l23.y)}, Uv[2] = {pk2(u01.x, u01.y), pk2(u23.x, u23.y)};
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp) {
+              Lv[hp] = TR::Z ? fma2(Lv[hp], SL[hp], ZL[hp]) : mul2(Lv[hp], SL[hp]);
+              Uv[hp] = TR::Z ? fma2(Uv[hp], SU[hp], ZU[hp]) : mul2(Uv[hp], SU[hp]);
+            }
+            rope_key_frags(cs, Lv, Uv, rr, ah, al);
           }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
@@ -1102,10 +1106,9 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
               const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&wl1));
               const float2 b0 = __half22float2(*reinterpret_cast<const __half2*>(&wu0));
               const float2 b1 = __half22float2(*reinterpret_cast<const __half2*>(&wu1));
-              const float lv[4] = {a0.x, a1.x, a0.y, a1.y};
-              const float uv[4] = {b0.x, b1.x, b0.y, b1.y};
+              const uint64_t Lv[2] = {pk2(a0.x, a1.x), pk2(a0.y, a1.y)}, Uv[2] = {pk2(b0.x, b1.x), pk2(b0.y, b1.y)};
               const float4 cs[2] = {__ldg(fr + (2 * k) * 32), __ldg(fr + (2 * k + 1) * 32)};
-              rope_key_frags(cs, lv, uv, rr, ah, al);
+              rope_key_frags(cs, Lv, Uv, rr, ah, al);
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {

@@ -118,7 +118,14 @@ __global__ void rope_tables_kernel(float2* rope, int base_rows, int D, double th
     const double inv = pow(theta, -2.0 * i / D);
     double s, c;
     sincos(pos * inv, &s, &c);
-    rope[e] = make_float2((float)c, (float)s);
+    if (e < plain) {
+      rope[e] = make_float2((float)c, (float)s);
+    } else {  // fragment order: per 16 bytes (cos q0, cos q1, sin q0, sin q1)
+      const int f2 = e - plain;
+      float* rf = reinterpret_cast<float*>(rope + plain);
+      rf[4 * (f2 >> 1) + (f2 & 1)] = (float)c;
+      rf[4 * (f2 >> 1) + 2 + (f2 & 1)] = (float)s;
+    }
   }
 }
 
