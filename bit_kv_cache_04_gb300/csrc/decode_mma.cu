@@ -20,7 +20,7 @@ bool dispatch_mma(const DecodeArgs& a, cudaStream_t st, bool dry, cudaError_t* e
     if (lo.D == 128 && lo.g <= 4)
       return run(Cfg<128, 1, T_<128, KF_TQ, 128, VF_TQ, 128>, T_<128, KF_TQ, 128, VF_TQ, 128>, false, false>{});
     if (lo.D == 256 && lo.g <= 8)
-      return run(Cfg<256, 2, T_<256, KF_TQ, 128, VF_TQ, 128>, T_<256, KF_TQ, 128, VF_TQ, 128>, false, false>{});
+      return run(Cfg<256, 1, T_<256, KF_TQ, 128, VF_TQ, 128>, T_<256, KF_TQ, 128, VF_TQ, 128>, false, false, true>{});
     return false;
   }
   const FmtInfo &k = lo.kf, &v = lo.vf;
@@ -69,8 +69,8 @@ bool dispatch_mma(const DecodeArgs& a, cudaStream_t st, bool dry, cudaError_t* e
   if (lo.D == 256 && lo.g <= 8) {
     using A4 = T_<256, KF_T4, 128, VF_T4, 128>;
     using A3 = T_<256, KF_T3, 128, VF_T3, 128>;
-    if (fmt_is(k, 4, 128, TOK) && fmt_is(v, 4, 128, TOK)) return run(Cfg<256, 2, A4, A4, false, false>{});
-    if (fmt_is(k, 3, 128, TOK) && fmt_is(v, 3, 128, TOK)) return run(Cfg<256, 2, A3, A3, false, false>{});
+    if (fmt_is(k, 4, 128, TOK) && fmt_is(v, 4, 128, TOK)) return run(Cfg<256, 1, A4, A4, false, false, true>{});
+    if (fmt_is(k, 3, 128, TOK) && fmt_is(v, 3, 128, TOK)) return run(Cfg<256, 1, A3, A3, false, false, true>{});
   }
   return false;
 }

@@ -52,7 +52,7 @@ enum : int { VF_T8 = 0, VF_T4 = 1, VF_T3 = 2, VF_T2 = 3, VF_TQ = 4 };
 
 constexpr int kWarps = 4;
 constexpr int kThreadsMma = kWarps * 32;
-constexpr int kStages = 2;  // per-warp cp.async ring: one group in flight while one is consumed
+constexpr int kMaxStages = 3;  // per-warp bulk-copy ring depth (Cfg::STAGES), at most
 constexpr float kLog2eF = 1.4426950408889634f;
 
 constexpr int bits_k(int kf) { return kf == KF_T8 ? 8 : kf == KF_T3 ? 3 : kf == KF_CH2 ? 2 : 4; }
@@ -89,24 +89,38 @@ struct Tier {
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
 // HOT: the only tier (COLD_ = false) or the hot tier; COLD: the cold tier.
-template <int D_, int NT_, class HOT_, class COLD_, bool HAS_COLD_, bool ROPE_>
+// HC: the MMA columns are the query heads themselves (8 per n-tile) and the
+// query / probability hi and lo parts are two B fragments accumulated into the
+// same C (for groups of more than 4 heads: the same MMAs as hi / lo columns,
+// half the accumulators).  Otherwise column 2h is head h's hi part and 2h + 1
+// its lo part.
+template <int D_, int NT_, class HOT_, class COLD_, bool HAS_COLD_, bool ROPE_, bool HC_ = false>
 struct Cfg {
   static constexpr int D = D_, NT = NT_;
+  static constexpr bool HC = HC_;
+  static constexpr int J = HC ? 2 : 1;  // heads per lane per n-tile
   using HOT = HOT_;
   using COLD = COLD_;
   static constexpr bool HAS_COLD = HAS_COLD_, ROPE = ROPE_;
   static constexpr bool Z = HOT::Z;
   static_assert(!HAS_COLD || COLD::Z == HOT::Z, "both tiers asymmetric or neither");
+  static_assert(!HC || (!HOT::KCH && !ROPE && !Z && !HAS_COLD && NT == 1), "heads as columns: per-token K only");
   static constexpr int KSTAGE = HAS_COLD ? cmax(HOT::KSTAGE, COLD::KSTAGE) : HOT::KSTAGE;
   static constexpr int VSTAGE = HAS_COLD ? cmax(HOT::VSTAGE, COLD::VSTAGE) : HOT::VSTAGE;
   static constexpr int VOFF = align16(KSTAGE + 16);
   static constexpr int STAGE = VOFF + align16(VSTAGE + 16);
   static constexpr int KC = D / 16;  // k-chunks
   static constexpr int NS = D / 32;  // spans
-  // per-lane query fragments (+ fp32 query for RoPE, + fp32 query by head for the zero terms)
-  static constexpr int QSM = KC * NT * 32 * (16 + (ROPE ? 16 : 0) + (Z ? 8 : 0));
+  // per-lane query fragments (+ fp32 query for RoPE, + fp32 query by head for
+  // the zero terms, + the lo fragments with heads as columns)
+  static constexpr bool QH = HOT::KCH || (HAS_COLD && COLD::KCH);  // query half pairs (per-channel K)
+  static constexpr int QSM = KC * NT * 32 * (8 + (QH ? 8 : 0) + (ROPE ? 16 : 0) + (Z ? 8 : 0) + (HC ? 8 : 0));
   static constexpr int MIN_CTAS = D == 128 ? 4 : 2;  // CTAs per SM the register budget aims at
-  static constexpr int SMEM = QSM + kWarps * kStages * STAGE;
+  // groups in flight per warp: one consumed while STAGES - 1 land (D = 256 runs two CTAs per SM,
+  // so each warp keeps two groups in flight)
+  static constexpr int STAGES = D == 256 ? 3 : 2;
+  static_assert(STAGES <= kMaxStages, "stage count");
+  static constexpr int SMEM = QSM + kWarps * STAGES * STAGE;
 };
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -324,7 +338,7 @@ __device__ __forceinline__ void v_pair4(const uint8_t* pa, const uint8_t* pb, in
 template <class C>
 struct WarpState {
   float o[C::KC][C::NT][4];
-  float m[C::NT], l[C::NT];
+  float m[C::NT * C::J], l[C::NT * C::J];  // per (n-tile, head of the lane)
   // asymmetric V: sum over this lane's tokens of p z' per 32-channel block
   // (for the lane's head 4 nt + tq), rescaled with o
   float zo[C::Z ? C::NS : 1][C::NT];
@@ -334,41 +348,58 @@ struct WarpState {
 // thread's four tokens 4gq..4gq+3 for each n-tile.
 template <class C>
 __device__ __forceinline__ void online_softmax(WarpState<C>& ws, float (&S)[2][C::NT][4], int n_valid, int gq,
-                                               float qscale, float (&p)[C::NT][4]) {
+                                               float qscale, float (&p)[C::NT][C::J][4]) {
 #pragma unroll
   for (int nt = 0; nt < C::NT; ++nt) {
-    float s[4];
-    s[0] = (S[0][nt][0] + S[0][nt][1]) * qscale;
-    s[1] = (S[0][nt][2] + S[0][nt][3]) * qscale;
-    s[2] = (S[1][nt][0] + S[1][nt][1]) * qscale;
-    s[3] = (S[1][nt][2] + S[1][nt][3]) * qscale;
-    float mx = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (4 * gq + k >= n_valid) s[k] = -INFINITY;
-      mx = fmaxf(mx, s[k]);
-    }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    const float m_new = fmaxf(ws.m[nt], mx);
-    const float alpha = exp2f(ws.m[nt] - m_new);
-    ws.m[nt] = m_new;
-    float sum = 0.f;
+    for (int j = 0; j < C::J; ++j) {
+      float s[4];
+      if constexpr (C::HC) {  // column 2tq + j is head 8 nt + 2 tq + j
+        s[0] = S[0][nt][j] * qscale;
+        s[1] = S[0][nt][2 + j] * qscale;
+        s[2] = S[1][nt][j] * qscale;
+        s[3] = S[1][nt][2 + j] * qscale;
+      } else {  // columns 2tq (hi) + 2tq + 1 (lo): head 4 nt + tq
+        s[0] = (S[0][nt][0] + S[0][nt][1]) * qscale;
+        s[1] = (S[0][nt][2] + S[0][nt][3]) * qscale;
+        s[2] = (S[1][nt][0] + S[1][nt][1]) * qscale;
+        s[3] = (S[1][nt][2] + S[1][nt][3]) * qscale;
+      }
+      float mx = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      p[nt][k] = exp2f(s[k] - m_new);
-      sum += p[nt][k];
-    }
-    ws.l[nt] = ws.l[nt] * alpha + sum;
-    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      for (int k = 0; k < 4; ++k) {
+        if (4 * gq + k >= n_valid) s[k] = -INFINITY;
+        mx = fmaxf(mx, s[k]);
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const int si = nt * C::J + j;
+      const float m_new = fmaxf(ws.m[si], mx);
+      const float alpha = exp2f(ws.m[si] - m_new);
+      ws.m[si] = m_new;
+      float sum = 0.f;
 #pragma unroll
-      for (int i = 0; i < C::KC; ++i)
+      for (int k = 0; k < 4; ++k) {
+        p[nt][j][k] = exp2f(s[k] - m_new);
+        sum += p[nt][j][k];
+      }
+      ws.l[si] = ws.l[si] * alpha + sum;
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) ws.o[i][nt][e] *= alpha;
-      if constexpr (C::Z) {
+        for (int i = 0; i < C::KC; ++i) {
+          if constexpr (C::HC) {
+            ws.o[i][nt][j] *= alpha;
+            ws.o[i][nt][2 + j] *= alpha;
+          } else {
 #pragma unroll
-        for (int s = 0; s < C::NS; ++s) ws.zo[s][nt] *= alpha;
+            for (int e = 0; e < 4; ++e) ws.o[i][nt][e] *= alpha;
+          }
+        }
+        if constexpr (C::Z) {
+#pragma unroll
+          for (int s2 = 0; s2 < C::NS; ++s2) ws.zo[s2][nt] *= alpha;
+        }
       }
     }
   }
@@ -383,13 +414,22 @@ __device__ __forceinline__ void p_fragments(float pa, float pb, uint32_t& b0, ui
   b1 = movtrans(pack_h2(hb, pb - hb));
 }
 
+// Heads as columns: the probabilities pA, pB of one token for the lane's two
+// heads (columns 2tq, 2tq + 1) as the hi and the lo B fragments.
+__device__ __forceinline__ void p_fragments_hc(float pA, float pB, uint32_t& hi, uint32_t& lo) {
+  const float hA = rn16(pA), hB = rn16(pB);
+  hi = movtrans(pack_h2(hA, hB));
+  lo = movtrans(pack_h2(pA - hA, pB - hB));
+}
+
 // Per-thread context of the decode kernel shared with its helpers.
 template <class C>
 struct Ctx {
   int gq, tq, lane, g;
   bool lo_part;
   uint32_t lo_mask;
-  const uint2* qb;        // [KC][NT][32]: B fragments (hi or lo part)
+  const uint2* qb;        // [KC][NT][32]: B fragments (hi or lo part; hi with heads as columns)
+  const uint2* qbl;       // [KC][NT][32]: lo B fragments (heads as columns)
   const uint2* qh;        // [KC][NT][32]: query half pairs
   const float4* qr;       // [KC][NT][32]: fp32 query (RoPE)
   const float* qz;        // [4 NT][D]: fp32 query by head, zero past g (asymmetric K)
@@ -451,12 +491,12 @@ __device__ __forceinline__ void rope_key_frags(const float4 (&cs)[2], const uint
 // value scales), O^T += V^T P^T.
 template <class C, class TR>
 __device__ __forceinline__ void pv_packed(const Ctx<C>& cx, WarpState<C>& ws, const uint8_t* vsm, int n_valid,
-                                          const float (&p)[C::NT][4]) {
+                                          const float (&p)[C::NT][C::J][4]) {
   constexpr int D = C::D, NT = C::NT;
   const int gq = cx.gq, tq = cx.tq;
 #pragma unroll
     for (int bv = 0; bv < D / TR::VG; ++bv) {
-      uint32_t pb[2][NT][2];
+      uint32_t pb[2][NT][2], pbl[C::HC ? 2 : 1][NT][2];  // hi (or hi/lo columns), lo (heads as columns)
 #pragma unroll
       for (int mu = 0; mu < 2; ++mu) {
         const int ra = 4 * gq + 2 * mu;
@@ -471,12 +511,18 @@ __device__ __forceinline__ void pv_packed(const Ctx<C>& cx, WarpState<C>& ws, co
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const float pa = ra < n_valid ? p[nt][2 * mu] * sva : 0.f;
-          const float pbb = ra + 1 < n_valid ? p[nt][2 * mu + 1] * svb : 0.f;
-          p_fragments(pa, pbb, pb[mu][nt][0], pb[mu][nt][1]);
+          if constexpr (C::HC) {
+            const float qa = ra < n_valid ? sva : 0.f, qb = ra + 1 < n_valid ? svb : 0.f;
+            p_fragments_hc(p[nt][0][2 * mu] * qa, p[nt][1][2 * mu] * qa, pb[mu][nt][0], pbl[mu][nt][0]);
+            p_fragments_hc(p[nt][0][2 * mu + 1] * qb, p[nt][1][2 * mu + 1] * qb, pb[mu][nt][1], pbl[mu][nt][1]);
+          } else {
+            const float pa = ra < n_valid ? p[nt][0][2 * mu] * sva : 0.f;
+            const float pbb = ra + 1 < n_valid ? p[nt][0][2 * mu + 1] * svb : 0.f;
+            p_fragments(pa, pbb, pb[mu][nt][0], pb[mu][nt][1]);
+          }
           if constexpr (TR::Z) {
-            const float za = ra < n_valid ? p[nt][2 * mu] * zpa : 0.f;
-            const float zb = ra + 1 < n_valid ? p[nt][2 * mu + 1] * zpb : 0.f;
+            const float za = ra < n_valid ? p[nt][0][2 * mu] * zpa : 0.f;
+            const float zb = ra + 1 < n_valid ? p[nt][0][2 * mu + 1] * zpb : 0.f;
             ws.zo[bv][nt] += za + zb;
           }
         }
@@ -495,6 +541,10 @@ __device__ __forceinline__ void pv_packed(const Ctx<C>& cx, WarpState<C>& ws, co
           for (int nt = 0; nt < NT; ++nt) {
             mma16816(ws.o[2 * s][nt], x12[0], x12[1], x34[0], x34[1], pb[mu][nt][0], pb[mu][nt][1]);
             mma16816(ws.o[2 * s + 1][nt], x12[2], x12[3], x34[2], x34[3], pb[mu][nt][0], pb[mu][nt][1]);
+            if constexpr (C::HC) {
+              mma16816(ws.o[2 * s][nt], x12[0], x12[1], x34[0], x34[1], pbl[mu][nt][0], pbl[mu][nt][1]);
+              mma16816(ws.o[2 * s + 1][nt], x12[2], x12[3], x34[2], x34[3], pbl[mu][nt][0], pbl[mu][nt][1]);
+            }
           }
         }
       }
@@ -700,6 +750,12 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
               const uint2 q1 = qb[((2 * s + 1) * NT + nt) * 32 + lane];
               mma16816(acc[mu][nt], wa[0], wb[0], wa[1], wb[1], q0.x, q0.y);
               mma16816(acc[mu][nt], wa[2], wb[2], wa[3], wb[3], q1.x, q1.y);
+              if constexpr (C::HC) {  // the query's lo parts, same accumulator
+                const uint2 r0 = cx.qbl[((2 * s) * NT + nt) * 32 + lane];
+                const uint2 r1 = cx.qbl[((2 * s + 1) * NT + nt) * 32 + lane];
+                mma16816(acc[mu][nt], wa[0], wb[0], wa[1], wb[1], r0.x, r0.y);
+                mma16816(acc[mu][nt], wa[2], wb[2], wa[3], wb[3], r1.x, r1.y);
+              }
             }
           }
         }
@@ -831,12 +887,14 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   extern __shared__ __align__(16) uint8_t smem[];
   uint2* qb = reinterpret_cast<uint2*>(smem);  // [KC][NT][32 lanes]: this lane's B fragment (b0, b1)
   uint2* qh = qb + KC * NT * 32;               // [KC][NT][32 lanes]: query half pairs (per-channel K)
-  float4* qr = reinterpret_cast<float4*>(qh + KC * NT * 32);  // [KC][NT][32 lanes]: fp32 query (RoPE)
+  float4* qr = reinterpret_cast<float4*>(qh + (C::QH ? KC * NT * 32 : 0));  // [KC][NT][32]: fp32 query (RoPE)
   float* qz = reinterpret_cast<float*>(qr + (C::ROPE ? KC * NT * 32 : 0));  // [4 NT][D] (asymmetric K)
+  uint2* qbl = reinterpret_cast<uint2*>(qz + (C::Z ? 4 * NT * D : 0));     // [KC][NT][32 lanes]: lo (HC)
   uint8_t* stage_base = smem + C::QSM;
   __shared__ float qmax_s[kWarps];
   __shared__ uint32_t bad_page;
-  __shared__ uint64_t mbar[kWarps * kStages];
+  constexpr int kStages = C::STAGES;
+  __shared__ uint64_t mbar[kWarps * kMaxStages];
   __shared__ int is_last;
 
   if constexpr (STEP != 0) {
@@ -907,8 +965,10 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     for (int e = tid; e < KC * NT * 32; e += kThreadsMma) {
       const int ln = e & 31, nt = (e >> 5) % NT, kc = (e >> 5) / NT;
       const int c = 32 * (kc >> 1) + 8 * (ln & 3) + 2 * (kc & 1);
-      const int hh = 4 * nt + ((ln >> 2) >> 1);
-      const bool lo = ((ln >> 2) & 1) != 0;
+      // column ln / 4: head 8 nt + column (heads as columns, hi fragment here)
+      // or head 4 nt + column / 2, hi / lo by the column's parity
+      const int hh = C::HC ? 8 * nt + (ln >> 2) : 4 * nt + ((ln >> 2) >> 1);
+      const bool lo = !C::HC && ((ln >> 2) & 1) != 0;
       float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
       if (hh < g) {
         const float* q = qf + hh * D;
@@ -919,7 +979,10 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
       }
       qb[e] = make_uint2(pack_h2(split_part(v0, lo), split_part(v1, lo)),
                          pack_h2(split_part(v2, lo), split_part(v3, lo)));
-      qh[e] = make_uint2(pack_h2(v0, v1), pack_h2(v2, v3));
+      if constexpr (C::HC)
+        qbl[e] = make_uint2(pack_h2(split_part(v0, true), split_part(v1, true)),
+                            pack_h2(split_part(v2, true), split_part(v3, true)));
+      if constexpr (C::QH) qh[e] = make_uint2(pack_h2(v0, v1), pack_h2(v2, v3));
       if constexpr (C::ROPE) qr[e] = make_float4(v0, v1, v2, v3);
     }
     if constexpr (C::Z) {
@@ -940,6 +1003,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   cx.lo_part = lo_part;
   cx.lo_mask = lo_mask;
   cx.qb = qb;
+  cx.qbl = qbl;
   cx.qh = qh;
   cx.qr = qr;
   cx.qz = qz;
@@ -966,9 +1030,12 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
 #pragma unroll
       for (int e = 0; e < 4; ++e) ws.o[i][nt][e] = 0.f;
 #pragma unroll
+  for (int i = 0; i < NT * C::J; ++i) {
+    ws.m[i] = -INFINITY;
+    ws.l[i] = 0.f;
+  }
+#pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    ws.m[nt] = -INFINITY;
-    ws.l[nt] = 0.f;
 #pragma unroll
     for (int s = 0; s < (C::Z ? C::NS : 1); ++s) ws.zo[s][nt] = 0.f;
   }
@@ -1053,7 +1120,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     for (int mu = 0; mu < 2; ++mu)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) S[mu][nt][0] = S[mu][nt][1] = S[mu][nt][2] = S[mu][nt][3] = 0.f;
-    float p[NT][4];
+    float p[NT][C::J][4];
 
     if (tile < n_c + n_m) {
       // ---------------- packed group from shared memory ----------------
@@ -1141,19 +1208,31 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
               const uint2 q1 = qb[((2 * s + 1) * NT + nt) * 32 + lane];
               mma16816(S[mu][nt], a0, b0, a1, b1, q0.x, q0.y);
               mma16816(S[mu][nt], a2, b2, a3, b3, q1.x, q1.y);
+              if constexpr (C::HC) {
+                const uint2 r0 = cx.qbl[((2 * s) * NT + nt) * 32 + lane];
+                const uint2 r1 = cx.qbl[((2 * s + 1) * NT + nt) * 32 + lane];
+                mma16816(S[mu][nt], a0, b0, a1, b1, r0.x, r0.y);
+                mma16816(S[mu][nt], a2, b2, a3, b3, r1.x, r1.y);
+              }
             }
           }
         }
       }
       online_softmax<C>(ws, S, n_valid, gq, qscale, p);
-      uint32_t pb[2][NT][2];
+      uint32_t pb[2][NT][2], pbl[C::HC ? 2 : 1][NT][2];
 #pragma unroll
       for (int mu = 0; mu < 2; ++mu) {
         const int ra = 4 * gq + 2 * mu;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          p_fragments(ra < n_valid ? p[nt][2 * mu] : 0.f, ra + 1 < n_valid ? p[nt][2 * mu + 1] : 0.f,
-                      pb[mu][nt][0], pb[mu][nt][1]);
+        for (int nt = 0; nt < NT; ++nt) {
+          const float va = ra < n_valid ? 1.f : 0.f, vb = ra + 1 < n_valid ? 1.f : 0.f;
+          if constexpr (C::HC) {
+            p_fragments_hc(p[nt][0][2 * mu] * va, p[nt][1][2 * mu] * va, pb[mu][nt][0], pbl[mu][nt][0]);
+            p_fragments_hc(p[nt][0][2 * mu + 1] * vb, p[nt][1][2 * mu + 1] * vb, pb[mu][nt][1], pbl[mu][nt][1]);
+          } else {
+            p_fragments(p[nt][0][2 * mu] * va, p[nt][0][2 * mu + 1] * vb, pb[mu][nt][0], pb[mu][nt][1]);
+          }
+        }
       }
 #pragma unroll
       for (int mu = 0; mu < 2; ++mu) {
@@ -1179,6 +1258,10 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
           for (int nt = 0; nt < NT; ++nt) {
             mma16816(ws.o[2 * s][nt], x0, x1, y0, y1, pb[mu][nt][0], pb[mu][nt][1]);
             mma16816(ws.o[2 * s + 1][nt], x2, x3, y2, y3, pb[mu][nt][0], pb[mu][nt][1]);
+            if constexpr (C::HC) {
+              mma16816(ws.o[2 * s][nt], x0, x1, y0, y1, pbl[mu][nt][0], pbl[mu][nt][1]);
+              mma16816(ws.o[2 * s + 1][nt], x2, x3, y2, y3, pbl[mu][nt][0], pbl[mu][nt][1]);
+            }
           }
         }
       }
@@ -1206,10 +1289,6 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   float* obuf = wo + kWarps * kMaxGqa * D;            // [g][D]
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    float l = ws.l[nt];
-    l += __shfl_xor_sync(0xffffffffu, l, 4);
-    l += __shfl_xor_sync(0xffffffffu, l, 8);
-    l += __shfl_xor_sync(0xffffffffu, l, 16);
     float zo[C::Z ? C::NS : 1] = {};  // zero-point part of the output per 32-channel block
     if constexpr (C::Z) {
 #pragma unroll
@@ -1221,22 +1300,34 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
         zo[s] = z;
       }
     }
-    const int hh = 4 * nt + tq;
-    if (hh < g) {
-      if (gq == 0) {
-        wm[warp * kMaxGqa + hh] = ws.m[nt];
-        wl[warp * kMaxGqa + hh] = l;
-      }
-      float* orow = wo + (warp * kMaxGqa + hh) * D;
 #pragma unroll
-      for (int s = 0; s < C::NS; ++s)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int ch = 32 * s + 4 * gq + 2 * e;
-          const float zadd = C::Z ? zo[C::Z ? s : 0] : 0.f;
-          orow[ch] = ws.o[2 * s + e][nt][0] + ws.o[2 * s + e][nt][1] + zadd;
-          orow[ch + 1] = ws.o[2 * s + e][nt][2] + ws.o[2 * s + e][nt][3] + zadd;
+    for (int j = 0; j < C::J; ++j) {
+      float l = ws.l[nt * C::J + j];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      const int hh = C::HC ? 8 * nt + 2 * tq + j : 4 * nt + tq;
+      if (hh < g) {
+        if (gq == 0) {
+          wm[warp * kMaxGqa + hh] = ws.m[nt * C::J + j];
+          wl[warp * kMaxGqa + hh] = l;
         }
+        float* orow = wo + (warp * kMaxGqa + hh) * D;
+#pragma unroll
+        for (int s = 0; s < C::NS; ++s)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int ch = 32 * s + 4 * gq + 2 * e;
+            if constexpr (C::HC) {  // column 2tq + j of rows gq, gq + 8
+              orow[ch] = ws.o[2 * s + e][nt][j];
+              orow[ch + 1] = ws.o[2 * s + e][nt][2 + j];
+            } else {  // hi + lo columns
+              const float zadd = C::Z ? zo[C::Z ? s : 0] : 0.f;
+              orow[ch] = ws.o[2 * s + e][nt][0] + ws.o[2 * s + e][nt][1] + zadd;
+              orow[ch + 1] = ws.o[2 * s + e][nt][2] + ws.o[2 * s + e][nt][3] + zadd;
+            }
+          }
+      }
     }
   }
   __syncthreads();

@@ -20,9 +20,9 @@ bool step_fused_d256(const DecodeArgs& a, cudaStream_t st, bool dry, cudaError_t
   using S2 = std::integral_constant<int, 2>;  // rotated formats
   if (k.zp || lo.tiered || rope || lo.ring) return false;
   if (fmt_is(k, 4, 128, TOK) && fmt_is(v, 4, 128, TOK))
-    return run(Cfg<256, 2, T_<256, KF_T4, 128, VF_T4, 128>, T_<256, KF_T4, 128, VF_T4, 128>, false, false>{}, S2{});
+    return run(Cfg<256, 1, T_<256, KF_T4, 128, VF_T4, 128>, T_<256, KF_T4, 128, VF_T4, 128>, false, false, true>{}, S2{});
   if (fmt_is(k, 3, 128, TOK) && fmt_is(v, 3, 128, TOK))
-    return run(Cfg<256, 2, T_<256, KF_T3, 128, VF_T3, 128>, T_<256, KF_T3, 128, VF_T3, 128>, false, false>{}, S2{});
+    return run(Cfg<256, 1, T_<256, KF_T3, 128, VF_T3, 128>, T_<256, KF_T3, 128, VF_T3, 128>, false, false, true>{}, S2{});
   return false;
 }
 
