@@ -215,14 +215,6 @@ __device__ __forceinline__ uint32_t ld_u24(const uint8_t* p) {
   return __funnelshift_r(w[0], w[1], (uint32_t)(ad & 3) * 8) & 0xFFFFFFu;
 }
 
-// Two codes of B bits at bit B*j of each 16-bit half of x, as an exact fp16
-// pair (code with the storage bias removed).
-template <int B>
-__device__ __forceinline__ uint32_t code_pair(uint32_t x, int j) {
-  if constexpr (B == 4) return hsub2u(((x >> (4 * j)) & 0x000F000Fu) | 0x64006400u, 0x64086408u);
-  if constexpr (B == 3) return hsub2u(((x >> (3 * j)) & 0x00070007u) | 0x64006400u, 0x64046404u);
-  return hsub2u(((x >> (2 * j)) & 0x00030003u) | 0x64006400u, 0x64026402u);
-}
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
@@ -232,6 +224,31 @@ __device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
+}
+
+// fp16 bits of -n for an integer 1 <= n < 2048 (exact).
+__host__ __device__ constexpr uint32_t neg_f16_bits(int n) {
+  int e = 0;
+  while ((2 << e) <= n) ++e;  // 2^e <= n < 2^(e+1)
+  return 0x8000u | (uint32_t)(e + 15) << 10 | (uint32_t)((n - (1 << e)) << (10 - e));
+}
+
+// Two codes of B bits at bit B*j of each 16-bit half of x, as an exact fp16
+// pair (code with the storage bias beta = 2^(B-1) removed).  A field inside
+// the fp16 mantissa (bits 0..9) is masked in place: 1024 + c 2^(Bj), times
+// 2^-(Bj), minus 2^(10 - Bj) + beta, is c - beta exactly (one fma); a field
+// reaching bit 10 is shifted down first.
+template <int B>
+__device__ __forceinline__ uint32_t code_pair(uint32_t x, int j) {
+  constexpr uint32_t m = (1u << B) - 1, beta = 1u << (B - 1);
+  if (j == 0) return hsub2u((x & (m * 0x00010001u)) | 0x64006400u, (0x6400u + beta) * 0x00010001u);
+  if (B * j + B <= 10) {
+    const int sh = B * j;
+    const uint32_t scale = (uint32_t)(15 - sh) << 10;  // 2^-sh
+    const uint32_t off = neg_f16_bits((1 << (10 - sh)) + (int)beta);
+    return hfma2u((x & ((m << sh) * 0x00010001u)) | 0x64006400u, scale * 0x00010001u, off * 0x00010001u);
+  }
+  return hsub2u(((x >> (B * j)) & (m * 0x00010001u)) | 0x64006400u, (0x6400u + beta) * 0x00010001u);
 }
 
 // Eight 4-bit codes, four per 16-bit half of x (nibble j of each half), as
