@@ -276,7 +276,7 @@ __device__ __forceinline__ void block_copy_out(uint8_t* dst, const uint8_t* src,
 constexpr int kTokItem = 128;
 
 template <int NC, int DT, int B, int CB, int which, bool Z>
-__global__ void __launch_bounds__(kAppendThreads) quant_token32_kernel(AppendArgs a) {
+__global__ void __launch_bounds__(kAppendThreads, 5) quant_token32_kernel(AppendArgs a) {
   constexpr int D = 128 * NC, SPR = D / 32, HDR = Z ? 4 : 2;
   constexpr int BB = HDR + 4 * B, ROW = SPR * BB;
   constexpr int CBB = CB ? HDR + 4 * CB : 0, CROW = SPR * CBB;
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kAppendThreads) quant_token32_kernel(AppendArg
 constexpr int kGroupSteps = 2;
 
 template <int NC, int DT, int B, int CB, int which, bool Z>
-__global__ void __launch_bounds__(kAppendThreads, 4) quant_channel32_kernel(AppendArgs a) {
+__global__ void __launch_bounds__(kAppendThreads, 5) quant_channel32_kernel(AppendArgs a) {
   constexpr int D = 128 * NC, PAIRS = D / 2, GPC = kAppendThreads / PAIRS, NG = GPC * kGroupSteps;
   constexpr int HDR = Z ? 4 : 2;
   constexpr int BB = HDR + 4 * B, GROW = D * BB;
