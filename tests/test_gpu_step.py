@@ -107,3 +107,40 @@ def test_step_on_an_empty_sequence():
     want = v_new.float().repeat_interleave(g, dim=2)
     assert torch.equal(out, want)
     assert cache.device_status() == 0
+
+
+def test_step_errors_are_refused_or_flagged():
+    """Bad arguments are refused on the host; a step past capacity and a new
+    token on a bad page set status bits and write nothing out of range."""
+    w = W.make("llama2_7b_kivi4").scaled(L=1, lengths=[40], extra=8)
+    cfg = w.cfg
+    cache, seq, _, _ = appended_cache(w, with_oracle=False)
+    q = W.queries(w, 1, "cuda")
+    out = torch.empty((1, 1, cfg.H_q, cfg.D), dtype=torch.float32, device="cuda")
+    kn = torch.zeros((1, 1, cfg.H_kv, cfg.D), dtype=torch.float16, device="cuda")
+    with pytest.raises(K.KvqError):
+        cache.decode_step(0, 1, None, kn, q, seq, out)
+    flat = torch.zeros(1 + cfg.H_kv * cfg.D, dtype=torch.float16, device="cuda")
+    with pytest.raises(K.KvqError):  # 2-byte aligned rows
+        cache.decode_step(0, 1, flat[1:].view(1, 1, cfg.H_kv, cfg.D), kn, q, seq, out)
+    with pytest.raises(K.KvqError):
+        cache.decode_step(0, 2, kn, kn, q, seq, out)  # layers beyond L
+    # past capacity: flagged, the cache unchanged
+    full = torch.full((1,), cfg.max_T, dtype=torch.int32, device="cuda")
+    before = cache.buffer_numpy()
+    cache.decode_step(0, 1, kn, kn, q, full, out)
+    torch.cuda.synchronize()
+    assert cache.device_status() != 0
+    after = cache.buffer_numpy()
+    assert all(np.array_equal(before[n], after[n]) for n in before)
+    # paged layout: the page of sequence 0's new token (position 32, page 2) is out of range
+    w2 = W.make("gqa8b_hadamard4_paged").scaled(L=1, lengths=[32, 16], extra=32)
+    c2 = w2.cfg
+    cache2, seq2, _, _ = appended_cache(w2, with_oracle=False)
+    cache2.block_table[0, 2] = c2.n_pages + 3
+    kn2 = torch.zeros((1, 2, c2.H_kv, c2.D), dtype=torch.float16, device="cuda")
+    q2 = W.queries(w2, 1, "cuda")
+    out2 = torch.empty((1, 2, c2.H_q, c2.D), dtype=torch.float32, device="cuda")
+    cache2.decode_step(0, 1, kn2, kn2, q2, seq2, out2)
+    torch.cuda.synchronize()
+    assert cache2.device_status() & K.DEV_PAGE
