@@ -130,40 +130,37 @@ __device__ __forceinline__ void block32(float (&v)[32], float m, uint8_t* dst, f
 // the format's op order: with mn, mx the block's minimum (a zero as +0) and
 // maximum, s16 = fp16(min((mx - mn) / (2^B - 1), 65504)), z16 = fp16(mn
 // clipped to +-65504), code = clamp(rint((x - z) / s), 0, 2^B - 1), 0 when
-// s = 0.  The quotient is first taken as q = RN(RN(x - z) RN(1/s)), within
-// two ulps of RN((x - z) / s); the rounding to an integer can differ only when
-// q lies that close to a half step, and below 2^B + 1 (the only range where
-// a code is decided) two ulps are at most 2^-18.  A value whose q lies within
-// 2^-16 of a half step is therefore recomputed with the IEEE divide.
-// Clamping the magic-number sum to [magic, magic + 2^B - 1] is the clamp of
-// the rounded quotient.
-constexpr float kNearHalf = 0.5f - 1.52587890625e-05f;  // 1/2 - 2^-16
+// s = 0.  The quotient RN(d / s) of d = RN(x - z) is taken with Markstein's
+// correction step (as div_by_scale); with rcp = 0 when s = 0 it gives 0.
+// The code is a nondecreasing function of x, so when the codes of the
+// block's minimum and maximum lie in [0, 2^B - 1] no value needs the clamp;
+// any other block (a saturated or nearly degenerate scale, an infinity) is
+// quantized by the serial form, quant_zp32, with the IEEE divide and the clamp.
+template <int B>
+__device__ __forceinline__ float zp_magic_code(float x, float sf, float zf, float rcp) {
+  return __fadd_rn(div_by_scale(__fsub_rn(x, zf), sf, rcp), kRoundMagic);
+}
 
 template <int B>
 __device__ __forceinline__ void codes_zp(const float (&v)[32], float sf, float zf, float rcp, uint32_t (&w)[B],
                                          float* dq) {
-  constexpr float top = kRoundMagic + (float)((1 << B) - 1);
   uint32_t corr[B];
 #pragma unroll
   for (int k = 0; k < B; ++k) w[k] = corr[k] = 0;
-  // x - z, the quotient, the rounding and the half-step distance on pairs of
-  // values (each half rounded like the scalar operation)
-  const uint64_t Z2 = pk2(zf, zf), R2 = pk2(rcp, rcp), M2 = pk2(kRoundMagic, kRoundMagic);
+  // x - z, the quotient and the rounding on pairs of values (each half
+  // rounded like the scalar operation)
+  const uint64_t Z2 = pk2(zf, zf), R2 = pk2(rcp, rcp), NS2 = pk2(-sf, -sf), M2 = pk2(kRoundMagic, kRoundMagic);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const uint64_t Dd = sub2(pk2(v[2 * i], v[2 * i + 1]), Z2);
-    const uint64_t Q = mul2(Dd, R2);
-    const uint64_t R0 = add2(Q, M2);
-    float d[2], r0[2], df[2];
-    upk2(Dd, d[0], d[1]);
+    const uint64_t Q0 = mul2(Dd, R2);
+    const uint64_t R0 = add2(fma2(fma2(Q0, NS2, Dd), R2, Q0), M2);
+    float r0[2];
     upk2(R0, r0[0], r0[1]);
-    upk2(sub2(Q, sub2(R0, M2)), df[0], df[1]);
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int j = 2 * i + c;
-      float rc = r0[c];
-      if (fabsf(df[c]) > kNearHalf) rc = __fadd_rn(__fdiv_rn(d[c], sf), kRoundMagic);
-      const float r = fminf(fmaxf(rc, kRoundMagic), top);
+      const float r = r0[c];
       if (dq) dq[j] = __fadd_rn(__fmul_rn(__fsub_rn(r, kRoundMagic), sf), zf);
       const int bit = B * j, k = bit / 32, sh = bit % 32;
       w[k] += __float_as_uint(r) << sh;
@@ -182,6 +179,11 @@ __device__ __forceinline__ void block32_zp(const float (&v)[32], float mn, float
   const __half z16 = __float2half_rn(fminf(fmaxf(mn, -65504.0f), 65504.0f));
   const float sf = __half2float(s16), zf = __half2float(z16);
   const float rcp = sf == 0.f ? 0.f : __frcp_rn(sf);
+  if (!(zp_magic_code<B>(mn, sf, zf, rcp) >= kRoundMagic &&
+        zp_magic_code<B>(mx, sf, zf, rcp) <= kRoundMagic + (float)qlev)) {
+    quant_zp32(v, B, dst, dq);
+    return;
+  }
   uint32_t w[B];
   codes_zp<B>(v, sf, zf, rcp, w, dq);
   if (!dst) return;
@@ -266,6 +268,71 @@ __device__ __forceinline__ void block_copy_out(uint8_t* dst, const uint8_t* src,
   } else {
     for (int e = threadIdx.x; e < bytes / 4; e += blockDim.x)
       reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(src)[e];
+  }
+}
+
+// Two asymmetric blocks at once: channels c and c + 1 of 32 tokens, raw[j]
+// holding token j's two 16-bit values.  The codes of both blocks are taken on
+// f32x2 pairs (one lane per channel) as codes_zp does, consuming raw as they
+// go; when either block needs the clamp, both go through the serial form.
+template <int DT, int B>
+__device__ __forceinline__ void block32_zp_x2(const uint32_t (&raw)[32], float2 mn, float2 mx, uint8_t* dst0,
+                                              uint8_t* dst1) {
+  constexpr int qlev = (1 << B) - 1;
+  float sf[2], zf[2], rcp[2];
+  __half s16[2], z16[2];
+  bool ok = true;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const float lo = __fadd_rn(c ? mn.y : mn.x, 0.0f), hi = c ? mx.y : mx.x;
+    s16[c] = __float2half_rn(fminf(__fdiv_rn(__fsub_rn(hi, lo), (float)qlev), 65504.0f));
+    z16[c] = __float2half_rn(fminf(fmaxf(lo, -65504.0f), 65504.0f));
+    sf[c] = __half2float(s16[c]);
+    zf[c] = __half2float(z16[c]);
+    rcp[c] = sf[c] == 0.f ? 0.f : __frcp_rn(sf[c]);
+    ok = ok && zp_magic_code<B>(lo, sf[c], zf[c], rcp[c]) >= kRoundMagic &&
+         zp_magic_code<B>(hi, sf[c], zf[c], rcp[c]) <= kRoundMagic + (float)qlev;
+  }
+  if (!ok) {
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+      float t[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) t[j] = in_to_f32_t<DT>(c ? (raw[j] >> 16) : (raw[j] & 0xFFFFu));
+      quant_zp32_mem(t, B, c ? dst1 : dst0, nullptr);
+    }
+    return;
+  }
+  const uint64_t Z2 = pk2(zf[0], zf[1]), R2 = pk2(rcp[0], rcp[1]), NS2 = pk2(-sf[0], -sf[1]),
+                 M2 = pk2(kRoundMagic, kRoundMagic);
+  uint32_t w0[B], w1[B], corr[B];
+#pragma unroll
+  for (int k = 0; k < B; ++k) w0[k] = w1[k] = corr[k] = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float2 x = raw_pair_to_f32<DT>(raw[j]);
+    const uint64_t Dd = sub2(pk2(x.x, x.y), Z2);
+    const uint64_t Q0 = mul2(Dd, R2);
+    float r0, r1;
+    upk2(add2(fma2(fma2(Q0, NS2, Dd), R2, Q0), M2), r0, r1);
+    const int bit = B * j, k = bit / 32, sh = bit % 32;
+    w0[k] += __float_as_uint(r0) << sh;
+    w1[k] += __float_as_uint(r1) << sh;
+    corr[k] += kRoundMagicBits << sh;
+  }
+  uint16_t* p0 = reinterpret_cast<uint16_t*>(dst0);
+  uint16_t* p1 = reinterpret_cast<uint16_t*>(dst1);
+  p0[0] = __half_as_ushort(s16[0]);
+  p0[1] = __half_as_ushort(z16[0]);
+  p1[0] = __half_as_ushort(s16[1]);
+  p1[1] = __half_as_ushort(z16[1]);
+#pragma unroll
+  for (int k = 0; k < B; ++k) {
+    const uint32_t a = w0[k] - corr[k], b = w1[k] - corr[k];
+    p0[2 + 2 * k] = (uint16_t)a;
+    p0[3 + 2 * k] = (uint16_t)(a >> 16);
+    p1[2 + 2 * k] = (uint16_t)b;
+    p1[3 + 2 * k] = (uint16_t)(b >> 16);
   }
 }
 
@@ -432,6 +499,12 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_channel32_kernel(Appe
       }
       mn2 = raw_pair_to_f32<DT>(lo2);
       mx2 = raw_pair_to_f32<DT>(hi2);
+    }
+    if constexpr (Z) {
+      if (!to_cold) {
+        block32_zp_x2<DT, B>(raw, mn2, mx2, out + gi * SLOT + 2 * cp * BB, out + gi * SLOT + (2 * cp + 1) * BB);
+        continue;
+      }
     }
 #pragma unroll
     for (int hc = 0; hc < 2; ++hc) {

@@ -37,6 +37,7 @@ namespace kvq {
 namespace {
 
 constexpr int kRotItem = 128;  // tokens per CTA
+constexpr float kNearHalf = 0.5f - 1.52587890625e-05f;  // 1/2 - 2^-16
 
 // Codes of 32 values as a 32*B-bit little-endian stream of biased codes.
 // Fast: q = RN(v[j] f[j]) (f[j] the value's factor over the scale).  EXACT:

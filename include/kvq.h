@@ -224,7 +224,9 @@ KVQ_API kvq_status kvq_workspace_init(const kvq_config* cfg, void* workspace, si
  *  total_new, max_new: host copies of cu_new[batch] and of the largest
  *            per-sequence count (they size the grids).
  * Window tokens move into the quantized tiers by whole groups; bulk append
- * and token-by-token append give the same cache. */
+ * and token-by-token append give the same cache.  Inputs are finite or
+ * infinite numbers; a block holding a NaN gets unspecified codes (and a NaN
+ * or unspecified scale), and no other block is affected. */
 KVQ_API kvq_status kvq_append(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0, int32_t n_layers,
                       const void* k, const void* v, const int32_t* cu_new, const int32_t* seq_lens,
                       int32_t total_new, int32_t max_new, void* workspace, size_t ws_bytes, void* stream);

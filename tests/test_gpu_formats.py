@@ -12,7 +12,12 @@ of input:
 * seeded N(0, 1) values with a few large channels.
 
 * for the asymmetric (scale + zero point) blocks, exact half steps between
-  each block's minimum and maximum with a power-of-two range / (2^b - 1).
+  each block's minimum and maximum with a power-of-two range / (2^b - 1);
+* for the asymmetric blocks also blocks whose unclamped codes leave
+  [0, 2^b - 1] (the kernels quantize those with the clamp): ranges of a few
+  steps of 2^-24 (fp16 scales that round down), bf16 values beyond the fp16
+  zero point's range, and single infinities.  The test checks on the CPU that
+  such blocks occur.
 
 Each case appends in two calls (a bulk prefix, then a ragged remainder) and
 compares every packed byte with the oracle.
@@ -64,9 +69,27 @@ LENGTHS = [301, 160, 33]
 PREFIX = [200, 64, 0]
 
 
-def _inputs(kind, n_tok, H, D, bits, gen, zp=False):
+def _inputs(kind, n_tok, H, D, bits, gen, zp=False, bf16=False):
     """[n_tok, H, D] input values (float64) for one tensor; token index is the
     position within the sequence."""
+    if kind == "clamp" and zp:
+        # heads in turn: tiny integer steps, large magnitudes (with a few
+        # infinities), N(0, 1); W is constant over every block of either axis
+        t = torch.arange(n_tok).view(-1, 1, 1)
+        c = torch.arange(D).view(1, 1, -1)
+        hh = torch.arange(H).view(1, -1, 1)
+        W = (16 + ((t // 32) * 5 + (c // 32) * 11 + hh * 3) % 40).double()
+        k = torch.floor(torch.rand((n_tok, H, D), generator=gen, dtype=torch.float64) * (W + 1))
+        sign = torch.where(((t // 32) + (c // 32) + hh) % 2 == 0, 1.0, -1.0).double()
+        tiny = (k - 7) * 2.0 ** -24
+        big = sign * ((2.0 ** 16 + k * 512) if bf16 else (61440 + k * 32))
+        inf = torch.zeros((n_tok, H, D), dtype=torch.float64)
+        inf = torch.where(((t % 97) == 5) & ((c % 53) == 1), float("inf"), inf)
+        inf = torch.where(((t % 89) == 7) & ((c % 59) == 2), float("-inf"), inf)
+        big = torch.where(inf != 0, inf, big)
+        mode = (hh % 3).expand(n_tok, H, D)
+        rnd = torch.randn((n_tok, H, D), generator=gen, dtype=torch.float64)
+        return torch.where(mode == 0, tiny, torch.where(mode == 1, big, rnd))
     if kind == "ties" and zp:
         # asymmetric ties: every block holds its minimum -off*s (where token
         # and channel agree mod 32, shifted by one) and its maximum
@@ -104,11 +127,33 @@ def _case_tensors(kind, cfg, lengths, which, gen):
     bits = (cfg.k_fmt if which == 0 else cfg.v_fmt).bits
     zp = bool(cfg.flags & (K.ZP_K if which == 0 else K.ZP_V))
     dt = torch.float16 if cfg.in_dtype == K.DT_F16 else torch.bfloat16
-    return [_inputs(kind, T, cfg.H_kv, cfg.D, bits, gen, zp).to(dt) for T in lengths]
+    return [_inputs(kind, T, cfg.H_kv, cfg.D, bits, gen, zp, dt == torch.bfloat16).to(dt) for T in lengths]
 
 
-@pytest.mark.parametrize("kind", ["ties", "random"])
-@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def _blocks_needing_clamp(x, fmt):
+    """How many full 32-value blocks of x ([T, H, D] 16-bit) along the
+    format's axis have an unclamped code outside [0, 2^b - 1] (numpy fp32, the
+    quantizer's op order; a coverage count, not a parity check)."""
+    a = x.float().numpy()
+    if fmt.axis == CH:
+        n = a.shape[0] // 32 * 32
+        a = a[:n].reshape(n // 32, 32, *a.shape[1:]).transpose(0, 2, 3, 1)
+    else:
+        a = a.reshape(*a.shape[:-1], a.shape[-1] // 32, 32)
+    qlev = np.float32((1 << fmt.bits) - 1)
+    with np.errstate(all="ignore"):
+        mn = a.min(-1) + np.float32(0.0)
+        s = np.minimum((a.max(-1) - mn) / qlev, np.float32(65504)).astype(np.float16).astype(np.float32)
+        z = np.clip(mn, -65504, 65504).astype(np.float16).astype(np.float32)
+        r = np.rint((a - z[..., None]) / s[..., None])
+    out = ((r < 0) | (r > qlev)) & (s[..., None] != 0)
+    return int(out.any(-1).sum())
+
+
+KIND_CASES = [(c, k) for c in CASES for k in ("ties", "random")] + [(c, "clamp") for c in CASES if len(c) > 9]
+
+
+@pytest.mark.parametrize("case,kind", KIND_CASES, ids=[f"{c[0]}-{k}" for c, k in KIND_CASES])
 def test_append_bytes_match_oracle(case, kind):
     name, D, dtype, kf, vf, kc, vc, hot, R = case[:9]
     flags = case[9] if len(case) > 9 else 0
@@ -120,6 +165,10 @@ def test_append_bytes_match_oracle(case, kind):
     gen = torch.Generator().manual_seed(zlib.crc32(f"{name}/{kind}".encode()))
     ks = _case_tensors(kind, cfg, LENGTHS, 0, gen)
     vs = _case_tensors(kind, cfg, LENGTHS, 1, gen)
+    if kind == "clamp":
+        for which, xs, f in ((0, ks, kf), (1, vs, vf)):
+            if flags & (K.ZP_K if which == 0 else K.ZP_V):
+                assert sum(_blocks_needing_clamp(x, f) for x in xs) > 0, (name, which)
     cache = K.KVCache(cfg, "cuda")
     ref = O.new_buffers(oc)
     seq_lens = torch.zeros(cfg.batch, dtype=torch.int32, device="cuda")
@@ -146,7 +195,7 @@ def test_append_bytes_match_oracle(case, kind):
             total, diff, maxd, sdiff = codes_differ(oc, {n: got}, {n: ref[n]}) \
                 if not n.endswith("resid") else (0, -1, -1, -1)
             pytest.fail(f"{name}/{kind} {n}: bytes differ (codes {diff}/{total}, max |dc| {maxd}, scales {sdiff})")
-    if flags:  # asymmetric blocks: decode over the GPU's bytes against fp64 attention
+    if flags and kind != "clamp":  # asymmetric blocks: decode over the GPU's bytes against fp64 attention
         dtq = torch.float16 if dtype == K.DT_F16 else torch.bfloat16
         q = torch.randn((1, cfg.batch, cfg.H_q, D), generator=gen).to(dtq).cuda()
         out = torch.full((1, cfg.batch, cfg.H_q, D), float("nan"), dtype=torch.float32, device="cuda")
