@@ -28,10 +28,15 @@
 // TBQ4 blocks (same 66 B: fp16 L2 norm, 4-bit indices into the 16-entry
 // Lloyd-Max table; trefon.com, same section): a lane's 32 consecutive values
 // are exactly one of the norm's partial sums p_k (index order), S = (p0 + p1)
-// + (p2 + p3) by two shuffles, u = y / norm with the IEEE divide, and the
-// index counts the table midpoints strictly below u (a 4-step search over the
-// 15 ascending midpoints in shared memory).
+// + (p2 + p3) by two shuffles, u = RN(y / norm), and the index counts the table
+// midpoints strictly below u by one lookup in a binned table
+// (tbq4_bins.cuh).  The quotient comes from Markstein's correction step on
+// fp32x2 pairs, exact when the norm is 0 (u = 0: rcp = 0 gives +-0) or below
+// 65504 (every y finite) and every |y| is at least 2^-100 (the remainder
+// y - q0 norm is then exact and the quotient normal); a lane outside those
+// bounds divides with the IEEE divide.
 #include "append_fast.cuh"
+#include "tbq4_bins.cuh"
 
 namespace kvq {
 namespace {
@@ -142,7 +147,7 @@ __global__ void __launch_bounds__(kAppendThreads) quant_rot128_kernel(AppendArgs
   static_assert(kAppendThreads == 128 && WTOK % TPS == 0, "tile geometry");
   __shared__ __align__(16) uint8_t out[kRotItem * ROW];
   __shared__ uint32_t page_bad;
-  __shared__ float cbt[16];  // TBQ4 midpoints
+  __shared__ float2 tbin[2 * kTbqBins];  // TBQ4 lookup: (midpoint inside, count below) per bin
   const Layout& lo = a.lo;
   const int li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B, h = blockIdx.y;
   const int layer = a.layer0 + li;
@@ -154,8 +159,17 @@ __global__ void __launch_bounds__(kAppendThreads) quant_rot128_kernel(AppendArgs
   if (u0 >= u1) return;
   const int n_tok = u1 - u0;
   if (threadIdx.x == 0) page_bad = 0;
-  if (TQ && threadIdx.x < 15) cbt[threadIdx.x] = a.lo.cbt[threadIdx.x];
-  if (TQ) __syncthreads();
+  int k0 = 0;
+  if constexpr (TQ) {
+    k0 = tbq4_bin_k0(lo.cbt);
+    if (threadIdx.x < 2 * kTbqBins) {
+      float th;
+      int base;
+      tbq4_bin_entry(lo.cbt, k0, threadIdx.x, &th, &base);
+      tbin[threadIdx.x] = make_float2(th, __int_as_float(base));
+    }
+    __syncthreads();
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int a4 = lane & 3, slot = lane >> 2;
   const int tok_in_step = slot / NC, chunk = slot % NC;
@@ -243,32 +257,55 @@ __global__ void __launch_bounds__(kAppendThreads) quant_rot128_kernel(AppendArgs
       }
     }
     if constexpr (TQ) {
-      float y[32];  // the format's values d2 RN(t c), signed
-      float ss = 0.f;
+      // y = d2 RN(t c) on pairs; the lane's partial sum of squares in index
+      // order; the smallest |y| (the bound of the fast quotient)
+      const uint64_t C2 = pk2(hadamard_scale(), hadamard_scale());
+      uint64_t Y[16];
+      float ss = 0.f, ymin = INFINITY;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        float lo, hi;
-        upk2(P[i], lo, hi);
-        y[2 * i] = __uint_as_float(__float_as_uint(__fmul_rn(lo, hadamard_scale())) ^ (((d2w >> (2 * i)) & 1u) << 31));
-        y[2 * i + 1] =
-            __uint_as_float(__float_as_uint(__fmul_rn(hi, hadamard_scale())) ^ (((d2w >> (2 * i + 1)) & 1u) << 31));
-        ss = __fadd_rn(ss, __fmul_rn(y[2 * i], y[2 * i]));
-        ss = __fadd_rn(ss, __fmul_rn(y[2 * i + 1], y[2 * i + 1]));
+        const uint64_t V = mul2(P[i], C2);
+        float lo, hi, q0, q1;
+        upk2(V, lo, hi);
+        upk2(mul2(V, V), q0, q1);
+        ss = __fadd_rn(__fadd_rn(ss, q0), q1);
+        ymin = fminf(ymin, fminf(fabsf(lo), fabsf(hi)));
+        lo = __uint_as_float(__float_as_uint(lo) ^ ((d2w << (31 - 2 * i)) & 0x80000000u));
+        hi = __uint_as_float(__float_as_uint(hi) ^ ((d2w << (30 - 2 * i)) & 0x80000000u));
+        Y[i] = pk2(lo, hi);
       }
       ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 1));
       ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 2));
       if (j >= n_tok) continue;  // the shuffles above are done
       const __half n16 = __float2half_rn(fminf(__fsqrt_rn(ss), 65504.0f));
       const float nf = __half2float(n16);
+      // magnitude clamps of the lookup: keys k0 and k0 + kTbqBins - 1
+      const float alo = __uint_as_float((uint32_t)k0 << 20), ahi = __uint_as_float((uint32_t)(k0 + kTbqBins - 1) << 20);
+      auto index = [&](float u) -> uint32_t {
+        const uint32_t ub = __float_as_uint(u);
+        const int key = (int)(__float_as_uint(fminf(fmaxf(fabsf(u), alo), ahi)) >> 20);
+        const float2 e = tbin[key - k0 + (int)(ub >> 31) * kTbqBins];
+        return (uint32_t)__float_as_int(e.y) + (u > e.x ? 1u : 0u);
+      };
       uint32_t w[4] = {0, 0, 0, 0};
+      if (nf == 0.f || (nf < 65504.f && ymin >= 0x1p-100f)) {
+        const float r = nf == 0.f ? 0.f : __frcp_rn(nf);
+        const uint64_t R2 = pk2(r, r), NN2 = pk2(-nf, -nf);
 #pragma unroll
-      for (int b = 0; b < 32; ++b) {
-        const float u = nf > 0.f ? __fdiv_rn(y[b], nf) : 0.f;
-        int k = u > cbt[7] ? 8 : 0;
-        k += u > cbt[k + 3] ? 4 : 0;
-        k += u > cbt[k + 1] ? 2 : 0;
-        k += u > cbt[k] ? 1 : 0;
-        w[b >> 3] |= (uint32_t)k << (4 * (b & 7));
+        for (int i = 0; i < 16; ++i) {
+          const uint64_t Q0 = mul2(Y[i], R2);
+          float u0, u1;
+          upk2(fma2(fma2(Q0, NN2, Y[i]), R2, Q0), u0, u1);
+          w[i >> 2] |= index(u0) << (8 * (i & 3)) | index(u1) << (8 * (i & 3) + 4);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float y0, y1;
+          upk2(Y[i], y0, y1);
+          const float u0 = nf > 0.f ? __fdiv_rn(y0, nf) : 0.f, u1 = nf > 0.f ? __fdiv_rn(y1, nf) : 0.f;
+          w[i >> 2] |= index(u0) << (8 * (i & 3)) | index(u1) << (8 * (i & 3) + 4);
+        }
       }
       uint8_t* blk = out + j * ROW + chunk * BB;
       if (a4 == 0) *reinterpret_cast<__half*>(blk) = n16;

@@ -10,6 +10,7 @@
 #include <string>
 
 #include "kvq_internal.cuh"
+#include "tbq4_bins.cuh"
 
 using namespace kvq;
 
@@ -98,6 +99,8 @@ kvq_status check_config(const kvq_config* c, bool allow16) {
     if (!(c->flags & tb)) continue;
     if (!(c->flags & rb) || f.bits != 4 || f.group != 128 || f.axis != KVQ_AXIS_TOKEN || c->hot_window > 0)
       return fail(KVQ_ERR_UNSUPPORTED, "TBQ4 needs the rotation, 4-bit per-token blocks of 128 and one tier");
+    if (!kvq::tbq4_bins_ok())
+      return fail(KVQ_ERR_UNSUPPORTED, "TBQ4 midpoints too close for the binned index lookup");
   }
   if (c->page_tokens < 0) return fail(KVQ_ERR_ARG, "page_tokens < 0");
   if (c->page_tokens > 0) {
@@ -346,6 +349,20 @@ void tbq4_tables(float* centroids, float* thresholds) {
   });
   std::memcpy(centroids, c32, sizeof(c32));
   std::memcpy(thresholds, t32, sizeof(t32));
+}
+
+// The append kernels look TBQ4 indices up in bins holding one midpoint each
+// (tbq4_bins.cuh): true when the table's midpoints allow that.
+bool tbq4_bins_ok() {
+  float c[16], t[15];
+  tbq4_tables(c, t);
+  const int k0 = tbq4_bin_k0(t);
+  for (int e = 0; e < 2 * kTbqBins; ++e) {
+    float th;
+    int base;
+    if (tbq4_bin_entry(t, k0, e, &th, &base) > 1) return false;
+  }
+  return true;
 }
 
 }  // namespace kvq

@@ -157,6 +157,7 @@ __device__ __forceinline__ float sign_of(const uint32_t* mask, int i) {
 
 // TBQ4 tables (host, computed once): 16 centroids, 15 thresholds, fp32.
 void tbq4_tables(float* centroids, float* thresholds);
+bool tbq4_bins_ok();
 
 // ---- launchers (defined in the kernel translation units) -------------------
 
