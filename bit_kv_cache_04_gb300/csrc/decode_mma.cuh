@@ -208,11 +208,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
 // four bytes at an even address
 __device__ __forceinline__ uint32_t ld_u32e(const uint8_t* p) { return ld_u16(p) | (ld_u16(p + 2) << 16); }
-// 24 bits at any byte address (reads the aligned word after it too)
-__device__ __forceinline__ uint32_t ld_u24(const uint8_t* p) {
-  const uintptr_t ad = reinterpret_cast<uintptr_t>(p);
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(ad & ~uintptr_t(3));
-  return __funnelshift_r(w[0], w[1], (uint32_t)(ad & 3) * 8) & 0xFFFFFFu;
+// 32 bits of a row's bit stream from bit 8 off + lb on, where the row is
+// 4-byte aligned, off a byte offset that is a constant after unrolling and lb
+// the lane's bit offset: two aligned words funnel-shifted (the word after the
+// field lies inside the stage buffer).  The word index and shift depend on
+// off mod 4 and the lane only, so they are computed once per lane.
+__device__ __forceinline__ uint32_t ld_bits(const uint8_t* row, int off, int lb) {
+  const int t = 8 * (off & 3) + lb;
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(row + (off & ~3)) + (t >> 5);
+  return __funnelshift_r(w[0], w[1], (uint32_t)t);
 }
 
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
@@ -291,6 +295,15 @@ __device__ __forceinline__ void dqt(uint32_t x, uint32_t (&r)[4], const uint32_t
   }
 }
 
+// Eight 3-bit K codes (channels c0..c0+7 of one token, bits 24 tq of the span
+// at byte off of the 4-byte aligned row) as four fp16 pairs (c0+j, c0+j+4).
+__device__ __forceinline__ void k_token_pairs3(const uint8_t* row, int off, int tq, uint32_t (&r)[4]) {
+  const uint32_t w = ld_bits(row, off, 24 * tq);
+  const uint32_t x = (w & 0xFFFu) | ((w << 4) & 0x0FFF0000u);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) r[j] = code_pair<3>(x, j);
+}
+
 // Eight K codes (channels c0..c0+7 of one token) as four fp16 pairs
 // (c0+j, c0+j+4), j = 0..3.  `p` points at the first code byte of the span.
 template <class C>
@@ -306,11 +319,8 @@ __device__ __forceinline__ void k_token_pairs(const uint8_t* p, int tq, uint32_t
     r[1] = code_pair8(xa, 1);
     r[2] = code_pair8(xb, 0);
     r[3] = code_pair8(xb, 1);
-  } else {  // 3 bits, 8 codes in 24 bits
-    const uint32_t w = ld_u24(p + 3 * tq);
-    const uint32_t x = (w & 0xFFFu) | ((w << 4) & 0x0FFF0000u);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) r[j] = code_pair<3>(x, j);
+  } else {
+    static_assert(C::KB != 3, "3-bit K codes: k_token_pairs3");
   }
 }
 
@@ -328,14 +338,11 @@ __device__ __forceinline__ void v_pair4(const uint8_t* pa, const uint8_t* pb, in
     r[2] = code_pair8(xb, 0);
     r[3] = code_pair8(xb, 1);
   } else {
+    static_assert(C::VB != 3, "3-bit V codes: v_pair4_3");
     uint32_t ua, ub;
     if constexpr (C::VB == 4) {
       ua = ld_u16(pa + 2 * gq);
       ub = ld_u16(pb + 2 * gq);
-    } else if constexpr (C::VB == 3) {  // 12 bits at bit 12*gq of the span
-      const int sh = 12 * (gq & 1), bo = 3 * (gq >> 1);
-      ua = (ld_u24(pa + bo) >> sh) & 0xFFFu;
-      ub = (ld_u24(pb + bo) >> sh) & 0xFFFu;
     } else {  // 2 bits: byte gq of the span
       ua = pa[gq];
       ub = pb[gq];
@@ -350,6 +357,16 @@ __device__ __forceinline__ void v_pair4(const uint8_t* pa, const uint8_t* pb, in
       for (int j = 0; j < 4; ++j) r[j] = code_pair<C::VB>(x, j);
     }
   }
+}
+
+// Four 3-bit V codes (channels 4 gq .. 4 gq + 3: bits 12 gq of the span at
+// byte off) of the 4-byte aligned token rows ra and rb as four fp16 pairs
+// (row a, row b).  Bits 12..15 of each half hold the next lane's codes, which
+// the field masks of code_pair drop.
+__device__ __forceinline__ void v_pair4_3(const uint8_t* ra, const uint8_t* rb, int off, int gq, uint32_t (&r)[4]) {
+  const uint32_t x = __byte_perm(ld_bits(ra, off, 12 * gq), ld_bits(rb, off, 12 * gq), 0x5410);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) r[j] = code_pair<3>(x, j);
 }
 
 template <class C>
@@ -552,8 +569,14 @@ __device__ __forceinline__ void pv_packed(const Ctx<C>& cx, WarpState<C>& ws, co
         for (int mu = 0; mu < 2; ++mu) {
           const int T1 = 8 * tq + 2 * mu;
           uint32_t x12[4], x34[4];
-          v_pair4<TR>(vsm + T1 * TR::VROW + off, vsm + (T1 + 4) * TR::VROW + off, gq, x12, cx.lut);
-          v_pair4<TR>(vsm + (T1 + 1) * TR::VROW + off, vsm + (T1 + 5) * TR::VROW + off, gq, x34, cx.lut);
+          if constexpr (TR::VB == 3) {
+            static_assert(TR::VROW % 4 == 0 && C::VOFF % 4 == 0 && C::STAGE % 4 == 0, "4-byte aligned rows");
+            v_pair4_3(vsm + T1 * TR::VROW, vsm + (T1 + 4) * TR::VROW, off, gq, x12);
+            v_pair4_3(vsm + (T1 + 1) * TR::VROW, vsm + (T1 + 5) * TR::VROW, off, gq, x34);
+          } else {
+            v_pair4<TR>(vsm + T1 * TR::VROW + off, vsm + (T1 + 4) * TR::VROW + off, gq, x12, cx.lut);
+            v_pair4<TR>(vsm + (T1 + 1) * TR::VROW + off, vsm + (T1 + 5) * TR::VROW + off, gq, x34, cx.lut);
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             mma16816(ws.o[2 * s][nt], x12[0], x12[1], x34[0], x34[1], pb[mu][nt][0], pb[mu][nt][1]);
@@ -759,8 +782,15 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
           for (int mu = 0; mu < 2; ++mu) {
             const int ra = 4 * gq + 2 * mu;
             uint32_t wa[4], wb[4];
-            k_token_pairs<TR>(ksm + ra * TR::KROW + kb * TR::KBB + TR::HDR + ss * TR::KSPAN, tq, wa, cx.lut);
-            k_token_pairs<TR>(ksm + (ra + 1) * TR::KROW + kb * TR::KBB + TR::HDR + ss * TR::KSPAN, tq, wb, cx.lut);
+            if constexpr (TR::KB == 3) {
+              static_assert(TR::KROW % 4 == 0 && C::STAGE % 4 == 0, "4-byte aligned rows");
+              const int off = kb * TR::KBB + TR::HDR + ss * TR::KSPAN;
+              k_token_pairs3(ksm + ra * TR::KROW, off, tq, wa);
+              k_token_pairs3(ksm + (ra + 1) * TR::KROW, off, tq, wb);
+            } else {
+              k_token_pairs<TR>(ksm + ra * TR::KROW + kb * TR::KBB + TR::HDR + ss * TR::KSPAN, tq, wa, cx.lut);
+              k_token_pairs<TR>(ksm + (ra + 1) * TR::KROW + kb * TR::KBB + TR::HDR + ss * TR::KSPAN, tq, wb, cx.lut);
+            }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               const uint2 q0 = qb[((2 * s) * NT + nt) * 32 + lane];

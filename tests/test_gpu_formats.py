@@ -211,20 +211,52 @@ TBQ4_CASES = [
     ("tbq4_f16_d128", 128, K.DT_F16, 0, 32),          # window: the generic decode kernel
     ("tbq4_f16_d128_mma", 128, K.DT_F16, 7, 0),        # the tensor-core decode, D = 128
     ("tbq4_bf16_d256_seed", 256, K.DT_BF16, 0x5EED, 0),  # the tensor-core decode, D = 256
+    # blocks outside the fast quotient's bounds (bytes only)
+    ("tbq4_bf16_d256_edge", 256, K.DT_BF16, 3, 0, "edge"),
+    ("tbq4_f16_d128_edge", 128, K.DT_F16, 5, 0, "edge"),
 ]
+
+
+def _tbq4_edge(n_tok, H, D, gen, bf16):
+    """[n_tok, H, D] values whose 128-value blocks take every branch of the
+    TBQ4 quantizer, by token index mod 6: N(0, 1); all zeros (zero norm);
+    a few units of 2^-24 (tiny norms, some rotated values exactly 0); huge
+    values (the norm saturates at 65504); N(0, 1) with one infinity; 1 and +-1
+    in channels 10, 11 and beta in channel 70, zeros elsewhere: where the
+    sign flips make the first butterfly cancel, half the rotated values are
+    +-beta c (beta = 2^-110 for bf16: far below 2^-100 next to values near 1)."""
+    x = torch.randn((n_tok, H, D), generator=gen, dtype=torch.float64)
+    kind = (torch.arange(n_tok) % 6).view(-1, 1, 1).expand(n_tok, H, D)
+    tiny = torch.randint(-3, 4, (n_tok, H, D), generator=gen).double() * 2.0 ** -24
+    huge = x * 1e30 if bf16 else (x * 30000.0).clamp(-65504.0, 65504.0)
+    one_inf = torch.where((torch.arange(D) == 17).view(1, 1, -1), float("inf"), x)
+    c = torch.arange(D).view(1, 1, -1)
+    sgn = torch.where(torch.rand((n_tok, H, 1), generator=gen) < 0.5, -1.0, 1.0).double()
+    beta = 2.0 ** (-110 if bf16 else -24)
+    cancel = torch.where(c == 10, 1.0, torch.where(c == 11, sgn, torch.where(c == 70, beta, 0.0)))
+    out = torch.where(kind == 1, 0.0, x)
+    out = torch.where(kind == 2, tiny, out)
+    out = torch.where(kind == 3, huge, out)
+    out = torch.where(kind == 4, one_inf, out)
+    return torch.where(kind == 5, cancel.expand(n_tok, H, D), out)
 
 
 @pytest.mark.parametrize("case", TBQ4_CASES, ids=[c[0] for c in TBQ4_CASES])
 def test_tbq4_bytes_decode_and_dequantize(case):
-    name, D, dtype, seed, R = case
+    name, D, dtype, seed, R = case[:5]
+    edge = len(case) > 5
     flags = K.ROTATE_K | K.ROTATE_V | K.TBQ4_K | K.TBQ4_V
     cfg = K.Config(L=1, H_kv=3, H_q=6, D=D, batch=len(LENGTHS), max_T=max(LENGTHS) + 32, in_dtype=dtype,
                    k_fmt=K.Fmt(4, 128), v_fmt=K.Fmt(4, 128), residual_window=R, flags=flags, sign_seed=seed)
     oc = oracle_cfg(cfg)
     gen = torch.Generator().manual_seed(zlib.crc32(name.encode()))
     dt = torch.float16 if dtype == K.DT_F16 else torch.bfloat16
-    ks = [_inputs("random", T, cfg.H_kv, D, 4, gen).to(dt) for T in LENGTHS]
-    vs = [_inputs("random", T, cfg.H_kv, D, 4, gen).to(dt) for T in LENGTHS]
+    if edge:
+        ks = [_tbq4_edge(T, cfg.H_kv, D, gen, dt == torch.bfloat16).to(dt) for T in LENGTHS]
+        vs = [_tbq4_edge(T, cfg.H_kv, D, gen, dt == torch.bfloat16).to(dt) for T in LENGTHS]
+    else:
+        ks = [_inputs("random", T, cfg.H_kv, D, 4, gen).to(dt) for T in LENGTHS]
+        vs = [_inputs("random", T, cfg.H_kv, D, 4, gen).to(dt) for T in LENGTHS]
     cache = K.KVCache(cfg, "cuda")
     ref = O.new_buffers(oc)
     seq_lens = torch.zeros(cfg.batch, dtype=torch.int32, device="cuda")
@@ -250,6 +282,8 @@ def test_tbq4_bytes_decode_and_dequantize(case):
             total, diff, maxd, sdiff = codes_differ(oc, {n: got[n]}, {n: ref[n]}) \
                 if not n.endswith("resid") else (0, -1, -1, -1)
             pytest.fail(f"{name} {n}: bytes differ (codes {diff}/{total}, max |dc| {maxd}, scales {sdiff})")
+    if edge:
+        return
     # decode over the GPU's own bytes, against fp64 attention
     q = torch.randn((1, cfg.batch, cfg.H_q, D), generator=gen).to(dt).cuda()
     out = torch.full((1, cfg.batch, cfg.H_q, D), float("nan"), dtype=torch.float32, device="cuda")
