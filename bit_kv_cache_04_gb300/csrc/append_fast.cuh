@@ -338,9 +338,16 @@ __device__ __forceinline__ void block32_zp_x2(const uint32_t (&raw)[32], float2 
 
 // Per-token 32-value blocks: a block of 128 threads takes 128 consecutive
 // tokens of one (layer, sequence, kv head); thread j quantizes token row j
-// slice by slice, with the loads of the following slices in flight.
-// The rows are built in shared memory and written out whole.
+// slice by slice.  At D = 128 (when the static shared memory allows) the rows
+// arrive through a shared stage filled by cp.async with 16 consecutive threads
+// per 256-byte row: a load of each thread's own row touches 32 lines per warp
+// instruction and kept the L1 pipe saturated.  16-byte chunk q of row r sits
+// at chunk q ^ (r mod 16), so the copy and each thread's row reads are free of
+// bank conflicts.  Otherwise each thread loads its own row with the following
+// slices in flight.  The outputs are built in shared memory and written out
+// whole.
 constexpr int kTokItem = 128;
+constexpr int kStageChunks = 16;  // 16-byte chunks of a staged row: 128 16-bit values
 
 template <int NC, int DT, int B, int CB, int which, bool Z>
 __global__ void __launch_bounds__(kAppendThreads, 5) quant_token32_kernel(AppendArgs a) {
@@ -348,8 +355,12 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_token32_kernel(Append
   constexpr int BB = HDR + 4 * B, ROW = SPR * BB;
   constexpr int CBB = CB ? HDR + 4 * CB : 0, CROW = SPR * CBB;
   constexpr int OUTB = kTokItem * (ROW > CROW ? ROW : CROW);
+  // staged rows: one pass, and the stage fits the 48 KB of static shared memory
+  constexpr bool STAGED = NC == 1 && OUTB + kTokItem * (16 * kStageChunks + 8) + 64 <= 48 * 1024;
   static_assert(kTokItem == kAppendThreads, "one token row per thread");
   __shared__ __align__(16) uint8_t out[OUTB];
+  __shared__ __align__(16) uint4 stage[STAGED ? kTokItem * kStageChunks : 1];
+  __shared__ const uint4* rowp[STAGED ? kTokItem : 1];
   __shared__ uint32_t page_bad;
   const Layout& lo = a.lo;
   const int li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B, h = blockIdx.y;
@@ -367,10 +378,62 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_token32_kernel(Append
   // tiered chunks start at multiples of 32 (Gamma = 32), and cold rows come
   // before hot rows, so rows of both strides never overlap in the tile
   const bool to_cold = CB != 0 && lo.tiered && t < c1;
-  if (j < n_tok) {
+  uint8_t* dst = out + j * (to_cold ? CROW : ROW);
+  // one 32-value slice: r holds its 16-bit values
+  auto slice = [&](const uint4 (&r)[4], int sl) {
+    float v[32], mn = 0.f, mx = 0.f;
+    if constexpr (Z) {  // block extremes on the 16-bit pairs
+      uint32_t lo2 = r[0].x, hi2 = lo2;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t ww[4] = {r[q].x, r[q].y, r[q].z, r[q].w};
+#pragma unroll
+        for (int e = (q == 0 ? 1 : 0); e < 4; ++e) {
+          lo2 = min2_16<DT>(lo2, ww[e]);
+          hi2 = max2_16<DT>(hi2, ww[e]);
+        }
+      }
+      const float2 l = raw_pair_to_f32<DT>(lo2), h = raw_pair_to_f32<DT>(hi2);
+      mn = fminf(l.x, l.y);
+      mx = fmaxf(h.x, h.y);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t ww[4] = {r[q].x, r[q].y, r[q].z, r[q].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = raw_pair_to_f32<DT>(ww[e]);
+        v[8 * q + 2 * e] = f.x;
+        v[8 * q + 2 * e + 1] = f.y;
+      }
+    }
+    hot_or_cold<B, CB, Z>(v, to_cold, dst + sl * BB, dst + sl * CBB, mn, mx);
+  };
+  if constexpr (STAGED) {
+    if (j < n_tok)
+      rowp[j] = reinterpret_cast<const uint4*>(t < s.T0 ? resid_row(lo, a.cp, which, layer, seq, h, t)
+                                                        : input_row(a, which, li, s, h, t));
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kTokItem * kStageChunks / kAppendThreads; ++i) {
+      const int f = i * kAppendThreads + threadIdx.x, r = f / kStageChunks, q = f % kStageChunks;
+      if (r < n_tok) cp_async16(&stage[r * kStageChunks + (q ^ (r % kStageChunks))], rowp[r] + q);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    if (j < n_tok) {
+#pragma unroll
+      for (int sl = 0; sl < SPR; ++sl) {
+        uint4 r[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) r[q] = stage[j * kStageChunks + ((4 * sl + q) ^ (j % kStageChunks))];
+        slice(r, sl);
+      }
+    }
+  } else if (j < n_tok) {
     const uint4* src = reinterpret_cast<const uint4*>(t < s.T0 ? resid_row(lo, a.cp, which, layer, seq, h, t)
                                                                  : input_row(a, which, li, s, h, t));
-    uint8_t* dst = out + j * (to_cold ? CROW : ROW);
     // PF slices of the row in flight: the whole 128-value row, or two slices
     // of a 256-value row
     constexpr int PF = SPR <= 4 ? SPR : 2;
@@ -381,39 +444,14 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_token32_kernel(Append
       for (int q = 0; q < 4; ++q) r[p][q] = src[4 * p + q];
 #pragma unroll
     for (int sl = 0; sl < SPR; ++sl) {
-      float v[32], mn = 0.f, mx = 0.f;
-      if constexpr (Z) {  // block extremes on the 16-bit pairs
-        uint32_t lo2 = r[sl % PF][0].x, hi2 = lo2;
+      uint4 c[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 c = r[sl % PF][q];
-          const uint32_t ww[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-          for (int e = (q == 0 ? 1 : 0); e < 4; ++e) {
-            lo2 = min2_16<DT>(lo2, ww[e]);
-            hi2 = max2_16<DT>(hi2, ww[e]);
-          }
-        }
-        const float2 l = raw_pair_to_f32<DT>(lo2), h = raw_pair_to_f32<DT>(hi2);
-        mn = fminf(l.x, l.y);
-        mx = fmaxf(h.x, h.y);
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 c = r[sl % PF][q];
-        const uint32_t ww[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = raw_pair_to_f32<DT>(ww[e]);
-          v[8 * q + 2 * e] = f.x;
-          v[8 * q + 2 * e + 1] = f.y;
-        }
-      }
+      for (int q = 0; q < 4; ++q) c[q] = r[sl % PF][q];
       if (sl + PF < SPR) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) r[sl % PF][q] = src[4 * (sl + PF) + q];
       }
-      hot_or_cold<B, CB, Z>(v, to_cold, dst + sl * BB, dst + sl * CBB, mn, mx);
+      slice(c, sl);
     }
   }
   __syncthreads();
@@ -443,8 +481,9 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_token32_kernel(Append
 
 // Per-channel blocks over 32-token groups: thread = (group lane, channel
 // pair); a block takes NG = GPC x kGroupSteps consecutive groups, each thread
-// kGroupSteps of them in turn.  Each group row (D blocks) is built in shared
-// memory and written out whole.
+// kGroupSteps of them in turn.  A warp's loads of one token row are 32
+// consecutive words (one line), so the rows are read in place.  Each group
+// row (D blocks) is built in shared memory and written out whole.
 constexpr int kGroupSteps = 2;
 
 template <int NC, int DT, int B, int CB, int which, bool Z>
@@ -472,11 +511,11 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_channel32_kernel(Appe
     const bool to_cold = CB != 0 && lo.tiered && t0 < c1;
     // the group's rows: window ring slots for tokens below T0, new input rows
     // (a fixed stride apart) from T0 on
+    uint32_t raw[32];
     const int n_rw = min(max(s.T0 - t0, 0), kTile);  // leading tokens from the window
     const uint32_t* in = nullptr;
     if (n_rw < kTile) in = reinterpret_cast<const uint32_t*>(input_row(a, which, li, s, h, t0 + n_rw)) + cp;
     const int in_stride = lo.H * D / 2;
-    uint32_t raw[32];
     if (n_rw == 0) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) raw[j] = in[j * in_stride];
