@@ -385,7 +385,11 @@ __global__ void __launch_bounds__(kAppendThreads) quant_rot128_kernel(AppendArgs
                    ((((int64_t)layer * lo.n_pages + page) * lo.H + h) * lo.pt + ta % lo.pt) * ROW;
     const uint8_t* src = out + (ta - u0) * ROW;
     const int bytes = (tb - ta) * ROW;
-    if (((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) | (uintptr_t)bytes) & 3u) == 0) {
+    const uintptr_t al = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) | (uintptr_t)bytes;
+    if ((al & 15u) == 0) {  // whole pages: 16 rows of 66 or 50 bytes are whole 16-byte words
+      for (int e = lane; e < bytes / 16; e += 32)
+        reinterpret_cast<uint4*>(dst)[e] = reinterpret_cast<const uint4*>(src)[e];
+    } else if ((al & 3u) == 0) {
       for (int e = lane; e < bytes / 4; e += 32)
         reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(src)[e];
     } else {
