@@ -943,6 +943,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   constexpr int kStages = C::STAGES;
   __shared__ uint64_t mbar[kWarps * kMaxStages];
   __shared__ int is_last;
+  __shared__ int pf_page[kWarps][2][2];  // paged: next tile's page ids per warp, by issue parity
 
   if constexpr (STEP != 0) {
     // the step's cache writes first, then this block's decode reads them:
@@ -1088,6 +1089,12 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   }
   uint8_t* wst = stage_base + warp * kStages * C::STAGE;
 
+  // Paged tiles: lane 0 copies the page ids of the next tile it will issue
+  // into shared memory (4-byte cp.async) one issue ahead, so the block-table
+  // reads overlap a group of compute instead of stalling the copy issue; no
+  // register holds them across the loop.
+  const int first = tb + warp;  // this warp takes tiles first, first + kWarps, ...
+
   // Bulk copies of packed tile `tile` (cold or hot/only tier) into stage
   // `st`, issued by lane 0: exactly one arrival on the stage's barrier per
   // packed tile of this warp (with no bytes when a page id is bad).
@@ -1112,28 +1119,42 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     const int t0 = ce + (tile - n_c) * kTile;
     bool bad = false;
     if (lo.paged) {
+      // one or two pages (16-token pages when the group is complete); tiles
+      // start at multiples of 32, so at row 0 of a page
       const int np = (qe - t0 > lo.pt) ? kTile / lo.pt : 1;
       const int kb = lo.pt * HT::KROW, vb = lo.pt * HT::VROW;
-      // one or two pages (16-token pages when the group is complete)
-      const uint8_t* kg0 = main_row(lo, a.cp, 0, layer, seq, h, t0, &bad);
-      const uint8_t* vg0 = main_row(lo, a.cp, 1, layer, seq, h, t0, &bad);
-      const uint8_t* kg1 = kg0;
-      const uint8_t* vg1 = vg0;
-      if (np == 2) {
-        kg1 = main_row(lo, a.cp, 0, layer, seq, h, t0 + lo.pt, &bad);
-        vg1 = main_row(lo, a.cp, 1, layer, seq, h, t0 + lo.pt, &bad);
+      // this warp issues tiles first, first + kWarps, ...: the ids of every
+      // tile after the first were copied by the issue before it
+      const int par = ((tile - first) / kWarps) & 1;
+      const int* bt_row = a.cp.block_table + (int64_t)seq * lo.max_pages;
+      int p0, p1;
+      if (tile == first || (tile - kWarps) < n_c) {
+        p0 = bt_row[t0 / lo.pt];
+        p1 = np == 2 ? bt_row[t0 / lo.pt + 1] : p0;
+      } else {
+        cp_async_wait<0>();
+        p0 = pf_page[warp][par][0];
+        p1 = np == 2 ? pf_page[warp][par][1] : p0;
       }
-      if (bad) {
+      const int nx = tile + kWarps;  // the next tile this warp issues
+      if (nx < te && nx >= n_c && nx < n_c + n_m) {
+        const int pn = (ce + (nx - n_c) * kTile) / lo.pt;
+        cp_async4(&pf_page[warp][par ^ 1][0], bt_row + pn);
+        cp_async4(&pf_page[warp][par ^ 1][1], bt_row + pn + (qe - pn * lo.pt > lo.pt ? 1 : 0));
+        cp_async_commit();
+      }
+      if (p0 < 0 || p0 >= lo.n_pages || p1 < 0 || p1 >= lo.n_pages) {
         bad_page = 1;
         mbar_arrive_tx(bar, 0);
         return;
       }
+      auto row0 = [&](int page) { return (((int64_t)layer * lo.n_pages + page) * lo.H + h) * lo.pt; };
       mbar_arrive_tx(bar, np * (kb + vb));
-      bulk_g2s(ks, kg0, kb, bar);
-      bulk_g2s(vs, vg0, vb, bar);
+      bulk_g2s(ks, a.cp.k_main + row0(p0) * lo.kf.row, kb, bar);
+      bulk_g2s(vs, a.cp.v_main + row0(p0) * lo.vf.row, vb, bar);
       if (np == 2) {
-        bulk_g2s(ks + kb, kg1, kb, bar);
-        bulk_g2s(vs + vb, vg1, vb, bar);
+        bulk_g2s(ks + kb, a.cp.k_main + row0(p1) * lo.kf.row, kb, bar);
+        bulk_g2s(vs + vb, a.cp.v_main + row0(p1) * lo.vf.row, vb, bar);
       }
       return;
     }
@@ -1145,7 +1166,6 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   };
 
   // ---- per-warp pipeline over this CTA's groups --------------------------------
-  const int first = tb + warp;
   // the query scratch in the stage buffers was written through the generic
   // proxy; order it before the bulk copies, and publish the barriers
   fence_proxy_async();
