@@ -471,7 +471,7 @@ def _oracle_sample(w, heads, T, seed=0):
 # with the SHA-256 of the kernel source it was taken on; the roofline reports
 # them scaled to the timed launch while the source is unchanged, else null.
 DECODE_TRAFFIC = {
-    "llama2_7b_kivi4": {"sha256": "f71eb89d533e351baa3e21574588e747d5277e315f7d479466d00a62f5c171b1", "bytes_per_layer": (610.749440e6 + 11.714816e6) / 4,
+    "llama2_7b_kivi4": {"sha256": "3d355fc169ef465b96786ccd7979d3abe4d1cb12e7b72d211a7d6ca1725178bf", "bytes_per_layer": (610.753024e6 + 11.729408e6) / 4,
                         "capture": "4-layer fused step launch, profiles/decode_step_llama2_7b_kivi4_4layers.md"},
 }
 

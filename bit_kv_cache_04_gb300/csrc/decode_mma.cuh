@@ -1337,6 +1337,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     fence_proxy_async();
     __syncwarp();
   }
+  if (lo.paged && lane == 0) cp_async_wait<0>();  // a page-id copy issued for a tile not reached
   if (stall_it >= 0) {
     // a copy did not land in time: flag it, give this warp's copies still in
     // flight (that tile's and the next one's) a last bounded wait, and merge
