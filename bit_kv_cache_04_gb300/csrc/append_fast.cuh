@@ -271,6 +271,80 @@ __device__ __forceinline__ void block_copy_out(uint8_t* dst, const uint8_t* src,
   }
 }
 
+// Two symmetric blocks at once: channels c and c + 1 of 32 tokens, raw[j]
+// holding token j's two 16-bit values, each block as block32 computes it
+// (absolute maxima on the 16-bit pairs, exact; the quotient, correction and
+// rounding on f32x2 lanes, one per channel).  Returns false, writing
+// nothing, when either scale is subnormal or saturated in fp16: those blocks
+// need the clamp and go through block32 one by one.
+template <int DT, int B>
+__device__ __forceinline__ bool block32_x2(const uint32_t (&raw)[32], uint8_t* dst0, uint8_t* dst1) {
+  constexpr int qmax = (1 << (B - 1)) - 1;
+  constexpr float magic = kRoundMagic + (float)(qmax + 1);
+  uint32_t a2 = raw[0] & 0x7FFF7FFFu;
+#pragma unroll
+  for (int j = 1; j < 32; ++j) a2 = max2_16<DT>(a2, raw[j] & 0x7FFF7FFFu);
+  const float2 m = raw_pair_to_f32<DT>(a2);
+  const __half s0 = block_scale_of(m.x, qmax), s1 = block_scale_of(m.y, qmax);
+  const float f0 = __half2float(s0), f1 = __half2float(s1);
+  if (!(f0 >= kMinNormalF16 && f0 < 65504.f && f1 >= kMinNormalF16 && f1 < 65504.f)) return false;
+  const uint64_t R2 = pk2(__frcp_rn(f0), __frcp_rn(f1)), NS2 = pk2(-f0, -f1), M2 = pk2(magic, magic);
+  uint32_t w0[B], w1[B], corr[B];
+#pragma unroll
+  for (int k = 0; k < B; ++k) w0[k] = w1[k] = corr[k] = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float2 x = raw_pair_to_f32<DT>(raw[j]);
+    const uint64_t X = pk2(x.x, x.y);
+    const uint64_t Q0 = mul2(X, R2);
+    float r0, r1;
+    upk2(add2(fma2(fma2(Q0, NS2, X), R2, Q0), M2), r0, r1);
+    const uint32_t b0 = __float_as_uint(r0), b1 = __float_as_uint(r1);
+    const int bit = B * j, k = bit / 32, sh = bit % 32;
+    if (sh + B > 32) {  // a 3-bit code across two words: place the true biased code
+      const uint32_t u0 = b0 - kRoundMagicBits, u1 = b1 - kRoundMagicBits;
+      w0[k] += u0 << sh;
+      w0[k + 1] += u0 >> (32 - sh);
+      w1[k] += u1 << sh;
+      w1[k + 1] += u1 >> (32 - sh);
+    } else {
+      w0[k] += b0 << sh;
+      w1[k] += b1 << sh;
+      corr[k] += kRoundMagicBits << sh;
+    }
+  }
+  uint16_t* p0 = reinterpret_cast<uint16_t*>(dst0);
+  uint16_t* p1 = reinterpret_cast<uint16_t*>(dst1);
+  p0[0] = __half_as_ushort(s0);
+  p1[0] = __half_as_ushort(s1);
+#pragma unroll
+  for (int k = 0; k < B; ++k) {
+    uint32_t a = w0[k] - corr[k], b = w1[k] - corr[k];
+    if (B == 8) {
+      a ^= 0x80808080u;
+      b ^= 0x80808080u;
+    }
+    p0[1 + 2 * k] = (uint16_t)a;
+    p0[2 + 2 * k] = (uint16_t)(a >> 16);
+    p1[1 + 2 * k] = (uint16_t)b;
+    p1[2 + 2 * k] = (uint16_t)(b >> 16);
+  }
+  return true;
+}
+
+// The blocks block32_x2 declines (a subnormal or saturated scale), one
+// channel at a time through block32; out of line, with the 16-bit pairs in
+// local memory, so that the common path keeps its registers.
+template <int DT, int B>
+__device__ __noinline__ void block32_pair_slow(const uint32_t* raw, uint8_t* dst0, uint8_t* dst1) {
+  for (int hc = 0; hc < 2; ++hc) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = in_to_f32_t<DT>(hc ? (raw[j] >> 16) : (raw[j] & 0xFFFFu));
+    block32<B>(v, amax_of(v), hc ? dst1 : dst0, nullptr);
+  }
+}
+
 // Two asymmetric blocks at once: channels c and c + 1 of 32 tokens, raw[j]
 // holding token j's two 16-bit values.  The codes of both blocks are taken on
 // f32x2 pairs (one lane per channel) as codes_zp does, consuming raw as they
@@ -486,8 +560,14 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_token32_kernel(Append
 // row (D blocks) is built in shared memory and written out whole.
 constexpr int kGroupSteps = 2;
 
+// One tier (the pair quantizers, no 32-value float arrays): 72 registers and
+// seven CTAs per SM hide more of the load latency; measured faster than five
+// or six CTAs even where the asymmetric body spills a few words.
+template <int CB, bool Z>
+constexpr int channel_ctas() { return CB == 0 ? 7 : 5; }
+
 template <int NC, int DT, int B, int CB, int which, bool Z>
-__global__ void __launch_bounds__(kAppendThreads, 5) quant_channel32_kernel(AppendArgs a) {
+__global__ void __launch_bounds__(kAppendThreads, channel_ctas<CB, Z>()) quant_channel32_kernel(AppendArgs a) {
   constexpr int D = 128 * NC, PAIRS = D / 2, GPC = kAppendThreads / PAIRS, NG = GPC * kGroupSteps;
   constexpr int HDR = Z ? 4 : 2;
   constexpr int BB = HDR + 4 * B, GROW = D * BB;
@@ -503,15 +583,12 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_channel32_kernel(Appe
   const int base = (q0 / (kTile * NG)) * (kTile * NG) + blockIdx.x * (kTile * NG);
   if (base + kTile * NG <= q0 || base >= q1) return;
   const int gl = threadIdx.x / PAIRS, cp = threadIdx.x % PAIRS;
-#pragma unroll 1
-  for (int gs = 0; gs < kGroupSteps; ++gs) {
-    const int gi = gs * GPC + gl;
-    const int t0 = base + kTile * gi;
-    if (t0 < q0 || t0 >= q1) continue;
-    const bool to_cold = CB != 0 && lo.tiered && t0 < c1;
-    // the group's rows: window ring slots for tokens below T0, new input rows
-    // (a fixed stride apart) from T0 on
-    uint32_t raw[32];
+  // the rows of group step gs for this thread's channel pair: window ring
+  // slots for tokens below T0, new input rows (a fixed stride apart) from T0
+  // on; false when the group is outside this call's range
+  auto load_group = [&](int gs, uint32_t (&raw)[32]) -> bool {
+    const int t0 = base + kTile * (gs * GPC + gl);
+    if (t0 < q0 || t0 >= q1) return false;
     const int n_rw = min(max(s.T0 - t0, 0), kTile);  // leading tokens from the window
     const uint32_t* in = nullptr;
     if (n_rw < kTile) in = reinterpret_cast<const uint32_t*>(input_row(a, which, li, s, h, t0 + n_rw)) + cp;
@@ -528,6 +605,12 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_channel32_kernel(Appe
         slot = slot + 1 == lo.ring ? 0 : slot + 1;
       }
     }
+    return true;
+  };
+  auto quant_group = [&](int gs, const uint32_t (&raw)[32]) {
+    const int gi = gs * GPC + gl;
+    const int t0 = base + kTile * gi;
+    const bool to_cold = CB != 0 && lo.tiered && t0 < c1;
     float2 mn2 = make_float2(0.f, 0.f), mx2 = mn2;
     if constexpr (Z) {  // extremes of both channels' blocks on the 16-bit pairs
       uint32_t lo2 = raw[0], hi2 = raw[0];
@@ -538,12 +621,19 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_channel32_kernel(Appe
       }
       mn2 = raw_pair_to_f32<DT>(lo2);
       mx2 = raw_pair_to_f32<DT>(hi2);
-    }
-    if constexpr (Z) {
       if (!to_cold) {
         block32_zp_x2<DT, B>(raw, mn2, mx2, out + gi * SLOT + 2 * cp * BB, out + gi * SLOT + (2 * cp + 1) * BB);
-        continue;
+        return;
       }
+    } else if (!to_cold) {
+      uint8_t* d0 = out + gi * SLOT + 2 * cp * BB;
+      if (!block32_x2<DT, B>(raw, d0, d0 + BB)) {
+        uint32_t t[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) t[j] = raw[j];
+        block32_pair_slow<DT, B>(t, d0, d0 + BB);
+      }
+      return;
     }
 #pragma unroll
     for (int hc = 0; hc < 2; ++hc) {
@@ -557,6 +647,11 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_channel32_kernel(Appe
       hot_or_cold<B, CB, Z>(v, to_cold, out + gi * SLOT + c * BB, out + gi * SLOT + c * CBB, hc ? mn2.y : mn2.x,
                             hc ? mx2.y : mx2.x);
     }
+  };
+#pragma unroll 1
+  for (int gs = 0; gs < kGroupSteps; ++gs) {
+    uint32_t raw[32];
+    if (load_group(gs, raw)) quant_group(gs, raw);
   }
   __syncthreads();
 #pragma unroll
