@@ -241,11 +241,19 @@ int64_t fmt_bytes(const kvq_fmt& f, int64_t n_tokens, int D, bool zp) {
 // whole waves of resident CTAs best (152 SMs x 4 CTAs for D = 128, x 2 for
 // D = 256), with at least 8 tiles per split and no more growth once the grid
 // holds 8 waves.
+constexpr int64_t kMinTilesPerSplit = 8, kMinTilesPerSplitRotated = 48;
+
 int splits_for(const kvq_config* c, int n_layers) {
   const int64_t units = (int64_t)n_layers * c->batch * c->H_kv;
   const int64_t tiles = (c->max_T + kTile - 1) / kTile + 2;
   const int64_t resident = 152 * (c->D == 128 ? 4 : 2);
-  int64_t cap = tiles / 8;
+  // every split keeps at least a minimum of tiles of capacity.  Rotated
+  // layouts set a higher one: their per-block setup also rotates the query
+  // and un-rotates the output (a ragged batch of 2K-8K-token sequences
+  // decoded per layer took 2.15 ms with 19 splits per unit, 1.53 ms with 4;
+  // unrotated 1K-token layouts run faster with small splits)
+  const bool rotated = (c->flags & (KVQ_ROTATE_K | KVQ_ROTATE_V)) != 0;
+  int64_t cap = tiles / (rotated ? kMinTilesPerSplitRotated : kMinTilesPerSplit);
   if (cap < 1) cap = 1;
   if (cap > kMaxSplits) cap = kMaxSplits;
   int best = 1;

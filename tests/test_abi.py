@@ -111,6 +111,20 @@ def test_split_heuristic_fits_workspace():
             assert ws >= units * s * g * (cfg.D + 2) * 4 or s == 1
 
 
+def test_split_heuristic_keeps_whole_splits():
+    """Each split of the automatic policy covers at least 8 tiles of 32
+    tokens of capacity, 48 for rotated layouts (or there is one split)."""
+    for name in W.ALL:
+        cfg = W.make(name).cfg
+        tiles = (cfg.max_T + 31) // 32 + 2
+        least = 48 if cfg.flags & (K.ROTATE_K | K.ROTATE_V) else 8
+        for n in (1, cfg.L):
+            s = K.kvq_decode_splits(cfg, n)
+            assert s == 1 or tiles // s >= least, (name, n, s)
+    # the headline per-layer call keeps its measured-best 19 splits
+    assert K.kvq_decode_splits(W.make("llama2_7b_kivi4").cfg, 1) == 19
+
+
 def test_launch_counts():
     # append: [requant to cold] + quantize (two specialized kernels or one
     # generic) + [window copy]; decode: one launch
