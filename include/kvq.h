@@ -121,7 +121,10 @@ enum {
    * 4-bit 128-value block holds the block's L2 norm (fp16) and, per value, the index
    * of the nearest of the 16 Lloyd-Max centroids of N(0, 1/128) (see
    * kvq_tbq4_codebook).  Needs the tensor's rotation flag, 4 bits, group 128,
-   * per-token blocks, one tier.  Same 66 B per 128 values. */
+   * per-token blocks, one tier.  Same 66 B per 128 values.  The append kernels
+   * find an index with one lookup in bins of 1/8 octave of |u|; validation
+   * answers KVQ_ERR_UNSUPPORTED if two nonzero thresholds ever shared a bin
+   * (the built-in table's never do). */
   KVQ_TBQ4_K = 1u << 3,
   KVQ_TBQ4_V = 1u << 4,
   /* Asymmetric blocks ("scale and zero point", nalar.dev, "Granularitas
