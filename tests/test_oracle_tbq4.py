@@ -109,3 +109,46 @@ def test_tbq4_cache_round_trip():
     rows = bufs["k_main"][0, 0, :, :40]  # [H, T, row]
     got = np.moveaxis(rows, 0, 1).reshape(40, 2, 2, 66)
     assert np.array_equal(got[..., :2].copy().view(np.float16)[..., 0], n16)
+
+
+def test_thresholds_fall_in_distinct_eighth_octave_bins():
+    """The append kernels find a TBQ4 index with one lookup in bins of the
+    float bits of |u| >> 20 (eight bins per octave), each bin holding at most
+    one midpoint: the table's nonzero thresholds must sit in distinct bins,
+    the zero threshold alone below the first of them, and the lookup must
+    agree with the direct count on values next to every threshold."""
+    _, t = O.tbq4_codebook()
+    t = np.asarray(t, np.float32)
+    keys = [int(np.abs(x).view(np.uint32)) >> 20 for x in t if x != 0]
+    assert len(keys) == 14 and np.count_nonzero(t == 0) == 1
+    pos = sorted(k for k, x in zip(keys, t[t != 0]) if x > 0)
+    neg = sorted(k for k, x in zip(keys, t[t != 0]) if x < 0)
+    assert len(set(pos)) == len(pos) and len(set(neg)) == len(neg)
+    k0 = min(keys) - 1
+
+    def lookup(u):  # one bin per key of |u|, clamped; base count + at most one midpoint
+        u = np.float32(u)
+        a = int(np.abs(u).view(np.uint32)) >> 20
+        b = min(max(a, k0), k0 + 31)
+        lo = 0.0 if b == k0 else np.uint32(b << 20).view(np.float32)
+        hi = np.inf if b == k0 + 31 else np.uint32((b + 1) << 20).view(np.float32)
+        if not np.signbit(u):
+            inside = [x for x in t if lo <= x < hi]
+            base = int(np.sum(t < lo))
+        else:
+            inside = [x for x in t if -hi < x <= -lo]
+            base = int(np.sum(t <= -hi))
+        assert len(inside) <= 1
+        return base + (1 if inside and u > inside[0] else 0)
+
+    vals = [0.0, -0.0, 1e-30, -1e-30, 3.0, -3.0]
+    for x in t:
+        v = np.float32(x)
+        for d in (-2, -1, 0, 1, 2):
+            w = v
+            for _ in range(abs(d)):
+                w = np.nextafter(w, np.float32(np.inf if d > 0 else -np.inf))
+            vals.append(w)
+    vals += list(np.random.default_rng(3).standard_normal(2000).astype(np.float32) / np.float32(11.3))
+    for u in vals:
+        assert lookup(u) == int(np.sum(t < np.float32(u))), u
