@@ -136,7 +136,6 @@ __device__ __forceinline__ void block32(float (&v)[32], float m, uint8_t* dst, f
 // block's minimum and maximum lie in [0, 2^B - 1] no value needs the clamp;
 // any other block (a saturated or nearly degenerate scale, an infinity) is
 // quantized by the serial form, quant_zp32, with the IEEE divide and the clamp.
-template <int B>
 __device__ __forceinline__ float zp_magic_code(float x, float sf, float zf, float rcp) {
   return __fadd_rn(div_by_scale(__fsub_rn(x, zf), sf, rcp), kRoundMagic);
 }
@@ -179,8 +178,8 @@ __device__ __forceinline__ void block32_zp(const float (&v)[32], float mn, float
   const __half z16 = __float2half_rn(fminf(fmaxf(mn, -65504.0f), 65504.0f));
   const float sf = __half2float(s16), zf = __half2float(z16);
   const float rcp = sf == 0.f ? 0.f : __frcp_rn(sf);
-  if (!(zp_magic_code<B>(mn, sf, zf, rcp) >= kRoundMagic &&
-        zp_magic_code<B>(mx, sf, zf, rcp) <= kRoundMagic + (float)qlev)) {
+  if (!(zp_magic_code(mn, sf, zf, rcp) >= kRoundMagic &&
+        zp_magic_code(mx, sf, zf, rcp) <= kRoundMagic + (float)qlev)) {
     quant_zp32(v, B, dst, dq);
     return;
   }
@@ -364,8 +363,8 @@ __device__ __forceinline__ void block32_zp_x2(const uint32_t (&raw)[32], float2 
     sf[c] = __half2float(s16[c]);
     zf[c] = __half2float(z16[c]);
     rcp[c] = sf[c] == 0.f ? 0.f : __frcp_rn(sf[c]);
-    ok = ok && zp_magic_code<B>(lo, sf[c], zf[c], rcp[c]) >= kRoundMagic &&
-         zp_magic_code<B>(hi, sf[c], zf[c], rcp[c]) <= kRoundMagic + (float)qlev;
+    ok = ok && zp_magic_code(lo, sf[c], zf[c], rcp[c]) >= kRoundMagic &&
+         zp_magic_code(hi, sf[c], zf[c], rcp[c]) <= kRoundMagic + (float)qlev;
   }
   if (!ok) {
 #pragma unroll 1
