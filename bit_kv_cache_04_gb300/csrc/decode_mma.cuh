@@ -33,8 +33,9 @@
 // is channel 32s + 4(r & 7) + 2e + (r >> 3).
 //
 // Work split: CTA = 4 warps on one (layer, sequence, kv head, token split);
-// each warp streams its own groups through a 2-stage cp.async ring and keeps
-// its own online softmax; warps merge in shared memory and splits merge in
+// each warp streams its own groups through a ring of 2 or 3 shared-memory
+// stages filled by 1-D bulk copies (TMA engine) that complete on per-stage
+// mbarriers, and keeps its own online softmax; warps merge in shared memory and splits merge in
 // the workspace (the last CTA to take a ticket combines; nobody waits).
 #pragma once
 

@@ -24,7 +24,6 @@ bool step_fused_kivi(const DecodeArgs& a, cudaStream_t st, bool dry, cudaError_t
   if (k.zp) return run(Cfg<128, 1, T_<128, KF_CH4, 32, VF_T4, 32, true>, T_<128, KF_CH4, 32, VF_T4, 32, true>, false,
                            false>{}, S1{});
   return run(Cfg<128, 1, T_<128, KF_CH4, 32, VF_T4, 32>, T_<128, KF_CH4, 32, VF_T4, 32>, false, false>{}, S1{});
-  return false;
 }
 
 }  // namespace kvq

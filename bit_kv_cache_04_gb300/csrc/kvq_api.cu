@@ -237,8 +237,32 @@ int64_t fmt_bytes(const kvq_fmt& f, int64_t n_tokens, int D, bool zp) {
   return (n_tokens / f.group) * D * bb;
 }
 
+// Streaming multiprocessors of the current device, read once per device
+// from its attributes.  Without a usable device (host-only sizing queries)
+// the count of a GB300 (152) stands in, so sizes stay deterministic there.
+int sm_count() {
+  constexpr int kMaxDev = 64, kDefaultSms = 152;
+  static std::mutex mu;
+  static int cached[kMaxDev] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    (void)cudaGetLastError();
+    return kDefaultSms;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+      (void)cudaGetLastError();
+      n = kDefaultSms;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 // Token splits per (layer, sequence, kv head): the count whose grid fills
-// whole waves of resident CTAs best (152 SMs x 4 CTAs for D = 128, x 2 for
+// whole waves of resident CTAs best (SMs x 4 CTAs for D = 128, x 2 for
 // D = 256), with at least 8 tiles per split and no more growth once the grid
 // holds 8 waves.
 constexpr int64_t kMinTilesPerSplit = 8, kMinTilesPerSplitRotated = 48;
@@ -246,7 +270,7 @@ constexpr int64_t kMinTilesPerSplit = 8, kMinTilesPerSplitRotated = 48;
 int splits_for(const kvq_config* c, int n_layers) {
   const int64_t units = (int64_t)n_layers * c->batch * c->H_kv;
   const int64_t tiles = (c->max_T + kTile - 1) / kTile + 2;
-  const int64_t resident = 152 * (c->D == 128 ? 4 : 2);
+  const int64_t resident = (int64_t)sm_count() * (c->D == 128 ? 4 : 2);
   // every split keeps at least a minimum of tiles of capacity.  Rotated
   // layouts set a higher one: their per-block setup also rotates the query
   // and un-rotates the output (a ragged batch of 2K-8K-token sequences

@@ -9,29 +9,15 @@ from __future__ import annotations
 
 import ctypes
 import os
-from dataclasses import dataclass, field, fields
+from dataclasses import fields
 from typing import Optional, Tuple
+
+from .config import (AXIS_CHANNEL, AXIS_TOKEN, DEV_CAPACITY, DEV_LENGTH, DEV_PAGE, DEV_RANGE,  # noqa: F401
+                     DEV_STALL, DT_BF16, DT_F16, K_PRE_ROPE, ROTATE_K, ROTATE_V, TBQ4_K, TBQ4_V, ZP_K, ZP_V,
+                     Config, Fmt)
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libkvq.so")
-
-AXIS_TOKEN = 0
-AXIS_CHANNEL = 1
-ROTATE_K = 1
-ROTATE_V = 2
-K_PRE_ROPE = 4
-TBQ4_K = 8
-TBQ4_V = 16
-ZP_K = 32
-ZP_V = 64
-DT_F16 = 0
-DT_BF16 = 1
-
-DEV_CAPACITY = 1
-DEV_PAGE = 2
-DEV_RANGE = 4
-DEV_LENGTH = 8
-DEV_STALL = 16
 
 STATUS_NAMES = {0: "OK", 1: "ERR_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_CUDA", 4: "ERR_CAPACITY", 5: "ERR_WORKSPACE"}
 
@@ -63,48 +49,18 @@ class _Cache(ctypes.Structure):
                                                   "block_table")]
 
 
-@dataclass(frozen=True)
-class Fmt:
-    bits: int
-    group: int
-    axis: int = AXIS_TOKEN
-
-
-@dataclass
-class Config:
-    """Mirror of kvq_config."""
-
-    L: int
-    H_kv: int
-    H_q: int
-    D: int
-    batch: int
-    max_T: int
-    in_dtype: int = DT_F16
-    k_fmt: Fmt = Fmt(4, 32)
-    v_fmt: Fmt = Fmt(4, 32)
-    k_cold: Optional[Fmt] = None
-    v_cold: Optional[Fmt] = None
-    hot_window: int = 0
-    residual_window: int = 0
-    flags: int = 0
-    rope_theta: float = 10000.0
-    sign_seed: int = 0
-    page_tokens: int = 0
-    n_pages: int = 0
-    max_pages_per_seq: int = 0
-
-    def to_c(self) -> _Config:
-        c = _Config()
-        for f in fields(self):
-            v = getattr(self, f.name)
-            if isinstance(v, Fmt) or (v is None and f.name in ("k_cold", "v_cold")):
-                v = v or Fmt(0, 0, 0)
-                setattr(c, f.name, _Fmt(v.bits, v.group, v.axis))
-            else:
-                setattr(c, f.name, v)
-        c.reserved = 0
-        return c
+def _to_c(cfg: Config) -> _Config:
+    """kvq_config of a Config."""
+    c = _Config()
+    for f in fields(cfg):
+        v = getattr(cfg, f.name)
+        if isinstance(v, Fmt) or (v is None and f.name in ("k_cold", "v_cold")):
+            v = v or Fmt(0, 0, 0)
+            setattr(c, f.name, _Fmt(v.bits, v.group, v.axis))
+        else:
+            setattr(c, f.name, v)
+    c.reserved = 0
+    return c
 
 
 def _load():
@@ -167,7 +123,7 @@ def kvq_version() -> str:
 
 
 def kvq_validate_config(cfg: Config) -> None:
-    _check(LIB.kvq_validate_config(ctypes.byref(cfg.to_c())))
+    _check(LIB.kvq_validate_config(ctypes.byref(_to_c(cfg))))
 
 
 def kvq_block_bytes(bits: int, group: int) -> int:
@@ -178,19 +134,19 @@ def kvq_block_bytes(bits: int, group: int) -> int:
 
 def kvq_bytes_per_token(cfg: Config) -> int:
     out = ctypes.c_int64()
-    _check(LIB.kvq_bytes_per_token(ctypes.byref(cfg.to_c()), ctypes.byref(out)))
+    _check(LIB.kvq_bytes_per_token(ctypes.byref(_to_c(cfg)), ctypes.byref(out)))
     return out.value
 
 
 def kvq_cache_bytes(cfg: Config, T: int) -> int:
     out = ctypes.c_int64()
-    _check(LIB.kvq_cache_bytes(ctypes.byref(cfg.to_c()), T, ctypes.byref(out)))
+    _check(LIB.kvq_cache_bytes(ctypes.byref(_to_c(cfg)), T, ctypes.byref(out)))
     return out.value
 
 
 def kvq_buffer_sizes(cfg: Config) -> Tuple[int, ...]:
     arr = (ctypes.c_size_t * 6)()
-    _check(LIB.kvq_buffer_sizes(ctypes.byref(cfg.to_c()), arr))
+    _check(LIB.kvq_buffer_sizes(ctypes.byref(_to_c(cfg)), arr))
     return tuple(arr)
 
 
@@ -205,26 +161,26 @@ def kvq_tbq4_codebook():
 def kvq_launch_counts(cfg: Config):
     """(kernel launches of one kvq_append call, of one kvq_decode_attention call)."""
     a, d = ctypes.c_int32(), ctypes.c_int32()
-    _check(LIB.kvq_launch_counts(ctypes.byref(cfg.to_c()), ctypes.byref(a), ctypes.byref(d)))
+    _check(LIB.kvq_launch_counts(ctypes.byref(_to_c(cfg)), ctypes.byref(a), ctypes.byref(d)))
     return a.value, d.value
 
 
 def kvq_step_launches(cfg: Config) -> int:
     """Kernel launches of one kvq_decode_step call (1 when fused)."""
     n = ctypes.c_int32()
-    _check(LIB.kvq_step_launches(ctypes.byref(cfg.to_c()), ctypes.byref(n)))
+    _check(LIB.kvq_step_launches(ctypes.byref(_to_c(cfg)), ctypes.byref(n)))
     return n.value
 
 
 def kvq_workspace_bytes(cfg: Config) -> int:
     out = ctypes.c_size_t()
-    _check(LIB.kvq_workspace_bytes(ctypes.byref(cfg.to_c()), ctypes.byref(out)))
+    _check(LIB.kvq_workspace_bytes(ctypes.byref(_to_c(cfg)), ctypes.byref(out)))
     return out.value
 
 
 def kvq_decode_splits(cfg: Config, n_layers: int) -> int:
     out = ctypes.c_int32()
-    _check(LIB.kvq_decode_splits(ctypes.byref(cfg.to_c()), n_layers, ctypes.byref(out)))
+    _check(LIB.kvq_decode_splits(ctypes.byref(_to_c(cfg)), n_layers, ctypes.byref(out)))
     return out.value
 
 
@@ -250,7 +206,7 @@ class KVCache:
         import torch
 
         self.cfg = cfg
-        self.c_cfg = cfg.to_c()
+        self.c_cfg = _to_c(cfg)
         self.device = torch.device(device)
         sizes = kvq_buffer_sizes(cfg)
         self.buffers = {}

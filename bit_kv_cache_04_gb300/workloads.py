@@ -25,8 +25,8 @@ from typing import List, Optional
 
 import torch
 
-from .kvq import (AXIS_CHANNEL, AXIS_TOKEN, DT_BF16, DT_F16, K_PRE_ROPE, ROTATE_K, ROTATE_V, TBQ4_K, TBQ4_V, ZP_K, ZP_V,
-                  Config, Fmt)
+from .config import (AXIS_CHANNEL, AXIS_TOKEN, DT_BF16, DT_F16, K_PRE_ROPE, ROTATE_K, ROTATE_V, TBQ4_K, TBQ4_V,
+                     ZP_K, ZP_V, Config, Fmt)
 
 SIGN_SEED = 0x5EED5EED
 

@@ -132,7 +132,9 @@ enum {
    * s, the fp16 zero z (the block minimum), then codes c in [0, 2^b - 1] in the
    * usual bit fields, x = c s + z: 2 more bytes per block (20 B / 32 values
    * at 4 bits, 12 B / 32 at 2 bits).  Needs 4- or 2-bit
-   * blocks of 32 values, no rotation.  Decode takes the generic kernel. */
+   * blocks of 32 values, no rotation.  The tensor-core decode reads them when
+   * both tensors are asymmetric (the zero adds one term per block to the
+   * scores or the output); other mixes take the generic decode kernel. */
   KVQ_ZP_K = 1u << 5,
   KVQ_ZP_V = 1u << 6
 };
@@ -159,7 +161,8 @@ typedef struct {
   kvq_fmt k_cold, v_cold; /* cold tier when hot_window > 0 (same axis and group, fewer bits) */
   int32_t hot_window;      /* W: tokens kept in the hot tier (multiple of Gamma), 0 = one tier */
   int32_t residual_window; /* R: tokens kept in the 16-bit window, 0 allowed */
-  uint32_t flags;          /* KVQ_ROTATE_K | KVQ_ROTATE_V | KVQ_K_PRE_ROPE */
+  uint32_t flags;          /* OR of KVQ_ROTATE_K, KVQ_ROTATE_V, KVQ_K_PRE_ROPE, KVQ_TBQ4_K,
+                              KVQ_TBQ4_V, KVQ_ZP_K, KVQ_ZP_V (see the flags above) */
   float rope_theta;        /* RoPE base (KVQ_K_PRE_ROPE), e.g. 10000 */
   uint64_t sign_seed;      /* 0: plain Sylvester transform; else SplitMix64 sign vectors */
   int32_t page_tokens;     /* 0 = contiguous; 16 = paged main tier */
@@ -215,7 +218,12 @@ KVQ_API kvq_status kvq_workspace_bytes(const kvq_config* cfg, size_t* bytes);
  * it; later calls keep the tickets at zero themselves. */
 KVQ_API kvq_status kvq_workspace_init(const kvq_config* cfg, void* workspace, size_t ws_bytes, void* stream);
 
-/* Quantize-on-append for layers [layer0, layer0 + n_layers).
+/* Quantize-on-append for layers [layer0, layer0 + n_layers): every new
+ * token is rotated (flags), scaled per block and coded into the layout above
+ * (trefon.com, format table of "Przyklad: model 27B przy 262K"; per-channel
+ * keys and per-token values as troisinh.com "Tai sao Key va Value lai khac
+ * nhau?"; the recent window kept unquantized as nalar.dev "Evaluasi harus
+ * memisahkan...").
  *  k, v:     [n_layers][total_new][H_kv][D] in_dtype, device, 16-byte
  *            aligned (KVQ_ERR_ARG otherwise); sequences back
  *            to back in batch order (post-RoPE keys, or pre-RoPE with
@@ -239,7 +247,11 @@ KVQ_API kvq_status kvq_commit_lengths(const kvq_config* cfg, const int32_t* cu_n
 
 /* Decode attention of one query token per sequence, for layers
  * [layer0, layer0 + n_layers) (independent per-layer queries; n_layers > 1
- * only saves launches).
+ * only saves launches), read straight from the packed blocks: scores
+ * s_t = q.k_t / sqrt(D) and output sum_t p_t v_t as nalar.dev "Error pada
+ * key mengubah input softmax" and "Error pada value masuk setelah attention
+ * probability" define them; rotated blocks are read in the rotated domain
+ * (trefon.com, "Jak 4-bitowemu cache to uchodzi: najpierw obrot").
  *  q:        [n_layers][batch][H_q][D] in_dtype, device, post-RoPE.
  *  seq_lens: [batch] int32 device, tokens currently cached.
  *  out:      [n_layers][batch][H_q][D] fp32, device:
@@ -281,8 +293,10 @@ KVQ_API kvq_status kvq_step_launches(const kvq_config* cfg, int32_t* launches);
 KVQ_API kvq_status kvq_decode_splits(const kvq_config* cfg, int32_t n_layers, int32_t* splits);
 
 /* Dequantizes tokens [t0, t1) of (layer, seq) to fp32 k_out, v_out
- * [t1 - t0][H_kv][D] (device) in the original domain: rotation undone, keys
- * as stored (pre-RoPE when flagged).  seq_lens as for decode; a range beyond
+ * [t1 - t0][H_kv][D] (device) in the original domain: x = code * scale
+ * (+ zero) per block (trefon.com, format table), rotation undone, keys as
+ * stored (pre-RoPE when flagged).  k_out and v_out hold at least
+ * (t1 - t0) * H_kv * D floats each; the caller owns them.  seq_lens as for decode; a range beyond
  * the current length sets KVQ_DEV_RANGE and writes nothing. */
 KVQ_API kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_cache* cache, int32_t layer, int32_t seq,
                           int32_t t0, int32_t t1, const int32_t* seq_lens, float* k_out, float* v_out,
