@@ -200,9 +200,9 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // Bounded wait for phase `parity` of `bar`; false when the limit ran out
 // (the same answer on every lane of the warp).
 constexpr int kSpinLimit = 1 << 22;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int limit = kSpinLimit) {
   bool ok = false;
-  for (int i = 0; i < kSpinLimit && !ok; ++i) ok = mbar_test(bar, parity);
+  for (int i = 0; i < limit && !ok; ++i) ok = mbar_test(bar, parity);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -943,6 +943,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   __shared__ uint32_t bad_page;
   constexpr int kStages = C::STAGES;
   __shared__ uint64_t mbar[kWarps * kMaxStages];
+  __shared__ uint64_t never_bar;  // no thread ever arrives on it (failure-detection test mode)
   __shared__ int is_last;
   __shared__ int pf_page[kWarps][2][2];  // paged: next tile's page ids per warp, by issue parity
 
@@ -984,6 +985,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     for (int e = tid; e < g * D; e += kThreadsMma) qf[e] = in_to_f32(a.q[qrow * D + e], lo.dtype);
     if (tid == 0) bad_page = 0;
     if (tid < kWarps * kStages) mbar_init(mbar + tid, 1);
+    if (tid == kThreadsMma - 1) mbar_init(&never_bar, 1);
     fence_mbar_init();
     __syncthreads();
     if (lo.flags & KVQ_ROTATE_K) {
@@ -1178,9 +1180,16 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     const int tile = first + kWarps * it;
     if (tile >= te) break;
     issue(tile + kWarps * (kStages - 1), (it + kStages - 1) % kStages);
-    if (tile < n_c + n_m && !mbar_wait(mbar + warp * kStages + it % kStages, (it / kStages) & 1)) {
-      stall_it = it;
-      break;
+    if (tile < n_c + n_m) {
+      // test mode: the first wait is on a barrier nothing completes, bounded
+      // by a.stall_polls polls, so the stall path below runs for real
+      const bool landed = (a.stall_polls > 0 && it == 0)
+                              ? mbar_wait(&never_bar, 0, a.stall_polls)
+                              : mbar_wait(mbar + warp * kStages + it % kStages, (it / kStages) & 1);
+      if (!landed) {
+        stall_it = it;
+        break;
+      }
     }
 
     float S[2][NT][4];

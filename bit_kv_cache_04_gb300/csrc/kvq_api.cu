@@ -4,6 +4,7 @@
 #include <stdio.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -569,6 +570,9 @@ kvq_status kvq_commit_lengths(const kvq_config* cfg, const int32_t* cu_new, int3
   return ok();
 }
 
+// Failure-detection test mode of the tensor-core decode (kvq_test_force_stall).
+std::atomic<int> g_stall_polls{0};
+
 // Checks the decode arguments and fills *a (everything but the step).
 static kvq_status prep_decode(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0, int32_t n_layers,
                        const void* q, const int32_t* seq_lens, float* out, int32_t num_splits, void* workspace,
@@ -598,6 +602,7 @@ static kvq_status prep_decode(const kvq_config* cfg, const kvq_cache* cache, int
   a->partials = (float*)((char*)workspace + w.partials);
   a->rope = (const float2*)((char*)workspace + w.rope);
   a->rope_base_rows = w.rope_base_rows;
+  a->stall_polls = g_stall_polls.load();
   return KVQ_OK;
 }
 
@@ -686,6 +691,12 @@ kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_cache* cache, int32_t
   a.status = (uint32_t*)((char*)workspace + w.status);
   cudaError_t e = launch_dequantize(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "dequantize kernel");
+  return ok();
+}
+
+kvq_status kvq_test_force_stall(int32_t polls) {
+  if (polls < 0 || polls > (1 << 20)) return fail(KVQ_ERR_ARG, "polls=%d not in [0, 2^20]", polls);
+  g_stall_polls.store(polls);
   return ok();
 }
 
@@ -791,6 +802,7 @@ extern "C" kvq_status kvq_decode_attention_static(const kvq_config* cfg, const k
   a.partials = (float*)((char*)base + off_partials);
   a.rope = (const float2*)((char*)base + off_rope);
   a.rope_base_rows = rope_rows;
+  a.stall_polls = g_stall_polls.load();
   e = launch_decode(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
   return ok();

@@ -188,6 +188,7 @@ struct DecodeArgs {
   const float2* rope;  // base rows then offsets
   int rope_base_rows;
   int len_add;      // the attended length is seq_lens[b] + len_add (1 in a decode step)
+  int stall_polls;  // > 0: failure-detection test mode (kvq_test_force_stall)
   AppendArgs step;  // fused decode step: the append of the new token (step.k == nullptr otherwise)
 };
 

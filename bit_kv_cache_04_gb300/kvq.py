@@ -90,6 +90,7 @@ def _load():
         "kvq_tbq4_codebook": ([P(ctypes.c_float), P(ctypes.c_float)], ctypes.c_int),
         "kvq_decode_attention_static": ([cfgp, cachep, i32, i32, vp, vp, vp, i32, vp], ctypes.c_int),
         "kvq_dequantize": ([cfgp, cachep, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "kvq_test_force_stall": ([i32], ctypes.c_int),
         "kvq_read_device_status": ([vp, P(u32), vp], ctypes.c_int),
         "kvq_clear_device_status": ([vp, vp], ctypes.c_int),
     }
@@ -107,7 +108,7 @@ EXPORTED = ("kvq_version", "kvq_last_error", "kvq_validate_config", "kvq_block_b
             "kvq_cache_bytes", "kvq_buffer_sizes", "kvq_workspace_bytes", "kvq_workspace_init", "kvq_append",
             "kvq_commit_lengths", "kvq_decode_attention", "kvq_decode_splits", "kvq_decode_attention_static",
             "kvq_dequantize", "kvq_launch_counts", "kvq_tbq4_codebook", "kvq_decode_step", "kvq_step_launches",
-            "kvq_read_device_status", "kvq_clear_device_status")
+            "kvq_read_device_status", "kvq_clear_device_status", "kvq_test_force_stall")
 
 
 def _check(st: int):
@@ -182,6 +183,11 @@ def kvq_decode_splits(cfg: Config, n_layers: int) -> int:
     out = ctypes.c_int32()
     _check(LIB.kvq_decode_splits(ctypes.byref(_to_c(cfg)), n_layers, ctypes.byref(out)))
     return out.value
+
+
+def kvq_test_force_stall(polls: int) -> None:
+    """Failure-detection test mode of the tensor-core decode (0 = off)."""
+    _check(LIB.kvq_test_force_stall(polls))
 
 
 def _ptr(t) -> Optional[int]:

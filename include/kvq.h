@@ -351,6 +351,17 @@ KVQ_API kvq_status kvq_launch_counts(const kvq_config* cfg, int32_t* append_laun
  * order.  No device work; the tables are computed once per process. */
 KVQ_API kvq_status kvq_tbq4_codebook(float centroids[16], float thresholds[15]);
 
+/* Testing hook of the failure-detection path; no counterpart on the pages.
+ * While polls > 0, every tensor-core decode launch (kvq_decode_attention,
+ * kvq_decode_step, kvq_decode_attention_static) makes its warps' first copy
+ * wait on a shared-memory barrier that nothing ever completes, bounded by
+ * `polls` polls: the wait runs out, KVQ_DEV_STALL is set, the warp waits
+ * (with the normal bound) for its bulk copies still in flight and the
+ * kernel finishes; that call's outputs are undefined.  polls = 0 (the
+ * default) turns it off.  Process-wide; polls outside [0, 2^20] give
+ * KVQ_ERR_ARG.  Not for production use. */
+KVQ_API kvq_status kvq_test_force_stall(int32_t polls);
+
 /* Synchronizes `stream` and reads the device status word (KVQ_DEV_* bits). */
 KVQ_API kvq_status kvq_read_device_status(const void* workspace, uint32_t* bits, void* stream);
 

@@ -517,6 +517,24 @@ def tbq4_quantize(y: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
     return n16, idx
 
 
+def tbq4_quantize_f64norm(y: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """TBQ4 blocks with the norm read as its plain definition (trefon.com,
+    "Jak 4-bitowemu cache to uchodzi: najpierw obrot": one fp16 L2 norm per
+    block): n16 = fp16(min(sqrt(sum y_i^2), 65504)) with the sum and the root
+    in fp64, then the same fp32 quotient and nearest-entry index as
+    tbq4_quantize.  The format fixes no summation order; this variant shows
+    how far the indices move when the order changes."""
+    y = np.asarray(y, np.float32)
+    _, thr = tbq4_codebook()
+    S = np.sum(y.astype(np.float64) ** 2, axis=-1)
+    n16 = np.minimum(np.sqrt(S), 65504.0).astype(np.float16)
+    nf = n16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        u = np.where(nf > 0, np.divide(y, nf, dtype=np.float32), np.float32(0.0))
+    idx = (u[..., None] > thr).sum(axis=-1).astype(np.uint8)
+    return n16, idx
+
+
 def tbq4_dequantize_f64(n16: np.ndarray, idx: np.ndarray) -> np.ndarray:
     """table entry (an fp16 value) * norm, exact in fp64."""
     cent, _ = tbq4_codebook()

@@ -215,3 +215,11 @@ def test_step_launches():
     for name in ("q4_0_mha_1k", "ctx262k_tbq4", "llama2_7b_kivi2_zp"):
         a, d = K.kvq_launch_counts(W.make(name).cfg)
         assert K.kvq_step_launches(W.make(name).cfg) == a + d, name
+
+
+def test_stall_test_mode_bounds():
+    # the failure-detection test hook takes 0 (off) .. 2^20 polls; nothing launches here
+    for bad in (-1, (1 << 20) + 1):
+        with pytest.raises(K.KvqError):
+            K.kvq_test_force_stall(bad)
+    K.kvq_test_force_stall(0)

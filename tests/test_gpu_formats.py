@@ -284,6 +284,21 @@ def test_tbq4_bytes_decode_and_dequantize(case):
             pytest.fail(f"{name} {n}: bytes differ (codes {diff}/{total}, max |dc| {maxd}, scales {sdiff})")
     if edge:
         return
+    if R == 0:
+        # the GPU's indices against the plain reading of the norm (fp64 sum,
+        # no summation order): within 1 on at most 1e-4 of the elements
+        signs = O.hadamard_signs(seed)
+        total = differ = 0
+        for name_, xs in (("k_main", ks), ("v_main", vs)):
+            for b, T in enumerate(LENGTHS):
+                rows = np.moveaxis(got[name_][0, b, :, :T], 0, 1).reshape(T, cfg.H_kv, D // 128, 66)
+                gi = O.decode_blocks(rows, 4, 128)[1].astype(np.int64) + 8
+                y = O.rotate_f32(O.input_to_f32(raw16(xs[b]), dtype), *signs).reshape(T, cfg.H_kv, D // 128, 128)
+                d = np.abs(gi - O.tbq4_quantize_f64norm(y)[1].astype(np.int64))
+                assert d.max() <= 1, (name, name_, b)
+                total += d.size
+                differ += int(np.count_nonzero(d))
+        assert differ <= 1e-4 * total, (name, differ, total)
     # decode over the GPU's own bytes, against fp64 attention
     q = torch.randn((1, cfg.batch, cfg.H_q, D), generator=gen).to(dt).cuda()
     out = torch.full((1, cfg.batch, cfg.H_q, D), float("nan"), dtype=torch.float32, device="cuda")

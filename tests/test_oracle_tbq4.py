@@ -152,3 +152,37 @@ def test_thresholds_fall_in_distinct_eighth_octave_bins():
     vals += list(np.random.default_rng(3).standard_normal(2000).astype(np.float32) / np.float32(11.3))
     for u in vals:
         assert lookup(u) == int(np.sum(t < np.float32(u))), u
+
+
+def test_norm_summation_order_moves_few_indices():
+    """The format gives one fp16 L2 norm per block and no order for its sum.
+    The oracle sums y^2 in four index-order runs of 32, (p0 + p1) + (p2 + p3);
+    the plain definition sums in fp64.  On the 262K-context recipe (bf16
+    N(0, 1) keys and values, 1% outlier channels x10, randomized Hadamard-128)
+    the two readings give indices that differ by at most 1 on at most 1e-4 of
+    the elements, and norms at most one fp16 ulp apart: the bit-exact TBQ4
+    parity does not hinge on the partitioned order."""
+    import torch
+
+    from bit_kv_cache_04_gb300 import workloads as W
+
+    w = W.make("ctx262k_tbq4", extra_tokens=0).scaled(L=1, T=4096)
+    k, v = W.kv_tokens(w, 0, 0, 0, 4096, "cpu", 0)
+    d1, d2 = O.hadamard_signs(w.cfg.sign_seed)
+    total = differ = 0
+    for x in (k, v):
+        raw = x.contiguous().view(torch.int16).numpy().view(np.uint16)
+        y = O.rotate_f32(O.input_to_f32(raw, w.cfg.in_dtype).reshape(-1, 128), d1, d2)
+        n1, i1 = O.tbq4_quantize(y)
+        n2, i2 = O.tbq4_quantize_f64norm(y)
+        d = np.abs(i1.astype(np.int64) - i2.astype(np.int64))
+        assert d.max() <= 1
+        total += d.size
+        differ += int(np.count_nonzero(d))
+        ulp = np.abs(n1.view(np.int16).astype(np.int64) - n2.view(np.int16).astype(np.int64))
+        assert ulp.max() <= 1 and np.count_nonzero(ulp) <= 1e-4 * ulp.size
+    assert differ <= 1e-4 * total, (differ, total)
+    # the variant is the plain definition: its norm is the fp64 L2 norm rounded once
+    y = np.random.default_rng(9).standard_normal((64, 128)).astype(np.float32)
+    n2, _ = O.tbq4_quantize_f64norm(y)
+    assert np.array_equal(n2, np.sqrt((y.astype(np.float64) ** 2).sum(-1)).astype(np.float16))
