@@ -12,6 +12,7 @@
 // the output back once).  Scores follow nalar.dev "Kuantisasi KV Cache...":
 // s_i = q.k_i / sqrt(D), output = sum_i p_i v_i.
 #include "block_codec.cuh"
+#include "split_combine.cuh"
 
 namespace kvq {
 namespace {
@@ -245,16 +246,17 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
       if (hh < g) obuf[hh * D + d] = l_s[hh] > 0.0f ? acc[r] / l_s[hh] : 0.0f;
     }
   } else {
-    float* part = a.partials + (unit * a.splits + split) * (int64_t)g * (D + 2);
+    constexpr int PR = part_row(D);
+    float* part = a.partials + (unit * a.splits + split) * (int64_t)g * PR;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int pidx = tid + r * kThreads;
       const int hh = pidx / D, d = pidx % D;
-      if (hh < g) part[hh * (D + 2) + 2 + d] = acc[r];
+      if (hh < g) part[hh * PR + d] = acc[r];
     }
     if (tid < g) {
-      part[tid * (D + 2)] = m_s[tid];
-      part[tid * (D + 2) + 1] = l_s[tid];
+      part[tid * PR + D] = m_s[tid];
+      part[tid * PR + D + 1] = l_s[tid];
     }
     __threadfence();
     __syncthreads();
@@ -265,22 +267,9 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) 
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    const float* base = a.partials + unit * a.splits * (int64_t)g * (D + 2);
-    for (int e = tid; e < g * D; e += kThreads) {
-      const int hh = e / D, d = e % D;
-      float M = -INFINITY;
-      for (int s = 0; s < a.splits; ++s) M = fmaxf(M, __ldcg(base + ((int64_t)s * g + hh) * (D + 2)));
-      float L = 0.0f, O = 0.0f;
-      if (M != -INFINITY) {
-        for (int s = 0; s < a.splits; ++s) {
-          const float* p = base + ((int64_t)s * g + hh) * (D + 2);
-          const float w = exp2f(__ldcg(p) - M);
-          L += w * __ldcg(p + 1);
-          O += w * __ldcg(p + 2 + d);
-        }
-      }
-      obuf[hh * D + d] = L > 0.0f ? O / L : 0.0f;
-    }
+    // the V tile is dead here: the merge weights use it
+    static_assert(kTile * LD >= kMaxGqa * kMaxSplits, "merge weights fit in the V tile");
+    combine_splits<D, kThreads>(a.partials + unit * a.splits * (int64_t)g * PR, a.splits, g, obuf, vs, l_s);
     if (tid == 0) a.tickets[unit] = 0;
   }
   __syncthreads();

@@ -40,6 +40,7 @@
 #pragma once
 
 #include "append_generic.cuh"
+#include "split_combine.cuh"
 
 namespace kvq {
 
@@ -1412,7 +1413,8 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   if (tid == 0 && bad_page) atomicOr(a.status, KVQ_DEV_PAGE);
   // CTA partial per head: M = max_w m_w, L = sum_w 2^(m_w - M) l_w, O likewise
   const int64_t unit = ((int64_t)li * lo.B + seq) * lo.H + h;
-  float* part = a.partials + (unit * a.splits + split) * (int64_t)g * (D + 2);
+  constexpr int PR = part_row(D);
+  float* part = a.partials + (unit * a.splits + split) * (int64_t)g * PR;
   for (int e = tid; e < g * D; e += kThreadsMma) {
     const int hh = e / D, d = e % D;
     float M = -INFINITY;
@@ -1428,10 +1430,10 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     if (a.splits == 1) {
       obuf[e] = L > 0.f ? O / L : 0.f;
     } else {
-      part[hh * (D + 2) + 2 + d] = O;
+      part[hh * PR + d] = O;
       if (d == 0) {
-        part[hh * (D + 2)] = M;
-        part[hh * (D + 2) + 1] = L;
+        part[hh * PR + D] = M;
+        part[hh * PR + D + 1] = L;
       }
     }
   }
@@ -1442,22 +1444,9 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    const float* base = a.partials + unit * a.splits * (int64_t)g * (D + 2);
-    for (int e = tid; e < g * D; e += kThreadsMma) {
-      const int hh = e / D, d = e % D;
-      float M = -INFINITY;
-      for (int sp = 0; sp < a.splits; ++sp) M = fmaxf(M, __ldcg(base + ((int64_t)sp * g + hh) * (D + 2)));
-      float L = 0.f, O = 0.f;
-      if (M != -INFINITY) {
-        for (int sp = 0; sp < a.splits; ++sp) {
-          const float* pp = base + ((int64_t)sp * g + hh) * (D + 2);
-          const float w = exp2f(__ldcg(pp) - M);
-          L += w * __ldcg(pp + 1);
-          O += w * __ldcg(pp + 2 + d);
-        }
-      }
-      obuf[e] = L > 0.f ? O / L : 0.f;
-    }
+    // the per-warp partials in wo are dead here: the merge weights reuse them
+    static_assert(kWarps * kMaxGqa * D >= kMaxGqa * kMaxSplits, "merge weights fit in the warp partials");
+    combine_splits<D, kThreadsMma>(a.partials + unit * a.splits * (int64_t)g * PR, a.splits, g, obuf, wo, wm);
     if (tid == 0) a.tickets[unit] = 0;
   }
   __syncthreads();

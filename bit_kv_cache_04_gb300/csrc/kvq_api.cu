@@ -11,6 +11,7 @@
 #include <string>
 
 #include "kvq_internal.cuh"
+#include "split_combine.cuh"
 #include "tbq4_bins.cuh"
 
 using namespace kvq;
@@ -323,7 +324,7 @@ WsLayout ws_layout(const kvq_config* c) {
   int64_t one = (int64_t)c->batch * c->H_kv * 64;
   if (one > mp) mp = one;
   w.max_partials = (int)mp;
-  off = align_up(off + sizeof(float) * (size_t)mp * g * (c->D + 2));
+  off = align_up(off + sizeof(float) * (size_t)mp * g * part_row(c->D));
   w.total = off;
   return w;
 }
@@ -776,7 +777,7 @@ extern "C" kvq_status kvq_decode_attention_static(const kvq_config* cfg, const k
     off = align_up(off + sizeof(float2) * (size_t)(rope_rows + 2 * kTile) * (cfg->D / 2));
   }
   const size_t off_partials = off;
-  if (splits > 1) off = align_up(off + sizeof(float) * units * splits * g * (cfg->D + 2));
+  if (splits > 1) off = align_up(off + sizeof(float) * units * splits * g * part_row(cfg->D));
   if (off > (size_t)KVQ_STATIC_SCRATCH_BYTES)
     return fail(KVQ_ERR_WORKSPACE, "this call needs %zu B of scratch; the static scratch holds %u B", off,
                 (unsigned)KVQ_STATIC_SCRATCH_BYTES);

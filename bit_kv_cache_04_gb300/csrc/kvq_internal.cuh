@@ -68,7 +68,7 @@ struct WsLayout {
   size_t status;    // uint32 status word
   size_t tickets;   // uint32 per decode unit
   size_t rope;      // float2 base[n_base][D/2] then off[kTile][D/2]
-  size_t partials;  // float per (unit, split): g * (D + 2)
+  size_t partials;  // float per (unit, split): g * part_row(D)
   size_t total;
   int max_units;
   int max_partials;  // unit-split pairs
