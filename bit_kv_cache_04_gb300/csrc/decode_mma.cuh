@@ -407,10 +407,23 @@ __device__ __forceinline__ void online_softmax(WarpState<C>& ws, float (&S)[2][C
         if (4 * gq + k >= n_valid) s[k] = -INFINITY;
         mx = fmaxf(mx, s[k]);
       }
+      const int si = nt * C::J + j;
+      if (__all_sync(0xffffffffu, mx <= ws.m[si])) {
+        // no score above the running maximum: it stays, so the update is
+        // p = 2^(s - m), l += sum p (what the full update below gives when
+        // its maximum does not move), without the cross-lane reduction
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          p[nt][j][k] = exp2f(s[k] - ws.m[si]);
+          sum += p[nt][j][k];
+        }
+        ws.l[si] += sum;
+        continue;
+      }
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      const int si = nt * C::J + j;
       const float m_new = fmaxf(ws.m[si], mx);
       const float alpha = exp2f(ws.m[si] - m_new);
       ws.m[si] = m_new;
@@ -471,6 +484,7 @@ struct Ctx {
   const float* qz;        // [4 NT][D]: fp32 query by head, zero past g (asymmetric K)
   const float2* rope_base;
   const float4* rope_frag;  // [KC/2][4 tokens k][2 pairs][32 lanes]: (cos, cos, sin, sin) of R(j), lane's channels
+  const uint4* rope_tab;    // [KC/2][4 tokens k][32 lanes][2]: fp16 hi / lo cos and sin of R(j), lane's channel pairs
   uint32_t lut[4];          // TBQ4 table magnitudes: low bytes (2 words), high bytes (2 words)
 };
 
@@ -494,6 +508,36 @@ __device__ __forceinline__ void rope_query_pair(const Ctx<C>& cx, const float2* 
     qu[nt][0] = pack_h2(split_part(u0, cx.lo_part), split_part(u1, cx.lo_part));
     qu[nt][1] = pack_h2(split_part(u2, cx.lo_part), split_part(u3, cx.lo_part));
   }
+}
+
+// The query turned by -t0 (pre-RoPE keys), fp32, for the k-chunk pair (kcp,
+// kcp + KC/2): l[nt] = lower channels (c, c + 4, c + 1, c + 5), u[nt] their
+// partners c + D/2, ..., for the lane's head of n-tile nt.
+template <class C>
+__device__ __forceinline__ void rope_query_f32(const Ctx<C>& cx, const float2* base, int kcp, float4 (&l)[C::NT],
+                                               float4 (&u)[C::NT]) {
+  constexpr int NT = C::NT, KC = C::KC;
+  const int c = 32 * (kcp >> 1) + 8 * cx.tq + 2 * (kcp & 1);  // even: (c, c + 1) is one 16-byte load
+  const float4 f02 = __ldg(reinterpret_cast<const float4*>(base + c));
+  const float4 f13 = __ldg(reinterpret_cast<const float4*>(base + c + 4));
+  const float2 f0 = make_float2(f02.x, f02.y), f2 = make_float2(f02.z, f02.w);
+  const float2 f1 = make_float2(f13.x, f13.y), f3 = make_float2(f13.z, f13.w);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const float4 a = cx.qr[(kcp * NT + nt) * 32 + cx.lane], b = cx.qr[((kcp + KC / 2) * NT + nt) * 32 + cx.lane];
+    l[nt] = make_float4(a.x * f0.x + b.x * f0.y, a.y * f1.x + b.y * f1.y, a.z * f2.x + b.z * f2.y,
+                        a.w * f3.x + b.w * f3.y);
+    u[nt] = make_float4(b.x * f0.x - a.x * f0.y, b.y * f1.x - a.y * f1.y, b.z * f2.x - a.z * f2.y,
+                        b.w * f3.x - a.w * f3.y);
+  }
+}
+
+// fp16 pair of (x0, x1) for this lane's B column: the values rounded to fp16
+// (m = 0: hi columns) or the fp16 rounding of their remainders x - fp16(x)
+// (m = 1: lo columns); x - fp16(x) is exact in fp32.
+__device__ __forceinline__ uint32_t col_pair(float x0, float x1, float m) {
+  const float2 b = __half22float2(__floats2half2_rn(x0, x1));
+  return pack_h2(fmaf(-m, b.x, x0), fmaf(-m, b.y, x1));
 }
 
 // Key values of lower channels ch[0..3] (L: pairs (ch0, ch1), (ch2, ch3))
@@ -601,7 +645,112 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
   const uint32_t lo_mask = cx.lo_mask;
   const uint2* qb = cx.qb;
   const uint2* qh = cx.qh;
-    if constexpr (TR::KCH && C::ROPE) {
+    if constexpr (TR::KCH && C::ROPE && !TR::Z) {
+      // Pre-RoPE per-channel keys, t = t0 + j: with q' = R(-t0) q (fp32) and
+      // codes c, scales s,
+      //   q . R(t) k = sum_i cos(j th_i) (c_i s_i q'_i + c_u s_u q'_u)
+      //                    + sin(j th_i) (c_i s_i q'_u - c_u s_u q'_i),  u = i + D/2.
+      // The A operands are code x table entry, exact in fp16 (the table's hi
+      // parts have 8 significant bits), for the hi and lo parts of cos and
+      // sin; the B operands are the scaled, turned query in hi / lo columns.
+      // Per k-chunk pair: 16 MMAs on two accumulator chains.
+      const float2* base = cx.rope_base + (int64_t)(t0 / kTile) * (D / 2);
+      const float mlo = cx.lo_part ? 1.f : 0.f;
+      float Sx[2][NT][4];
+#pragma unroll
+      for (int mu = 0; mu < 2; ++mu)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) Sx[mu][nt][0] = Sx[mu][nt][1] = Sx[mu][nt][2] = Sx[mu][nt][3] = 0.f;
+#pragma unroll 1
+      for (int kcp = 0; kcp < KC / 2; ++kcp) {
+        float4 ql[NT], qu[NT];
+        rope_query_f32<C>(cx, base, kcp, ql, qu);
+        const int c = 32 * (kcp >> 1) + 8 * tq + 2 * (kcp & 1);
+        const int ch[4] = {c, c + 4, c + 1, c + 5};
+        float sl[4], su[4];
+        uint32_t chl[4], chu[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint8_t* bl = ksm + ch[q] * TR::KBB;
+          const uint8_t* bu = ksm + (ch[q] + D / 2) * TR::KBB;
+          sl[q] = block_scale(bl);
+          su[q] = block_scale(bu);
+          chl[q] = TR::KB == 4 ? ld_u16(bl + TR::HDR + 2 * gq) : (uint32_t)bl[TR::HDR + gq];
+          chu[q] = TR::KB == 4 ? ld_u16(bu + TR::HDR + 2 * gq) : (uint32_t)bu[TR::HDR + gq];
+        }
+        // codes as exact fp16 pairs: [0] channels (c, c + 4), [1] (c + 1, c + 5), of token k
+        uint32_t cl[2][4], cu[2][4];
+        {
+          const uint32_t xl0 = __byte_perm(chl[0], chl[1], 0x5410), xl1 = __byte_perm(chl[2], chl[3], 0x5410);
+          const uint32_t xu0 = __byte_perm(chu[0], chu[1], 0x5410), xu1 = __byte_perm(chu[2], chu[3], 0x5410);
+          if constexpr (TR::KB == 4) {
+            dq4(xl0, cl[0]);
+            dq4(xl1, cl[1]);
+            dq4(xu0, cu[0]);
+            dq4(xu1, cu[1]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              cl[0][k] = code_pair<2>(xl0, k);
+              cl[1][k] = code_pair<2>(xl1, k);
+              cu[0][k] = code_pair<2>(xu0, k);
+              cu[1][k] = code_pair<2>(xu1, k);
+            }
+          }
+        }
+        // B fragments of this lane's column (head gq / 2, hi or lo part)
+        uint32_t bcl[NT][2], bsl[NT][2], bcu[NT][2], bsu[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float4 a = ql[nt], b = qu[nt];
+          bcl[nt][0] = col_pair(sl[0] * a.x, sl[1] * a.y, mlo);
+          bcl[nt][1] = col_pair(sl[2] * a.z, sl[3] * a.w, mlo);
+          bsl[nt][0] = col_pair(sl[0] * b.x, sl[1] * b.y, mlo);
+          bsl[nt][1] = col_pair(sl[2] * b.z, sl[3] * b.w, mlo);
+          bcu[nt][0] = col_pair(su[0] * b.x, su[1] * b.y, mlo);
+          bcu[nt][1] = col_pair(su[2] * b.z, su[3] * b.w, mlo);
+          bsu[nt][0] = col_pair(-su[0] * a.x, -su[1] * a.y, mlo);
+          bsu[nt][1] = col_pair(-su[2] * a.z, -su[3] * a.w, mlo);
+        }
+        const uint4* tb = cx.rope_tab + (kcp * 4 * 2) * 32 + lane;  // [k][cos / sin][lane]
+#pragma unroll
+        for (int mu = 0; mu < 2; ++mu) {
+          // turn table of the lane's tokens 2 mu (A rows gq) and 2 mu + 1 (rows gq + 8)
+          const uint4 ca = __ldg(tb + (2 * mu) * 64), sa = __ldg(tb + (2 * mu) * 64 + 32);
+          const uint4 cb = __ldg(tb + (2 * mu + 1) * 64), sb = __ldg(tb + (2 * mu + 1) * 64 + 32);
+          const int ka = 2 * mu, kb = 2 * mu + 1;
+#pragma unroll
+          for (int side = 0; side < 2; ++side) {  // 0: lower channels, 1: partners
+            const uint32_t(&x)[2][4] = side ? cu : cl;
+            const uint32_t a_ch0 = hmul2u(x[0][ka], ca.x), a_ch1 = hmul2u(x[0][kb], cb.x);
+            const uint32_t a_ch2 = hmul2u(x[1][ka], ca.y), a_ch3 = hmul2u(x[1][kb], cb.y);
+            const uint32_t a_cl0 = hmul2u(x[0][ka], ca.z), a_cl1 = hmul2u(x[0][kb], cb.z);
+            const uint32_t a_cl2 = hmul2u(x[1][ka], ca.w), a_cl3 = hmul2u(x[1][kb], cb.w);
+            const uint32_t a_sh0 = hmul2u(x[0][ka], sa.x), a_sh1 = hmul2u(x[0][kb], sb.x);
+            const uint32_t a_sh2 = hmul2u(x[1][ka], sa.y), a_sh3 = hmul2u(x[1][kb], sb.y);
+            const uint32_t a_sl0 = hmul2u(x[0][ka], sa.z), a_sl1 = hmul2u(x[0][kb], sb.z);
+            const uint32_t a_sl2 = hmul2u(x[1][ka], sa.w), a_sl3 = hmul2u(x[1][kb], sb.w);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const uint32_t(&bc)[2] = side ? bcu[nt] : bcl[nt];
+              const uint32_t(&bs)[2] = side ? bsu[nt] : bsl[nt];
+              mma16816(S[mu][nt], a_ch0, a_ch1, a_ch2, a_ch3, bc[0], bc[1]);
+              mma16816(Sx[mu][nt], a_cl0, a_cl1, a_cl2, a_cl3, bc[0], bc[1]);
+              mma16816(S[mu][nt], a_sh0, a_sh1, a_sh2, a_sh3, bs[0], bs[1]);
+              mma16816(Sx[mu][nt], a_sl0, a_sl1, a_sl2, a_sl3, bs[0], bs[1]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int mu = 0; mu < 2; ++mu)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) S[mu][nt][e] += Sx[mu][nt][e];
+    } else if constexpr (TR::KCH && C::ROPE) {
+      // asymmetric blocks: each key value dequantized (with its zero point),
+      // turned by R(j) in fp32 and split into fp16 hi + lo
       const float2* base = cx.rope_base + (int64_t)(t0 / kTile) * (D / 2);
 #pragma unroll 1
       for (int kcp = 0; kcp < KC / 2; ++kcp) {
@@ -1012,6 +1161,9 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     m = fmaxf(fmaxf(qmax_s[0], qmax_s[1]), fmaxf(qmax_s[2], qmax_s[3]));
     int ex = 0;
     if (m > 0.f) frexpf(m, &ex);
+    // pre-RoPE keys: one more halving, so the turned query (|q'| < sqrt(2))
+    // times an fp16 scale stays below 65504
+    if constexpr (C::ROPE) ex += 1;
     const float qnorm = ldexpf(1.f, -ex);
     qexp = ldexpf(1.f, ex);
     for (int e = tid; e < KC * NT * 32; e += kThreadsMma) {
@@ -1062,6 +1214,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   cx.g = g;
   cx.rope_base = a.rope;
   cx.rope_frag = reinterpret_cast<const float4*>(a.rope + (int64_t)(a.rope_base_rows + kTile) * (D / 2));
+  cx.rope_tab = reinterpret_cast<const uint4*>(a.rope + (int64_t)(a.rope_base_rows + 2 * kTile) * (D / 2));
   if constexpr (C::HOT::KLUT || C::HOT::VLUT) {
     uint32_t m[8];
 #pragma unroll

@@ -129,6 +129,49 @@ __global__ void rope_tables_kernel(float2* rope, int base_rows, int D, double th
   }
 }
 
+// x rounded to 8 significant bits (nearest, ties to even), then to fp16:
+// exact for |x| >= 2^-17, so that x_hi times any integer code of magnitude at
+// most 8 is exact in fp16; smaller values land on fp16's 2^-24 grid.
+__device__ __half hi8_of(double x) {
+  if (x == 0.0) return __double2half(0.0);
+  int e;
+  frexp(x, &e);  // x = m 2^e, 0.5 <= |m| < 1
+  return __double2half(ldexp(rint(ldexp(x, 8 - e)), e - 8));
+}
+
+// The turn table of the tensor-core decode's per-channel keys: cos and sin of
+// j theta_i (j = 0..31 the token's offset in its 32-token group), each split
+// into an fp16 part with 8 significant bits (hi) and the fp16 rounding of the
+// rest (lo), so hi + lo holds about 20 bits and code x hi is exact.  Layout:
+// uint4 [D/32 chunk pairs kcp][4 tokens k][2 halves][32 lanes] (a warp's
+// load of one half is 512 contiguous bytes): for lane (gq, tq), token
+// j = 4 gq + k and channel pairs P0 = (c, c + 4), P1 = (c + 1, c + 5),
+// c = 32 (kcp / 2) + 8 tq + 2 (kcp % 2), as fp16 pairs (low half the first
+// channel): half 0 = (cos hi P0, cos hi P1, cos lo P0, cos lo P1),
+// half 1 = (sin hi P0, sin hi P1, sin lo P0, sin lo P1).
+__global__ void rope_hilo_kernel(uint32_t* tab, int D, double theta) {
+  const int total = (D / 32) * 4 * 32 * 8;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+    // e = (((kcp * 4 + k) * 2 + half) * 32 + lane) * 4 + word
+    const int lane = (e >> 2) & 31, k = (e >> 8) & 3, kcp = e >> 10;
+    const int w = 4 * ((e >> 7) & 1) + (e & 3);  // word of the 8 (cos hi, cos hi, cos lo, cos lo, sin ...)
+    const int p = w & 1, type = w >> 1;  // type: 0 cos hi, 1 cos lo, 2 sin hi, 3 sin lo
+    const int c0 = 32 * (kcp >> 1) + 8 * (lane & 3) + 2 * (kcp & 1) + p;
+    const double j = (double)(4 * (lane >> 2) + k);
+    uint32_t word = 0;
+    for (int half_ = 0; half_ < 2; ++half_) {
+      const int i = c0 + 4 * half_;
+      double s, c;
+      sincos(j * pow(theta, -2.0 * i / D), &s, &c);
+      const double x = type < 2 ? c : s;
+      const __half hi = hi8_of(x);
+      const __half v = (type & 1) ? __double2half(x - (double)__half2float(hi)) : hi;
+      word |= (uint32_t)__half_as_ushort(v) << (16 * half_);
+    }
+    tab[e] = word;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_dequantize(const DequantArgs& a, cudaStream_t st) {
@@ -140,6 +183,11 @@ cudaError_t launch_dequantize(const DequantArgs& a, cudaStream_t st) {
 
 cudaError_t launch_rope_tables(float2* rope, int base_rows, int D, float theta, cudaStream_t st) {
   rope_tables_kernel<<<256, 256, 0, st>>>(rope, base_rows, D, (double)theta);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the fp16 hi / lo table follows the fp32 tables: (base_rows + 2 kTile) rows of D/2 float2
+  rope_hilo_kernel<<<(D / 32) * 4 * 32 * 8 / 256, 256, 0, st>>>(
+      reinterpret_cast<uint32_t*>(rope + (int64_t)(base_rows + 2 * kTile) * (D / 2)), D, (double)theta);
   return cudaGetLastError();
 }
 

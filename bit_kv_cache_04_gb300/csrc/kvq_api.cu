@@ -309,7 +309,7 @@ WsLayout ws_layout(const kvq_config* c) {
   w.rope = off;
   if (c->flags & KVQ_K_PRE_ROPE) {
     w.rope_base_rows = (c->max_T + kTile - 1) / kTile + 1;
-    off = align_up(off + sizeof(float2) * (size_t)(w.rope_base_rows + 2 * kTile) * (c->D / 2));
+    off = align_up(off + sizeof(float2) * (size_t)(w.rope_base_rows + kRopeExtraRows) * (c->D / 2));
   }
   w.partials = off;
   int64_t mp = 0;
@@ -774,7 +774,7 @@ extern "C" kvq_status kvq_decode_attention_static(const kvq_config* cfg, const k
   int rope_rows = 0;
   if (cfg->flags & KVQ_K_PRE_ROPE) {
     rope_rows = (cfg->max_T + kTile - 1) / kTile + 1;
-    off = align_up(off + sizeof(float2) * (size_t)(rope_rows + 2 * kTile) * (cfg->D / 2));
+    off = align_up(off + sizeof(float2) * (size_t)(rope_rows + kRopeExtraRows) * (cfg->D / 2));
   }
   const size_t off_partials = off;
   if (splits > 1) off = align_up(off + sizeof(float) * units * splits * g * part_row(cfg->D));

@@ -19,6 +19,9 @@ constexpr int kMaxGqa = 8;       // query heads per kv head
 constexpr int kTargetCtas = 608; // 4 x 152 SMs: split heuristic target
 constexpr int kMaxSplits = 256;
 constexpr size_t kWsAlign = 256;
+// float2 rows of D/2 after the base rows of the RoPE tables: the plain
+// offsets, the offsets in the lanes' order, the fp16 hi / lo turn table
+constexpr int kRopeExtraRows = 3 * kTile;
 
 struct FmtInfo {
   int bits;   // 8, 4, 3, 2 (0 = unused)
@@ -67,7 +70,8 @@ struct CachePtrs {
 struct WsLayout {
   size_t status;    // uint32 status word
   size_t tickets;   // uint32 per decode unit
-  size_t rope;      // float2 base[n_base][D/2] then off[kTile][D/2]
+  size_t rope;      // float2 base[n_base][D/2], off[kTile][D/2], off in lane order (kTile x D/2),
+                    // then the fp16 hi / lo turn table (kTile x D/2 float2 of space)
   size_t partials;  // float per (unit, split): g * part_row(D)
   size_t total;
   int max_units;
