@@ -20,9 +20,12 @@ from bit_kv_cache_04_gb300 import kvq as K  # noqa: E402
 from bit_kv_cache_04_gb300 import workloads as W  # noqa: E402
 
 
-@pytest.mark.parametrize("name", ["llama2_7b_kivi4", "ctx262k_hadamard4"])
+LENGTHS = {"llama2_7b_kivi4": [3000, 1500], "ctx262k_hadamard4": [4000], "mistral7b_hotcold": [6000, 4500]}
+
+
+@pytest.mark.parametrize("name", sorted(LENGTHS))
 def test_wait_that_runs_out_sets_stall_and_returns(name):
-    w = W.make(name).scaled(L=2, lengths=[3000, 1500] if name == "llama2_7b_kivi4" else [4000])
+    w = W.make(name).scaled(L=2, lengths=LENGTHS[name])
     cache, seq_lens, _, _ = appended_cache(w, with_oracle=False)
     cfg = w.cfg
     q = W.queries(w, cfg.L, "cuda", 3)
