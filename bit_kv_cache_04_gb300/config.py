@@ -28,6 +28,7 @@ DEV_PAGE = 2
 DEV_RANGE = 4
 DEV_LENGTH = 8
 DEV_STALL = 16
+DEV_BOUNDS = 32
 
 
 @dataclass(frozen=True)

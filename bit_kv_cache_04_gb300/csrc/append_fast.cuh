@@ -530,7 +530,8 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_token32_kernel(Append
   __syncthreads();
   if (!lo.paged && !lo.tiered) {
     bool bad = false;
-    block_copy_out(main_row(lo, a.cp, which, layer, seq, h, u0, &bad), out, n_tok * ROW);
+    uint8_t* dst = main_row(lo, a.cp, which, layer, seq, h, u0, &bad);
+    if (span_ok(lo, a.cp, which, dst, (int64_t)n_tok * ROW)) block_copy_out(dst, out, n_tok * ROW);
     return;
   }
   // tiered or paged: whole rows, one warp per row

@@ -364,7 +364,8 @@ __global__ void __launch_bounds__(kAppendThreads) quant_rot128_kernel(AppendArgs
   __syncthreads();
   if (!lo.paged) {
     bool bad = false;
-    copy_out_any(main_row(lo, a.cp, which, layer, seq, h, u0, &bad), out, n_tok * ROW);
+    uint8_t* dst = main_row(lo, a.cp, which, layer, seq, h, u0, &bad);
+    if (span_ok(lo, a.cp, which, dst, (int64_t)n_tok * ROW)) copy_out_any(dst, out, n_tok * ROW);
     return;
   }
   // paged: the tile's page ids are read once, in parallel; then one warp per
@@ -385,6 +386,7 @@ __global__ void __launch_bounds__(kAppendThreads) quant_rot128_kernel(AppendArgs
                    ((((int64_t)layer * lo.n_pages + page) * lo.H + h) * lo.pt + ta % lo.pt) * ROW;
     const uint8_t* src = out + (ta - u0) * ROW;
     const int bytes = (tb - ta) * ROW;
+    if (!span_ok(lo, a.cp, which, dst, bytes)) continue;  // bounds-checked build only
     const uintptr_t al = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) | (uintptr_t)bytes;
     if ((al & 15u) == 0) {  // whole pages: 16 rows of 66 or 50 bytes are whole 16-byte words
       for (int e = lane; e < bytes / 16; e += 32)

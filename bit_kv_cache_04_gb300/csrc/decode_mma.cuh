@@ -1266,6 +1266,10 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
         const int t0 = tile * kTile;
         const uint8_t* kg = cold_row(lo, a.cp, 0, layer, seq, h, t0);
         const uint8_t* vg = cold_row(lo, a.cp, 1, layer, seq, h, t0);
+        if (!(span_ok(lo, a.cp, 2, kg, C::COLD::KSTAGE) & span_ok(lo, a.cp, 3, vg, C::COLD::VSTAGE))) {
+          mbar_arrive_tx(bar, 0);  // bounds-checked build only: skipped
+          return;
+        }
         mbar_arrive_tx(bar, C::COLD::KSTAGE + C::COLD::VSTAGE);
         bulk_g2s(ks, kg, C::COLD::KSTAGE, bar);
         bulk_g2s(vs, vg, C::COLD::VSTAGE, bar);
@@ -1306,6 +1310,13 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
         return;
       }
       auto row0 = [&](int page) { return (((int64_t)layer * lo.n_pages + page) * lo.H + h) * lo.pt; };
+      if (!(span_ok(lo, a.cp, 0, a.cp.k_main + row0(p0) * lo.kf.row, kb) &
+            span_ok(lo, a.cp, 1, a.cp.v_main + row0(p0) * lo.vf.row, vb) &
+            span_ok(lo, a.cp, 0, a.cp.k_main + row0(p1) * lo.kf.row, kb) &
+            span_ok(lo, a.cp, 1, a.cp.v_main + row0(p1) * lo.vf.row, vb))) {
+        mbar_arrive_tx(bar, 0);  // bounds-checked build only: skipped
+        return;
+      }
       mbar_arrive_tx(bar, np * (kb + vb));
       bulk_g2s(ks, a.cp.k_main + row0(p0) * lo.kf.row, kb, bar);
       bulk_g2s(vs, a.cp.v_main + row0(p0) * lo.vf.row, vb, bar);
@@ -1317,6 +1328,10 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     }
     const uint8_t* kg = main_row(lo, a.cp, 0, layer, seq, h, t0, &bad);
     const uint8_t* vg = main_row(lo, a.cp, 1, layer, seq, h, t0, &bad);
+    if (!(span_ok(lo, a.cp, 0, kg, HT::KSTAGE) & span_ok(lo, a.cp, 1, vg, HT::VSTAGE))) {
+      mbar_arrive_tx(bar, 0);  // bounds-checked build only: skipped
+      return;
+    }
     mbar_arrive_tx(bar, HT::KSTAGE + HT::VSTAGE);
     bulk_g2s(ks, kg, HT::KSTAGE, bar);
     bulk_g2s(vs, vg, HT::VSTAGE, bar);

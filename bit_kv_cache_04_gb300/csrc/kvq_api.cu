@@ -18,6 +18,10 @@ using namespace kvq;
 
 namespace {
 
+// Rows taken off every cache segment's limit in the bounds-checked build
+// (kvq_test_shrink_bounds); read by make_layout.
+std::atomic<int> g_bounds_shrink{0};
+
 thread_local std::string g_last_error;
 
 kvq_status fail(kvq_status st, const char* fmt, ...) {
@@ -194,6 +198,7 @@ Layout make_layout(const kvq_config* c) {
   lo.max_pages = c->max_pages_per_seq;
   lo.flags = c->flags;
   lo.theta = c->rope_theta;
+  lo.bounds_shrink = g_bounds_shrink.load();
   if (c->sign_seed != 0) {
     uint64_t st = c->sign_seed, w[4];
     for (int i = 0; i < 4; ++i) w[i] = splitmix64_next(&st);
@@ -540,6 +545,7 @@ kvq_status kvq_append(const kvq_config* cfg, const kvq_cache* cache, int32_t lay
   a.total_new = total_new;
   a.max_new = max_new;
   a.status = (uint32_t*)((char*)workspace + w.status);
+  a.cp.status = a.status;
   cudaError_t e = launch_append(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "append kernels");
   return ok();
@@ -599,6 +605,7 @@ static kvq_status prep_decode(const kvq_config* cfg, const kvq_cache* cache, int
   a->out = out;
   a->splits = splits;
   a->status = (uint32_t*)((char*)workspace + w.status);
+  a->cp.status = a->status;
   a->tickets = (uint32_t*)((char*)workspace + w.tickets);
   a->partials = (float*)((char*)workspace + w.partials);
   a->rope = (const float2*)((char*)workspace + w.rope);
@@ -690,9 +697,21 @@ kvq_status kvq_dequantize(const kvq_config* cfg, const kvq_cache* cache, int32_t
   a.k_out = k_out;
   a.v_out = v_out;
   a.status = (uint32_t*)((char*)workspace + w.status);
+  a.cp.status = a.status;
   cudaError_t e = launch_dequantize(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "dequantize kernel");
   return ok();
+}
+
+kvq_status kvq_test_shrink_bounds(int32_t rows) {
+#ifdef KVQ_BOUNDS_CHECK
+  if (rows < 0 || rows > (1 << 20)) return fail(KVQ_ERR_ARG, "rows=%d not in [0, 2^20]", rows);
+  g_bounds_shrink.store(rows);
+  return ok();
+#else
+  if (rows == 0) return ok();
+  return fail(KVQ_ERR_UNSUPPORTED, "bounds checks are compiled into libkvq_checked.so only");
+#endif
 }
 
 kvq_status kvq_test_force_stall(int32_t polls) {
@@ -799,6 +818,7 @@ extern "C" kvq_status kvq_decode_attention_static(const kvq_config* cfg, const k
   a.out = out;
   a.splits = splits;
   a.status = (uint32_t*)base;
+  a.cp.status = a.status;
   a.tickets = (uint32_t*)((char*)base + off_tickets);
   a.partials = (float*)((char*)base + off_partials);
   a.rope = (const float2*)((char*)base + off_rope);

@@ -54,6 +54,7 @@ struct Layout {
   int hot_ring_k, hot_ring_v;        // ring length of the hot tier (rows) when tiered
   float cb[16];                      // TBQ4 centroid table (fp16 values, ascending), when used
   float cbt[15];                     // TBQ4 decision thresholds
+  int bounds_shrink;                 // bounds-checked build: rows taken off every segment's limit (tests)
 };
 
 struct CachePtrs {
@@ -64,6 +65,7 @@ struct CachePtrs {
   uint16_t* k_resid;
   uint16_t* v_resid;
   const int32_t* block_table;
+  uint32_t* status;  // device status word (the bounds-checked build records misses there)
 };
 
 // Workspace layout offsets (bytes).
@@ -103,6 +105,22 @@ KVQ_HD int c_end_of(const Layout& lo, int T) {
 
 // ---- addresses --------------------------------------------------------------
 
+// Bounds-checked build (-DKVQ_BOUNDS_CHECK, a stand-in for a memory checker):
+// every row helper checks its indices against the buffer's dimensions
+// (layer, sequence, kv head, row or page of the segment); a miss sets
+// KVQ_DEV_BOUNDS and yields row 0 of the buffer, so nothing outside the
+// caller's buffers is touched.  Sites that move several rows from one row
+// pointer check the run with span_ok.  The normal build compiles none of it.
+#if defined(KVQ_BOUNDS_CHECK) && defined(__CUDA_ARCH__)
+__device__ __forceinline__ bool kvq_bound(const CachePtrs& cp, bool ok) {
+  if (!ok && cp.status) atomicOr(cp.status, KVQ_DEV_BOUNDS);
+  return ok;
+}
+#define KVQ_CHECK(cond) kvq_bound(cp, (cond))
+#else
+#define KVQ_CHECK(cond) true
+#endif
+
 KVQ_HD const FmtInfo& fmt_main(const Layout& lo, int which) { return which ? lo.vf : lo.kf; }
 KVQ_HD const FmtInfo& fmt_cold(const Layout& lo, int which) { return which ? lo.vc : lo.kc; }
 
@@ -113,11 +131,14 @@ KVQ_HD uint8_t* main_row(const Layout& lo, const CachePtrs& cp, int which, int l
   const FmtInfo& f = fmt_main(lo, which);
   uint8_t* base = which ? cp.v_main : cp.k_main;
   if (lo.paged) {
+    if (!KVQ_CHECK(seq >= 0 && seq < lo.B && t >= 0 && t / lo.pt < lo.max_pages)) return base;
     int page = cp.block_table[(int64_t)seq * lo.max_pages + t / lo.pt];
     if (page < 0 || page >= lo.n_pages) {
       *bad = true;
       return nullptr;
     }
+    if (!KVQ_CHECK(layer >= 0 && layer < lo.L && h >= 0 && h < lo.H && t % lo.pt < lo.pt - lo.bounds_shrink))
+      return base;
     int64_t idx = (((int64_t)layer * lo.n_pages + page) * lo.H + h) * lo.pt + (t % lo.pt);
     return base + idx * f.row;
   }
@@ -129,6 +150,9 @@ KVQ_HD uint8_t* main_row(const Layout& lo, const CachePtrs& cp, int which, int l
   } else {
     r = lo.tiered ? (t % (which ? lo.hot_ring_v : lo.hot_ring_k)) : t;
   }
+  if (!KVQ_CHECK(layer >= 0 && layer < lo.L && seq >= 0 && seq < lo.B && h >= 0 && h < lo.H && t >= 0 &&
+                 r < rows - lo.bounds_shrink))
+    return base;
   int64_t idx = (((int64_t)layer * lo.B + seq) * lo.H + h) * rows + r;
   return base + idx * f.row;
 }
@@ -138,14 +162,53 @@ KVQ_HD uint8_t* cold_row(const Layout& lo, const CachePtrs& cp, int which, int l
   uint8_t* base = which ? cp.v_cold : cp.k_cold;
   int64_t rows = which ? lo.rows_v_cold : lo.rows_k_cold;
   int64_t r = (f.axis == KVQ_AXIS_CHANNEL) ? t / f.group : t;
+  if (!KVQ_CHECK(layer >= 0 && layer < lo.L && seq >= 0 && seq < lo.B && h >= 0 && h < lo.H && t >= 0 &&
+                 r < rows - lo.bounds_shrink))
+    return base;
   int64_t idx = (((int64_t)layer * lo.B + seq) * lo.H + h) * rows + r;
   return base + idx * f.row;
 }
 
 KVQ_HD uint16_t* resid_row(const Layout& lo, const CachePtrs& cp, int which, int layer, int seq, int h, int t) {
   uint16_t* base = which ? cp.v_resid : cp.k_resid;
+  if (!KVQ_CHECK(layer >= 0 && layer < lo.L && seq >= 0 && seq < lo.B && h >= 0 && h < lo.H && t >= 0 &&
+                 t % lo.ring < lo.ring - lo.bounds_shrink))
+    return base;
   int64_t idx = (((int64_t)layer * lo.B + seq) * lo.H + h) * lo.ring + (t % lo.ring);
   return base + idx * lo.D;
+}
+
+// Whether [p, p + bytes) lies inside one segment of cache buffer `buf` (0
+// k_main, 1 v_main, 2 k_cold, 3 v_cold): the rows of one (layer, sequence, kv
+// head), or of one page and kv head when paged.  Always true in the normal
+// build; in the bounds-checked build a miss sets KVQ_DEV_BOUNDS.
+KVQ_HD bool span_ok(const Layout& lo, const CachePtrs& cp, int buf, const void* p, int64_t bytes) {
+#if defined(KVQ_BOUNDS_CHECK) && defined(__CUDA_ARCH__)
+  const bool cold = buf >= 2;
+  const int which = buf & 1;
+  const FmtInfo& f = cold ? fmt_cold(lo, which) : fmt_main(lo, which);
+  const uint8_t* base = cold ? (which ? cp.v_cold : cp.k_cold) : (which ? cp.v_main : cp.k_main);
+  int64_t rows, n_seg;
+  if (!cold && lo.paged) {
+    rows = lo.pt;
+    n_seg = (int64_t)lo.L * lo.n_pages * lo.H;
+  } else {
+    rows = cold ? (which ? lo.rows_v_cold : lo.rows_k_cold) : (which ? lo.rows_v_main : lo.rows_k_main);
+    n_seg = (int64_t)lo.L * lo.B * lo.H;
+  }
+  const int64_t seg_bytes = rows * f.row;
+  const int64_t off = reinterpret_cast<const uint8_t*>(p) - base;
+  const int64_t seg = off >= 0 ? off / seg_bytes : -1;
+  return kvq_bound(cp, bytes >= 0 && seg >= 0 && seg < n_seg &&
+                           off + bytes <= seg * seg_bytes + (rows - lo.bounds_shrink) * f.row);
+#else
+  (void)lo;
+  (void)cp;
+  (void)buf;
+  (void)p;
+  (void)bytes;
+  return true;
+#endif
 }
 
 // ---- number helpers -----------------------------------------------------------

@@ -12,12 +12,14 @@ import os
 from dataclasses import fields
 from typing import Optional, Tuple
 
-from .config import (AXIS_CHANNEL, AXIS_TOKEN, DEV_CAPACITY, DEV_LENGTH, DEV_PAGE, DEV_RANGE,  # noqa: F401
-                     DEV_STALL, DT_BF16, DT_F16, K_PRE_ROPE, ROTATE_K, ROTATE_V, TBQ4_K, TBQ4_V, ZP_K, ZP_V,
+from .config import (AXIS_CHANNEL, AXIS_TOKEN, DEV_BOUNDS, DEV_CAPACITY, DEV_LENGTH, DEV_PAGE,  # noqa: F401
+                     DEV_RANGE, DEV_STALL, DT_BF16, DT_F16, K_PRE_ROPE, ROTATE_K, ROTATE_V, TBQ4_K, TBQ4_V, ZP_K, ZP_V,
                      Config, Fmt)
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libkvq.so")
+# KVQ_LIBRARY selects another build of the same ABI (the tests use it for the
+# bounds-checked libkvq_checked.so).
+LIB_PATH = os.environ.get("KVQ_LIBRARY") or os.path.join(_PKG, "libkvq.so")
 
 STATUS_NAMES = {0: "OK", 1: "ERR_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_CUDA", 4: "ERR_CAPACITY", 5: "ERR_WORKSPACE"}
 
@@ -91,6 +93,7 @@ def _load():
         "kvq_decode_attention_static": ([cfgp, cachep, i32, i32, vp, vp, vp, i32, vp], ctypes.c_int),
         "kvq_dequantize": ([cfgp, cachep, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "kvq_test_force_stall": ([i32], ctypes.c_int),
+        "kvq_test_shrink_bounds": ([i32], ctypes.c_int),
         "kvq_read_device_status": ([vp, P(u32), vp], ctypes.c_int),
         "kvq_clear_device_status": ([vp, vp], ctypes.c_int),
     }
@@ -108,7 +111,8 @@ EXPORTED = ("kvq_version", "kvq_last_error", "kvq_validate_config", "kvq_block_b
             "kvq_cache_bytes", "kvq_buffer_sizes", "kvq_workspace_bytes", "kvq_workspace_init", "kvq_append",
             "kvq_commit_lengths", "kvq_decode_attention", "kvq_decode_splits", "kvq_decode_attention_static",
             "kvq_dequantize", "kvq_launch_counts", "kvq_tbq4_codebook", "kvq_decode_step", "kvq_step_launches",
-            "kvq_read_device_status", "kvq_clear_device_status", "kvq_test_force_stall")
+            "kvq_read_device_status", "kvq_clear_device_status", "kvq_test_force_stall",
+            "kvq_test_shrink_bounds")
 
 
 def _check(st: int):
@@ -183,6 +187,12 @@ def kvq_decode_splits(cfg: Config, n_layers: int) -> int:
     out = ctypes.c_int32()
     _check(LIB.kvq_decode_splits(ctypes.byref(_to_c(cfg)), n_layers, ctypes.byref(out)))
     return out.value
+
+
+def kvq_test_shrink_bounds(rows: int) -> None:
+    """Bounds-checked build: treat the last `rows` rows of every cache segment
+    as outside it (0 = off)."""
+    _check(LIB.kvq_test_shrink_bounds(rows))
 
 
 def kvq_test_force_stall(polls: int) -> None:

@@ -145,8 +145,10 @@ enum {
   KVQ_DEV_PAGE = 1u << 1,     /* a block_table entry outside [0, n_pages) */
   KVQ_DEV_RANGE = 1u << 2,    /* kvq_dequantize range outside [0, T) */
   KVQ_DEV_LENGTH = 1u << 3,   /* a sequence length < 0 or > max_T, or cu_new not ascending */
-  KVQ_DEV_STALL = 1u << 4     /* a decode kernel's own bulk copy into shared memory did not complete
+  KVQ_DEV_STALL = 1u << 4,    /* a decode kernel's own bulk copy into shared memory did not complete
                                  within its bounded wait; that call's outputs are undefined */
+  KVQ_DEV_BOUNDS = 1u << 5    /* bounds-checked build only (libkvq_checked.so): a computed cache address
+                                 fell outside its buffer segment; the access was skipped */
 };
 
 typedef struct {
@@ -361,6 +363,14 @@ KVQ_API kvq_status kvq_tbq4_codebook(float centroids[16], float thresholds[15]);
  * default) turns it off.  Process-wide; polls outside [0, 2^20] give
  * KVQ_ERR_ARG.  Not for production use. */
 KVQ_API kvq_status kvq_test_force_stall(int32_t polls);
+
+/* Testing hook of the bounds-checked build (libkvq_checked.so, compiled
+ * with KVQ_BOUNDS_CHECK); no counterpart on the pages.  Later calls treat
+ * the last `rows` rows (or page rows) of every cache segment as outside the
+ * buffer, so accesses there set KVQ_DEV_BOUNDS and are skipped: a test that
+ * the checks fire without any real out-of-bounds access.  0 (the default)
+ * turns it off.  The normal build answers KVQ_ERR_UNSUPPORTED for rows > 0. */
+KVQ_API kvq_status kvq_test_shrink_bounds(int32_t rows);
 
 /* Synchronizes `stream` and reads the device status word (KVQ_DEV_* bits). */
 KVQ_API kvq_status kvq_read_device_status(const void* workspace, uint32_t* bits, void* stream);

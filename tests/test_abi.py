@@ -223,3 +223,12 @@ def test_stall_test_mode_bounds():
         with pytest.raises(K.KvqError):
             K.kvq_test_force_stall(bad)
     K.kvq_test_force_stall(0)
+
+
+def test_bounds_hook_needs_the_checked_build():
+    # kvq_test_shrink_bounds only acts in libkvq_checked.so; the normal build refuses rows > 0
+    if K.LIB_PATH.endswith("libkvq_checked.so"):
+        pytest.skip("running under the checked build")
+    with pytest.raises(K.KvqError):
+        K.kvq_test_shrink_bounds(1)
+    K.kvq_test_shrink_bounds(0)
