@@ -115,6 +115,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) decode_generic_kernel(DecodeArgs a) {
+  // programmatic dependent launch: see launch_dependent
+  grid_dependency_wait();
+  grid_launch_dependents();
   constexpr int LD = D + 1;
   constexpr int R = (kMaxGqa * D + kThreads - 1) / kThreads;
   extern __shared__ float sm[];
@@ -290,8 +293,7 @@ cudaError_t launch_generic(const DecodeArgs& a, cudaStream_t st) {
     attr_done = true;
   }
   dim3 grid(a.splits, a.lo.H, a.n_layers * a.lo.B);
-  decode_generic_kernel<D><<<grid, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(decode_generic_kernel<D>, grid, dim3(kThreads), smem, st, a);
 }
 
 }  // namespace

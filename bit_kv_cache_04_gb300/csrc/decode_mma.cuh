@@ -1083,6 +1083,11 @@ template <class C, int STEP>
 __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(DecodeArgs a) {
   constexpr int D = C::D, NT = C::NT, KC = C::KC;
   extern __shared__ __align__(16) uint8_t smem[];
+  // launched with programmatic stream serialization: wait for the previous
+  // grid of the stream (and its memory) before reading anything, and let the
+  // next grid's blocks become resident as soon as this grid's blocks leave
+  grid_dependency_wait();
+  grid_launch_dependents();
   uint2* qb = reinterpret_cast<uint2*>(smem);  // [KC][NT][32 lanes]: this lane's B fragment (b0, b1)
   uint2* qh = qb + KC * NT * 32;               // [KC][NT][32 lanes]: query half pairs (per-channel K)
   float4* qr = reinterpret_cast<float4*>(qh + (C::QH ? KC * NT * 32 : 0));  // [KC][NT][32]: fp32 query (RoPE)
@@ -1128,15 +1133,121 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   const int te = (int)((int64_t)(split + 1) * ntiles / a.splits);
   const int64_t qrow = ((int64_t)li * lo.B + seq) * lo.Hq + (int64_t)h * g;
 
+  // ---- barriers, then the first bulk copies: they land while the query is prepared ----
+  if (tid == 0) bad_page = 0;
+  if (tid < kWarps * kStages) mbar_init(mbar + tid, 1);
+  if (tid == kThreadsMma - 1) mbar_init(&never_bar, 1);
+  fence_mbar_init();
+  // (the step's scratch rows in shared memory were written through the
+  // generic proxy: order them before the bulk copies into the same bytes)
+  fence_proxy_async();
+  __syncthreads();
+  uint8_t* wst = stage_base + warp * kStages * C::STAGE;
+
+  // Paged tiles: lane 0 copies the page ids of the next tile it will issue
+  // into shared memory (4-byte cp.async) one issue ahead, so the block-table
+  // reads overlap a group of compute instead of stalling the copy issue; no
+  // register holds them across the loop.
+  const int first = tb + warp;  // this warp takes tiles first, first + kWarps, ...
+
+  // Bulk copies of packed tile `tile` (cold or hot/only tier) into stage
+  // `st`, issued by lane 0: exactly one arrival on the stage's barrier per
+  // packed tile of this warp (with no bytes when a page id is bad).
+  auto issue = [&](int tile, int st) {
+    if (tile >= te || tile >= n_c + n_m) return;
+    if (lane != 0) return;
+    uint8_t* ks = wst + st * C::STAGE;
+    uint8_t* vs = ks + C::VOFF;
+    uint64_t* bar = mbar + warp * kStages + st;
+    if constexpr (C::HAS_COLD) {
+      if (tile < n_c) {
+        const int t0 = tile * kTile;
+        const uint8_t* kg = cold_row(lo, a.cp, 0, layer, seq, h, t0);
+        const uint8_t* vg = cold_row(lo, a.cp, 1, layer, seq, h, t0);
+        if (!(span_ok(lo, a.cp, 2, kg, C::COLD::KSTAGE) & span_ok(lo, a.cp, 3, vg, C::COLD::VSTAGE))) {
+          mbar_arrive_tx(bar, 0);  // bounds-checked build only: skipped
+          return;
+        }
+        mbar_arrive_tx(bar, C::COLD::KSTAGE + C::COLD::VSTAGE);
+        bulk_g2s(ks, kg, C::COLD::KSTAGE, bar);
+        bulk_g2s(vs, vg, C::COLD::VSTAGE, bar);
+        return;
+      }
+    }
+    using HT = typename C::HOT;
+    const int t0 = ce + (tile - n_c) * kTile;
+    bool bad = false;
+    if (lo.paged) {
+      // one or two pages (16-token pages when the group is complete); tiles
+      // start at multiples of 32, so at row 0 of a page
+      const int np = (qe - t0 > lo.pt) ? kTile / lo.pt : 1;
+      const int kb = lo.pt * HT::KROW, vb = lo.pt * HT::VROW;
+      // this warp issues tiles first, first + kWarps, ...: the ids of every
+      // tile after the first were copied by the issue before it
+      const int par = ((tile - first) / kWarps) & 1;
+      const int* bt_row = a.cp.block_table + (int64_t)seq * lo.max_pages;
+      int p0, p1;
+      if (tile == first || (tile - kWarps) < n_c) {
+        p0 = bt_row[t0 / lo.pt];
+        p1 = np == 2 ? bt_row[t0 / lo.pt + 1] : p0;
+      } else {
+        cp_async_wait<0>();
+        p0 = pf_page[warp][par][0];
+        p1 = np == 2 ? pf_page[warp][par][1] : p0;
+      }
+      const int nx = tile + kWarps;  // the next tile this warp issues
+      if (nx < te && nx >= n_c && nx < n_c + n_m) {
+        const int pn = (ce + (nx - n_c) * kTile) / lo.pt;
+        cp_async4(&pf_page[warp][par ^ 1][0], bt_row + pn);
+        cp_async4(&pf_page[warp][par ^ 1][1], bt_row + pn + (qe - pn * lo.pt > lo.pt ? 1 : 0));
+        cp_async_commit();
+      }
+      if (p0 < 0 || p0 >= lo.n_pages || p1 < 0 || p1 >= lo.n_pages) {
+        bad_page = 1;
+        mbar_arrive_tx(bar, 0);
+        return;
+      }
+      auto row0 = [&](int page) { return (((int64_t)layer * lo.n_pages + page) * lo.H + h) * lo.pt; };
+      if (!(span_ok(lo, a.cp, 0, a.cp.k_main + row0(p0) * lo.kf.row, kb) &
+            span_ok(lo, a.cp, 1, a.cp.v_main + row0(p0) * lo.vf.row, vb) &
+            span_ok(lo, a.cp, 0, a.cp.k_main + row0(p1) * lo.kf.row, kb) &
+            span_ok(lo, a.cp, 1, a.cp.v_main + row0(p1) * lo.vf.row, vb))) {
+        mbar_arrive_tx(bar, 0);  // bounds-checked build only: skipped
+        return;
+      }
+      mbar_arrive_tx(bar, np * (kb + vb));
+      bulk_g2s(ks, a.cp.k_main + row0(p0) * lo.kf.row, kb, bar);
+      bulk_g2s(vs, a.cp.v_main + row0(p0) * lo.vf.row, vb, bar);
+      if (np == 2) {
+        bulk_g2s(ks + kb, a.cp.k_main + row0(p1) * lo.kf.row, kb, bar);
+        bulk_g2s(vs + vb, a.cp.v_main + row0(p1) * lo.vf.row, vb, bar);
+      }
+      return;
+    }
+    const uint8_t* kg = main_row(lo, a.cp, 0, layer, seq, h, t0, &bad);
+    const uint8_t* vg = main_row(lo, a.cp, 1, layer, seq, h, t0, &bad);
+    if (!(span_ok(lo, a.cp, 0, kg, HT::KSTAGE) & span_ok(lo, a.cp, 1, vg, HT::VSTAGE))) {
+      mbar_arrive_tx(bar, 0);  // bounds-checked build only: skipped
+      return;
+    }
+    mbar_arrive_tx(bar, HT::KSTAGE + HT::VSTAGE);
+    bulk_g2s(ks, kg, HT::KSTAGE, bar);
+    bulk_g2s(vs, vg, HT::VSTAGE, bar);
+  };
+
+  // the query scratch takes the last QSLOTS stage slots of the last warp,
+  // which that warp fills only after the query is prepared
+  constexpr int QSLOTS = ((C::HC ? 8 : 4 * NT) * D * 4 + C::STAGE - 1) / C::STAGE;
+  static_assert(QSLOTS <= kStages, "query scratch fits in the last warp's stage slots");
+#pragma unroll
+  for (int i = 0; i < kStages - 1; ++i)
+    if (warp != kWarps - 1 || i < kStages - QSLOTS) issue(first + kWarps * i, i);
+
   // ---- query: fp32, rotated when K is stored rotated; per-lane fragments ----
   float qexp = 1.f;
   {
-    float* qf = reinterpret_cast<float*>(stage_base);  // [g][D] scratch
+    float* qf = reinterpret_cast<float*>(stage_base + (kWarps * kStages - QSLOTS) * C::STAGE);  // [g][D]
     for (int e = tid; e < g * D; e += kThreadsMma) qf[e] = in_to_f32(a.q[qrow * D + e], lo.dtype);
-    if (tid == 0) bad_page = 0;
-    if (tid < kWarps * kStages) mbar_init(mbar + tid, 1);
-    if (tid == kThreadsMma - 1) mbar_init(&never_bar, 1);
-    fence_mbar_init();
     __syncthreads();
     if (lo.flags & KVQ_ROTATE_K) {
       for (int r = warp; r < g * (D / 128); r += kWarps) {
@@ -1244,106 +1355,15 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
 #pragma unroll
     for (int s = 0; s < (C::Z ? C::NS : 1); ++s) ws.zo[s][nt] = 0.f;
   }
-  uint8_t* wst = stage_base + warp * kStages * C::STAGE;
-
-  // Paged tiles: lane 0 copies the page ids of the next tile it will issue
-  // into shared memory (4-byte cp.async) one issue ahead, so the block-table
-  // reads overlap a group of compute instead of stalling the copy issue; no
-  // register holds them across the loop.
-  const int first = tb + warp;  // this warp takes tiles first, first + kWarps, ...
-
-  // Bulk copies of packed tile `tile` (cold or hot/only tier) into stage
-  // `st`, issued by lane 0: exactly one arrival on the stage's barrier per
-  // packed tile of this warp (with no bytes when a page id is bad).
-  auto issue = [&](int tile, int st) {
-    if (tile >= te || tile >= n_c + n_m) return;
-    if (lane != 0) return;
-    uint8_t* ks = wst + st * C::STAGE;
-    uint8_t* vs = ks + C::VOFF;
-    uint64_t* bar = mbar + warp * kStages + st;
-    if constexpr (C::HAS_COLD) {
-      if (tile < n_c) {
-        const int t0 = tile * kTile;
-        const uint8_t* kg = cold_row(lo, a.cp, 0, layer, seq, h, t0);
-        const uint8_t* vg = cold_row(lo, a.cp, 1, layer, seq, h, t0);
-        if (!(span_ok(lo, a.cp, 2, kg, C::COLD::KSTAGE) & span_ok(lo, a.cp, 3, vg, C::COLD::VSTAGE))) {
-          mbar_arrive_tx(bar, 0);  // bounds-checked build only: skipped
-          return;
-        }
-        mbar_arrive_tx(bar, C::COLD::KSTAGE + C::COLD::VSTAGE);
-        bulk_g2s(ks, kg, C::COLD::KSTAGE, bar);
-        bulk_g2s(vs, vg, C::COLD::VSTAGE, bar);
-        return;
-      }
-    }
-    using HT = typename C::HOT;
-    const int t0 = ce + (tile - n_c) * kTile;
-    bool bad = false;
-    if (lo.paged) {
-      // one or two pages (16-token pages when the group is complete); tiles
-      // start at multiples of 32, so at row 0 of a page
-      const int np = (qe - t0 > lo.pt) ? kTile / lo.pt : 1;
-      const int kb = lo.pt * HT::KROW, vb = lo.pt * HT::VROW;
-      // this warp issues tiles first, first + kWarps, ...: the ids of every
-      // tile after the first were copied by the issue before it
-      const int par = ((tile - first) / kWarps) & 1;
-      const int* bt_row = a.cp.block_table + (int64_t)seq * lo.max_pages;
-      int p0, p1;
-      if (tile == first || (tile - kWarps) < n_c) {
-        p0 = bt_row[t0 / lo.pt];
-        p1 = np == 2 ? bt_row[t0 / lo.pt + 1] : p0;
-      } else {
-        cp_async_wait<0>();
-        p0 = pf_page[warp][par][0];
-        p1 = np == 2 ? pf_page[warp][par][1] : p0;
-      }
-      const int nx = tile + kWarps;  // the next tile this warp issues
-      if (nx < te && nx >= n_c && nx < n_c + n_m) {
-        const int pn = (ce + (nx - n_c) * kTile) / lo.pt;
-        cp_async4(&pf_page[warp][par ^ 1][0], bt_row + pn);
-        cp_async4(&pf_page[warp][par ^ 1][1], bt_row + pn + (qe - pn * lo.pt > lo.pt ? 1 : 0));
-        cp_async_commit();
-      }
-      if (p0 < 0 || p0 >= lo.n_pages || p1 < 0 || p1 >= lo.n_pages) {
-        bad_page = 1;
-        mbar_arrive_tx(bar, 0);
-        return;
-      }
-      auto row0 = [&](int page) { return (((int64_t)layer * lo.n_pages + page) * lo.H + h) * lo.pt; };
-      if (!(span_ok(lo, a.cp, 0, a.cp.k_main + row0(p0) * lo.kf.row, kb) &
-            span_ok(lo, a.cp, 1, a.cp.v_main + row0(p0) * lo.vf.row, vb) &
-            span_ok(lo, a.cp, 0, a.cp.k_main + row0(p1) * lo.kf.row, kb) &
-            span_ok(lo, a.cp, 1, a.cp.v_main + row0(p1) * lo.vf.row, vb))) {
-        mbar_arrive_tx(bar, 0);  // bounds-checked build only: skipped
-        return;
-      }
-      mbar_arrive_tx(bar, np * (kb + vb));
-      bulk_g2s(ks, a.cp.k_main + row0(p0) * lo.kf.row, kb, bar);
-      bulk_g2s(vs, a.cp.v_main + row0(p0) * lo.vf.row, vb, bar);
-      if (np == 2) {
-        bulk_g2s(ks + kb, a.cp.k_main + row0(p1) * lo.kf.row, kb, bar);
-        bulk_g2s(vs + vb, a.cp.v_main + row0(p1) * lo.vf.row, vb, bar);
-      }
-      return;
-    }
-    const uint8_t* kg = main_row(lo, a.cp, 0, layer, seq, h, t0, &bad);
-    const uint8_t* vg = main_row(lo, a.cp, 1, layer, seq, h, t0, &bad);
-    if (!(span_ok(lo, a.cp, 0, kg, HT::KSTAGE) & span_ok(lo, a.cp, 1, vg, HT::VSTAGE))) {
-      mbar_arrive_tx(bar, 0);  // bounds-checked build only: skipped
-      return;
-    }
-    mbar_arrive_tx(bar, HT::KSTAGE + HT::VSTAGE);
-    bulk_g2s(ks, kg, HT::KSTAGE, bar);
-    bulk_g2s(vs, vg, HT::VSTAGE, bar);
-  };
-
   // ---- per-warp pipeline over this CTA's groups --------------------------------
-  // the query scratch in the stage buffers was written through the generic
-  // proxy; order it before the bulk copies, and publish the barriers
+  // the query scratch was written through the generic proxy: order it before
+  // the bulk copies into those slots (the last warp's deferred ones, the loop's)
   fence_proxy_async();
   __syncthreads();
+  if (warp == kWarps - 1) {
 #pragma unroll
-  for (int i = 0; i < kStages - 1; ++i) issue(first + kWarps * i, i);
+    for (int i = kStages - QSLOTS; i < kStages - 1; ++i) issue(first + kWarps * i, i);
+  }
   int stall_it = -1;
   for (int it = 0;; ++it) {
     const int tile = first + kWarps * it;
@@ -1645,9 +1665,8 @@ cudaError_t launch_mma(const DecodeArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  dim3 grid(a.splits, a.lo.H, a.n_layers * a.lo.B);
-  decode_mma_kernel<C, STEP><<<grid, kThreadsMma, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(decode_mma_kernel<C, STEP>, dim3(a.splits, a.lo.H, a.n_layers * a.lo.B),
+                          dim3(kThreadsMma), smem, st, a);
 }
 
 bool fmt_is(const FmtInfo& f, int bits, int group, int axis) {

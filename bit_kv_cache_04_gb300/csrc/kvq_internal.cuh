@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/kvq.h"
 
 #define KVQ_HD __host__ __device__ __forceinline__
@@ -225,6 +227,32 @@ __device__ __forceinline__ float sign_of(const uint32_t* mask, int i) {
 // TBQ4 tables (host, computed once): 16 centroids, 15 thresholds, fp32.
 void tbq4_tables(float* centroids, float* thresholds);
 bool tbq4_bins_ok();
+
+// ---- programmatic dependent launch -------------------------------------------
+// Decode kernels are launched with programmatic stream serialization: the
+// stream's next kernel may launch while this one drains, and every such
+// kernel first waits (griddepcontrol.wait) for the previous grid of the
+// stream to complete with its memory visible, so the order of effects is the
+// plain stream order.  Consecutive decode calls then overlap one grid's tail
+// with the next one's block launch.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::); }
+
+template <class... KArgs, class... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- launchers (defined in the kernel translation units) -------------------
 
