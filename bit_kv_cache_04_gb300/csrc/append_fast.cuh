@@ -344,6 +344,138 @@ __device__ __noinline__ void block32_pair_slow(const uint32_t* raw, uint8_t* dst
   }
 }
 
+// Cold 2-bit blocks straight from 16-bit inputs.  A token that enters the
+// cache in the cold tier is quantized to its hot block, dequantized and
+// quantized again to 2 bits (the tiers' op order).  For a symmetric hot block
+// with a normal fp16 scale s = fp16(amax / qmax), amax / s lies within
+// qmax 2^-10 of qmax, so the largest hot code magnitude is qmax (odd), the
+// cold block's absolute maximum is qmax s (exact in fp32) and its scale is
+// c = fp16(qmax s), within 2^-11 of qmax s.  A hot magnitude m then gets the
+// cold magnitude rint(m s / c): m s / c lies within 2^-10 of m / qmax, which is
+// at least 1/2 + 1/(2 qmax) for m >= k = (qmax + 1) / 2 = 2^(B-2) and at most
+// 1/2 - 1/(2 qmax) below it, so the cold code is nonzero exactly when m >= k.
+// m = rint(q) for the fp32 quotient q = RN(|x| / s) reaches k when
+// q >= k - 1/2 (a tie rounds to k when k is even, B >= 3) or q > k - 1/2
+// (k = 1, B = 2); and since a 16-bit x over an fp16 s never has an fp32
+// quotient that rounds onto k - 1/2 from either side, that is |x| >= th
+// (or > th) for th = (k - 1/2) s, an exact fp32 product.  In 16-bit terms:
+// |x| >= ru16(th) (or |x| > rd16(th)), one packed compare per pair of values.
+// The cold code is sign(x) where nonzero.  Blocks whose hot scale is
+// subnormal or saturated, or whose cold scale saturates, go the two-pass way.
+template <int DT, int B>
+__device__ __forceinline__ bool cold2_rule(float amax, uint16_t& thr, __half& c16) {
+  static_assert(B >= 2 && B <= 8, "hot bits");
+  constexpr int qmax = (1 << (B - 1)) - 1;
+  const float sf = __half2float(block_scale_of(amax, qmax));
+  if (!(sf >= kMinNormalF16 && sf < 65504.f)) return false;
+  c16 = __float2half_rn(__fmul_rn((float)qmax, sf));  // the cold block's scale, qmax s / 1
+  if (!(__half2float(c16) < 65504.f)) return false;
+  const float th = __fmul_rn((float)(1 << (B - 2)) - 0.5f, sf);
+  if constexpr (DT == KVQ_DT_F16)
+    thr = __half_as_ushort(B >= 3 ? __float2half_ru(th) : __float2half_rd(th));
+  else
+    thr = __bfloat16_as_ushort(B >= 3 ? __float2bfloat16_ru(th) : __float2bfloat16_rd(th));
+  return true;
+}
+
+// Per half of x: 0xFFFF when |x| passes the threshold t (>= for B >= 3, >
+// for B = 2), else 0.
+template <int DT, int B>
+__device__ __forceinline__ uint32_t cold2_mask(uint32_t x, uint32_t t) {
+  if constexpr (DT == KVQ_DT_F16) {
+    const __half2 a = __habs2(*reinterpret_cast<const __half2*>(&x)), b = *reinterpret_cast<const __half2*>(&t);
+    return B >= 3 ? __hge2_mask(a, b) : __hgt2_mask(a, b);
+  } else {
+    const __nv_bfloat162 a = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&x));
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&t);
+    return B >= 3 ? __hge2_mask(a, b) : __hgt2_mask(a, b);
+  }
+}
+
+// The 2-bit fields of eight pairs p[0..7]: pair e's low value at bits 2e,
+// its high value at bits 16 + 2e, each field (nonzero, nonzero and negative)
+// so that field ^ 2 is the biased cold code (1, 2, 3 for -1, 0, +1).  Each
+// pair's fields enter at bits 14 and 30 and move down two bits per later pair.
+template <int DT, int B>
+__device__ __forceinline__ uint32_t cold2_fields8(const uint32_t* p, uint32_t thr2) {
+  uint32_t q = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const uint32_t m = cold2_mask<DT, B>(p[e], thr2);
+    q = (q >> 2) | (m & (p[e] | 0x40004000u) & 0xC000C000u);
+  }
+  return q;
+}
+
+// 2-bit fields L0..L7 (low half) and H0..H7 (high half) of x as L0 H0 L1 H1 ...
+__device__ __forceinline__ uint32_t interleave2(uint32_t x) {
+  x = __byte_perm(x, 0, 0x3120);
+  x = (x & 0xF00FF00Fu) | ((x & 0x00F000F0u) << 4) | ((x >> 4) & 0x00F000F0u);
+  return (x & 0xC3C3C3C3u) | ((x & 0x0C0C0C0Cu) << 2) | ((x >> 2) & 0x0C0C0C0Cu);
+}
+
+__device__ __forceinline__ void put_cold2(uint8_t* dst, __half c16, uint32_t w0, uint32_t w1) {
+  uint16_t* p = reinterpret_cast<uint16_t*>(dst);
+  w0 ^= 0xAAAAAAAAu;
+  w1 ^= 0xAAAAAAAAu;
+  p[0] = __half_as_ushort(c16);
+  p[1] = (uint16_t)w0;
+  p[2] = (uint16_t)(w0 >> 16);
+  p[3] = (uint16_t)w1;
+  p[4] = (uint16_t)(w1 >> 16);
+}
+
+// One cold block from a 32-value slice of a token row (w[e] holding values
+// 2e and 2e + 1).  Returns false, writing nothing, where the rule above does
+// not apply.
+template <int DT, int B>
+__device__ __forceinline__ bool cold2_slice(const uint32_t (&w)[16], uint8_t* dst) {
+  uint32_t a2 = w[0] & 0x7FFF7FFFu;
+#pragma unroll
+  for (int e = 1; e < 16; ++e) a2 = max2_16<DT>(a2, w[e] & 0x7FFF7FFFu);
+  const float2 m = raw_pair_to_f32<DT>(a2);
+  uint16_t thr;
+  __half c16;
+  if (!cold2_rule<DT, B>(fmaxf(m.x, m.y), thr, c16)) return false;
+  const uint32_t t2 = thr * 0x00010001u;
+  put_cold2(dst, c16, interleave2(cold2_fields8<DT, B>(w, t2)), interleave2(cold2_fields8<DT, B>(w + 8, t2)));
+  return true;
+}
+
+// Two cold blocks: channels c and c + 1 of 32 tokens, raw[j] holding token
+// j's two 16-bit values.  Returns false, writing nothing, where the rule
+// above does not apply to either block.
+template <int DT, int B>
+__device__ __forceinline__ bool cold2_x2(const uint32_t (&raw)[32], uint8_t* dst0, uint8_t* dst1) {
+  uint32_t a2 = raw[0] & 0x7FFF7FFFu;
+#pragma unroll
+  for (int j = 1; j < 32; ++j) a2 = max2_16<DT>(a2, raw[j] & 0x7FFF7FFFu);
+  const float2 m = raw_pair_to_f32<DT>(a2);
+  uint16_t t0, t1;
+  __half c0, c1;
+  if (!(cold2_rule<DT, B>(m.x, t0, c0) && cold2_rule<DT, B>(m.y, t1, c1))) return false;
+  const uint32_t t2 = t0 | ((uint32_t)t1 << 16);
+  uint32_t q[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) q[g] = cold2_fields8<DT, B>(raw + 8 * g, t2);
+  put_cold2(dst0, c0, __byte_perm(q[0], q[1], 0x5410), __byte_perm(q[2], q[3], 0x5410));
+  put_cold2(dst1, c1, __byte_perm(q[0], q[1], 0x7632), __byte_perm(q[2], q[3], 0x7632));
+  return true;
+}
+
+// The blocks the direct rule declines, one channel at a time the two-pass
+// way; out of line, with the 16-bit pairs in local memory.
+template <int DT, int B, int CB>
+__device__ __noinline__ void cold_pair_slow(const uint32_t* raw, uint8_t* dst0, uint8_t* dst1) {
+  for (int hc = 0; hc < 2; ++hc) {
+    float v[32], dq[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = in_to_f32_t<DT>(hc ? (raw[j] >> 16) : (raw[j] & 0xFFFFu));
+    block32<B>(v, amax_of(v), nullptr, dq);
+    block32<CB>(dq, amax_of(dq), hc ? dst1 : dst0, nullptr);
+  }
+}
+
 // Two asymmetric blocks at once: channels c and c + 1 of 32 tokens, raw[j]
 // holding token j's two 16-bit values.  The codes of both blocks are taken on
 // f32x2 pairs (one lane per channel) as codes_zp does, consuming raw as they
@@ -454,6 +586,13 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_token32_kernel(Append
   uint8_t* dst = out + j * (to_cold ? CROW : ROW);
   // one 32-value slice: r holds its 16-bit values
   auto slice = [&](const uint4 (&r)[4], int sl) {
+    if constexpr (CB == 2 && !Z) {
+      if (to_cold) {
+        const uint32_t w[16] = {r[0].x, r[0].y, r[0].z, r[0].w, r[1].x, r[1].y, r[1].z, r[1].w,
+                                r[2].x, r[2].y, r[2].z, r[2].w, r[3].x, r[3].y, r[3].z, r[3].w};
+        if (cold2_slice<DT, B>(w, dst + sl * CBB)) return;
+      }
+    }
     float v[32], mn = 0.f, mx = 0.f;
     if constexpr (Z) {  // block extremes on the 16-bit pairs
       uint32_t lo2 = r[0].x, hi2 = lo2;
@@ -632,6 +771,16 @@ __global__ void __launch_bounds__(kAppendThreads, channel_ctas<CB, Z>()) quant_c
 #pragma unroll
         for (int j = 0; j < 32; ++j) t[j] = raw[j];
         block32_pair_slow<DT, B>(t, d0, d0 + BB);
+      }
+      return;
+    }
+    if constexpr (CB == 2 && !Z) {  // to_cold
+      uint8_t* d0 = out + gi * SLOT + 2 * cp * CBB;
+      if (!cold2_x2<DT, B>(raw, d0, d0 + CBB)) {
+        uint32_t t[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) t[j] = raw[j];
+        cold_pair_slow<DT, B, CB>(t, d0, d0 + CBB);
       }
       return;
     }
