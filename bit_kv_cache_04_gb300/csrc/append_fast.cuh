@@ -782,19 +782,19 @@ __global__ void __launch_bounds__(kAppendThreads, channel_ctas<CB, Z>()) quant_c
         for (int j = 0; j < 32; ++j) t[j] = raw[j];
         cold_pair_slow<DT, B, CB>(t, d0, d0 + CBB);
       }
-      return;
-    }
+    } else {
 #pragma unroll
-    for (int hc = 0; hc < 2; ++hc) {
-      float v[32];
+      for (int hc = 0; hc < 2; ++hc) {
+        float v[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const uint32_t h16 = hc ? (raw[j] >> 16) : (raw[j] & 0xFFFFu);
-        v[j] = in_to_f32_t<DT>(h16);
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t h16 = hc ? (raw[j] >> 16) : (raw[j] & 0xFFFFu);
+          v[j] = in_to_f32_t<DT>(h16);
+        }
+        const int c = 2 * cp + hc;
+        hot_or_cold<B, CB, Z>(v, to_cold, out + gi * SLOT + c * BB, out + gi * SLOT + c * CBB, hc ? mn2.y : mn2.x,
+                              hc ? mx2.y : mx2.x);
       }
-      const int c = 2 * cp + hc;
-      hot_or_cold<B, CB, Z>(v, to_cold, out + gi * SLOT + c * BB, out + gi * SLOT + c * CBB, hc ? mn2.y : mn2.x,
-                            hc ? mx2.y : mx2.x);
     }
   };
 #pragma unroll 1

@@ -32,8 +32,8 @@
 // k-chunk kc + D/32 at the same slot (the RoPE partner); d-tile (s, e) row r
 // is channel 32s + 4(r & 7) + 2e + (r >> 3).
 //
-// Work split: CTA = 4 warps on one (layer, sequence, kv head, token split);
-// each warp streams its own groups through a ring of 2 or 3 shared-memory
+// Work split: CTA = 4 warps on one chunk of tiles of one (layer, sequence,
+// kv head) (see plan_work); each warp streams its own groups through a ring of 2 or 3 shared-memory
 // stages filled by 1-D bulk copies (TMA engine) that complete on per-stage
 // mbarriers, and keeps its own online softmax; warps merge in shared memory and splits merge in
 // the workspace (the last CTA to take a ticket combines; nobody waits).
@@ -973,6 +973,185 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
     }
   }
 
+// Chunked token splits.  The grid holds n_units x splits blocks (the block
+// budget), spread over the units by tile count rather than evenly per unit:
+// every unit of n tiles is cut into ceil(n / C) nearly equal chunks (a unit
+// with no tiles into one empty chunk), C the smallest chunk of at least min_chunk
+// tiles (and of the longest unit / kMaxSplits; of the longest unit / splits
+// when the caller fixed the count) whose chunks fit the grid.  Uniform
+// lengths give every unit `splits` chunks, as an even split would; in a
+// ragged batch long sequences get more chunks and short ones fewer, so every
+// block carries about the same number of tiles.  Blocks are numbered
+// unit-major (layer, sequence, kv head, chunk): a unit's chunks, and so its
+// partial rows, are consecutive.  Blocks past the last chunk have no work.
+// Warp 0 plans from every sequence's length (batches of up to kChunkSeqs
+// sequences; larger ones, one block per unit, grids of more than two waves
+// of resident blocks and batches of equal lengths split evenly).
+constexpr int kChunkSeqs = 256;
+
+struct Work {
+  int li, seq, h, T, chunk, n_chunks, tb, te, first;  // first: linear index of the unit's chunk 0
+  int active, bad_len;
+};
+
+// Tiles of a unit of T tokens (cold, hot / main, window; the first two 32-token
+// groups, the window in 32-token tiles).
+template <bool HAS_COLD>
+__device__ __forceinline__ int unit_tiles(const Layout& lo, int T) {
+  const int qe = q_end_of(lo, T);
+  const int ce = HAS_COLD ? c_end_of(lo, T) : 0;
+  return ce / kTile + (qe - ce + kTile - 1) / kTile + (T - qe + kTile - 1) / kTile;
+}
+
+// n / C rounded down and up, for 0 <= n < 2^22 and C >= 1 (tile counts), with
+// rc = 1/C in fp32: n rc lies within n/C 2^-23 <= 1/2 of n / C, so its
+// truncation is off by at most one, which one exact step corrects.
+__device__ __forceinline__ int floor_div_tiles(int n, int C, float rc) {
+  int q = (int)__fmul_rn((float)n, rc);
+  if (q * C > n) --q;
+  else if ((q + 1) * C <= n) ++q;
+  return q;
+}
+__device__ __forceinline__ int ceil_div_tiles(int n, int C, float rc) {
+  const int q = floor_div_tiles(n, C, rc);
+  return q + (q * C < n ? 1 : 0);
+}
+
+// The attended length of sequence s (0, flagged by the caller, when outside
+// [0, max_T]).
+__device__ __forceinline__ int attended_len(const DecodeArgs& a, int s, int* bad) {
+  const int T = a.seq_lens[s] + a.len_add;
+  if (T < 0 || T > a.lo.max_T) {
+    *bad = 1;
+    return 0;
+  }
+  *bad = 0;
+  return T;
+}
+
+// This block's work (all threads call it; one __syncthreads inside).
+template <bool HAS_COLD>
+__device__ __forceinline__ Work plan_work(const DecodeArgs& a, Work* sw) {
+  const Layout& lo = a.lo;
+  const int B = lo.B, H = lo.H, S = a.splits, k = blockIdx.x;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    Work w{};
+    // even split of every unit: one block per unit, a multi-wave grid (the
+    // block scheduler balances it), batches too large to plan, or (found
+    // below) equal tile counts
+    bool even = S == 1 || !a.chunked || B > kChunkSeqs || lo.max_T >= (1 << 26);
+    constexpr int kPer = kChunkSeqs / 32;
+    int n[kPer], bad[kPer], T[kPer], maxn = 0, minn = 0x7FFFFFFF, sum = 0;
+    // lane l holds sequences [l per, (l + 1) per)
+    const int per = (B + 31) / 32, s0 = lane * per;
+    if (!even) {
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        n[j] = 0;
+        bad[j] = 0;
+        T[j] = 0;
+        if (j < per && s0 + j < B) {
+          T[j] = attended_len(a, s0 + j, &bad[j]);
+          n[j] = unit_tiles<HAS_COLD>(lo, T[j]);
+          maxn = max(maxn, n[j]);
+          minn = min(minn, n[j]);
+          sum += n[j];
+        }
+      }
+      maxn = __reduce_max_sync(0xFFFFFFFFu, maxn);
+      minn = __reduce_min_sync(0xFFFFFFFFu, minn);
+      even = maxn == minn && !a.fixed_splits;
+    }
+    if (even) {
+      const int unit = k / S;
+      w.chunk = k % S;
+      w.n_chunks = S;
+      w.first = unit * S;
+      w.h = unit % H;
+      w.seq = (unit / H) % B;
+      w.li = unit / (H * B);
+      w.active = w.li < a.n_layers;
+      if (w.active) {
+        w.T = attended_len(a, w.seq, &w.bad_len);
+        const int n = unit_tiles<HAS_COLD>(lo, w.T);
+        w.tb = (int)((int64_t)w.chunk * n / S);
+        w.te = (int)((int64_t)(w.chunk + 1) * n / S);
+      }
+      if (lane == 0) *sw = w;
+    } else {
+      const int N = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)sum), K = B * S;  // one layer's kv head
+      int c_lo = max(max(a.min_chunk, 1), (maxn + kMaxSplits - 1) / kMaxSplits);
+      if (a.fixed_splits) c_lo = max(c_lo, (maxn + S - 1) / S);
+      // the smallest C >= c_lo with chunks(C) <= K: chunks(C) >= N / C, and
+      // chunks(C) < N / C + B, so it lies in [N / K, N / (K - B)] (K > B as
+      // S > 1), and C = maxn gives B chunks
+      auto chunks = [&](int C) {
+        const float rc = __frcp_rn((float)C);
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+          if (j < per && s0 + j < B) c += max(1, ceil_div_tiles(n[j], C, rc));
+        return (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)c);
+      };
+      int c_hi = max(c_lo, min(maxn, (N + K - B - 1) / (K - B)));
+      c_lo = min(c_hi, max(c_lo, (N + K - 1) / K));
+      while (c_lo < c_hi) {
+        const int mid = c_lo + (c_hi - c_lo) / 2;
+        if (chunks(mid) <= K) c_hi = mid;
+        else c_lo = mid + 1;
+      }
+      const int C = c_lo;
+      const float rc = __frcp_rn((float)C);
+      int nch[kPer], mine = 0;  // chunks per sequence; this lane's, times H (one layer)
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        nch[j] = (j < per && s0 + j < B) ? max(1, ceil_div_tiles(n[j], C, rc)) : 0;
+        mine += H * nch[j];
+      }
+      int incl = mine;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += y;
+      }
+      const int P = __shfl_sync(0xFFFFFFFFu, incl, 31);  // blocks per layer
+      const int li = k / P, r = k - li * P;
+      if (li >= a.n_layers) {
+        if (lane == 0) *sw = w;  // inactive
+      } else if (r >= incl - mine && r < incl) {  // exactly one lane
+        int base = incl - mine;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          if (j < per && s0 + j < B) {
+            const int nc = nch[j];
+            if (r < base + H * nc) {
+              const int o = r - base;
+              w.li = li;
+              w.seq = s0 + j;
+              w.h = floor_div_tiles(o, nc, __frcp_rn((float)nc));
+              w.chunk = o - w.h * nc;
+              w.n_chunks = nc;
+              w.first = k - w.chunk;
+              w.T = T[j];
+              w.bad_len = bad[j];
+              // the unit's tiles in nc nearly equal chunks (at most C each)
+              w.tb = (int)((int64_t)w.chunk * n[j] / nc);
+              w.te = (int)((int64_t)(w.chunk + 1) * n[j] / nc);
+              w.active = 1;
+              *sw = w;
+              break;
+            }
+            base += H * nc;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  return *sw;
+}
+
 // Fused decode step: the append of this step's token for the tiles it changes
 // that lie in this block's range [tb, te) (tiles after the step: cold, hot /
 // main, window).  The token changes at most three tiles: the group that moves
@@ -1044,19 +1223,15 @@ __device__ __noinline__ void step_phase_c(const AppendArgs& s, int li, int seq, 
 }
 
 template <class C, bool ROT>
-__device__ __forceinline__ void step_append(const DecodeArgs& a, uint8_t* sm) {
+__device__ __forceinline__ void step_append(const DecodeArgs& a, const Work& w, uint8_t* sm) {
   const Layout& lo = a.lo;
-  const int split = blockIdx.x, h = blockIdx.y, li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B;
-  const int T0 = a.seq_lens[seq], T = T0 + 1;
-  if (T0 < 0 || T > lo.max_T) return;  // flagged by the decode
+  const int T = w.T, T0 = T - 1;  // attended length T0 + 1 (one new token)
+  if (!w.active || w.bad_len || T0 < 0) return;  // flagged by the decode
+  const int h = w.h, li = w.li, seq = w.seq, tb = w.tb, te = w.te;
   const int qe = q_end_of(lo, T);
   const int ce = C::HAS_COLD ? c_end_of(lo, T) : 0;
   const int n_c = ce / kTile;
   const int n_m = (qe - ce + kTile - 1) / kTile;
-  const int n_w = (T - qe + kTile - 1) / kTile;
-  const int ntiles = n_c + n_m + n_w;
-  const int tb = (int)((int64_t)split * ntiles / a.splits);
-  const int te = (int)((int64_t)(split + 1) * ntiles / a.splits);
   const int q0 = q_end_of(lo, T0);
   const int c0 = C::HAS_COLD ? c_end_of(lo, T0) : 0;
   auto mine = [&](int tile) { return tile >= tb && tile < te; };
@@ -1101,11 +1276,17 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   __shared__ uint64_t never_bar;  // no thread ever arrives on it (failure-detection test mode)
   __shared__ int is_last;
   __shared__ int pf_page[kWarps][2][2];  // paged: next tile's page ids per warp, by issue parity
+  __shared__ Work work_s;
 
+  // the plan stays in shared memory: its fields are read where needed, not
+  // held in registers across the group loop
+  (void)plan_work<C::HAS_COLD>(a, &work_s);
+  const Work& w = work_s;
+  if (!w.active) return;
   if constexpr (STEP != 0) {
     // the step's cache writes first, then this block's decode reads them:
     // generic-proxy writes ordered before the bulk copies (async proxy)
-    step_append<C, STEP == 2>(a, smem);
+    step_append<C, STEP == 2>(a, w, smem);
     asm volatile("fence.proxy.async.global;\n" ::: "memory");
     __syncthreads();
   }
@@ -1113,24 +1294,14 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   const int g = lo.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  const int split = blockIdx.x, h = blockIdx.y;
-  const int li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B;
+  const int h = w.h, li = w.li, seq = w.seq, tb = w.tb, te = w.te, T = w.T;
   const int layer = a.layer0 + li;
   const int tid = threadIdx.x;
-
-  int T = a.seq_lens[seq] + a.len_add;
-  if (T < 0 || T > lo.max_T) {
-    if (split == 0 && h == 0 && tid == 0) atomicOr(a.status, KVQ_DEV_LENGTH);
-    T = 0;
-  }
+  if (w.bad_len && w.chunk == 0 && h == 0 && tid == 0) atomicOr(a.status, KVQ_DEV_LENGTH);
   const int qe = q_end_of(lo, T);
   const int ce = C::HAS_COLD ? c_end_of(lo, T) : 0;
   const int n_c = ce / kTile;
   const int n_m = (qe - ce + kTile - 1) / kTile;
-  const int n_w = (T - qe + kTile - 1) / kTile;
-  const int ntiles = n_c + n_m + n_w;
-  const int tb = (int)((int64_t)split * ntiles / a.splits);
-  const int te = (int)((int64_t)(split + 1) * ntiles / a.splits);
   const int64_t qrow = ((int64_t)li * lo.B + seq) * lo.Hq + (int64_t)h * g;
 
   // ---- barriers, then the first bulk copies: they land while the query is prepared ----
@@ -1602,20 +1773,20 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   // CTA partial per head: M = max_w m_w, L = sum_w 2^(m_w - M) l_w, O likewise
   const int64_t unit = ((int64_t)li * lo.B + seq) * lo.H + h;
   constexpr int PR = part_row(D);
-  float* part = a.partials + (unit * a.splits + split) * (int64_t)g * PR;
+  float* part = a.partials + (int64_t)(w.first + w.chunk) * g * PR;
   for (int e = tid; e < g * D; e += kThreadsMma) {
     const int hh = e / D, d = e % D;
     float M = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * kMaxGqa + hh]);
+    for (int wi = 0; wi < kWarps; ++wi) M = fmaxf(M, wm[wi * kMaxGqa + hh]);
     float L = 0.f, O = 0.f;
     if (M != -INFINITY) {
-      for (int w = 0; w < kWarps; ++w) {
-        const float sc = exp2f(wm[w * kMaxGqa + hh] - M);
-        L += sc * wl[w * kMaxGqa + hh];
-        O += sc * wo[(w * kMaxGqa + hh) * D + d];
+      for (int wi = 0; wi < kWarps; ++wi) {
+        const float sc = exp2f(wm[wi * kMaxGqa + hh] - M);
+        L += sc * wl[wi * kMaxGqa + hh];
+        O += sc * wo[(wi * kMaxGqa + hh) * D + d];
       }
     }
-    if (a.splits == 1) {
+    if (w.n_chunks == 1) {
       obuf[e] = L > 0.f ? O / L : 0.f;
     } else {
       part[hh * PR + d] = O;
@@ -1625,17 +1796,38 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
       }
     }
   }
-  if (a.splits > 1) {
+  if (w.n_chunks > 1) {
+    // two levels when the unit has at least 4 kCombineFan chunks: the last
+    // chunk of each group of kCombineFan merges the group into the group's
+    // first row, then the last group merges the group rows (one level below
+    // that: two serial merges cost more than one longer merge)
+    constexpr int F = kCombineFan;
+    uint32_t* tk = a.tickets + unit * kTicketsPerUnit;  // [0]: the unit, [1 + group]: its groups
+    float* rows = a.partials + (int64_t)w.first * g * PR;
+    const int n_grp = w.n_chunks >= 4 * F ? (w.n_chunks + F - 1) / F : 1, grp = w.chunk / F, g0 = grp * F;
+    const int gn = min(F, w.n_chunks - g0);
+    // the per-warp partials in wo are dead here: the merge weights reuse them
+    static_assert(kWarps * kMaxGqa * D >= kMaxGqa * kMaxSplits, "merge weights fit in the warp partials");
     __threadfence();
     __syncthreads();
-    if (tid == 0) is_last = atomicAdd(a.tickets + unit, 1u) == (unsigned)(a.splits - 1);
+    if (n_grp > 1 && gn > 1) {
+      if (tid == 0) is_last = atomicAdd(tk + 1 + grp, 1u) == (unsigned)(gn - 1);
+      __syncthreads();
+      if (!is_last) return;
+      __threadfence();
+      float* grow = rows + (int64_t)g0 * g * PR;
+      combine_rows<D, kThreadsMma, false>(grow, gn, 1, g, grow, wo, wm);
+      if (tid == 0) tk[1 + grp] = 0;
+      __threadfence();
+      __syncthreads();
+    }
+    const int n_last = n_grp > 1 ? n_grp : w.n_chunks;  // rows of the final merge
+    if (tid == 0) is_last = atomicAdd(tk, 1u) == (unsigned)(n_last - 1);
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    // the per-warp partials in wo are dead here: the merge weights reuse them
-    static_assert(kWarps * kMaxGqa * D >= kMaxGqa * kMaxSplits, "merge weights fit in the warp partials");
-    combine_splits<D, kThreadsMma>(a.partials + unit * a.splits * (int64_t)g * PR, a.splits, g, obuf, wo, wm);
-    if (tid == 0) a.tickets[unit] = 0;
+    combine_rows<D, kThreadsMma, true>(rows, n_last, n_grp > 1 ? F : 1, g, obuf, wo, wm);
+    if (tid == 0) tk[0] = 0;
   }
   __syncthreads();
   if (lo.flags & KVQ_ROTATE_V) {
@@ -1665,7 +1857,7 @@ cudaError_t launch_mma(const DecodeArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  return launch_dependent(decode_mma_kernel<C, STEP>, dim3(a.splits, a.lo.H, a.n_layers * a.lo.B),
+  return launch_dependent(decode_mma_kernel<C, STEP>, dim3(a.splits * a.lo.H * a.n_layers * a.lo.B),
                           dim3(kThreadsMma), smem, st, a);
 }
 

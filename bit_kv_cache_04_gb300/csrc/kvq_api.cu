@@ -302,6 +302,19 @@ int splits_for(const kvq_config* c, int n_layers) {
   return best;
 }
 
+// The chunking of the tensor-core decode (see plan_work): the least tiles per
+// chunk, whether the caller fixed the split count, and whether to plan chunks
+// by tile count at all (grids of up to two waves of resident blocks; larger
+// grids are balanced by the block scheduler).
+void set_chunking(const kvq_config* c, int num_splits, int n_layers, int splits, DecodeArgs* a) {
+  const bool rotated = (c->flags & (KVQ_ROTATE_K | KVQ_ROTATE_V)) != 0;
+  const int64_t blocks = (int64_t)n_layers * c->batch * c->H_kv * splits;
+  const int64_t resident = (int64_t)sm_count() * (c->D == 128 ? 4 : 2);
+  a->fixed_splits = num_splits ? 1 : 0;
+  a->min_chunk = num_splits ? 1 : (int)(rotated ? kMinTilesPerSplitRotated : kMinTilesPerSplit);
+  a->chunked = (num_splits || blocks <= 2 * resident) ? 1 : 0;
+}
+
 size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
 
 WsLayout ws_layout(const kvq_config* c) {
@@ -310,7 +323,7 @@ WsLayout ws_layout(const kvq_config* c) {
   w.status = 0;
   w.tickets = kWsAlign;
   w.max_units = c->L * c->batch * c->H_kv;
-  size_t off = align_up(w.tickets + sizeof(uint32_t) * (size_t)w.max_units);
+  size_t off = align_up(w.tickets + sizeof(uint32_t) * kTicketsPerUnit * (size_t)w.max_units);
   w.rope = off;
   if (c->flags & KVQ_K_PRE_ROPE) {
     w.rope_base_rows = (c->max_T + kTile - 1) / kTile + 1;
@@ -604,6 +617,7 @@ static kvq_status prep_decode(const kvq_config* cfg, const kvq_cache* cache, int
   a->seq_lens = seq_lens;
   a->out = out;
   a->splits = splits;
+  set_chunking(cfg, num_splits, n_layers, splits, a);
   a->status = (uint32_t*)((char*)workspace + w.status);
   a->cp.status = a->status;
   a->tickets = (uint32_t*)((char*)workspace + w.tickets);
@@ -788,7 +802,7 @@ extern "C" kvq_status kvq_decode_attention_static(const kvq_config* cfg, const k
   const size_t units = (size_t)n_layers * cfg->batch * cfg->H_kv;
   // this call's scratch: status word, tickets, RoPE tables, split partials
   const size_t off_tickets = kWsAlign;
-  size_t off = align_up(off_tickets + sizeof(uint32_t) * units);
+  size_t off = align_up(off_tickets + sizeof(uint32_t) * kTicketsPerUnit * units);
   const size_t off_rope = off;
   int rope_rows = 0;
   if (cfg->flags & KVQ_K_PRE_ROPE) {
@@ -817,6 +831,7 @@ extern "C" kvq_status kvq_decode_attention_static(const kvq_config* cfg, const k
   a.seq_lens = seq_lens;
   a.out = out;
   a.splits = splits;
+  set_chunking(cfg, num_splits, n_layers, splits, &a);
   a.status = (uint32_t*)base;
   a.cp.status = a.status;
   a.tickets = (uint32_t*)((char*)base + off_tickets);

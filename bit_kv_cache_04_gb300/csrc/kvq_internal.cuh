@@ -20,6 +20,10 @@ constexpr int kTile = 32;        // tokens per decode / append tile
 constexpr int kMaxGqa = 8;       // query heads per kv head
 constexpr int kTargetCtas = 608; // 4 x 152 SMs: split heuristic target
 constexpr int kMaxSplits = 256;
+// Split partials merge in groups of kCombineFan consecutive chunks, then the
+// group rows: tickets per unit are one for the unit and one per group.
+constexpr int kCombineFan = 8;
+constexpr int kTicketsPerUnit = 1 + kMaxSplits / kCombineFan;
 constexpr size_t kWsAlign = 256;
 // float2 rows of D/2 after the base rows of the RoPE tables: the plain
 // offsets, the offsets in the lanes' order, the fp16 hi / lo turn table
@@ -276,7 +280,10 @@ struct DecodeArgs {
   const uint16_t* q;
   const int32_t* seq_lens;
   float* out;
-  int splits;
+  int splits;        // blocks per (layer, sequence, kv head) in the grid (the block budget)
+  int min_chunk;     // tensor-core decode: least tiles per chunk of a unit
+  int fixed_splits;  // 1: the caller fixed `splits`, so no unit is cut into more chunks
+  int chunked;       // 1: plan chunks by tile count; 0: split every unit evenly
   uint32_t* status;
   uint32_t* tickets;
   float* partials;
