@@ -273,7 +273,7 @@ def score_distortion(w, cache, seq_lens, dev, seed):
             "what": "layer 0, sequence 0: max |q.(k_hat - k)| / sqrt(D) over the packed tokens, every query head"}
 
 
-def measure(wname, steps, warm, dev, rank, ws, headline=False, ablation=False, layers=0):
+def measure(wname, steps, warm, dev, rank, ws, headline=False, ablation=False, layers=0, batch=0):
     """Fills a workload's cache and times its decode steps.  Returns a dict
     of figures (the headline also keeps the raw pieces of the JSON line)."""
     import torch
@@ -283,8 +283,8 @@ def measure(wname, steps, warm, dev, rank, ws, headline=False, ablation=False, l
 
     extra = 3 * (steps + warm) + 16  # fused steps, unfused steps, end-to-end steps
     w = W.make(wname, extra_tokens=extra)
-    if layers:
-        w = w.scaled(L=layers, lengths=w.lengths, extra=extra)
+    if layers or batch:
+        w = w.scaled(L=layers or None, lengths=w.lengths[: batch or len(w.lengths)], extra=extra)
     cfg = w.cfg
     L, B, H, Hq, D = cfg.L, cfg.batch, cfg.H_kv, cfg.H_q, cfg.D
     stream = torch.cuda.current_stream(dev)
@@ -511,7 +511,7 @@ def run_ours(args):
     head = args.workload or HEADLINE
     side = [] if (args.workload or args.only_headline) else [x for x in WORKLOADS if x != head]
     main = measure(head, args.steps, args.warmup, dev, rank, ws, headline=True, ablation=args.ablation,
-                   layers=args.layers)
+                   layers=args.layers, batch=args.batch)
     rows = {head: _per_config_row(main)}
     for wname in side:
         r = measure(wname, min(args.steps, SIDE_STEPS), 3, dev, rank, ws)
@@ -579,16 +579,23 @@ def run_ours(args):
 DECODE_TRAFFIC = {
     "llama2_7b_kivi4": {"sha256": "3d355fc169ef465b96786ccd7979d3abe4d1cb12e7b72d211a7d6ca1725178bf",
                         "bytes_per_layer": (610.753024e6 + 11.729408e6) / 4},
+    # a 2-layer step (64 sequences x 32768 tokens) captured whole, halved
+    "mistral7b_hotcold": {"sha256": "5198fccaa304bb10b118647fb8b903e6683b50d7b452e20581f4263f45a321f1",
+                          "bytes_per_layer": (3026.939648e6 + 22.270464e6) / 2},
 }
-_TRAFFIC_SOURCES = ("decode_mma.cuh", "decode_step_kivi.cu", "append_generic.cuh", "append_common.cuh",
-                    "block_codec.cuh")
+# the sources each workload's decode-step kernel is built from
+_COMMON_SOURCES = ("decode_mma.cuh", "append_generic.cuh", "append_common.cuh", "block_codec.cuh")
+_TRAFFIC_SOURCES = {
+    "llama2_7b_kivi4": _COMMON_SOURCES[:1] + ("decode_step_kivi.cu",) + _COMMON_SOURCES[1:],
+    "mistral7b_hotcold": _COMMON_SOURCES + ("decode_step_d128.cu", "split_combine.cuh", "kvq_internal.cuh"),
+}
 
 
-def _kernel_sha() -> str:
+def _kernel_sha(workload: str) -> str:
     import hashlib
 
     h = hashlib.sha256()
-    for f in _TRAFFIC_SOURCES:
+    for f in _TRAFFIC_SOURCES.get(workload, ()):
         with open(os.path.join(ROOT, "bit_kv_cache_04_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -596,7 +603,7 @@ def _kernel_sha() -> str:
 
 def _traffic(workload: str, layers: int):
     rec = DECODE_TRAFFIC.get(workload)
-    if rec is None or rec["sha256"] != _kernel_sha():
+    if rec is None or rec["sha256"] != _kernel_sha(workload):
         return None
     return round(rec["bytes_per_layer"] * layers)
 
@@ -913,6 +920,8 @@ def main():
                     help="also time the unfused path: kvq_dequantize to fp32, then dense attention (torch)")
     ap.add_argument("--layers", type=int, default=0,
                     help="use only this many layers of the headline workload (small cases for profiler captures)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="use only the first this many sequences of the headline workload (profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

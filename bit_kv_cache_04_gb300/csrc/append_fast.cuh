@@ -699,11 +699,12 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_token32_kernel(Append
 // row (D blocks) is built in shared memory and written out whole.
 constexpr int kGroupSteps = 2;
 
-// One tier (the pair quantizers, no 32-value float arrays): 72 registers and
-// seven CTAs per SM hide more of the load latency; measured faster than five
-// or six CTAs even where the asymmetric body spills a few words.
+// One tier, or symmetric tiers (the pair quantizers and the direct cold rule,
+// no 32-value float arrays in line): 72 registers and seven CTAs per SM hide
+// more of the load latency; measured faster than five or six CTAs even where
+// the asymmetric body spills a few words.
 template <int CB, bool Z>
-constexpr int channel_ctas() { return CB == 0 ? 7 : 5; }
+constexpr int channel_ctas() { return CB == 0 || (CB == 2 && !Z) ? 7 : 5; }
 
 template <int NC, int DT, int B, int CB, int which, bool Z>
 __global__ void __launch_bounds__(kAppendThreads, channel_ctas<CB, Z>()) quant_channel32_kernel(AppendArgs a) {
