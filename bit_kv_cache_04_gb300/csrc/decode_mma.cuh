@@ -1037,10 +1037,10 @@ __device__ __forceinline__ Work plan_work(const DecodeArgs& a, Work* sw) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     Work w{};
-    // even split of every unit: one block per unit, a multi-wave grid (the
-    // block scheduler balances it), batches too large to plan, or (found
-    // below) equal tile counts
-    bool even = S == 1 || !a.chunked || B > kChunkSeqs || lo.max_T >= (1 << 26);
+    // even split of every unit: one block per unit, one sequence, a
+    // multi-wave grid (the block scheduler balances it), batches too large to
+    // plan, or (found below) equal tile counts
+    bool even = S == 1 || B == 1 || !a.chunked || B > kChunkSeqs || lo.max_T >= (1 << 26);
     constexpr int kPer = kChunkSeqs / 32;
     int n[kPer], bad[kPer], T[kPer], maxn = 0, minn = 0x7FFFFFFF, sum = 0;
     // lane l holds sequences [l per, (l + 1) per)
