@@ -86,6 +86,16 @@ def test_full_size_decode_and_codes(name):
     torch.cuda.synchronize()
     assert torch.isfinite(out).all()
     assert cache.device_status() == 0
+    # the sampled layers again as single-layer calls (the split planner's
+    # chunks, and the two-level merge where a unit has 32 or more): the same
+    # outputs up to the order of the fp32 sums, which over up to 1024 groups
+    # of a sequence stays within 1024 * 2^-24 ~ 6e-5
+    for layer in sorted({x[0] for x in SAMPLES[name]}):
+        o1 = torch.full_like(out[layer:layer + 1], float("nan"))
+        cache.decode(layer, 1, q[layer:layer + 1].contiguous(), seq_lens, o1)
+        torch.cuda.synchronize()
+        assert cache.device_status() == 0
+        assert rel_err(o1.cpu().numpy(), out[layer:layer + 1].cpu().numpy()) < 1e-4, (layer, K.kvq_decode_splits(cfg, 1))
     qh = raw16(q)
     g = cfg.H_q // cfg.H_kv
     lengths = [w.lengths[b] for b in range(cfg.batch)]

@@ -109,6 +109,10 @@ def test_split_count_does_not_matter(name):
     for s in (2, 5, 16):
         _, o = _decode(cache, w, seq_lens, splits=s)
         assert rel_err(o.cpu().numpy(), base.cpu().numpy()) < 1e-5, s
+    # one layer in 48 chunks per unit (the workspace holds up to 64 for one
+    # layer): units of 32 chunks or more merge in two levels
+    _, o = _decode(cache, w, seq_lens, n_layers=1, splits=48)
+    assert rel_err(o.cpu().numpy(), base[:1].cpu().numpy()) < 1e-5
 
 
 def test_per_layer_calls_equal_multi_layer_call():
