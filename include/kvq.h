@@ -260,7 +260,16 @@ KVQ_API kvq_status kvq_commit_lengths(const kvq_config* cfg, const int32_t* cu_n
  *            out = sum_t softmax_t(q.k_t/sqrt(D)) v_t over the dequantized
  *            cache (keys RoPE-rotated at position t when stored pre-RoPE);
  *            0 for an empty sequence.
- *  num_splits: token splits per (layer, seq, kv head); 0 picks one. */
+ *  num_splits: blocks per (layer, seq, kv head), 1..256; 0 picks the
+ *            count (kvq_decode_splits).  With more than one, the tensor-core
+ *            decode plans on the device from all lengths: when its grid is
+ *            at most two waves of resident blocks, each unit of n tiles
+ *            (32 tokens) is cut into ceil(n / C) nearly equal chunks for the
+ *            smallest C that fits the budget, so long sequences get more
+ *            blocks and short ones fewer (with a count passed here, no unit
+ *            gets more than num_splits).  The result does not depend on the
+ *            split beyond the order of fp32 sums.  KVQ_ERR_WORKSPACE when the
+ *            workspace's partial rows cannot hold the blocks. */
 KVQ_API kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0,
                                 int32_t n_layers, const void* q, const int32_t* seq_lens, float* out,
                                 int32_t num_splits, void* workspace, size_t ws_bytes, void* stream);
@@ -291,7 +300,10 @@ KVQ_API kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_cache* cache
 /* Kernel launches one kvq_decode_step call makes (1 when fused). */
 KVQ_API kvq_status kvq_step_launches(const kvq_config* cfg, int32_t* launches);
 
-/* The split count kvq_decode_attention picks for num_splits = 0. */
+/* The block budget per (layer, seq, kv head) kvq_decode_attention takes for
+ * num_splits = 0: the count with the best fill of whole waves of resident
+ * blocks (the device's SM count), each block keeping at least 8 tiles of the
+ * longest possible sequence (48 for rotated formats). */
 KVQ_API kvq_status kvq_decode_splits(const kvq_config* cfg, int32_t n_layers, int32_t* splits);
 
 /* Dequantizes tokens [t0, t1) of (layer, seq) to fp32 k_out, v_out
