@@ -116,7 +116,13 @@ struct Cfg {
   // per-lane query fragments (+ fp32 query for RoPE, + fp32 query by head for
   // the zero terms, + the lo fragments with heads as columns)
   static constexpr bool QH = HOT::KCH || (HAS_COLD && COLD::KCH);  // query half pairs (per-channel K)
-  static constexpr int QSM = KC * NT * 32 * (8 + (QH ? 8 : 0) + (ROPE ? 16 : 0) + (Z ? 8 : 0) + (HC ? 8 : 0));
+  // per-token K codes read as fp16 subnormals (see k_token_pairs): one tier of
+  // 8-, 4- or 3-bit uniform codes; KBLK K blocks per token row
+  static constexpr bool KSUB = !HOT::KCH && !HOT::KLUT && !HAS_COLD && !ROPE && !Z &&
+                               (HOT::KB == 8 || HOT::KB == 4 || HOT::KB == 3);
+  static constexpr int KBLK = HOT::KCH ? 1 : D / HOT::KG;
+  static constexpr int QSM = KC * NT * 32 * (8 + (QH ? 8 : 0) + (ROPE ? 16 : 0) + (Z ? 8 : 0) + (HC ? 8 : 0)) +
+                             (KSUB ? 4 * KBLK * NT * 8 : 0);
   static constexpr int MIN_CTAS = D == 128 ? 4 : 2;  // CTAs per SM the register budget aims at
   // groups in flight per warp: one consumed while STAGES - 1 land (D = 256 runs two CTAs per SM,
   // so each warp keeps two groups in flight)
@@ -297,30 +303,82 @@ __device__ __forceinline__ void dqt(uint32_t x, uint32_t (&r)[4], const uint32_t
   }
 }
 
+// Codes read as fp16 subnormals: a 16-bit field p below 0x800 is the fp16
+// value p 2^-24 exactly (subnormals and the first binade are one linear
+// scale), and the tensor cores multiply subnormal operands exactly.  So a
+// biased code n masked in place at bit position sh is the exact operand
+// n 2^sh 2^-24, one logic operation per pair and no conversion.  The 2^sh of
+// each position is taken out of the query fragment that meets it, the 2^-24
+// out of the score, and the storage bias beta by subtracting beta times the
+// sum of that query fragment (one constant per K block and column).
+// k_sub_shift(bits, odd_chunk, b1): log2 of the factor the codes meeting query
+// fragment b1 (else b0) of an odd (else even) k-chunk carry.
+__host__ __device__ constexpr int k_sub_shift(int bits, bool odd_chunk, bool b1) {
+  return bits == 4 ? (b1 ? 4 : 0) : bits == 3 ? (odd_chunk ? 6 : (b1 ? 3 : 0)) : 0;
+}
+__host__ __device__ constexpr int k_sub_bias(int bits) { return bits == 8 ? 128 : 1 << (bits - 1); }
+
+// A query fragment pair (b0, b1) of an even (ODD = false) or odd k-chunk with
+// the position factors of the subnormal codes multiplied back in.
+template <int BITS, bool ODD>
+__device__ __forceinline__ uint2 unsub_frag(uint2 q) {
+  constexpr int s0 = k_sub_shift(BITS, ODD, false), s1 = k_sub_shift(BITS, ODD, true);
+  constexpr uint32_t h0 = (uint32_t)(15 + s0) << 10, h1 = (uint32_t)(15 + s1) << 10;  // fp16 2^s
+  if constexpr (s0 != 0) q.x = hmul2u(q.x, h0 * 0x00010001u);
+  if constexpr (s1 != 0) q.y = hmul2u(q.y, h1 * 0x00010001u);
+  return q;
+}
+
 // Eight 3-bit K codes (channels c0..c0+7 of one token, bits 24 tq of the span
-// at byte off of the 4-byte aligned row) as four fp16 pairs (c0+j, c0+j+4).
+// at byte off of the 4-byte aligned row) as four fp16 pairs (c0+j, c0+j+4);
+// SUB: biased codes as subnormals at bit positions 0, 3, 6, 6.
+template <bool SUB = false>
 __device__ __forceinline__ void k_token_pairs3(const uint8_t* row, int off, int tq, uint32_t (&r)[4]) {
   const uint32_t w = ld_bits(row, off, 24 * tq);
   const uint32_t x = (w & 0xFFFu) | ((w << 4) & 0x0FFF0000u);
+  if constexpr (SUB) {
+    r[0] = x & 0x00070007u;
+    r[1] = x & 0x00380038u;
+    r[2] = x & 0x01C001C0u;
+    r[3] = (x >> 3) & 0x01C001C0u;
+  } else {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) r[j] = code_pair<3>(x, j);
+    for (int j = 0; j < 4; ++j) r[j] = code_pair<3>(x, j);
+  }
 }
 
 // Eight K codes (channels c0..c0+7 of one token) as four fp16 pairs
 // (c0+j, c0+j+4), j = 0..3.  `p` points at the first code byte of the span.
-template <class C>
+// SUB: biased codes as subnormals (4-bit: nibbles in place, positions 0 and
+// 4; 8-bit: the int8 code with its sign bit flipped, position 0).
+template <class C, bool SUB = false>
 __device__ __forceinline__ void k_token_pairs(const uint8_t* p, int tq, uint32_t (&r)[4], const uint32_t (&lut)[4]) {
   if constexpr (C::KLUT) {
     dqt(ld_u32e(p + 4 * tq), r, lut);
   } else if constexpr (C::KB == 4) {
-    dq4(ld_u32e(p + 4 * tq), r);
+    const uint32_t x = ld_u32e(p + 4 * tq);
+    if constexpr (SUB) {
+      r[0] = x & 0x000F000Fu;
+      r[1] = x & 0x00F000F0u;
+      r[2] = (x >> 8) & 0x000F000Fu;
+      r[3] = (x >> 8) & 0x00F000F0u;
+    } else {
+      dq4(x, r);
+    }
   } else if constexpr (C::KB == 8) {
     const uint32_t w0 = ld_u32e(p + 8 * tq), w1 = ld_u32e(p + 8 * tq + 4);
     const uint32_t xa = __byte_perm(w0, w1, 0x5410), xb = __byte_perm(w0, w1, 0x7632);
-    r[0] = code_pair8(xa, 0);
-    r[1] = code_pair8(xa, 1);
-    r[2] = code_pair8(xb, 0);
-    r[3] = code_pair8(xb, 1);
+    if constexpr (SUB) {
+      r[0] = (xa & 0x00FF00FFu) ^ 0x00800080u;
+      r[1] = ((xa >> 8) & 0x00FF00FFu) ^ 0x00800080u;
+      r[2] = (xb & 0x00FF00FFu) ^ 0x00800080u;
+      r[3] = ((xb >> 8) & 0x00FF00FFu) ^ 0x00800080u;
+    } else {
+      r[0] = code_pair8(xa, 0);
+      r[1] = code_pair8(xa, 1);
+      r[2] = code_pair8(xb, 0);
+      r[3] = code_pair8(xb, 1);
+    }
   } else {
     static_assert(C::KB != 3, "3-bit K codes: k_token_pairs3");
   }
@@ -482,6 +540,7 @@ struct Ctx {
   const uint2* qh;        // [KC][NT][32]: query half pairs
   const float4* qr;       // [KC][NT][32]: fp32 query (RoPE)
   const float* qz;        // [4 NT][D]: fp32 query by head, zero past g (asymmetric K)
+  const float* kq;        // [KBLK][NT][8 columns]: beta times the column's query sum per K block (KSUB)
   const float2* rope_base;
   const float4* rope_frag;  // [KC/2][4 tokens k][2 pairs][32 lanes]: (cos, cos, sin, sin) of R(j), lane's channels
   const uint4* rope_tab;    // [KC/2][4 tokens k][32 lanes][2]: fp16 hi / lo cos and sin of R(j), lane's channel pairs
@@ -936,11 +995,13 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
             if constexpr (TR::KB == 3) {
               static_assert(TR::KROW % 4 == 0 && C::STAGE % 4 == 0, "4-byte aligned rows");
               const int off = kb * TR::KBB + TR::HDR + ss * TR::KSPAN;
-              k_token_pairs3(ksm + ra * TR::KROW, off, tq, wa);
-              k_token_pairs3(ksm + (ra + 1) * TR::KROW, off, tq, wb);
+              k_token_pairs3<C::KSUB>(ksm + ra * TR::KROW, off, tq, wa);
+              k_token_pairs3<C::KSUB>(ksm + (ra + 1) * TR::KROW, off, tq, wb);
             } else {
-              k_token_pairs<TR>(ksm + ra * TR::KROW + kb * TR::KBB + TR::HDR + ss * TR::KSPAN, tq, wa, cx.lut);
-              k_token_pairs<TR>(ksm + (ra + 1) * TR::KROW + kb * TR::KBB + TR::HDR + ss * TR::KSPAN, tq, wb, cx.lut);
+              k_token_pairs<TR, C::KSUB>(ksm + ra * TR::KROW + kb * TR::KBB + TR::HDR + ss * TR::KSPAN, tq, wa,
+                                         cx.lut);
+              k_token_pairs<TR, C::KSUB>(ksm + (ra + 1) * TR::KROW + kb * TR::KBB + TR::HDR + ss * TR::KSPAN, tq, wb,
+                                         cx.lut);
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -963,10 +1024,20 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
           const float sb = block_scale(ksm + (4 * gq + 2 * mu + 1) * TR::KROW + kb * TR::KBB);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            S[mu][nt][0] += acc[mu][nt][0] * sa;
-            S[mu][nt][1] += acc[mu][nt][1] * sa;
-            S[mu][nt][2] += acc[mu][nt][2] * sb;
-            S[mu][nt][3] += acc[mu][nt][3] * sb;
+            if constexpr (C::KSUB) {
+              // subnormal codes: (2^24 acc - beta sum of the column's query) s
+              const float2 kq = reinterpret_cast<const float2*>(cx.kq)[(kb * NT + nt) * 4 + tq];
+              const float ua = sa * 0x1p24f, ub = sb * 0x1p24f;
+              S[mu][nt][0] = fmaf(acc[mu][nt][0], ua, fmaf(-kq.x, sa, S[mu][nt][0]));
+              S[mu][nt][1] = fmaf(acc[mu][nt][1], ua, fmaf(-kq.y, sa, S[mu][nt][1]));
+              S[mu][nt][2] = fmaf(acc[mu][nt][2], ub, fmaf(-kq.x, sb, S[mu][nt][2]));
+              S[mu][nt][3] = fmaf(acc[mu][nt][3], ub, fmaf(-kq.y, sb, S[mu][nt][3]));
+            } else {
+              S[mu][nt][0] += acc[mu][nt][0] * sa;
+              S[mu][nt][1] += acc[mu][nt][1] * sa;
+              S[mu][nt][2] += acc[mu][nt][2] * sb;
+              S[mu][nt][3] += acc[mu][nt][3] * sb;
+            }
           }
         }
       }
@@ -1268,6 +1339,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   float4* qr = reinterpret_cast<float4*>(qh + (C::QH ? KC * NT * 32 : 0));  // [KC][NT][32]: fp32 query (RoPE)
   float* qz = reinterpret_cast<float*>(qr + (C::ROPE ? KC * NT * 32 : 0));  // [4 NT][D] (asymmetric K)
   uint2* qbl = reinterpret_cast<uint2*>(qz + (C::Z ? 4 * NT * D : 0));     // [KC][NT][32 lanes]: lo (HC)
+  float* kq = reinterpret_cast<float*>(qbl + (C::HC ? KC * NT * 32 : 0));  // [KBLK][NT][8] (KSUB)
   uint8_t* stage_base = smem + C::QSM;
   __shared__ float qmax_s[kWarps];
   __shared__ uint32_t bad_page;
@@ -1462,6 +1534,14 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
         v1 = q[c + 4] * qnorm;
         v2 = q[c + 1] * qnorm;
         v3 = q[c + 5] * qnorm;
+        if constexpr (C::KSUB) {  // the codes' position factors, taken out of the query (exact)
+          const float f0 = ldexpf(1.f, -k_sub_shift(C::HOT::KB, kc & 1, false));
+          const float f1 = ldexpf(1.f, -k_sub_shift(C::HOT::KB, kc & 1, true));
+          v0 *= f0;
+          v1 *= f0;
+          v2 *= f1;
+          v3 *= f1;
+        }
       }
       qb[e] = make_uint2(pack_h2(split_part(v0, lo), split_part(v1, lo)),
                          pack_h2(split_part(v2, lo), split_part(v3, lo)));
@@ -1475,6 +1555,33 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
       for (int e = tid; e < 4 * NT * D; e += kThreadsMma) {
         const int hh = e / D;
         qz[e] = hh < g ? qf[e] * qnorm : 0.f;
+      }
+    }
+    if constexpr (C::KSUB) {
+      // beta times the sum, over each K block's channels, of the fp16 values
+      // each column's MMAs multiply (the fragments times their position
+      // factors; hi and lo fragments with heads as columns)
+      __syncthreads();
+      constexpr int CPB = KC / C::KBLK;  // k-chunks per K block
+      for (int e = tid; e < C::KBLK * NT * 8; e += kThreadsMma) {
+        const int col = e & 7, nt = (e >> 3) % NT, kb = (e >> 3) / NT;
+        float sum = 0.f;
+        for (int kc = kb * CPB; kc < (kb + 1) * CPB; ++kc) {
+          const float f0 = ldexpf(1.f, k_sub_shift(C::HOT::KB, kc & 1, false));
+          const float f1 = ldexpf(1.f, k_sub_shift(C::HOT::KB, kc & 1, true));
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int i = (kc * NT + nt) * 32 + 4 * col + t;
+            uint2 fr[2] = {qb[i], C::HC ? qbl[i] : make_uint2(0u, 0u)};
+#pragma unroll
+            for (int u = 0; u < (C::HC ? 2 : 1); ++u) {
+              const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&fr[u].x));
+              const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&fr[u].y));
+              sum += f0 * (x.x + x.y) + f1 * (y.x + y.y);
+            }
+          }
+        }
+        kq[e] = (float)k_sub_bias(C::HOT::KB) * sum;
       }
     }
     __syncthreads();
@@ -1493,6 +1600,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   cx.qh = qh;
   cx.qr = qr;
   cx.qz = qz;
+  cx.kq = kq;
   cx.g = g;
   cx.rope_base = a.rope;
   cx.rope_frag = reinterpret_cast<const float4*>(a.rope + (int64_t)(a.rope_base_rows + kTile) * (D / 2));
@@ -1641,13 +1749,26 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
             const uint32_t b2 = __byte_perm(vb.y, vb.w, 0x5410), b3 = __byte_perm(vb.y, vb.w, 0x7632);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              const uint2 q0 = qb[((2 * s) * NT + nt) * 32 + lane];
-              const uint2 q1 = qb[((2 * s + 1) * NT + nt) * 32 + lane];
+              uint2 q0 = qb[((2 * s) * NT + nt) * 32 + lane];
+              uint2 q1 = qb[((2 * s + 1) * NT + nt) * 32 + lane];
+              uint2 r0, r1;
+              if constexpr (C::HC) {
+                r0 = cx.qbl[((2 * s) * NT + nt) * 32 + lane];
+                r1 = cx.qbl[((2 * s + 1) * NT + nt) * 32 + lane];
+              }
+              if constexpr (C::KSUB) {
+                // 16-bit keys carry no position factors: put them back into
+                // the query fragments (powers of two)
+                q0 = unsub_frag<C::HOT::KB, false>(q0);
+                q1 = unsub_frag<C::HOT::KB, true>(q1);
+                if constexpr (C::HC) {
+                  r0 = unsub_frag<C::HOT::KB, false>(r0);
+                  r1 = unsub_frag<C::HOT::KB, true>(r1);
+                }
+              }
               mma16816(S[mu][nt], a0, b0, a1, b1, q0.x, q0.y);
               mma16816(S[mu][nt], a2, b2, a3, b3, q1.x, q1.y);
               if constexpr (C::HC) {
-                const uint2 r0 = cx.qbl[((2 * s) * NT + nt) * 32 + lane];
-                const uint2 r1 = cx.qbl[((2 * s + 1) * NT + nt) * 32 + lane];
                 mma16816(S[mu][nt], a0, b0, a1, b1, r0.x, r0.y);
                 mma16816(S[mu][nt], a2, b2, a3, b3, r1.x, r1.y);
               }
