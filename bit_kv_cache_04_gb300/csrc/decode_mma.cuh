@@ -121,6 +121,13 @@ struct Cfg {
   static constexpr bool KSUB = !HOT::KCH && !HOT::KLUT && !HAS_COLD && !ROPE && !Z &&
                                (HOT::KB == 8 || HOT::KB == 4 || HOT::KB == 3);
   static constexpr int KBLK = HOT::KCH ? 1 : D / HOT::KG;
+  // V codes read as subnormals (see v_pair4): one tier of 8-, 4- or 2-bit
+  // uniform codes, not with heads as columns (there the bias MMAs of the hi
+  // and lo fragments cost more than the conversions they replace); NBV V
+  // blocks per token row
+  static constexpr bool VSUB =
+      !HAS_COLD && !Z && !HC && !HOT::VLUT && (HOT::VB == 8 || HOT::VB == 4 || HOT::VB == 2);
+  static constexpr int NBV = D / HOT::VG;
   static constexpr int QSM = KC * NT * 32 * (8 + (QH ? 8 : 0) + (ROPE ? 16 : 0) + (Z ? 8 : 0) + (HC ? 8 : 0)) +
                              (KSUB ? 4 * KBLK * NT * 8 : 0);
   static constexpr int MIN_CTAS = D == 128 ? 4 : 2;  // CTAs per SM the register budget aims at
@@ -318,6 +325,16 @@ __host__ __device__ constexpr int k_sub_shift(int bits, bool odd_chunk, bool b1)
 }
 __host__ __device__ constexpr int k_sub_bias(int bits) { return bits == 8 ? 128 : 1 << (bits - 1); }
 
+// v_sub_shift(bits, j): log2 of the factor the V code of channel 4 gq + j of
+// a span carries (4-bit nibbles in place: 0, 4, 0, 4; 2-bit fields 0, 2, 4, 6).
+__host__ __device__ constexpr int v_sub_shift(int bits, int j) {
+  return bits == 4 ? ((j & 1) ? 4 : 0) : bits == 2 ? 2 * j : 0;
+}
+// fp16 pair of -beta 2^v_sub_shift 2^-24 (a negative subnormal, exact).
+__host__ __device__ constexpr uint32_t v_sub_neg(int bits, int j) {
+  return (0x8000u | ((uint32_t)(1 << (bits - 1)) << v_sub_shift(bits, j))) * 0x00010001u;
+}
+
 // A query fragment pair (b0, b1) of an even (ODD = false) or odd k-chunk with
 // the position factors of the subnormal codes multiplied back in.
 template <int BITS, bool ODD>
@@ -387,16 +404,24 @@ __device__ __forceinline__ void k_token_pairs(const uint8_t* p, int tq, uint32_t
 // Four V codes (channels 4*gq..4*gq+3 of a span) of token rows ra and rb as
 // four fp16 pairs (row a, row b) for channel 4gq+j.  p* point at the span's
 // first code byte of each row.
-template <class C>
+// SUB: biased codes as subnormals at the positions of v_sub_shift.
+template <class C, bool SUB = false>
 __device__ __forceinline__ void v_pair4(const uint8_t* pa, const uint8_t* pb, int gq, uint32_t (&r)[4],
                                         const uint32_t (&lut)[4]) {
   if constexpr (C::VB == 8) {
     const uint32_t wa = ld_u32e(pa + 4 * gq), wb = ld_u32e(pb + 4 * gq);
     const uint32_t xa = __byte_perm(wa, wb, 0x5410), xb = __byte_perm(wa, wb, 0x7632);
-    r[0] = code_pair8(xa, 0);
-    r[1] = code_pair8(xa, 1);
-    r[2] = code_pair8(xb, 0);
-    r[3] = code_pair8(xb, 1);
+    if constexpr (SUB) {
+      r[0] = (xa & 0x00FF00FFu) ^ 0x00800080u;
+      r[1] = ((xa >> 8) & 0x00FF00FFu) ^ 0x00800080u;
+      r[2] = (xb & 0x00FF00FFu) ^ 0x00800080u;
+      r[3] = ((xb >> 8) & 0x00FF00FFu) ^ 0x00800080u;
+    } else {
+      r[0] = code_pair8(xa, 0);
+      r[1] = code_pair8(xa, 1);
+      r[2] = code_pair8(xb, 0);
+      r[3] = code_pair8(xb, 1);
+    }
   } else {
     static_assert(C::VB != 3, "3-bit V codes: v_pair4_3");
     uint32_t ua, ub;
@@ -410,6 +435,16 @@ __device__ __forceinline__ void v_pair4(const uint8_t* pa, const uint8_t* pb, in
     const uint32_t x = __byte_perm(ua, ub, 0x5410);
     if constexpr (C::VLUT) {
       dqt(x, r, lut);
+    } else if constexpr (SUB && C::VB == 4) {
+      r[0] = x & 0x000F000Fu;
+      r[1] = x & 0x00F000F0u;
+      r[2] = (x >> 8) & 0x000F000Fu;
+      r[3] = (x >> 8) & 0x00F000F0u;
+    } else if constexpr (SUB) {  // 2 bits
+      r[0] = x & 0x00030003u;
+      r[1] = x & 0x000C000Cu;
+      r[2] = x & 0x00300030u;
+      r[3] = x & 0x00C000C0u;
     } else if constexpr (C::VB == 4) {
       dq4(x, r);
     } else {
@@ -437,6 +472,28 @@ struct WarpState {
   // (for the lane's head 4 nt + tq), rescaled with o
   float zo[C::Z ? C::NS : 1][C::NT];
 };
+
+// Subnormal V codes: the output so far from 2^-24 units with position factors
+// (row gq of d-tile (s, e) holds channel 4 gq + 2 e, row gq + 8 channel
+// 4 gq + 2 e + 1 of span s) back to plain units.  Linear in o, so it may run
+// at any point between groups; it runs once per warp, before any 16-bit
+// window group adds plain products.
+template <class C>
+__device__ __forceinline__ void vsub_finish(WarpState<C>& ws) {
+  if constexpr (C::VSUB) {
+    constexpr int VB = C::HOT::VB;
+#pragma unroll
+    for (int sp = 0; sp < C::NS; ++sp)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            ws.o[2 * sp + e][nt][k] *= ldexpf(1.f, 24 - v_sub_shift(VB, 2 * e + (k >> 1)));
+          }
+  }
+}
 
 // Online softmax over one group's scores; returns the probabilities of the
 // thread's four tokens 4gq..4gq+3 for each n-tile.
@@ -507,6 +564,7 @@ __device__ __forceinline__ void online_softmax(WarpState<C>& ws, float (&S)[2][C
 #pragma unroll
           for (int s2 = 0; s2 < C::NS; ++s2) ws.zo[s2][nt] *= alpha;
         }
+
       }
     }
   }
@@ -679,8 +737,9 @@ __device__ __forceinline__ void pv_packed(const Ctx<C>& cx, WarpState<C>& ws, co
             v_pair4_3(vsm + T1 * TR::VROW, vsm + (T1 + 4) * TR::VROW, off, gq, x12);
             v_pair4_3(vsm + (T1 + 1) * TR::VROW, vsm + (T1 + 5) * TR::VROW, off, gq, x34);
           } else {
-            v_pair4<TR>(vsm + T1 * TR::VROW + off, vsm + (T1 + 4) * TR::VROW + off, gq, x12, cx.lut);
-            v_pair4<TR>(vsm + (T1 + 1) * TR::VROW + off, vsm + (T1 + 5) * TR::VROW + off, gq, x34, cx.lut);
+            v_pair4<TR, C::VSUB>(vsm + T1 * TR::VROW + off, vsm + (T1 + 4) * TR::VROW + off, gq, x12, cx.lut);
+            v_pair4<TR, C::VSUB>(vsm + (T1 + 1) * TR::VROW + off, vsm + (T1 + 5) * TR::VROW + off, gq, x34,
+                                 cx.lut);
           }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
@@ -689,6 +748,19 @@ __device__ __forceinline__ void pv_packed(const Ctx<C>& cx, WarpState<C>& ws, co
             if constexpr (C::HC) {
               mma16816(ws.o[2 * s][nt], x12[0], x12[1], x34[0], x34[1], pbl[mu][nt][0], pbl[mu][nt][1]);
               mma16816(ws.o[2 * s + 1][nt], x12[2], x12[3], x34[2], x34[3], pbl[mu][nt][0], pbl[mu][nt][1]);
+            }
+            if constexpr (C::VSUB) {
+              // the storage bias, removed in the same accumulator with every
+              // group (rows: -beta 2^sh 2^-24 of their channel), so that o
+              // never carries beta times the running probability sum
+              constexpr uint32_t n0 = v_sub_neg(TR::VB, 0), n1 = v_sub_neg(TR::VB, 1);
+              constexpr uint32_t n2 = v_sub_neg(TR::VB, 2), n3 = v_sub_neg(TR::VB, 3);
+              mma16816(ws.o[2 * s][nt], n0, n1, n0, n1, pb[mu][nt][0], pb[mu][nt][1]);
+              mma16816(ws.o[2 * s + 1][nt], n2, n3, n2, n3, pb[mu][nt][0], pb[mu][nt][1]);
+              if constexpr (C::HC) {
+                mma16816(ws.o[2 * s][nt], n0, n1, n0, n1, pbl[mu][nt][0], pbl[mu][nt][1]);
+                mma16816(ws.o[2 * s + 1][nt], n2, n3, n2, n3, pbl[mu][nt][0], pbl[mu][nt][1]);
+              }
             }
           }
         }
@@ -1633,6 +1705,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
     for (int s = 0; s < (C::Z ? C::NS : 1); ++s) ws.zo[s][nt] = 0.f;
+
   }
   // ---- per-warp pipeline over this CTA's groups --------------------------------
   // the query scratch was written through the generic proxy: order it before
@@ -1644,6 +1717,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     for (int i = kStages - QSLOTS; i < kStages - 1; ++i) issue(first + kWarps * i, i);
   }
   int stall_it = -1;
+  bool vsub_done = false;  // subnormal V: o is in plain units
   for (int it = 0;; ++it) {
     const int tile = first + kWarps * it;
     if (tile >= te) break;
@@ -1689,6 +1763,10 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
       }
     } else {
       // ---------------- 16-bit window group from global memory ----------------
+      if (!vsub_done) {  // a warp's window groups come after all its packed groups
+        vsub_finish<C>(ws);
+        vsub_done = true;
+      }
       const int t0 = qe + (tile - n_c - n_m) * kTile;
       const int n_valid = min(kTile, T - t0);
       if constexpr (C::ROPE) {
@@ -1828,6 +1906,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     fence_proxy_async();
     __syncwarp();
   }
+  if (!vsub_done) vsub_finish<C>(ws);
   if (lo.paged && lane == 0) cp_async_wait<0>();  // a page-id copy issued for a tile not reached
   if (stall_it >= 0) {
     // a copy did not land in time: flag it, give this warp's copies still in
