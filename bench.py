@@ -691,14 +691,27 @@ def unfused_ablation(cache, cfg, w, seq_lens, stream, layers=4):
 # ---------------------------------------------------------------------------
 
 
+# Arm implementer / part codes of /proc/cpuinfo (it has no model name on Arm)
+_ARM_PARTS = {(0x41, 0xD4F): "Arm Neoverse-V2", (0x41, 0xD40): "Arm Neoverse-V1", (0x41, 0xD0C): "Arm Neoverse-N1",
+              (0x41, 0xD49): "Arm Neoverse-N2", (0x41, 0xD8E): "Arm Neoverse-N3", (0x41, 0xD84): "Arm Neoverse-V3"}
+
+
 def _cpu_model() -> str:
+    impl = part = None
     try:
         with open("/proc/cpuinfo") as fh:
             for line in fh:
-                if line.lower().startswith(("model name", "cpu model")):
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model"):
                     return line.split(":", 1)[1].strip()
-    except OSError:
+                if key == "cpu implementer" and impl is None:
+                    impl = int(line.split(":", 1)[1].strip(), 0)
+                if key == "cpu part" and part is None:
+                    part = int(line.split(":", 1)[1].strip(), 0)
+    except (OSError, ValueError):
         pass
+    if impl is not None and part is not None:
+        return _ARM_PARTS.get((impl, part), f"aarch64 (implementer {impl:#x}, part {part:#x})")
     import platform
 
     return platform.processor() or platform.machine()
