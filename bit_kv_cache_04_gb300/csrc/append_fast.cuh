@@ -541,6 +541,19 @@ __device__ __forceinline__ void block32_zp_x2(const uint32_t (&raw)[32], float2 
   }
 }
 
+// Rows [r0, r1) of a shared tile of W-word rows (row r at src + 4 W r) to
+// their destinations d[r], skipping null ones: word e of the run goes to
+// thread e mod blockDim.x.
+template <int W>
+__device__ __forceinline__ void rows_out(uint8_t* const* d, const uint8_t* src, int r0, int r1) {
+  const uint32_t* s = reinterpret_cast<const uint32_t*>(src);
+  for (int e = r0 * W + (int)threadIdx.x; e < r1 * W; e += blockDim.x) {
+    const int r = e / W;
+    uint32_t* row = reinterpret_cast<uint32_t*>(d[r]);
+    if (row) row[e - r * W] = s[e];
+  }
+}
+
 // Per-token 32-value blocks: a block of 128 threads takes 128 consecutive
 // tokens of one (layer, sequence, kv head); thread j quantizes token row j
 // slice by slice.  At D = 128 (when the static shared memory allows) the rows
@@ -561,11 +574,12 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_token32_kernel(Append
   constexpr int CBB = CB ? HDR + 4 * CB : 0, CROW = SPR * CBB;
   constexpr int OUTB = kTokItem * (ROW > CROW ? ROW : CROW);
   // staged rows: one pass, and the stage fits the 48 KB of static shared memory
-  constexpr bool STAGED = NC == 1 && OUTB + kTokItem * (16 * kStageChunks + 8) + 64 <= 48 * 1024;
+  constexpr bool STAGED = NC == 1 && OUTB + kTokItem * (16 * kStageChunks + 16) + 64 <= 48 * 1024;
   static_assert(kTokItem == kAppendThreads, "one token row per thread");
   __shared__ __align__(16) uint8_t out[OUTB];
   __shared__ __align__(16) uint4 stage[STAGED ? kTokItem * kStageChunks : 1];
   __shared__ const uint4* rowp[STAGED ? kTokItem : 1];
+  __shared__ uint8_t* rowd[kTokItem];  // tiered or paged: each row's destination
   __shared__ uint32_t page_bad;
   const Layout& lo = a.lo;
   const int li = blockIdx.z / lo.B, seq = blockIdx.z % lo.B, h = blockIdx.y;
@@ -673,22 +687,20 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_token32_kernel(Append
     if (span_ok(lo, a.cp, which, dst, (int64_t)n_tok * ROW)) block_copy_out(dst, out, n_tok * ROW);
     return;
   }
-  // tiered or paged: whole rows, one warp per row
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < n_tok; r += kAppendThreads / 32) {
-    const bool cold = CB != 0 && lo.tiered && u0 + r < c1;
-    const int rowb = cold ? CROW : ROW;
+  // tiered or paged: thread j finds token row j's destination (a row of a
+  // page, of the hot ring or of the cold tier); then the block writes the
+  // tile word by word, consecutive threads on consecutive words, so that a
+  // run of consecutive rows goes out as whole lines
+  if (j < n_tok) {
     bool bad = false;
-    uint8_t* dst = cold ? cold_row(lo, a.cp, which, layer, seq, h, u0 + r)
-                        : main_row(lo, a.cp, which, layer, seq, h, u0 + r, &bad);
-    if (bad) {
-      page_bad = 1;
-      continue;
-    }
-    for (int e = lane; e < rowb / 4; e += 32)
-      reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(out + r * rowb)[e];
+    uint8_t* d = to_cold ? cold_row(lo, a.cp, which, layer, seq, h, t) : main_row(lo, a.cp, which, layer, seq, h, t, &bad);
+    if (bad) page_bad = 1;
+    rowd[j] = bad ? nullptr : d;
   }
   __syncthreads();
+  const int n_c = CB != 0 && lo.tiered ? min(max(c1 - u0, 0), n_tok) : 0;
+  if constexpr (CB != 0) rows_out<CROW / 4>(rowd, out, 0, n_c);
+  rows_out<ROW / 4>(rowd, out, n_c, n_tok);
   if (threadIdx.x == 0 && page_bad) atomicOr(a.status, KVQ_DEV_PAGE);
 }
 
