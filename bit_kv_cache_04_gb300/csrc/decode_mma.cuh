@@ -649,12 +649,17 @@ __device__ __forceinline__ void rope_query_f32(const Ctx<C>& cx, const float2* b
   }
 }
 
-// fp16 pair of (x0, x1) for this lane's B column: the values rounded to fp16
-// (m = 0: hi columns) or the fp16 rounding of their remainders x - fp16(x)
-// (m = 1: lo columns); x - fp16(x) is exact in fp32.
-__device__ __forceinline__ uint32_t col_pair(float x0, float x1, float m) {
+// fp16 pair of the packed fp32 pair X for this lane's B column: the values
+// rounded to fp16 (NM = (-0, -0): hi columns) or the fp16 rounding of their
+// remainders x - fp16(x) (NM = (-1, -1): lo columns); x - fp16(x) is exact in
+// fp32.
+__device__ __forceinline__ uint32_t col_pair(uint64_t X, uint64_t NM) {
+  float x0, x1;
+  upk2(X, x0, x1);
   const float2 b = __half22float2(__floats2half2_rn(x0, x1));
-  return pack_h2(fmaf(-m, b.x, x0), fmaf(-m, b.y, x1));
+  float r0, r1;
+  upk2(fma2(NM, pk2(b.x, b.y), X), r0, r1);
+  return pack_h2(r0, r1);
 }
 
 // Key values of lower channels ch[0..3] (L: pairs (ch0, ch1), (ch2, ch3))
@@ -786,7 +791,7 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
       // sin; the B operands are the scaled, turned query in hi / lo columns.
       // Per k-chunk pair: 16 MMAs on two accumulator chains.
       const float2* base = cx.rope_base + (int64_t)(t0 / kTile) * (D / 2);
-      const float mlo = cx.lo_part ? 1.f : 0.f;
+      const uint64_t NM = cx.lo_part ? pk2(-1.f, -1.f) : pk2(-0.f, -0.f);
       float Sx[2][NT][4];
 #pragma unroll
       for (int mu = 0; mu < 2; ++mu)
@@ -831,17 +836,21 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
         }
         // B fragments of this lane's column (head gq / 2, hi or lo part)
         uint32_t bcl[NT][2], bsl[NT][2], bcu[NT][2], bsu[NT][2];
+        const uint64_t L01 = pk2(sl[0], sl[1]), L23 = pk2(sl[2], sl[3]);
+        const uint64_t U01 = pk2(su[0], su[1]), U23 = pk2(su[2], su[3]);
+        const uint64_t N01 = pk2(-su[0], -su[1]), N23 = pk2(-su[2], -su[3]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const float4 a = ql[nt], b = qu[nt];
-          bcl[nt][0] = col_pair(sl[0] * a.x, sl[1] * a.y, mlo);
-          bcl[nt][1] = col_pair(sl[2] * a.z, sl[3] * a.w, mlo);
-          bsl[nt][0] = col_pair(sl[0] * b.x, sl[1] * b.y, mlo);
-          bsl[nt][1] = col_pair(sl[2] * b.z, sl[3] * b.w, mlo);
-          bcu[nt][0] = col_pair(su[0] * b.x, su[1] * b.y, mlo);
-          bcu[nt][1] = col_pair(su[2] * b.z, su[3] * b.w, mlo);
-          bsu[nt][0] = col_pair(-su[0] * a.x, -su[1] * a.y, mlo);
-          bsu[nt][1] = col_pair(-su[2] * a.z, -su[3] * a.w, mlo);
+          const uint64_t a01 = pk2(ql[nt].x, ql[nt].y), a23 = pk2(ql[nt].z, ql[nt].w);
+          const uint64_t b01 = pk2(qu[nt].x, qu[nt].y), b23 = pk2(qu[nt].z, qu[nt].w);
+          bcl[nt][0] = col_pair(mul2(L01, a01), NM);
+          bcl[nt][1] = col_pair(mul2(L23, a23), NM);
+          bsl[nt][0] = col_pair(mul2(L01, b01), NM);
+          bsl[nt][1] = col_pair(mul2(L23, b23), NM);
+          bcu[nt][0] = col_pair(mul2(U01, b01), NM);
+          bcu[nt][1] = col_pair(mul2(U23, b23), NM);
+          bsu[nt][0] = col_pair(mul2(N01, a01), NM);
+          bsu[nt][1] = col_pair(mul2(N23, a23), NM);
         }
         const uint4* tb = cx.rope_tab + (kcp * 4 * 2) * 32 + lane;  // [k][cos / sin][lane]
 #pragma unroll
