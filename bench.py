@@ -577,11 +577,11 @@ def run_ours(args):
 # with the SHA-256 of the kernel sources it was taken on; the roofline reports
 # them scaled to the timed launch while those sources are unchanged, else null.
 DECODE_TRAFFIC = {
-    "llama2_7b_kivi4": {"sha256": "e8937c0c255be1cf8e436bf84d9a8a79564118f47567d7c9c7e5d89168b1d94a",
-                        "bytes_per_layer": (610.572544e6 + 7.600384e6) / 4},
+    "llama2_7b_kivi4": {"sha256": "067138d798bf001e1492510820b2e742c0cd3d46432ad64481858f8688725a5f",
+                        "bytes_per_layer": (610.576128e6 + 7.600128e6) / 4},
     # a 2-layer step (64 sequences x 32768 tokens) captured whole, halved
-    "mistral7b_hotcold": {"sha256": "7e10c85152f2b0d79c1c31dee474c724a3e52faacc4db5359965a28a97d586f0",
-                          "bytes_per_layer": (3021.656064e6 + 17.421824e6) / 2},
+    "mistral7b_hotcold": {"sha256": "4870c541f8be49dd5bf9a94b24986e91bfe0755780e41a94f9a713e1d224dc32",
+                          "bytes_per_layer": (3021.635584e6 + 17.55392e6) / 2},
 }
 # the sources each workload's decode-step kernel is built from
 _COMMON_SOURCES = ("decode_mma.cuh", "append_generic.cuh", "append_common.cuh", "block_codec.cuh")

@@ -1263,12 +1263,13 @@ __device__ __forceinline__ Work plan_work(const DecodeArgs& a, Work* sw) {
       }
       if (lane == 0) *sw = w;
     } else {
-      const int N = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)sum), K = B * S;  // one layer's kv head
+      const int N = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)sum), K = a.budget;  // one layer's kv head
       int c_lo = max(max(a.min_chunk, 1), (maxn + kMaxSplits - 1) / kMaxSplits);
       if (a.fixed_splits) c_lo = max(c_lo, (maxn + S - 1) / S);
       // the smallest C >= c_lo with chunks(C) <= K: chunks(C) >= N / C, and
-      // chunks(C) < N / C + B, so it lies in [N / K, N / (K - B)] (K > B as
-      // S > 1), and C = maxn gives B chunks
+      // chunks(C) < N / C + B, so it lies in [N / K, N / (K - B)] (K > B: the
+      // host gives a budget of at least 2 B when S > 1), and C = maxn gives B
+      // chunks
       auto chunks = [&](int C) {
         const float rc = __frcp_rn((float)C);
         int c = 0;

@@ -273,6 +273,10 @@ int sm_count() {
 // D = 256), with at least 8 tiles per split and no more growth once the grid
 // holds 8 waves.
 constexpr int64_t kMinTilesPerSplit = 8, kMinTilesPerSplitRotated = 48;
+// The least tiles per chunk when the device plans chunks (rotated layouts):
+// with the one-wave budget a ragged batch of 2K-8K-token sequences decoded
+// per layer took 1.12 ms with a floor of 16, 24 or 32 tiles, 1.28 ms with 48.
+constexpr int kMinChunkRotated = 32;
 
 int splits_for(const kvq_config* c, int n_layers) {
   const int64_t units = (int64_t)n_layers * c->batch * c->H_kv;
@@ -302,17 +306,32 @@ int splits_for(const kvq_config* c, int n_layers) {
   return best;
 }
 
-// The chunking of the tensor-core decode (see plan_work): the least tiles per
-// chunk, whether the caller fixed the split count, and whether to plan chunks
-// by tile count at all (grids of up to two waves of resident blocks; larger
-// grids are balanced by the block scheduler).
-void set_chunking(const kvq_config* c, int num_splits, int n_layers, int splits, DecodeArgs* a) {
+// The grid and chunking of a decode call (see plan_work): the grid's blocks
+// per (layer, sequence, kv head) `*splits` (the caller's count, else
+// splits_for), the least tiles per chunk, whether the caller fixed the split
+// count, whether to plan chunks by tile count at all (grids of up to two
+// waves of resident blocks; larger grids are balanced by the block
+// scheduler), and the plan's budget of blocks per (layer, kv head).  A
+// planned call without a caller's count may use one whole wave of resident
+// blocks, shared by its (layer, kv head) pairs, even where that is not a
+// multiple of the batch: the grid then grows by up to one block per unit, and
+// blocks past the last chunk exit at once.
+void set_chunking(const kvq_config* c, int num_splits, int n_layers, int* splits, DecodeArgs* a) {
   const bool rotated = (c->flags & (KVQ_ROTATE_K | KVQ_ROTATE_V)) != 0;
-  const int64_t blocks = (int64_t)n_layers * c->batch * c->H_kv * splits;
+  const int64_t blocks = (int64_t)n_layers * c->batch * c->H_kv * *splits;
   const int64_t resident = (int64_t)sm_count() * (c->D == 128 ? 4 : 2);
   a->fixed_splits = num_splits ? 1 : 0;
-  a->min_chunk = num_splits ? 1 : (int)(rotated ? kMinTilesPerSplitRotated : kMinTilesPerSplit);
+  a->min_chunk = num_splits ? 1 : (int)(rotated ? kMinChunkRotated : kMinTilesPerSplit);
   a->chunked = (num_splits || blocks <= 2 * resident) ? 1 : 0;
+  a->budget = c->batch * *splits;
+  if (a->chunked && !num_splits && *splits > 1) {
+    const int64_t wave = resident / ((int64_t)n_layers * c->H_kv);
+    if (wave > a->budget) {
+      const int s2 = (int)std::min<int64_t>((wave + c->batch - 1) / c->batch, kMaxSplits);
+      a->budget = (int)std::min<int64_t>(wave, (int64_t)c->batch * s2);
+      *splits = s2;
+    }
+  }
 }
 
 size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
@@ -610,6 +629,15 @@ static kvq_status prep_decode(const kvq_config* cfg, const kvq_cache* cache, int
   int64_t units = (int64_t)n_layers * cfg->batch * cfg->H_kv;
   if (splits > 1 && units * splits > w.max_partials)
     return fail(KVQ_ERR_WORKSPACE, "%d splits x %lld units exceed the workspace", splits, (long long)units);
+  DecodeArgs planned = *a;
+  int grown = splits;
+  set_chunking(cfg, num_splits, n_layers, &grown, &planned);
+  if (units * grown > w.max_partials) {  // no room for the wider grid: keep the plain budget
+    planned.budget = cfg->batch * splits;
+    grown = splits;
+  }
+  splits = grown;
+  *a = planned;
   a->lo = make_layout(cfg);
   a->layer0 = layer0;
   a->n_layers = n_layers;
@@ -617,7 +645,6 @@ static kvq_status prep_decode(const kvq_config* cfg, const kvq_cache* cache, int
   a->seq_lens = seq_lens;
   a->out = out;
   a->splits = splits;
-  set_chunking(cfg, num_splits, n_layers, splits, a);
   a->status = (uint32_t*)((char*)workspace + w.status);
   a->cp.status = a->status;
   a->tickets = (uint32_t*)((char*)workspace + w.tickets);
@@ -797,7 +824,9 @@ extern "C" kvq_status kvq_decode_attention_static(const kvq_config* cfg, const k
   if (num_splits < 0 || num_splits > kMaxSplits) return fail(KVQ_ERR_ARG, "num_splits=%d", num_splits);
   DecodeArgs a{};
   if ((st = cache_ptrs(cfg, cache, &a.cp)) != KVQ_OK) return st;
-  const int splits = num_splits ? num_splits : splits_for(cfg, n_layers);
+  const int plain = num_splits ? num_splits : splits_for(cfg, n_layers);
+  int splits = plain;
+  set_chunking(cfg, num_splits, n_layers, &splits, &a);
   const int g = cfg->H_q / cfg->H_kv;
   const size_t units = (size_t)n_layers * cfg->batch * cfg->H_kv;
   // this call's scratch: status word, tickets, RoPE tables, split partials
@@ -810,7 +839,12 @@ extern "C" kvq_status kvq_decode_attention_static(const kvq_config* cfg, const k
     off = align_up(off + sizeof(float2) * (size_t)(rope_rows + kRopeExtraRows) * (cfg->D / 2));
   }
   const size_t off_partials = off;
-  if (splits > 1) off = align_up(off + sizeof(float) * units * splits * g * part_row(cfg->D));
+  auto partials_end = [&](int sp) { return sp > 1 ? align_up(off + sizeof(float) * units * sp * g * part_row(cfg->D)) : off; };
+  if (splits != plain && partials_end(splits) > (size_t)KVQ_STATIC_SCRATCH_BYTES) {
+    splits = plain;  // no room for the wider grid: keep the plain budget
+    a.budget = cfg->batch * plain;
+  }
+  off = partials_end(splits);
   if (off > (size_t)KVQ_STATIC_SCRATCH_BYTES)
     return fail(KVQ_ERR_WORKSPACE, "this call needs %zu B of scratch; the static scratch holds %u B", off,
                 (unsigned)KVQ_STATIC_SCRATCH_BYTES);
@@ -831,7 +865,6 @@ extern "C" kvq_status kvq_decode_attention_static(const kvq_config* cfg, const k
   a.seq_lens = seq_lens;
   a.out = out;
   a.splits = splits;
-  set_chunking(cfg, num_splits, n_layers, splits, &a);
   a.status = (uint32_t*)base;
   a.cp.status = a.status;
   a.tickets = (uint32_t*)((char*)base + off_tickets);

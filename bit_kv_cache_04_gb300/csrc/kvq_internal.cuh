@@ -280,7 +280,8 @@ struct DecodeArgs {
   const uint16_t* q;
   const int32_t* seq_lens;
   float* out;
-  int splits;        // blocks per (layer, sequence, kv head) in the grid (the block budget)
+  int splits;        // blocks per (layer, sequence, kv head) in the grid
+  int budget;        // chunk plan: blocks per (layer, kv head) it may use (at most batch x splits)
   int min_chunk;     // tensor-core decode: least tiles per chunk of a unit
   int fixed_splits;  // 1: the caller fixed `splits`, so no unit is cut into more chunks
   int chunked;       // 1: plan chunks by tile count; 0: split every unit evenly

@@ -267,7 +267,12 @@ KVQ_API kvq_status kvq_commit_lengths(const kvq_config* cfg, const int32_t* cu_n
  *            (32 tokens) is cut into ceil(n / C) nearly equal chunks for the
  *            smallest C that fits the budget, so long sequences get more
  *            blocks and short ones fewer (with a count passed here, no unit
- *            gets more than num_splits).  The result does not depend on the
+ *            gets more than num_splits).  With 0, the budget is one whole
+ *            wave of resident blocks per call where that exceeds batch x
+ *            kvq_decode_splits blocks per (layer, kv head), and the grid
+ *            grows to hold it (blocks past the last chunk exit at once;
+ *            without room in the workspace the plain budget stays).  The
+ *            result does not depend on the
  *            split beyond the order of fp32 sums.  KVQ_ERR_WORKSPACE when the
  *            workspace's partial rows cannot hold the blocks. */
 KVQ_API kvq_status kvq_decode_attention(const kvq_config* cfg, const kvq_cache* cache, int32_t layer0,
@@ -300,10 +305,12 @@ KVQ_API kvq_status kvq_decode_step(const kvq_config* cfg, const kvq_cache* cache
 /* Kernel launches one kvq_decode_step call makes (1 when fused). */
 KVQ_API kvq_status kvq_step_launches(const kvq_config* cfg, int32_t* launches);
 
-/* The block budget per (layer, seq, kv head) kvq_decode_attention takes for
+/* The split count per (layer, seq, kv head) kvq_decode_attention takes for
  * num_splits = 0: the count with the best fill of whole waves of resident
  * blocks (the device's SM count), each block keeping at least 8 tiles of the
- * longest possible sequence (48 for rotated formats). */
+ * longest possible sequence (48 for rotated formats).  A call whose chunks
+ * are planned on the device may widen it to give the plan one whole wave
+ * (kvq_decode_attention). */
 KVQ_API kvq_status kvq_decode_splits(const kvq_config* cfg, int32_t n_layers, int32_t* splits);
 
 /* Dequantizes tokens [t0, t1) of (layer, seq) to fp32 k_out, v_out
