@@ -101,6 +101,40 @@ def test_bulk_and_incremental_append_agree(name):
     assert torch.equal(o1, o2)
 
 
+# Paged layouts of the unrotated 32-value per-token formats (their rows leave
+# the per-token append kernel through the block table, one destination per
+# token row): pages of 16 and of 8 tokens, a 16-bit window, asymmetric blocks.
+PAGED = {
+    "q4_0_p16": ("q4_0_mha_1k", dict(page_tokens=16), [1000, 333, 129]),
+    "q8_0_p8_window": ("q8_0_mha_1k", dict(page_tokens=8, residual_window=128), [700, 77, 200]),
+    "q4_0_zp_p16": ("q4_0_mha_1k", dict(page_tokens=16, flags=K.ZP_K | K.ZP_V), [513, 31, 260]),
+}
+
+
+def _paged(key):
+    from dataclasses import replace
+
+    name, kw, lengths = PAGED[key]
+    w = W.make(name)
+    w = W.Workload(w.name, replace(w.cfg, **kw), w.lengths, w.values, w.extra_tokens)
+    return w.scaled(lengths=lengths)
+
+
+@pytest.mark.parametrize("key", sorted(PAGED))
+def test_paged_per_token_formats(key):
+    w = _paged(key)
+    oc = oracle_cfg(w.cfg)
+    for chunks in (None, [257, 1, 1, 33, 31, 1, 64, 500, 3]):
+        cache, seq_lens, ref, table = appended_cache(w, chunks=chunks)
+        assert cache.device_status() == 0
+        got = gpu_buffers_as_oracle(cache, oc)
+        for n in ref:
+            assert np.array_equal(got[n], ref[n]), (n, chunks)
+    q, out = _decode(cache, w, seq_lens)
+    ref_o = O.decode_attention(oc, got, 0, w.cfg.L, raw16(q), w.lengths, block_table=table)
+    assert rel_err(out.cpu().numpy(), ref_o) <= TOL
+
+
 @pytest.mark.parametrize("name", ["llama2_7b_kivi4", "ctx262k_hadamard4", "mistral7b_hotcold"])
 def test_split_count_does_not_matter(name):
     w = _workload(name)
