@@ -56,3 +56,29 @@ def gpu_buffers_as_oracle(cache, oc):
         shape, dt = shapes[name]
         out[name] = arr.view(dt).reshape(shape)
     return out
+
+
+# Paged layouts of the unrotated 32-value per-token formats (their rows leave
+# the per-token append kernel through the block table, one destination per
+# token row): pages of 16 and of 8 tokens, a 16-bit window, asymmetric blocks.
+PAGED_PER_TOKEN = {
+    "q4_0_p16": ("q4_0_mha_1k", dict(page_tokens=16), [1000, 333, 129]),
+    "q8_0_p8_window": ("q8_0_mha_1k", dict(page_tokens=8, residual_window=128), [700, 77, 200]),
+    "q4_0_zp_p16": ("q4_0_mha_1k", dict(page_tokens=16, zp=True), [513, 31, 260]),
+}
+
+
+def paged_workload(key):
+    """The paged workload `key` of PAGED_PER_TOKEN, scaled to its lengths."""
+    from dataclasses import replace
+
+    from bit_kv_cache_04_gb300 import config as C
+    from bit_kv_cache_04_gb300 import workloads as W
+
+    name, kw, lengths = PAGED_PER_TOKEN[key]
+    kw = dict(kw)
+    if kw.pop("zp", False):
+        kw["flags"] = C.ZP_K | C.ZP_V
+    w = W.make(name)
+    w = W.Workload(w.name, replace(w.cfg, **kw), w.lengths, w.values, w.extra_tokens)
+    return w.scaled(lengths=lengths)

@@ -4,7 +4,7 @@ address is checked against its buffer segment (layer, sequence, kv head, row
 or page), and a miss sets KVQ_DEV_BOUNDS and skips the access.
 
 * On every kernel path (per-channel and per-token appends, the tiers'
-  requantization, the window ring, paged rotated rows, the tensor-core and
+  requantization, the window ring, paged rotated and per-token rows, the tensor-core and
   generic decodes, the fused decode step, dequantize), across the tiny-shape
   sweep's lengths and scaled workloads, no check fires and the bytes still
   equal the oracle's.
@@ -45,7 +45,7 @@ def _checked_run():
     sys.path.insert(0, ROOT)
     from bit_kv_cache_04_gb300 import kvq as K
     from bit_kv_cache_04_gb300 import workloads as W
-    from tests.gpu_cases import appended_cache, gpu_buffers_as_oracle
+    from tests.gpu_cases import PAGED_PER_TOKEN, appended_cache, gpu_buffers_as_oracle, paged_workload
     from tests.helpers import oracle_cfg
     from tests.test_gpu_tiny_shapes import CASES as TINY, LENGTHS as TINY_LENGTHS, _cfg as tiny_cfg
 
@@ -79,6 +79,8 @@ def _checked_run():
 
     for name, kw in SCALED.items():
         exercise(name, W.make(name).scaled(**kw))
+    for key in PAGED_PER_TOKEN:
+        exercise(key, paged_workload(key))
     for kind, D, R in TINY:
         cfg, values = tiny_cfg(kind, D, R)
         exercise(f"tiny_{kind}_d{D}_r{R}", W.Workload(f"tiny_{kind}", cfg, list(TINY_LENGTHS), values, 40))

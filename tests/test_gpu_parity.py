@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 from oracle import kvq_oracle as O
-from tests.gpu_cases import appended_cache, gpu_buffers_as_oracle
+from tests.gpu_cases import PAGED_PER_TOKEN, appended_cache, gpu_buffers_as_oracle, paged_workload
 from tests.helpers import codes_differ, oracle_cfg, raw16, rel_err
 
 pytestmark = pytest.mark.gpu
@@ -101,28 +101,9 @@ def test_bulk_and_incremental_append_agree(name):
     assert torch.equal(o1, o2)
 
 
-# Paged layouts of the unrotated 32-value per-token formats (their rows leave
-# the per-token append kernel through the block table, one destination per
-# token row): pages of 16 and of 8 tokens, a 16-bit window, asymmetric blocks.
-PAGED = {
-    "q4_0_p16": ("q4_0_mha_1k", dict(page_tokens=16), [1000, 333, 129]),
-    "q8_0_p8_window": ("q8_0_mha_1k", dict(page_tokens=8, residual_window=128), [700, 77, 200]),
-    "q4_0_zp_p16": ("q4_0_mha_1k", dict(page_tokens=16, flags=K.ZP_K | K.ZP_V), [513, 31, 260]),
-}
-
-
-def _paged(key):
-    from dataclasses import replace
-
-    name, kw, lengths = PAGED[key]
-    w = W.make(name)
-    w = W.Workload(w.name, replace(w.cfg, **kw), w.lengths, w.values, w.extra_tokens)
-    return w.scaled(lengths=lengths)
-
-
-@pytest.mark.parametrize("key", sorted(PAGED))
+@pytest.mark.parametrize("key", sorted(PAGED_PER_TOKEN))
 def test_paged_per_token_formats(key):
-    w = _paged(key)
+    w = paged_workload(key)
     oc = oracle_cfg(w.cfg)
     for chunks in (None, [257, 1, 1, 33, 31, 1, 64, 500, 3]):
         cache, seq_lens, ref, table = appended_cache(w, chunks=chunks)
