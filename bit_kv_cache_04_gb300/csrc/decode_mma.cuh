@@ -122,11 +122,12 @@ struct Cfg {
                                (HOT::KB == 8 || HOT::KB == 4 || HOT::KB == 3);
   static constexpr int KBLK = HOT::KCH ? 1 : D / HOT::KG;
   // V codes read as subnormals (see v_pair4): one tier of 8-, 4- or 2-bit
-  // uniform codes, not with heads as columns (there the bias MMAs of the hi
-  // and lo fragments cost more than the conversions they replace); NBV V
-  // blocks per token row
+  // uniform codes, symmetric or asymmetric (the bias MMA leaves field - beta;
+  // the zero term adds z' = z + beta s), not with heads as columns (there the
+  // bias MMAs of the hi and lo fragments cost more than the conversions they
+  // replace); NBV V blocks per token row
   static constexpr bool VSUB =
-      !HAS_COLD && !Z && !HC && !HOT::VLUT && (HOT::VB == 8 || HOT::VB == 4 || HOT::VB == 2);
+      !HAS_COLD && !HC && !HOT::VLUT && (HOT::VB == 8 || HOT::VB == 4 || HOT::VB == 2);
   static constexpr int NBV = D / HOT::VG;
   static constexpr int QSM = KC * NT * 32 * (8 + (QH ? 8 : 0) + (ROPE ? 16 : 0) + (Z ? 8 : 0) + (HC ? 8 : 0)) +
                              (KSUB ? 4 * KBLK * NT * 8 : 0);
@@ -968,11 +969,12 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
     } else if constexpr (TR::KCH) {
       // per-channel K: block c = channel c over the group's 32 tokens; the
       // channel scales multiply the query columns.  Even and odd k-chunks
-      // accumulate separately (two independent MMA chains).  Symmetric codes
-      // are read as subnormals (as v_pair4's), the token of a row fixing its
-      // position factor; the bias comes off by one constant-row MMA per
-      // k-chunk, the factors and 2^-24 once per group.
-      constexpr bool SUBK = !TR::Z;
+      // accumulate separately (two independent MMA chains).  Codes are read
+      // as subnormals (as v_pair4's), the token of a row fixing its position
+      // factor; the bias comes off by one constant-row MMA per k-chunk, the
+      // factors and 2^-24 once per group.  Asymmetric codes too: what remains
+      // is field - beta, as the converted codes give, and the zero term below
+      // adds z' = z + beta s.
       float Sx[2][NT][4];
 #pragma unroll
       for (int mu = 0; mu < 2; ++mu)
@@ -989,31 +991,22 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
         if constexpr (TR::KB == 4) {
           const uint32_t x12 = __byte_perm(ld_u16(b1p + TR::HDR + 2 * gq), ld_u16(b2p + TR::HDR + 2 * gq), 0x5410);
           const uint32_t x34 = __byte_perm(ld_u16(b3p + TR::HDR + 2 * gq), ld_u16(b4p + TR::HDR + 2 * gq), 0x5410);
-          if constexpr (SUBK) {  // subnormal codes: token nibbles in place (positions 0, 4, 0, 4)
-            k12[0] = x12 & 0x000F000Fu;
-            k12[1] = x12 & 0x00F000F0u;
-            k12[2] = (x12 >> 8) & 0x000F000Fu;
-            k12[3] = (x12 >> 8) & 0x00F000F0u;
-            k34[0] = x34 & 0x000F000Fu;
-            k34[1] = x34 & 0x00F000F0u;
-            k34[2] = (x34 >> 8) & 0x000F000Fu;
-            k34[3] = (x34 >> 8) & 0x00F000F0u;
-          } else {
-            dq4(x12, k12);
-            dq4(x34, k34);
-          }
+          // token nibbles in place (positions 0, 4, 0, 4)
+          k12[0] = x12 & 0x000F000Fu;
+          k12[1] = x12 & 0x00F000F0u;
+          k12[2] = (x12 >> 8) & 0x000F000Fu;
+          k12[3] = (x12 >> 8) & 0x00F000F0u;
+          k34[0] = x34 & 0x000F000Fu;
+          k34[1] = x34 & 0x00F000F0u;
+          k34[2] = (x34 >> 8) & 0x000F000Fu;
+          k34[3] = (x34 >> 8) & 0x00F000F0u;
         } else {
           const uint32_t x12 = __byte_perm((uint32_t)b1p[TR::HDR + gq], (uint32_t)b2p[TR::HDR + gq], 0x5410);
           const uint32_t x34 = __byte_perm((uint32_t)b3p[TR::HDR + gq], (uint32_t)b4p[TR::HDR + gq], 0x5410);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            if constexpr (SUBK) {  // subnormal codes: token fields in place (positions 0, 2, 4, 6)
-              k12[k] = x12 & (0x00030003u << (2 * k));
-              k34[k] = x34 & (0x00030003u << (2 * k));
-            } else {
-              k12[k] = code_pair<2>(x12, k);
-              k34[k] = code_pair<2>(x34, k);
-            }
+          for (int k = 0; k < 4; ++k) {  // token fields in place (positions 0, 2, 4, 6)
+            k12[k] = x12 & (0x00030003u << (2 * k));
+            k34[k] = x34 & (0x00030003u << (2 * k));
           }
         }
         const uint32_t s12 = __byte_perm(ld_u16(b1p), ld_u16(b2p), 0x5410);
@@ -1029,11 +1022,9 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
           for (int mu = 0; mu < 2; ++mu) {
             float (&acc)[4] = (kc & 1) ? Sx[mu][nt] : S[mu][nt];
             mma16816(acc, k12[2 * mu], k12[2 * mu + 1], k34[2 * mu], k34[2 * mu + 1], bq0, bq1);
-            if constexpr (SUBK) {
-              // the storage bias of the rows' tokens, in the same accumulator
-              const uint32_t na = v_sub_neg(TR::KB, 2 * mu), nb = v_sub_neg(TR::KB, 2 * mu + 1);
-              mma16816(acc, na, nb, na, nb, bq0, bq1);
-            }
+            // the storage bias of the rows' tokens, in the same accumulator
+            const uint32_t na = v_sub_neg(TR::KB, 2 * mu), nb = v_sub_neg(TR::KB, 2 * mu + 1);
+            mma16816(acc, na, nb, na, nb, bq0, bq1);
           }
         }
       }
@@ -1045,7 +1036,7 @@ __device__ __forceinline__ void scores_packed(const Ctx<C>& cx, const uint8_t* k
           for (int e = 0; e < 4; ++e) {
             S[mu][nt][e] += Sx[mu][nt][e];
             // subnormal codes: rows gq / gq + 8 hold tokens 4 gq + 2 mu / + 1
-            if constexpr (SUBK) S[mu][nt][e] *= ldexpf(1.f, 24 - v_sub_shift(TR::KB, 2 * mu + (e >> 1)));
+            S[mu][nt][e] *= ldexpf(1.f, 24 - v_sub_shift(TR::KB, 2 * mu + (e >> 1)));
           }
       if constexpr (TR::Z) {
         // zero term of the group, the same for its 32 tokens: sum_c q'_c z'_c
