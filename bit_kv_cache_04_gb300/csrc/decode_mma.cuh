@@ -1238,19 +1238,22 @@ __device__ __forceinline__ Work plan_work(const DecodeArgs& a, Work* sw) {
       even = maxn == minn && !a.fixed_splits;
     }
     if (even) {
+      // the unit's share of the budget: the grid's S blocks, or fewer when
+      // the grid was widened for a budget that is not a multiple of B
+      const int nc = max(1, min(S, a.budget / B));
       const int unit = k / S;
       w.chunk = k % S;
-      w.n_chunks = S;
+      w.n_chunks = nc;
       w.first = unit * S;
       w.h = unit % H;
       w.seq = (unit / H) % B;
       w.li = unit / (H * B);
-      w.active = w.li < a.n_layers;
+      w.active = w.li < a.n_layers && w.chunk < nc;
       if (w.active) {
         w.T = attended_len(a, w.seq, &w.bad_len);
         const int n = unit_tiles<HAS_COLD>(lo, w.T);
-        w.tb = (int)((int64_t)w.chunk * n / S);
-        w.te = (int)((int64_t)(w.chunk + 1) * n / S);
+        w.tb = (int)((int64_t)w.chunk * n / nc);
+        w.te = (int)((int64_t)(w.chunk + 1) * n / nc);
       }
       if (lane == 0) *sw = w;
     } else {

@@ -325,9 +325,12 @@ void set_chunking(const kvq_config* c, int num_splits, int n_layers, int* splits
   a->chunked = (num_splits || blocks <= 2 * resident) ? 1 : 0;
   a->budget = c->batch * *splits;
   if (a->chunked && !num_splits && *splits > 1) {
+    // no more splits per unit than the planning floor allows at full capacity
+    const int64_t tiles = (c->max_T + kTile - 1) / kTile + 2;
+    const int64_t cap = std::min<int64_t>(std::max<int64_t>(1, tiles / a->min_chunk), kMaxSplits);
     const int64_t wave = resident / ((int64_t)n_layers * c->H_kv);
-    if (wave > a->budget) {
-      const int s2 = (int)std::min<int64_t>((wave + c->batch - 1) / c->batch, kMaxSplits);
+    const int s2 = (int)std::min<int64_t>((wave + c->batch - 1) / c->batch, cap);
+    if (s2 > *splits) {
       a->budget = (int)std::min<int64_t>(wave, (int64_t)c->batch * s2);
       *splits = s2;
     }
