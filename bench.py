@@ -577,11 +577,11 @@ def run_ours(args):
 # with the SHA-256 of the kernel sources it was taken on; the roofline reports
 # them scaled to the timed launch while those sources are unchanged, else null.
 DECODE_TRAFFIC = {
-    "llama2_7b_kivi4": {"sha256": "89f0144b9a93c5e749afddb60a0673448051248f50c9acd20e2e835062a700ca",
-                        "bytes_per_layer": (610.590976e6 + 7.614976e6) / 4},
+    "llama2_7b_kivi4": {"sha256": "00efabdf9efc34ced41ce48672c30ce1e45cf635bfff041c1a39d11756ad4aba",
+                        "bytes_per_layer": (610.680832e6 + 7.627776e6) / 4},
     # a 2-layer step (64 sequences x 32768 tokens) captured whole, halved
-    "mistral7b_hotcold": {"sha256": "c5cd9041cc8169e48b2b04f22abe009d5e2cfcf5d28f6e5090778f2b43602f59",
-                          "bytes_per_layer": (3021.657088e6 + 17.51552e6) / 2},
+    "mistral7b_hotcold": {"sha256": "3eabc0e9aa994ed37606f785b112c8497aefe044b02e2b0bda3c8ab9cae8cbc9",
+                          "bytes_per_layer": (3021.731328e6 + 17.688064e6) / 2},
 }
 # the sources each workload's decode-step kernel is built from
 _COMMON_SOURCES = ("decode_mma.cuh", "append_generic.cuh", "append_common.cuh", "block_codec.cuh")
