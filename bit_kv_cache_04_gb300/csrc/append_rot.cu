@@ -183,15 +183,29 @@ __global__ void __launch_bounds__(kAppendThreads) quant_rot128_kernel(AppendArgs
   // 2^B - f = (f ^ (2^B - 1)) + 1 (biased codes are >= 1, so no field
   // overflows): negx holds the fields' bits, negl their lowest bits
   uint32_t negx[B], negl[B];
+  if constexpr (B == 4) {
+    // word k holds values 8k .. 8k + 7: their d2 bits spread to nibble
+    // starts (0, 4, ..., 28), then each made a whole nibble
 #pragma unroll
-  for (int k = 0; k < B; ++k) negx[k] = negl[k] = 0;
+    for (int k = 0; k < 4; ++k) {
+      uint32_t x = (d2w >> (8 * k)) & 0xFFu;
+      x = (x | (x << 12)) & 0x000F000Fu;
+      x = (x | (x << 6)) & 0x03030303u;
+      x = (x | (x << 3)) & 0x11111111u;
+      negl[k] = x;
+      negx[k] = x * 15u;
+    }
+  } else {
 #pragma unroll
-  for (int b = 0; b < 32; ++b) {
-    const uint32_t on = (d2w >> b) & 1u;
-    const int bit = B * b, k = bit / 32, sh = bit % 32;
-    negx[k] |= (on * ((1u << B) - 1)) << sh;
-    if (sh + B > 32) negx[k + 1] |= (on * ((1u << B) - 1)) >> (32 - sh);
-    negl[k] |= on << sh;
+    for (int k = 0; k < B; ++k) negx[k] = negl[k] = 0;
+#pragma unroll
+    for (int b = 0; b < 32; ++b) {
+      const uint32_t on = (d2w >> b) & 1u;
+      const int bit = B * b, k = bit / 32, sh = bit % 32;
+      negx[k] |= (on * ((1u << B) - 1)) << sh;
+      if (sh + B > 32) negx[k + 1] |= (on * ((1u << B) - 1)) >> (32 - sh);
+      negl[k] |= on << sh;
+    }
   }
 
   auto row_src = [&](int t) -> const uint4* {
