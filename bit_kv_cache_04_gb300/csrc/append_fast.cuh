@@ -693,7 +693,8 @@ __global__ void __launch_bounds__(kAppendThreads, 5) quant_token32_kernel(Append
   // run of consecutive rows goes out as whole lines
   if (j < n_tok) {
     bool bad = false;
-    uint8_t* d = to_cold ? cold_row(lo, a.cp, which, layer, seq, h, t) : main_row(lo, a.cp, which, layer, seq, h, t, &bad);
+    uint8_t* d = to_cold ? cold_row(lo, a.cp, which, layer, seq, h, t)
+                         : main_row(lo, a.cp, which, layer, seq, h, t, &bad);
     if (bad) page_bad = 1;
     rowd[j] = bad ? nullptr : d;
   }
