@@ -1456,6 +1456,7 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   __shared__ int is_last;
   __shared__ int pf_page[kWarps][2][2];  // paged: next tile's page ids per warp, by issue parity
   __shared__ Work work_s;
+  __shared__ const uint8_t* lin[2];  // cold tile 0's K and V addresses (tiered kernels)
 
   // the plan stays in shared memory: its fields are read where needed, not
   // held in registers across the group loop
@@ -1484,7 +1485,13 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   const int64_t qrow = ((int64_t)li * lo.B + seq) * lo.Hq + (int64_t)h * g;
 
   // ---- barriers, then the first bulk copies: they land while the query is prepared ----
-  if (tid == 0) bad_page = 0;
+  if (tid == 0) {
+    bad_page = 0;
+    if constexpr (C::HAS_COLD) {
+      lin[0] = cold_row(lo, a.cp, 0, layer, seq, h, 0);
+      lin[1] = cold_row(lo, a.cp, 1, layer, seq, h, 0);
+    }
+  }
   if (tid < kWarps * kStages) mbar_init(mbar + tid, 1);
   if (tid == kThreadsMma - 1) mbar_init(&never_bar, 1);
   fence_mbar_init();
@@ -1500,6 +1507,22 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   // register holds them across the loop.
   const int first = tb + warp;  // this warp takes tiles first, first + kWarps, ...
 
+  // Cold tiles, and the tiles of an untiered contiguous main tier, lie one
+  // tile stride apart: tile t of this unit starts t strides after tile 0.
+  // Tile 0's K and V addresses sit in shared memory (lin[0], lin[1]) for the
+  // tiered kernels, whose registers are fuller, and in lane 0's registers
+  // (k_lin, v_lin) otherwise.  (The hot ring and the pages look each tile's
+  // rows up.)
+  const uint8_t* k_lin = nullptr;
+  const uint8_t* v_lin = nullptr;
+  if constexpr (!C::HAS_COLD) {
+    if (lane == 0 && !lo.paged && !lo.tiered) {
+      bool unused = false;
+      k_lin = main_row(lo, a.cp, 0, layer, seq, h, 0, &unused);
+      v_lin = main_row(lo, a.cp, 1, layer, seq, h, 0, &unused);
+    }
+  }
+
   // Bulk copies of packed tile `tile` (cold or hot/only tier) into stage
   // `st`, issued by lane 0: exactly one arrival on the stage's barrier per
   // packed tile of this warp (with no bytes when a page id is bad).
@@ -1511,9 +1534,8 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     uint64_t* bar = mbar + warp * kStages + st;
     if constexpr (C::HAS_COLD) {
       if (tile < n_c) {
-        const int t0 = tile * kTile;
-        const uint8_t* kg = cold_row(lo, a.cp, 0, layer, seq, h, t0);
-        const uint8_t* vg = cold_row(lo, a.cp, 1, layer, seq, h, t0);
+        const uint8_t* kg = lin[0] + (int64_t)tile * C::COLD::KSTAGE;
+        const uint8_t* vg = lin[1] + (int64_t)tile * C::COLD::VSTAGE;
         if (!(span_ok(lo, a.cp, 2, kg, C::COLD::KSTAGE) & span_ok(lo, a.cp, 3, vg, C::COLD::VSTAGE))) {
           mbar_arrive_tx(bar, 0);  // bounds-checked build only: skipped
           return;
@@ -1574,8 +1596,8 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
       }
       return;
     }
-    const uint8_t* kg = main_row(lo, a.cp, 0, layer, seq, h, t0, &bad);
-    const uint8_t* vg = main_row(lo, a.cp, 1, layer, seq, h, t0, &bad);
+    const uint8_t* kg = k_lin ? k_lin + (int64_t)tile * HT::KSTAGE : main_row(lo, a.cp, 0, layer, seq, h, t0, &bad);
+    const uint8_t* vg = k_lin ? v_lin + (int64_t)tile * HT::VSTAGE : main_row(lo, a.cp, 1, layer, seq, h, t0, &bad);
     if (!(span_ok(lo, a.cp, 0, kg, HT::KSTAGE) & span_ok(lo, a.cp, 1, vg, HT::VSTAGE))) {
       mbar_arrive_tx(bar, 0);  // bounds-checked build only: skipped
       return;
