@@ -577,11 +577,11 @@ def run_ours(args):
 # with the SHA-256 of the kernel sources it was taken on; the roofline reports
 # them scaled to the timed launch while those sources are unchanged, else null.
 DECODE_TRAFFIC = {
-    "llama2_7b_kivi4": {"sha256": "00efabdf9efc34ced41ce48672c30ce1e45cf635bfff041c1a39d11756ad4aba",
-                        "bytes_per_layer": (610.680832e6 + 7.627776e6) / 4},
+    "llama2_7b_kivi4": {"sha256": "0dbc018da0e4ae104975bd31377fb0d916f7fef1741e6c5beef99036a7342651",
+                        "bytes_per_layer": (610.593536e6 + 8.645632e6) / 4},
     # a 2-layer step (64 sequences x 32768 tokens) captured whole, halved
-    "mistral7b_hotcold": {"sha256": "3eabc0e9aa994ed37606f785b112c8497aefe044b02e2b0bda3c8ab9cae8cbc9",
-                          "bytes_per_layer": (3021.731328e6 + 17.688064e6) / 2},
+    "mistral7b_hotcold": {"sha256": "5b5b3d7f5e44bb134b07dbd4c80c6c48941c9c0fa8b7d1a834600fc26bf22508",
+                          "bytes_per_layer": (3022.033152e6 + 17.609216e6) / 2},
 }
 # the sources each workload's decode-step kernel is built from
 _COMMON_SOURCES = ("decode_mma.cuh", "append_generic.cuh", "append_common.cuh", "block_codec.cuh")
