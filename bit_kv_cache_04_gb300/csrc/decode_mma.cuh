@@ -1456,7 +1456,8 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   __shared__ int is_last;
   __shared__ int pf_page[kWarps][2][2];  // paged: next tile's page ids per warp, by issue parity
   __shared__ Work work_s;
-  __shared__ const uint8_t* lin[2];  // cold tile 0's K and V addresses (tiered kernels)
+  __shared__ const uint8_t* lin[2];  // K and V addresses of cold tile 0 (tiered) or page 0 (paged)
+  __shared__ int pstride[2];         // paged: bytes from one page of this (layer, kv head) to the next
 
   // the plan stays in shared memory: its fields are read where needed, not
   // held in registers across the group loop
@@ -1490,6 +1491,12 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
     if constexpr (C::HAS_COLD) {
       lin[0] = cold_row(lo, a.cp, 0, layer, seq, h, 0);
       lin[1] = cold_row(lo, a.cp, 1, layer, seq, h, 0);
+    } else if (lo.paged) {
+      const int64_t r0 = ((int64_t)layer * lo.n_pages * lo.H + h) * lo.pt;  // page 0's first row
+      lin[0] = a.cp.k_main + r0 * lo.kf.row;
+      lin[1] = a.cp.v_main + r0 * lo.vf.row;
+      pstride[0] = lo.H * lo.pt * lo.kf.row;
+      pstride[1] = lo.H * lo.pt * lo.vf.row;
     }
   }
   if (tid < kWarps * kStages) mbar_init(mbar + tid, 1);
@@ -1511,8 +1518,9 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
   // tile stride apart: tile t of this unit starts t strides after tile 0.
   // Tile 0's K and V addresses sit in shared memory (lin[0], lin[1]) for the
   // tiered kernels, whose registers are fuller, and in lane 0's registers
-  // (k_lin, v_lin) otherwise.  (The hot ring and the pages look each tile's
-  // rows up.)
+  // (k_lin, v_lin) otherwise.  (The hot ring looks each tile's rows up.)
+  // Pages: page p of this (layer, kv head) starts p page strides (pstride)
+  // after page 0, whose addresses lin then holds.
   const uint8_t* k_lin = nullptr;
   const uint8_t* v_lin = nullptr;
   if constexpr (!C::HAS_COLD) {
@@ -1579,20 +1587,21 @@ __global__ void __launch_bounds__(kThreadsMma, C::MIN_CTAS) decode_mma_kernel(De
         mbar_arrive_tx(bar, 0);
         return;
       }
-      auto row0 = [&](int page) { return (((int64_t)layer * lo.n_pages + page) * lo.H + h) * lo.pt; };
-      if (!(span_ok(lo, a.cp, 0, a.cp.k_main + row0(p0) * lo.kf.row, kb) &
-            span_ok(lo, a.cp, 1, a.cp.v_main + row0(p0) * lo.vf.row, vb) &
-            span_ok(lo, a.cp, 0, a.cp.k_main + row0(p1) * lo.kf.row, kb) &
-            span_ok(lo, a.cp, 1, a.cp.v_main + row0(p1) * lo.vf.row, vb))) {
+      const uint8_t* k0 = lin[0] + (int64_t)p0 * pstride[0];
+      const uint8_t* v0 = lin[1] + (int64_t)p0 * pstride[1];
+      const uint8_t* k1 = lin[0] + (int64_t)p1 * pstride[0];
+      const uint8_t* v1 = lin[1] + (int64_t)p1 * pstride[1];
+      if (!(span_ok(lo, a.cp, 0, k0, kb) & span_ok(lo, a.cp, 1, v0, vb) & span_ok(lo, a.cp, 0, k1, kb) &
+            span_ok(lo, a.cp, 1, v1, vb))) {
         mbar_arrive_tx(bar, 0);  // bounds-checked build only: skipped
         return;
       }
       mbar_arrive_tx(bar, np * (kb + vb));
-      bulk_g2s(ks, a.cp.k_main + row0(p0) * lo.kf.row, kb, bar);
-      bulk_g2s(vs, a.cp.v_main + row0(p0) * lo.vf.row, vb, bar);
+      bulk_g2s(ks, k0, kb, bar);
+      bulk_g2s(vs, v0, vb, bar);
       if (np == 2) {
-        bulk_g2s(ks + kb, a.cp.k_main + row0(p1) * lo.kf.row, kb, bar);
-        bulk_g2s(vs + vb, a.cp.v_main + row0(p1) * lo.vf.row, vb, bar);
+        bulk_g2s(ks + kb, k1, kb, bar);
+        bulk_g2s(vs + vb, v1, vb, bar);
       }
       return;
     }
