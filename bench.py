@@ -577,11 +577,11 @@ def run_ours(args):
 # with the SHA-256 of the kernel sources it was taken on; the roofline reports
 # them scaled to the timed launch while those sources are unchanged, else null.
 DECODE_TRAFFIC = {
-    "llama2_7b_kivi4": {"sha256": "0dbc018da0e4ae104975bd31377fb0d916f7fef1741e6c5beef99036a7342651",
-                        "bytes_per_layer": (610.593536e6 + 8.645632e6) / 4},
+    "llama2_7b_kivi4": {"sha256": "83ae845cef27e59b91f0de995e58fe7892e40b85583ec76d462aa6229551f076",
+                        "bytes_per_layer": (610.612736e6 + 8.897536e6) / 4},
     # a 2-layer step (64 sequences x 32768 tokens) captured whole, halved
-    "mistral7b_hotcold": {"sha256": "5b5b3d7f5e44bb134b07dbd4c80c6c48941c9c0fa8b7d1a834600fc26bf22508",
-                          "bytes_per_layer": (3022.033152e6 + 17.609216e6) / 2},
+    "mistral7b_hotcold": {"sha256": "f2ef69394305ff6186fda78b363a1bd0bdd77670f6bf220ab59c59cba18c2fd9",
+                          "bytes_per_layer": (3022.001664e6 + 17.611264e6) / 2},
 }
 # the sources each workload's decode-step kernel is built from
 _COMMON_SOURCES = ("decode_mma.cuh", "append_generic.cuh", "append_common.cuh", "block_codec.cuh")
