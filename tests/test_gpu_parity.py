@@ -130,6 +130,31 @@ def test_split_count_does_not_matter(name):
     assert rel_err(o.cpu().numpy(), base[:1].cpu().numpy()) < 1e-5
 
 
+# Per-layer calls whose chunk plan takes one whole wave of resident blocks,
+# more than batch x splits (the grid is widened): equal lengths split evenly
+# over the budget's share of the grid, ragged lengths planned by tile count.
+# Both agree with the fp64 oracle, and with one split per unit up to the
+# order of the fp32 sums: each split rounds its probabilities' fp16 hi / lo
+# parts against its own running maximum, and over the 256 groups of an
+# 8192-token unit the two orders differ by ~3e-5 (the full-size test allows
+# 1e-4 for up to 1024 groups on the same grounds).
+WAVE_CASES = [("gqa8b_hadamard4_paged", [8192] * 3), ("gqa8b_hadamard4_paged", [8192, 3000, 500]),
+              ("mistral7b_hotcold", [8192] * 3), ("mistral7b_hotcold", [5000, 2500, 700, 64, 3000])]
+
+
+@pytest.mark.parametrize("name,lengths", WAVE_CASES)
+def test_one_wave_budget_matches_one_split_and_oracle(name, lengths):
+    w = W.make(name).scaled(L=1, lengths=lengths)
+    cache, seq_lens, _, table = appended_cache(w, with_oracle=False)
+    q, base = _decode(cache, w, seq_lens, splits=1)
+    _, out = _decode(cache, w, seq_lens)
+    assert cache.device_status() == 0
+    assert rel_err(out.cpu().numpy(), base.cpu().numpy()) < 1e-4
+    oc = oracle_cfg(w.cfg)
+    ref = O.decode_attention(oc, gpu_buffers_as_oracle(cache, oc), 0, 1, raw16(q), w.lengths, block_table=table)
+    assert rel_err(out.cpu().numpy(), ref) <= TOL
+
+
 def test_per_layer_calls_equal_multi_layer_call():
     w = _workload("llama2_7b_kivi4")
     cache, seq_lens, _, _ = appended_cache(w, with_oracle=False)
