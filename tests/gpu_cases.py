@@ -65,6 +65,7 @@ PAGED_PER_TOKEN = {
     "q4_0_p16": ("q4_0_mha_1k", dict(page_tokens=16), [1000, 333, 129]),
     "q8_0_p8_window": ("q8_0_mha_1k", dict(page_tokens=8, residual_window=128), [700, 77, 200]),
     "q4_0_zp_p16": ("q4_0_mha_1k", dict(page_tokens=16, zp=True), [513, 31, 260]),
+    "q8_0_p16_bf16": ("q8_0_mha_1k", dict(page_tokens=16, bf16=True), [640, 130, 33]),
 }
 
 
@@ -79,6 +80,8 @@ def paged_workload(key):
     kw = dict(kw)
     if kw.pop("zp", False):
         kw["flags"] = C.ZP_K | C.ZP_V
+    if kw.pop("bf16", False):
+        kw["in_dtype"] = C.DT_BF16
     w = W.make(name)
     w = W.Workload(w.name, replace(w.cfg, **kw), w.lengths, w.values, w.extra_tokens)
     return w.scaled(lengths=lengths)

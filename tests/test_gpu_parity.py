@@ -139,7 +139,8 @@ def test_split_count_does_not_matter(name):
 # 8192-token unit the two orders differ by ~3e-5 (the full-size test allows
 # 1e-4 for up to 1024 groups on the same grounds).
 WAVE_CASES = [("gqa8b_hadamard4_paged", [8192] * 3), ("gqa8b_hadamard4_paged", [8192, 3000, 500]),
-              ("mistral7b_hotcold", [8192] * 3), ("mistral7b_hotcold", [5000, 2500, 700, 64, 3000])]
+              ("mistral7b_hotcold", [8192] * 3), ("mistral7b_hotcold", [5000, 2500, 700, 64, 3000]),
+              ("ctx262k_hadamard4", [8192] * 3)]
 
 
 @pytest.mark.parametrize("name,lengths", WAVE_CASES)
